@@ -1,0 +1,267 @@
+"""CPU oracle for the DeepSeek-V3-style MoE layer.  TEST INFRASTRUCTURE ONLY.
+
+Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference
+legs may import or run this module.  The product path (moe_layer_gb300) never
+touches it, and the two share no code.
+
+It is the plain definition of the layer, written out in float64 numpy: every
+input is upcast to float64, every intermediate stays float64.  Library
+primitives (matrix products, a sort) are used as single steps; nothing is
+fused, blocked or reordered beyond the definitions cited below.
+
+Sources (titles and sections of the pages that define the method):
+  [Blog]  Mixture-of-Kittens blog post (full text), section "Overlapping
+          computation and communication in MoE": each token gets a router
+          projection, the top-k routed experts with one router weight each; each
+          selected expert runs up and gate projections, a SwiGLU activation and a
+          down projection; the shared and routed expert outputs are summed with
+          the router weights.  Section "Choosing the right communication
+          direction / Scheduling" gives the two-pass counting schedule.  Section
+          "Router weight gradient computation" gives the router-weight gradient
+          as the inner product of the SwiGLU activation and the down-projection
+          dgrad.  Section "Determinism" fixes the order of floating-point work.
+  [Paper] "Mixture-of-Kittens: MoE Megakernel for NVL72s", section 2.1: outputs
+          are summed using normalized router weights.
+
+Readings where the pages are silent (each one is listed in the design doc):
+  R1  the shared expert enters the sum with weight 1;
+  R2  router weights: softmax over all E logits, restricted to the k selected
+      experts and renormalized (equal to a softmax over the selected logits);
+  R3  SwiGLU(a, b) = SiLU(a) * b with a = gate projection, b = up projection,
+      SiLU(z) = z * sigmoid(z);
+  R4  top-k order: logits descending, ties broken towards the lower expert index;
+  R5  the backward propagates through the router weights into the logits (and
+      so into W_router and x); an optional router bias is a constant.
+
+Parity pins: every function here is checked by tests/test_oracle_pins.py
+against brute force, closed forms, library routines or finite differences.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "router_logits", "topk_route", "expert_schedule", "silu", "swiglu",
+    "moe_forward", "moe_backward",
+]
+
+
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+# ---------------------------------------------------------------- routing
+def router_logits(x, w_router, bias=None):
+    """Router projection l[t, e] = sum_i x[t, i] * W_r[e, i] (+ bias[e]).  [Blog]"""
+    logits = _f64(x) @ _f64(w_router).T
+    if bias is not None:
+        logits = logits + _f64(bias)[None, :]
+    return logits
+
+
+def topk_route(logits, k):
+    """Top-k routed experts per token and their normalized router weights.
+
+    Selection (R4): experts ordered by logit descending, equal logits by
+    ascending expert index; the first k form the token's slots 0..k-1.
+    Weights (R2): p = softmax over all E logits; g_j = p[e_j] / sum_i p[e_i].
+    The comparisons are made on the values as given (float32 logits compare
+    exactly as float32 because the upcast to float64 is exact).  [Blog], [Paper §2.1]
+    """
+    logits = _f64(logits)
+    T, E = logits.shape
+    # lexsort: the last key is the primary key
+    tie = np.broadcast_to(np.arange(E), (T, E))
+    order = np.lexsort((tie, -logits), axis=-1)
+    idx = order[:, :k].copy()
+    m = logits.max(axis=1, keepdims=True)
+    p = np.exp(logits - m)
+    p = p / p.sum(axis=1, keepdims=True)
+    sel = np.take_along_axis(p, idx, axis=1)
+    w = sel / sel.sum(axis=1, keepdims=True)
+    return idx.astype(np.int64), w
+
+
+def expert_schedule(topk_idx, E):
+    """Per-expert counts, offsets and the stable permutation of routes.
+
+    The one-rank form of the pages' two-pass schedule [Blog, "Scheduling"]:
+    pass 1 walks the routes (token ascending, slot ascending) and counts per
+    expert; the region offsets are the exclusive prefix sum of the counts;
+    pass 2 walks the routes in the same order and hands each one the next row
+    of its expert's region.  Returns counts[E], offsets[E+1],
+    perm_token[R] (row -> token), perm_slot[R] (row -> slot) and
+    route_row[T, k] ((token, slot) -> row).
+    """
+    idx = np.asarray(topk_idx).tolist()
+    T = len(idx)
+    k = len(idx[0]) if T else 0
+    counts = [0] * E
+    for t in range(T):
+        for j in range(k):
+            counts[idx[t][j]] += 1
+    offsets = [0] * (E + 1)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + counts[e]
+    cursor = offsets[:E]
+    perm_token = [0] * (T * k)
+    perm_slot = [0] * (T * k)
+    route_row = [[0] * k for _ in range(T)]
+    for t in range(T):
+        for j in range(k):
+            e = idx[t][j]
+            r = cursor[e]
+            cursor[e] = r + 1
+            perm_token[r] = t
+            perm_slot[r] = j
+            route_row[t][j] = r
+    return (np.array(counts, np.int64), np.array(offsets, np.int64),
+            np.array(perm_token, np.int64), np.array(perm_slot, np.int64),
+            np.array(route_row, np.int64).reshape(T, k))
+
+
+# ---------------------------------------------------------------- expert FFN
+def silu(z):
+    """SiLU(z) = z * sigmoid(z)  (R3)."""
+    z = _f64(z)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def dsilu(z):
+    """d/dz SiLU(z) = sigmoid(z) * (1 + z * (1 - sigmoid(z)))."""
+    z = _f64(z)
+    with np.errstate(over="ignore"):
+        s = 1.0 / (1.0 + np.exp(-z))
+    return s * (1.0 + z * (1.0 - s))
+
+
+def swiglu(a, b):
+    """SwiGLU(a, b) = SiLU(a) * b  (R3).  [Blog]"""
+    return silu(a) * _f64(b)
+
+
+def _ffn(x_rows, w_gate, w_up, w_down):
+    """One SwiGLU expert on a batch of rows: returns a, b, h, o."""
+    a = x_rows @ _f64(w_gate).T
+    b = x_rows @ _f64(w_up).T
+    h = swiglu(a, b)
+    o = h @ _f64(w_down).T
+    return a, b, h, o
+
+
+# ---------------------------------------------------------------- forward
+def moe_forward(x, w_router, w_gate, w_up, w_down, top_k, router_bias=None,
+                ws_gate=None, ws_up=None, ws_down=None, logits=None):
+    """The MoE layer forward, per token t:
+
+        y_t = FFN_shared(x_t) + sum_j g_tj * FFN_{e_tj}(x_t)
+
+    with FFN(v) = W_down (SiLU(W_gate v) * (W_up v)).  [Blog], [Paper §2.1]
+
+    w_gate/w_up/w_down are indexable by expert (w_gate[e] is [I, d],
+    w_down[e] is [d, I]).  `logits` may be given to route on precomputed
+    values (e.g. float32 values for an exact comparison of the routing);
+    otherwise they are computed in float64 from x and w_router.
+    Returns a dict with y [T, d] and everything the backward needs.
+    """
+    x = _f64(x)
+    T = x.shape[0]
+    E = len(w_gate)
+    if logits is None:
+        logits = router_logits(x, w_router, router_bias)
+    idx, w = topk_route(logits, top_k)
+    counts, offsets, perm_token, perm_slot, route_row = expert_schedule(idx, E)
+    d = x.shape[1]
+    y = np.zeros((T, d))
+    cache = {"a": {}, "b": {}, "h": {}, "o": {}}
+    # routed experts, one expert's rows at a time
+    for e in range(E):
+        rows = np.arange(offsets[e], offsets[e + 1])
+        if rows.size == 0:
+            continue
+        toks = perm_token[rows]
+        a, b, h, o = _ffn(x[toks], w_gate[e], w_up[e], w_down[e])
+        cache["a"][e], cache["b"][e], cache["h"][e], cache["o"][e] = a, b, h, o
+        g = w[toks, perm_slot[rows]]
+        np.add.at(y, toks, g[:, None] * o)
+    shared = None
+    if ws_gate is not None:
+        a_s, b_s, h_s, o_s = _ffn(x, ws_gate, ws_up, ws_down)
+        y += o_s  # R1: weight 1
+        shared = {"a": a_s, "b": b_s, "h": h_s}
+    return {
+        "y": y, "logits": logits, "topk_idx": idx, "topk_w": w, "counts": counts,
+        "offsets": offsets, "perm_token": perm_token, "perm_slot": perm_slot,
+        "route_row": route_row, "cache": cache, "shared": shared,
+    }
+
+
+# ---------------------------------------------------------------- backward
+def moe_backward(x, w_router, w_gate, w_up, w_down, dy, fwd,
+                 ws_gate=None, ws_up=None, ws_down=None):
+    """Gradients of L = sum(dy * y) for the forward `fwd` (from moe_forward).
+
+    Per route (t, j) with expert e and weight g, o = W_down h, h = SiLU(a)*b:
+      dh      = W_down^T dy_t                       (down-projection dgrad)
+      dg_tj   = <h, dh>                             [Blog, "Router weight gradient computation"]
+      dW_down += dy_t (g h)^T
+      da      = g dh * b * SiLU'(a);  db = g dh * SiLU(a)
+      dW_gate += da x_t^T;  dW_up += db x_t^T;  dx_t += W_gate^T da + W_up^T db
+    Router (R2, R5): g = softmax over the selected logits, so for selected e
+      dl_te = g_te (dg_te - sum_i g_ti dg_ti), and 0 elsewhere;
+      dW_router = dl^T x;  dx += dl W_router.
+    Shared expert: the same SwiGLU backward with g = 1.
+    Returns a dict of float64 arrays.
+    """
+    x = _f64(x)
+    dy = _f64(dy)
+    T, d = x.shape
+    E = len(w_gate)
+    idx, w = fwd["topk_idx"], fwd["topk_w"]
+    k = idx.shape[1]
+    offsets, perm_token, perm_slot = fwd["offsets"], fwd["perm_token"], fwd["perm_slot"]
+    dx = np.zeros((T, d))
+    dWg, dWu, dWd = [], [], []
+    dg = np.zeros((T, k))
+    for e in range(E):
+        rows = np.arange(offsets[e], offsets[e + 1])
+        wg, wu, wd = _f64(w_gate[e]), _f64(w_up[e]), _f64(w_down[e])
+        if rows.size == 0:
+            dWg.append(np.zeros_like(wg))
+            dWu.append(np.zeros_like(wu))
+            dWd.append(np.zeros_like(wd))
+            continue
+        toks, slots = perm_token[rows], perm_slot[rows]
+        a, b, h = fwd["cache"]["a"][e], fwd["cache"]["b"][e], fwd["cache"]["h"][e]
+        g = w[toks, slots][:, None]
+        dy_e = dy[toks]
+        dh = dy_e @ wd
+        dg[toks, slots] = np.sum(dh * h, axis=1)
+        dWd.append(dy_e.T @ (g * h))
+        da = g * dh * _f64(b) * dsilu(a)
+        db = g * dh * silu(a)
+        dWg.append(da.T @ x[toks])
+        dWu.append(db.T @ x[toks])
+        np.add.at(dx, toks, da @ wg + db @ wu)
+    # router
+    s = np.sum(w * dg, axis=1, keepdims=True)
+    dl_sel = w * (dg - s)
+    dlogits = np.zeros((T, E))
+    np.put_along_axis(dlogits, idx, dl_sel, axis=1)
+    dW_router = dlogits.T @ x
+    dx += dlogits @ _f64(w_router)
+    out = {"dx": dx, "dW_gate": np.stack(dWg), "dW_up": np.stack(dWu),
+           "dW_down": np.stack(dWd), "dW_router": dW_router, "d_topk_w": dg,
+           "dlogits": dlogits}
+    if ws_gate is not None:
+        sh = fwd["shared"]
+        wsg, wsu, wsd = _f64(ws_gate), _f64(ws_up), _f64(ws_down)
+        dh_s = dy @ wsd
+        da_s = dh_s * sh["b"] * dsilu(sh["a"])
+        db_s = dh_s * silu(sh["a"])
+        out["dWs_down"] = dy.T @ sh["h"]
+        out["dWs_gate"] = da_s.T @ x
+        out["dWs_up"] = db_s.T @ x
+        dx += da_s @ wsg + db_s @ wsu
+    return out

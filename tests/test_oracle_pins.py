@@ -1,0 +1,259 @@
+"""Pins for the CPU oracle: checks against what the method and mathematics fix
+(brute force, closed forms, library routines, finite differences), never
+against the oracle's own formulas retyped.  CPU only."""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from oracle import moe_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ------------------------------------------------------------------ top-k
+def _brute_topk_set(row, k):
+    """Max-sum k-subset; among equal sums the lexicographically smallest."""
+    best, best_key = None, None
+    for comb in itertools.combinations(range(len(row)), k):
+        key = (-sum(row[c] for c in comb), comb)
+        if best_key is None or key < best_key:
+            best, best_key = comb, key
+    return best
+
+
+@pytest.mark.parametrize("ties", [False, True])
+def test_topk_matches_bruteforce_subsets(ties):
+    rng = _rng(1 if ties else 2)
+    T, E, k = 60, 7, 3
+    logits = (rng.integers(-2, 3, (T, E)) * 0.5) if ties else rng.normal(size=(T, E))
+    idx, w = O.topk_route(logits, k)
+    for t in range(T):
+        assert tuple(sorted(idx[t])) == _brute_topk_set(list(logits[t]), k)
+        # slot order: non-increasing logits, ties in ascending expert index
+        for j in range(k - 1):
+            a, b = logits[t, idx[t, j]], logits[t, idx[t, j + 1]]
+            assert a > b or (a == b and idx[t, j] < idx[t, j + 1])
+
+
+def test_topk_weights_are_softmax_over_selected():
+    rng = _rng(3)
+    logits = rng.normal(size=(40, 16)) * 3
+    idx, w = O.topk_route(logits, 5)
+    sel = np.take_along_axis(logits, idx, axis=1)
+    np.testing.assert_allclose(w, scipy.special.softmax(sel, axis=1), rtol=1e-13, atol=0)
+    np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-15)
+
+
+def test_topk_uniform_logits_k_equals_E():
+    E = 8
+    idx, w = O.topk_route(np.zeros((5, E)), E)
+    assert (idx == np.arange(E)).all()
+    np.testing.assert_allclose(w, 1.0 / E, rtol=0, atol=1e-16)
+
+
+def test_topk_golden_ties():
+    g = json.load(open(os.path.join(GOLDEN, "topk_ties.json")))
+    idx, w = O.topk_route(np.array(g["logits"]), g["k"])
+    assert idx.tolist() == g["expected_idx"]
+    np.testing.assert_allclose(w, np.array(g["expected_w"]), rtol=1e-14)
+
+
+def test_topk_ignores_minus_inf_experts():
+    logits = np.array([[0.1, -np.inf, 0.3, -np.inf, 0.2]])
+    idx, w = O.topk_route(logits, 3)
+    assert idx.tolist() == [[2, 4, 0]]
+    assert np.isfinite(w).all()
+
+
+# ------------------------------------------------------------------ schedule
+@pytest.mark.parametrize("seed", [0, 1])
+def test_schedule_bruteforce(seed):
+    rng = _rng(seed)
+    T, E, k = 37, 9, 3
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    counts, offsets, perm_token, perm_slot, route_row = O.expert_schedule(idx, E)
+    # brute force: expert by expert, every (t, j) in ascending order
+    rows = []
+    for e in range(E):
+        rows += [(t, j) for t in range(T) for j in range(k) if idx[t, j] == e]
+    assert list(zip(perm_token.tolist(), perm_slot.tolist())) == rows
+    assert counts.sum() == T * k
+    assert sorted(perm_token.tolist()) == sorted(np.repeat(np.arange(T), k).tolist())
+    for t in range(T):
+        for j in range(k):
+            r = route_row[t, j]
+            assert perm_token[r] == t and perm_slot[r] == j
+            e = idx[t, j]
+            assert offsets[e] <= r < offsets[e + 1]
+    assert offsets[0] == 0 and (np.diff(offsets) == counts).all()
+
+
+def test_schedule_empty_experts():
+    idx = np.array([[0, 2], [2, 0]])
+    counts, offsets, perm_token, _, _ = O.expert_schedule(idx, 4)
+    assert counts.tolist() == [2, 0, 2, 0]
+    assert offsets.tolist() == [0, 2, 2, 4, 4]
+    assert perm_token.tolist() == [0, 1, 0, 1]
+
+
+# ------------------------------------------------------------------ forward
+def _weights(rng, E, d, I, I_s, std=0.3):
+    wg = rng.normal(size=(E, I, d)) * std
+    wu = rng.normal(size=(E, I, d)) * std
+    wd = rng.normal(size=(E, d, I)) * std
+    ws = (rng.normal(size=(I_s, d)) * std, rng.normal(size=(I_s, d)) * std,
+          rng.normal(size=(d, I_s)) * std)
+    return wg, wu, wd, ws
+
+
+def test_silu_special_values():
+    np.testing.assert_allclose(O.silu([0.0, 1.0, -1.0, 50.0, -800.0]),
+                               [0.0, 1.0 / (1.0 + np.exp(-1.0)), -1.0 / (1.0 + np.e), 50.0, 0.0],
+                               rtol=1e-15, atol=1e-300)
+    # SiLU(z) = z * scipy.special.expit(z)
+    z = np.linspace(-20, 20, 101)
+    np.testing.assert_allclose(O.silu(z), z * scipy.special.expit(z), rtol=1e-14, atol=1e-300)
+
+
+def test_forward_dense_reduction_k_equals_E():
+    """k = E and W_router = 0: every expert gets weight 1/E, so
+    y = shared(x) + mean_e FFN_e(x), computed here with einsum over all experts."""
+    rng = _rng(4)
+    T, d, I, E, I_s = 6, 10, 4, 5, 3
+    x = rng.normal(size=(T, d))
+    wg, wu, wd, (sg, su, sd) = _weights(rng, E, d, I, I_s)
+    fwd = O.moe_forward(x, np.zeros((E, d)), wg, wu, wd, E, ws_gate=sg, ws_up=su, ws_down=sd)
+    a = np.einsum("eid,td->eti", wg, x)
+    b = np.einsum("eid,td->eti", wu, x)
+    h = a * scipy.special.expit(a) * b
+    routed = np.einsum("edi,eti->td", wd, h) / E
+    a_s, b_s = x @ sg.T, x @ su.T
+    shared = (a_s * scipy.special.expit(a_s) * b_s) @ sd.T
+    np.testing.assert_allclose(fwd["y"], routed + shared, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_single_expert_closed_form():
+    """E = 1, k = 1: g = 1, y = W_d (SiLU(W_g x) * W_u x) + shared(x), via torch float64."""
+    rng = _rng(5)
+    T, d, I, I_s = 7, 12, 5, 3
+    x = rng.normal(size=(T, d))
+    wg, wu, wd, (sg, su, sd) = _weights(rng, 1, d, I, I_s)
+    wr = rng.normal(size=(1, d))
+    fwd = O.moe_forward(x, wr, wg, wu, wd, 1, ws_gate=sg, ws_up=su, ws_down=sd)
+    X = torch.from_numpy(x)
+    F = torch.nn.functional
+    ref = F.linear(F.silu(F.linear(X, torch.from_numpy(wg[0]))) * F.linear(X, torch.from_numpy(wu[0])),
+                   torch.from_numpy(wd[0]))
+    ref += F.linear(F.silu(F.linear(X, torch.from_numpy(sg))) * F.linear(X, torch.from_numpy(su)),
+                    torch.from_numpy(sd))
+    np.testing.assert_allclose(fwd["y"], ref.numpy(), rtol=1e-12, atol=1e-12)
+    assert (fwd["topk_w"] == 1.0).all()
+
+
+def test_forward_token_independence():
+    """The forward of a token subset equals the matching rows of the full forward."""
+    rng = _rng(6)
+    T, d, I, E, k = 20, 8, 4, 6, 2
+    x = rng.normal(size=(T, d))
+    wg, wu, wd, _ = _weights(rng, E, d, I, 1)
+    wr = rng.normal(size=(E, d))
+    full = O.moe_forward(x, wr, wg, wu, wd, k)["y"]
+    sub = [3, 11, 17]
+    part = O.moe_forward(x[sub], wr, wg, wu, wd, k)["y"]
+    np.testing.assert_allclose(part, full[sub], rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------------ backward
+def _tiny_problem(seed=7):
+    rng = _rng(seed)
+    T, d, I, E, k, I_s = 3, 8, 4, 4, 2, 4
+    x = rng.normal(size=(T, d))
+    wr = rng.normal(size=(E, d)) * 0.7
+    wg, wu, wd, (sg, su, sd) = _weights(rng, E, d, I, I_s, std=0.4)
+    dy = rng.normal(size=(T, d))
+    return dict(x=x, wr=wr, wg=wg, wu=wu, wd=wd, sg=sg, su=su, sd=sd, dy=dy, k=k)
+
+
+def _loss(P):
+    y = O.moe_forward(P["x"], P["wr"], P["wg"], P["wu"], P["wd"], P["k"],
+                      ws_gate=P["sg"], ws_up=P["su"], ws_down=P["sd"])["y"]
+    return float(np.sum(P["dy"] * y))
+
+
+def test_backward_finite_differences():
+    P = _tiny_problem()
+    fwd = O.moe_forward(P["x"], P["wr"], P["wg"], P["wu"], P["wd"], P["k"],
+                        ws_gate=P["sg"], ws_up=P["su"], ws_down=P["sd"])
+    # no top-k boundary may sit within the step: gap between k-th and (k+1)-th logit
+    srt = -np.sort(-fwd["logits"], axis=1)
+    assert (srt[:, P["k"] - 1] - srt[:, P["k"]]).min() > 1e-3
+    G = O.moe_backward(P["x"], P["wr"], P["wg"], P["wu"], P["wd"], P["dy"], fwd,
+                       ws_gate=P["sg"], ws_up=P["su"], ws_down=P["sd"])
+    eps = 1e-6
+    pairs = [("x", "dx"), ("wr", "dW_router"), ("wg", "dW_gate"), ("wu", "dW_up"),
+             ("wd", "dW_down"), ("sg", "dWs_gate"), ("su", "dWs_up"), ("sd", "dWs_down")]
+    for pname, gname in pairs:
+        base = P[pname]
+        num = np.zeros_like(base)
+        it = np.nditer(base, flags=["multi_index"])
+        for _ in it:
+            i = it.multi_index
+            orig = base[i]
+            base[i] = orig + eps
+            lp = _loss(P)
+            base[i] = orig - eps
+            lm = _loss(P)
+            base[i] = orig
+            num[i] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(G[gname], num, rtol=1e-6, atol=1e-7, err_msg=gname)
+
+
+def test_router_weight_grad_is_output_inner_product():
+    """dL/dg_tj = <dy_t, o_tj>, with o the expert's down-projection output:
+    the oracle's <h, W_down^T dy> must equal it."""
+    P = _tiny_problem(8)
+    fwd = O.moe_forward(P["x"], P["wr"], P["wg"], P["wu"], P["wd"], P["k"])
+    G = O.moe_backward(P["x"], P["wr"], P["wg"], P["wu"], P["wd"], P["dy"], fwd)
+    for t in range(P["x"].shape[0]):
+        for j in range(P["k"]):
+            e = fwd["topk_idx"][t, j]
+            xt = P["x"][t]
+            a, b = P["wg"][e] @ xt, P["wu"][e] @ xt
+            o = P["wd"][e] @ (a * scipy.special.expit(a) * b)
+            assert G["d_topk_w"][t, j] == pytest.approx(float(P["dy"][t] @ o), rel=1e-12, abs=1e-12)
+
+
+def test_backward_single_expert_router_grad_is_zero():
+    """E = 1: g is the constant 1, so the logits (and W_router) get no gradient."""
+    rng = _rng(9)
+    T, d, I = 5, 6, 3
+    x = rng.normal(size=(T, d))
+    wg, wu, wd, _ = _weights(rng, 1, d, I, 1)
+    wr = rng.normal(size=(1, d))
+    dy = rng.normal(size=(T, d))
+    fwd = O.moe_forward(x, wr, wg, wu, wd, 1)
+    G = O.moe_backward(x, wr, wg, wu, wd, dy, fwd)
+    assert (G["dlogits"] == 0).all() and (G["dW_router"] == 0).all()
+
+
+def test_backward_empty_expert_gets_zero_grad():
+    rng = _rng(10)
+    T, d, I, E = 4, 6, 3, 3
+    x = rng.normal(size=(T, d))
+    wg, wu, wd, _ = _weights(rng, E, d, I, 1)
+    wr = np.zeros((E, d))
+    bias = np.array([0.0, 0.0, -np.inf])
+    dy = rng.normal(size=(T, d))
+    fwd = O.moe_forward(x, wr, wg, wu, wd, 2, router_bias=bias)
+    assert fwd["counts"][2] == 0
+    G = O.moe_backward(x, wr, wg, wu, wd, dy, fwd)
+    assert (G["dW_gate"][2] == 0).all() and (G["dW_down"][2] == 0).all()
