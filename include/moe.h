@@ -1,0 +1,145 @@
+/*
+ * libmoe: a single-GPU DeepSeek-V3-style Mixture-of-Experts layer for GB300
+ * (sm_103a).  C ABI: plain pointers and sizes, no framework types.
+ *
+ * The layer (Mixture-of-Kittens blog post, section "Overlapping computation
+ * and communication in MoE"; "Mixture-of-Kittens: MoE Megakernel for NVL72s",
+ * section 2.1), per token t with x_t in R^d:
+ *
+ *   logits_t = W_router x_t (+ router_bias)                 router projection
+ *   (e_t0..e_t,k-1) = top-k of logits_t, descending, ties to the lower index
+ *   g_tj = softmax of the selected logits (= full softmax renormalized on them)
+ *   FFN_e(v) = W_down[e] (SiLU(W_gate[e] v) * (W_up[e] v))   SwiGLU expert
+ *   y_t = FFN_shared(x_t) + sum_j g_tj FFN_{e_tj}(x_t)       shared weight is 1
+ *
+ * Routes are grouped by expert with the two-pass counting schedule of the
+ * blog's "Scheduling" section (count, prefix offsets, stable write in
+ * (token, slot) order).  Floating-point work happens in a fixed order, so every
+ * output is bitwise reproducible run to run ("Determinism" section).  The
+ * backward returns the router-weight gradient <h, W_down^T dy> ("Router weight
+ * gradient computation" section) and propagates it through the softmax into
+ * W_router and x.
+ *
+ * Conventions for every entry point
+ *   - Matrices are row-major and contiguous; "bf16" is IEEE bfloat16.
+ *   - All pointers are DEVICE pointers unless stated otherwise, 16-byte
+ *     aligned.  The caller owns every buffer; the library never allocates,
+ *     frees or keeps a pointer after returning.
+ *   - `stream` is a cudaStream_t passed as void*; all work is enqueued on it
+ *     and nothing synchronizes the host (except moe_read_device_status).
+ *     Buffers must stay valid until the stream has executed the work.
+ *   - Argument and shape checks run before anything is enqueued: on any
+ *     error return nothing has been launched.
+ *   - Supported shapes: 1 <= E <= 512, 1 <= top_k <= min(E, 32),
+ *     d, I, I_shared multiples of 64, d >= 64, T*top_k + E*127 < 2^31.
+ *     T == 0 is valid and does nothing.  Other shapes give MOE_ERR_UNSUPPORTED.
+ *   - Device-side problems (a bounded wait that ran out) are recorded in a
+ *     status word at the start of the workspace; see moe_read_device_status.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, negative size */
+  MOE_ERR_UNSUPPORTED = 2,    /* shape or precision outside the supported set */
+  MOE_ERR_WORKSPACE = 3,      /* workspace pointer missing */
+  MOE_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE = 5,         /* a kernel saw an invalid value */
+  MOE_ERR_DEVICE_TIMEOUT = 6  /* a kernel's bounded wait ran out */
+} moe_status;
+
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
+
+typedef struct {
+  int64_t T;        /* tokens */
+  int64_t d;        /* model dimension */
+  int64_t I;        /* routed expert intermediate dimension */
+  int64_t E;        /* routed experts */
+  int64_t top_k;    /* experts per token */
+  int64_t n_shared; /* shared experts: 0 or 1 */
+  int64_t I_shared; /* shared expert intermediate dimension (ignored if n_shared == 0) */
+  int32_t precision;/* moe_precision; only MOE_BF16 is implemented */
+  uint32_t flags;   /* reserved, must be 0 */
+} moe_config;
+
+typedef struct {
+  const void* W_router;     /* [E, d] bf16 */
+  const float* router_bias; /* [E] fp32, or NULL; a constant (no gradient) */
+  const void* W_gate;       /* [E, I, d] bf16 */
+  const void* W_up;         /* [E, I, d] bf16 */
+  const void* W_down;       /* [E, d, I] bf16 */
+  const void* Ws_gate;      /* [I_s, d] bf16 (n_shared == 1) */
+  const void* Ws_up;        /* [I_s, d] bf16 */
+  const void* Ws_down;      /* [d, I_s] bf16 */
+} moe_weights;
+
+typedef struct {
+  float* dW_router; /* [E, d] fp32 */
+  void* dW_gate;    /* [E, I, d] bf16 */
+  void* dW_up;      /* [E, I, d] bf16 */
+  void* dW_down;    /* [E, d, I] bf16 */
+  void* dWs_gate;   /* [I_s, d] bf16 (n_shared == 1) */
+  void* dWs_up;     /* [I_s, d] bf16 */
+  void* dWs_down;   /* [d, I_s] bf16 */
+  float* d_topk_w;  /* [T, top_k] fp32 router-weight gradient dL/dg, or NULL */
+} moe_grads;
+
+/* Byte sizes of the caller-allocated buffers for a configuration:
+ *   fwd_ws  scratch for moe_forward and moe_route_topk
+ *   saved   state moe_forward leaves for moe_backward (routing, a and b)
+ *   bwd_ws  scratch for moe_backward
+ * Each buffer must be 256-byte aligned; its first 256 bytes hold the device
+ * status word and must be zero before the buffer's first use. */
+moe_status moe_workspace_size(const moe_config* cfg, size_t* fwd_ws, size_t* saved, size_t* bwd_ws);
+
+/* Router projection, softmax + top-k and the expert schedule (blog sections
+ * "Overlapping computation and communication in MoE" and "Scheduling").
+ *   x [T, d] bf16; W_router [E, d] bf16; router_bias [E] fp32 or NULL.
+ *   logits_in  [T, E] fp32 or NULL: when given, route these logits instead of
+ *              computing them (x and W_router may then be NULL).
+ *   logits_out [T, E] fp32 or NULL: receives the computed logits.
+ *   topk_idx [T, k] int32, topk_w [T, k] fp32: slots in descending-logit order.
+ *   counts [E] int32: routes per expert.  offsets [E+1] int32: exclusive
+ *   prefix sum of counts.  perm_token [T*k] int32: row r of the expert-grouped
+ *   order -> token.  route_row [T, k] int32: (token, slot) -> row.
+ *   Rows of one expert are in ascending (token, slot) order.
+ *   ws: forward workspace. */
+moe_status moe_route_topk(const moe_config* cfg, const void* x, const void* W_router,
+                          const float* router_bias, const float* logits_in, float* logits_out,
+                          int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                          int32_t* perm_token, int32_t* route_row, void* ws, void* stream);
+
+/* Forward of the whole layer: y [T, d] bf16 from x [T, d] bf16.
+ * saved: buffer of moe_workspace_size's `saved` bytes that moe_backward will
+ * read, or NULL for inference.  ws: forward workspace. */
+moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* w, void* y,
+                       void* saved, void* ws, void* stream);
+
+/* Backward of the layer for L = sum(dy * y), given the `saved` buffer of the
+ * matching moe_forward call.  dy [T, d] bf16 -> dx [T, d] bf16 and every
+ * weight gradient in `g` (all of them required, d_topk_w optional).  Gradients
+ * are written, not accumulated.  ws: backward workspace. */
+moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights* w, const void* dy,
+                        const void* saved, void* dx, const moe_grads* g, void* ws, void* stream);
+
+/* Synchronizes `stream`, reads the status word of workspace `ws` (device
+ * pointer), resets it to zero and returns it (MOE_OK when no kernel recorded a
+ * problem). */
+moe_status moe_read_device_status(void* ws, void* stream);
+
+/* Static English description of a status code. */
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,10 @@
+"""GB300-native single-GPU DeepSeek-V3-style MoE layer: a C-ABI CUDA library
+(libmoe.so, include/moe.h) and its Python binding."""
+from . import _abi
+from ._abi import (MoeConfig, MoeError, MoeGrads, MoeWeights, make_config, make_grads, make_weights,
+                   moe_backward, moe_forward, moe_read_device_status, moe_route_topk,
+                   moe_workspace_size)
+
+__all__ = ["MoeConfig", "MoeError", "MoeGrads", "MoeWeights", "make_config", "make_grads",
+           "make_weights", "moe_backward", "moe_forward", "moe_read_device_status",
+           "moe_route_topk", "moe_workspace_size", "_abi"]

@@ -1,0 +1,209 @@
+// Memory-bound kernels of the layer.  Each sums in one fixed order with no
+// floating-point atomics, so results are bitwise reproducible (Mixture-of-
+// Kittens blog post, section "Determinism"):
+//   combine        y_t = y_shared,t + sum_j o[row(t, j)]          (weighted sum;
+//                  the router weight is already applied by the down GEMM)
+//   router_grad    dg_tj = sum of the per-n-tile partials of <h, dh>, then the
+//                  softmax backward dl_tj = g_tj (dg_tj - sum_i g_ti dg_ti)
+//   router_wgrad   dW_router[e] = sum over e's rows (ascending) of dl_row x_token
+//   unpermute      dx_t = dx_shared,t + sum_j dxp[row(t, j)] + sum_j dl_tj W_router[e_tj]
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16lo(w[i]);
+    v[2 * i + 1] = bf16hi(w[i]);
+  }
+}
+__device__ __forceinline__ void st8(__nv_bfloat16* p, const float (&v)[8]) {
+  uint4 a;
+  a.x = pack_bf16x2(v[0], v[1]);
+  a.y = pack_bf16x2(v[2], v[3]);
+  a.z = pack_bf16x2(v[4], v[5]);
+  a.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = a;
+}
+
+constexpr int kEwThreads = 128;
+
+__global__ void __launch_bounds__(kEwThreads)
+    combine_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ ys,
+                   const int32_t* __restrict__ route_row_pad, int d, int k,
+                   __nv_bfloat16* __restrict__ y) {
+  __shared__ long long rows[kMaxTopK];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k)
+    rows[threadIdx.x] = static_cast<long long>(__ldg(route_row_pad + static_cast<size_t>(t) * k + threadIdx.x)) * d;
+  __syncthreads();
+  const int nv = d / 8;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float acc[8];
+    if (ys) {
+      ld8(ys + static_cast<size_t>(t) * d + 8 * v, acc);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    }
+    for (int j = 0; j < k; ++j) {
+      float u[8];
+      ld8(o + rows[j] + 8 * v, u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += u[i];
+    }
+    st8(y + static_cast<size_t>(t) * d + 8 * v, acc);
+  }
+}
+
+// one warp per token, lane j owns slot j
+__global__ void __launch_bounds__(256)
+    router_grad_kernel(const float* __restrict__ dg_part, int nparts,
+                       const int32_t* __restrict__ route_row_pad, const float* __restrict__ topk_w,
+                       int T, int k, float* __restrict__ d_topk_w, float* __restrict__ dl_tk,
+                       float* __restrict__ dl_row) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  float dg = 0.f, g = 0.f;
+  int row = 0;
+  if (lane < k) {
+    const size_t tj = static_cast<size_t>(t) * k + lane;
+    row = __ldg(route_row_pad + tj);
+    g = __ldg(topk_w + tj);
+    const float* pp = dg_part + static_cast<size_t>(row) * nparts;
+    for (int p = 0; p < nparts; ++p) dg += __ldg(pp + p);
+  }
+  float s = g * dg;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane < k) {
+    const size_t tj = static_cast<size_t>(t) * k + lane;
+    const float dl = g * (dg - s);
+    if (d_topk_w) d_topk_w[tj] = dg;
+    dl_tk[tj] = dl;
+    dl_row[row] = dl;
+  }
+}
+
+// grid (E, ceil(d / 512)); each thread owns two adjacent columns
+constexpr int kRwThreads = 256;
+__global__ void __launch_bounds__(kRwThreads)
+    router_wgrad_kernel(const float* __restrict__ dl_row, const int32_t* __restrict__ perm_token_pad,
+                        const int32_t* __restrict__ row_start, const int32_t* __restrict__ counts,
+                        const __nv_bfloat16* __restrict__ x, int d, float* __restrict__ dW) {
+  __shared__ int s_tok[kRwThreads];
+  __shared__ float s_dl[kRwThreads];
+  const int e = blockIdx.x;
+  const int c = (blockIdx.y * kRwThreads + threadIdx.x) * 2;
+  const int r0 = __ldg(row_start + e);
+  const int n = __ldg(counts + e);
+  float a0 = 0.f, a1 = 0.f;
+  for (int base = 0; base < n; base += kRwThreads) {
+    const int m = min(kRwThreads, n - base);
+    __syncthreads();
+    if (threadIdx.x < m) {
+      s_tok[threadIdx.x] = __ldg(perm_token_pad + r0 + base + threadIdx.x);
+      s_dl[threadIdx.x] = __ldg(dl_row + r0 + base + threadIdx.x);
+    }
+    __syncthreads();
+    if (c < d) {
+      for (int i = 0; i < m; ++i) {
+        const uint32_t w =
+            __ldg(reinterpret_cast<const unsigned int*>(x + static_cast<size_t>(s_tok[i]) * d + c));
+        a0 += s_dl[i] * bf16lo(w);
+        a1 += s_dl[i] * bf16hi(w);
+      }
+    }
+  }
+  if (c < d) {
+    dW[static_cast<size_t>(e) * d + c] = a0;
+    dW[static_cast<size_t>(e) * d + c + 1] = a1;
+  }
+}
+
+__global__ void __launch_bounds__(kEwThreads)
+    unpermute_kernel(const __nv_bfloat16* __restrict__ dxp, const __nv_bfloat16* __restrict__ dxs,
+                     const int32_t* __restrict__ route_row_pad, const int32_t* __restrict__ topk_idx,
+                     const float* __restrict__ dl_tk, const __nv_bfloat16* __restrict__ Wr, int d,
+                     int k, __nv_bfloat16* __restrict__ dx) {
+  __shared__ long long rows[kMaxTopK];
+  __shared__ long long erows[kMaxTopK];
+  __shared__ float dls[kMaxTopK];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) {
+    const size_t tj = static_cast<size_t>(t) * k + threadIdx.x;
+    rows[threadIdx.x] = static_cast<long long>(__ldg(route_row_pad + tj)) * d;
+    erows[threadIdx.x] = static_cast<long long>(__ldg(topk_idx + tj)) * d;
+    dls[threadIdx.x] = __ldg(dl_tk + tj);
+  }
+  __syncthreads();
+  const int nv = d / 8;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float acc[8];
+    if (dxs) {
+      ld8(dxs + static_cast<size_t>(t) * d + 8 * v, acc);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    }
+    for (int j = 0; j < k; ++j) {
+      float u[8];
+      ld8(dxp + rows[j] + 8 * v, u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += u[i];
+    }
+    for (int j = 0; j < k; ++j) {
+      float u[8];
+      ld8(Wr + erows[j] + 8 * v, u);
+      const float s = dls[j];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += s * u[i];
+    }
+    st8(dx + static_cast<size_t>(t) * d + 8 * v, acc);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const __nv_bfloat16* o, const __nv_bfloat16* ys,
+                           const int32_t* route_row_pad, int T, int d, int k, __nv_bfloat16* y,
+                           cudaStream_t st) {
+  combine_kernel<<<T, kEwThreads, 0, st>>>(o, ys, route_row_pad, d, k, y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_grad(const float* dg_part, int nparts, const int32_t* route_row_pad,
+                               const float* topk_w, int T, int k, float* d_topk_w, float* dl_tk,
+                               float* dl_row, cudaStream_t st) {
+  router_grad_kernel<<<(T + 7) / 8, 256, 0, st>>>(dg_part, nparts, route_row_pad, topk_w, T, k,
+                                                 d_topk_w, dl_tk, dl_row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_wgrad(const float* dl_row, const int32_t* perm_token_pad,
+                                const int32_t* row_start, const int32_t* counts,
+                                const __nv_bfloat16* x, int E, int d, float* dW_router,
+                                cudaStream_t st) {
+  dim3 grid(E, (d + 2 * kRwThreads - 1) / (2 * kRwThreads));
+  router_wgrad_kernel<<<grid, kRwThreads, 0, st>>>(dl_row, perm_token_pad, row_start, counts, x, d,
+                                                   dW_router);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute(const __nv_bfloat16* dxp, const __nv_bfloat16* dxs,
+                             const int32_t* route_row_pad, const int32_t* topk_idx,
+                             const float* dl_tk, const __nv_bfloat16* W_router, int T, int d,
+                             int k, __nv_bfloat16* dx, cudaStream_t st) {
+  unpermute_kernel<<<T, kEwThreads, 0, st>>>(dxp, dxs, route_row_pad, topk_idx, dl_tk, W_router, d,
+                                             k, dx);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,604 @@
+// Host side of libmoe: argument checks, workspace carving, tensor maps and the
+// launch sequence of the forward and backward passes.  Everything is enqueued
+// on the caller's stream; the host never waits for the device.
+#include <stdlib.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "gemm_launch.cuh"
+#include "moe_internal.h"
+#include "tc_gemm.cuh"
+#include "tmap.h"
+
+namespace moe {
+
+int gemm_smem_bytes() { return kGemmSmemBytes; }
+
+int device_sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev < 64) {
+    const int c = cache[dev].load();
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  if (dev < 64) cache[dev].store(n);
+  return n;
+}
+
+cudaError_t launch_gemm(GemmKind kind, const GemmParams& p, int grid, cudaStream_t st) {
+  if (kind <= GK_DOWN) return launch_gemm_fwd(kind, p, grid, st);
+  return launch_gemm_bwd(kind, p, grid, st);
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+struct Shape {
+  int64_t T, d, I, E, k, S, Is, R, Rp, nchunk, nparts;
+};
+
+// Carves 256-byte aligned sub-buffers from a base pointer (or only sizes them
+// when base is null).
+struct Carver {
+  char* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+  template <class T>
+  T* take(int64_t n) {
+    off = (off + kAlign - 1) / kAlign * kAlign;
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += static_cast<size_t>(n) * sizeof(T);
+    return p;
+  }
+};
+
+struct Routing {
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* row_start;
+  int32_t* perm_token;
+  int32_t* route_row;
+  int32_t* perm_token_pad;
+  int32_t* route_row_pad;
+  float* perm_w_pad;
+};
+
+void carve_routing(Carver& c, const Shape& s, Routing& r) {
+  r.topk_idx = c.take<int32_t>(s.T * s.k);
+  r.topk_w = c.take<float>(s.T * s.k);
+  r.counts = c.take<int32_t>(s.E);
+  r.offsets = c.take<int32_t>(s.E + 1);
+  r.row_start = c.take<int32_t>(s.E + 1);
+  r.perm_token = c.take<int32_t>(s.R);
+  r.route_row = c.take<int32_t>(s.T * s.k);
+  r.perm_token_pad = c.take<int32_t>(s.Rp);
+  r.route_row_pad = c.take<int32_t>(s.T * s.k);
+  r.perm_w_pad = c.take<float>(s.Rp);
+}
+
+struct Saved {
+  Routing rt;
+  __nv_bfloat16* ab;   // [Rp, 2I]
+  __nv_bfloat16* abs;  // [T, 2Is]
+};
+void carve_saved(void* base, const Shape& s, Saved& v, size_t* bytes) {
+  Carver c(base);
+  c.take<char>(kAlign);
+  carve_routing(c, s, v.rt);
+  v.ab = c.take<__nv_bfloat16>(s.Rp * 2 * s.I);
+  v.abs = c.take<__nv_bfloat16>(s.S ? s.T * 2 * s.Is : 0);
+  if (bytes) *bytes = c.off;
+}
+
+struct FwdWs {
+  int* status;
+  float* logits;
+  int32_t* chunk_counts;
+  int32_t* chunk_base;
+  Routing rt;          // used when the caller keeps no saved state
+  __nv_bfloat16* h;    // [Rp, I]
+  __nv_bfloat16* hs;   // [T, Is]
+  __nv_bfloat16* o;    // [Rp, d]
+  __nv_bfloat16* ys;   // [T, d]
+};
+void carve_fwd(void* base, const Shape& s, FwdWs& w, size_t* bytes) {
+  Carver c(base);
+  w.status = c.take<int>(kAlign / sizeof(int));
+  w.logits = c.take<float>(s.T * s.E);
+  w.chunk_counts = c.take<int32_t>(s.nchunk * s.E);
+  w.chunk_base = c.take<int32_t>(s.nchunk * s.E);
+  carve_routing(c, s, w.rt);
+  w.h = c.take<__nv_bfloat16>(s.Rp * s.I);
+  w.hs = c.take<__nv_bfloat16>(s.S ? s.T * s.Is : 0);
+  w.o = c.take<__nv_bfloat16>(s.Rp * s.d);
+  w.ys = c.take<__nv_bfloat16>(s.S ? s.T * s.d : 0);
+  if (bytes) *bytes = c.off;
+}
+
+struct BwdWs {
+  int* status;
+  __nv_bfloat16* dadb;   // [Rp, 2I]
+  __nv_bfloat16* hg;     // [Rp, I]
+  float* dg_part;        // [Rp, nparts]
+  __nv_bfloat16* dadbs;  // [T, 2Is]
+  __nv_bfloat16* hs;     // [T, Is]
+  float* dl_tk;          // [T, k]
+  float* dl_row;         // [Rp]
+  __nv_bfloat16* dxp;    // [Rp, d]
+  __nv_bfloat16* dxs;    // [T, d]
+};
+void carve_bwd(void* base, const Shape& s, BwdWs& w, size_t* bytes) {
+  Carver c(base);
+  w.status = c.take<int>(kAlign / sizeof(int));
+  w.dadb = c.take<__nv_bfloat16>(s.Rp * 2 * s.I);
+  w.hg = c.take<__nv_bfloat16>(s.Rp * s.I);
+  w.dg_part = c.take<float>(s.Rp * s.nparts);
+  w.dadbs = c.take<__nv_bfloat16>(s.S ? s.T * 2 * s.Is : 0);
+  w.hs = c.take<__nv_bfloat16>(s.S ? s.T * s.Is : 0);
+  w.dl_tk = c.take<float>(s.T * s.k);
+  w.dl_row = c.take<float>(s.Rp);
+  w.dxp = c.take<__nv_bfloat16>(s.Rp * s.d);
+  w.dxs = c.take<__nv_bfloat16>(s.S ? s.T * s.d : 0);
+  if (bytes) *bytes = c.off;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_config(const moe_config* cfg, Shape& s) {
+  if (!cfg) return MOE_ERR_INVALID_ARG;
+  if (cfg->T < 0 || cfg->d <= 0 || cfg->I <= 0 || cfg->E <= 0 || cfg->top_k <= 0 ||
+      cfg->n_shared < 0 || (cfg->n_shared && cfg->I_shared <= 0))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->precision != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (cfg->flags != 0) return MOE_ERR_UNSUPPORTED;
+  if (cfg->E > kMaxExperts || cfg->top_k > kMaxTopK || cfg->top_k > cfg->E) return MOE_ERR_UNSUPPORTED;
+  if (cfg->n_shared > 1) return MOE_ERR_UNSUPPORTED;
+  if (cfg->d % 64 || cfg->I % 64 || (cfg->n_shared && cfg->I_shared % 64)) return MOE_ERR_UNSUPPORTED;
+  s.T = cfg->T;
+  s.d = cfg->d;
+  s.I = cfg->I;
+  s.E = cfg->E;
+  s.k = cfg->top_k;
+  s.S = cfg->n_shared;
+  s.Is = cfg->n_shared ? cfg->I_shared : 0;
+  s.R = s.T * s.k;
+  s.Rp = s.R + s.E * (kRowAlign - 1);
+  s.nchunk = (s.T + kChunkTokens - 1) / kChunkTokens;
+  s.nparts = (s.I + kBN - 1) / kBN;
+  const int64_t lim = (int64_t(1) << 31) - 1;
+  if (s.Rp >= lim || s.T >= lim || s.d >= lim || s.I * s.E >= lim || s.d * s.E >= lim)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                        \
+  do {                                       \
+    const moe_status st__ = (expr);          \
+    if (st__ != MOE_OK) return st__;         \
+  } while (0)
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+void zero_params(GemmParams& p) { memset(static_cast<void*>(&p), 0, sizeof(p)); }
+
+// Tensor map over a row-major bf16 matrix [rows, cols] (pitch = cols).
+moe_status tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols, int box_rows) {
+  if (!make_tmap_bf16(m, base, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                      static_cast<uint64_t>(cols), box_cols, box_rows))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+// Persistent GEMM grid: one CTA per SM, fewer when there are fewer tiles.  The
+// environment variable MOE_GRID_LIMIT caps it further (used to check that
+// results do not depend on the grid size).
+int grid_for(int64_t max_tiles) {
+  int sms = device_sm_count();
+  if (const char* lim = getenv("MOE_GRID_LIMIT")) {
+    const int v = atoi(lim);
+    if (v > 0 && v < sms) sms = v;
+  }
+  if (max_tiles < 1) max_tiles = 1;
+  return static_cast<int>(max_tiles < sms ? max_tiles : sms);
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------- routing
+moe_status run_routing(const Shape& s, const void* x, const void* W_router, const float* bias,
+                       const float* logits_in, float* logits, const Routing& rt,
+                       int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t st) {
+  const float* lg = logits_in;
+  if (!lg) {
+    GemmParams p;
+    zero_params(p);
+    MOE_TRY(tmap(&p.tmA, x, s.T, s.d, 64, kBM));
+    MOE_TRY(tmap(&p.tmB0, W_router, s.E, s.d, 64, kBN));
+    p.dense_rows = static_cast<int>(s.T);
+    p.N = static_cast<int>(s.E);
+    p.K = static_cast<int>(s.d);
+    p.out = logits;
+    p.ldo = s.E;
+    p.bias = bias;
+    p.status = status;
+    MOE_CUDA(launch_gemm(GK_ROUTER, p, grid_for(cdiv(s.T, kBM) * cdiv(s.E, kBN)), st));
+    lg = logits;
+  }
+  MOE_CUDA(launch_topk_count(lg, static_cast<int>(s.T), static_cast<int>(s.E), static_cast<int>(s.k),
+                             rt.topk_idx, rt.topk_w, chunk_counts, status, st));
+  MOE_CUDA(launch_chunk_scan(chunk_counts, static_cast<int>(s.nchunk), static_cast<int>(s.E),
+                             chunk_base, rt.counts, st));
+  MOE_CUDA(launch_scatter(rt.topk_idx, rt.topk_w, static_cast<int>(s.T), static_cast<int>(s.E),
+                          static_cast<int>(s.k), chunk_base, rt.counts, rt.offsets, rt.row_start,
+                          rt.perm_token, rt.route_row, rt.perm_token_pad, rt.route_row_pad,
+                          rt.perm_w_pad, st));
+  return MOE_OK;
+}
+
+moe_status check_weights(const Shape& s, const moe_weights* w, bool need_router) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  if (need_router && (!w->W_router || !aligned16(w->W_router))) return MOE_ERR_INVALID_ARG;
+  const void* req[] = {w->W_gate, w->W_up, w->W_down};
+  for (const void* p : req)
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (s.S) {
+    const void* sh[] = {w->Ws_gate, w->Ws_up, w->Ws_down};
+    for (const void* p : sh)
+      if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status moe_workspace_size(const moe_config* cfg, size_t* fwd_ws, size_t* saved, size_t* bwd_ws) {
+  Shape s;
+  MOE_TRY(check_config(cfg, s));
+  if (fwd_ws) {
+    FwdWs w;
+    carve_fwd(nullptr, s, w, fwd_ws);
+  }
+  if (saved) {
+    Saved v;
+    carve_saved(nullptr, s, v, saved);
+  }
+  if (bwd_ws) {
+    BwdWs w;
+    carve_bwd(nullptr, s, w, bwd_ws);
+  }
+  return MOE_OK;
+}
+
+moe_status moe_route_topk(const moe_config* cfg, const void* x, const void* W_router,
+                          const float* router_bias, const float* logits_in, float* logits_out,
+                          int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                          int32_t* perm_token, int32_t* route_row, void* ws, void* stream) {
+  Shape s;
+  MOE_TRY(check_config(cfg, s));
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (s.T == 0) return MOE_OK;
+  if (!topk_idx || !topk_w || !counts || !offsets || !perm_token || !route_row)
+    return MOE_ERR_INVALID_ARG;
+  if (!logits_in && (!x || !W_router || !aligned16(x) || !aligned16(W_router))) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  FwdWs w;
+  carve_fwd(ws, s, w, nullptr);
+  Routing rt = w.rt;
+  rt.topk_idx = topk_idx;
+  rt.topk_w = topk_w;
+  rt.counts = counts;
+  rt.offsets = offsets;
+  rt.perm_token = perm_token;
+  rt.route_row = route_row;
+  float* logits = logits_out ? logits_out : w.logits;
+  return run_routing(s, x, W_router, router_bias, logits_in, logits, rt, w.chunk_counts,
+                     w.chunk_base, w.status, st);
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* wts, void* y,
+                       void* saved, void* ws, void* stream) {
+  Shape s;
+  MOE_TRY(check_config(cfg, s));
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (s.T == 0) return MOE_OK;
+  MOE_TRY(check_weights(s, wts, true));
+  if (!x || !y || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  FwdWs w;
+  carve_fwd(ws, s, w, nullptr);
+  Saved sv;
+  Routing rt = w.rt;
+  if (saved) {
+    carve_saved(saved, s, sv, nullptr);
+    rt = sv.rt;
+  }
+  MOE_TRY(run_routing(s, x, wts->W_router, wts->router_bias, nullptr, w.logits, rt, w.chunk_counts,
+                      w.chunk_base, w.status, st));
+  const int T = static_cast<int>(s.T), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
+  const int E = static_cast<int>(s.E);
+
+  // shared expert gate/up + SwiGLU (dense rows of x)
+  if (s.S) {
+    GemmParams p;
+    zero_params(p);
+    MOE_TRY(tmap(&p.tmA, x, s.T, s.d, 64, kBM));
+    MOE_TRY(tmap(&p.tmB0, wts->Ws_gate, s.Is, s.d, 64, kBN / 2));
+    MOE_TRY(tmap(&p.tmB1, wts->Ws_up, s.Is, s.d, 64, kBN / 2));
+    p.dense_rows = T;
+    p.N = static_cast<int>(s.Is);
+    p.K = d;
+    p.out = saved ? sv.abs : nullptr;
+    p.ldo = 2 * s.Is;
+    p.store_ab = saved ? 1 : 0;
+    p.out2 = w.hs;
+    p.ldo2 = s.Is;
+    p.I = static_cast<int>(s.Is);
+    p.status = w.status;
+    MOE_CUDA(launch_gemm(GK_GATEUP_DENSE, p, grid_for(cdiv(s.T, kBM) * cdiv(s.Is, kBN / 2)), st));
+  }
+  // routed gate/up + SwiGLU, x rows gathered by expert
+  {
+    GemmParams p;
+    zero_params(p);
+    MOE_TRY(tmap(&p.tmA, x, s.T, s.d, 64, 1));
+    MOE_TRY(tmap(&p.tmB0, wts->W_gate, s.E * s.I, s.d, 64, kBN / 2));
+    MOE_TRY(tmap(&p.tmB1, wts->W_up, s.E * s.I, s.d, 64, kBN / 2));
+    p.num_groups = E;
+    p.row_start = rt.row_start;
+    p.counts = rt.counts;
+    p.gather_idx = rt.perm_token_pad;
+    p.N = I;
+    p.K = d;
+    p.b_group_rows = I;
+    p.out = saved ? sv.ab : nullptr;
+    p.ldo = 2 * s.I;
+    p.store_ab = saved ? 1 : 0;
+    p.out2 = w.h;
+    p.ldo2 = s.I;
+    p.I = I;
+    p.status = w.status;
+    MOE_CUDA(launch_gemm(GK_GATEUP_ROUTED, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.I, kBN / 2)), st));
+  }
+  // routed down projection, scaled by the router weight of each row
+  {
+    GemmParams p;
+    zero_params(p);
+    MOE_TRY(tmap(&p.tmA, w.h, s.Rp, s.I, 64, kBM));
+    MOE_TRY(tmap(&p.tmB0, wts->W_down, s.E * s.d, s.I, 64, kBN));
+    p.num_groups = E;
+    p.row_start = rt.row_start;
+    p.counts = rt.counts;
+    p.N = d;
+    p.K = I;
+    p.b_group_rows = d;
+    p.out = w.o;
+    p.ldo = s.d;
+    p.row_scale = rt.perm_w_pad;
+    p.status = w.status;
+    MOE_CUDA(launch_gemm(GK_DOWN, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
+  }
+  // shared down projection
+  if (s.S) {
+    GemmParams p;
+    zero_params(p);
+    MOE_TRY(tmap(&p.tmA, w.hs, s.T, s.Is, 64, kBM));
+    MOE_TRY(tmap(&p.tmB0, wts->Ws_down, s.d, s.Is, 64, kBN));
+    p.dense_rows = T;
+    p.N = d;
+    p.K = static_cast<int>(s.Is);
+    p.out = w.ys;
+    p.ldo = s.d;
+    p.status = w.status;
+    MOE_CUDA(launch_gemm(GK_DOWN, p, grid_for(cdiv(s.T, kBM) * cdiv(s.d, kBN)), st));
+  }
+  MOE_CUDA(launch_combine(w.o, s.S ? w.ys : nullptr, rt.route_row_pad, T, d, static_cast<int>(s.k),
+                          static_cast<__nv_bfloat16*>(y), st));
+  return MOE_OK;
+}
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights* wts, const void* dy,
+                        const void* saved, void* dx, const moe_grads* g, void* ws, void* stream) {
+  Shape s;
+  MOE_TRY(check_config(cfg, s));
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (s.T == 0) return MOE_OK;
+  MOE_TRY(check_weights(s, wts, true));
+  if (!x || !dy || !saved || !dx || !g || !aligned16(x) || !aligned16(dy) || !aligned16(dx))
+    return MOE_ERR_INVALID_ARG;
+  if (!g->dW_router || !g->dW_gate || !g->dW_up || !g->dW_down) return MOE_ERR_INVALID_ARG;
+  if (s.S && (!g->dWs_gate || !g->dWs_up || !g->dWs_down)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Saved sv;
+  carve_saved(const_cast<void*>(saved), s, sv, nullptr);
+  const Routing& rt = sv.rt;
+  BwdWs w;
+  carve_bwd(ws, s, w, nullptr);
+  const int T = static_cast<int>(s.T), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
+  const int E = static_cast<int>(s.E), k = static_cast<int>(s.k), Is = static_cast<int>(s.Is);
+
+  // dgrad of the down projection with the fused SwiGLU backward and the
+  // router-weight gradient partials <h, dh> per n-tile
+  {
+    GemmParams p;
+    zero_params(p);
+    MOE_TRY(tmap(&p.tmA, dy, s.T, s.d, 64, 1));
+    MOE_TRY(tmap(&p.tmB0, wts->W_down, s.E * s.d, s.I, 64, 64));
+    p.num_groups = E;
+    p.row_start = rt.row_start;
+    p.counts = rt.counts;
+    p.gather_idx = rt.perm_token_pad;
+    p.N = I;
+    p.K = d;
+    p.b_group_rows = d;
+    p.out = w.dadb;
+    p.ldo = 2 * s.I;
+    p.out2 = w.hg;
+    p.ldo2 = s.I;
+    p.out3 = w.dg_part;
+    p.ldo3 = static_cast<int>(s.nparts);
+    p.ab = sv.ab;
+    p.I = I;
+    p.row_scale = rt.perm_w_pad;
+    p.status = w.status;
+    MOE_CUDA(launch_gemm(GK_DGRAD_DOWN_ROUTED, p, grid_for(cdiv(s.Rp, kBM) * s.nparts), st));
+  }
+  if (s.S) {
+    GemmParams p;
+    zero_params(p);
+    MOE_TRY(tmap(&p.tmA, dy, s.T, s.d, 64, kBM));
+    MOE_TRY(tmap(&p.tmB0, wts->Ws_down, s.d, s.Is, 64, 64));
+    p.dense_rows = T;
+    p.N = Is;
+    p.K = d;
+    p.out = w.dadbs;
+    p.ldo = 2 * s.Is;
+    p.out2 = w.hs;
+    p.ldo2 = s.Is;
+    p.ab = sv.abs;
+    p.I = Is;
+    p.status = w.status;
+    MOE_CUDA(launch_gemm(GK_DGRAD_DOWN_DENSE, p, grid_for(cdiv(s.T, kBM) * cdiv(s.Is, kBN)), st));
+  }
+  MOE_CUDA(launch_router_grad(w.dg_part, static_cast<int>(s.nparts), rt.route_row_pad, rt.topk_w, T,
+                              k, g->d_topk_w, w.dl_tk, w.dl_row, st));
+  // dgrad of gate/up: dx_row = [da | db] . [W_gate ; W_up]
+  {
+    GemmParams p;
+    zero_params(p);
+    MOE_TRY(tmap(&p.tmA, w.dadb, s.Rp, 2 * s.I, 64, kBM));
+    MOE_TRY(tmap(&p.tmB0, wts->W_gate, s.E * s.I, s.d, 64, 64));
+    MOE_TRY(tmap(&p.tmB1, wts->W_up, s.E * s.I, s.d, 64, 64));
+    p.num_groups = E;
+    p.row_start = rt.row_start;
+    p.counts = rt.counts;
+    p.N = d;
+    p.K = 2 * I;
+    p.b_group_rows = I;
+    p.b_split = I;
+    p.out = w.dxp;
+    p.ldo = s.d;
+    p.status = w.status;
+    MOE_CUDA(launch_gemm(GK_DGRAD_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
+  }
+  if (s.S) {
+    GemmParams p;
+    zero_params(p);
+    MOE_TRY(tmap(&p.tmA, w.dadbs, s.T, 2 * s.Is, 64, kBM));
+    MOE_TRY(tmap(&p.tmB0, wts->Ws_gate, s.Is, s.d, 64, 64));
+    MOE_TRY(tmap(&p.tmB1, wts->Ws_up, s.Is, s.d, 64, 64));
+    p.dense_rows = T;
+    p.N = d;
+    p.K = 2 * Is;
+    p.b_split = Is;
+    p.out = w.dxs;
+    p.ldo = s.d;
+    p.status = w.status;
+    MOE_CUDA(launch_gemm(GK_DGRAD_GATEUP, p, grid_for(cdiv(s.T, kBM) * cdiv(s.d, kBN)), st));
+  }
+  MOE_CUDA(launch_unpermute(w.dxp, s.S ? w.dxs : nullptr, rt.route_row_pad, rt.topk_idx, w.dl_tk,
+                            static_cast<const __nv_bfloat16*>(wts->W_router), T, d, k,
+                            static_cast<__nv_bfloat16*>(dx), st));
+  MOE_CUDA(launch_router_wgrad(w.dl_row, rt.perm_token_pad, rt.row_start, rt.counts,
+                               static_cast<const __nv_bfloat16*>(x), E, d, g->dW_router, st));
+  // weight gradients, reduced over each expert's full row range (no split-K)
+  {
+    GemmParams p;  // dW_down[e] = dy_rows^T . (g h)
+    zero_params(p);
+    MOE_TRY(tmap(&p.tmA, dy, s.T, s.d, 64, 1));
+    MOE_TRY(tmap(&p.tmB0, w.hg, s.Rp, s.I, 64, 64));
+    p.num_groups = E;
+    p.row_start = rt.row_start;
+    p.gather_idx = rt.perm_token_pad;
+    p.M_out = d;
+    p.N = I;
+    p.out = g->dW_down;
+    p.ldo = s.I;
+    p.status = w.status;
+    MOE_CUDA(launch_gemm(GK_WGRAD_GATHER_A, p, grid_for(s.E * cdiv(s.d, kBM) * cdiv(s.I, kBN)), st));
+  }
+  for (int half = 0; half < 2; ++half) {
+    GemmParams p;  // dW_gate[e] = da^T . x_rows ; dW_up[e] = db^T . x_rows
+    zero_params(p);
+    MOE_TRY(tmap(&p.tmA, w.dadb, s.Rp, 2 * s.I, 64, 64));
+    MOE_TRY(tmap(&p.tmB0, x, s.T, s.d, 64, 1));
+    p.num_groups = E;
+    p.row_start = rt.row_start;
+    p.gather_idx = rt.perm_token_pad;
+    p.M_out = I;
+    p.N = d;
+    p.a_col_off = half ? I : 0;
+    p.out = half ? g->dW_up : g->dW_gate;
+    p.ldo = s.d;
+    p.status = w.status;
+    MOE_CUDA(launch_gemm(GK_WGRAD_GATHER_B, p, grid_for(s.E * cdiv(s.I, kBM) * cdiv(s.d, kBN)), st));
+  }
+  if (s.S) {
+    {
+      GemmParams p;  // dWs_down = dy^T . h_s
+      zero_params(p);
+      MOE_TRY(tmap(&p.tmA, dy, s.T, s.d, 64, 64));
+      MOE_TRY(tmap(&p.tmB0, w.hs, s.T, s.Is, 64, 64));
+      p.dense_rows = T;
+      p.M_out = d;
+      p.N = Is;
+      p.out = g->dWs_down;
+      p.ldo = s.Is;
+      p.status = w.status;
+      MOE_CUDA(launch_gemm(GK_WGRAD_DENSE, p, grid_for(cdiv(s.d, kBM) * cdiv(s.Is, kBN)), st));
+    }
+    for (int half = 0; half < 2; ++half) {
+      GemmParams p;  // dWs_gate = da_s^T . x ; dWs_up = db_s^T . x
+      zero_params(p);
+      MOE_TRY(tmap(&p.tmA, w.dadbs, s.T, 2 * s.Is, 64, 64));
+      MOE_TRY(tmap(&p.tmB0, x, s.T, s.d, 64, 64));
+      p.dense_rows = T;
+      p.M_out = Is;
+      p.N = d;
+      p.a_col_off = half ? Is : 0;
+      p.out = half ? g->dWs_up : g->dWs_gate;
+      p.ldo = s.d;
+      p.status = w.status;
+      MOE_CUDA(launch_gemm(GK_WGRAD_DENSE, p, grid_for(cdiv(s.Is, kBM) * cdiv(s.d, kBN)), st));
+    }
+  }
+  return MOE_OK;
+}
+
+moe_status moe_read_device_status(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status>(v);
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape, precision or flag";
+    case MOE_ERR_WORKSPACE: return "workspace missing";
+    case MOE_ERR_CUDA: return "CUDA runtime or launch error";
+    case MOE_ERR_DEVICE: return "a kernel saw an invalid value";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

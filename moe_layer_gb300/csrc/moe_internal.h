@@ -1,0 +1,69 @@
+// Internal declarations shared by the translation units of libmoe.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+struct GemmParams;
+
+// Tokens per routing chunk (one CTA of the top-k and scatter kernels) and per
+// warp inside it.
+constexpr int kChunkTokens = 64;
+constexpr int kChunkWarps = 8;
+constexpr int kWarpTokens = kChunkTokens / kChunkWarps;
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopK = 32;
+constexpr int kRowAlign = 128;  // each expert's row group starts at a multiple of this
+
+// ---- routing kernels (routing.cu)
+cudaError_t launch_topk_count(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                              float* topk_w, int32_t* chunk_counts, int* status, cudaStream_t st);
+cudaError_t launch_chunk_scan(const int32_t* chunk_counts, int nchunk, int E, int32_t* chunk_base,
+                              int32_t* counts, cudaStream_t st);
+cudaError_t launch_scatter(const int32_t* topk_idx, const float* topk_w, int T, int E, int k,
+                           const int32_t* chunk_base, const int32_t* counts, int32_t* offsets,
+                           int32_t* row_start, int32_t* perm_token, int32_t* route_row,
+                           int32_t* perm_token_pad, int32_t* route_row_pad, float* perm_w_pad,
+                           cudaStream_t st);
+
+// ---- memory-bound kernels (elementwise.cu)
+cudaError_t launch_combine(const __nv_bfloat16* o, const __nv_bfloat16* ys,
+                           const int32_t* route_row_pad, int T, int d, int k, __nv_bfloat16* y,
+                           cudaStream_t st);
+cudaError_t launch_router_grad(const float* dg_part, int nparts, const int32_t* route_row_pad,
+                               const float* topk_w, int T, int k, float* d_topk_w, float* dl_tk,
+                               float* dl_row, cudaStream_t st);
+cudaError_t launch_router_wgrad(const float* dl_row, const int32_t* perm_token_pad,
+                                const int32_t* row_start, const int32_t* counts,
+                                const __nv_bfloat16* x, int E, int d, float* dW_router,
+                                cudaStream_t st);
+cudaError_t launch_unpermute(const __nv_bfloat16* dxp, const __nv_bfloat16* dxs,
+                             const int32_t* route_row_pad, const int32_t* topk_idx,
+                             const float* dl_tk, const __nv_bfloat16* W_router, int T, int d,
+                             int k, __nv_bfloat16* dx, cudaStream_t st);
+
+// ---- tensor-core GEMM instantiations (gemm_fwd.cu, gemm_bwd.cu)
+enum GemmKind : int {
+  GK_ROUTER = 0,        // dense rows, fp32 + bias
+  GK_GATEUP_ROUTED,     // gathered x rows, gate|up, SwiGLU epilogue
+  GK_GATEUP_DENSE,      // x rows, gate|up, SwiGLU epilogue (shared expert)
+  GK_DOWN,              // rows x K-major weights, bf16 (optionally g-scaled)
+  GK_DGRAD_DOWN_ROUTED, // gathered dy rows x MN-major W_down, SwiGLU backward
+  GK_DGRAD_DOWN_DENSE,  // dy rows x MN-major Ws_down, SwiGLU backward
+  GK_DGRAD_GATEUP,      // [da|db] rows x MN-major [W_gate; W_up]
+  GK_WGRAD_GATHER_A,    // dW_down: gathered dy (MN) x hg (MN)
+  GK_WGRAD_GATHER_B,    // dW_gate/up: da or db (MN) x gathered x (MN)
+  GK_WGRAD_DENSE,       // shared-expert weight gradients
+  GK_COUNT
+};
+cudaError_t launch_gemm(GemmKind kind, const GemmParams& p, int grid, cudaStream_t st);
+int gemm_smem_bytes();
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace moe

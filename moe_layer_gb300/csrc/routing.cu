@@ -1,0 +1,283 @@
+// Routing on the device, no host synchronization:
+//   topk_count  softmax + top-k per token (one warp per token) and a per-chunk
+//               expert histogram;
+//   chunk_scan  for every expert, the exclusive prefix of its chunk counts and
+//               its total count;
+//   scatter     expert offsets (plain and padded to kRowAlign), then the stable
+//               position of every route inside its expert's row range.
+// Together they are the one-rank form of the counting schedule in the
+// Mixture-of-Kittens blog post, section "Choosing the right communication
+// direction / Scheduling": a counting pass, region offsets, then a pass that
+// writes every route in (token, slot) order.  Only integer atomics on shared
+// memory are used, so the result is exact and deterministic.
+#include <float.h>
+#include <limits.h>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Softmax + top-k for the tokens of one chunk (kWarpTokens tokens per warp).
+// Selection: logits descending, equal logits to the lower expert index.
+// Weights: exp(l_j - l_max) / sum over the k selected (softmax over all E
+// logits restricted to the selection and renormalized).
+__global__ void __launch_bounds__(kChunkWarps * 32)
+    topk_count_kernel(const float* __restrict__ logits, int T, int E, int k,
+                      int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                      int32_t* __restrict__ chunk_counts, int* status) {
+  __shared__ int cnt[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nS = (E + 31) >> 5;
+  const int t0 = blockIdx.x * kChunkTokens + warp * kWarpTokens;
+  for (int i = 0; i < kWarpTokens; ++i) {
+    const int t = t0 + i;
+    if (t >= T) break;
+    const float* lr = logits + static_cast<size_t>(t) * E;
+    float v[16];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      const int e = lane + 32 * s;
+      if (s < nS && e < E) {
+        v[s] = __ldg(lr + e);
+      } else {
+        v[s] = -INFINITY;
+        taken |= 1u << s;
+      }
+    }
+    int my_e = 0;
+    float my_v = 0.f;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int be = INT_MAX;
+#pragma unroll
+      for (int s = 0; s < 16; ++s) {
+        if (!((taken >> s) & 1u)) {
+          const int e = lane + 32 * s;
+          if (v[s] > bv || (v[s] == bv && e < be)) {
+            bv = v[s];
+            be = e;
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, off);
+        const int oe = __shfl_xor_sync(kFull, be, off);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if (be >= E) {  // only reachable with NaN logits
+        if (lane == 0) atomicCAS(status, 0, kDevBadValue);
+        be = 0;
+      } else if ((be & 31) == lane) {
+        taken |= 1u << (be >> 5);
+      }
+      if (lane == j) {
+        my_e = be;
+        my_v = bv;
+      }
+    }
+    const float m = __shfl_sync(kFull, my_v, 0);
+    const float ex = lane < k ? expf(my_v - m) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    if (lane < k) {
+      topk_idx[static_cast<size_t>(t) * k + lane] = my_e;
+      topk_w[static_cast<size_t>(t) * k + lane] = ex / sum;
+      atomicAdd(&cnt[my_e], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    chunk_counts[static_cast<size_t>(blockIdx.x) * E + e] = cnt[e];
+}
+
+// One warp per expert: exclusive prefix of the expert's chunk counts.
+__global__ void __launch_bounds__(256)
+    chunk_scan_kernel(const int32_t* __restrict__ chunk_counts, int nchunk, int E,
+                      int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  if (e >= E) return;
+  int carry = 0;
+  for (int c0 = 0; c0 < nchunk; c0 += 32 * 8) {
+    int v[8];
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = c0 + lane * 8 + i;
+      v[i] = c < nchunk ? __ldg(chunk_counts + static_cast<size_t>(c) * E + e) : 0;
+      s += v[i];
+    }
+    int inc = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(kFull, inc, off);
+      if (lane >= off) inc += o;
+    }
+    int run = carry + inc - s;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = c0 + lane * 8 + i;
+      if (c < nchunk) chunk_base[static_cast<size_t>(c) * E + e] = run;
+      run += v[i];
+    }
+    carry += __shfl_sync(kFull, inc, 31);
+  }
+  if (lane == 0) counts[e] = carry;
+}
+
+__device__ __forceinline__ int pad_rows(int c) { return (c + kRowAlign - 1) / kRowAlign * kRowAlign; }
+
+__global__ void __launch_bounds__(kChunkWarps * 32)
+    scatter_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int T,
+                   int E, int k, const int32_t* __restrict__ chunk_base,
+                   const int32_t* __restrict__ counts, int32_t* __restrict__ offsets_out,
+                   int32_t* __restrict__ row_start_out, int32_t* __restrict__ perm_token,
+                   int32_t* __restrict__ route_row, int32_t* __restrict__ perm_token_pad,
+                   int32_t* __restrict__ route_row_pad, float* __restrict__ perm_w_pad) {
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_rs[kMaxExperts + 1];
+  __shared__ int wcnt[kChunkWarps][kMaxExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // 1. expert offsets: exclusive prefix of counts, plain and padded
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    int sum = 0, psum = 0;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        const int c = __ldg(counts + e);
+        sum += c;
+        psum += pad_rows(c);
+      }
+    }
+    int inc = sum, pinc = psum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(kFull, inc, off);
+      const int po = __shfl_up_sync(kFull, pinc, off);
+      if (lane >= off) {
+        inc += o;
+        pinc += po;
+      }
+    }
+    int run = inc - sum, prun = pinc - psum;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        s_off[e] = run;
+        s_rs[e] = prun;
+        const int c = __ldg(counts + e);
+        run += c;
+        prun += pad_rows(c);
+      }
+    }
+    if (lane == 31) {
+      s_off[E] = inc;
+      s_rs[E] = pinc;
+    }
+  }
+  for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) wcnt[i / E][i % E] = 0;
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+      offsets_out[e] = s_off[e];
+      row_start_out[e] = s_rs[e];
+    }
+  }
+  // padding rows of the padded layout: no token, weight 0
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    const int beg = s_rs[e] + __ldg(counts + e), end = s_rs[e + 1];
+    for (int r = beg + threadIdx.x; r < end; r += blockDim.x) {
+      perm_token_pad[r] = -1;
+      perm_w_pad[r] = 0.f;
+    }
+  }
+
+  // 2. per-warp expert counts of this chunk
+  const int tw0 = blockIdx.x * kChunkTokens + warp * kWarpTokens;
+  const int ntok = max(0, min(kWarpTokens, T - tw0));
+  const int nr = ntok * k;
+  const int32_t* my_idx = topk_idx + static_cast<size_t>(tw0) * k;
+  for (int r = lane; r < nr; r += 32) atomicAdd(&wcnt[warp][__ldg(my_idx + r)], 1);
+  __syncthreads();
+  // 3. warp bases: chunk base of the expert plus the routes of earlier warps
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int base = __ldg(chunk_base + static_cast<size_t>(blockIdx.x) * E + e);
+    for (int w = 0; w < kChunkWarps; ++w) {
+      const int c = wcnt[w][e];
+      wcnt[w][e] = base;
+      base += c;
+    }
+  }
+  __syncthreads();
+  // 4. stable ranks, 32 routes at a time in (token, slot) order
+  for (int r0 = 0; r0 < nr; r0 += 32) {
+    const int r = r0 + lane;
+    const bool valid = r < nr;
+    const int e = valid ? __ldg(my_idx + r) : -1;
+    const unsigned peers = __match_any_sync(kFull, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    int local = 0;
+    if (valid) local = wcnt[warp][e] + rank;
+    __syncwarp();
+    if (valid && rank == 0) wcnt[warp][e] += __popc(peers);
+    __syncwarp();
+    if (valid) {
+      const int tl = r / k;
+      const int t = tw0 + tl;
+      const int j = r - tl * k;
+      const size_t tj = static_cast<size_t>(t) * k + j;
+      const int ru = s_off[e] + local;
+      const int rp = s_rs[e] + local;
+      perm_token[ru] = t;
+      route_row[tj] = ru;
+      perm_token_pad[rp] = t;
+      route_row_pad[tj] = rp;
+      perm_w_pad[rp] = __ldg(topk_w + tj);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_topk_count(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                              float* topk_w, int32_t* chunk_counts, int* status, cudaStream_t st) {
+  const int nchunk = (T + kChunkTokens - 1) / kChunkTokens;
+  topk_count_kernel<<<nchunk, kChunkWarps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w,
+                                                         chunk_counts, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_scan(const int32_t* chunk_counts, int nchunk, int E, int32_t* chunk_base,
+                              int32_t* counts, cudaStream_t st) {
+  chunk_scan_kernel<<<(E + 7) / 8, 256, 0, st>>>(chunk_counts, nchunk, E, chunk_base, counts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const int32_t* topk_idx, const float* topk_w, int T, int E, int k,
+                           const int32_t* chunk_base, const int32_t* counts, int32_t* offsets,
+                           int32_t* row_start, int32_t* perm_token, int32_t* route_row,
+                           int32_t* perm_token_pad, int32_t* route_row_pad, float* perm_w_pad,
+                           cudaStream_t st) {
+  const int nchunk = (T + kChunkTokens - 1) / kChunkTokens;
+  scatter_kernel<<<nchunk, kChunkWarps * 32, 0, st>>>(topk_idx, topk_w, T, E, k, chunk_base, counts,
+                                                      offsets, row_start, perm_token, route_row,
+                                                      perm_token_pad, route_row_pad, perm_w_pad);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

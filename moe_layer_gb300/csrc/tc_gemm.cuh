@@ -1,0 +1,555 @@
+// Persistent warp-specialised GEMM on the 5th-generation tensor cores
+// (tcgen05.mma, accumulators in TMEM, operands staged by TMA with the 128-byte
+// swizzle).  One template serves every contraction of the MoE layer:
+//
+//   * the router projection (dense rows, fp32 + bias epilogue);
+//   * the expert-grouped gate/up projection with the SwiGLU epilogue, whose A
+//     rows are token rows gathered straight from x by TMA tile::gather4;
+//   * the expert-grouped down projection scaled by the router weight;
+//   * the backward dgrads (down with the fused SwiGLU backward and router
+//     weight-gradient partials; gate/up with two weight stacks along K);
+//   * the weight gradients, whose reduction axis is an expert's (ragged) row
+//     range and whose operands are both MN-major.
+//
+// The MoE computation these serve is the DeepSeek-V3-style layer described in
+// "Mixture-of-Kittens: MoE Megakernel for NVL72s" (blog post, section
+// "Overlapping computation and communication in MoE"; paper section 2.1).
+//
+// Roles per CTA (256 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer (lane 0 issues tile loads; all lanes issue gathers)
+//   warp 1      MMA issuer (lane 0), 128x256x16 bf16 MMAs into TMEM
+//   warp 2      TMEM allocator (512 columns = two 128x256 fp32 accumulators)
+//   warps 4..7  epilogue: TMEM -> registers -> fused math -> global memory
+// Pipelines: kStages smem stages (full/empty mbarriers), two accumulator
+// buffers (acc_full/acc_empty) so the epilogue of tile i overlaps the MMAs of
+// tile i+1.  Every wait is bounded (see mbar_wait): a stuck pipeline records
+// MOE_ERR_DEVICE_TIMEOUT in the status word and the CTA exits cleanly.
+#pragma once
+#include "ptx.cuh"
+
+namespace moe {
+
+constexpr int kBM = 128;  // rows per tile (TMEM lanes)
+constexpr int kBN = 256;  // accumulator columns per tile
+constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
+constexpr int kStages = 4;
+constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
+constexpr int kBTileBytes = kBN * kBK * 2;  // 32 KB
+constexpr int kStageBytes = kATileBytes + kBTileBytes;
+constexpr int kMNChunkBytes = kBK * 128;  // one 64-wide MN chunk of an MN-major tile
+constexpr int kTmemCols = 512;
+constexpr int kGemmThreads = 256;
+constexpr int kGemmSmemBytes = 1024 + kStages * kStageBytes + 256;
+
+enum AMode : int { A_K_TILE = 0, A_K_GATHER = 1, A_MN_TILE = 2, A_MN_GATHER = 3 };
+enum BMode : int { B_K_TILE = 0, B_K_DUAL_N = 1, B_MN_TILE = 2, B_MN_DUAL_K = 3, B_MN_GATHER = 4 };
+enum EpiMode : int { EPI_F32_BIAS = 0, EPI_SWIGLU_FWD = 1, EPI_BF16 = 2, EPI_SWIGLU_BWD = 3 };
+enum SchedMode : int { SCHED_ROWS = 0, SCHED_WGRAD = 1 };
+
+struct GemmParams {
+  CUtensorMap tmA;
+  CUtensorMap tmB0;
+  CUtensorMap tmB1;
+  // ---- schedule
+  int dense_rows;          // > 0: a single group of this many rows; 0: grouped by row_start
+  int num_groups;          // number of groups (experts) when grouped
+  const int* row_start;    // [G+1] padded row offsets, multiples of kBM (grouped)
+  const int* counts;       // [G] real rows per group (grouped)
+  const int* gather_idx;   // padded row -> source row, -1 for padding (gather modes)
+  int N;                   // output columns
+  int K;                   // reduction length (SCHED_ROWS)
+  int M_out;               // output rows per group (SCHED_WGRAD)
+  int b_group_rows;        // rows of the B tensor map per group (0: B rows are absolute)
+  int a_col_off;           // first column of A in its tensor (A_MN_TILE)
+  int b_split;             // B_MN_DUAL_K: K index from which B comes from tmB1
+  // ---- epilogue
+  void* out;
+  long long ldo;
+  void* out2;
+  long long ldo2;
+  float* out3;
+  int ldo3;
+  const float* bias;
+  const float* row_scale;
+  const __nv_bfloat16* ab;
+  int I;
+  int store_ab;
+  int* status;
+};
+
+template <int EPI>
+__host__ __device__ constexpr int tile_out_cols() {
+  return EPI == EPI_SWIGLU_FWD ? kBN / 2 : kBN;
+}
+
+struct TileInfo {
+  int e;           // group (expert)
+  int row0;        // first row of the tile (SCHED_ROWS) in the padded row space
+  int rows_valid;  // rows of the tile that hold real data
+  int m0;          // first output row (SCHED_WGRAD)
+  int n0;          // first output column
+  int nt;          // n-tile index
+  int kb0;         // first K block
+  int nkb;         // number of K blocks
+};
+
+__device__ __forceinline__ int find_group(const int* row_start, int G, int row) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(row_start + mid) <= row)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int EPI, int SCH>
+__device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
+  if constexpr (SCH == SCHED_ROWS) {
+    const int num_nt = (p.N + tile_out_cols<EPI>() - 1) / tile_out_cols<EPI>();
+    if (p.dense_rows > 0) return ((p.dense_rows + kBM - 1) / kBM) * num_nt;
+    return (__ldg(p.row_start + p.num_groups) / kBM) * num_nt;
+  } else {
+    const int num_nt = (p.N + kBN - 1) / kBN;
+    const int num_mt = (p.M_out + kBM - 1) / kBM;
+    const int G = p.dense_rows > 0 ? 1 : p.num_groups;
+    return G * num_mt * num_nt;
+  }
+}
+
+template <int EPI, int SCH>
+__device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau) {
+  TileInfo t;
+  if constexpr (SCH == SCHED_ROWS) {
+    constexpr int W = tile_out_cols<EPI>();
+    const int num_nt = (p.N + W - 1) / W;
+    int mt, nt;
+    if (p.dense_rows > 0) {
+      // m-tiles outer, n-tiles inner: the weight panel stays L2-resident while
+      // activation rows stream once.
+      mt = tau / num_nt;
+      nt = tau - mt * num_nt;
+      t.e = 0;
+      t.row0 = mt * kBM;
+      t.rows_valid = min(kBM, p.dense_rows - t.row0);
+    } else {
+      // expert outer, n-tile, m-tile inner: CTAs running at the same time share
+      // one weight tile, the expert's gathered rows stay in L2.
+      const int q = tau / num_nt;
+      const int e = find_group(p.row_start, p.num_groups, q * kBM);
+      const int rs = __ldg(p.row_start + e);
+      const int mt_e = (__ldg(p.row_start + e + 1) - rs) / kBM;
+      const int local = tau - (rs / kBM) * num_nt;
+      nt = local / mt_e;
+      mt = local - nt * mt_e;
+      t.e = e;
+      t.row0 = rs + mt * kBM;
+      t.rows_valid = max(0, min(kBM, __ldg(p.counts + e) - mt * kBM));
+    }
+    t.m0 = 0;
+    t.nt = nt;
+    t.n0 = nt * W;
+    t.kb0 = 0;
+    t.nkb = p.K / kBK;
+  } else {
+    const int num_nt = (p.N + kBN - 1) / kBN;
+    const int num_mt = (p.M_out + kBM - 1) / kBM;
+    const int per_g = num_mt * num_nt;
+    const int e = tau / per_g;
+    const int local = tau - e * per_g;
+    const int mt = local / num_nt;
+    const int nt = local - mt * num_nt;
+    t.e = e;
+    t.m0 = mt * kBM;
+    t.nt = nt;
+    t.n0 = nt * kBN;
+    t.row0 = 0;
+    t.rows_valid = 0;
+    if (p.dense_rows > 0) {
+      t.kb0 = 0;
+      t.nkb = (p.dense_rows + kBK - 1) / kBK;
+    } else {
+      const int rs = __ldg(p.row_start + e);
+      t.kb0 = rs / kBK;
+      t.nkb = (__ldg(p.row_start + e + 1) - rs) / kBK;
+    }
+  }
+  return t;
+}
+
+__device__ __forceinline__ int gidx(const int* idx, int row) {
+  const int v = __ldg(idx + row);
+  return v < 0 ? 0 : v;
+}
+
+// ------------------------------------------------------------------ producer
+template <int AM, int BMO, int EPI, int SCH>
+__device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_tiles,
+                                              uint32_t full0, uint32_t empty0, int num_tiles,
+                                              volatile int* abort_flag, int lane) {
+  int s = 0;
+  uint32_t ph = 0;
+  // Per stage: parity of the last load issued into it, or -1.
+  int issued_parity[kStages];
+#pragma unroll
+  for (int i = 0; i < kStages; ++i) issued_parity[i] = -1;
+  bool aborted = false;
+
+  for (int tau = blockIdx.x; tau < num_tiles && !aborted; tau += gridDim.x) {
+    const TileInfo t = gemm_tile<EPI, SCH>(p, tau);
+    int gi0 = 0, gi1 = 0, gi2 = 0, gi3 = 0;
+    if constexpr (AM == A_K_GATHER) {
+      const int r = t.row0 + 4 * lane;
+      gi0 = gidx(p.gather_idx, r);
+      gi1 = gidx(p.gather_idx, r + 1);
+      gi2 = gidx(p.gather_idx, r + 2);
+      gi3 = gidx(p.gather_idx, r + 3);
+    }
+    for (int kb = 0; kb < t.nkb; ++kb) {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, p.status);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) {
+        aborted = true;
+        break;
+      }
+      const uint32_t full = full0 + 8 * s;
+      const uint32_t sA = s_tiles + s * kStageBytes;
+      const uint32_t sB = sA + kATileBytes;
+      if (lane == 0) mbar_arrive_expect_tx(full, kStageBytes);
+      __syncwarp();
+      const int kabs = (t.kb0 + kb) * kBK;
+      // ---- A operand
+      if constexpr (AM == A_K_TILE) {
+        if (lane == 0) tma_load_2d(sA, &p.tmA, kabs, t.row0, full);
+      } else if constexpr (AM == A_K_GATHER) {
+        tma_gather4(sA + lane * 4 * 128, &p.tmA, kabs, gi0, gi1, gi2, gi3, full);
+      } else if constexpr (AM == A_MN_TILE) {
+        if (lane == 0) {
+          tma_load_2d(sA, &p.tmA, p.a_col_off + t.m0, kabs, full);
+          tma_load_2d(sA + kMNChunkBytes, &p.tmA, p.a_col_off + t.m0 + 64, kabs, full);
+        }
+      } else {  // A_MN_GATHER: K rows are gathered source rows
+        const int c = lane >> 4, q = lane & 15;
+        const int r = kabs + 4 * q;
+        tma_gather4(sA + c * kMNChunkBytes + q * 4 * 128, &p.tmA, t.m0 + 64 * c,
+                    gidx(p.gather_idx, r), gidx(p.gather_idx, r + 1), gidx(p.gather_idx, r + 2),
+                    gidx(p.gather_idx, r + 3), full);
+      }
+      // ---- B operand
+      if constexpr (BMO == B_K_TILE) {
+        if (lane == 0) tma_load_2d(sB, &p.tmB0, kabs, t.e * p.b_group_rows + t.n0, full);
+      } else if constexpr (BMO == B_K_DUAL_N) {
+        if (lane == 0) {
+          tma_load_2d(sB, &p.tmB0, kabs, t.e * p.b_group_rows + t.n0, full);
+          tma_load_2d(sB + kBTileBytes / 2, &p.tmB1, kabs, t.e * p.b_group_rows + t.n0, full);
+        }
+      } else if constexpr (BMO == B_MN_TILE) {
+        if (lane < 4)
+          tma_load_2d(sB + lane * kMNChunkBytes, &p.tmB0, t.n0 + 64 * lane,
+                      t.e * p.b_group_rows + kabs, full);
+      } else if constexpr (BMO == B_MN_DUAL_K) {
+        if (lane < 4) {
+          const bool second = kabs >= p.b_split;
+          const int kk = second ? kabs - p.b_split : kabs;
+          tma_load_2d(sB + lane * kMNChunkBytes, second ? (const void*)&p.tmB1 : (const void*)&p.tmB0,
+                      t.n0 + 64 * lane, t.e * p.b_group_rows + kk, full);
+        }
+      } else {  // B_MN_GATHER
+        const int c = lane >> 3, q = lane & 7;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = kabs + 8 * q + 4 * h;
+          tma_gather4(sB + c * kMNChunkBytes + (8 * q + 4 * h) * 128, &p.tmB0, t.n0 + 64 * c,
+                      gidx(p.gather_idx, r), gidx(p.gather_idx, r + 1), gidx(p.gather_idx, r + 2),
+                      gidx(p.gather_idx, r + 3), full);
+        }
+      }
+      issued_parity[s] = static_cast<int>(ph);
+      if (++s == kStages) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+  }
+  if (aborted && lane == 0) {
+    // Loads still in flight must land before the CTA's shared memory goes away.
+#pragma unroll
+    for (int i = 0; i < kStages; ++i)
+      if (issued_parity[i] >= 0)
+        mbar_wait(full0 + 8 * i, static_cast<uint32_t>(issued_parity[i]), abort_flag, p.status,
+                  false);
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+template <int AM, int BMO, int EPI, int SCH>
+__device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, uint32_t full0,
+                                         uint32_t empty0, uint32_t accf0, uint32_t acce0,
+                                         uint32_t drain, uint32_t tmem_base, int num_tiles,
+                                         volatile int* abort_flag) {
+  constexpr bool a_mn = (AM == A_MN_TILE || AM == A_MN_GATHER);
+  constexpr bool b_mn = (BMO == B_MN_TILE || BMO == B_MN_DUAL_K || BMO == B_MN_GATHER);
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+  int s = 0;
+  uint32_t ph = 0;
+  int acc = 0;
+  uint32_t aph = 0;
+  bool issued = false, aborted = false;
+  for (int tau = blockIdx.x; tau < num_tiles && !aborted; tau += gridDim.x) {
+    const TileInfo t = gemm_tile<EPI, SCH>(p, tau);
+    if (!mbar_wait(acce0 + 8 * acc, aph ^ 1, abort_flag, p.status)) {
+      aborted = true;
+      break;
+    }
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+    for (int kb = 0; kb < t.nkb; ++kb) {
+      if (!mbar_wait(full0 + 8 * s, ph, abort_flag, p.status)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sA = s_tiles + s * kStageBytes;
+      const uint32_t sB = sA + kATileBytes;
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        const uint64_t ad = a_mn ? smem_desc_sw128(sA + kk * 2048, kMNChunkBytes, 1024)
+                                 : smem_desc_sw128(sA + kk * 32, 16, 1024);
+        const uint64_t bd = b_mn ? smem_desc_sw128(sB + kk * 2048, kMNChunkBytes, 1024)
+                                 : smem_desc_sw128(sB + kk * 32, 16, 1024);
+        tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+      }
+      tc_commit(empty0 + 8 * s);
+      issued = true;
+      if (++s == kStages) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+    if (aborted) break;
+    if (t.nkb > 0)
+      tc_commit(accf0 + 8 * acc);
+    else
+      mbar_arrive(accf0 + 8 * acc);
+    if (++acc == 2) {
+      acc = 0;
+      aph ^= 1;
+    }
+  }
+  if (aborted && issued) {
+    // MMAs still in flight must finish before TMEM is released.
+    tc_commit(drain);
+    mbar_wait(drain, 0, abort_flag, p.status, false);
+  }
+}
+
+// ------------------------------------------------------------------ epilogue
+template <int EPI, int SCH>
+__device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf0, uint32_t acce0,
+                                              uint32_t tmem_base, int num_tiles,
+                                              volatile int* abort_flag, int warp_e, int lane) {
+  int acc = 0;
+  uint32_t aph = 0;
+  const int row = warp_e * 32 + lane;  // TMEM lane == tile row owned by this thread
+  for (int tau = blockIdx.x; tau < num_tiles; tau += gridDim.x) {
+    const TileInfo t = gemm_tile<EPI, SCH>(p, tau);
+    const bool ok = mbar_wait(accf0 + 8 * acc, aph, abort_flag, p.status);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    tc_fence_after();
+    const uint32_t tr = tmem_base + (static_cast<uint32_t>(warp_e * 32) << 16) +
+                        static_cast<uint32_t>(acc * kBN);
+
+    if constexpr (SCH == SCHED_WGRAD) {
+      const int orow = t.m0 + row;
+      const bool in_mem = orow < p.M_out;
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                         (static_cast<long long>(t.e) * p.M_out + orow) * p.ldo + t.n0;
+      for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 16) {
+        float v[16];
+        if (t.nkb > 0) {
+          tmem_ld16(tr + c0, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        }
+        if (in_mem) store_bf16x16(o + c0, v);
+      }
+    } else {
+      const bool dense = p.dense_rows > 0;
+      const bool real = row < t.rows_valid;
+      const bool in_mem = dense ? real : true;
+      const long long grow = static_cast<long long>(t.row0) + row;
+      if constexpr (EPI == EPI_F32_BIAS) {
+        float* o = reinterpret_cast<float*>(p.out) + grow * p.ldo;
+        for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 16) {
+          float v[16];
+          tmem_ld16(tr + c0, v);
+          tmem_ld_wait();
+          if (in_mem) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int n = t.n0 + c0 + i;
+              if (n < p.N) o[n] = v[i] + (p.bias ? __ldg(p.bias + n) : 0.f);
+            }
+          }
+        }
+      } else if constexpr (EPI == EPI_SWIGLU_FWD) {
+        __nv_bfloat16* ab = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
+        __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(p.out2) + grow * p.ldo2;
+        for (int c0 = 0; c0 < kBN / 2 && t.n0 + c0 < p.N; c0 += 16) {
+          float a[16], b[16], hv[16];
+          tmem_ld16(tr + c0, a);
+          tmem_ld16(tr + kBN / 2 + c0, b);
+          tmem_ld_wait();
+          if (in_mem) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              if (!real) {
+                a[i] = 0.f;
+                b[i] = 0.f;
+              }
+              hv[i] = a[i] * sigmoidf_(a[i]) * b[i];
+            }
+            if (p.store_ab) {
+              store_bf16x16(ab + t.n0 + c0, a);
+              store_bf16x16(ab + p.I + t.n0 + c0, b);
+            }
+            store_bf16x16(h + t.n0 + c0, hv);
+          }
+        }
+      } else if constexpr (EPI == EPI_BF16) {
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
+        float scale = 1.f;
+        if (in_mem && p.row_scale) scale = __ldg(p.row_scale + grow);
+        if (!real) scale = 0.f;
+        for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 16) {
+          float v[16];
+          tmem_ld16(tr + c0, v);
+          tmem_ld_wait();
+          if (in_mem) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] *= scale;
+            store_bf16x16(o + t.n0 + c0, v);
+          }
+        }
+      } else {  // EPI_SWIGLU_BWD
+        __nv_bfloat16* dadb = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
+        __nv_bfloat16* hg = reinterpret_cast<__nv_bfloat16*>(p.out2) + grow * p.ldo2;
+        const __nv_bfloat16* abr = p.ab + grow * (2LL * p.I);
+        float g = 1.f;
+        if (in_mem && real && p.row_scale) g = __ldg(p.row_scale + grow);
+        float dgp = 0.f;
+        for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 16) {
+          float dh[16];
+          tmem_ld16(tr + c0, dh);
+          tmem_ld_wait();
+          if (in_mem) {
+            float da[16], db[16], hv[16];
+            if (real) {
+              float a[16], b[16];
+              load_bf16x16(abr + t.n0 + c0, a);
+              load_bf16x16(abr + p.I + t.n0 + c0, b);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float sg = sigmoidf_(a[i]);
+                const float silu = a[i] * sg;
+                const float hh = silu * b[i];
+                dgp += dh[i] * hh;
+                const float dhs = g * dh[i];
+                da[i] = dhs * b[i] * sg * (1.f + a[i] * (1.f - sg));
+                db[i] = dhs * silu;
+                hv[i] = g * hh;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                da[i] = 0.f;
+                db[i] = 0.f;
+                hv[i] = 0.f;
+              }
+            }
+            store_bf16x16(dadb + t.n0 + c0, da);
+            store_bf16x16(dadb + p.I + t.n0 + c0, db);
+            store_bf16x16(hg + t.n0 + c0, hv);
+          }
+        }
+        if (in_mem && p.out3) p.out3[grow * p.ldo3 + t.nt] = real ? dgp : 0.f;
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+    if (++acc == 2) {
+      acc = 0;
+      aph ^= 1;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int AM, int BMO, int EPI, int SCH>
+__global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t s_tiles = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kStages;
+  const uint32_t accf0 = empty0 + 8 * kStages;
+  const uint32_t acce0 = accf0 + 16;
+  const uint32_t drain = acce0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(accf0 + 8 * i, 1);
+      mbar_init(acce0 + 8 * i, 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmB0);
+    if (BMO == B_K_DUAL_N || BMO == B_MN_DUAL_K) tma_prefetch_desc(&p.tmB1);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_tiles = gemm_num_tiles<EPI, SCH>(p);
+
+  if (warp == 0) {
+    gemm_producer<AM, BMO, EPI, SCH>(p, s_tiles, full0, empty0, num_tiles, abort_flag, lane);
+  } else if (warp == 1) {
+    if (lane == 0)
+      gemm_mma<AM, BMO, EPI, SCH>(p, s_tiles, full0, empty0, accf0, acce0, drain, tmem_base,
+                                  num_tiles, abort_flag);
+  } else if (warp >= 4) {
+    gemm_epilogue<EPI, SCH>(p, accf0, acce0, tmem_base, num_tiles, abort_flag, warp - 4, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,65 @@
+"""Thin convenience layer over the C ABI: allocates the caller-owned buffers
+with torch and forwards the calls.  No arithmetic happens here."""
+from __future__ import annotations
+
+import torch
+
+from . import _abi
+
+
+class MoEBuffers:
+    """Workspace, saved-state and output buffers for one configuration."""
+
+    def __init__(self, cfg: _abi.MoeConfig, device="cuda", training: bool = True):
+        self.cfg = cfg
+        f, s, b = _abi.moe_workspace_size(cfg)
+        dev = torch.device(device)
+        self.fwd_ws = torch.zeros(max(f, 256), dtype=torch.uint8, device=dev)
+        self.saved = torch.zeros(max(s, 256), dtype=torch.uint8, device=dev) if training else None
+        self.bwd_ws = torch.zeros(max(b, 256), dtype=torch.uint8, device=dev) if training else None
+
+
+def weights_from(inp: dict) -> _abi.MoeWeights:
+    return _abi.make_weights(inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                             inp.get("router_bias"), inp.get("Ws_gate"), inp.get("Ws_up"),
+                             inp.get("Ws_down"))
+
+
+def alloc_grads(cfg: _abi.MoeConfig, device="cuda", with_topk: bool = True) -> dict:
+    dev = torch.device(device)
+    T, d, I, E, k = cfg.T, cfg.d, cfg.I, cfg.E, cfg.top_k
+    g = {
+        "dW_router": torch.empty(E, d, dtype=torch.float32, device=dev),
+        "dW_gate": torch.empty(E, I, d, dtype=torch.bfloat16, device=dev),
+        "dW_up": torch.empty(E, I, d, dtype=torch.bfloat16, device=dev),
+        "dW_down": torch.empty(E, d, I, dtype=torch.bfloat16, device=dev),
+        "d_topk_w": torch.empty(T, k, dtype=torch.float32, device=dev) if with_topk else None,
+    }
+    if cfg.n_shared:
+        Is = cfg.I_shared
+        g["dWs_gate"] = torch.empty(Is, d, dtype=torch.bfloat16, device=dev)
+        g["dWs_up"] = torch.empty(Is, d, dtype=torch.bfloat16, device=dev)
+        g["dWs_down"] = torch.empty(d, Is, dtype=torch.bfloat16, device=dev)
+    else:
+        g["dWs_gate"] = g["dWs_up"] = g["dWs_down"] = None
+    return g
+
+
+def grads_struct(g: dict) -> _abi.MoeGrads:
+    return _abi.make_grads(g["dW_router"], g["dW_gate"], g["dW_up"], g["dW_down"], g["dWs_gate"],
+                           g["dWs_up"], g["dWs_down"], g["d_topk_w"])
+
+
+def forward(cfg, inp: dict, bufs: MoEBuffers, y=None, stream=None):
+    if y is None:
+        y = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=inp["x"].device)
+    _abi.moe_forward(cfg, inp["x"], weights_from(inp), y, bufs.saved, bufs.fwd_ws, stream)
+    return y
+
+
+def backward(cfg, inp: dict, dy, bufs: MoEBuffers, grads: dict, dx=None, stream=None):
+    if dx is None:
+        dx = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dy.device)
+    _abi.moe_backward(cfg, inp["x"], weights_from(inp), dy, bufs.saved, dx, grads_struct(grads),
+                      bufs.bwd_ws, stream)
+    return dx

@@ -1,0 +1,73 @@
+"""Shared helpers for the GPU parity tests: building the library, running the
+layer through the C ABI, and running the oracle on the same seeded inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import moe_oracle as O
+
+
+def ensure_lib():
+    from moe_layer_gb300 import _abi, build_ext
+    build_ext.build()
+    _abi.load()
+
+
+def f64(t):
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def rel_err(gpu, ref):
+    """max |gpu - ref| / max |ref| (inputs: tensor or array)."""
+    g = f64(gpu) if isinstance(gpu, torch.Tensor) else np.asarray(gpu, np.float64)
+    r = np.asarray(ref, np.float64)
+    return float(np.abs(g - r).max() / max(np.abs(r).max(), 1e-300))
+
+
+class LazyExperts:
+    """Indexable view of an [E, ...] bf16 tensor that upcasts one expert at a time."""
+
+    def __init__(self, t):
+        self.t = t
+        self.cache = {}
+
+    def __len__(self):
+        return self.t.shape[0]
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.cache:
+            self.cache[e] = f64(self.t[e])
+        return self.cache[e]
+
+
+def oracle_forward(inp, k, logits=None, tokens=None):
+    """Oracle forward on the CPU copies of the inputs (optionally a token subset)."""
+    x = f64(inp["x"]) if tokens is None else f64(inp["x"][tokens])
+    bias = None if inp.get("router_bias") is None else f64(inp["router_bias"])
+    sh = inp.get("Ws_gate") is not None
+    return O.moe_forward(x, f64(inp["W_router"]), LazyExperts(inp["W_gate"]), LazyExperts(inp["W_up"]),
+                         LazyExperts(inp["W_down"]), k, router_bias=bias,
+                         ws_gate=f64(inp["Ws_gate"]) if sh else None,
+                         ws_up=f64(inp["Ws_up"]) if sh else None,
+                         ws_down=f64(inp["Ws_down"]) if sh else None, logits=logits)
+
+
+def oracle_backward(inp, fwd, tokens=None):
+    x = f64(inp["x"]) if tokens is None else f64(inp["x"][tokens])
+    dy = f64(inp["dy"]) if tokens is None else f64(inp["dy"][tokens])
+    sh = inp.get("Ws_gate") is not None
+    return O.moe_backward(x, f64(inp["W_router"]), LazyExperts(inp["W_gate"]), LazyExperts(inp["W_up"]),
+                          LazyExperts(inp["W_down"]), dy, fwd,
+                          ws_gate=f64(inp["Ws_gate"]) if sh else None,
+                          ws_up=f64(inp["Ws_up"]) if sh else None,
+                          ws_down=f64(inp["Ws_down"]) if sh else None)
+
+
+def topk_gap(logits, k):
+    """Gap between the k-th and (k+1)-th largest logit per token (inf if k == E)."""
+    s = -np.sort(-np.asarray(logits, np.float64), axis=1)
+    if s.shape[1] == k:
+        return np.full(s.shape[0], np.inf)
+    return s[:, k - 1] - s[:, k]

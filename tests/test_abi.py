@@ -1,0 +1,88 @@
+"""The C-ABI library loads and exports every entry point include/moe.h
+declares; host-only calls (sizes, argument checks) behave.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_layer_gb300 import _abi, build_ext
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_ext.build()
+    return _abi.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(moe_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_expected_api():
+    syms = declared_symbols()
+    for name in ["moe_workspace_size", "moe_route_topk", "moe_forward", "moe_backward",
+                 "moe_read_device_status", "moe_status_string"]:
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert _abi.status_string(0) == "ok"
+    assert "unsupported" in _abi.status_string(2)
+
+
+def test_workspace_sizes_scale_with_shape(lib):
+    small = _abi.moe_workspace_size(_abi.make_config(512, 256, 128, 8, 2, 1, 128))
+    big = _abi.moe_workspace_size(_abi.make_config(16384, 7168, 2048, 256, 8, 1, 2048))
+    assert all(s > 0 for s in small) and all(b > s for b, s in zip(big, small))
+    # saved state holds at least a and b for every (padded) route row
+    assert big[1] >= 16384 * 8 * 2 * 2048 * 2
+
+
+@pytest.mark.parametrize("cfg,code", [
+    ((512, 100, 128, 8, 2, 0, 0), 2),     # d not a multiple of 64
+    ((512, 256, 96, 8, 2, 0, 0), 2),      # I not a multiple of 64
+    ((512, 256, 128, 8, 9, 0, 0), 2),     # top_k > E
+    ((512, 256, 128, 600, 2, 0, 0), 2),   # E > 512
+    ((512, 256, 128, 64, 33, 0, 0), 2),   # top_k > 32
+    ((-1, 256, 128, 8, 2, 0, 0), 1),      # negative T
+    ((512, 256, 128, 8, 2, 1, 0), 1),     # shared expert without width
+])
+def test_invalid_configs_rejected(lib, cfg, code):
+    c = _abi.make_config(*cfg)
+    a = ctypes.c_size_t()
+    assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(a), None, None) == code
+
+
+def test_mxfp8_precision_reported_unsupported(lib):
+    c = _abi.make_config(512, 256, 128, 8, 2, precision=_abi.MOE_MXFP8)
+    a = ctypes.c_size_t()
+    assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(a), None, None) == 2
+
+
+def test_null_arguments_rejected_before_launch(lib):
+    c = _abi.make_config(64, 128, 64, 4, 2)
+    w = _abi.MoeWeights()
+    # no workspace
+    assert lib.moe_forward(ctypes.byref(c), None, ctypes.byref(w), None, None, None, None) == 3
+    # workspace given but weights missing: invalid argument, nothing launched
+    assert lib.moe_forward(ctypes.byref(c), None, ctypes.byref(w), None, None, 256, None) == 1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    c = _abi.make_config(0, 128, 64, 4, 2)
+    w = _abi.MoeWeights()
+    assert lib.moe_forward(ctypes.byref(c), None, ctypes.byref(w), None, None, 256, None) == 0
+
+
+def test_package_imports_without_gpu():
+    import moe_layer_gb300
+    assert moe_layer_gb300.moe_forward is _abi.moe_forward
