@@ -1,0 +1,391 @@
+"""Benchmark of the MoE layer hot path (forward + backward) through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload dsv3|qwen3|tiny]
+
+One step = forward + backward of the whole layer on one batch of seeded
+synthetic input of the workload (default: the DeepSeek-V3-shaped layer,
+T=16384 tokens, d=7168, I=2048, E=256 routed experts, top-8, one shared
+expert).  Inputs and weights are resident in HBM before the timed region;
+they are larger than L2 (x 235 MB, expert weights 22.6 GB), so no L2 flush is
+done between steps.  With N > 1 (torchrun) every rank runs an independent
+replica on its own tokens (weak scaling, no collective on the data path);
+the timed region is bracketed by barriers and the slowest rank's time counts.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead
+(bounded sample per step) and prints the same metric with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s and TFLOPS (fwd, fwd+bwd) at 1 GB300, % of tensor peak"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm": p["hbm_gbs"], "bf16": p["bf16_tflops"],
+                "bf16_sustained": p["bf16_tflops_sustained"], "src": "measured"}
+    except Exception:
+        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
+
+
+def _workload(name):
+    from synth.inputs import CONFIGS
+    s = CONFIGS[name]
+    desc = {
+        "dsv3": "DSV3-shaped BF16 MoE layer forward+backward",
+        "qwen3": "Qwen3-235B-shaped BF16 MoE layer forward+backward (Zipf-skewed routing)",
+        "tiny": "tiny BF16 MoE layer forward+backward",
+    }[name]
+    return s, desc
+
+
+def _flops(s):
+    """Algorithmic flops per token of the forward pass (backward = 2x)."""
+    return 6 * s.d * s.I * s.k + 6 * s.d * s.I_shared * s.n_shared + 2 * s.d * s.E
+
+
+def _kernel_flops(name, s):
+    """Algorithmic flops of one launch of a tensor-core kernel."""
+    R, T, d, I, Is, E = s.T * s.k, s.T, s.d, s.I, s.I_shared, s.E
+    table = {
+        "router_gemm": 2 * T * d * E,
+        "gateup_routed": 4 * R * d * I, "down_routed": 2 * R * d * I,
+        "dgrad_down_routed": 2 * R * d * I, "dgrad_gateup_routed": 4 * R * d * I,
+        "wgrad_down": 2 * R * d * I, "wgrad_gate": 2 * R * d * I, "wgrad_up": 2 * R * d * I,
+        "gateup_shared": 4 * T * d * Is, "down_shared": 2 * T * d * Is,
+        "dgrad_down_shared": 2 * T * d * Is, "dgrad_gateup_shared": 4 * T * d * Is,
+        "wgrad_shared_down": 2 * T * d * Is, "wgrad_shared_gate": 2 * T * d * Is,
+        "wgrad_shared_up": 2 * T * d * Is,
+    }
+    return table.get(name)
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        try:
+            sm = [float(r[1]) for r in rows]
+            smax = max(float(r[2]) for r in rows)
+        except ValueError:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def _lazy_experts(t):
+    import numpy as np
+    import torch
+
+    class Lazy:
+        def __init__(self):
+            self.cache = {}
+
+        def __len__(self):
+            return t.shape[0]
+
+        def __getitem__(self, e):
+            e = int(e)
+            if e not in self.cache:
+                self.cache[e] = t[e].to(torch.float64).cpu().numpy()
+            return self.cache[e]
+    return Lazy()
+
+
+def _oracle_step(inp, s, tokens):
+    """The CPU oracle's forward + backward on a token sample (test infrastructure,
+    used only for the reported CPU baseline)."""
+    import torch
+    from oracle import moe_oracle as O
+    f = lambda t: t.to(torch.float64).cpu().numpy()
+    x = f(inp["x"][tokens])
+    dy = f(inp["dy"][tokens])
+    wr = f(inp["W_router"])
+    bias = None if inp.get("router_bias") is None else f(inp["router_bias"])
+    wg, wu, wd = _lazy_experts(inp["W_gate"]), _lazy_experts(inp["W_up"]), _lazy_experts(inp["W_down"])
+    sh = {}
+    if s.n_shared:
+        sh = dict(ws_gate=f(inp["Ws_gate"]), ws_up=f(inp["Ws_up"]), ws_down=f(inp["Ws_down"]))
+    fwd = O.moe_forward(x, wr, wg, wu, wd, s.k, router_bias=bias, **sh)
+    O.moe_backward(x, wr, wg, wu, wd, dy, fwd, dense_expert_grads=False, **sh)
+
+
+def _cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(inp, s, n_tokens, rounds, seed=1):
+    """Oracle forward+backward on `rounds` independent random samples of
+    `n_tokens` tokens each (each round upcasts only the experts its tokens
+    touch, which bounds host memory)."""
+    import torch
+    g = torch.Generator().manual_seed(seed)
+    dt = 0.0
+    for _ in range(rounds):
+        tokens = torch.randperm(s.T, generator=g)[:n_tokens].sort().values.to(inp["x"].device)
+        t0 = time.perf_counter()
+        _oracle_step(inp, s, tokens)
+        dt += time.perf_counter() - t0
+    n = n_tokens * rounds
+    return {"value": n / dt, "unit": "tokens/s", "cores": _cpu_cores(), "kind": "oracle",
+            "sample": f"float64 numpy oracle forward+backward, {rounds} rounds of {n_tokens} random tokens "
+                      f"of the same workload ({n} tokens, expert weights upcast on first use per round), "
+                      f"{dt:.1f} s; numpy BLAS default threading"}
+
+
+def run_reference(args):
+    """The CPU oracle timed on the host cores, each step a bounded sample."""
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from synth.inputs import make_inputs
+    s, desc = _workload(args.workload)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = make_inputs(s, seed=0, device=dev)
+    per_step = args.ref_tokens
+    g = torch.Generator().manual_seed(1)
+    for _ in range(args.warmup):
+        _oracle_step(inp, s, torch.randperm(s.T, generator=g)[:per_step].sort().values.to(dev))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(inp, s, torch.randperm(s.T, generator=g)[:per_step].sort().values.to(dev))
+    dt = (time.perf_counter() - t0) / args.steps
+    value = per_step / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "T": s.T, "d": s.d, "I": s.I, "E": s.E, "top_k": s.k,
+                   "n_shared": s.n_shared, "I_shared": s.I_shared, "tokens_per_step": per_step},
+        "tflops": value * 3 * _flops(s) / 1e12,
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cpu_cores(), "kind": "oracle",
+                         "sample": f"{per_step} random tokens per step, oracle forward+backward"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dsv3", choices=["dsv3", "qwen3", "tiny"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=4, help="oracle tokens per cpu_baseline round (0 = skip)")
+    ap.add_argument("--cpu-rounds", type=int, default=4, help="cpu_baseline rounds")
+    ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per reference step")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    from moe_layer_gb300 import _abi, layer
+    from synth.inputs import make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    _abi.load()
+    s, desc = _workload(args.workload)
+    inp = make_inputs(s, seed=rank, device="cuda")
+    cfg = _abi.make_config(s.T, s.d, s.I, s.E, s.k, s.n_shared, s.I_shared)
+    bufs = layer.MoEBuffers(cfg)
+    grads = layer.alloc_grads(cfg)
+    y = torch.empty(s.T, s.d, dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty_like(y)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        layer.forward(cfg, inp, bufs, y)
+        layer.backward(cfg, inp, inp["dy"], bufs, grads, dx)
+
+    def timed(fn, n):
+        torch.cuda.synchronize()
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return a.elapsed_time(b) / n
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = _abi.moe_read_device_status(bufs.fwd_ws) or _abi.moe_read_device_status(bufs.bwd_ws)
+    if st:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    # forward + backward: the headline, with per-kernel events and clock samples
+    sampler = ClockSampler(local)
+    sampler.start()
+    _abi.moe_profile_enable(True)
+    ms = timed(step, args.steps)
+    _abi.moe_profile_enable(False)
+    clocks = sampler.stop()
+    prof = _abi.moe_profile_report()
+    ms = max_over_ranks(ms)
+    # forward alone
+    for _ in range(2):
+        layer.forward(cfg, inp, bufs, y)
+    ms_fwd = max_over_ranks(timed(lambda: layer.forward(cfg, inp, bufs, y), args.steps))
+
+    tokens = s.T * world
+    flops_tok = _flops(s)
+    peaks = _peaks()
+    value = tokens / (ms * 1e-3)
+    tflops = value * 3 * flops_tok / 1e12
+    fwd_value = tokens / (ms_fwd * 1e-3)
+
+    launches = sum(n for n, _ in prof.values())
+    kern_ms = {k: v[1] for k, v in prof.items()}
+    total_kern = sum(kern_ms.values())
+    top = max(kern_ms, key=kern_ms.get)
+    n_top, ms_top = prof[top]
+    fl = _kernel_flops(top, s)
+    roofline = None
+    if fl is not None:
+        achieved = fl / (ms_top / n_top * 1e-3) / 1e12
+        roofline = {"kernel": top, "bound": "tensor", "achieved": achieved,
+                    "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["bf16_sustained"], "traffic": None,
+                    "peak_src": peaks["src"] + " bf16 sustained (kernel timed inside a long step)"}
+
+    e2e = None
+    if not args.no_e2e:
+        xh = inp["x"].cpu().pin_memory()
+        dyh = inp["dy"].cpu().pin_memory()
+        yh = torch.empty(s.T, s.d, dtype=torch.bfloat16).pin_memory()
+        dxh = torch.empty_like(yh).pin_memory()
+        xd = torch.empty_like(inp["x"])
+        dyd = torch.empty_like(inp["dy"])
+        inp_e2e = dict(inp)
+        inp_e2e["x"] = xd
+
+        def e2e_step():
+            xd.copy_(xh, non_blocking=True)
+            dyd.copy_(dyh, non_blocking=True)
+            layer.forward(cfg, inp_e2e, bufs, y)
+            layer.backward(cfg, inp_e2e, dyd, bufs, grads, dx)
+            yh.copy_(y, non_blocking=True)
+            dxh.copy_(dx, non_blocking=True)
+
+        e2e_step()
+        ms_e2e = max_over_ranks(timed(e2e_step, args.steps))
+        nb = s.T * s.d * 2
+        e2e = {"value": tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": 2 * nb,
+               "d2h_bytes_per_step": 2 * nb, "ms_per_step": ms_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_tokens > 0:
+        cpu = cpu_baseline(inp, s, args.cpu_tokens, args.cpu_rounds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": desc, "T": s.T, "d": s.d, "I": s.I, "E": s.E, "top_k": s.k,
+                       "n_shared": s.n_shared, "I_shared": s.I_shared, "tokens_per_gpu": s.T,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (x 235 MB, expert weights 22.6 GB at dsv3); no flush"},
+            "tflops": tflops, "pct_bf16_peak": tflops / peaks["bf16"],
+            "pct_bf16_peak_sustained": tflops / peaks["bf16_sustained"],
+            "fwd": {"value": fwd_value, "unit": "tokens/s", "ms": ms_fwd,
+                    "tflops": fwd_value * flops_tok / 1e12},
+            "roofline": roofline,
+            "kernels_ms_per_step": {k: round(v / args.steps, 4) for k, v in
+                                    sorted(kern_ms.items(), key=lambda kv: -kv[1])},
+            "kernel_share": {k: round(v / total_kern, 4) for k, v in kern_ms.items()},
+            "gpu_launches": launches,
+            "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -19,7 +19,7 @@ MOE_BF16 = 0
 MOE_MXFP8 = 1
 
 EXPORTED = ["moe_workspace_size", "moe_route_topk", "moe_forward", "moe_backward",
-            "moe_read_device_status", "moe_status_string"]
+            "moe_read_device_status", "moe_profile_enable", "moe_profile_report", "moe_status_string"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -66,6 +66,8 @@ def load():
     lib.moe_backward.argtypes = [cfgp, P, ctypes.POINTER(MoeWeights), P, P, P,
                                  ctypes.POINTER(MoeGrads), P, P]
     lib.moe_read_device_status.argtypes = [P, P]
+    lib.moe_profile_enable.argtypes = [ctypes.c_int]
+    lib.moe_profile_report.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
     lib.moe_status_string.argtypes = [ctypes.c_int]
     lib.moe_status_string.restype = ctypes.c_char_p
     for name in EXPORTED[:-1]:
@@ -149,3 +151,18 @@ def moe_backward(cfg, x, weights: MoeWeights, dy, saved, dx, grads: MoeGrads, ws
 
 def moe_read_device_status(ws, stream=None) -> int:
     return int(load().moe_read_device_status(_ptr(ws), _stream(stream)))
+
+
+def moe_profile_enable(enable: bool = True):
+    _check(load().moe_profile_enable(1 if enable else 0), "moe_profile_enable")
+
+
+def moe_profile_report() -> dict:
+    """{kernel name: (launches, total_ms)} for the launches recorded since the last report."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    _check(load().moe_profile_report(buf, len(buf)), "moe_profile_report")
+    out = {}
+    for line in buf.value.decode().splitlines():
+        name, n, ms = line.split()
+        out[name] = (int(n), float(ms))
+    return out

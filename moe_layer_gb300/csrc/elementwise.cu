@@ -7,6 +7,8 @@
 //                  softmax backward dl_tj = g_tj (dg_tj - sum_i g_ti dg_ti)
 //   router_wgrad   dW_router[e] = sum over e's rows (ascending) of dl_row x_token
 //   unpermute      dx_t = dx_shared,t + sum_j dxp[row(t, j)] + sum_j dl_tj W_router[e_tj]
+//   permute_rows   copies token rows into the expert-grouped row order (the
+//                  "dispatch" of the pages, local to one GPU)
 #include "moe_internal.h"
 #include "ptx.cuh"
 
@@ -170,7 +172,44 @@ __global__ void __launch_bounds__(kEwThreads)
   }
 }
 
+// dst[r] = src[idx[r]] for every row r of the padded expert-grouped layout
+// (idx -1 marks a padding row, which gets zeros).  Blocks past the padded total
+// written by the scatter kernel return at once.
+__global__ void __launch_bounds__(kEwThreads)
+    permute_rows_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __restrict__ idx,
+                        const int32_t* __restrict__ total_rows, int d,
+                        __nv_bfloat16* __restrict__ dst) {
+  const int r = blockIdx.x;
+  if (r >= __ldg(total_rows)) return;
+  const int t = __ldg(idx + r);
+  const uint4* s = reinterpret_cast<const uint4*>(src + static_cast<size_t>(t < 0 ? 0 : t) * d);
+  uint4* o = reinterpret_cast<uint4*>(dst + static_cast<size_t>(r) * d);
+  const int nv = d / 8;
+  if (t < 0) {
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) o[v] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  int v = threadIdx.x;
+  for (; v + 3 * kEwThreads < nv; v += 4 * kEwThreads) {
+    const uint4 a0 = __ldg(s + v), a1 = __ldg(s + v + kEwThreads);
+    const uint4 a2 = __ldg(s + v + 2 * kEwThreads), a3 = __ldg(s + v + 3 * kEwThreads);
+    o[v] = a0;
+    o[v + kEwThreads] = a1;
+    o[v + 2 * kEwThreads] = a2;
+    o[v + 3 * kEwThreads] = a3;
+  }
+  for (; v < nv; v += kEwThreads) o[v] = __ldg(s + v);
+}
+
 }  // namespace
+
+cudaError_t launch_permute_rows(const __nv_bfloat16* src, const int32_t* idx_pad,
+                                const int32_t* total_rows, int rows_max, int d,
+                                __nv_bfloat16* dst, cudaStream_t st) {
+  if (rows_max <= 0) return cudaSuccess;
+  permute_rows_kernel<<<rows_max, kEwThreads, 0, st>>>(src, idx_pad, total_rows, d, dst);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const __nv_bfloat16* o, const __nv_bfloat16* ys,
                            const int32_t* route_row_pad, int T, int d, int k, __nv_bfloat16* y,

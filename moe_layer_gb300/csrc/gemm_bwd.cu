@@ -5,17 +5,11 @@ namespace moe {
 
 cudaError_t launch_gemm_bwd(GemmKind kind, const GemmParams& p, int grid, cudaStream_t st) {
   switch (kind) {
-    case GK_DGRAD_DOWN_ROUTED:
-      return launch_gemm_inst<A_K_GATHER, B_MN_TILE, EPI_SWIGLU_BWD, SCHED_ROWS>(p, grid, st);
-    case GK_DGRAD_DOWN_DENSE:
+    case GK_DGRAD_DOWN:
       return launch_gemm_inst<A_K_TILE, B_MN_TILE, EPI_SWIGLU_BWD, SCHED_ROWS>(p, grid, st);
     case GK_DGRAD_GATEUP:
       return launch_gemm_inst<A_K_TILE, B_MN_DUAL_K, EPI_BF16, SCHED_ROWS>(p, grid, st);
-    case GK_WGRAD_GATHER_A:
-      return launch_gemm_inst<A_MN_GATHER, B_MN_TILE, EPI_BF16, SCHED_WGRAD>(p, grid, st);
-    case GK_WGRAD_GATHER_B:
-      return launch_gemm_inst<A_MN_TILE, B_MN_GATHER, EPI_BF16, SCHED_WGRAD>(p, grid, st);
-    case GK_WGRAD_DENSE:
+    case GK_WGRAD:
       return launch_gemm_inst<A_MN_TILE, B_MN_TILE, EPI_BF16, SCHED_WGRAD>(p, grid, st);
     default:
       return cudaErrorInvalidValue;

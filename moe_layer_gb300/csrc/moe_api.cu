@@ -1,10 +1,14 @@
 // Host side of libmoe: argument checks, workspace carving, tensor maps and the
 // launch sequence of the forward and backward passes.  Everything is enqueued
 // on the caller's stream; the host never waits for the device.
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
+#include <string>
+#include <vector>
 
 #include "gemm_launch.cuh"
 #include "moe_internal.h"
@@ -30,8 +34,55 @@ int device_sm_count() {
 }
 
 cudaError_t launch_gemm(GemmKind kind, const GemmParams& p, int grid, cudaStream_t st) {
-  if (kind <= GK_DOWN) return launch_gemm_fwd(kind, p, grid, st);
+  if (kind == GK_ROUTER || kind == GK_GATEUP || kind == GK_DOWN) return launch_gemm_fwd(kind, p, grid, st);
   return launch_gemm_bwd(kind, p, grid, st);
+}
+
+// ---------------------------------------------------------------- profiling
+// Optional per-kernel timing (moe_profile_enable / moe_profile_report): each
+// launch is bracketed by two CUDA events recorded on the launching stream.
+enum ProfLabel : int {
+  PL_ROUTER_GEMM, PL_TOPK, PL_CHUNK_SCAN, PL_SCATTER, PL_PERMUTE_X, PL_GATEUP_SHARED, PL_GATEUP_ROUTED,
+  PL_DOWN_ROUTED, PL_DOWN_SHARED, PL_COMBINE, PL_DGRAD_DOWN_ROUTED, PL_DGRAD_DOWN_SHARED,
+  PL_ROUTER_GRAD, PL_DGRAD_GATEUP_ROUTED, PL_DGRAD_GATEUP_SHARED, PL_UNPERMUTE, PL_ROUTER_WGRAD,
+  PL_WGRAD_DOWN, PL_WGRAD_GATE, PL_WGRAD_UP, PL_WGRAD_SHARED_DOWN, PL_WGRAD_SHARED_GATE,
+  PL_WGRAD_SHARED_UP, PL_PERMUTE_DY, PL_COUNT
+};
+static const char* const kProfNames[PL_COUNT] = {
+    "router_gemm", "topk_count", "chunk_scan", "scatter", "permute_x", "gateup_shared", "gateup_routed",
+    "down_routed", "down_shared", "combine", "dgrad_down_routed", "dgrad_down_shared",
+    "router_grad", "dgrad_gateup_routed", "dgrad_gateup_shared", "unpermute", "router_wgrad",
+    "wgrad_down", "wgrad_gate", "wgrad_up", "wgrad_shared_down", "wgrad_shared_gate",
+    "wgrad_shared_up", "permute_dy"};
+
+struct ProfRecord {
+  int label;
+  cudaEvent_t start, stop;
+};
+struct Profiler {
+  std::mutex mu;
+  std::atomic<bool> on{false};
+  std::vector<ProfRecord> recs;
+};
+Profiler& profiler() {
+  static Profiler p;
+  return p;
+}
+
+template <class F>
+moe_status prof_launch(int label, cudaStream_t st, F&& f) {
+  Profiler& P = profiler();
+  if (!P.on.load(std::memory_order_relaxed)) return f() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaEventRecord(a, st);
+  const cudaError_t e = f();
+  cudaEventRecord(b, st);
+  {
+    std::lock_guard<std::mutex> g(P.mu);
+    P.recs.push_back({label, a, b});
+  }
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 namespace {
@@ -85,6 +136,7 @@ void carve_routing(Carver& c, const Shape& s, Routing& r) {
 
 struct Saved {
   Routing rt;
+  __nv_bfloat16* xp;   // [Rp, d] x rows in expert-grouped order
   __nv_bfloat16* ab;   // [Rp, 2I]
   __nv_bfloat16* abs;  // [T, 2Is]
 };
@@ -92,6 +144,7 @@ void carve_saved(void* base, const Shape& s, Saved& v, size_t* bytes) {
   Carver c(base);
   c.take<char>(kAlign);
   carve_routing(c, s, v.rt);
+  v.xp = c.take<__nv_bfloat16>(s.Rp * s.d);
   v.ab = c.take<__nv_bfloat16>(s.Rp * 2 * s.I);
   v.abs = c.take<__nv_bfloat16>(s.S ? s.T * 2 * s.Is : 0);
   if (bytes) *bytes = c.off;
@@ -103,6 +156,7 @@ struct FwdWs {
   int32_t* chunk_counts;
   int32_t* chunk_base;
   Routing rt;          // used when the caller keeps no saved state
+  __nv_bfloat16* xp;   // [Rp, d], used when the caller keeps no saved state
   __nv_bfloat16* h;    // [Rp, I]
   __nv_bfloat16* hs;   // [T, Is]
   __nv_bfloat16* o;    // [Rp, d]
@@ -115,6 +169,7 @@ void carve_fwd(void* base, const Shape& s, FwdWs& w, size_t* bytes) {
   w.chunk_counts = c.take<int32_t>(s.nchunk * s.E);
   w.chunk_base = c.take<int32_t>(s.nchunk * s.E);
   carve_routing(c, s, w.rt);
+  w.xp = c.take<__nv_bfloat16>(s.Rp * s.d);
   w.h = c.take<__nv_bfloat16>(s.Rp * s.I);
   w.hs = c.take<__nv_bfloat16>(s.S ? s.T * s.Is : 0);
   w.o = c.take<__nv_bfloat16>(s.Rp * s.d);
@@ -124,6 +179,7 @@ void carve_fwd(void* base, const Shape& s, FwdWs& w, size_t* bytes) {
 
 struct BwdWs {
   int* status;
+  __nv_bfloat16* dyp;    // [Rp, d] dy rows in expert-grouped order
   __nv_bfloat16* dadb;   // [Rp, 2I]
   __nv_bfloat16* hg;     // [Rp, I]
   float* dg_part;        // [Rp, nparts]
@@ -137,6 +193,7 @@ struct BwdWs {
 void carve_bwd(void* base, const Shape& s, BwdWs& w, size_t* bytes) {
   Carver c(base);
   w.status = c.take<int>(kAlign / sizeof(int));
+  w.dyp = c.take<__nv_bfloat16>(s.Rp * s.d);
   w.dadb = c.take<__nv_bfloat16>(s.Rp * 2 * s.I);
   w.hg = c.take<__nv_bfloat16>(s.Rp * s.I);
   w.dg_part = c.take<float>(s.Rp * s.nparts);
@@ -186,6 +243,7 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
     if (st__ != MOE_OK) return st__;         \
   } while (0)
 #define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+#define MOE_LAUNCH(label, stream, expr) MOE_TRY(prof_launch((label), (stream), [&]() { return (expr); }))
 
 void zero_params(GemmParams& p) { memset(static_cast<void*>(&p), 0, sizeof(p)); }
 
@@ -229,14 +287,14 @@ moe_status run_routing(const Shape& s, const void* x, const void* W_router, cons
     p.ldo = s.E;
     p.bias = bias;
     p.status = status;
-    MOE_CUDA(launch_gemm(GK_ROUTER, p, grid_for(cdiv(s.T, kBM) * cdiv(s.E, kBN)), st));
+    MOE_LAUNCH(PL_ROUTER_GEMM, st, launch_gemm(GK_ROUTER, p, grid_for(cdiv(s.T, kBM) * cdiv(s.E, kBN)), st));
     lg = logits;
   }
-  MOE_CUDA(launch_topk_count(lg, static_cast<int>(s.T), static_cast<int>(s.E), static_cast<int>(s.k),
+  MOE_LAUNCH(PL_TOPK, st, launch_topk_count(lg, static_cast<int>(s.T), static_cast<int>(s.E), static_cast<int>(s.k),
                              rt.topk_idx, rt.topk_w, chunk_counts, status, st));
-  MOE_CUDA(launch_chunk_scan(chunk_counts, static_cast<int>(s.nchunk), static_cast<int>(s.E),
+  MOE_LAUNCH(PL_CHUNK_SCAN, st, launch_chunk_scan(chunk_counts, static_cast<int>(s.nchunk), static_cast<int>(s.E),
                              chunk_base, rt.counts, st));
-  MOE_CUDA(launch_scatter(rt.topk_idx, rt.topk_w, static_cast<int>(s.T), static_cast<int>(s.E),
+  MOE_LAUNCH(PL_SCATTER, st, launch_scatter(rt.topk_idx, rt.topk_w, static_cast<int>(s.T), static_cast<int>(s.E),
                           static_cast<int>(s.k), chunk_base, rt.counts, rt.offsets, rt.row_start,
                           rt.perm_token, rt.route_row, rt.perm_token_pad, rt.route_row_pad,
                           rt.perm_w_pad, st));
@@ -330,6 +388,10 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
   const int T = static_cast<int>(s.T), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
   const int E = static_cast<int>(s.E);
 
+  // dispatch: x rows into expert-grouped order (zeros in padding rows)
+  __nv_bfloat16* xp = saved ? sv.xp : w.xp;
+  MOE_LAUNCH(PL_PERMUTE_X, st, launch_permute_rows(static_cast<const __nv_bfloat16*>(x), rt.perm_token_pad,
+                                                  rt.row_start + E, static_cast<int>(s.Rp), d, xp, st));
   // shared expert gate/up + SwiGLU (dense rows of x)
   if (s.S) {
     GemmParams p;
@@ -347,19 +409,18 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.ldo2 = s.Is;
     p.I = static_cast<int>(s.Is);
     p.status = w.status;
-    MOE_CUDA(launch_gemm(GK_GATEUP_DENSE, p, grid_for(cdiv(s.T, kBM) * cdiv(s.Is, kBN / 2)), st));
+    MOE_LAUNCH(PL_GATEUP_SHARED, st, launch_gemm(GK_GATEUP, p, grid_for(cdiv(s.T, kBM) * cdiv(s.Is, kBN / 2)), st));
   }
-  // routed gate/up + SwiGLU, x rows gathered by expert
+  // routed gate/up + SwiGLU over the expert-grouped rows
   {
     GemmParams p;
     zero_params(p);
-    MOE_TRY(tmap(&p.tmA, x, s.T, s.d, 64, 1));
+    MOE_TRY(tmap(&p.tmA, xp, s.Rp, s.d, 64, kBM));
     MOE_TRY(tmap(&p.tmB0, wts->W_gate, s.E * s.I, s.d, 64, kBN / 2));
     MOE_TRY(tmap(&p.tmB1, wts->W_up, s.E * s.I, s.d, 64, kBN / 2));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.counts = rt.counts;
-    p.gather_idx = rt.perm_token_pad;
     p.N = I;
     p.K = d;
     p.b_group_rows = I;
@@ -370,7 +431,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.ldo2 = s.I;
     p.I = I;
     p.status = w.status;
-    MOE_CUDA(launch_gemm(GK_GATEUP_ROUTED, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.I, kBN / 2)), st));
+    MOE_LAUNCH(PL_GATEUP_ROUTED, st, launch_gemm(GK_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.I, kBN / 2)), st));
   }
   // routed down projection, scaled by the router weight of each row
   {
@@ -388,7 +449,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.ldo = s.d;
     p.row_scale = rt.perm_w_pad;
     p.status = w.status;
-    MOE_CUDA(launch_gemm(GK_DOWN, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
+    MOE_LAUNCH(PL_DOWN_ROUTED, st, launch_gemm(GK_DOWN, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
   }
   // shared down projection
   if (s.S) {
@@ -402,9 +463,9 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.out = w.ys;
     p.ldo = s.d;
     p.status = w.status;
-    MOE_CUDA(launch_gemm(GK_DOWN, p, grid_for(cdiv(s.T, kBM) * cdiv(s.d, kBN)), st));
+    MOE_LAUNCH(PL_DOWN_SHARED, st, launch_gemm(GK_DOWN, p, grid_for(cdiv(s.T, kBM) * cdiv(s.d, kBN)), st));
   }
-  MOE_CUDA(launch_combine(w.o, s.S ? w.ys : nullptr, rt.route_row_pad, T, d, static_cast<int>(s.k),
+  MOE_LAUNCH(PL_COMBINE, st, launch_combine(w.o, s.S ? w.ys : nullptr, rt.route_row_pad, T, d, static_cast<int>(s.k),
                           static_cast<__nv_bfloat16*>(y), st));
   return MOE_OK;
 }
@@ -429,17 +490,19 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
   const int T = static_cast<int>(s.T), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
   const int E = static_cast<int>(s.E), k = static_cast<int>(s.k), Is = static_cast<int>(s.Is);
 
+  // dy rows into expert-grouped order (zeros in padding rows)
+  MOE_LAUNCH(PL_PERMUTE_DY, st, launch_permute_rows(static_cast<const __nv_bfloat16*>(dy), rt.perm_token_pad,
+                                                   rt.row_start + E, static_cast<int>(s.Rp), d, w.dyp, st));
   // dgrad of the down projection with the fused SwiGLU backward and the
   // router-weight gradient partials <h, dh> per n-tile
   {
     GemmParams p;
     zero_params(p);
-    MOE_TRY(tmap(&p.tmA, dy, s.T, s.d, 64, 1));
+    MOE_TRY(tmap(&p.tmA, w.dyp, s.Rp, s.d, 64, kBM));
     MOE_TRY(tmap(&p.tmB0, wts->W_down, s.E * s.d, s.I, 64, 64));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.counts = rt.counts;
-    p.gather_idx = rt.perm_token_pad;
     p.N = I;
     p.K = d;
     p.b_group_rows = d;
@@ -453,7 +516,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.I = I;
     p.row_scale = rt.perm_w_pad;
     p.status = w.status;
-    MOE_CUDA(launch_gemm(GK_DGRAD_DOWN_ROUTED, p, grid_for(cdiv(s.Rp, kBM) * s.nparts), st));
+    MOE_LAUNCH(PL_DGRAD_DOWN_ROUTED, st, launch_gemm(GK_DGRAD_DOWN, p, grid_for(cdiv(s.Rp, kBM) * s.nparts), st));
   }
   if (s.S) {
     GemmParams p;
@@ -470,10 +533,10 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.ab = sv.abs;
     p.I = Is;
     p.status = w.status;
-    MOE_CUDA(launch_gemm(GK_DGRAD_DOWN_DENSE, p, grid_for(cdiv(s.T, kBM) * cdiv(s.Is, kBN)), st));
+    MOE_LAUNCH(PL_DGRAD_DOWN_SHARED, st, launch_gemm(GK_DGRAD_DOWN, p, grid_for(cdiv(s.T, kBM) * cdiv(s.Is, kBN)), st));
   }
-  MOE_CUDA(launch_router_grad(w.dg_part, static_cast<int>(s.nparts), rt.route_row_pad, rt.topk_w, T,
-                              k, g->d_topk_w, w.dl_tk, w.dl_row, st));
+  MOE_LAUNCH(PL_ROUTER_GRAD, st, launch_router_grad(w.dg_part, static_cast<int>(s.nparts), rt.route_row_pad,
+                                                    rt.topk_w, T, k, g->d_topk_w, w.dl_tk, w.dl_row, st));
   // dgrad of gate/up: dx_row = [da | db] . [W_gate ; W_up]
   {
     GemmParams p;
@@ -491,7 +554,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.out = w.dxp;
     p.ldo = s.d;
     p.status = w.status;
-    MOE_CUDA(launch_gemm(GK_DGRAD_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
+    MOE_LAUNCH(PL_DGRAD_GATEUP_ROUTED, st, launch_gemm(GK_DGRAD_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
   }
   if (s.S) {
     GemmParams p;
@@ -506,44 +569,42 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.out = w.dxs;
     p.ldo = s.d;
     p.status = w.status;
-    MOE_CUDA(launch_gemm(GK_DGRAD_GATEUP, p, grid_for(cdiv(s.T, kBM) * cdiv(s.d, kBN)), st));
+    MOE_LAUNCH(PL_DGRAD_GATEUP_SHARED, st, launch_gemm(GK_DGRAD_GATEUP, p, grid_for(cdiv(s.T, kBM) * cdiv(s.d, kBN)), st));
   }
-  MOE_CUDA(launch_unpermute(w.dxp, s.S ? w.dxs : nullptr, rt.route_row_pad, rt.topk_idx, w.dl_tk,
-                            static_cast<const __nv_bfloat16*>(wts->W_router), T, d, k,
-                            static_cast<__nv_bfloat16*>(dx), st));
-  MOE_CUDA(launch_router_wgrad(w.dl_row, rt.perm_token_pad, rt.row_start, rt.counts,
-                               static_cast<const __nv_bfloat16*>(x), E, d, g->dW_router, st));
+  MOE_LAUNCH(PL_UNPERMUTE, st, launch_unpermute(w.dxp, s.S ? w.dxs : nullptr, rt.route_row_pad, rt.topk_idx,
+                                                w.dl_tk, static_cast<const __nv_bfloat16*>(wts->W_router), T, d,
+                                                k, static_cast<__nv_bfloat16*>(dx), st));
+  MOE_LAUNCH(PL_ROUTER_WGRAD, st, launch_router_wgrad(w.dl_row, rt.perm_token_pad, rt.row_start, rt.counts,
+                                                      static_cast<const __nv_bfloat16*>(x), E, d, g->dW_router, st));
   // weight gradients, reduced over each expert's full row range (no split-K)
   {
     GemmParams p;  // dW_down[e] = dy_rows^T . (g h)
     zero_params(p);
-    MOE_TRY(tmap(&p.tmA, dy, s.T, s.d, 64, 1));
+    MOE_TRY(tmap(&p.tmA, w.dyp, s.Rp, s.d, 64, 64));
     MOE_TRY(tmap(&p.tmB0, w.hg, s.Rp, s.I, 64, 64));
     p.num_groups = E;
     p.row_start = rt.row_start;
-    p.gather_idx = rt.perm_token_pad;
     p.M_out = d;
     p.N = I;
     p.out = g->dW_down;
     p.ldo = s.I;
     p.status = w.status;
-    MOE_CUDA(launch_gemm(GK_WGRAD_GATHER_A, p, grid_for(s.E * cdiv(s.d, kBM) * cdiv(s.I, kBN)), st));
+    MOE_LAUNCH(PL_WGRAD_DOWN, st, launch_gemm(GK_WGRAD, p, grid_for(s.E * cdiv(s.d, kBM) * cdiv(s.I, kBN)), st));
   }
   for (int half = 0; half < 2; ++half) {
     GemmParams p;  // dW_gate[e] = da^T . x_rows ; dW_up[e] = db^T . x_rows
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, w.dadb, s.Rp, 2 * s.I, 64, 64));
-    MOE_TRY(tmap(&p.tmB0, x, s.T, s.d, 64, 1));
+    MOE_TRY(tmap(&p.tmB0, sv.xp, s.Rp, s.d, 64, 64));
     p.num_groups = E;
     p.row_start = rt.row_start;
-    p.gather_idx = rt.perm_token_pad;
     p.M_out = I;
     p.N = d;
     p.a_col_off = half ? I : 0;
     p.out = half ? g->dW_up : g->dW_gate;
     p.ldo = s.d;
     p.status = w.status;
-    MOE_CUDA(launch_gemm(GK_WGRAD_GATHER_B, p, grid_for(s.E * cdiv(s.I, kBM) * cdiv(s.d, kBN)), st));
+    MOE_LAUNCH(half ? PL_WGRAD_UP : PL_WGRAD_GATE, st, launch_gemm(GK_WGRAD, p, grid_for(s.E * cdiv(s.I, kBM) * cdiv(s.d, kBN)), st));
   }
   if (s.S) {
     {
@@ -557,7 +618,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
       p.out = g->dWs_down;
       p.ldo = s.Is;
       p.status = w.status;
-      MOE_CUDA(launch_gemm(GK_WGRAD_DENSE, p, grid_for(cdiv(s.d, kBM) * cdiv(s.Is, kBN)), st));
+      MOE_LAUNCH(PL_WGRAD_SHARED_DOWN, st, launch_gemm(GK_WGRAD, p, grid_for(cdiv(s.d, kBM) * cdiv(s.Is, kBN)), st));
     }
     for (int half = 0; half < 2; ++half) {
       GemmParams p;  // dWs_gate = da_s^T . x ; dWs_up = db_s^T . x
@@ -571,7 +632,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
       p.out = half ? g->dWs_up : g->dWs_gate;
       p.ldo = s.d;
       p.status = w.status;
-      MOE_CUDA(launch_gemm(GK_WGRAD_DENSE, p, grid_for(cdiv(s.Is, kBM) * cdiv(s.d, kBN)), st));
+      MOE_LAUNCH(half ? PL_WGRAD_SHARED_UP : PL_WGRAD_SHARED_GATE, st, launch_gemm(GK_WGRAD, p, grid_for(cdiv(s.Is, kBM) * cdiv(s.d, kBN)), st));
     }
   }
   return MOE_OK;
@@ -586,6 +647,45 @@ moe_status moe_read_device_status(void* ws, void* stream) {
   if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
   return static_cast<moe_status>(v);
+}
+
+moe_status moe_profile_enable(int enable) {
+  profiler().on.store(enable != 0);
+  return MOE_OK;
+}
+
+moe_status moe_profile_report(char* buf, size_t buflen) {
+  Profiler& P = profiler();
+  std::vector<ProfRecord> recs;
+  {
+    std::lock_guard<std::mutex> g(P.mu);
+    recs.swap(P.recs);
+  }
+  double total[PL_COUNT] = {0};
+  long long count[PL_COUNT] = {0};
+  moe_status status = MOE_OK;
+  for (const ProfRecord& r : recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+      status = MOE_ERR_CUDA;
+    total[r.label] += ms;
+    count[r.label] += 1;
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  std::string out;
+  for (int i = 0; i < PL_COUNT; ++i) {
+    if (!count[i]) continue;
+    char line[128];
+    snprintf(line, sizeof(line), "%s %lld %.6f\n", kProfNames[i], count[i], total[i]);
+    out += line;
+  }
+  if (buf && buflen) {
+    const size_t n = out.size() < buflen - 1 ? out.size() : buflen - 1;
+    memcpy(buf, out.data(), n);
+    buf[n] = 0;
+  }
+  return status;
 }
 
 const char* moe_status_string(moe_status s) {

@@ -41,6 +41,9 @@ cudaError_t launch_router_wgrad(const float* dl_row, const int32_t* perm_token_p
                                 const int32_t* row_start, const int32_t* counts,
                                 const __nv_bfloat16* x, int E, int d, float* dW_router,
                                 cudaStream_t st);
+cudaError_t launch_permute_rows(const __nv_bfloat16* src, const int32_t* idx_pad,
+                                const int32_t* total_rows, int rows_max, int d,
+                                __nv_bfloat16* dst, cudaStream_t st);
 cudaError_t launch_unpermute(const __nv_bfloat16* dxp, const __nv_bfloat16* dxs,
                              const int32_t* route_row_pad, const int32_t* topk_idx,
                              const float* dl_tk, const __nv_bfloat16* W_router, int T, int d,
@@ -48,16 +51,12 @@ cudaError_t launch_unpermute(const __nv_bfloat16* dxp, const __nv_bfloat16* dxs,
 
 // ---- tensor-core GEMM instantiations (gemm_fwd.cu, gemm_bwd.cu)
 enum GemmKind : int {
-  GK_ROUTER = 0,        // dense rows, fp32 + bias
-  GK_GATEUP_ROUTED,     // gathered x rows, gate|up, SwiGLU epilogue
-  GK_GATEUP_DENSE,      // x rows, gate|up, SwiGLU epilogue (shared expert)
-  GK_DOWN,              // rows x K-major weights, bf16 (optionally g-scaled)
-  GK_DGRAD_DOWN_ROUTED, // gathered dy rows x MN-major W_down, SwiGLU backward
-  GK_DGRAD_DOWN_DENSE,  // dy rows x MN-major Ws_down, SwiGLU backward
-  GK_DGRAD_GATEUP,      // [da|db] rows x MN-major [W_gate; W_up]
-  GK_WGRAD_GATHER_A,    // dW_down: gathered dy (MN) x hg (MN)
-  GK_WGRAD_GATHER_B,    // dW_gate/up: da or db (MN) x gathered x (MN)
-  GK_WGRAD_DENSE,       // shared-expert weight gradients
+  GK_ROUTER = 0,     // x rows . W_router^T, fp32 + bias
+  GK_GATEUP,         // rows . [W_gate; W_up]^T, SwiGLU epilogue
+  GK_DOWN,           // rows . W_down^T, bf16 (optionally scaled by the router weight)
+  GK_DGRAD_DOWN,     // dy rows . W_down (MN-major), SwiGLU backward epilogue
+  GK_DGRAD_GATEUP,   // [da|db] rows . [W_gate; W_up] (MN-major, two stacks along K)
+  GK_WGRAD,          // A^T . B over a group's rows (both MN-major): weight gradients
   GK_COUNT
 };
 cudaError_t launch_gemm(GemmKind kind, const GemmParams& p, int grid, cudaStream_t st);

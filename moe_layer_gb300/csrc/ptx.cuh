@@ -1,4 +1,4 @@
-// Inline-PTX helpers for sm_103a: mbarrier, TMA (tile and gather4), tcgen05
+// Inline-PTX helpers for sm_103a: mbarrier, TMA tile loads, tcgen05
 // (TMEM alloc, MMA, commit, load) and the bounded waits every kernel of this
 // library uses instead of unbounded spins.
 #pragma once
@@ -92,17 +92,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-
-// Four-row gather: loads rows r0..r3 (each one box of c0-width) into four
-// consecutive box-rows of shared memory.  The tensor map's box is one row high.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int c0, int r0,
-                                            int r1, int r2, int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(tmap), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
       : "memory");
 }
 

@@ -3,8 +3,8 @@
 // swizzle).  One template serves every contraction of the MoE layer:
 //
 //   * the router projection (dense rows, fp32 + bias epilogue);
-//   * the expert-grouped gate/up projection with the SwiGLU epilogue, whose A
-//     rows are token rows gathered straight from x by TMA tile::gather4;
+//   * the expert-grouped gate/up projection with the SwiGLU epilogue, over
+//     token rows already permuted into expert order;
 //   * the expert-grouped down projection scaled by the router weight;
 //   * the backward dgrads (down with the fused SwiGLU backward and router
 //     weight-gradient partials; gate/up with two weight stacks along K);
@@ -16,7 +16,7 @@
 // "Overlapping computation and communication in MoE"; paper section 2.1).
 //
 // Roles per CTA (256 threads, one CTA per SM, persistent over tiles):
-//   warp 0      TMA producer (lane 0 issues tile loads; all lanes issue gathers)
+//   warp 0      TMA producer (lane 0 issues the tile loads)
 //   warp 1      MMA issuer (lane 0), 128x256x16 bf16 MMAs into TMEM
 //   warp 2      TMEM allocator (512 columns = two 128x256 fp32 accumulators)
 //   warps 4..7  epilogue: TMEM -> registers -> fused math -> global memory
@@ -41,8 +41,8 @@ constexpr int kTmemCols = 512;
 constexpr int kGemmThreads = 256;
 constexpr int kGemmSmemBytes = 1024 + kStages * kStageBytes + 256;
 
-enum AMode : int { A_K_TILE = 0, A_K_GATHER = 1, A_MN_TILE = 2, A_MN_GATHER = 3 };
-enum BMode : int { B_K_TILE = 0, B_K_DUAL_N = 1, B_MN_TILE = 2, B_MN_DUAL_K = 3, B_MN_GATHER = 4 };
+enum AMode : int { A_K_TILE = 0, A_MN_TILE = 1 };
+enum BMode : int { B_K_TILE = 0, B_K_DUAL_N = 1, B_MN_TILE = 2, B_MN_DUAL_K = 3 };
 enum EpiMode : int { EPI_F32_BIAS = 0, EPI_SWIGLU_FWD = 1, EPI_BF16 = 2, EPI_SWIGLU_BWD = 3 };
 enum SchedMode : int { SCHED_ROWS = 0, SCHED_WGRAD = 1 };
 
@@ -55,7 +55,6 @@ struct GemmParams {
   int num_groups;          // number of groups (experts) when grouped
   const int* row_start;    // [G+1] padded row offsets, multiples of kBM (grouped)
   const int* counts;       // [G] real rows per group (grouped)
-  const int* gather_idx;   // padded row -> source row, -1 for padding (gather modes)
   int N;                   // output columns
   int K;                   // reduction length (SCHED_ROWS)
   int M_out;               // output rows per group (SCHED_WGRAD)
@@ -136,7 +135,7 @@ __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau) {
       t.rows_valid = min(kBM, p.dense_rows - t.row0);
     } else {
       // expert outer, n-tile, m-tile inner: CTAs running at the same time share
-      // one weight tile, the expert's gathered rows stay in L2.
+      // one weight tile, the expert's activation rows stay in L2.
       const int q = tau / num_nt;
       const int e = find_group(p.row_start, p.num_groups, q * kBM);
       const int rs = __ldg(p.row_start + e);
@@ -179,11 +178,6 @@ __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau) {
   return t;
 }
 
-__device__ __forceinline__ int gidx(const int* idx, int row) {
-  const int v = __ldg(idx + row);
-  return v < 0 ? 0 : v;
-}
-
 // ------------------------------------------------------------------ producer
 template <int AM, int BMO, int EPI, int SCH>
 __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_tiles,
@@ -199,14 +193,6 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
 
   for (int tau = blockIdx.x; tau < num_tiles && !aborted; tau += gridDim.x) {
     const TileInfo t = gemm_tile<EPI, SCH>(p, tau);
-    int gi0 = 0, gi1 = 0, gi2 = 0, gi3 = 0;
-    if constexpr (AM == A_K_GATHER) {
-      const int r = t.row0 + 4 * lane;
-      gi0 = gidx(p.gather_idx, r);
-      gi1 = gidx(p.gather_idx, r + 1);
-      gi2 = gidx(p.gather_idx, r + 2);
-      gi3 = gidx(p.gather_idx, r + 3);
-    }
     for (int kb = 0; kb < t.nkb; ++kb) {
       bool ok = true;
       if (lane == 0) ok = mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, p.status);
@@ -224,19 +210,11 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
       // ---- A operand
       if constexpr (AM == A_K_TILE) {
         if (lane == 0) tma_load_2d(sA, &p.tmA, kabs, t.row0, full);
-      } else if constexpr (AM == A_K_GATHER) {
-        tma_gather4(sA + lane * 4 * 128, &p.tmA, kabs, gi0, gi1, gi2, gi3, full);
-      } else if constexpr (AM == A_MN_TILE) {
+      } else {  // A_MN_TILE
         if (lane == 0) {
           tma_load_2d(sA, &p.tmA, p.a_col_off + t.m0, kabs, full);
           tma_load_2d(sA + kMNChunkBytes, &p.tmA, p.a_col_off + t.m0 + 64, kabs, full);
         }
-      } else {  // A_MN_GATHER: K rows are gathered source rows
-        const int c = lane >> 4, q = lane & 15;
-        const int r = kabs + 4 * q;
-        tma_gather4(sA + c * kMNChunkBytes + q * 4 * 128, &p.tmA, t.m0 + 64 * c,
-                    gidx(p.gather_idx, r), gidx(p.gather_idx, r + 1), gidx(p.gather_idx, r + 2),
-                    gidx(p.gather_idx, r + 3), full);
       }
       // ---- B operand
       if constexpr (BMO == B_K_TILE) {
@@ -250,21 +228,12 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
         if (lane < 4)
           tma_load_2d(sB + lane * kMNChunkBytes, &p.tmB0, t.n0 + 64 * lane,
                       t.e * p.b_group_rows + kabs, full);
-      } else if constexpr (BMO == B_MN_DUAL_K) {
+      } else {  // B_MN_DUAL_K
         if (lane < 4) {
           const bool second = kabs >= p.b_split;
           const int kk = second ? kabs - p.b_split : kabs;
           tma_load_2d(sB + lane * kMNChunkBytes, second ? (const void*)&p.tmB1 : (const void*)&p.tmB0,
                       t.n0 + 64 * lane, t.e * p.b_group_rows + kk, full);
-        }
-      } else {  // B_MN_GATHER
-        const int c = lane >> 3, q = lane & 7;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = kabs + 8 * q + 4 * h;
-          tma_gather4(sB + c * kMNChunkBytes + (8 * q + 4 * h) * 128, &p.tmB0, t.n0 + 64 * c,
-                      gidx(p.gather_idx, r), gidx(p.gather_idx, r + 1), gidx(p.gather_idx, r + 2),
-                      gidx(p.gather_idx, r + 3), full);
         }
       }
       issued_parity[s] = static_cast<int>(ph);
@@ -290,8 +259,8 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
                                          uint32_t empty0, uint32_t accf0, uint32_t acce0,
                                          uint32_t drain, uint32_t tmem_base, int num_tiles,
                                          volatile int* abort_flag) {
-  constexpr bool a_mn = (AM == A_MN_TILE || AM == A_MN_GATHER);
-  constexpr bool b_mn = (BMO == B_MN_TILE || BMO == B_MN_DUAL_K || BMO == B_MN_GATHER);
+  constexpr bool a_mn = (AM == A_MN_TILE);
+  constexpr bool b_mn = (BMO == B_MN_TILE || BMO == B_MN_DUAL_K);
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, a_mn ? 1 : 0, b_mn ? 1 : 0);
   int s = 0;
   uint32_t ph = 0;

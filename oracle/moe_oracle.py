@@ -199,7 +199,7 @@ def moe_forward(x, w_router, w_gate, w_up, w_down, top_k, router_bias=None,
 
 # ---------------------------------------------------------------- backward
 def moe_backward(x, w_router, w_gate, w_up, w_down, dy, fwd,
-                 ws_gate=None, ws_up=None, ws_down=None):
+                 ws_gate=None, ws_up=None, ws_down=None, dense_expert_grads=True):
     """Gradients of L = sum(dy * y) for the forward `fwd` (from moe_forward).
 
     Per route (t, j) with expert e and weight g, o = W_down h, h = SiLU(a)*b:
@@ -212,7 +212,10 @@ def moe_backward(x, w_router, w_gate, w_up, w_down, dy, fwd,
       dl_te = g_te (dg_te - sum_i g_ti dg_ti), and 0 elsewhere;
       dW_router = dl^T x;  dx += dl W_router.
     Shared expert: the same SwiGLU backward with g = 1.
-    Returns a dict of float64 arrays.
+    Returns a dict of float64 arrays.  With dense_expert_grads=False the
+    expert weight gradients are dicts {expert: array} holding only experts
+    that received tokens (the others are zero), which keeps large layers in
+    memory.
     """
     x = _f64(x)
     dy = _f64(dy)
@@ -222,27 +225,24 @@ def moe_backward(x, w_router, w_gate, w_up, w_down, dy, fwd,
     k = idx.shape[1]
     offsets, perm_token, perm_slot = fwd["offsets"], fwd["perm_token"], fwd["perm_slot"]
     dx = np.zeros((T, d))
-    dWg, dWu, dWd = [], [], []
+    dWg, dWu, dWd = {}, {}, {}
     dg = np.zeros((T, k))
     for e in range(E):
         rows = np.arange(offsets[e], offsets[e + 1])
-        wg, wu, wd = _f64(w_gate[e]), _f64(w_up[e]), _f64(w_down[e])
         if rows.size == 0:
-            dWg.append(np.zeros_like(wg))
-            dWu.append(np.zeros_like(wu))
-            dWd.append(np.zeros_like(wd))
             continue
+        wg, wu, wd = _f64(w_gate[e]), _f64(w_up[e]), _f64(w_down[e])
         toks, slots = perm_token[rows], perm_slot[rows]
         a, b, h = fwd["cache"]["a"][e], fwd["cache"]["b"][e], fwd["cache"]["h"][e]
         g = w[toks, slots][:, None]
         dy_e = dy[toks]
         dh = dy_e @ wd
         dg[toks, slots] = np.sum(dh * h, axis=1)
-        dWd.append(dy_e.T @ (g * h))
+        dWd[e] = dy_e.T @ (g * h)
         da = g * dh * _f64(b) * dsilu(a)
         db = g * dh * silu(a)
-        dWg.append(da.T @ x[toks])
-        dWu.append(db.T @ x[toks])
+        dWg[e] = da.T @ x[toks]
+        dWu[e] = db.T @ x[toks]
         np.add.at(dx, toks, da @ wg + db @ wu)
     # router
     s = np.sum(w * dg, axis=1, keepdims=True)
@@ -251,9 +251,16 @@ def moe_backward(x, w_router, w_gate, w_up, w_down, dy, fwd,
     np.put_along_axis(dlogits, idx, dl_sel, axis=1)
     dW_router = dlogits.T @ x
     dx += dlogits @ _f64(w_router)
-    out = {"dx": dx, "dW_gate": np.stack(dWg), "dW_up": np.stack(dWu),
-           "dW_down": np.stack(dWd), "dW_router": dW_router, "d_topk_w": dg,
-           "dlogits": dlogits}
+    if dense_expert_grads:
+        I = np.shape(w_gate[0])[0]
+        dense = {"dW_gate": np.zeros((E, I, d)), "dW_up": np.zeros((E, I, d)),
+                 "dW_down": np.zeros((E, d, I))}
+        for name, part in (("dW_gate", dWg), ("dW_up", dWu), ("dW_down", dWd)):
+            for e, v in part.items():
+                dense[name][e] = v
+        dWg, dWu, dWd = dense["dW_gate"], dense["dW_up"], dense["dW_down"]
+    out = {"dx": dx, "dW_gate": dWg, "dW_up": dWu, "dW_down": dWd, "dW_router": dW_router,
+           "d_topk_w": dg, "dlogits": dlogits}
     if ws_gate is not None:
         sh = fwd["shared"]
         wsg, wsu, wsd = _f64(ws_gate), _f64(ws_up), _f64(ws_down)
