@@ -43,7 +43,9 @@ def _peaks():
         return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
 
 
-def _workload(name):
+def _workload(name, tokens=0, experts=0):
+    import dataclasses
+
     from synth.inputs import CONFIGS
     s = CONFIGS[name]
     desc = {
@@ -51,6 +53,9 @@ def _workload(name):
         "qwen3": "Qwen3-235B-shaped BF16 MoE layer forward+backward (Zipf-skewed routing)",
         "tiny": "tiny BF16 MoE layer forward+backward",
     }[name]
+    if tokens or experts:  # scaled-down variant (profiling captures)
+        s = dataclasses.replace(s, T=tokens or s.T, E=experts or s.E)
+        desc += f" (scaled: T={s.T}, E={s.E})"
     return s, desc
 
 
@@ -196,7 +201,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     from synth.inputs import make_inputs
-    s, desc = _workload(args.workload)
+    s, desc = _workload(args.workload, args.tokens, args.experts)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = make_inputs(s, seed=0, device=dev)
     per_step = args.ref_tokens
@@ -230,6 +235,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dsv3", choices=["dsv3", "qwen3", "tiny"])
+    ap.add_argument("--tokens", type=int, default=0, help="override T (scaled-down profiling runs)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (scaled-down profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=4, help="oracle tokens per cpu_baseline round (0 = skip)")
     ap.add_argument("--cpu-rounds", type=int, default=4, help="cpu_baseline rounds")
@@ -264,7 +271,7 @@ def main():
         return float(t.item())
 
     _abi.load()
-    s, desc = _workload(args.workload)
+    s, desc = _workload(args.workload, args.tokens, args.experts)
     inp = make_inputs(s, seed=rank, device="cuda")
     cfg = _abi.make_config(s.T, s.d, s.I, s.E, s.k, s.n_shared, s.I_shared)
     bufs = layer.MoEBuffers(cfg)

@@ -258,6 +258,18 @@ moe_status tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, in
 // Persistent GEMM grid: one CTA per SM, fewer when there are fewer tiles.  The
 // environment variable MOE_GRID_LIMIT caps it further (used to check that
 // results do not depend on the grid size).
+// Output map: boxes of 64 columns x 32 rows (one epilogue warp's staging box).
+moe_status omap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+  return tmap(m, base, rows, cols, 64, 32);
+}
+// Per-expert output [G, rows, cols]: a box never crosses into the next expert.
+moe_status omap3(CUtensorMap* m, const void* base, int64_t G, int64_t rows, int64_t cols) {
+  if (!make_tmap_bf16_3d(m, base, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                         static_cast<uint64_t>(G), 64, 32))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 int grid_for(int64_t max_tiles) {
   int sms = device_sm_count();
   if (const char* lim = getenv("MOE_GRID_LIMIT")) {
@@ -402,11 +414,12 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.dense_rows = T;
     p.N = static_cast<int>(s.Is);
     p.K = d;
-    p.out = saved ? sv.abs : nullptr;
-    p.ldo = 2 * s.Is;
+    MOE_TRY(omap(&p.tmO1, w.hs, s.T, s.Is));
+    if (saved)
+      MOE_TRY(omap(&p.tmO0, sv.abs, s.T, 2 * s.Is));
+    else
+      p.tmO0 = p.tmO1;  // a and b are not kept in inference
     p.store_ab = saved ? 1 : 0;
-    p.out2 = w.hs;
-    p.ldo2 = s.Is;
     p.I = static_cast<int>(s.Is);
     p.status = w.status;
     MOE_LAUNCH(PL_GATEUP_SHARED, st, launch_gemm(GK_GATEUP, p, grid_for(cdiv(s.T, kBM) * cdiv(s.Is, kBN / 2)), st));
@@ -424,11 +437,12 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.N = I;
     p.K = d;
     p.b_group_rows = I;
-    p.out = saved ? sv.ab : nullptr;
-    p.ldo = 2 * s.I;
+    MOE_TRY(omap(&p.tmO1, w.h, s.Rp, s.I));
+    if (saved)
+      MOE_TRY(omap(&p.tmO0, sv.ab, s.Rp, 2 * s.I));
+    else
+      p.tmO0 = p.tmO1;  // a and b are not kept in inference
     p.store_ab = saved ? 1 : 0;
-    p.out2 = w.h;
-    p.ldo2 = s.I;
     p.I = I;
     p.status = w.status;
     MOE_LAUNCH(PL_GATEUP_ROUTED, st, launch_gemm(GK_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.I, kBN / 2)), st));
@@ -445,8 +459,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.N = d;
     p.K = I;
     p.b_group_rows = d;
-    p.out = w.o;
-    p.ldo = s.d;
+    MOE_TRY(omap(&p.tmO0, w.o, s.Rp, s.d));
     p.row_scale = rt.perm_w_pad;
     p.status = w.status;
     MOE_LAUNCH(PL_DOWN_ROUTED, st, launch_gemm(GK_DOWN, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
@@ -460,8 +473,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.dense_rows = T;
     p.N = d;
     p.K = static_cast<int>(s.Is);
-    p.out = w.ys;
-    p.ldo = s.d;
+    MOE_TRY(omap(&p.tmO0, w.ys, s.T, s.d));
     p.status = w.status;
     MOE_LAUNCH(PL_DOWN_SHARED, st, launch_gemm(GK_DOWN, p, grid_for(cdiv(s.T, kBM) * cdiv(s.d, kBN)), st));
   }
@@ -551,8 +563,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.K = 2 * I;
     p.b_group_rows = I;
     p.b_split = I;
-    p.out = w.dxp;
-    p.ldo = s.d;
+    MOE_TRY(omap(&p.tmO0, w.dxp, s.Rp, s.d));
     p.status = w.status;
     MOE_LAUNCH(PL_DGRAD_GATEUP_ROUTED, st, launch_gemm(GK_DGRAD_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
   }
@@ -566,8 +577,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.N = d;
     p.K = 2 * Is;
     p.b_split = Is;
-    p.out = w.dxs;
-    p.ldo = s.d;
+    MOE_TRY(omap(&p.tmO0, w.dxs, s.T, s.d));
     p.status = w.status;
     MOE_LAUNCH(PL_DGRAD_GATEUP_SHARED, st, launch_gemm(GK_DGRAD_GATEUP, p, grid_for(cdiv(s.T, kBM) * cdiv(s.d, kBN)), st));
   }
@@ -586,8 +596,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.row_start = rt.row_start;
     p.M_out = d;
     p.N = I;
-    p.out = g->dW_down;
-    p.ldo = s.I;
+    MOE_TRY(omap3(&p.tmO0, g->dW_down, s.E, s.d, s.I));
     p.status = w.status;
     MOE_LAUNCH(PL_WGRAD_DOWN, st, launch_gemm(GK_WGRAD, p, grid_for(s.E * cdiv(s.d, kBM) * cdiv(s.I, kBN)), st));
   }
@@ -601,8 +610,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.M_out = I;
     p.N = d;
     p.a_col_off = half ? I : 0;
-    p.out = half ? g->dW_up : g->dW_gate;
-    p.ldo = s.d;
+    MOE_TRY(omap3(&p.tmO0, half ? g->dW_up : g->dW_gate, s.E, s.I, s.d));
     p.status = w.status;
     MOE_LAUNCH(half ? PL_WGRAD_UP : PL_WGRAD_GATE, st, launch_gemm(GK_WGRAD, p, grid_for(s.E * cdiv(s.I, kBM) * cdiv(s.d, kBN)), st));
   }
@@ -615,8 +623,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
       p.dense_rows = T;
       p.M_out = d;
       p.N = Is;
-      p.out = g->dWs_down;
-      p.ldo = s.Is;
+      MOE_TRY(omap(&p.tmO0, g->dWs_down, s.d, s.Is));
       p.status = w.status;
       MOE_LAUNCH(PL_WGRAD_SHARED_DOWN, st, launch_gemm(GK_WGRAD, p, grid_for(cdiv(s.d, kBM) * cdiv(s.Is, kBN)), st));
     }
@@ -629,8 +636,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
       p.M_out = Is;
       p.N = d;
       p.a_col_off = half ? Is : 0;
-      p.out = half ? g->dWs_up : g->dWs_gate;
-      p.ldo = s.d;
+      MOE_TRY(omap(&p.tmO0, half ? g->dWs_up : g->dWs_gate, s.Is, s.d));
       p.status = w.status;
       MOE_LAUNCH(half ? PL_WGRAD_SHARED_UP : PL_WGRAD_SHARED_GATE, st, launch_gemm(GK_WGRAD, p, grid_for(cdiv(s.Is, kBM) * cdiv(s.d, kBN)), st));
     }

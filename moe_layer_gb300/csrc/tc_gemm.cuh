@@ -19,7 +19,8 @@
 //   warp 0      TMA producer (lane 0 issues the tile loads)
 //   warp 1      MMA issuer (lane 0), 128x256x16 bf16 MMAs into TMEM
 //   warp 2      TMEM allocator (512 columns = two 128x256 fp32 accumulators)
-//   warps 4..7  epilogue: TMEM -> registers -> fused math -> global memory
+//   warps 4..7  epilogue: TMEM -> registers -> fused math -> swizzled smem
+//               staging -> TMA bulk stores
 // Pipelines: kStages smem stages (full/empty mbarriers), two accumulator
 // buffers (acc_full/acc_empty) so the epilogue of tile i overlaps the MMAs of
 // tile i+1.  Every wait is bounded (see mbar_wait): a stuck pipeline records
@@ -39,7 +40,11 @@ constexpr int kStageBytes = kATileBytes + kBTileBytes;
 constexpr int kMNChunkBytes = kBK * 128;  // one 64-wide MN chunk of an MN-major tile
 constexpr int kTmemCols = 512;
 constexpr int kGemmThreads = 256;
-constexpr int kGemmSmemBytes = 1024 + kStages * kStageBytes + 256;
+// Epilogue staging: per epilogue warp two 4 KB boxes (32 rows x 64 bf16) that
+// TMA stores to global memory while the next box is being filled.
+constexpr int kStageBoxBytes = 32 * 128;
+constexpr int kEpiStagingBytes = 4 * 2 * kStageBoxBytes;
+constexpr int kGemmSmemBytes = 1024 + kStages * kStageBytes + kEpiStagingBytes + 256;
 
 enum AMode : int { A_K_TILE = 0, A_MN_TILE = 1 };
 enum BMode : int { B_K_TILE = 0, B_K_DUAL_N = 1, B_MN_TILE = 2, B_MN_DUAL_K = 3 };
@@ -50,6 +55,11 @@ struct GemmParams {
   CUtensorMap tmA;
   CUtensorMap tmB0;
   CUtensorMap tmB1;
+  // Output tensor maps (boxes of 64 columns x 32 rows, 128-byte swizzle):
+  //   EPI_BF16      tmO0 over `out` ([rows, N], or [G, M_out, N] for SCHED_WGRAD)
+  //   EPI_SWIGLU_FWD tmO0 over the [a|b] rows, tmO1 over h
+  CUtensorMap tmO0;
+  CUtensorMap tmO1;
   // ---- schedule
   int dense_rows;          // > 0: a single group of this many rows; 0: grouped by row_start
   int num_groups;          // number of groups (experts) when grouped
@@ -62,9 +72,9 @@ struct GemmParams {
   int a_col_off;           // first column of A in its tensor (A_MN_TILE)
   int b_split;             // B_MN_DUAL_K: K index from which B comes from tmB1
   // ---- epilogue
-  void* out;
+  void* out;               // direct-store outputs: EPI_F32_BIAS logits; EPI_SWIGLU_BWD [da|db]
   long long ldo;
-  void* out2;
+  void* out2;              // EPI_SWIGLU_BWD g*h
   long long ldo2;
   float* out3;
   int ldo3;
@@ -316,13 +326,53 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
 }
 
 // ------------------------------------------------------------------ epilogue
+// Each epilogue thread owns one accumulator row (TMEM lane).  Results are
+// converted to bf16 and written into the warp's staging boxes in the swizzled
+// layout, then one lane issues a TMA store of the 32 x 64 box; the two boxes
+// of a warp alternate so filling one overlaps the store of the other.
+struct EpiStager {
+  uint32_t base;  // this warp's two boxes
+  int slot;
+  int lane;
+  __device__ __forceinline__ uint32_t begin() {
+    if (lane == 0) bulk_wait_group_read<1>();  // the box about to be filled is free
+    __syncwarp();
+    return base + static_cast<uint32_t>(slot) * kStageBoxBytes;
+  }
+  __device__ __forceinline__ void store2d(const CUtensorMap* tm, uint32_t box, int c0, int c1) {
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tm, c0, c1, box);
+      bulk_commit_group();
+    }
+    slot ^= 1;
+  }
+  __device__ __forceinline__ void store3d(const CUtensorMap* tm, uint32_t box, int c0, int c1, int c2) {
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tm, c0, c1, c2, box);
+      bulk_commit_group();
+    }
+    slot ^= 1;
+  }
+  // stage 64 values of this thread's row and store them at (c0, c1)
+  __device__ __forceinline__ void row64_2d(const CUtensorMap* tm, const float* v, int c0, int c1) {
+    const uint32_t box = begin();
+    stage_row_sw128(box, lane, v);
+    store2d(tm, box, c0, c1);
+  }
+};
+
 template <int EPI, int SCH>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf0, uint32_t acce0,
-                                              uint32_t tmem_base, int num_tiles,
+                                              uint32_t tmem_base, uint32_t s_staging, int num_tiles,
                                               volatile int* abort_flag, int warp_e, int lane) {
   int acc = 0;
   uint32_t aph = 0;
   const int row = warp_e * 32 + lane;  // TMEM lane == tile row owned by this thread
+  EpiStager stg{s_staging + static_cast<uint32_t>(warp_e) * 2u * kStageBoxBytes, 0, lane};
   for (int tau = blockIdx.x; tau < num_tiles; tau += gridDim.x) {
     const TileInfo t = gemm_tile<EPI, SCH>(p, tau);
     const bool ok = mbar_wait(accf0 + 8 * acc, aph, abort_flag, p.status);
@@ -332,27 +382,30 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
                         static_cast<uint32_t>(acc * kBN);
 
     if constexpr (SCH == SCHED_WGRAD) {
-      const int orow = t.m0 + row;
-      const bool in_mem = orow < p.M_out;
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                         (static_cast<long long>(t.e) * p.M_out + orow) * p.ldo + t.n0;
-      for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 16) {
-        float v[16];
+      const int r0 = t.m0 + warp_e * 32;
+      for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 64) {
+        float v[64];
         if (t.nkb > 0) {
-          tmem_ld16(tr + c0, v);
+          tmem_ld32(tr + c0, v);
+          tmem_ld32(tr + c0 + 32, v + 32);
           tmem_ld_wait();
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          for (int i = 0; i < 64; ++i) v[i] = 0.f;
         }
-        if (in_mem) store_bf16x16(o + c0, v);
+        const uint32_t box = stg.begin();
+        stage_row_sw128(box, lane, v);
+        if (p.dense_rows > 0)
+          stg.store2d(&p.tmO0, box, t.n0 + c0, r0);
+        else
+          stg.store3d(&p.tmO0, box, t.n0 + c0, r0, t.e);
       }
     } else {
-      const bool dense = p.dense_rows > 0;
       const bool real = row < t.rows_valid;
-      const bool in_mem = dense ? real : true;
       const long long grow = static_cast<long long>(t.row0) + row;
+      const int r0 = t.row0 + warp_e * 32;
       if constexpr (EPI == EPI_F32_BIAS) {
+        const bool in_mem = p.dense_rows > 0 ? real : true;
         float* o = reinterpret_cast<float*>(p.out) + grow * p.ldo;
         for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 16) {
           float v[16];
@@ -367,45 +420,43 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
           }
         }
       } else if constexpr (EPI == EPI_SWIGLU_FWD) {
-        __nv_bfloat16* ab = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
-        __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(p.out2) + grow * p.ldo2;
-        for (int c0 = 0; c0 < kBN / 2 && t.n0 + c0 < p.N; c0 += 16) {
-          float a[16], b[16], hv[16];
-          tmem_ld16(tr + c0, a);
-          tmem_ld16(tr + kBN / 2 + c0, b);
+        for (int c0 = 0; c0 < kBN / 2 && t.n0 + c0 < p.N; c0 += 64) {
+          float a[64], b[64];
+          tmem_ld32(tr + c0, a);
+          tmem_ld32(tr + c0 + 32, a + 32);
+          tmem_ld32(tr + kBN / 2 + c0, b);
+          tmem_ld32(tr + kBN / 2 + c0 + 32, b + 32);
           tmem_ld_wait();
-          if (in_mem) {
+          if (!real) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              if (!real) {
-                a[i] = 0.f;
-                b[i] = 0.f;
-              }
-              hv[i] = a[i] * sigmoidf_(a[i]) * b[i];
+            for (int i = 0; i < 64; ++i) {
+              a[i] = 0.f;
+              b[i] = 0.f;
             }
-            if (p.store_ab) {
-              store_bf16x16(ab + t.n0 + c0, a);
-              store_bf16x16(ab + p.I + t.n0 + c0, b);
-            }
-            store_bf16x16(h + t.n0 + c0, hv);
           }
+          if (p.store_ab) {
+            stg.row64_2d(&p.tmO0, a, t.n0 + c0, r0);
+            stg.row64_2d(&p.tmO0, b, p.I + t.n0 + c0, r0);
+          }
+#pragma unroll
+          for (int i = 0; i < 64; ++i) a[i] = a[i] * sigmoidf_(a[i]) * b[i];
+          stg.row64_2d(&p.tmO1, a, t.n0 + c0, r0);
         }
       } else if constexpr (EPI == EPI_BF16) {
-        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
         float scale = 1.f;
-        if (in_mem && p.row_scale) scale = __ldg(p.row_scale + grow);
+        if (p.row_scale && p.dense_rows == 0) scale = __ldg(p.row_scale + grow);
         if (!real) scale = 0.f;
-        for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 16) {
-          float v[16];
-          tmem_ld16(tr + c0, v);
+        for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 64) {
+          float v[64];
+          tmem_ld32(tr + c0, v);
+          tmem_ld32(tr + c0 + 32, v + 32);
           tmem_ld_wait();
-          if (in_mem) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] *= scale;
-            store_bf16x16(o + t.n0 + c0, v);
-          }
+          for (int i = 0; i < 64; ++i) v[i] *= scale;
+          stg.row64_2d(&p.tmO0, v, t.n0 + c0, r0);
         }
-      } else {  // EPI_SWIGLU_BWD
+      } else {  // EPI_SWIGLU_BWD: direct row stores; a long K loop hides this epilogue
+        const bool in_mem = p.dense_rows > 0 ? real : true;
         __nv_bfloat16* dadb = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
         __nv_bfloat16* hg = reinterpret_cast<__nv_bfloat16*>(p.out2) + grow * p.ldo2;
         const __nv_bfloat16* abr = p.ab + grow * (2LL * p.I);
@@ -457,6 +508,9 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
       aph ^= 1;
     }
   }
+  // every TMA store of this warp has finished before the CTA may exit
+  if (lane == 0) bulk_wait_group<0>();
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -466,7 +520,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t s_tiles = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  const uint32_t s_staging = s_tiles + kStages * kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kEpiStagingBytes);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * kStages;
   const uint32_t accf0 = empty0 + 8 * kStages;
@@ -493,6 +548,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     tma_prefetch_desc(&p.tmA);
     tma_prefetch_desc(&p.tmB0);
     if (BMO == B_K_DUAL_N || BMO == B_MN_DUAL_K) tma_prefetch_desc(&p.tmB1);
+    if (EPI == EPI_BF16 || EPI == EPI_SWIGLU_FWD) tma_prefetch_desc(&p.tmO0);
+    if (EPI == EPI_SWIGLU_FWD) tma_prefetch_desc(&p.tmO1);
   }
   if (warp == 2) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -511,7 +568,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       gemm_mma<AM, BMO, EPI, SCH>(p, s_tiles, full0, empty0, accf0, acce0, drain, tmem_base,
                                   num_tiles, abort_flag);
   } else if (warp >= 4) {
-    gemm_epilogue<EPI, SCH>(p, accf0, acce0, tmem_base, num_tiles, abort_flag, warp - 4, lane);
+    gemm_epilogue<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging, num_tiles, abort_flag, warp - 4,
+                            lane);
   }
   tc_fence_before();
   __syncthreads();
