@@ -117,6 +117,33 @@ moe_status moe_route_topk(const moe_config* cfg, const void* x, const void* W_ro
                           int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
                           int32_t* perm_token, int32_t* route_row, void* ws, void* stream);
 
+/* Routing for callers that cannot allocate device memory.  (The method's pages
+ * have no counterpart to this entry point: it exists for the library's users.)
+ * Some callers cannot hand the library a workspace: their device memory is
+ * owned by a pool fixed when the process starts, or they must not create
+ * allocations while they run because an allocation can block, fail or
+ * fragment memory that another component manages.  This call computes exactly
+ * what moe_route_topk computes, with the same arguments and results, but keeps
+ * its intermediate arrays in one static device array owned by the library
+ * (8 MiB, resident on every GPU that loads the library until the process
+ * exits) instead of in `ws`.  It allocates nothing.
+ *   - logits_out is required when logits_in is NULL (the computed logits are
+ *     not kept in the static array).
+ *   - Shapes whose intermediates do not fit in the static array (about 64K
+ *     tokens at top-8 with 256 experts) return MOE_ERR_UNSUPPORTED.
+ *   - The first call on a device looks up the device address of the static
+ *     array (cudaGetSymbolAddress) with that device current; make that first
+ *     call before capturing the stream into a CUDA graph.
+ *   - All calls on a device share the array.  Calls whose GPU work overlaps
+ *     (different streams without ordering between them) race on it and give
+ *     wrong results; calls ordered on one stream are safe.
+ *   - Device-side problems (NaN logits) are not reported; use moe_route_topk
+ *     and moe_read_device_status when that matters. */
+moe_status moe_route_topk_noalloc(const moe_config* cfg, const void* x, const void* W_router,
+                                  const float* router_bias, const float* logits_in, float* logits_out,
+                                  int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                                  int32_t* perm_token, int32_t* route_row, void* stream);
+
 /* Forward of the whole layer: y [T, d] bf16 from x [T, d] bf16.
  * saved: buffer of moe_workspace_size's `saved` bytes that moe_backward will
  * read, or NULL for inference.  ws: forward workspace. */

@@ -18,8 +18,9 @@ MOE_OK = 0
 MOE_BF16 = 0
 MOE_MXFP8 = 1
 
-EXPORTED = ["moe_workspace_size", "moe_route_topk", "moe_forward", "moe_backward",
-            "moe_read_device_status", "moe_profile_enable", "moe_profile_report", "moe_status_string"]
+EXPORTED = ["moe_workspace_size", "moe_route_topk", "moe_route_topk_noalloc", "moe_forward",
+            "moe_backward", "moe_read_device_status", "moe_profile_enable", "moe_profile_report",
+            "moe_status_string"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -62,6 +63,7 @@ def load():
     sz = ctypes.POINTER(ctypes.c_size_t)
     lib.moe_workspace_size.argtypes = [cfgp, sz, sz, sz]
     lib.moe_route_topk.argtypes = [cfgp] + [P] * 13
+    lib.moe_route_topk_noalloc.argtypes = [cfgp] + [P] * 12
     lib.moe_forward.argtypes = [cfgp, P, ctypes.POINTER(MoeWeights), P, P, P, P]
     lib.moe_backward.argtypes = [cfgp, P, ctypes.POINTER(MoeWeights), P, P, P,
                                  ctypes.POINTER(MoeGrads), P, P]
@@ -124,6 +126,16 @@ def moe_route_topk(cfg, x, W_router, router_bias, logits_in, logits_out, topk_id
                                  _ptr(logits_in), _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w),
                                  _ptr(counts), _ptr(offsets), _ptr(perm_token), _ptr(route_row),
                                  _ptr(ws), _stream(stream)), "moe_route_topk")
+
+
+def moe_route_topk_noalloc(cfg, x, W_router, router_bias, logits_in, logits_out, topk_idx, topk_w,
+                           counts, offsets, perm_token, route_row, stream=None):
+    """moe_route_topk without a workspace: for callers that cannot allocate
+    device memory (see include/moe.h)."""
+    _check(load().moe_route_topk_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(W_router), _ptr(router_bias),
+                                         _ptr(logits_in), _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w),
+                                         _ptr(counts), _ptr(offsets), _ptr(perm_token), _ptr(route_row),
+                                         _stream(stream)), "moe_route_topk_noalloc")
 
 
 def make_weights(W_router, W_gate, W_up, W_down, router_bias=None, Ws_gate=None, Ws_up=None,
