@@ -80,6 +80,13 @@ def _kernel_flops(name, s):
     return table.get(name)
 
 
+# DRAM bytes per launch (read + write) of kernels measured with ncu
+# (dram__bytes_read.sum + dram__bytes_write.sum, one pass) on the named
+# workload; see profiles/tc_gemm_dgrad_gateup.md.  Remove an entry when its
+# kernel changes.
+NCU_TRAFFIC = {("dsv3", "dgrad_gateup_routed"): 16.52e9 + 2.10e9}
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle sampling during the timed region."""
 
@@ -334,9 +341,11 @@ def main():
     roofline = None
     if fl is not None:
         achieved = fl / (ms_top / n_top * 1e-3) / 1e12
+        traffic = NCU_TRAFFIC.get((args.workload, top)) if not (args.tokens or args.experts) else None
         roofline = {"kernel": top, "bound": "tensor", "achieved": achieved,
                     "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                    "frac": achieved / peaks["bf16_sustained"], "traffic": None,
+                    "frac": achieved / peaks["bf16_sustained"], "traffic": traffic,
+                    "algorithmic_flops_per_launch": fl,
                     "peak_src": peaks["src"] + " bf16 sustained (kernel timed inside a long step)"}
 
     e2e = None

@@ -42,7 +42,7 @@ import numpy as np
 
 __all__ = [
     "router_logits", "topk_route", "expert_schedule", "silu", "swiglu",
-    "moe_forward", "moe_backward",
+    "moe_forward", "moe_backward", "expert_forward", "expert_backward",
 ]
 
 
@@ -141,6 +141,12 @@ def swiglu(a, b):
     return silu(a) * _f64(b)
 
 
+def expert_forward(x_rows, w_gate, w_up, w_down):
+    """One SwiGLU expert FFN on a batch of rows: returns a, b, h, o with
+    a = x W_gate^T, b = x W_up^T, h = SiLU(a) * b, o = h W_down^T.  [Blog]"""
+    return _ffn(_f64(x_rows), w_gate, w_up, w_down)
+
+
 def _ffn(x_rows, w_gate, w_up, w_down):
     """One SwiGLU expert on a batch of rows: returns a, b, h, o."""
     a = x_rows @ _f64(w_gate).T
@@ -198,6 +204,27 @@ def moe_forward(x, w_router, w_gate, w_up, w_down, top_k, router_bias=None,
 
 
 # ---------------------------------------------------------------- backward
+def expert_backward(x_rows, dy_rows, g, a, b, h, w_gate_e, w_up_e, w_down_e):
+    """Backward of one routed expert over its rows (tokens routed to it).
+
+    x_rows, dy_rows [n, d]; g [n] router weights; a, b, h [n, I] from the
+    forward.  Per row, with dh = W_down^T dy:
+      dg = <h, dh>                                 [Blog, "Router weight gradient computation"]
+      dW_down = sum dy (g h)^T;  da = g dh * b * SiLU'(a);  db = g dh * SiLU(a)
+      dW_gate = sum da x^T;  dW_up = sum db x^T;  dx_row = W_gate^T da + W_up^T db
+    Returns (dW_gate, dW_up, dW_down, dg [n], dx_rows [n, d]).
+    """
+    x_rows, dy_rows = _f64(x_rows), _f64(dy_rows)
+    wg, wu, wd = _f64(w_gate_e), _f64(w_up_e), _f64(w_down_e)
+    g = _f64(g)[:, None]
+    dh = dy_rows @ wd
+    dg = np.sum(dh * h, axis=1)
+    dW_down = dy_rows.T @ (g * h)
+    da = g * dh * _f64(b) * dsilu(a)
+    db = g * dh * silu(a)
+    return da.T @ x_rows, db.T @ x_rows, dW_down, dg, da @ wg + db @ wu
+
+
 def moe_backward(x, w_router, w_gate, w_up, w_down, dy, fwd,
                  ws_gate=None, ws_up=None, ws_down=None, dense_expert_grads=True):
     """Gradients of L = sum(dy * y) for the forward `fwd` (from moe_forward).
@@ -231,19 +258,13 @@ def moe_backward(x, w_router, w_gate, w_up, w_down, dy, fwd,
         rows = np.arange(offsets[e], offsets[e + 1])
         if rows.size == 0:
             continue
-        wg, wu, wd = _f64(w_gate[e]), _f64(w_up[e]), _f64(w_down[e])
         toks, slots = perm_token[rows], perm_slot[rows]
-        a, b, h = fwd["cache"]["a"][e], fwd["cache"]["b"][e], fwd["cache"]["h"][e]
-        g = w[toks, slots][:, None]
-        dy_e = dy[toks]
-        dh = dy_e @ wd
-        dg[toks, slots] = np.sum(dh * h, axis=1)
-        dWd[e] = dy_e.T @ (g * h)
-        da = g * dh * _f64(b) * dsilu(a)
-        db = g * dh * silu(a)
-        dWg[e] = da.T @ x[toks]
-        dWu[e] = db.T @ x[toks]
-        np.add.at(dx, toks, da @ wg + db @ wu)
+        c = fwd["cache"]
+        dWg[e], dWu[e], dWd[e], dg_e, dx_rows = expert_backward(
+            x[toks], dy[toks], w[toks, slots], c["a"][e], c["b"][e], c["h"][e],
+            w_gate[e], w_up[e], w_down[e])
+        dg[toks, slots] = dg_e
+        np.add.at(dx, toks, dx_rows)
     # router
     s = np.sum(w * dg, axis=1, keepdims=True)
     dl_sel = w * (dg - s)

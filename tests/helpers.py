@@ -71,3 +71,15 @@ def topk_gap(logits, k):
     if s.shape[1] == k:
         return np.full(s.shape[0], np.inf)
     return s[:, k - 1] - s[:, k]
+
+
+def order_gap(logits, k):
+    """Smallest gap between consecutive values among the k+1 largest logits per
+    token: below it, float error could swap two slots or the k-th choice."""
+    s = -np.sort(-np.asarray(logits, np.float64), axis=1)
+    kk = min(k + 1, s.shape[1])
+    if kk < 2:
+        return np.full(s.shape[0], np.inf)
+    d = s[:, :kk - 1] - s[:, 1:kk]
+    d = np.where(np.isfinite(d), d, np.inf)
+    return d.min(axis=1)

@@ -1,0 +1,196 @@
+"""Full-size workloads through the C ABI, in the launch configuration bench.py
+times (same entry points, persistent grids, seeded inputs generated on the
+GPU), checked against the oracle on sampled outputs it can afford, and on
+properties that hold at any size.
+
+Workloads: the DSV3-shaped layer (T=16384, d=7168, I=2048, E=256, top-8, one
+shared expert), the Qwen3-235B-shaped layer with Zipf-skewed routing (T=8192,
+d=4096, I=1536, E=128, no shared expert), and two points of the token sweep at
+DSV3 dims (T=512 with Zipf skew and 8 zero-token experts, T=32768 uniform).
+"""
+import numpy as np
+import pytest
+import torch
+
+from moe_layer_gb300 import _abi, layer
+from oracle import moe_oracle as O
+from synth.inputs import CONFIGS, make_inputs, sweep_shape
+
+from .helpers import ensure_lib, f64, order_gap, topk_gap
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+WORKLOADS = {
+    "dsv3": CONFIGS["dsv3"],
+    "qwen3": CONFIGS["qwen3"],
+    "sweep512_zipf_zero": sweep_shape(512, zipf=True, zero_experts=8),
+    "sweep32768": sweep_shape(32768),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    ensure_lib()
+
+
+class Experts32:
+    """Indexable [E, ...] bf16 device tensor, one expert copied to the host (as
+    float32, exact for bf16) on first use."""
+
+    def __init__(self, t):
+        self.t, self.cache = t, {}
+
+    def __len__(self):
+        return self.t.shape[0]
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.cache:
+            self.cache[e] = self.t[e].float().cpu().numpy()
+        return self.cache[e]
+
+
+def _run(shape, seed=0):
+    inp = make_inputs(shape, seed=seed, device="cuda")
+    cfg = _abi.make_config(shape.T, shape.d, shape.I, shape.E, shape.k, shape.n_shared, shape.I_shared)
+    bufs = layer.MoEBuffers(cfg)
+    grads = layer.alloc_grads(cfg)
+    y = layer.forward(cfg, inp, bufs)
+    dx = layer.backward(cfg, inp, inp["dy"], bufs, grads)
+    # the routing the forward used, through the routing entry point (same kernels)
+    T, E, k = shape.T, shape.E, shape.k
+    rt = dict(logits=torch.empty(T, E, device="cuda"), idx=torch.empty(T, k, dtype=torch.int32, device="cuda"),
+              w=torch.empty(T, k, device="cuda"), counts=torch.empty(E, dtype=torch.int32, device="cuda"),
+              offsets=torch.empty(E + 1, dtype=torch.int32, device="cuda"),
+              perm=torch.empty(T * k, dtype=torch.int32, device="cuda"),
+              route_row=torch.empty(T, k, dtype=torch.int32, device="cuda"))
+    rbufs = layer.MoEBuffers(cfg, training=False)
+    _abi.moe_route_topk(cfg, inp["x"], inp["W_router"], inp["router_bias"], None, rt["logits"], rt["idx"], rt["w"],
+                        rt["counts"], rt["offsets"], rt["perm"], rt["route_row"], rbufs.fwd_ws)
+    torch.cuda.synchronize()
+    for b in (bufs.fwd_ws, bufs.bwd_ws, rbufs.fwd_ws):
+        assert _abi.moe_read_device_status(b) == 0
+    return dict(shape=shape, inp=inp, cfg=cfg, y=y, dx=dx, grads=grads, rt=rt)
+
+
+@pytest.fixture(scope="module", params=list(WORKLOADS))
+def run(request):
+    r = _run(WORKLOADS[request.param])
+    s, inp = r["shape"], r["inp"]
+    bias = None if inp["router_bias"] is None else f64(inp["router_bias"])
+    r["ref_logits"] = O.router_logits(f64(inp["x"]), f64(inp["W_router"]), bias)
+    lg, ref = f64(r["rt"]["logits"]), r["ref_logits"]
+    fin = np.isfinite(ref)
+    r["logit_err"] = float(np.abs(lg[fin] - ref[fin]).max()) if fin.any() else 0.0
+    # a token's top-k choice can differ between the GPU's float32 logits and the
+    # oracle's float64 ones only if its k-th/(k+1)-th gap is within twice the error
+    r["tie_band"] = 2.0 * r["logit_err"] + 1e-7
+    r["name"] = request.param
+    yield r
+    del r
+    torch.cuda.empty_cache()
+
+
+def _oracle_tokens(r, tokens):
+    s, inp = r["shape"], r["inp"]
+    bias = None if inp["router_bias"] is None else f64(inp["router_bias"])
+    wg, wu, wd = Experts32(inp["W_gate"]), Experts32(inp["W_up"]), Experts32(inp["W_down"])
+    sh = {}
+    if s.n_shared:
+        sh = dict(ws_gate=f64(inp["Ws_gate"]), ws_up=f64(inp["Ws_up"]), ws_down=f64(inp["Ws_down"]))
+    x, dy = f64(inp["x"][tokens]), f64(inp["dy"][tokens])
+    fwd = O.moe_forward(x, f64(inp["W_router"]), wg, wu, wd, s.k, router_bias=bias, **sh)
+    bwd = O.moe_backward(x, f64(inp["W_router"]), wg, wu, wd, dy, fwd, dense_expert_grads=False, **sh)
+    return fwd, bwd
+
+
+def test_routing_matches_oracle_outside_near_ties(run):
+    s, rt, ref = run["shape"], run["rt"], run["ref_logits"]
+    lg = f64(rt["logits"])
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(lg), fin)
+    assert np.abs(lg[fin] - ref[fin]).max() <= 1e-5 * np.abs(ref[fin]).max()
+    band = run["tie_band"]
+    ridx, _ = O.topk_route(ref, s.k)
+    gidx = rt["idx"].cpu().numpy().astype(np.int64)
+    # the selected set is unique wherever the k-th/(k+1)-th gap exceeds the band
+    safe = topk_gap(ref, s.k) > band
+    assert (np.sort(gidx[safe], axis=1) == np.sort(ridx[safe], axis=1)).all()
+    # ... and the slot order wherever every gap among the top k+1 does
+    assert (gidx[order_gap(ref, s.k) > band] == ridx[order_gap(ref, s.k) > band]).all()
+    # everywhere: the GPU's choice is a valid top-k in descending order within the band
+    chosen = np.take_along_axis(ref, gidx, axis=1)
+    kth = -np.sort(-ref, axis=1)[:, s.k - 1]
+    assert (chosen.min(axis=1) >= kth - band).all()
+    assert (np.diff(chosen, axis=1) <= band).all()
+
+
+def test_schedule_properties(run):
+    """counts/offsets/permutation are the stable counting sort of the GPU's own
+    top-k choice (unique given that choice)."""
+    s, rt = run["shape"], run["rt"]
+    idx = rt["idx"].cpu().numpy().astype(np.int64)
+    counts, offsets = rt["counts"].cpu().numpy(), rt["offsets"].cpu().numpy()
+    perm, route_row = rt["perm"].cpu().numpy(), rt["route_row"].cpu().numpy()
+    assert (counts == np.bincount(idx.ravel(), minlength=s.E)).all()
+    assert offsets[0] == 0 and (np.diff(offsets) == counts).all()
+    tok = np.repeat(np.arange(s.T), s.k)
+    flat = idx.ravel()
+    order = np.lexsort((np.arange(s.T * s.k), flat))  # stable sort by expert, then (t, j)
+    assert (perm == tok[order]).all()
+    assert (route_row.ravel()[order] == np.arange(s.T * s.k)).all()
+    if s.zero_experts:
+        assert (counts[s.E - s.zero_experts:] == 0).all()
+
+
+def test_sampled_tokens_forward_backward(run):
+    s, ref = run["shape"], run["ref_logits"]
+    rng = np.random.default_rng(0)
+    cand = np.nonzero(order_gap(ref, s.k) > 1e-3)[0]
+    tokens = np.sort(rng.choice(cand, size=3, replace=False))
+    fwd, bwd = _oracle_tokens(run, torch.as_tensor(tokens, device="cuda"))
+    y = f64(run["y"][tokens])
+    dx = f64(run["dx"][tokens])
+    dg = f64(run["grads"]["d_topk_w"][tokens])
+    rel = lambda a, b: np.abs(a - b).max() / np.abs(b).max()
+    assert rel(y, fwd["y"]) <= TOL
+    assert rel(dx, bwd["dx"]) <= TOL
+    assert rel(dg, bwd["d_topk_w"]) <= TOL
+
+
+def test_sampled_expert_weight_gradients(run):
+    s, inp, ref = run["shape"], run["inp"], run["ref_logits"]
+    ridx, rw = O.topk_route(ref, s.k)
+    gap = topk_gap(ref, s.k)
+    srt = np.argsort(-ref, axis=1, kind="stable")
+    near = gap <= run["tie_band"]
+    # experts at a near-tie boundary could legitimately get a different token set
+    touchy = set(srt[near, s.k - 1].tolist()) | set(srt[near, s.k].tolist()) if s.k < s.E else set()
+    counts = np.bincount(ridx.ravel(), minlength=s.E)
+    order = [e for e in np.argsort(-counts) if e not in touchy and counts[e] > 0]
+    experts = [order[0], order[len(order) // 2]]
+    for e in experts:
+        t, j = np.nonzero(ridx == e)
+        xs, dys = f64(inp["x"][torch.as_tensor(t, device="cuda")]), f64(inp["dy"][torch.as_tensor(t, device="cuda")])
+        wg, wu, wd = f64(inp["W_gate"][e]), f64(inp["W_up"][e]), f64(inp["W_down"][e])
+        a, b, h, _ = O.expert_forward(xs, wg, wu, wd)
+        dWg, dWu, dWd, _, _ = O.expert_backward(xs, dys, rw[t, j], a, b, h, wg, wu, wd)
+        g = run["grads"]
+        for gpu, refw, name in ((g["dW_gate"][e], dWg, "dW_gate"), (g["dW_up"][e], dWu, "dW_up"),
+                                (g["dW_down"][e], dWd, "dW_down")):
+            assert np.abs(f64(gpu) - refw).max() / np.abs(refw).max() <= TOL, (name, e)
+    if s.zero_experts:
+        for e in range(s.E - s.zero_experts, s.E):
+            assert (run["grads"]["dW_gate"][e] == 0).all() and (run["grads"]["dW_down"][e] == 0).all()
+
+
+def test_rerun_is_bitwise_identical(run):
+    if run["name"] != "dsv3":
+        pytest.skip("checked on the DSV3 workload")
+    r2 = _run(run["shape"])
+    assert torch.equal(r2["y"], run["y"]) and torch.equal(r2["dx"], run["dx"])
+    for key in ("dW_gate", "dW_down", "dW_router", "d_topk_w"):
+        assert torch.equal(r2["grads"][key], run["grads"][key]), key

@@ -12,7 +12,7 @@ from moe_layer_gb300 import _abi, layer
 from oracle import moe_oracle as O
 from synth.inputs import MoEShape, make_inputs, random_logits
 
-from .helpers import ensure_lib, f64, oracle_backward, oracle_forward, rel_err, topk_gap
+from .helpers import ensure_lib, f64, oracle_backward, oracle_forward, order_gap, rel_err, topk_gap
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
@@ -114,6 +114,8 @@ def test_forward_backward_parity(name):
     # except possibly at near-ties, which these seeds do not have
     gap = topk_gap(fwd["logits"], shape.k)
     assert gap.min() > 1e-4, "seeded input has a near-tie; pick another seed"
+    # slot order too (d_topk_w is compared slot by slot); logit errors here are ~1e-6
+    assert order_gap(fwd["logits"], shape.k).min() > 1e-5
     bwd = oracle_backward(inp, fwd)
     assert rel_err(r["y"], fwd["y"]) <= TOL
     assert rel_err(r["dx"], bwd["dx"]) <= TOL
