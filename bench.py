@@ -84,7 +84,7 @@ def _kernel_flops(name, s):
 # (dram__bytes_read.sum + dram__bytes_write.sum, one pass) on the named
 # workload; see profiles/tc_gemm_dgrad_gateup.md.  Remove an entry when its
 # kernel changes.
-NCU_TRAFFIC = {("dsv3", "dgrad_gateup_routed"): 16.52e9 + 2.10e9}
+NCU_TRAFFIC = {}
 
 
 class ClockSampler:

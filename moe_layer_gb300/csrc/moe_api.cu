@@ -258,6 +258,14 @@ moe_status tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, in
 // Persistent GEMM grid: one CTA per SM, fewer when there are fewer tiles.  The
 // environment variable MOE_GRID_LIMIT caps it further (used to check that
 // results do not depend on the grid size).
+// MN-major operand map: one box = box_chunks 64-column chunks of 64 K-rows.
+moe_status mnmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_chunks) {
+  if (!make_tmap_mn3d(m, base, static_cast<uint64_t>(rows), static_cast<uint64_t>(cols), 64,
+                      static_cast<uint32_t>(box_chunks)))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 // Output map: boxes of 64 columns x 32 rows (one epilogue warp's staging box).
 moe_status omap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
   return tmap(m, base, rows, cols, 64, 32);
@@ -511,7 +519,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, w.dyp, s.Rp, s.d, 64, kBM));
-    MOE_TRY(tmap(&p.tmB0, wts->W_down, s.E * s.d, s.I, 64, 64));
+    MOE_TRY(mnmap(&p.tmB0, wts->W_down, s.E * s.d, s.I, 4));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.counts = rt.counts;
@@ -534,7 +542,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, dy, s.T, s.d, 64, kBM));
-    MOE_TRY(tmap(&p.tmB0, wts->Ws_down, s.d, s.Is, 64, 64));
+    MOE_TRY(mnmap(&p.tmB0, wts->Ws_down, s.d, s.Is, 4));
     p.dense_rows = T;
     p.N = Is;
     p.K = d;
@@ -554,8 +562,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, w.dadb, s.Rp, 2 * s.I, 64, kBM));
-    MOE_TRY(tmap(&p.tmB0, wts->W_gate, s.E * s.I, s.d, 64, 64));
-    MOE_TRY(tmap(&p.tmB1, wts->W_up, s.E * s.I, s.d, 64, 64));
+    MOE_TRY(mnmap(&p.tmB0, wts->W_gate, s.E * s.I, s.d, 4));
+    MOE_TRY(mnmap(&p.tmB1, wts->W_up, s.E * s.I, s.d, 4));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.counts = rt.counts;
@@ -571,8 +579,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, w.dadbs, s.T, 2 * s.Is, 64, kBM));
-    MOE_TRY(tmap(&p.tmB0, wts->Ws_gate, s.Is, s.d, 64, 64));
-    MOE_TRY(tmap(&p.tmB1, wts->Ws_up, s.Is, s.d, 64, 64));
+    MOE_TRY(mnmap(&p.tmB0, wts->Ws_gate, s.Is, s.d, 4));
+    MOE_TRY(mnmap(&p.tmB1, wts->Ws_up, s.Is, s.d, 4));
     p.dense_rows = T;
     p.N = d;
     p.K = 2 * Is;
@@ -590,8 +598,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
   {
     GemmParams p;  // dW_down[e] = dy_rows^T . (g h)
     zero_params(p);
-    MOE_TRY(tmap(&p.tmA, w.dyp, s.Rp, s.d, 64, 64));
-    MOE_TRY(tmap(&p.tmB0, w.hg, s.Rp, s.I, 64, 64));
+    MOE_TRY(mnmap(&p.tmA, w.dyp, s.Rp, s.d, 2));
+    MOE_TRY(mnmap(&p.tmB0, w.hg, s.Rp, s.I, 4));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.M_out = d;
@@ -603,8 +611,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
   for (int half = 0; half < 2; ++half) {
     GemmParams p;  // dW_gate[e] = da^T . x_rows ; dW_up[e] = db^T . x_rows
     zero_params(p);
-    MOE_TRY(tmap(&p.tmA, w.dadb, s.Rp, 2 * s.I, 64, 64));
-    MOE_TRY(tmap(&p.tmB0, sv.xp, s.Rp, s.d, 64, 64));
+    MOE_TRY(mnmap(&p.tmA, w.dadb, s.Rp, 2 * s.I, 2));
+    MOE_TRY(mnmap(&p.tmB0, sv.xp, s.Rp, s.d, 4));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.M_out = I;
@@ -618,8 +626,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     {
       GemmParams p;  // dWs_down = dy^T . h_s
       zero_params(p);
-      MOE_TRY(tmap(&p.tmA, dy, s.T, s.d, 64, 64));
-      MOE_TRY(tmap(&p.tmB0, w.hs, s.T, s.Is, 64, 64));
+      MOE_TRY(mnmap(&p.tmA, dy, s.T, s.d, 2));
+      MOE_TRY(mnmap(&p.tmB0, w.hs, s.T, s.Is, 4));
       p.dense_rows = T;
       p.M_out = d;
       p.N = Is;
@@ -630,8 +638,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     for (int half = 0; half < 2; ++half) {
       GemmParams p;  // dWs_gate = da_s^T . x ; dWs_up = db_s^T . x
       zero_params(p);
-      MOE_TRY(tmap(&p.tmA, w.dadbs, s.T, 2 * s.Is, 64, 64));
-      MOE_TRY(tmap(&p.tmB0, x, s.T, s.d, 64, 64));
+      MOE_TRY(mnmap(&p.tmA, w.dadbs, s.T, 2 * s.Is, 2));
+      MOE_TRY(mnmap(&p.tmB0, x, s.T, s.d, 4));
       p.dense_rows = T;
       p.M_out = Is;
       p.N = d;

@@ -95,6 +95,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// 3-D tiled load (used for MN-major operands: one instruction fetches every
+// 64-column chunk of a tile).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int c0, int c1, int c2,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
 // Tiled bulk tensor stores shared -> global (bulk-group completion).  Parts of
 // the box outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, int c0, int c1, uint32_t src) {

@@ -52,6 +52,9 @@ enum EpiMode : int { EPI_F32_BIAS = 0, EPI_SWIGLU_FWD = 1, EPI_BF16 = 2, EPI_SWI
 enum SchedMode : int { SCHED_ROWS = 0, SCHED_WGRAD = 1 };
 
 struct GemmParams {
+  // Operand maps: K-major operands are 2-D [rows, K] maps with 64 x rows
+  // boxes; MN-major operands are 3-D maps (make_tmap_mn3d) whose box holds
+  // every 64-column chunk of the tile (2 for A, 4 for B).
   CUtensorMap tmA;
   CUtensorMap tmB0;
   CUtensorMap tmB1;
@@ -220,11 +223,8 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
       // ---- A operand
       if constexpr (AM == A_K_TILE) {
         if (lane == 0) tma_load_2d(sA, &p.tmA, kabs, t.row0, full);
-      } else {  // A_MN_TILE
-        if (lane == 0) {
-          tma_load_2d(sA, &p.tmA, p.a_col_off + t.m0, kabs, full);
-          tma_load_2d(sA + kMNChunkBytes, &p.tmA, p.a_col_off + t.m0 + 64, kabs, full);
-        }
+      } else {  // A_MN_TILE: both 64-column chunks with one 3-D box
+        if (lane == 0) tma_load_3d(sA, &p.tmA, 0, kabs, (p.a_col_off + t.m0) / 64, full);
       }
       // ---- B operand
       if constexpr (BMO == B_K_TILE) {
@@ -234,16 +234,14 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
           tma_load_2d(sB, &p.tmB0, kabs, t.e * p.b_group_rows + t.n0, full);
           tma_load_2d(sB + kBTileBytes / 2, &p.tmB1, kabs, t.e * p.b_group_rows + t.n0, full);
         }
-      } else if constexpr (BMO == B_MN_TILE) {
-        if (lane < 4)
-          tma_load_2d(sB + lane * kMNChunkBytes, &p.tmB0, t.n0 + 64 * lane,
-                      t.e * p.b_group_rows + kabs, full);
+      } else if constexpr (BMO == B_MN_TILE) {  // four 64-column chunks, one 3-D box
+        if (lane == 0) tma_load_3d(sB, &p.tmB0, 0, t.e * p.b_group_rows + kabs, t.n0 / 64, full);
       } else {  // B_MN_DUAL_K
-        if (lane < 4) {
+        if (lane == 0) {
           const bool second = kabs >= p.b_split;
           const int kk = second ? kabs - p.b_split : kabs;
-          tma_load_2d(sB + lane * kMNChunkBytes, second ? (const void*)&p.tmB1 : (const void*)&p.tmB0,
-                      t.n0 + 64 * lane, t.e * p.b_group_rows + kk, full);
+          tma_load_3d(sB, second ? (const void*)&p.tmB1 : (const void*)&p.tmB0, 0,
+                      t.e * p.b_group_rows + kk, t.n0 / 64, full);
         }
       }
       issued_parity[s] = static_cast<int>(ph);

@@ -46,6 +46,25 @@ inline bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, u
   return r == CUDA_SUCCESS;
 }
 
+// Row-major bf16 matrix [rows, cols] (cols a multiple of 64) viewed as
+// {64 elements, rows, cols / 64 chunks} with boxes of 64 x box_rows x
+// box_chunks.  One box lands in shared memory as box_chunks consecutive
+// [box_rows x 128-byte] blocks: the MN-major operand layout of the tensor-core
+// GEMM, fetched with a single TMA instruction.
+inline bool make_tmap_mn3d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows, uint32_t box_chunks) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn || cols % 64) return false;
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, box_chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Row-major bf16 tensor [d2, d1, d0] (contiguous), boxes box0 x box1 x 1,
 // 128-byte swizzle.  Used for per-expert outputs so a box never spills into
 // the next expert's rows.
