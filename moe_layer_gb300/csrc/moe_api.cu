@@ -114,6 +114,7 @@ struct Routing {
   int32_t* counts;
   int32_t* offsets;
   int32_t* row_start;
+  int32_t* tile_start;
   int32_t* perm_token;
   int32_t* route_row;
   int32_t* perm_token_pad;
@@ -127,6 +128,7 @@ void carve_routing(Carver& c, const Shape& s, Routing& r) {
   r.counts = c.take<int32_t>(s.E);
   r.offsets = c.take<int32_t>(s.E + 1);
   r.row_start = c.take<int32_t>(s.E + 1);
+  r.tile_start = c.take<int32_t>(s.E + 1);
   r.perm_token = c.take<int32_t>(s.R);
   r.route_row = c.take<int32_t>(s.T * s.k);
   r.perm_token_pad = c.take<int32_t>(s.Rp);
@@ -270,6 +272,13 @@ moe_status mnmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, i
 moe_status omap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
   return tmap(m, base, rows, cols, 64, 32);
 }
+// Output maps of a grouped GEMM: 32-row boxes and 16-row boxes (for the
+// 64-row tail tiles).
+moe_status omap2(CUtensorMap* m32, CUtensorMap* m16, const void* base, int64_t rows, int64_t cols) {
+  MOE_TRY(tmap(m32, base, rows, cols, 64, 32));
+  return tmap(m16, base, rows, cols, 64, 16);
+}
+
 // Per-expert output [G, rows, cols]: a box never crosses into the next expert.
 moe_status omap3(CUtensorMap* m, const void* base, int64_t G, int64_t rows, int64_t cols) {
   if (!make_tmap_bf16_3d(m, base, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
@@ -316,8 +325,8 @@ moe_status run_routing(const Shape& s, const void* x, const void* W_router, cons
                              chunk_base, rt.counts, st));
   MOE_LAUNCH(PL_SCATTER, st, launch_scatter(rt.topk_idx, rt.topk_w, static_cast<int>(s.T), static_cast<int>(s.E),
                           static_cast<int>(s.k), chunk_base, rt.counts, rt.offsets, rt.row_start,
-                          rt.perm_token, rt.route_row, rt.perm_token_pad, rt.route_row_pad,
-                          rt.perm_w_pad, st));
+                          rt.tile_start, rt.perm_token, rt.route_row, rt.perm_token_pad,
+                          rt.route_row_pad, rt.perm_w_pad, st));
   return MOE_OK;
 }
 
@@ -427,6 +436,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
       MOE_TRY(omap(&p.tmO0, sv.abs, s.T, 2 * s.Is));
     else
       p.tmO0 = p.tmO1;  // a and b are not kept in inference
+    p.tmO0h = p.tmO0;  // dense rows: no tail tiles
+    p.tmO1h = p.tmO1;
     p.store_ab = saved ? 1 : 0;
     p.I = static_cast<int>(s.Is);
     p.status = w.status;
@@ -445,11 +456,14 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.N = I;
     p.K = d;
     p.b_group_rows = I;
-    MOE_TRY(omap(&p.tmO1, w.h, s.Rp, s.I));
-    if (saved)
-      MOE_TRY(omap(&p.tmO0, sv.ab, s.Rp, 2 * s.I));
-    else
+    MOE_TRY(omap2(&p.tmO1, &p.tmO1h, w.h, s.Rp, s.I));
+    if (saved) {
+      MOE_TRY(omap2(&p.tmO0, &p.tmO0h, sv.ab, s.Rp, 2 * s.I));
+    } else {
       p.tmO0 = p.tmO1;  // a and b are not kept in inference
+      p.tmO0h = p.tmO1h;
+    }
+    p.tile_start = rt.tile_start;
     p.store_ab = saved ? 1 : 0;
     p.I = I;
     p.status = w.status;
@@ -467,7 +481,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.N = d;
     p.K = I;
     p.b_group_rows = d;
-    MOE_TRY(omap(&p.tmO0, w.o, s.Rp, s.d));
+    MOE_TRY(omap2(&p.tmO0, &p.tmO0h, w.o, s.Rp, s.d));
+    p.tile_start = rt.tile_start;
     p.row_scale = rt.perm_w_pad;
     p.status = w.status;
     MOE_LAUNCH(PL_DOWN_ROUTED, st, launch_gemm(GK_DOWN, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
@@ -482,6 +497,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.N = d;
     p.K = static_cast<int>(s.Is);
     MOE_TRY(omap(&p.tmO0, w.ys, s.T, s.d));
+    p.tmO0h = p.tmO0;  // dense rows: no tail tiles
     p.status = w.status;
     MOE_LAUNCH(PL_DOWN_SHARED, st, launch_gemm(GK_DOWN, p, grid_for(cdiv(s.T, kBM) * cdiv(s.d, kBN)), st));
   }
@@ -534,6 +550,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.ldo3 = static_cast<int>(s.nparts);
     p.ab = sv.ab;
     p.I = I;
+    p.tile_start = rt.tile_start;
     p.row_scale = rt.perm_w_pad;
     p.status = w.status;
     MOE_LAUNCH(PL_DGRAD_DOWN_ROUTED, st, launch_gemm(GK_DGRAD_DOWN, p, grid_for(cdiv(s.Rp, kBM) * s.nparts), st));
@@ -571,7 +588,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.K = 2 * I;
     p.b_group_rows = I;
     p.b_split = I;
-    MOE_TRY(omap(&p.tmO0, w.dxp, s.Rp, s.d));
+    MOE_TRY(omap2(&p.tmO0, &p.tmO0h, w.dxp, s.Rp, s.d));
+    p.tile_start = rt.tile_start;
     p.status = w.status;
     MOE_LAUNCH(PL_DGRAD_GATEUP_ROUTED, st, launch_gemm(GK_DGRAD_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
   }
@@ -586,6 +604,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.K = 2 * Is;
     p.b_split = Is;
     MOE_TRY(omap(&p.tmO0, w.dxs, s.T, s.d));
+    p.tmO0h = p.tmO0;  // dense rows: no tail tiles
     p.status = w.status;
     MOE_LAUNCH(PL_DGRAD_GATEUP_SHARED, st, launch_gemm(GK_DGRAD_GATEUP, p, grid_for(cdiv(s.T, kBM) * cdiv(s.d, kBN)), st));
   }

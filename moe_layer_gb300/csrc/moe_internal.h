@@ -17,7 +17,11 @@ constexpr int kChunkWarps = 8;
 constexpr int kWarpTokens = kChunkTokens / kChunkWarps;
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
-constexpr int kRowAlign = 128;  // each expert's row group starts at a multiple of this
+// Each expert's row group starts at a multiple of kRowAlign rows.  The GEMMs
+// cut a group into 128-row tiles plus, when its length is an odd multiple of
+// 64, one 64-row tail tile (computed with an M=64 MMA).
+constexpr int kRowAlign = 64;
+constexpr int kTileRows = 128;
 
 // ---- routing kernels (routing.cu)
 cudaError_t launch_topk_count(const float* logits, int T, int E, int k, int32_t* topk_idx,
@@ -26,7 +30,8 @@ cudaError_t launch_chunk_scan(const int32_t* chunk_counts, int nchunk, int E, in
                               int32_t* counts, cudaStream_t st);
 cudaError_t launch_scatter(const int32_t* topk_idx, const float* topk_w, int T, int E, int k,
                            const int32_t* chunk_base, const int32_t* counts, int32_t* offsets,
-                           int32_t* row_start, int32_t* perm_token, int32_t* route_row,
+                           int32_t* row_start, int32_t* tile_start, int32_t* perm_token,
+                           int32_t* route_row,
                            int32_t* perm_token_pad, int32_t* route_row_pad, float* perm_w_pad,
                            cudaStream_t st);
 

@@ -57,7 +57,8 @@ moe_status scratch_for_current_device(void** out) {
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct NoAllocLayout {
-  size_t status, chunk_counts, chunk_base, row_start, perm_token_pad, route_row_pad, perm_w_pad, total;
+  size_t status, chunk_counts, chunk_base, row_start, tile_start, perm_token_pad, route_row_pad, perm_w_pad,
+      total;
 };
 
 NoAllocLayout noalloc_bytes(int64_t T, int64_t E, int64_t k) {
@@ -72,6 +73,8 @@ NoAllocLayout noalloc_bytes(int64_t T, int64_t E, int64_t k) {
   L.chunk_base = off;
   off = align256(off + size_t(nchunk * E) * 4);
   L.row_start = off;
+  off = align256(off + size_t(E + 1) * 4);
+  L.tile_start = off;
   off = align256(off + size_t(E + 1) * 4);
   L.perm_token_pad = off;
   off = align256(off + size_t(Rp) * 4);
@@ -117,6 +120,7 @@ extern "C" moe_status moe_route_topk_noalloc(const moe_config* cfg, const void* 
   int32_t* chunk_counts = reinterpret_cast<int32_t*>(b + L.chunk_counts);
   int32_t* chunk_base = reinterpret_cast<int32_t*>(b + L.chunk_base);
   int32_t* row_start = reinterpret_cast<int32_t*>(b + L.row_start);
+  int32_t* tile_start = reinterpret_cast<int32_t*>(b + L.tile_start);
   int32_t* perm_token_pad = reinterpret_cast<int32_t*>(b + L.perm_token_pad);
   int32_t* route_row_pad = reinterpret_cast<int32_t*>(b + L.route_row_pad);
   float* perm_w_pad = reinterpret_cast<float*>(b + L.perm_w_pad);
@@ -149,8 +153,8 @@ extern "C" moe_status moe_route_topk_noalloc(const moe_config* cfg, const void* 
   if (launch_topk_count(lg, Ti, Ei, ki, topk_idx, topk_w, chunk_counts, status, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_chunk_scan(chunk_counts, nchunk, Ei, chunk_base, counts, st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_scatter(topk_idx, topk_w, Ti, Ei, ki, chunk_base, counts, offsets, row_start, perm_token,
-                     route_row, perm_token_pad, route_row_pad, perm_w_pad, st) != cudaSuccess)
+  if (launch_scatter(topk_idx, topk_w, Ti, Ei, ki, chunk_base, counts, offsets, row_start, tile_start,
+                     perm_token, route_row, perm_token_pad, route_row_pad, perm_w_pad, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

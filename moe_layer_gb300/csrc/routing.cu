@@ -3,8 +3,9 @@
 //               expert histogram;
 //   chunk_scan  for every expert, the exclusive prefix of its chunk counts and
 //               its total count;
-//   scatter     expert offsets (plain and padded to kRowAlign), then the stable
-//               position of every route inside its expert's row range.
+//   scatter     expert offsets (plain, padded to kRowAlign, and in GEMM row
+//               tiles), then the stable position of every route inside its
+//               expert's row range.
 // Together they are the one-rank form of the counting schedule in the
 // Mixture-of-Kittens blog post, section "Choosing the right communication
 // direction / Scheduling": a counting pass, region offsets, then a pass that
@@ -139,55 +140,65 @@ __global__ void __launch_bounds__(256)
 }
 
 __device__ __forceinline__ int pad_rows(int c) { return (c + kRowAlign - 1) / kRowAlign * kRowAlign; }
+__device__ __forceinline__ int row_tiles(int c) { return (pad_rows(c) + kTileRows - 1) / kTileRows; }
 
 __global__ void __launch_bounds__(kChunkWarps * 32)
     scatter_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int T,
                    int E, int k, const int32_t* __restrict__ chunk_base,
                    const int32_t* __restrict__ counts, int32_t* __restrict__ offsets_out,
-                   int32_t* __restrict__ row_start_out, int32_t* __restrict__ perm_token,
+                   int32_t* __restrict__ row_start_out, int32_t* __restrict__ tile_start_out,
+                   int32_t* __restrict__ perm_token,
                    int32_t* __restrict__ route_row, int32_t* __restrict__ perm_token_pad,
                    int32_t* __restrict__ route_row_pad, float* __restrict__ perm_w_pad) {
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_rs[kMaxExperts + 1];
+  __shared__ int s_ts[kMaxExperts + 1];
   __shared__ int wcnt[kChunkWarps][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // 1. expert offsets: exclusive prefix of counts, plain and padded
+  // 1. expert offsets: exclusive prefix of counts, of padded row counts and of
+  //    GEMM row tiles
   if (warp == 0) {
     const int per = (E + 31) / 32;
-    int sum = 0, psum = 0;
+    int sum = 0, psum = 0, tsum = 0;
     for (int i = 0; i < per; ++i) {
       const int e = lane * per + i;
       if (e < E) {
         const int c = __ldg(counts + e);
         sum += c;
         psum += pad_rows(c);
+        tsum += row_tiles(c);
       }
     }
-    int inc = sum, pinc = psum;
+    int inc = sum, pinc = psum, tinc = tsum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int o = __shfl_up_sync(kFull, inc, off);
       const int po = __shfl_up_sync(kFull, pinc, off);
+      const int to = __shfl_up_sync(kFull, tinc, off);
       if (lane >= off) {
         inc += o;
         pinc += po;
+        tinc += to;
       }
     }
-    int run = inc - sum, prun = pinc - psum;
+    int run = inc - sum, prun = pinc - psum, trun = tinc - tsum;
     for (int i = 0; i < per; ++i) {
       const int e = lane * per + i;
       if (e < E) {
         s_off[e] = run;
         s_rs[e] = prun;
+        s_ts[e] = trun;
         const int c = __ldg(counts + e);
         run += c;
         prun += pad_rows(c);
+        trun += row_tiles(c);
       }
     }
     if (lane == 31) {
       s_off[E] = inc;
       s_rs[E] = pinc;
+      s_ts[E] = tinc;
     }
   }
   for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) wcnt[i / E][i % E] = 0;
@@ -196,6 +207,7 @@ __global__ void __launch_bounds__(kChunkWarps * 32)
     for (int e = threadIdx.x; e <= E; e += blockDim.x) {
       offsets_out[e] = s_off[e];
       row_start_out[e] = s_rs[e];
+      tile_start_out[e] = s_ts[e];
     }
   }
   // padding rows of the padded layout: no token, weight 0
@@ -270,13 +282,14 @@ cudaError_t launch_chunk_scan(const int32_t* chunk_counts, int nchunk, int E, in
 
 cudaError_t launch_scatter(const int32_t* topk_idx, const float* topk_w, int T, int E, int k,
                            const int32_t* chunk_base, const int32_t* counts, int32_t* offsets,
-                           int32_t* row_start, int32_t* perm_token, int32_t* route_row,
-                           int32_t* perm_token_pad, int32_t* route_row_pad, float* perm_w_pad,
-                           cudaStream_t st) {
+                           int32_t* row_start, int32_t* tile_start, int32_t* perm_token,
+                           int32_t* route_row, int32_t* perm_token_pad, int32_t* route_row_pad,
+                           float* perm_w_pad, cudaStream_t st) {
   const int nchunk = (T + kChunkTokens - 1) / kChunkTokens;
   scatter_kernel<<<nchunk, kChunkWarps * 32, 0, st>>>(topk_idx, topk_w, T, E, k, chunk_base, counts,
-                                                      offsets, row_start, perm_token, route_row,
-                                                      perm_token_pad, route_row_pad, perm_w_pad);
+                                                      offsets, row_start, tile_start, perm_token,
+                                                      route_row, perm_token_pad, route_row_pad,
+                                                      perm_w_pad);
   return cudaGetLastError();
 }
 

@@ -63,10 +63,15 @@ struct GemmParams {
   //   EPI_SWIGLU_FWD tmO0 over the [a|b] rows, tmO1 over h
   CUtensorMap tmO0;
   CUtensorMap tmO1;
+  // The same outputs with 16-row boxes, for the 64-row tail tiles of grouped
+  // problems (an M=64 accumulator leaves 16 rows per epilogue warp).
+  CUtensorMap tmO0h;
+  CUtensorMap tmO1h;
   // ---- schedule
   int dense_rows;          // > 0: a single group of this many rows; 0: grouped by row_start
   int num_groups;          // number of groups (experts) when grouped
-  const int* row_start;    // [G+1] padded row offsets, multiples of kBM (grouped)
+  const int* row_start;    // [G+1] padded row offsets, multiples of 64 (grouped)
+  const int* tile_start;   // [G+1] prefix of 128-row tiles per group (grouped SCHED_ROWS)
   const int* counts;       // [G] real rows per group (grouped)
   int N;                   // output columns
   int K;                   // reduction length (SCHED_ROWS)
@@ -98,6 +103,7 @@ struct TileInfo {
   int e;           // group (expert)
   int row0;        // first row of the tile (SCHED_ROWS) in the padded row space
   int rows_valid;  // rows of the tile that hold real data
+  int m64;         // 1: 64-row tail tile of a group (M=64 MMA, 16 rows per epilogue warp)
   int m0;          // first output row (SCHED_WGRAD)
   int n0;          // first output column
   int nt;          // n-tile index
@@ -122,7 +128,7 @@ __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
   if constexpr (SCH == SCHED_ROWS) {
     const int num_nt = (p.N + tile_out_cols<EPI>() - 1) / tile_out_cols<EPI>();
     if (p.dense_rows > 0) return ((p.dense_rows + kBM - 1) / kBM) * num_nt;
-    return (__ldg(p.row_start + p.num_groups) / kBM) * num_nt;
+    return __ldg(p.tile_start + p.num_groups) * num_nt;
   } else {
     const int num_nt = (p.N + kBN - 1) / kBN;
     const int num_mt = (p.M_out + kBM - 1) / kBM;
@@ -146,19 +152,21 @@ __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau) {
       t.e = 0;
       t.row0 = mt * kBM;
       t.rows_valid = min(kBM, p.dense_rows - t.row0);
+      t.m64 = 0;
     } else {
       // expert outer, n-tile, m-tile inner: CTAs running at the same time share
       // one weight tile, the expert's activation rows stay in L2.
       const int q = tau / num_nt;
-      const int e = find_group(p.row_start, p.num_groups, q * kBM);
-      const int rs = __ldg(p.row_start + e);
-      const int mt_e = (__ldg(p.row_start + e + 1) - rs) / kBM;
-      const int local = tau - (rs / kBM) * num_nt;
+      const int e = find_group(p.tile_start, p.num_groups, q);
+      const int ts = __ldg(p.tile_start + e);
+      const int mt_e = __ldg(p.tile_start + e + 1) - ts;
+      const int local = tau - ts * num_nt;
       nt = local / mt_e;
       mt = local - nt * mt_e;
       t.e = e;
-      t.row0 = rs + mt * kBM;
-      t.rows_valid = max(0, min(kBM, __ldg(p.counts + e) - mt * kBM));
+      t.row0 = __ldg(p.row_start + e) + mt * kBM;
+      t.m64 = (__ldg(p.row_start + e + 1) - t.row0) < kBM ? 1 : 0;
+      t.rows_valid = max(0, min(t.m64 ? kBM / 2 : kBM, __ldg(p.counts + e) - mt * kBM));
     }
     t.m0 = 0;
     t.nt = nt;
@@ -179,6 +187,7 @@ __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau) {
     t.n0 = nt * kBN;
     t.row0 = 0;
     t.rows_valid = 0;
+    t.m64 = 0;
     if (p.dense_rows > 0) {
       t.kb0 = 0;
       t.nkb = (p.dense_rows + kBK - 1) / kBK;
@@ -269,7 +278,8 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
                                          volatile int* abort_flag) {
   constexpr bool a_mn = (AM == A_MN_TILE);
   constexpr bool b_mn = (BMO == B_MN_TILE || BMO == B_MN_DUAL_K);
-  constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+  constexpr uint32_t idesc128 = idesc_bf16_f32(kBM, kBN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+  constexpr uint32_t idesc64 = idesc_bf16_f32(kBM / 2, kBN, a_mn ? 1 : 0, b_mn ? 1 : 0);
   int s = 0;
   uint32_t ph = 0;
   int acc = 0;
@@ -283,6 +293,7 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
     }
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+    const uint32_t idesc = t.m64 ? idesc64 : idesc128;
     for (int kb = 0; kb < t.nkb; ++kb) {
       if (!mbar_wait(full0 + 8 * s, ph, abort_flag, p.status)) {
         aborted = true;
@@ -369,10 +380,15 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
                                               volatile int* abort_flag, int warp_e, int lane) {
   int acc = 0;
   uint32_t aph = 0;
-  const int row = warp_e * 32 + lane;  // TMEM lane == tile row owned by this thread
   EpiStager stg{s_staging + static_cast<uint32_t>(warp_e) * 2u * kStageBoxBytes, 0, lane};
   for (int tau = blockIdx.x; tau < num_tiles; tau += gridDim.x) {
     const TileInfo t = gemm_tile<EPI, SCH>(p, tau);
+    // Tile row held by this thread's TMEM lane: lane l of warp w is row 32w + l
+    // of an M=128 accumulator; an M=64 accumulator keeps rows 16w..16w+15 in
+    // lanes 0..15 of each warp (lanes 16..31 hold nothing of this tile).
+    const int wrows = t.m64 ? 16 : 32;
+    const bool lane_ok = lane < wrows;
+    const int row = warp_e * wrows + lane;
     const bool ok = mbar_wait(accf0 + 8 * acc, aph, abort_flag, p.status);
     if (!__all_sync(0xffffffffu, ok)) break;
     tc_fence_after();
@@ -399,11 +415,13 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
           stg.store3d(&p.tmO0, box, t.n0 + c0, r0, t.e);
       }
     } else {
-      const bool real = row < t.rows_valid;
+      const bool real = lane_ok && row < t.rows_valid;
       const long long grow = static_cast<long long>(t.row0) + row;
-      const int r0 = t.row0 + warp_e * 32;
+      const int r0 = t.row0 + warp_e * wrows;
+      const CUtensorMap* o0 = t.m64 ? &p.tmO0h : &p.tmO0;
+      const CUtensorMap* o1 = t.m64 ? &p.tmO1h : &p.tmO1;
       if constexpr (EPI == EPI_F32_BIAS) {
-        const bool in_mem = p.dense_rows > 0 ? real : true;
+        const bool in_mem = p.dense_rows > 0 ? real : lane_ok;
         float* o = reinterpret_cast<float*>(p.out) + grow * p.ldo;
         for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 16) {
           float v[16];
@@ -433,16 +451,16 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
             }
           }
           if (p.store_ab) {
-            stg.row64_2d(&p.tmO0, a, t.n0 + c0, r0);
-            stg.row64_2d(&p.tmO0, b, p.I + t.n0 + c0, r0);
+            stg.row64_2d(o0, a, t.n0 + c0, r0);
+            stg.row64_2d(o0, b, p.I + t.n0 + c0, r0);
           }
 #pragma unroll
           for (int i = 0; i < 64; ++i) a[i] = a[i] * sigmoidf_(a[i]) * b[i];
-          stg.row64_2d(&p.tmO1, a, t.n0 + c0, r0);
+          stg.row64_2d(o1, a, t.n0 + c0, r0);
         }
       } else if constexpr (EPI == EPI_BF16) {
         float scale = 1.f;
-        if (p.row_scale && p.dense_rows == 0) scale = __ldg(p.row_scale + grow);
+        if (p.row_scale && p.dense_rows == 0 && lane_ok) scale = __ldg(p.row_scale + grow);
         if (!real) scale = 0.f;
         for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 64) {
           float v[64];
@@ -451,10 +469,10 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 64; ++i) v[i] *= scale;
-          stg.row64_2d(&p.tmO0, v, t.n0 + c0, r0);
+          stg.row64_2d(o0, v, t.n0 + c0, r0);
         }
       } else {  // EPI_SWIGLU_BWD: direct row stores; a long K loop hides this epilogue
-        const bool in_mem = p.dense_rows > 0 ? real : true;
+        const bool in_mem = p.dense_rows > 0 ? real : lane_ok;
         __nv_bfloat16* dadb = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
         __nv_bfloat16* hg = reinterpret_cast<__nv_bfloat16*>(p.out2) + grow * p.ldo2;
         const __nv_bfloat16* abr = p.ab + grow * (2LL * p.I);
@@ -547,6 +565,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     tma_prefetch_desc(&p.tmB0);
     if (BMO == B_K_DUAL_N || BMO == B_MN_DUAL_K) tma_prefetch_desc(&p.tmB1);
     if (EPI == EPI_BF16 || EPI == EPI_SWIGLU_FWD) tma_prefetch_desc(&p.tmO0);
+    if ((EPI == EPI_BF16 || EPI == EPI_SWIGLU_FWD) && SCH == SCHED_ROWS) tma_prefetch_desc(&p.tmO0h);
+    if (EPI == EPI_SWIGLU_FWD) tma_prefetch_desc(&p.tmO1h);
     if (EPI == EPI_SWIGLU_FWD) tma_prefetch_desc(&p.tmO1);
   }
   if (warp == 2) {
