@@ -43,6 +43,7 @@ import numpy as np
 __all__ = [
     "router_logits", "topk_route", "expert_schedule", "silu", "swiglu",
     "moe_forward", "moe_backward", "expert_forward", "expert_backward",
+    "e4m3_decode", "e4m3_quantize", "mx_quantize", "mx_dequantize", "mx_round", "E4M3_TABLE",
 ]
 
 
@@ -141,24 +142,105 @@ def swiglu(a, b):
     return silu(a) * _f64(b)
 
 
-def expert_forward(x_rows, w_gate, w_up, w_down):
+def expert_forward(x_rows, w_gate, w_up, w_down, mxfp8=False):
     """One SwiGLU expert FFN on a batch of rows: returns a, b, h, o with
-    a = x W_gate^T, b = x W_up^T, h = SiLU(a) * b, o = h W_down^T.  [Blog]"""
-    return _ffn(_f64(x_rows), w_gate, w_up, w_down)
+    a = x W_gate^T, b = x W_up^T, h = SiLU(a) * b, o = h W_down^T.  [Blog]
+    With mxfp8=True every operand of the two GEMMs goes through an MXFP8
+    round trip along that GEMM's reduction axis first: x and W_gate/W_up along
+    d, h and W_down along I [Blog, "MXFP8 support"]; the returned h is the
+    unquantized one."""
+    return _ffn(_f64(x_rows), w_gate, w_up, w_down, mxfp8)
 
 
-def _ffn(x_rows, w_gate, w_up, w_down):
+def _ffn(x_rows, w_gate, w_up, w_down, mxfp8=False):
     """One SwiGLU expert on a batch of rows: returns a, b, h, o."""
-    a = x_rows @ _f64(w_gate).T
-    b = x_rows @ _f64(w_up).T
+    q = mx_round if mxfp8 else (lambda v, axis=-1: _f64(v))
+    xq = q(x_rows, axis=-1)
+    a = xq @ q(w_gate, axis=-1).T
+    b = xq @ q(w_up, axis=-1).T
     h = swiglu(a, b)
-    o = h @ _f64(w_down).T
+    o = q(h, axis=-1) @ q(w_down, axis=-1).T
     return a, b, h, o
+
+
+# ---------------------------------------------------------------- MXFP8
+# The MX block format (MXFP8 with E4M3 elements and E8M0 shared scales) that
+# the pages' MXFP8 mode uses [Blog, "MXFP8 support"; the MX format reference
+# the pages cite].  Reading taken here (listed in DESIGN.md):
+#   * a block is 32 consecutive elements along the reduction axis of the GEMM
+#     the operand feeds;
+#   * shared scale X = 2^(floor(log2(amax)) - 8), 8 being the largest exponent
+#     of E4M3; X is stored as the biased exponent E8M0 (bias 127); an all-zero
+#     block gets the smallest scale code 0;
+#   * each element is v / X rounded to the nearest E4M3 value (ties to even
+#     mantissa), saturating at +-448.
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(code):
+    """Value of an E4M3 byte: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa
+    bits; exponent 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN (no inf)."""
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+E4M3_TABLE = np.array([e4m3_decode(c) for c in range(256)])
+_E4M3_POS = np.array([E4M3_TABLE[c] for c in range(0x7F)])  # 0x00..0x7E, ascending
+
+
+def e4m3_quantize(v):
+    """Round float64 values to E4M3 codes: nearest value, ties to the even
+    mantissa (even code), magnitudes beyond 448 saturate to 448."""
+    v = np.asarray(v, np.float64)
+    a = np.minimum(np.abs(v), E4M3_MAX)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, len(_E4M3_POS) - 1)
+    lo = np.maximum(hi - 1, 0)
+    dlo, dhi = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = pick.astype(np.uint8)
+    neg = (v < 0) & (code != 0)
+    return np.where(neg, code | 0x80, code).astype(np.uint8)
+
+
+def mx_quantize(v, axis=-1):
+    """MXFP8 quantization of v along `axis` in blocks of 32 (the axis length
+    must be a multiple of 32).  Returns (codes uint8, same shape as v; scale
+    exponents uint8 (E8M0 codes) with that axis divided by 32)."""
+    v = np.moveaxis(np.asarray(v, np.float64), axis, -1)
+    shp = v.shape
+    blk = v.reshape(shp[:-1] + (shp[-1] // 32, 32))
+    amax = np.abs(blk).max(axis=-1)
+    with np.errstate(divide="ignore"):
+        e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 8, -127)
+    e = np.clip(e, -127, 127)
+    scale = np.ldexp(1.0, e.astype(np.int64))
+    codes = e4m3_quantize(blk / scale[..., None]).reshape(shp)
+    return np.moveaxis(codes, -1, axis), np.moveaxis((e + 127).astype(np.uint8), -1, axis)
+
+
+def mx_dequantize(codes, scale_codes, axis=-1):
+    """Float64 values of MXFP8 codes with their E8M0 block scales."""
+    c = np.moveaxis(np.asarray(codes), axis, -1)
+    s = np.moveaxis(np.asarray(scale_codes), axis, -1).astype(np.int64) - 127
+    vals = E4M3_TABLE[c.astype(np.int64)]
+    return np.moveaxis(vals * np.ldexp(1.0, np.repeat(s, 32, axis=-1)), -1, axis)
+
+
+def mx_round(v, axis=-1):
+    """v after an MXFP8 round trip along `axis` (the value the GEMM sees)."""
+    return mx_dequantize(*mx_quantize(v, axis), axis=axis)
 
 
 # ---------------------------------------------------------------- forward
 def moe_forward(x, w_router, w_gate, w_up, w_down, top_k, router_bias=None,
-                ws_gate=None, ws_up=None, ws_down=None, logits=None):
+                ws_gate=None, ws_up=None, ws_down=None, logits=None, mxfp8=False):
     """The MoE layer forward, per token t:
 
         y_t = FFN_shared(x_t) + sum_j g_tj * FFN_{e_tj}(x_t)
@@ -168,7 +250,9 @@ def moe_forward(x, w_router, w_gate, w_up, w_down, top_k, router_bias=None,
     w_gate/w_up/w_down are indexable by expert (w_gate[e] is [I, d],
     w_down[e] is [d, I]).  `logits` may be given to route on precomputed
     values (e.g. float32 values for an exact comparison of the routing);
-    otherwise they are computed in float64 from x and w_router.
+    otherwise they are computed in float64 from x and w_router.  mxfp8=True
+    runs the routed experts' GEMMs on MXFP8 operands (expert_forward); the
+    router and the shared expert stay in full precision [Blog, "MXFP8 support"].
     Returns a dict with y [T, d] and everything the backward needs.
     """
     x = _f64(x)
@@ -187,7 +271,7 @@ def moe_forward(x, w_router, w_gate, w_up, w_down, top_k, router_bias=None,
         if rows.size == 0:
             continue
         toks = perm_token[rows]
-        a, b, h, o = _ffn(x[toks], w_gate[e], w_up[e], w_down[e])
+        a, b, h, o = _ffn(x[toks], w_gate[e], w_up[e], w_down[e], mxfp8)
         cache["a"][e], cache["b"][e], cache["h"][e], cache["o"][e] = a, b, h, o
         g = w[toks, perm_slot[rows]]
         np.add.at(y, toks, g[:, None] * o)
@@ -199,12 +283,22 @@ def moe_forward(x, w_router, w_gate, w_up, w_down, top_k, router_bias=None,
     return {
         "y": y, "logits": logits, "topk_idx": idx, "topk_w": w, "counts": counts,
         "offsets": offsets, "perm_token": perm_token, "perm_slot": perm_slot,
-        "route_row": route_row, "cache": cache, "shared": shared,
+        "route_row": route_row, "cache": cache, "shared": shared, "mxfp8": mxfp8,
     }
 
 
 # ---------------------------------------------------------------- backward
-def expert_backward(x_rows, dy_rows, g, a, b, h, w_gate_e, w_up_e, w_down_e):
+def _mx_rows(v):
+    """MXFP8 round trip along the token axis (axis 0) in blocks of 32 rows, the
+    rows padded with zeros to a multiple of 32 (the padding is dropped)."""
+    v = _f64(v)
+    n = v.shape[0]
+    pad = (-n) % 32
+    vp = np.concatenate([v, np.zeros((pad,) + v.shape[1:])], axis=0) if pad else v
+    return mx_round(vp, axis=0)[:n]
+
+
+def expert_backward(x_rows, dy_rows, g, a, b, h, w_gate_e, w_up_e, w_down_e, mxfp8=False):
     """Backward of one routed expert over its rows (tokens routed to it).
 
     x_rows, dy_rows [n, d]; g [n] router weights; a, b, h [n, I] from the
@@ -213,16 +307,31 @@ def expert_backward(x_rows, dy_rows, g, a, b, h, w_gate_e, w_up_e, w_down_e):
       dW_down = sum dy (g h)^T;  da = g dh * b * SiLU'(a);  db = g dh * SiLU(a)
       dW_gate = sum da x^T;  dW_up = sum db x^T;  dx_row = W_gate^T da + W_up^T db
     Returns (dW_gate, dW_up, dW_down, dg [n], dx_rows [n, d]).
+    With mxfp8=True every operand of the five GEMMs goes through an MXFP8 round
+    trip along that GEMM's reduction axis: dy and W_down along d for dh;
+    [da | db] and [W_gate; W_up] along 2I for dx; the token axis (blocks of 32
+    rows of this expert, zero-padded) for the three weight gradients.  dg uses
+    the unquantized h and dh [Blog, "MXFP8 support", "Router weight gradient
+    computation"].
     """
     x_rows, dy_rows = _f64(x_rows), _f64(dy_rows)
     wg, wu, wd = _f64(w_gate_e), _f64(w_up_e), _f64(w_down_e)
     g = _f64(g)[:, None]
-    dh = dy_rows @ wd
+    if mxfp8:
+        dh = mx_round(dy_rows, axis=-1) @ mx_round(wd, axis=0)
+    else:
+        dh = dy_rows @ wd
     dg = np.sum(dh * h, axis=1)
-    dW_down = dy_rows.T @ (g * h)
     da = g * dh * _f64(b) * dsilu(a)
     db = g * dh * silu(a)
-    return da.T @ x_rows, db.T @ x_rows, dW_down, dg, da @ wg + db @ wu
+    hg = g * h
+    if not mxfp8:
+        return da.T @ x_rows, db.T @ x_rows, dy_rows.T @ hg, dg, da @ wg + db @ wu
+    dadb = mx_round(np.concatenate([da, db], axis=1), axis=-1)
+    wgu = mx_round(np.concatenate([wg, wu], axis=0), axis=0)
+    xr = _mx_rows(x_rows)
+    return (_mx_rows(da).T @ xr, _mx_rows(db).T @ xr, _mx_rows(dy_rows).T @ _mx_rows(hg), dg,
+            dadb @ wgu)
 
 
 def moe_backward(x, w_router, w_gate, w_up, w_down, dy, fwd,
@@ -262,7 +371,7 @@ def moe_backward(x, w_router, w_gate, w_up, w_down, dy, fwd,
         c = fwd["cache"]
         dWg[e], dWu[e], dWd[e], dg_e, dx_rows = expert_backward(
             x[toks], dy[toks], w[toks, slots], c["a"][e], c["b"][e], c["h"][e],
-            w_gate[e], w_up[e], w_down[e])
+            w_gate[e], w_up[e], w_down[e], fwd.get("mxfp8", False))
         dg[toks, slots] = dg_e
         np.add.at(dx, toks, dx_rows)
     # router

@@ -257,3 +257,100 @@ def test_backward_empty_expert_gets_zero_grad():
     assert fwd["counts"][2] == 0
     G = O.moe_backward(x, wr, wg, wu, wd, dy, fwd)
     assert (G["dW_gate"][2] == 0).all() and (G["dW_down"][2] == 0).all()
+
+
+# ------------------------------------------------------------------ MXFP8
+def test_e4m3_table_matches_torch_float8():
+    """Every non-NaN E4M3 code decodes as torch's float8_e4m3fn does; the
+    format's fixed points: max 448, smallest subnormal 2^-9, NaN at S.1111.111."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert nan.tolist() == [c in (0x7F, 0xFF) for c in range(256)]
+    assert np.isnan(O.E4M3_TABLE[nan]).all()
+    np.testing.assert_array_equal(O.E4M3_TABLE[~nan], ref[~nan])
+    assert O.E4M3_TABLE[0x7E] == 448.0 and O.E4M3_TABLE[1] == 2.0 ** -9
+
+
+def _brute_e4m3(v):
+    vals = O.E4M3_TABLE[:0x7F]  # non-negative codes
+    a = min(abs(v), 448.0)
+    d = np.abs(vals - a)
+    best = np.nonzero(d == d.min())[0]
+    code = int(best[0]) if len(best) == 1 else int(best[best % 2 == 0][0])  # tie: even mantissa
+    return O.E4M3_TABLE[code] * (-1.0 if v < 0 else 1.0)
+
+
+def test_e4m3_quantize_bruteforce_nearest_even():
+    rng = _rng(11)
+    vals = np.concatenate([rng.normal(size=300) * 50, rng.normal(size=100) * 1e-2,
+                           O.E4M3_TABLE[:0x7E] + 1e-12, [0.0, 448.0, 464.0, 1000.0, -1000.0, 2.0 ** -10]])
+    got = O.E4M3_TABLE[O.e4m3_quantize(vals)]
+    want = np.array([_brute_e4m3(v) for v in vals])
+    np.testing.assert_array_equal(got, want)
+    # exact midpoints between neighbours go to the even-mantissa code
+    pos = O.E4M3_TABLE[:0x7E]
+    mids = (pos[:-1] + pos[1:]) / 2
+    codes = O.e4m3_quantize(mids)
+    assert (codes % 2 == 0).all()
+
+
+def test_e4m3_quantize_matches_torch_cast_in_range():
+    rng = _rng(12)
+    v = np.clip(rng.normal(size=2000) * 60, -448, 448)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = O.e4m3_quantize(v)
+    np.testing.assert_array_equal(O.E4M3_TABLE[got], O.E4M3_TABLE[ref])
+
+
+def test_mx_block_scale_definition():
+    """amax / 2^(E-127) lies in [256, 512) for every non-zero block (the E8M0
+    scale is 2^(floor(log2 amax) - 8)); an all-zero block gets code 0 and zero
+    elements; every element is within half an E4M3 step of v / X, or saturated."""
+    rng = _rng(13)
+    v = rng.normal(size=(20, 96)) * np.exp(rng.normal(size=(20, 1)) * 4)
+    v[3, 32:64] = 0.0
+    codes, sc = O.mx_quantize(v, axis=1)
+    X = np.ldexp(1.0, sc.astype(np.int64) - 127)
+    amax = np.abs(v.reshape(20, 3, 32)).max(-1)
+    nz = amax > 0
+    r = amax[nz] / X[nz]
+    assert (r >= 256).all() and (r < 512).all()
+    assert sc[3, 1] == 0 and (codes[3, 32:64] == 0).all()
+    y = O.mx_dequantize(codes, sc, axis=1)
+    Xe = np.repeat(X, 32, axis=1)
+    scaled = v / Xe
+    sat = np.abs(scaled) > 448
+    assert (np.abs(y[sat]) == 448 * Xe[sat]).all()
+    # E4M3 step at magnitude m (normal range) is 2^(floor(log2 m) - 3)
+    m = np.abs(scaled[~sat & (np.abs(scaled) >= 2 ** -6)])
+    step = np.ldexp(1.0, np.floor(np.log2(m)).astype(np.int64) - 3)
+    assert (np.abs(y[~sat & (np.abs(scaled) >= 2 ** -6)] / Xe[~sat & (np.abs(scaled) >= 2 ** -6)] - np.sign(scaled[~sat & (np.abs(scaled) >= 2 ** -6)]) * m) <= step / 2).all()
+
+
+def test_mx_round_is_idempotent_and_axis_consistent():
+    rng = _rng(14)
+    v = rng.normal(size=(64, 96))
+    r1 = O.mx_round(v, axis=1)
+    np.testing.assert_array_equal(O.mx_round(r1, axis=1), r1)
+    np.testing.assert_array_equal(O.mx_round(v.T, axis=0), r1.T)
+
+
+def test_mxfp8_layer_stays_near_full_precision():
+    """The MXFP8 layer differs from the full-precision one only by the
+    quantization of the routed GEMM operands (a few percent at most)."""
+    rng = _rng(15)
+    T, d, I, E, k, I_s = 9, 64, 64, 4, 2, 32
+    wg, wu, wd, (sg, su, sd) = _weights(rng, E, d, I, I_s, std=0.2)
+    P = dict(x=rng.normal(size=(T, d)), wr=rng.normal(size=(E, d)) * 0.3, wg=wg, wu=wu, wd=wd,
+             dy=rng.normal(size=(T, d)), k=k)
+    kw = dict(ws_gate=sg, ws_up=su, ws_down=sd)
+    f = O.moe_forward(P["x"], P["wr"], P["wg"], P["wu"], P["wd"], P["k"], **kw)
+    fq = O.moe_forward(P["x"], P["wr"], P["wg"], P["wu"], P["wd"], P["k"], mxfp8=True, **kw)
+    rel = np.abs(fq["y"] - f["y"]).max() / np.abs(f["y"]).max()
+    assert 0 < rel < 0.1
+    b = O.moe_backward(P["x"], P["wr"], P["wg"], P["wu"], P["wd"], P["dy"], f, **kw)
+    bq = O.moe_backward(P["x"], P["wr"], P["wg"], P["wu"], P["wd"], P["dy"], fq, **kw)
+    for key in ["dx", "dW_gate", "dW_up", "dW_down", "dW_router"]:
+        r = np.abs(bq[key] - b[key]).max() / np.abs(b[key]).max()
+        assert 0 < r < 0.15, key
