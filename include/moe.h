@@ -66,7 +66,7 @@ typedef struct {
   int64_t top_k;    /* experts per token */
   int64_t n_shared; /* shared experts: 0 or 1 */
   int64_t I_shared; /* shared expert intermediate dimension (ignored if n_shared == 0) */
-  int32_t precision;/* moe_precision; only MOE_BF16 is implemented */
+  int32_t precision;/* moe_precision */
   uint32_t flags;   /* reserved, must be 0 */
 } moe_config;
 
@@ -99,6 +99,23 @@ typedef struct {
  * Each buffer must be 256-byte aligned; its first 256 bytes hold the device
  * status word and must be zero before the buffer's first use. */
 moe_status moe_workspace_size(const moe_config* cfg, size_t* fwd_ws, size_t* saved, size_t* bwd_ws);
+
+/* MXFP8 mode (precision = MOE_MXFP8, d and I multiples of 128; blog section
+ * "MXFP8 support"): the routed experts' GEMMs run on E4M3 operands with one
+ * E8M0 scale per 32 elements along each GEMM's reduction axis
+ * (X = 2^(floor(log2 amax) - 8), elements rounded to nearest even and
+ * saturated at 448); router and shared expert stay bf16.
+ * moe_mxfp8_weights_size gives the bytes of the buffer that holds the
+ * pre-quantized weights; moe_quantize_weights_mxfp8 fills it from the bf16
+ * weights (once per weight update).  The buffer holds, in order, each
+ * 256-byte aligned: W_gate and W_up as [E*I, d] along d, W_down as [E*d, I]
+ * along I, W_down^T per expert as [E*I, d] along d, and [W_gate; W_up]^T per
+ * expert as [E*d, 2I] along 2I, each followed by its scales: for R rows and
+ * K columns, R/128 x K/128 blocks of 512 bytes (block (q, g) at offset
+ * (g * R/128 + q) * 512; inside it row r, 32-column block j at
+ * 16*(r%32) + 4*(r/32) + j). */
+moe_status moe_mxfp8_weights_size(const moe_config* cfg, size_t* bytes);
+moe_status moe_quantize_weights_mxfp8(const moe_config* cfg, const moe_weights* w, void* mx, void* stream);
 
 /* Router projection, softmax + top-k and the expert schedule (blog sections
  * "Overlapping computation and communication in MoE" and "Scheduling").

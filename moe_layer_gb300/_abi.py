@@ -18,7 +18,8 @@ MOE_OK = 0
 MOE_BF16 = 0
 MOE_MXFP8 = 1
 
-EXPORTED = ["moe_workspace_size", "moe_route_topk", "moe_route_topk_noalloc", "moe_forward",
+EXPORTED = ["moe_workspace_size", "moe_mxfp8_weights_size", "moe_quantize_weights_mxfp8",
+            "moe_route_topk", "moe_route_topk_noalloc", "moe_forward",
             "moe_backward", "moe_read_device_status", "moe_profile_enable", "moe_profile_report",
             "moe_status_string"]
 
@@ -62,6 +63,8 @@ def load():
     cfgp = ctypes.POINTER(MoeConfig)
     sz = ctypes.POINTER(ctypes.c_size_t)
     lib.moe_workspace_size.argtypes = [cfgp, sz, sz, sz]
+    lib.moe_mxfp8_weights_size.argtypes = [cfgp, sz]
+    lib.moe_quantize_weights_mxfp8.argtypes = [cfgp, ctypes.POINTER(MoeWeights), P, P]
     lib.moe_route_topk.argtypes = [cfgp] + [P] * 13
     lib.moe_route_topk_noalloc.argtypes = [cfgp] + [P] * 12
     lib.moe_forward.argtypes = [cfgp, P, ctypes.POINTER(MoeWeights), P, P, P, P]
@@ -118,6 +121,17 @@ def moe_workspace_size(cfg: MoeConfig):
     _check(load().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(a), ctypes.byref(b),
                                      ctypes.byref(c)), "moe_workspace_size")
     return a.value, b.value, c.value
+
+
+def moe_mxfp8_weights_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t()
+    _check(load().moe_mxfp8_weights_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_mxfp8_weights_size")
+    return n.value
+
+
+def moe_quantize_weights_mxfp8(cfg, weights: MoeWeights, mx, stream=None):
+    _check(load().moe_quantize_weights_mxfp8(ctypes.byref(cfg), ctypes.byref(weights), _ptr(mx),
+                                             _stream(stream)), "moe_quantize_weights_mxfp8")
 
 
 def moe_route_topk(cfg, x, W_router, router_bias, logits_in, logits_out, topk_idx, topk_w,

@@ -46,14 +46,14 @@ enum ProfLabel : int {
   PL_DOWN_ROUTED, PL_DOWN_SHARED, PL_COMBINE, PL_DGRAD_DOWN_ROUTED, PL_DGRAD_DOWN_SHARED,
   PL_ROUTER_GRAD, PL_DGRAD_GATEUP_ROUTED, PL_DGRAD_GATEUP_SHARED, PL_UNPERMUTE, PL_ROUTER_WGRAD,
   PL_WGRAD_DOWN, PL_WGRAD_GATE, PL_WGRAD_UP, PL_WGRAD_SHARED_DOWN, PL_WGRAD_SHARED_GATE,
-  PL_WGRAD_SHARED_UP, PL_PERMUTE_DY, PL_COUNT
+  PL_WGRAD_SHARED_UP, PL_PERMUTE_DY, PL_MX_WEIGHTS, PL_COUNT
 };
 static const char* const kProfNames[PL_COUNT] = {
     "router_gemm", "topk_count", "chunk_scan", "scatter", "permute_x", "gateup_shared", "gateup_routed",
     "down_routed", "down_shared", "combine", "dgrad_down_routed", "dgrad_down_shared",
     "router_grad", "dgrad_gateup_routed", "dgrad_gateup_shared", "unpermute", "router_wgrad",
     "wgrad_down", "wgrad_gate", "wgrad_up", "wgrad_shared_down", "wgrad_shared_gate",
-    "wgrad_shared_up", "permute_dy"};
+    "wgrad_shared_up", "permute_dy", "mx_quantize_weights"};
 
 struct ProfRecord {
   int label;
@@ -208,6 +208,30 @@ void carve_bwd(void* base, const Shape& s, BwdWs& w, size_t* bytes) {
   if (bytes) *bytes = c.off;
 }
 
+// MXFP8 copies of the routed expert weights (E4M3 codes + E8M0 scales in the
+// tcgen05.cp block order), one per GEMM orientation:
+//   wg/wu  [E*I, d]  W_gate, W_up quantized along d          (gate/up forward)
+//   wd     [E*d, I]  W_down quantized along I                (down forward)
+//   wdt    [E*I, d]  W_down^T per expert, along d            (dgrad of down)
+//   wgut   [E*d, 2I] [W_gate; W_up]^T per expert, along 2I   (dgrad of gate/up)
+struct MxWeights {
+  uint8_t *wg, *wg_sf, *wu, *wu_sf, *wd, *wd_sf, *wdt, *wdt_sf, *wgut, *wgut_sf;
+};
+void carve_mx(void* base, const Shape& s, MxWeights& m, size_t* bytes) {
+  Carver c(base);
+  m.wg = c.take<uint8_t>(s.E * s.I * s.d);
+  m.wg_sf = c.take<uint8_t>(mx_sf_bytes(s.E * s.I, s.d));
+  m.wu = c.take<uint8_t>(s.E * s.I * s.d);
+  m.wu_sf = c.take<uint8_t>(mx_sf_bytes(s.E * s.I, s.d));
+  m.wd = c.take<uint8_t>(s.E * s.d * s.I);
+  m.wd_sf = c.take<uint8_t>(mx_sf_bytes(s.E * s.d, s.I));
+  m.wdt = c.take<uint8_t>(s.E * s.I * s.d);
+  m.wdt_sf = c.take<uint8_t>(mx_sf_bytes(s.E * s.I, s.d));
+  m.wgut = c.take<uint8_t>(s.E * s.d * 2 * s.I);
+  m.wgut_sf = c.take<uint8_t>(mx_sf_bytes(s.E * s.d, 2 * s.I));
+  if (bytes) *bytes = c.off;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 moe_status check_config(const moe_config* cfg, Shape& s) {
@@ -215,7 +239,8 @@ moe_status check_config(const moe_config* cfg, Shape& s) {
   if (cfg->T < 0 || cfg->d <= 0 || cfg->I <= 0 || cfg->E <= 0 || cfg->top_k <= 0 ||
       cfg->n_shared < 0 || (cfg->n_shared && cfg->I_shared <= 0))
     return MOE_ERR_INVALID_ARG;
-  if (cfg->precision != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (cfg->precision != MOE_BF16 && cfg->precision != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
+  if (cfg->precision == MOE_MXFP8 && (cfg->d % 128 || cfg->I % 128)) return MOE_ERR_UNSUPPORTED;
   if (cfg->flags != 0) return MOE_ERR_UNSUPPORTED;
   if (cfg->E > kMaxExperts || cfg->top_k > kMaxTopK || cfg->top_k > cfg->E) return MOE_ERR_UNSUPPORTED;
   if (cfg->n_shared > 1) return MOE_ERR_UNSUPPORTED;
@@ -366,6 +391,39 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* fwd_ws, size_t* sav
     BwdWs w;
     carve_bwd(nullptr, s, w, bwd_ws);
   }
+  return MOE_OK;
+}
+
+moe_status moe_mxfp8_weights_size(const moe_config* cfg, size_t* bytes) {
+  Shape s;
+  MOE_TRY(check_config(cfg, s));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  if (cfg->precision != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
+  MxWeights m;
+  carve_mx(nullptr, s, m, bytes);
+  return MOE_OK;
+}
+
+moe_status moe_quantize_weights_mxfp8(const moe_config* cfg, const moe_weights* w, void* mx, void* stream) {
+  Shape s;
+  MOE_TRY(check_config(cfg, s));
+  if (cfg->precision != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
+  if (!w || !mx || !w->W_gate || !w->W_up || !w->W_down || !aligned16(mx)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MxWeights m;
+  carve_mx(mx, s, m, nullptr);
+  const auto* Wg = static_cast<const __nv_bfloat16*>(w->W_gate);
+  const auto* Wu = static_cast<const __nv_bfloat16*>(w->W_up);
+  const auto* Wd = static_cast<const __nv_bfloat16*>(w->W_down);
+  const int d = static_cast<int>(s.d), I = static_cast<int>(s.I), E = static_cast<int>(s.E);
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_rows(Wg, d, nullptr, nullptr, s.E * s.I, d, m.wg, m.wg_sf, nullptr, st));
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_rows(Wu, d, nullptr, nullptr, s.E * s.I, d, m.wu, m.wu_sf, nullptr, st));
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_rows(Wd, I, nullptr, nullptr, s.E * s.d, I, m.wd, m.wd_sf, nullptr, st));
+  // W_down[e] is [d, I]: its transpose [I, d] quantized along d
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wd, I, s.d * s.I, d, I, E, m.wdt, d, I, 0, m.wdt_sf, s.E * s.I, st));
+  // W_gate[e], W_up[e] are [I, d]: [W_gate; W_up]^T is [d, 2I], quantized along 2I
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wg, d, s.I * s.d, I, d, E, m.wgut, 2 * s.I, d, 0, m.wgut_sf, s.E * s.d, st));
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wu, d, s.I * s.d, I, d, E, m.wgut, 2 * s.I, d, I, m.wgut_sf, s.E * s.d, st));
   return MOE_OK;
 }
 

@@ -54,6 +54,18 @@ cudaError_t launch_unpermute(const __nv_bfloat16* dxp, const __nv_bfloat16* dxs,
                              const float* dl_tk, const __nv_bfloat16* W_router, int T, int d,
                              int k, __nv_bfloat16* dx, cudaStream_t st);
 
+// ---- MXFP8 quantization (mxfp8.cu)
+cudaError_t launch_mx_rows(const __nv_bfloat16* src, long long src_ld, const int32_t* idx,
+                           const int32_t* total_rows, int64_t R, int K, uint8_t* dst, uint8_t* sf,
+                           __nv_bfloat16* dst_bf16, cudaStream_t st);
+cudaError_t launch_mx_cols(const __nv_bfloat16* src, long long src_ld, long long src_bstride, int rows,
+                           int cols, int batch, uint8_t* dst, long long dst_ld, long long dst_brows,
+                           int k_off, uint8_t* sf, long long dst_rows_total, cudaStream_t st);
+// Bytes of the scale array of an MXFP8 operand with `rows` rows and K columns.
+inline size_t mx_sf_bytes(int64_t rows, int64_t K) {
+  return static_cast<size_t>(((rows + 127) / 128) * (K / 128) * 512);
+}
+
 // ---- tensor-core GEMM instantiations (gemm_fwd.cu, gemm_bwd.cu)
 enum GemmKind : int {
   GK_ROUTER = 0,     // x rows . W_router^T, fp32 + bias

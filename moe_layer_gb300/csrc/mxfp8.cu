@@ -1,0 +1,207 @@
+// MXFP8 quantization kernels (E4M3 elements, one E8M0 scale per 32 elements
+// along the reduction axis of the GEMM the operand feeds).  The MX rule: the
+// block scale is X = 2^(floor(log2(amax)) - 8) (8 = largest E4M3 exponent),
+// stored as the biased exponent (bias 127); elements are v / X rounded to the
+// nearest E4M3 value with saturation at +-448; an all-zero block gets scale
+// code 0.  (Mixture-of-Kittens blog post, section "MXFP8 support": weights are
+// pre-quantized, activation quantization is fused into the data movement.)
+//
+// Scale layout ("tcgen05.cp 32x128b" order): for an operand with R rows and K
+// columns, the scales of rows [128 q, 128 q + 128) and columns
+// [128 g, 128 g + 128) form one 512-byte block at offset (g * R/128 + q) * 512;
+// inside it the byte of row r (0..127) and 32-column block j (0..3) sits at
+// 16 * (r % 32) + 4 * (r / 32) + j.  The GEMM copies one such block straight
+// into tensor memory per operand tile and stage.
+#include <cuda_fp8.h>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+// floor(log2(a)) for a > 0 (fp32, normal or subnormal).
+__device__ __forceinline__ int floor_log2(float a) {
+  const uint32_t b = __float_as_uint(a);
+  const int e = static_cast<int>((b >> 23) & 0xFF);
+  if (e != 0) return e - 127;
+  const uint32_t m = b & 0x7FFFFFu;  // subnormal: a = m * 2^-149
+  return (31 - __clz(static_cast<int>(m))) - 149;
+}
+
+// Block scale exponent (unbiased) and its E8M0 code for a block maximum.
+__device__ __forceinline__ int mx_scale_exp(float amax) {
+  if (!(amax > 0.f)) return -127;
+  int e = floor_log2(amax) - 8;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+__device__ __forceinline__ uint8_t to_e4m3(float v) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Quantizes 32 values with scale 2^e into 32 E4M3 bytes (two 16-byte words).
+__device__ __forceinline__ void quant32(const float* v, int e, uint4& lo, uint4& hi) {
+  const float inv = ldexpf(1.0f, -e);  // exact power of two
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    w[i] = static_cast<uint32_t>(to_e4m3(v[4 * i] * inv)) |
+           (static_cast<uint32_t>(to_e4m3(v[4 * i + 1] * inv)) << 8) |
+           (static_cast<uint32_t>(to_e4m3(v[4 * i + 2] * inv)) << 16) |
+           (static_cast<uint32_t>(to_e4m3(v[4 * i + 3] * inv)) << 24);
+  }
+  lo = make_uint4(w[0], w[1], w[2], w[3]);
+  hi = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+__device__ __forceinline__ size_t sf_word_offset(int64_t row, int64_t kgroup, int64_t rblocks) {
+  return static_cast<size_t>((kgroup * rblocks + row / 128) * 512 + 16 * (row % 32) +
+                             4 * ((row % 128) / 32));
+}
+
+// Row-wise quantization: dst row r = src row idx[r] (or row r when idx is
+// null; a negative index gives a zero row), blocks of 32 along the row.
+// Optionally also writes the (gathered) bf16 row to dst_bf16.  One group of
+// four threads per (row, 128-column group).
+constexpr int kQThreads = 256;
+__global__ void __launch_bounds__(kQThreads)
+    mx_rows_kernel(const __nv_bfloat16* __restrict__ src, long long src_ld, const int32_t* __restrict__ idx,
+                   const int32_t* __restrict__ total_rows, int64_t R, int K,
+                   uint8_t* __restrict__ dst, uint8_t* __restrict__ sf, __nv_bfloat16* __restrict__ dst_bf16) {
+  const int64_t ng = K / 128;
+  const int64_t units = R * ng;
+  const int64_t rows_used = total_rows ? static_cast<int64_t>(__ldg(total_rows)) : R;
+  for (int64_t u = (static_cast<int64_t>(blockIdx.x) * kQThreads + threadIdx.x) / 4; u < units;
+       u += static_cast<int64_t>(gridDim.x) * kQThreads / 4) {
+    const int64_t r = u / ng, g = u - r * ng;
+    if (r >= rows_used) continue;  // rows past the used total are never read
+    const int j = threadIdx.x & 3;
+    const int col = static_cast<int>(g * 128 + 32 * j);
+    float v[32];
+    bool live = true;
+    int64_t srow = r;
+    if (idx && live) {
+      const int t = __ldg(idx + r);
+      live = t >= 0;
+      srow = t;
+    }
+    if (live) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src + srow * src_ld + col);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = __ldg(s4 + q);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[8 * q + 2 * i] = bf16lo(ws[i]);
+          v[8 * q + 2 * i + 1] = bf16hi(ws[i]);
+        }
+        if (dst_bf16) reinterpret_cast<uint4*>(dst_bf16 + r * static_cast<int64_t>(K) + col)[q] = w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      if (dst_bf16) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          reinterpret_cast<uint4*>(dst_bf16 + r * static_cast<int64_t>(K) + col)[q] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int e = mx_scale_exp(amax);
+    uint4 lo, hi;
+    quant32(v, e, lo, hi);
+    uint4* d4 = reinterpret_cast<uint4*>(dst + r * static_cast<int64_t>(K) + col);
+    d4[0] = lo;
+    d4[1] = hi;
+    // the four scale codes of this (row, 128-column group) form one word; only
+    // the group's four lanes take part (other groups of the warp may have left
+    // the loop)
+    const unsigned gmask = 0xFu << (threadIdx.x & 28u);
+    uint32_t code = static_cast<uint32_t>(e + 127) << (8 * j);
+    code |= __shfl_xor_sync(gmask, code, 1);
+    code |= __shfl_xor_sync(gmask, code, 2);
+    if (j == 0) *reinterpret_cast<uint32_t*>(sf + sf_word_offset(r, g, R / 128)) = code;
+  }
+}
+
+// Transposing quantization: src is [rows, cols] (row pitch src_ld) and feeds
+// a GEMM whose reduction axis is `rows`.  Writes dst[c, k_off + r] (row pitch
+// dst_ld, K-major for the GEMM) with blocks of 32 along r.  blockIdx.z walks a
+// batch of such matrices (per expert): src += z * src_bstride, dst row offset
+// += z * dst_brows.  Tile: 128 rows x 64 columns per block.
+__global__ void __launch_bounds__(kQThreads)
+    mx_cols_kernel(const __nv_bfloat16* __restrict__ src, long long src_ld, long long src_bstride, int rows,
+                   int cols, uint8_t* __restrict__ dst, long long dst_ld, long long dst_brows, int k_off,
+                   uint8_t* __restrict__ sf, long long dst_rows_total) {
+  __shared__ float tile[128][65];
+  const int r0 = blockIdx.y * 128, c0 = blockIdx.x * 64;
+  const __nv_bfloat16* s = src + static_cast<long long>(blockIdx.z) * src_bstride;
+  // coalesced load: each warp reads rows, 64 columns = 128 bytes per row
+  for (int i = threadIdx.x; i < 128 * 32; i += kQThreads) {
+    const int r = i / 32, cp = (i % 32) * 2;
+    float a = 0.f, b = 0.f;
+    if (r0 + r < rows && c0 + cp < cols) {
+      const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(s + static_cast<long long>(r0 + r) * src_ld + c0 + cp));
+      a = bf16lo(w);
+      b = bf16hi(w);
+    }
+    tile[r][cp] = a;
+    tile[r][cp + 1] = b;
+  }
+  __syncthreads();
+  const int c = threadIdx.x >> 2, j = threadIdx.x & 3;
+  float v[32];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = tile[32 * j + i][c];
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+  const int e = mx_scale_exp(amax);
+  uint4 lo, hi;
+  quant32(v, e, lo, hi);
+  if (c0 + c < cols) {
+    const long long drow = static_cast<long long>(blockIdx.z) * dst_brows + c0 + c;
+    uint4* d4 = reinterpret_cast<uint4*>(dst + drow * dst_ld + k_off + r0 + 32 * j);
+    d4[0] = lo;
+    d4[1] = hi;
+  }
+  uint32_t code = static_cast<uint32_t>(e + 127) << (8 * j);
+  code |= __shfl_xor_sync(0xffffffffu, code, 1);
+  code |= __shfl_xor_sync(0xffffffffu, code, 2);
+  if (j == 0 && c0 + c < cols) {
+    const long long drow = static_cast<long long>(blockIdx.z) * dst_brows + c0 + c;
+    *reinterpret_cast<uint32_t*>(sf + sf_word_offset(drow, (k_off + r0) / 128, dst_rows_total / 128)) = code;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_mx_rows(const __nv_bfloat16* src, long long src_ld, const int32_t* idx,
+                           const int32_t* total_rows, int64_t R, int K, uint8_t* dst, uint8_t* sf,
+                           __nv_bfloat16* dst_bf16, cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  const int64_t units = R * (K / 128);
+  int64_t blocks = (units * 4 + kQThreads - 1) / kQThreads;
+  if (blocks > 65535LL * 16) blocks = 65535LL * 16;
+  mx_rows_kernel<<<static_cast<unsigned>(blocks), kQThreads, 0, st>>>(src, src_ld, idx, total_rows, R, K,
+                                                                      dst, sf, dst_bf16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_cols(const __nv_bfloat16* src, long long src_ld, long long src_bstride, int rows,
+                           int cols, int batch, uint8_t* dst, long long dst_ld, long long dst_brows,
+                           int k_off, uint8_t* sf, long long dst_rows_total, cudaStream_t st) {
+  if (rows <= 0 || cols <= 0 || batch <= 0) return cudaSuccess;
+  dim3 grid((cols + 63) / 64, (rows + 127) / 128, batch);
+  mx_cols_kernel<<<grid, kQThreads, 0, st>>>(src, src_ld, src_bstride, rows, cols, dst, dst_ld, dst_brows,
+                                             k_off, sf, dst_rows_total);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

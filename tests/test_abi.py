@@ -62,10 +62,13 @@ def test_invalid_configs_rejected(lib, cfg, code):
     assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(a), None, None) == code
 
 
-def test_mxfp8_precision_reported_unsupported(lib):
-    c = _abi.make_config(512, 256, 128, 8, 2, precision=_abi.MOE_MXFP8)
+def test_mxfp8_needs_dims_multiple_of_128(lib):
     a = ctypes.c_size_t()
-    assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(a), None, None) == 2
+    bad = _abi.make_config(512, 256, 192, 8, 2, precision=_abi.MOE_MXFP8)
+    assert lib.moe_workspace_size(ctypes.byref(bad), ctypes.byref(a), None, None) == 2
+    good = _abi.make_config(512, 256, 128, 8, 2, precision=_abi.MOE_MXFP8)
+    assert lib.moe_workspace_size(ctypes.byref(good), ctypes.byref(a), None, None) == 0
+    assert _abi.moe_mxfp8_weights_size(good) >= 3 * 8 * 128 * 256 * 2  # five fp8 weight copies
 
 
 def test_null_arguments_rejected_before_launch(lib):
