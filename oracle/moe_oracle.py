@@ -44,6 +44,7 @@ __all__ = [
     "router_logits", "topk_route", "expert_schedule", "silu", "swiglu",
     "moe_forward", "moe_backward", "expert_forward", "expert_backward",
     "e4m3_decode", "e4m3_quantize", "mx_quantize", "mx_dequantize", "mx_round", "E4M3_TABLE",
+    "bf16_round",
 ]
 
 
@@ -238,6 +239,18 @@ def mx_round(v, axis=-1):
     return mx_dequantize(*mx_quantize(v, axis), axis=axis)
 
 
+def bf16_round(v):
+    """v as a bfloat16 value (float64 result): rounded to float32 first, then to
+    the nearest bfloat16 (8-bit significand), ties to the even significand --
+    the value a float32 computation leaves after a bfloat16 store.  Used only
+    where an MXFP8 quantization decision is taken on a stored bf16 tensor
+    (reading R12)."""
+    f = np.ascontiguousarray(np.asarray(v, np.float64).astype(np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 # ---------------------------------------------------------------- forward
 def moe_forward(x, w_router, w_gate, w_up, w_down, top_k, router_bias=None,
                 ws_gate=None, ws_up=None, ws_down=None, logits=None, mxfp8=False):
@@ -312,12 +325,17 @@ def expert_backward(x_rows, dy_rows, g, a, b, h, w_gate_e, w_up_e, w_down_e, mxf
     [da | db] and [W_gate; W_up] along 2I for dx; the token axis (blocks of 32
     rows of this expert, zero-padded) for the three weight gradients.  dg uses
     the unquantized h and dh [Blog, "MXFP8 support", "Router weight gradient
-    computation"].
+    computation"].  Each quantization decision is taken on the value the
+    layer holds at that point (reading R12): a and b as saved in bf16 (h is
+    recomputed from them); da and db unrounded for the dx operand; da, db and
+    g*h after their bf16 store for the weight-gradient operands.
     """
     x_rows, dy_rows = _f64(x_rows), _f64(dy_rows)
     wg, wu, wd = _f64(w_gate_e), _f64(w_up_e), _f64(w_down_e)
     g = _f64(g)[:, None]
     if mxfp8:
+        a, b = bf16_round(a), bf16_round(b)
+        h = swiglu(a, b)
         dh = mx_round(dy_rows, axis=-1) @ mx_round(wd, axis=0)
     else:
         dh = dy_rows @ wd
@@ -330,7 +348,8 @@ def expert_backward(x_rows, dy_rows, g, a, b, h, w_gate_e, w_up_e, w_down_e, mxf
     dadb = mx_round(np.concatenate([da, db], axis=1), axis=-1)
     wgu = mx_round(np.concatenate([wg, wu], axis=0), axis=0)
     xr = _mx_rows(x_rows)
-    return (_mx_rows(da).T @ xr, _mx_rows(db).T @ xr, _mx_rows(dy_rows).T @ _mx_rows(hg), dg,
+    da_s, db_s, hg_s = bf16_round(da), bf16_round(db), bf16_round(hg)
+    return (_mx_rows(da_s).T @ xr, _mx_rows(db_s).T @ xr, _mx_rows(dy_rows).T @ _mx_rows(hg_s), dg,
             dadb @ wgu)
 
 

@@ -354,3 +354,44 @@ def test_mxfp8_layer_stays_near_full_precision():
     for key in ["dx", "dW_gate", "dW_up", "dW_down", "dW_router"]:
         r = np.abs(bq[key] - b[key]).max() / np.abs(b[key]).max()
         assert 0 < r < 0.15, key
+
+
+def test_bf16_round_matches_torch_bfloat16_cast():
+    """float32 values round to bfloat16 as torch's cast does (nearest, ties to
+    the even significand), including exact ties, signed zero, subnormals and
+    overflow to infinity."""
+    rng = _rng(16)
+    v32 = np.concatenate([rng.normal(size=3000) * np.exp(rng.normal(size=3000) * 6),
+                          [0.0, -0.0, 1e-40, -3e-39, 3.4e38, -3.4e38, 1.0, 2.0 ** -126]]).astype(np.float32)
+    # exact ties: low 16 bits 0x8000, even and odd upper halves
+    ties = (np.array([0x3F808000, 0x3F818000, 0xC0A08000, 0x00018000], np.uint32)).view(np.float32)
+    v32 = np.concatenate([v32, ties])
+    ref = torch.from_numpy(v32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.bf16_round(v32.astype(np.float64)), ref)
+    assert O.bf16_round(np.array([1.0 + 2.0 ** -8]))[0] == 1.0        # tie to even (down)
+    assert O.bf16_round(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 1.0 + 2.0 ** -6  # tie to even (up)
+
+
+def test_mxfp8_backward_takes_decisions_on_stored_values():
+    """MXFP8 backward: a and b enter as their stored bf16 values, so moving
+    them by less than half a bf16 step changes no output bit, and h is
+    recomputed from them (the h argument does not matter)."""
+    rng = _rng(17)
+    n, d, I = 40, 64, 32
+    x = rng.normal(size=(n, d))
+    dy = rng.normal(size=(n, d))
+    g = rng.uniform(0.1, 1.0, size=n)
+    a0 = O.bf16_round(rng.normal(size=(n, I)))
+    b0 = O.bf16_round(rng.normal(size=(n, I)))
+    a1 = a0 * (1 + 1e-5 * rng.uniform(-1, 1, size=a0.shape))
+    b1 = b0 * (1 + 1e-5 * rng.uniform(-1, 1, size=b0.shape))
+    assert (a1 != a0).any()
+    wg, wu, wd = rng.normal(size=(I, d)), rng.normal(size=(I, d)), rng.normal(size=(d, I))
+    r0 = O.expert_backward(x, dy, g, a0, b0, O.swiglu(a0, b0), wg, wu, wd, mxfp8=True)
+    r1 = O.expert_backward(x, dy, g, a1, b1, O.swiglu(a0, b0) + 1.0, wg, wu, wd, mxfp8=True)
+    for u, v in zip(r0, r1):
+        np.testing.assert_array_equal(u, v)
+    # without MXFP8 the same perturbation is visible (the rounding is MXFP8-only)
+    f0 = O.expert_backward(x, dy, g, a0, b0, O.swiglu(a0, b0), wg, wu, wd)
+    f1 = O.expert_backward(x, dy, g, a1, b1, O.swiglu(a1, b1), wg, wu, wd)
+    assert not np.array_equal(f0[4], f1[4])
