@@ -79,6 +79,8 @@ typedef struct {
   const void* Ws_gate;      /* [I_s, d] bf16 (n_shared == 1) */
   const void* Ws_up;        /* [I_s, d] bf16 */
   const void* Ws_down;      /* [d, I_s] bf16 */
+  const void* mxfp8;        /* MOE_MXFP8: the buffer moe_quantize_weights_mxfp8 filled from
+                               W_gate, W_up and W_down (NULL in bf16 mode) */
 } moe_weights;
 
 typedef struct {
@@ -113,7 +115,10 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* fwd_ws, size_t* sav
  * expert as [E*d, 2I] along 2I, each followed by its scales: for R rows and
  * K columns, R/128 x K/128 blocks of 512 bytes (block (q, g) at offset
  * (g * R/128 + q) * 512; inside it row r, 32-column block j at
- * 16*(r%32) + 4*(r/32) + j). */
+ * 16*(r%32) + 4*(r/32) + j) and one spare 512-byte block.  moe_forward and
+ * moe_backward read it through moe_weights.mxfp8 (the bf16 W_gate, W_up and
+ * W_down must still be given: the shared expert and the router stay bf16,
+ * and the saved state is laid out as in bf16 mode). */
 moe_status moe_mxfp8_weights_size(const moe_config* cfg, size_t* bytes);
 moe_status moe_quantize_weights_mxfp8(const moe_config* cfg, const moe_weights* w, void* mx, void* stream);
 

@@ -33,7 +33,8 @@ class MoeConfig(ctypes.Structure):
 class MoeWeights(ctypes.Structure):
     _fields_ = [("W_router", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
                 ("W_gate", ctypes.c_void_p), ("W_up", ctypes.c_void_p), ("W_down", ctypes.c_void_p),
-                ("Ws_gate", ctypes.c_void_p), ("Ws_up", ctypes.c_void_p), ("Ws_down", ctypes.c_void_p)]
+                ("Ws_gate", ctypes.c_void_p), ("Ws_up", ctypes.c_void_p), ("Ws_down", ctypes.c_void_p),
+                ("mxfp8", ctypes.c_void_p)]
 
 
 class MoeGrads(ctypes.Structure):
@@ -153,9 +154,9 @@ def moe_route_topk_noalloc(cfg, x, W_router, router_bias, logits_in, logits_out,
 
 
 def make_weights(W_router, W_gate, W_up, W_down, router_bias=None, Ws_gate=None, Ws_up=None,
-                 Ws_down=None) -> MoeWeights:
+                 Ws_down=None, mxfp8=None) -> MoeWeights:
     return MoeWeights(_ptr(W_router), _ptr(router_bias), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
-                      _ptr(Ws_gate), _ptr(Ws_up), _ptr(Ws_down))
+                      _ptr(Ws_gate), _ptr(Ws_up), _ptr(Ws_down), _ptr(mxfp8))
 
 
 def make_grads(dW_router, dW_gate, dW_up, dW_down, dWs_gate=None, dWs_up=None, dWs_down=None,

@@ -35,6 +35,7 @@ int device_sm_count() {
 
 cudaError_t launch_gemm(GemmKind kind, const GemmParams& p, int grid, cudaStream_t st) {
   if (kind == GK_ROUTER || kind == GK_GATEUP || kind == GK_DOWN) return launch_gemm_fwd(kind, p, grid, st);
+  if (kind >= GK_MX_GATEUP) return launch_gemm_mx(kind, p, grid, st);
   return launch_gemm_bwd(kind, p, grid, st);
 }
 
@@ -46,14 +47,16 @@ enum ProfLabel : int {
   PL_DOWN_ROUTED, PL_DOWN_SHARED, PL_COMBINE, PL_DGRAD_DOWN_ROUTED, PL_DGRAD_DOWN_SHARED,
   PL_ROUTER_GRAD, PL_DGRAD_GATEUP_ROUTED, PL_DGRAD_GATEUP_SHARED, PL_UNPERMUTE, PL_ROUTER_WGRAD,
   PL_WGRAD_DOWN, PL_WGRAD_GATE, PL_WGRAD_UP, PL_WGRAD_SHARED_DOWN, PL_WGRAD_SHARED_GATE,
-  PL_WGRAD_SHARED_UP, PL_PERMUTE_DY, PL_MX_WEIGHTS, PL_COUNT
+  PL_WGRAD_SHARED_UP, PL_PERMUTE_DY, PL_MX_WEIGHTS, PL_MX_QUANT_X, PL_MX_QUANT_DY, PL_MX_TRANSPOSE,
+  PL_COUNT
 };
 static const char* const kProfNames[PL_COUNT] = {
     "router_gemm", "topk_count", "chunk_scan", "scatter", "permute_x", "gateup_shared", "gateup_routed",
     "down_routed", "down_shared", "combine", "dgrad_down_routed", "dgrad_down_shared",
     "router_grad", "dgrad_gateup_routed", "dgrad_gateup_shared", "unpermute", "router_wgrad",
     "wgrad_down", "wgrad_gate", "wgrad_up", "wgrad_shared_down", "wgrad_shared_gate",
-    "wgrad_shared_up", "permute_dy", "mx_quantize_weights"};
+    "wgrad_shared_up", "permute_dy", "mx_quantize_weights", "mx_permute_quant_x", "mx_permute_quant_dy",
+    "mx_transpose_quant"};
 
 struct ProfRecord {
   int label;
@@ -91,6 +94,8 @@ constexpr size_t kAlign = 256;
 
 struct Shape {
   int64_t T, d, I, E, k, S, Is, R, Rp, nchunk, nparts;
+  int64_t ra;  // row alignment of the expert groups
+  bool mx;     // MXFP8 routed experts
 };
 
 // Carves 256-byte aligned sub-buffers from a base pointer (or only sizes them
@@ -163,6 +168,9 @@ struct FwdWs {
   __nv_bfloat16* hs;   // [T, Is]
   __nv_bfloat16* o;    // [Rp, d]
   __nv_bfloat16* ys;   // [T, d]
+  // MXFP8: x rows and h rows as E4M3 codes + scales (h is not kept in bf16)
+  uint8_t *xq, *xq_sf;  // [Rp, d]
+  uint8_t *hq, *hq_sf;  // [Rp, I]
 };
 void carve_fwd(void* base, const Shape& s, FwdWs& w, size_t* bytes) {
   Carver c(base);
@@ -172,10 +180,15 @@ void carve_fwd(void* base, const Shape& s, FwdWs& w, size_t* bytes) {
   w.chunk_base = c.take<int32_t>(s.nchunk * s.E);
   carve_routing(c, s, w.rt);
   w.xp = c.take<__nv_bfloat16>(s.Rp * s.d);
-  w.h = c.take<__nv_bfloat16>(s.Rp * s.I);
+  w.h = c.take<__nv_bfloat16>(s.mx ? 0 : s.Rp * s.I);
   w.hs = c.take<__nv_bfloat16>(s.S ? s.T * s.Is : 0);
   w.o = c.take<__nv_bfloat16>(s.Rp * s.d);
   w.ys = c.take<__nv_bfloat16>(s.S ? s.T * s.d : 0);
+  const int64_t m = s.mx ? 1 : 0;
+  w.xq = c.take<uint8_t>(m * s.Rp * s.d);
+  w.xq_sf = c.take<uint8_t>(m * mx_sf_alloc(s.Rp, s.d));
+  w.hq = c.take<uint8_t>(m * s.Rp * s.I);
+  w.hq_sf = c.take<uint8_t>(m * mx_sf_alloc(s.Rp, s.I));
   if (bytes) *bytes = c.off;
 }
 
@@ -191,6 +204,15 @@ struct BwdWs {
   float* dl_row;         // [Rp]
   __nv_bfloat16* dxp;    // [Rp, d]
   __nv_bfloat16* dxs;    // [T, d]
+  // MXFP8: E4M3 codes + scales of the GEMM operands.  Row operands along
+  // their columns; the *_t ones are transposes (token rows become K, blocks
+  // of 32 tokens) for the weight gradients.
+  uint8_t *dyq, *dyq_sf;      // [Rp, d]
+  uint8_t *dadbq, *dadbq_sf;  // [Rp, 2I]
+  uint8_t *dy_t, *dy_t_sf;    // [d, Rp]
+  uint8_t *hg_t, *hg_t_sf;    // [I, Rp]
+  uint8_t *dadb_t, *dadb_t_sf;  // [2I, Rp]
+  uint8_t *x_t, *x_t_sf;      // [d, Rp]
 };
 void carve_bwd(void* base, const Shape& s, BwdWs& w, size_t* bytes) {
   Carver c(base);
@@ -205,6 +227,19 @@ void carve_bwd(void* base, const Shape& s, BwdWs& w, size_t* bytes) {
   w.dl_row = c.take<float>(s.Rp);
   w.dxp = c.take<__nv_bfloat16>(s.Rp * s.d);
   w.dxs = c.take<__nv_bfloat16>(s.S ? s.T * s.d : 0);
+  const int64_t m = s.mx ? 1 : 0;
+  w.dyq = c.take<uint8_t>(m * s.Rp * s.d);
+  w.dyq_sf = c.take<uint8_t>(m * mx_sf_alloc(s.Rp, s.d));
+  w.dadbq = c.take<uint8_t>(m * s.Rp * 2 * s.I);
+  w.dadbq_sf = c.take<uint8_t>(m * mx_sf_alloc(s.Rp, 2 * s.I));
+  w.dy_t = c.take<uint8_t>(m * s.d * s.Rp);
+  w.dy_t_sf = c.take<uint8_t>(m * mx_sf_alloc(s.d, s.Rp));
+  w.hg_t = c.take<uint8_t>(m * s.I * s.Rp);
+  w.hg_t_sf = c.take<uint8_t>(m * mx_sf_alloc(s.I, s.Rp));
+  w.dadb_t = c.take<uint8_t>(m * 2 * s.I * s.Rp);
+  w.dadb_t_sf = c.take<uint8_t>(m * mx_sf_alloc(2 * s.I, s.Rp));
+  w.x_t = c.take<uint8_t>(m * s.d * s.Rp);
+  w.x_t_sf = c.take<uint8_t>(m * mx_sf_alloc(s.d, s.Rp));
   if (bytes) *bytes = c.off;
 }
 
@@ -220,15 +255,15 @@ struct MxWeights {
 void carve_mx(void* base, const Shape& s, MxWeights& m, size_t* bytes) {
   Carver c(base);
   m.wg = c.take<uint8_t>(s.E * s.I * s.d);
-  m.wg_sf = c.take<uint8_t>(mx_sf_bytes(s.E * s.I, s.d));
+  m.wg_sf = c.take<uint8_t>(mx_sf_alloc(s.E * s.I, s.d));
   m.wu = c.take<uint8_t>(s.E * s.I * s.d);
-  m.wu_sf = c.take<uint8_t>(mx_sf_bytes(s.E * s.I, s.d));
+  m.wu_sf = c.take<uint8_t>(mx_sf_alloc(s.E * s.I, s.d));
   m.wd = c.take<uint8_t>(s.E * s.d * s.I);
-  m.wd_sf = c.take<uint8_t>(mx_sf_bytes(s.E * s.d, s.I));
+  m.wd_sf = c.take<uint8_t>(mx_sf_alloc(s.E * s.d, s.I));
   m.wdt = c.take<uint8_t>(s.E * s.I * s.d);
-  m.wdt_sf = c.take<uint8_t>(mx_sf_bytes(s.E * s.I, s.d));
+  m.wdt_sf = c.take<uint8_t>(mx_sf_alloc(s.E * s.I, s.d));
   m.wgut = c.take<uint8_t>(s.E * s.d * 2 * s.I);
-  m.wgut_sf = c.take<uint8_t>(mx_sf_bytes(s.E * s.d, 2 * s.I));
+  m.wgut_sf = c.take<uint8_t>(mx_sf_alloc(s.E * s.d, 2 * s.I));
   if (bytes) *bytes = c.off;
 }
 
@@ -253,7 +288,10 @@ moe_status check_config(const moe_config* cfg, Shape& s) {
   s.S = cfg->n_shared;
   s.Is = cfg->n_shared ? cfg->I_shared : 0;
   s.R = s.T * s.k;
-  s.Rp = s.R + s.E * (kRowAlign - 1);
+  s.mx = cfg->precision == MOE_MXFP8;
+  s.ra = s.mx ? kRowAlignMx : kRowAlign;
+  s.Rp = s.R + s.E * (s.ra - 1);
+  if (s.mx) s.Rp = (s.Rp + kRowAlignMx - 1) / kRowAlignMx * kRowAlignMx;  // whole scale blocks
   s.nchunk = (s.T + kChunkTokens - 1) / kChunkTokens;
   s.nparts = (s.I + kBN - 1) / kBN;
   const int64_t lim = (int64_t(1) << 31) - 1;
@@ -278,6 +316,14 @@ void zero_params(GemmParams& p) { memset(static_cast<void*>(&p), 0, sizeof(p)); 
 moe_status tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols, int box_rows) {
   if (!make_tmap_bf16(m, base, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
                       static_cast<uint64_t>(cols), box_cols, box_rows))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+// E4M3 operand [rows, cols] (K = cols), boxes of 128 columns x box_rows.
+moe_status qmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
+  if (!make_tmap_u8(m, base, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                    static_cast<uint32_t>(box_rows)))
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -349,7 +395,7 @@ moe_status run_routing(const Shape& s, const void* x, const void* W_router, cons
   MOE_LAUNCH(PL_CHUNK_SCAN, st, launch_chunk_scan(chunk_counts, static_cast<int>(s.nchunk), static_cast<int>(s.E),
                              chunk_base, rt.counts, st));
   MOE_LAUNCH(PL_SCATTER, st, launch_scatter(rt.topk_idx, rt.topk_w, static_cast<int>(s.T), static_cast<int>(s.E),
-                          static_cast<int>(s.k), chunk_base, rt.counts, rt.offsets, rt.row_start,
+                          static_cast<int>(s.k), static_cast<int>(s.ra), chunk_base, rt.counts, rt.offsets, rt.row_start,
                           rt.tile_start, rt.perm_token, rt.route_row, rt.perm_token_pad,
                           rt.route_row_pad, rt.perm_w_pad, st));
   return MOE_OK;
@@ -365,6 +411,122 @@ moe_status check_weights(const Shape& s, const moe_weights* w, bool need_router)
     const void* sh[] = {w->Ws_gate, w->Ws_up, w->Ws_down};
     for (const void* p : sh)
       if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  }
+  if (s.mx && (!w->mxfp8 || (reinterpret_cast<uintptr_t>(w->mxfp8) & 255u))) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// Sets the MXFP8 operand scales of a GEMM: A's scales with A's row count,
+// B's (one or two stacks) with B's row count.
+void set_mx_scales(GemmParams& p, const uint8_t* sfa, int64_t a_rows, const uint8_t* sfb0,
+                   const uint8_t* sfb1, int64_t b_rows) {
+  p.sfa = sfa;
+  p.sfa_rb = cdiv(a_rows, 128);
+  p.sfb0 = sfb0;
+  p.sfb1 = sfb1;
+  p.sfb_rb = cdiv(b_rows, 128);
+}
+
+// Routed experts of the forward in MXFP8 mode (blog section "MXFP8 support"):
+// x rows already quantized (w.xq); gate/up with the SwiGLU epilogue writing h
+// as E4M3 + scales; down projection on the quantized h, scaled by the router
+// weight of each row.
+moe_status forward_routed_mx(const Shape& s, const moe_weights* wts, const Routing& rt, const Saved* sv,
+                             const FwdWs& w, cudaStream_t st) {
+  MxWeights m;
+  carve_mx(const_cast<void*>(wts->mxfp8), s, m, nullptr);
+  const int d = static_cast<int>(s.d), I = static_cast<int>(s.I), E = static_cast<int>(s.E);
+  {
+    GemmParams p;
+    zero_params(p);
+    MOE_TRY(qmap(&p.tmA, w.xq, s.Rp, s.d, kBM));
+    MOE_TRY(qmap(&p.tmB0, m.wg, s.E * s.I, s.d, kBN / 2));
+    MOE_TRY(qmap(&p.tmB1, m.wu, s.E * s.I, s.d, kBN / 2));
+    set_mx_scales(p, w.xq_sf, s.Rp, m.wg_sf, m.wu_sf, s.E * s.I);
+    p.num_groups = E;
+    p.row_start = rt.row_start;
+    p.tile_start = rt.tile_start;
+    p.counts = rt.counts;
+    p.N = I;
+    p.K = d;
+    p.b_group_rows = I;
+    if (sv) {
+      MOE_TRY(omap2(&p.tmO0, &p.tmO0h, sv->ab, s.Rp, 2 * s.I));
+      p.store_ab = 1;
+    }
+    p.I = I;
+    p.qout = w.hq;
+    p.qld = s.I;
+    p.qsf = w.hq_sf;
+    p.q_rb = cdiv(s.Rp, 128);
+    p.status = w.status;
+    MOE_LAUNCH(PL_GATEUP_ROUTED, st, launch_gemm(GK_MX_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.I, kBN / 2)), st));
+  }
+  {
+    GemmParams p;
+    zero_params(p);
+    MOE_TRY(qmap(&p.tmA, w.hq, s.Rp, s.I, kBM));
+    MOE_TRY(qmap(&p.tmB0, m.wd, s.E * s.d, s.I, kBN));
+    set_mx_scales(p, w.hq_sf, s.Rp, m.wd_sf, nullptr, s.E * s.d);
+    p.num_groups = E;
+    p.row_start = rt.row_start;
+    p.tile_start = rt.tile_start;
+    p.counts = rt.counts;
+    p.N = d;
+    p.K = I;
+    p.b_group_rows = d;
+    MOE_TRY(omap2(&p.tmO0, &p.tmO0h, w.o, s.Rp, s.d));
+    p.row_scale = rt.perm_w_pad;
+    p.status = w.status;
+    MOE_LAUNCH(PL_DOWN_ROUTED, st, launch_gemm(GK_MX_DOWN, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
+  }
+  return MOE_OK;
+}
+
+// Weight gradients of the routed experts in MXFP8 mode.  Their reduction axis
+// is the token rows of each expert, so dy, g*h, [da | db] and x are first
+// transposed and quantized in blocks of 32 rows (expert groups start on
+// 128-row boundaries, so a block never mixes experts); then
+//   dW_down[e] = dy^T (g h),  dW_gate[e] = da^T x,  dW_up[e] = db^T x
+// run as K-major block-scaled GEMMs over [row_start[e], row_start[e+1]).
+moe_status wgrad_routed_mx(const Shape& s, const Routing& rt, const Saved& sv, const BwdWs& w,
+                           const moe_grads* g, cudaStream_t st) {
+  const int Rp = static_cast<int>(s.Rp), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
+  const int E = static_cast<int>(s.E);
+  const int32_t* used = rt.row_start + E;  // rows past the last group are never read
+  MOE_LAUNCH(PL_MX_TRANSPOSE, st, launch_mx_cols(w.dyp, d, 0, Rp, d, 1, w.dy_t, Rp, 0, 0, w.dy_t_sf, d, used, st));
+  MOE_LAUNCH(PL_MX_TRANSPOSE, st, launch_mx_cols(w.hg, I, 0, Rp, I, 1, w.hg_t, Rp, 0, 0, w.hg_t_sf, I, used, st));
+  MOE_LAUNCH(PL_MX_TRANSPOSE, st, launch_mx_cols(w.dadb, 2 * s.I, 0, Rp, 2 * I, 1, w.dadb_t, Rp, 0, 0, w.dadb_t_sf,
+                                                 2 * s.I, used, st));
+  MOE_LAUNCH(PL_MX_TRANSPOSE, st, launch_mx_cols(sv.xp, d, 0, Rp, d, 1, w.x_t, Rp, 0, 0, w.x_t_sf, d, used, st));
+  {
+    GemmParams p;  // dW_down[e] = dy_rows^T . (g h)
+    zero_params(p);
+    MOE_TRY(qmap(&p.tmA, w.dy_t, s.d, s.Rp, kBM));
+    MOE_TRY(qmap(&p.tmB0, w.hg_t, s.I, s.Rp, kBN));
+    set_mx_scales(p, w.dy_t_sf, s.d, w.hg_t_sf, nullptr, s.I);
+    p.num_groups = E;
+    p.row_start = rt.row_start;
+    p.M_out = d;
+    p.N = I;
+    MOE_TRY(omap3(&p.tmO0, g->dW_down, s.E, s.d, s.I));
+    p.status = w.status;
+    MOE_LAUNCH(PL_WGRAD_DOWN, st, launch_gemm(GK_MX_WGRAD, p, grid_for(s.E * cdiv(s.d, kBM) * cdiv(s.I, kBN)), st));
+  }
+  for (int half = 0; half < 2; ++half) {
+    GemmParams p;  // dW_gate[e] = da^T . x_rows ; dW_up[e] = db^T . x_rows
+    zero_params(p);
+    MOE_TRY(qmap(&p.tmA, w.dadb_t, 2 * s.I, s.Rp, kBM));
+    MOE_TRY(qmap(&p.tmB0, w.x_t, s.d, s.Rp, kBN));
+    set_mx_scales(p, w.dadb_t_sf, 2 * s.I, w.x_t_sf, nullptr, s.d);
+    p.num_groups = E;
+    p.row_start = rt.row_start;
+    p.M_out = I;
+    p.N = d;
+    p.a_col_off = half ? I : 0;
+    MOE_TRY(omap3(&p.tmO0, half ? g->dW_up : g->dW_gate, s.E, s.I, s.d));
+    p.status = w.status;
+    MOE_LAUNCH(half ? PL_WGRAD_UP : PL_WGRAD_GATE, st, launch_gemm(GK_MX_WGRAD, p, grid_for(s.E * cdiv(s.I, kBM) * cdiv(s.d, kBN)), st));
   }
   return MOE_OK;
 }
@@ -420,10 +582,10 @@ moe_status moe_quantize_weights_mxfp8(const moe_config* cfg, const moe_weights* 
   MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_rows(Wu, d, nullptr, nullptr, s.E * s.I, d, m.wu, m.wu_sf, nullptr, st));
   MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_rows(Wd, I, nullptr, nullptr, s.E * s.d, I, m.wd, m.wd_sf, nullptr, st));
   // W_down[e] is [d, I]: its transpose [I, d] quantized along d
-  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wd, I, s.d * s.I, d, I, E, m.wdt, d, I, 0, m.wdt_sf, s.E * s.I, st));
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wd, I, s.d * s.I, d, I, E, m.wdt, d, I, 0, m.wdt_sf, s.E * s.I, nullptr, st));
   // W_gate[e], W_up[e] are [I, d]: [W_gate; W_up]^T is [d, 2I], quantized along 2I
-  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wg, d, s.I * s.d, I, d, E, m.wgut, 2 * s.I, d, 0, m.wgut_sf, s.E * s.d, st));
-  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wu, d, s.I * s.d, I, d, E, m.wgut, 2 * s.I, d, I, m.wgut_sf, s.E * s.d, st));
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wg, d, s.I * s.d, I, d, E, m.wgut, 2 * s.I, d, 0, m.wgut_sf, s.E * s.d, nullptr, st));
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wu, d, s.I * s.d, I, d, E, m.wgut, 2 * s.I, d, I, m.wgut_sf, s.E * s.d, nullptr, st));
   return MOE_OK;
 }
 
@@ -475,10 +637,16 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
   const int T = static_cast<int>(s.T), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
   const int E = static_cast<int>(s.E);
 
-  // dispatch: x rows into expert-grouped order (zeros in padding rows)
+  // dispatch: x rows into expert-grouped order (zeros in padding rows); in
+  // MXFP8 mode quantized on the way, the bf16 copy kept only for training
   __nv_bfloat16* xp = saved ? sv.xp : w.xp;
-  MOE_LAUNCH(PL_PERMUTE_X, st, launch_permute_rows(static_cast<const __nv_bfloat16*>(x), rt.perm_token_pad,
-                                                  rt.row_start + E, static_cast<int>(s.Rp), d, xp, st));
+  if (s.mx)
+    MOE_LAUNCH(PL_MX_QUANT_X, st, launch_mx_rows(static_cast<const __nv_bfloat16*>(x), d, rt.perm_token_pad,
+                                                 rt.row_start + E, s.Rp, d, w.xq, w.xq_sf,
+                                                 saved ? sv.xp : nullptr, st));
+  else
+    MOE_LAUNCH(PL_PERMUTE_X, st, launch_permute_rows(static_cast<const __nv_bfloat16*>(x), rt.perm_token_pad,
+                                                    rt.row_start + E, static_cast<int>(s.Rp), d, xp, st));
   // shared expert gate/up + SwiGLU (dense rows of x)
   if (s.S) {
     GemmParams p;
@@ -501,6 +669,9 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.status = w.status;
     MOE_LAUNCH(PL_GATEUP_SHARED, st, launch_gemm(GK_GATEUP, p, grid_for(cdiv(s.T, kBM) * cdiv(s.Is, kBN / 2)), st));
   }
+  if (s.mx) {
+    MOE_TRY(forward_routed_mx(s, wts, rt, saved ? &sv : nullptr, w, st));
+  } else {
   // routed gate/up + SwiGLU over the expert-grouped rows
   {
     GemmParams p;
@@ -545,6 +716,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.status = w.status;
     MOE_LAUNCH(PL_DOWN_ROUTED, st, launch_gemm(GK_DOWN, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
   }
+  }
   // shared down projection
   if (s.S) {
     GemmParams p;
@@ -584,12 +756,48 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
   const int T = static_cast<int>(s.T), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
   const int E = static_cast<int>(s.E), k = static_cast<int>(s.k), Is = static_cast<int>(s.Is);
 
-  // dy rows into expert-grouped order (zeros in padding rows)
-  MOE_LAUNCH(PL_PERMUTE_DY, st, launch_permute_rows(static_cast<const __nv_bfloat16*>(dy), rt.perm_token_pad,
-                                                   rt.row_start + E, static_cast<int>(s.Rp), d, w.dyp, st));
+  MxWeights m;
+  if (s.mx) carve_mx(const_cast<void*>(wts->mxfp8), s, m, nullptr);
+  // dy rows into expert-grouped order (zeros in padding rows); in MXFP8 mode
+  // quantized on the way (the bf16 copy feeds the transposed quantization)
+  if (s.mx)
+    MOE_LAUNCH(PL_MX_QUANT_DY, st, launch_mx_rows(static_cast<const __nv_bfloat16*>(dy), d, rt.perm_token_pad,
+                                                  rt.row_start + E, s.Rp, d, w.dyq, w.dyq_sf, w.dyp, st));
+  else
+    MOE_LAUNCH(PL_PERMUTE_DY, st, launch_permute_rows(static_cast<const __nv_bfloat16*>(dy), rt.perm_token_pad,
+                                                     rt.row_start + E, static_cast<int>(s.Rp), d, w.dyp, st));
   // dgrad of the down projection with the fused SwiGLU backward and the
-  // router-weight gradient partials <h, dh> per n-tile
-  {
+  // router-weight gradient partials <h, dh> per n-tile; in MXFP8 mode the
+  // epilogue also quantizes [da | db] for the gate/up dgrad
+  if (s.mx) {
+    GemmParams p;
+    zero_params(p);
+    MOE_TRY(qmap(&p.tmA, w.dyq, s.Rp, s.d, kBM));
+    MOE_TRY(qmap(&p.tmB0, m.wdt, s.E * s.I, s.d, kBN));
+    set_mx_scales(p, w.dyq_sf, s.Rp, m.wdt_sf, nullptr, s.E * s.I);
+    p.num_groups = E;
+    p.row_start = rt.row_start;
+    p.counts = rt.counts;
+    p.N = I;
+    p.K = d;
+    p.b_group_rows = I;
+    p.out = w.dadb;
+    p.ldo = 2 * s.I;
+    p.out2 = w.hg;
+    p.ldo2 = s.I;
+    p.out3 = w.dg_part;
+    p.ldo3 = static_cast<int>(s.nparts);
+    p.ab = sv.ab;
+    p.I = I;
+    p.tile_start = rt.tile_start;
+    p.row_scale = rt.perm_w_pad;
+    p.qout = w.dadbq;
+    p.qld = 2 * s.I;
+    p.qsf = w.dadbq_sf;
+    p.q_rb = cdiv(s.Rp, 128);
+    p.status = w.status;
+    MOE_LAUNCH(PL_DGRAD_DOWN_ROUTED, st, launch_gemm(GK_MX_DGRAD_DOWN, p, grid_for(cdiv(s.Rp, kBM) * s.nparts), st));
+  } else {
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, w.dyp, s.Rp, s.d, 64, kBM));
@@ -633,7 +841,23 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
   MOE_LAUNCH(PL_ROUTER_GRAD, st, launch_router_grad(w.dg_part, static_cast<int>(s.nparts), rt.route_row_pad,
                                                     rt.topk_w, T, k, g->d_topk_w, w.dl_tk, w.dl_row, st));
   // dgrad of gate/up: dx_row = [da | db] . [W_gate ; W_up]
-  {
+  if (s.mx) {
+    GemmParams p;
+    zero_params(p);
+    MOE_TRY(qmap(&p.tmA, w.dadbq, s.Rp, 2 * s.I, kBM));
+    MOE_TRY(qmap(&p.tmB0, m.wgut, s.E * s.d, 2 * s.I, kBN));
+    set_mx_scales(p, w.dadbq_sf, s.Rp, m.wgut_sf, nullptr, s.E * s.d);
+    p.num_groups = E;
+    p.row_start = rt.row_start;
+    p.counts = rt.counts;
+    p.N = d;
+    p.K = 2 * I;
+    p.b_group_rows = d;
+    MOE_TRY(omap2(&p.tmO0, &p.tmO0h, w.dxp, s.Rp, s.d));
+    p.tile_start = rt.tile_start;
+    p.status = w.status;
+    MOE_LAUNCH(PL_DGRAD_GATEUP_ROUTED, st, launch_gemm(GK_MX_DGRAD_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
+  } else {
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, w.dadb, s.Rp, 2 * s.I, 64, kBM));
@@ -672,6 +896,9 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
   MOE_LAUNCH(PL_ROUTER_WGRAD, st, launch_router_wgrad(w.dl_row, rt.perm_token_pad, rt.row_start, rt.counts,
                                                       static_cast<const __nv_bfloat16*>(x), E, d, g->dW_router, st));
   // weight gradients, reduced over each expert's full row range (no split-K)
+  if (s.mx) {
+    MOE_TRY(wgrad_routed_mx(s, rt, sv, w, g, st));
+  } else {
   {
     GemmParams p;  // dW_down[e] = dy_rows^T . (g h)
     zero_params(p);
@@ -698,6 +925,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     MOE_TRY(omap3(&p.tmO0, half ? g->dW_up : g->dW_gate, s.E, s.I, s.d));
     p.status = w.status;
     MOE_LAUNCH(half ? PL_WGRAD_UP : PL_WGRAD_GATE, st, launch_gemm(GK_WGRAD, p, grid_for(s.E * cdiv(s.I, kBM) * cdiv(s.d, kBN)), st));
+  }
   }
   if (s.S) {
     {

@@ -19,8 +19,11 @@ constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
 // Each expert's row group starts at a multiple of kRowAlign rows.  The GEMMs
 // cut a group into 128-row tiles plus, when its length is an odd multiple of
-// 64, one 64-row tail tile (computed with an M=64 MMA).
+// 64, one 64-row tail tile (computed with an M=64 MMA).  The MXFP8 path pads
+// groups to kRowAlignMx rows: its weight-gradient GEMMs take K (token rows)
+// 128 at a time and its scale blocks cover 128 rows.
 constexpr int kRowAlign = 64;
+constexpr int kRowAlignMx = 128;
 constexpr int kTileRows = 128;
 
 // ---- routing kernels (routing.cu)
@@ -29,7 +32,7 @@ cudaError_t launch_topk_count(const float* logits, int T, int E, int k, int32_t*
 cudaError_t launch_chunk_scan(const int32_t* chunk_counts, int nchunk, int E, int32_t* chunk_base,
                               int32_t* counts, cudaStream_t st);
 cudaError_t launch_scatter(const int32_t* topk_idx, const float* topk_w, int T, int E, int k,
-                           const int32_t* chunk_base, const int32_t* counts, int32_t* offsets,
+                           int row_align, const int32_t* chunk_base, const int32_t* counts, int32_t* offsets,
                            int32_t* row_start, int32_t* tile_start, int32_t* perm_token,
                            int32_t* route_row,
                            int32_t* perm_token_pad, int32_t* route_row_pad, float* perm_w_pad,
@@ -60,11 +63,16 @@ cudaError_t launch_mx_rows(const __nv_bfloat16* src, long long src_ld, const int
                            __nv_bfloat16* dst_bf16, cudaStream_t st);
 cudaError_t launch_mx_cols(const __nv_bfloat16* src, long long src_ld, long long src_bstride, int rows,
                            int cols, int batch, uint8_t* dst, long long dst_ld, long long dst_brows,
-                           int k_off, uint8_t* sf, long long dst_rows_total, cudaStream_t st);
+                           int k_off, uint8_t* sf, long long dst_rows_total, const int32_t* total_rows,
+                           cudaStream_t st);
 // Bytes of the scale array of an MXFP8 operand with `rows` rows and K columns.
 inline size_t mx_sf_bytes(int64_t rows, int64_t K) {
   return static_cast<size_t>(((rows + 127) / 128) * (K / 128) * 512);
 }
+// Scale arrays are allocated with one spare 512-byte block: a 256-row B tile
+// whose second half lies past the operand's last row still fetches two blocks
+// (the columns it feeds are never stored).
+inline size_t mx_sf_alloc(int64_t rows, int64_t K) { return mx_sf_bytes(rows, K) + 512; }
 
 // ---- tensor-core GEMM instantiations (gemm_fwd.cu, gemm_bwd.cu)
 enum GemmKind : int {
@@ -74,6 +82,12 @@ enum GemmKind : int {
   GK_DGRAD_DOWN,     // dy rows . W_down (MN-major), SwiGLU backward epilogue
   GK_DGRAD_GATEUP,   // [da|db] rows . [W_gate; W_up] (MN-major, two stacks along K)
   GK_WGRAD,          // A^T . B over a group's rows (both MN-major): weight gradients
+  // MXFP8 block-scaled forms (E4M3 operands, all K-major):
+  GK_MX_GATEUP,       // x rows . [W_gate; W_up]^T, SwiGLU epilogue quantizing h
+  GK_MX_DOWN,         // h rows . W_down^T, scaled by the router weight
+  GK_MX_DGRAD_DOWN,   // dy rows . W_down (as W_down^T rows), SwiGLU backward quantizing [da|db]
+  GK_MX_DGRAD_GATEUP, // [da|db] rows . [W_gate; W_up] (as its transpose's rows)
+  GK_MX_WGRAD,        // weight gradients from operands transposed to token-major K
   GK_COUNT
 };
 cudaError_t launch_gemm(GemmKind kind, const GemmParams& p, int grid, cudaStream_t st);

@@ -12,54 +12,13 @@
 // inside it the byte of row r (0..127) and 32-column block j (0..3) sits at
 // 16 * (r % 32) + 4 * (r / 32) + j.  The GEMM copies one such block straight
 // into tensor memory per operand tile and stage.
-#include <cuda_fp8.h>
-
 #include "moe_internal.h"
+#include "mx_common.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 
 namespace {
-
-// floor(log2(a)) for a > 0 (fp32, normal or subnormal).
-__device__ __forceinline__ int floor_log2(float a) {
-  const uint32_t b = __float_as_uint(a);
-  const int e = static_cast<int>((b >> 23) & 0xFF);
-  if (e != 0) return e - 127;
-  const uint32_t m = b & 0x7FFFFFu;  // subnormal: a = m * 2^-149
-  return (31 - __clz(static_cast<int>(m))) - 149;
-}
-
-// Block scale exponent (unbiased) and its E8M0 code for a block maximum.
-__device__ __forceinline__ int mx_scale_exp(float amax) {
-  if (!(amax > 0.f)) return -127;
-  int e = floor_log2(amax) - 8;
-  return e < -127 ? -127 : (e > 127 ? 127 : e);
-}
-
-__device__ __forceinline__ uint8_t to_e4m3(float v) {
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
-
-// Quantizes 32 values with scale 2^e into 32 E4M3 bytes (two 16-byte words).
-__device__ __forceinline__ void quant32(const float* v, int e, uint4& lo, uint4& hi) {
-  const float inv = ldexpf(1.0f, -e);  // exact power of two
-  uint32_t w[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    w[i] = static_cast<uint32_t>(to_e4m3(v[4 * i] * inv)) |
-           (static_cast<uint32_t>(to_e4m3(v[4 * i + 1] * inv)) << 8) |
-           (static_cast<uint32_t>(to_e4m3(v[4 * i + 2] * inv)) << 16) |
-           (static_cast<uint32_t>(to_e4m3(v[4 * i + 3] * inv)) << 24);
-  }
-  lo = make_uint4(w[0], w[1], w[2], w[3]);
-  hi = make_uint4(w[4], w[5], w[6], w[7]);
-}
-
-__device__ __forceinline__ size_t sf_word_offset(int64_t row, int64_t kgroup, int64_t rblocks) {
-  return static_cast<size_t>((kgroup * rblocks + row / 128) * 512 + 16 * (row % 32) +
-                             4 * ((row % 128) / 32));
-}
 
 // Row-wise quantization: dst row r = src row idx[r] (or row r when idx is
 // null; a negative index gives a zero row), blocks of 32 along the row.
@@ -125,7 +84,7 @@ __global__ void __launch_bounds__(kQThreads)
     uint32_t code = static_cast<uint32_t>(e + 127) << (8 * j);
     code |= __shfl_xor_sync(gmask, code, 1);
     code |= __shfl_xor_sync(gmask, code, 2);
-    if (j == 0) *reinterpret_cast<uint32_t*>(sf + sf_word_offset(r, g, R / 128)) = code;
+    if (j == 0) *reinterpret_cast<uint32_t*>(sf + sf_word_offset(r, g, (R + 127) / 128)) = code;
   }
 }
 
@@ -133,13 +92,16 @@ __global__ void __launch_bounds__(kQThreads)
 // a GEMM whose reduction axis is `rows`.  Writes dst[c, k_off + r] (row pitch
 // dst_ld, K-major for the GEMM) with blocks of 32 along r.  blockIdx.z walks a
 // batch of such matrices (per expert): src += z * src_bstride, dst row offset
-// += z * dst_brows.  Tile: 128 rows x 64 columns per block.
+// += z * dst_brows.  Tile: 128 rows x 64 columns per block.  When total_rows
+// is given, source rows from *total_rows on are neither read nor written
+// (whole 128-row tiles; *total_rows is a multiple of 128 there).
 __global__ void __launch_bounds__(kQThreads)
     mx_cols_kernel(const __nv_bfloat16* __restrict__ src, long long src_ld, long long src_bstride, int rows,
                    int cols, uint8_t* __restrict__ dst, long long dst_ld, long long dst_brows, int k_off,
-                   uint8_t* __restrict__ sf, long long dst_rows_total) {
+                   uint8_t* __restrict__ sf, long long dst_rows_total, const int32_t* __restrict__ total_rows) {
   __shared__ float tile[128][65];
   const int r0 = blockIdx.y * 128, c0 = blockIdx.x * 64;
+  if (total_rows && r0 >= __ldg(total_rows)) return;
   const __nv_bfloat16* s = src + static_cast<long long>(blockIdx.z) * src_bstride;
   // coalesced load: each warp reads rows, 64 columns = 128 bytes per row
   for (int i = threadIdx.x; i < 128 * 32; i += kQThreads) {
@@ -196,11 +158,12 @@ cudaError_t launch_mx_rows(const __nv_bfloat16* src, long long src_ld, const int
 
 cudaError_t launch_mx_cols(const __nv_bfloat16* src, long long src_ld, long long src_bstride, int rows,
                            int cols, int batch, uint8_t* dst, long long dst_ld, long long dst_brows,
-                           int k_off, uint8_t* sf, long long dst_rows_total, cudaStream_t st) {
+                           int k_off, uint8_t* sf, long long dst_rows_total, const int32_t* total_rows,
+                           cudaStream_t st) {
   if (rows <= 0 || cols <= 0 || batch <= 0) return cudaSuccess;
   dim3 grid((cols + 63) / 64, (rows + 127) / 128, batch);
   mx_cols_kernel<<<grid, kQThreads, 0, st>>>(src, src_ld, src_bstride, rows, cols, dst, dst_ld, dst_brows,
-                                             k_off, sf, dst_rows_total);
+                                             k_off, sf, dst_rows_total, total_rows);
   return cudaGetLastError();
 }
 

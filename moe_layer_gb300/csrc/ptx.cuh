@@ -95,6 +95,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // 3-D tiled load (used for MN-major operands: one instruction fetches every
 // 64-column chunk of a tile).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int c0, int c1, int c2,
@@ -166,6 +173,40 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// D[tmem] (+)= (A . 2^sfA) * (B . 2^sfB)^T with E4M3 operands and E8M0 block
+// scales (one per 32 K-elements) read from TMEM; K = 32 per instruction.
+__device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copies a 32 x 128-bit block (512 contiguous bytes of shared memory) into
+// TMEM lanes 0..31 of all four lane quadrants, four 32-bit columns.
+__device__ __forceinline__ void tc_cp_32x128b(uint32_t taddr, uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(128 >> 4) << 32;  // 8-row core-matrix stride
+  d |= static_cast<uint64_t>(1) << 46;
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+}
+
+// Instruction descriptor of the block-scaled kind::mxf8f6f4 MMA: E4M3 A and B
+// (both K-major), E8M0 scales, sf_id selecting the byte (32-element block) of
+// the scale words in TMEM for A and B.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id) {
+  return (static_cast<uint32_t>(sf_id) << 4)          // B scale byte
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (1u << 23)                                // scale format: E8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)     // M / 16
+         | (static_cast<uint32_t>(sf_id) << 29);     // A scale byte
 }
 
 // The mbarrier gets one arrival once every tcgen05 operation this thread

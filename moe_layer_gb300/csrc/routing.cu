@@ -3,7 +3,7 @@
 //               expert histogram;
 //   chunk_scan  for every expert, the exclusive prefix of its chunk counts and
 //               its total count;
-//   scatter     expert offsets (plain, padded to kRowAlign, and in GEMM row
+//   scatter     expert offsets (plain, padded to the row alignment, and in GEMM row
 //               tiles), then the stable position of every route inside its
 //               expert's row range.
 // Together they are the one-rank form of the counting schedule in the
@@ -139,12 +139,14 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) counts[e] = carry;
 }
 
-__device__ __forceinline__ int pad_rows(int c) { return (c + kRowAlign - 1) / kRowAlign * kRowAlign; }
-__device__ __forceinline__ int row_tiles(int c) { return (pad_rows(c) + kTileRows - 1) / kTileRows; }
+__device__ __forceinline__ int pad_rows(int c, int align) { return (c + align - 1) / align * align; }
+__device__ __forceinline__ int row_tiles(int c, int align) {
+  return (pad_rows(c, align) + kTileRows - 1) / kTileRows;
+}
 
 __global__ void __launch_bounds__(kChunkWarps * 32)
     scatter_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int T,
-                   int E, int k, const int32_t* __restrict__ chunk_base,
+                   int E, int k, int align, const int32_t* __restrict__ chunk_base,
                    const int32_t* __restrict__ counts, int32_t* __restrict__ offsets_out,
                    int32_t* __restrict__ row_start_out, int32_t* __restrict__ tile_start_out,
                    int32_t* __restrict__ perm_token,
@@ -166,8 +168,8 @@ __global__ void __launch_bounds__(kChunkWarps * 32)
       if (e < E) {
         const int c = __ldg(counts + e);
         sum += c;
-        psum += pad_rows(c);
-        tsum += row_tiles(c);
+        psum += pad_rows(c, align);
+        tsum += row_tiles(c, align);
       }
     }
     int inc = sum, pinc = psum, tinc = tsum;
@@ -191,8 +193,8 @@ __global__ void __launch_bounds__(kChunkWarps * 32)
         s_ts[e] = trun;
         const int c = __ldg(counts + e);
         run += c;
-        prun += pad_rows(c);
-        trun += row_tiles(c);
+        prun += pad_rows(c, align);
+        trun += row_tiles(c, align);
       }
     }
     if (lane == 31) {
@@ -281,12 +283,12 @@ cudaError_t launch_chunk_scan(const int32_t* chunk_counts, int nchunk, int E, in
 }
 
 cudaError_t launch_scatter(const int32_t* topk_idx, const float* topk_w, int T, int E, int k,
-                           const int32_t* chunk_base, const int32_t* counts, int32_t* offsets,
+                           int row_align, const int32_t* chunk_base, const int32_t* counts, int32_t* offsets,
                            int32_t* row_start, int32_t* tile_start, int32_t* perm_token,
                            int32_t* route_row, int32_t* perm_token_pad, int32_t* route_row_pad,
                            float* perm_w_pad, cudaStream_t st) {
   const int nchunk = (T + kChunkTokens - 1) / kChunkTokens;
-  scatter_kernel<<<nchunk, kChunkWarps * 32, 0, st>>>(topk_idx, topk_w, T, E, k, chunk_base, counts,
+  scatter_kernel<<<nchunk, kChunkWarps * 32, 0, st>>>(topk_idx, topk_w, T, E, k, row_align, chunk_base, counts,
                                                       offsets, row_start, tile_start, perm_token,
                                                       route_row, perm_token_pad, route_row_pad,
                                                       perm_w_pad);

@@ -9,42 +9,71 @@
 //   * the backward dgrads (down with the fused SwiGLU backward and router
 //     weight-gradient partials; gate/up with two weight stacks along K);
 //   * the weight gradients, whose reduction axis is an expert's (ragged) row
-//     range and whose operands are both MN-major.
+//     range.
 //
 // The MoE computation these serve is the DeepSeek-V3-style layer described in
 // "Mixture-of-Kittens: MoE Megakernel for NVL72s" (blog post, section
 // "Overlapping computation and communication in MoE"; paper section 2.1).
 //
+// Two number formats:
+//   bf16   kind::f16 MMAs (128x256x16), K = 64 per pipeline stage, operands
+//          K-major or MN-major;
+//   MXFP8  (MX = true; blog section "MXFP8 support") kind::mxf8f6f4 block-scaled
+//          MMAs (128x256x32) on E4M3 operands, both K-major, K = 128 per stage.
+//          Each stage also brings the E8M0 scales of its A and B tiles (one
+//          512-byte tcgen05.cp block per 128 rows); the MMA thread copies them
+//          into a ring of TMEM columns next to the accumulator before issuing
+//          the stage's four MMAs.
+//
 // Roles per CTA (256 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (lane 0 issues the tile loads)
-//   warp 1      MMA issuer (lane 0), 128x256x16 bf16 MMAs into TMEM
-//   warp 2      TMEM allocator (512 columns = two 128x256 fp32 accumulators)
+//   warp 1      MMA issuer (lane 0)
+//   warp 2      TMEM allocator (512 columns)
 //   warps 4..7  epilogue: TMEM -> registers -> fused math -> swizzled smem
 //               staging -> TMA bulk stores
-// Pipelines: kStages smem stages (full/empty mbarriers), two accumulator
-// buffers (acc_full/acc_empty) so the epilogue of tile i overlaps the MMAs of
-// tile i+1.  Every wait is bounded (see mbar_wait): a stuck pipeline records
-// MOE_ERR_DEVICE_TIMEOUT in the status word and the CTA exits cleanly.
+// Pipelines: kStages smem stages (full/empty mbarriers) and accumulator
+// buffers (acc_full/acc_empty): two 256-column buffers in bf16 mode so the
+// epilogue of tile i overlaps the MMAs of tile i+1; one in MXFP8 mode, whose
+// other TMEM columns hold the scale ring.  Every wait is bounded (see
+// mbar_wait): a stuck pipeline records MOE_ERR_DEVICE_TIMEOUT in the status
+// word and the CTA exits cleanly.
 #pragma once
+#include "mx_common.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 
 constexpr int kBM = 128;  // rows per tile (TMEM lanes)
 constexpr int kBN = 256;  // accumulator columns per tile
-constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
+constexpr int kBK = 64;   // bf16 K per stage: one 128-byte swizzle row
+constexpr int kBKmx = 128;  // MXFP8 K per stage: one 128-byte swizzle row of E4M3
 constexpr int kStages = 4;
-constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
-constexpr int kBTileBytes = kBN * kBK * 2;  // 32 KB
+constexpr int kATileBytes = kBM * 128;  // 16 KB (128 rows of 128 bytes)
+constexpr int kBTileBytes = kBN * 128;  // 32 KB
 constexpr int kStageBytes = kATileBytes + kBTileBytes;
-constexpr int kMNChunkBytes = kBK * 128;  // one 64-wide MN chunk of an MN-major tile
+constexpr int kSfStageBytes = 512 + 1024;  // MXFP8: scales of the A tile and the B tile
+constexpr int kSfTmemCol = 256;            // MXFP8: first TMEM column of the scale ring
+constexpr int kSfTmemStride = 16;          // MXFP8: columns per stage (A at +0, B at +8)
+constexpr int kMNChunkBytes = kBK * 128;   // one 64-wide MN chunk of an MN-major tile
 constexpr int kTmemCols = 512;
 constexpr int kGemmThreads = 256;
-// Epilogue staging: per epilogue warp two 4 KB boxes (32 rows x 64 bf16) that
-// TMA stores to global memory while the next box is being filled.
-constexpr int kStageBoxBytes = 32 * 128;
-constexpr int kEpiStagingBytes = 4 * 2 * kStageBoxBytes;
-constexpr int kGemmSmemBytes = 1024 + kStages * kStageBytes + kEpiStagingBytes + 256;
+constexpr int kStageBoxBytes = 32 * 128;   // one epilogue staging box: 32 rows x 128 bytes
+
+// Epilogue staging: per epilogue warp two 4 KB boxes (bf16 mode) that TMA
+// stores to global memory while the next box is being filled; one box in
+// MXFP8 mode, whose scale stages use the rest of shared memory.
+template <bool MX>
+__host__ __device__ constexpr int epi_slots() { return MX ? 1 : 2; }
+template <bool MX>
+__host__ __device__ constexpr int acc_bufs() { return MX ? 1 : 2; }
+template <bool MX>
+__host__ __device__ constexpr int stage_k() { return MX ? kBKmx : kBK; }
+template <bool MX>
+__host__ __device__ constexpr int gemm_smem_bytes_for() {
+  return 1024 + kStages * kStageBytes + (MX ? kStages * kSfStageBytes : 0) +
+         4 * epi_slots<MX>() * kStageBoxBytes + 256;
+}
+constexpr int kGemmSmemBytes = gemm_smem_bytes_for<false>();
 
 enum AMode : int { A_K_TILE = 0, A_MN_TILE = 1 };
 enum BMode : int { B_K_TILE = 0, B_K_DUAL_N = 1, B_MN_TILE = 2, B_MN_DUAL_K = 3 };
@@ -52,7 +81,7 @@ enum EpiMode : int { EPI_F32_BIAS = 0, EPI_SWIGLU_FWD = 1, EPI_BF16 = 2, EPI_SWI
 enum SchedMode : int { SCHED_ROWS = 0, SCHED_WGRAD = 1 };
 
 struct GemmParams {
-  // Operand maps: K-major operands are 2-D [rows, K] maps with 64 x rows
+  // Operand maps: K-major operands are 2-D [rows, K] maps with 128-byte x rows
   // boxes; MN-major operands are 3-D maps (make_tmap_mn3d) whose box holds
   // every 64-column chunk of the tile (2 for A, 4 for B).
   CUtensorMap tmA;
@@ -70,15 +99,21 @@ struct GemmParams {
   // ---- schedule
   int dense_rows;          // > 0: a single group of this many rows; 0: grouped by row_start
   int num_groups;          // number of groups (experts) when grouped
-  const int* row_start;    // [G+1] padded row offsets, multiples of 64 (grouped)
+  const int* row_start;    // [G+1] padded row offsets, multiples of 64 (128 in MXFP8 mode)
   const int* tile_start;   // [G+1] prefix of 128-row tiles per group (grouped SCHED_ROWS)
   const int* counts;       // [G] real rows per group (grouped)
   int N;                   // output columns
   int K;                   // reduction length (SCHED_ROWS)
   int M_out;               // output rows per group (SCHED_WGRAD)
   int b_group_rows;        // rows of the B tensor map per group (0: B rows are absolute)
-  int a_col_off;           // first column of A in its tensor (A_MN_TILE)
+  int a_col_off;           // SCHED_WGRAD: first column (A_MN_TILE) or row (A_K_TILE) of A's M range
   int b_split;             // B_MN_DUAL_K: K index from which B comes from tmB1
+  // ---- MXFP8 operand scales (tcgen05.cp block layout, see mx_common.cuh)
+  const uint8_t* sfa;      // scales of A; rows of A / 128 = sfa_rb
+  long long sfa_rb;
+  const uint8_t* sfb0;     // scales of B (of the first stack for B_K_DUAL_N)
+  const uint8_t* sfb1;     // scales of the second stack (B_K_DUAL_N)
+  long long sfb_rb;
   // ---- epilogue
   void* out;               // direct-store outputs: EPI_F32_BIAS logits; EPI_SWIGLU_BWD [da|db]
   long long ldo;
@@ -91,6 +126,12 @@ struct GemmParams {
   const __nv_bfloat16* ab;
   int I;
   int store_ab;
+  // MXFP8 quantized epilogue output (E4M3 rows + scales): h for
+  // EPI_SWIGLU_FWD, [da|db] for EPI_SWIGLU_BWD; null when not wanted.
+  uint8_t* qout;
+  long long qld;
+  uint8_t* qsf;
+  long long q_rb;
   int* status;
 };
 
@@ -137,7 +178,7 @@ __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
   }
 }
 
-template <int EPI, int SCH>
+template <int EPI, int SCH, int BK>
 __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau) {
   TileInfo t;
   if constexpr (SCH == SCHED_ROWS) {
@@ -172,7 +213,7 @@ __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau) {
     t.nt = nt;
     t.n0 = nt * W;
     t.kb0 = 0;
-    t.nkb = p.K / kBK;
+    t.nkb = p.K / BK;
   } else {
     const int num_nt = (p.N + kBN - 1) / kBN;
     const int num_mt = (p.M_out + kBM - 1) / kBM;
@@ -190,21 +231,23 @@ __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau) {
     t.m64 = 0;
     if (p.dense_rows > 0) {
       t.kb0 = 0;
-      t.nkb = (p.dense_rows + kBK - 1) / kBK;
+      t.nkb = (p.dense_rows + BK - 1) / BK;
     } else {
       const int rs = __ldg(p.row_start + e);
-      t.kb0 = rs / kBK;
-      t.nkb = (__ldg(p.row_start + e + 1) - rs) / kBK;
+      t.kb0 = rs / BK;
+      t.nkb = (__ldg(p.row_start + e + 1) - rs) / BK;
     }
   }
   return t;
 }
 
 // ------------------------------------------------------------------ producer
-template <int AM, int BMO, int EPI, int SCH>
-__device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_tiles,
+template <int AM, int BMO, int EPI, int SCH, bool MX>
+__device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_tiles, uint32_t s_sf,
                                               uint32_t full0, uint32_t empty0, int num_tiles,
                                               volatile int* abort_flag, int lane) {
+  constexpr int BK = stage_k<MX>();
+  constexpr uint32_t kTx = kStageBytes + (MX ? kSfStageBytes : 0);
   int s = 0;
   uint32_t ph = 0;
   // Per stage: parity of the last load issued into it, or -1.
@@ -214,7 +257,10 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
   bool aborted = false;
 
   for (int tau = blockIdx.x; tau < num_tiles && !aborted; tau += gridDim.x) {
-    const TileInfo t = gemm_tile<EPI, SCH>(p, tau);
+    const TileInfo t = gemm_tile<EPI, SCH, BK>(p, tau);
+    // row coordinate of the A tile: token rows, or output rows of a weight gradient
+    const int arow = SCH == SCHED_WGRAD ? p.a_col_off + t.m0 : t.row0;
+    const int brow = t.e * p.b_group_rows + t.n0;
     for (int kb = 0; kb < t.nkb; ++kb) {
       bool ok = true;
       if (lane == 0) ok = mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, p.status);
@@ -226,22 +272,22 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
       const uint32_t full = full0 + 8 * s;
       const uint32_t sA = s_tiles + s * kStageBytes;
       const uint32_t sB = sA + kATileBytes;
-      if (lane == 0) mbar_arrive_expect_tx(full, kStageBytes);
+      if (lane == 0) mbar_arrive_expect_tx(full, kTx);
       __syncwarp();
-      const int kabs = (t.kb0 + kb) * kBK;
+      const int kabs = (t.kb0 + kb) * BK;
       // ---- A operand
       if constexpr (AM == A_K_TILE) {
-        if (lane == 0) tma_load_2d(sA, &p.tmA, kabs, t.row0, full);
+        if (lane == 0) tma_load_2d(sA, &p.tmA, kabs, arow, full);
       } else {  // A_MN_TILE: both 64-column chunks with one 3-D box
         if (lane == 0) tma_load_3d(sA, &p.tmA, 0, kabs, (p.a_col_off + t.m0) / 64, full);
       }
       // ---- B operand
       if constexpr (BMO == B_K_TILE) {
-        if (lane == 0) tma_load_2d(sB, &p.tmB0, kabs, t.e * p.b_group_rows + t.n0, full);
+        if (lane == 0) tma_load_2d(sB, &p.tmB0, kabs, brow, full);
       } else if constexpr (BMO == B_K_DUAL_N) {
         if (lane == 0) {
-          tma_load_2d(sB, &p.tmB0, kabs, t.e * p.b_group_rows + t.n0, full);
-          tma_load_2d(sB + kBTileBytes / 2, &p.tmB1, kabs, t.e * p.b_group_rows + t.n0, full);
+          tma_load_2d(sB, &p.tmB0, kabs, brow, full);
+          tma_load_2d(sB + kBTileBytes / 2, &p.tmB1, kabs, brow, full);
         }
       } else if constexpr (BMO == B_MN_TILE) {  // four 64-column chunks, one 3-D box
         if (lane == 0) tma_load_3d(sB, &p.tmB0, 0, t.e * p.b_group_rows + kabs, t.n0 / 64, full);
@@ -251,6 +297,21 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
           const int kk = second ? kabs - p.b_split : kabs;
           tma_load_3d(sB, second ? (const void*)&p.tmB1 : (const void*)&p.tmB0, 0,
                       t.e * p.b_group_rows + kk, t.n0 / 64, full);
+        }
+      }
+      // ---- MXFP8 scales of this stage's A and B tiles (one 128-column group)
+      if constexpr (MX) {
+        if (lane == 0) {
+          const long long g = kabs / kBKmx;
+          const uint32_t sfs = s_sf + s * kSfStageBytes;
+          bulk_load(sfs, p.sfa + (g * p.sfa_rb + arow / 128) * 512, 512, full);
+          const size_t boff = static_cast<size_t>((g * p.sfb_rb + brow / 128) * 512);
+          if constexpr (BMO == B_K_DUAL_N) {
+            bulk_load(sfs + 512, p.sfb0 + boff, 512, full);
+            bulk_load(sfs + 1024, p.sfb1 + boff, 512, full);
+          } else {
+            bulk_load(sfs + 512, p.sfb0 + boff, 1024, full);
+          }
         }
       }
       issued_parity[s] = static_cast<int>(ph);
@@ -271,11 +332,12 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <int AM, int BMO, int EPI, int SCH>
-__device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, uint32_t full0,
-                                         uint32_t empty0, uint32_t accf0, uint32_t acce0,
-                                         uint32_t drain, uint32_t tmem_base, int num_tiles,
-                                         volatile int* abort_flag) {
+template <int AM, int BMO, int EPI, int SCH, bool MX>
+__device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, uint32_t s_sf,
+                                         uint32_t full0, uint32_t empty0, uint32_t accf0,
+                                         uint32_t acce0, uint32_t drain, uint32_t tmem_base,
+                                         int num_tiles, volatile int* abort_flag) {
+  constexpr int BK = stage_k<MX>();
   constexpr bool a_mn = (AM == A_MN_TILE);
   constexpr bool b_mn = (BMO == B_MN_TILE || BMO == B_MN_DUAL_K);
   constexpr uint32_t idesc128 = idesc_bf16_f32(kBM, kBN, a_mn ? 1 : 0, b_mn ? 1 : 0);
@@ -286,7 +348,7 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
   uint32_t aph = 0;
   bool issued = false, aborted = false;
   for (int tau = blockIdx.x; tau < num_tiles && !aborted; tau += gridDim.x) {
-    const TileInfo t = gemm_tile<EPI, SCH>(p, tau);
+    const TileInfo t = gemm_tile<EPI, SCH, BK>(p, tau);
     if (!mbar_wait(acce0 + 8 * acc, aph ^ 1, abort_flag, p.status)) {
       aborted = true;
       break;
@@ -302,13 +364,29 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
       tc_fence_after();
       const uint32_t sA = s_tiles + s * kStageBytes;
       const uint32_t sB = sA + kATileBytes;
+      if constexpr (MX) {
+        // scale ring slot s: reused by stage s + kStages, whose data can only
+        // have been loaded after these MMAs released stage s
+        const uint32_t sfa_t = tmem_base + kSfTmemCol + s * kSfTmemStride;
+        const uint32_t sfs = s_sf + s * kSfStageBytes;
+        tc_cp_32x128b(sfa_t, sfs);
+        tc_cp_32x128b(sfa_t + 8, sfs + 512);
+        tc_cp_32x128b(sfa_t + 12, sfs + 1024);
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint64_t ad = a_mn ? smem_desc_sw128(sA + kk * 2048, kMNChunkBytes, 1024)
-                                 : smem_desc_sw128(sA + kk * 32, 16, 1024);
-        const uint64_t bd = b_mn ? smem_desc_sw128(sB + kk * 2048, kMNChunkBytes, 1024)
-                                 : smem_desc_sw128(sB + kk * 32, 16, 1024);
-        tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBKmx / 32; ++kk) {
+          tc_mma_mxf8(d_tmem, smem_desc_sw128(sA + kk * 32, 16, 1024),
+                      smem_desc_sw128(sB + kk * 32, 16, 1024), idesc_mxf8(kBM, kBN, kk), sfa_t,
+                      sfa_t + 8, (kb > 0 || kk > 0) ? 1u : 0u);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint64_t ad = a_mn ? smem_desc_sw128(sA + kk * 2048, kMNChunkBytes, 1024)
+                                   : smem_desc_sw128(sA + kk * 32, 16, 1024);
+          const uint64_t bd = b_mn ? smem_desc_sw128(sB + kk * 2048, kMNChunkBytes, 1024)
+                                   : smem_desc_sw128(sB + kk * 32, 16, 1024);
+          tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        }
       }
       tc_commit(empty0 + 8 * s);
       issued = true;
@@ -322,7 +400,7 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
       tc_commit(accf0 + 8 * acc);
     else
       mbar_arrive(accf0 + 8 * acc);
-    if (++acc == 2) {
+    if (++acc == acc_bufs<MX>()) {
       acc = 0;
       aph ^= 1;
     }
@@ -337,17 +415,19 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
 // ------------------------------------------------------------------ epilogue
 // Each epilogue thread owns one accumulator row (TMEM lane).  Results are
 // converted to bf16 and written into the warp's staging boxes in the swizzled
-// layout, then one lane issues a TMA store of the 32 x 64 box; the two boxes
-// of a warp alternate so filling one overlaps the store of the other.
+// layout, then one lane issues a TMA store of the 32 x 64 box; with two boxes
+// per warp, filling one overlaps the store of the other.
+template <int NSLOT>
 struct EpiStager {
-  uint32_t base;  // this warp's two boxes
+  uint32_t base;  // this warp's boxes
   int slot;
   int lane;
   __device__ __forceinline__ uint32_t begin() {
-    if (lane == 0) bulk_wait_group_read<1>();  // the box about to be filled is free
+    if (lane == 0) bulk_wait_group_read<NSLOT - 1>();  // the box about to be filled is free
     __syncwarp();
     return base + static_cast<uint32_t>(slot) * kStageBoxBytes;
   }
+  __device__ __forceinline__ void next() { slot = slot + 1 == NSLOT ? 0 : slot + 1; }
   __device__ __forceinline__ void store2d(const CUtensorMap* tm, uint32_t box, int c0, int c1) {
     fence_proxy_async_shared();
     __syncwarp();
@@ -355,7 +435,7 @@ struct EpiStager {
       tma_store_2d(tm, c0, c1, box);
       bulk_commit_group();
     }
-    slot ^= 1;
+    next();
   }
   __device__ __forceinline__ void store3d(const CUtensorMap* tm, uint32_t box, int c0, int c1, int c2) {
     fence_proxy_async_shared();
@@ -364,7 +444,7 @@ struct EpiStager {
       tma_store_3d(tm, c0, c1, c2, box);
       bulk_commit_group();
     }
-    slot ^= 1;
+    next();
   }
   // stage 64 values of this thread's row and store them at (c0, c1)
   __device__ __forceinline__ void row64_2d(const CUtensorMap* tm, const float* v, int c0, int c1) {
@@ -374,15 +454,17 @@ struct EpiStager {
   }
 };
 
-template <int EPI, int SCH>
+template <int EPI, int SCH, bool MX>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf0, uint32_t acce0,
                                               uint32_t tmem_base, uint32_t s_staging, int num_tiles,
                                               volatile int* abort_flag, int warp_e, int lane) {
+  constexpr int BK = stage_k<MX>();
   int acc = 0;
   uint32_t aph = 0;
-  EpiStager stg{s_staging + static_cast<uint32_t>(warp_e) * 2u * kStageBoxBytes, 0, lane};
+  EpiStager<epi_slots<MX>()> stg{
+      s_staging + static_cast<uint32_t>(warp_e) * epi_slots<MX>() * kStageBoxBytes, 0, lane};
   for (int tau = blockIdx.x; tau < num_tiles; tau += gridDim.x) {
-    const TileInfo t = gemm_tile<EPI, SCH>(p, tau);
+    const TileInfo t = gemm_tile<EPI, SCH, BK>(p, tau);
     // Tile row held by this thread's TMEM lane: lane l of warp w is row 32w + l
     // of an M=128 accumulator; an M=64 accumulator keeps rows 16w..16w+15 in
     // lanes 0..15 of each warp (lanes 16..31 hold nothing of this tile).
@@ -436,6 +518,11 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
           }
         }
       } else if constexpr (EPI == EPI_SWIGLU_FWD) {
+        // quantized h (MXFP8): the tile's 128 h columns are one 128-column
+        // group, so each row's four block scales form one word
+        const bool q_out = MX && p.qout != nullptr;
+        const bool q_in_mem = q_out && lane_ok;
+        uint32_t qword = 0;
         for (int c0 = 0; c0 < kBN / 2 && t.n0 + c0 < p.N; c0 += 64) {
           float a[64], b[64];
           tmem_ld32(tr + c0, a);
@@ -456,8 +543,20 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
           }
 #pragma unroll
           for (int i = 0; i < 64; ++i) a[i] = a[i] * sigmoidf_(a[i]) * b[i];
-          stg.row64_2d(o1, a, t.n0 + c0, r0);
+          if (q_out) {
+            if constexpr (MX) {
+              if (q_in_mem) {
+                uint8_t* q = p.qout + grow * p.qld + t.n0 + c0;
+                qword |= quant32_store(a, q) << (8 * (c0 / 32));
+                qword |= quant32_store(a + 32, q + 32) << (8 * (c0 / 32 + 1));
+              }
+            }
+          } else {
+            stg.row64_2d(o1, a, t.n0 + c0, r0);
+          }
         }
+        if (MX && q_in_mem)
+          *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, t.n0 / 128, p.q_rb)) = qword;
       } else if constexpr (EPI == EPI_BF16) {
         float scale = 1.f;
         if (p.row_scale && p.dense_rows == 0 && lane_ok) scale = __ldg(p.row_scale + grow);
@@ -472,6 +571,8 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
           stg.row64_2d(o0, v, t.n0 + c0, r0);
         }
       } else {  // EPI_SWIGLU_BWD: direct row stores; a long K loop hides this epilogue
+        // columns per step: 16, or 32 in MXFP8 mode (one scale block of da and db)
+        constexpr int CW = MX ? 32 : 16;
         const bool in_mem = p.dense_rows > 0 ? real : lane_ok;
         __nv_bfloat16* dadb = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
         __nv_bfloat16* hg = reinterpret_cast<__nv_bfloat16*>(p.out2) + grow * p.ldo2;
@@ -479,38 +580,60 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
         float g = 1.f;
         if (in_mem && real && p.row_scale) g = __ldg(p.row_scale + grow);
         float dgp = 0.f;
-        for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 16) {
-          float dh[16];
-          tmem_ld16(tr + c0, dh);
+        uint32_t wa = 0, wb = 0;  // MXFP8: scale words of da and db for the current 128 columns
+        for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += CW) {
+          float dh[CW];
+          if constexpr (CW == 32) {
+            tmem_ld32(tr + c0, dh);
+          } else {
+            tmem_ld16(tr + c0, dh);
+          }
           tmem_ld_wait();
           if (in_mem) {
-            float da[16], db[16], hv[16];
-            if (real) {
-              float a[16], b[16];
-              load_bf16x16(abr + t.n0 + c0, a);
-              load_bf16x16(abr + p.I + t.n0 + c0, b);
+            float da[CW], db[CW], hv[CW];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float sg = sigmoidf_(a[i]);
-                const float silu = a[i] * sg;
-                const float hh = silu * b[i];
-                dgp += dh[i] * hh;
-                const float dhs = g * dh[i];
-                da[i] = dhs * b[i] * sg * (1.f + a[i] * (1.f - sg));
-                db[i] = dhs * silu;
-                hv[i] = g * hh;
+            for (int h16 = 0; h16 < CW / 16; ++h16) {
+              if (real) {
+                float a[16], b[16];
+                load_bf16x16(abr + t.n0 + c0 + 16 * h16, a);
+                load_bf16x16(abr + p.I + t.n0 + c0 + 16 * h16, b);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const float sg = sigmoidf_(a[i]);
+                  const float silu = a[i] * sg;
+                  const float hh = silu * b[i];
+                  const float d = dh[16 * h16 + i];
+                  dgp += d * hh;
+                  const float dhs = g * d;
+                  da[16 * h16 + i] = dhs * b[i] * sg * (1.f + a[i] * (1.f - sg));
+                  db[16 * h16 + i] = dhs * silu;
+                  hv[16 * h16 + i] = g * hh;
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  da[16 * h16 + i] = 0.f;
+                  db[16 * h16 + i] = 0.f;
+                  hv[16 * h16 + i] = 0.f;
+                }
               }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                da[i] = 0.f;
-                db[i] = 0.f;
-                hv[i] = 0.f;
+              store_bf16x16(dadb + t.n0 + c0 + 16 * h16, *reinterpret_cast<const float(*)[16]>(da + 16 * h16));
+              store_bf16x16(dadb + p.I + t.n0 + c0 + 16 * h16, *reinterpret_cast<const float(*)[16]>(db + 16 * h16));
+              store_bf16x16(hg + t.n0 + c0 + 16 * h16, *reinterpret_cast<const float(*)[16]>(hv + 16 * h16));
+            }
+            if constexpr (MX) {
+              if (p.qout) {
+                const int col = t.n0 + c0, j = (col / 32) & 3;
+                wa |= quant32_store(da, p.qout + grow * p.qld + col) << (8 * j);
+                wb |= quant32_store(db, p.qout + grow * p.qld + p.I + col) << (8 * j);
+                if (j == 3) {
+                  *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, col / 128, p.q_rb)) = wa;
+                  *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, (p.I + col) / 128, p.q_rb)) = wb;
+                  wa = 0;
+                  wb = 0;
+                }
               }
             }
-            store_bf16x16(dadb + t.n0 + c0, da);
-            store_bf16x16(dadb + p.I + t.n0 + c0, db);
-            store_bf16x16(hg + t.n0 + c0, hv);
           }
         }
         if (in_mem && p.out3) p.out3[grow * p.ldo3 + t.nt] = real ? dgp : 0.f;
@@ -519,7 +642,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(acce0 + 8 * acc);
-    if (++acc == 2) {
+    if (++acc == acc_bufs<MX>()) {
       acc = 0;
       aph ^= 1;
     }
@@ -530,14 +653,17 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
 }
 
 // ------------------------------------------------------------------ kernel
-template <int AM, int BMO, int EPI, int SCH>
+template <int AM, int BMO, int EPI, int SCH, bool MX = false>
 __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  constexpr int kSfBytes = MX ? kStages * kSfStageBytes : 0;
+  constexpr int kStagingBytes = 4 * epi_slots<MX>() * kStageBoxBytes;
   const uint32_t s_tiles = smem_u32(smem);
   const uint32_t s_staging = s_tiles + kStages * kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kEpiStagingBytes);
+  const uint32_t s_sf = s_staging + kStagingBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kStagingBytes + kSfBytes);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * kStages;
   const uint32_t accf0 = empty0 + 8 * kStages;
@@ -564,10 +690,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     tma_prefetch_desc(&p.tmA);
     tma_prefetch_desc(&p.tmB0);
     if (BMO == B_K_DUAL_N || BMO == B_MN_DUAL_K) tma_prefetch_desc(&p.tmB1);
-    if (EPI == EPI_BF16 || EPI == EPI_SWIGLU_FWD) tma_prefetch_desc(&p.tmO0);
-    if ((EPI == EPI_BF16 || EPI == EPI_SWIGLU_FWD) && SCH == SCHED_ROWS) tma_prefetch_desc(&p.tmO0h);
-    if (EPI == EPI_SWIGLU_FWD) tma_prefetch_desc(&p.tmO1h);
-    if (EPI == EPI_SWIGLU_FWD) tma_prefetch_desc(&p.tmO1);
+    // only the output maps this launch stores through (the others may be unset)
+    if (EPI == EPI_BF16 || (EPI == EPI_SWIGLU_FWD && (p.store_ab || p.qout == nullptr))) {
+      tma_prefetch_desc(&p.tmO0);
+      if (SCH == SCHED_ROWS) tma_prefetch_desc(&p.tmO0h);
+    }
+    if (EPI == EPI_SWIGLU_FWD && p.qout == nullptr) {
+      tma_prefetch_desc(&p.tmO1);
+      tma_prefetch_desc(&p.tmO1h);
+    }
   }
   if (warp == 2) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -580,14 +711,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   const int num_tiles = gemm_num_tiles<EPI, SCH>(p);
 
   if (warp == 0) {
-    gemm_producer<AM, BMO, EPI, SCH>(p, s_tiles, full0, empty0, num_tiles, abort_flag, lane);
+    gemm_producer<AM, BMO, EPI, SCH, MX>(p, s_tiles, s_sf, full0, empty0, num_tiles, abort_flag, lane);
   } else if (warp == 1) {
     if (lane == 0)
-      gemm_mma<AM, BMO, EPI, SCH>(p, s_tiles, full0, empty0, accf0, acce0, drain, tmem_base,
-                                  num_tiles, abort_flag);
+      gemm_mma<AM, BMO, EPI, SCH, MX>(p, s_tiles, s_sf, full0, empty0, accf0, acce0, drain,
+                                      tmem_base, num_tiles, abort_flag);
   } else if (warp >= 4) {
-    gemm_epilogue<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging, num_tiles, abort_flag, warp - 4,
-                            lane);
+    gemm_epilogue<EPI, SCH, MX>(p, accf0, acce0, tmem_base, s_staging, num_tiles, abort_flag,
+                                warp - 4, lane);
   }
   tc_fence_before();
   __syncthreads();

@@ -46,6 +46,22 @@ inline bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, u
   return r == CUDA_SUCCESS;
 }
 
+// Row-major byte matrix [outer, inner] (E4M3 codes), boxes of 128 bytes x
+// box_outer rows, 128-byte swizzle, zero fill out of bounds.
+inline bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                         uint32_t box_outer) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {128, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Row-major bf16 matrix [rows, cols] (cols a multiple of 64) viewed as
 // {64 elements, rows, cols / 64 chunks} with boxes of 64 x box_rows x
 // box_chunks.  One box lands in shared memory as box_chunks consecutive

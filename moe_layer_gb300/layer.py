@@ -22,7 +22,22 @@ class MoEBuffers:
 def weights_from(inp: dict) -> _abi.MoeWeights:
     return _abi.make_weights(inp["W_router"], inp["W_gate"], inp["W_up"], inp["W_down"],
                              inp.get("router_bias"), inp.get("Ws_gate"), inp.get("Ws_up"),
-                             inp.get("Ws_down"))
+                             inp.get("Ws_down"), inp.get("mxfp8"))
+
+
+def quantize_weights(cfg, inp: dict, stream=None):
+    """MXFP8 mode: allocates the pre-quantized weight buffer, fills it from the
+    bf16 expert weights and stores it as inp["mxfp8"] (redo after a weight
+    update)."""
+    if cfg.precision != _abi.MOE_MXFP8:
+        raise ValueError("quantize_weights needs an MXFP8 configuration")
+    n = _abi.moe_mxfp8_weights_size(cfg)
+    mx = inp.get("mxfp8")
+    if mx is None or mx.numel() < n:
+        mx = torch.empty(n, dtype=torch.uint8, device=inp["W_gate"].device)
+    _abi.moe_quantize_weights_mxfp8(cfg, weights_from(inp), mx, stream)
+    inp["mxfp8"] = mx
+    return mx
 
 
 def alloc_grads(cfg: _abi.MoeConfig, device="cuda", with_topk: bool = True) -> dict:

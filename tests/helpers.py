@@ -42,7 +42,7 @@ class LazyExperts:
         return self.cache[e]
 
 
-def oracle_forward(inp, k, logits=None, tokens=None):
+def oracle_forward(inp, k, logits=None, tokens=None, mxfp8=False):
     """Oracle forward on the CPU copies of the inputs (optionally a token subset)."""
     x = f64(inp["x"]) if tokens is None else f64(inp["x"][tokens])
     bias = None if inp.get("router_bias") is None else f64(inp["router_bias"])
@@ -51,7 +51,7 @@ def oracle_forward(inp, k, logits=None, tokens=None):
                          LazyExperts(inp["W_down"]), k, router_bias=bias,
                          ws_gate=f64(inp["Ws_gate"]) if sh else None,
                          ws_up=f64(inp["Ws_up"]) if sh else None,
-                         ws_down=f64(inp["Ws_down"]) if sh else None, logits=logits)
+                         ws_down=f64(inp["Ws_down"]) if sh else None, logits=logits, mxfp8=mxfp8)
 
 
 def oracle_backward(inp, fwd, tokens=None):

@@ -10,9 +10,13 @@ import torch
 from moe_layer_gb300 import _abi, layer
 from oracle import moe_oracle as O
 
-from .helpers import ensure_lib, f64
+from synth.inputs import MoEShape, make_inputs
+
+from .helpers import ensure_lib, f64, oracle_backward, oracle_forward, order_gap, rel_err, topk_gap
 
 pytestmark = pytest.mark.gpu
+# MXFP8 outputs vs the oracle's MXFP8 emulation: max|err| / max|ref|
+TOL_MX = 5e-2
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -43,7 +47,7 @@ def _mx_buffers(cfg, E, I, d, mx):
         off = al(off + R * K)
         nsf = (R // 128) * (K // 128) * 512
         sf = mx[off:off + nsf]
-        off = al(off + nsf)
+        off = al(off + nsf + 512)  # one spare scale block
         out.append((q, sf, R, K))
     return out
 
@@ -78,3 +82,93 @@ def test_weight_quantization_bit_exact():
         # +0 and -0 encode the same value
         same = (got_q == codes) | ((got_q & 0x7F) == 0) & ((codes & 0x7F) == 0)
         assert same.all(), (name, np.argwhere(~same)[:5])
+
+
+MX_SHAPES = {
+    "mx_small": MoEShape(T=512, d=256, I=256, E=8, k=2, n_shared=1, I_shared=128, w_std=0.05),
+    # d % 256 == 128: the last n-tile of every B operand has a 128-row second half
+    "mx_ragged": MoEShape(T=333, d=384, I=128, E=5, k=3, n_shared=0, I_shared=0, w_std=0.05),
+    "mx_zipf_zero": MoEShape(T=640, d=256, I=384, E=32, k=4, n_shared=1, I_shared=128, w_std=0.05,
+                             zipf=True, zero_experts=8),
+}
+MX_SEEDS = {}
+
+
+def _cuda(inp):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def _run_mx(shape, seed=0, backward=True):
+    inp_cpu = make_inputs(shape, seed=seed, with_dy=backward)
+    inp = _cuda(inp_cpu)
+    cfg = _abi.make_config(shape.T, shape.d, shape.I, shape.E, shape.k, shape.n_shared, shape.I_shared,
+                           precision=_abi.MOE_MXFP8)
+    layer.quantize_weights(cfg, inp)
+    bufs = layer.MoEBuffers(cfg, training=backward)
+    y = layer.forward(cfg, inp, bufs)
+    res = {"y": y, "inp_cpu": inp_cpu}
+    if backward:
+        grads = layer.alloc_grads(cfg)
+        dx = layer.backward(cfg, inp, inp["dy"], bufs, grads)
+        res.update(dx=dx, grads=grads)
+    torch.cuda.synchronize()
+    assert _abi.moe_read_device_status(bufs.fwd_ws) == 0
+    if backward:
+        assert _abi.moe_read_device_status(bufs.bwd_ws) == 0
+    return res
+
+
+@pytest.mark.parametrize("name", list(MX_SHAPES))
+def test_mxfp8_forward_backward_parity(name):
+    """Forward and backward in MXFP8 mode vs the oracle's MXFP8 emulation
+    (every operand of the routed experts' GEMMs rounded through MXFP8 along
+    its reduction axis), and measurably farther from the full-precision
+    oracle: the kernels do quantize."""
+    shape = MX_SHAPES[name]
+    r = _run_mx(shape, seed=MX_SEEDS.get(name, 0))
+    inp = r["inp_cpu"]
+    fwd = oracle_forward(inp, shape.k, mxfp8=True)
+    assert topk_gap(fwd["logits"], shape.k).min() > 1e-4, "seeded input has a near-tie"
+    assert order_gap(fwd["logits"], shape.k).min() > 1e-5
+    bwd = oracle_backward(inp, fwd)
+    e_y = rel_err(r["y"], fwd["y"])
+    assert e_y <= TOL_MX, e_y
+    assert rel_err(r["dx"], bwd["dx"]) <= TOL_MX
+    g = r["grads"]
+    for key in ["dW_gate", "dW_up", "dW_down", "dW_router", "d_topk_w"]:
+        assert rel_err(g[key], bwd[key]) <= TOL_MX, key
+    if shape.n_shared:
+        for key in ["dWs_gate", "dWs_up", "dWs_down"]:
+            assert rel_err(g[key], bwd[key]) <= TOL_MX, key
+    if shape.zero_experts:
+        for e in range(shape.E - shape.zero_experts, shape.E):
+            assert fwd["counts"][e] == 0
+            for key in ["dW_gate", "dW_up", "dW_down", "dW_router"]:
+                assert (g[key][e] == 0).all(), (key, e)
+    full = oracle_forward(inp, shape.k, mxfp8=False)
+    assert e_y < 0.5 * rel_err(r["y"], full["y"])
+
+
+def test_mxfp8_inference_matches_training_forward_and_is_deterministic(monkeypatch):
+    shape = MX_SHAPES["mx_ragged"]
+    a = _run_mx(shape, seed=4, backward=False)
+    b = _run_mx(shape, seed=4, backward=True)
+    assert torch.equal(a["y"], b["y"])
+    monkeypatch.setenv("MOE_GRID_LIMIT", "3")
+    c = _run_mx(shape, seed=4, backward=True)
+    assert torch.equal(b["y"], c["y"])
+    assert torch.equal(b["dx"], c["dx"])
+    for key in b["grads"]:
+        if b["grads"][key] is not None:
+            assert torch.equal(b["grads"][key], c["grads"][key]), key
+
+
+def test_mxfp8_forward_requires_quantized_weights():
+    shape = MX_SHAPES["mx_small"]
+    inp = _cuda(make_inputs(shape, seed=0, with_dy=False))
+    cfg = _abi.make_config(shape.T, shape.d, shape.I, shape.E, shape.k, shape.n_shared, shape.I_shared,
+                           precision=_abi.MOE_MXFP8)
+    bufs = layer.MoEBuffers(cfg, training=False)
+    with pytest.raises(_abi.MoeError) as ei:
+        layer.forward(cfg, inp, bufs)
+    assert ei.value.code == 1
