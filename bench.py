@@ -1,7 +1,7 @@
 """Benchmark of the MoE layer hot path (forward + backward) through the C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload dsv3|qwen3|tiny]
+                    [--workload dsv3|qwen3|tiny|dsv3_mxfp8]
 
 One step = forward + backward of the whole layer on one batch of seeded
 synthetic input of the workload (default: the DeepSeek-V3-shaped layer,
@@ -14,6 +14,11 @@ the timed region is bracketed by barriers and the slowest rank's time counts.
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead
 (bounded sample per step) and prints the same metric with "impl": "reference".
+
+dsv3_mxfp8 runs the same layer with the routed experts in MXFP8.  Its weights
+are quantized once per weight update (moe_quantize_weights_mxfp8); that pass is
+timed on its own and reported as "weight_quant", together with the throughput
+of a step that includes it.
 """
 from __future__ import annotations
 
@@ -33,6 +38,10 @@ if ROOT not in sys.path:
 METRIC = "MoE layer tokens/s and TFLOPS (fwd, fwd+bwd) at 1 GB300, % of tensor peak"
 
 
+# Nominal dense FP8 (and MXFP8) / BF16 tensor rate ratio (4.5 vs 2.25 PFLOP/s).
+FP8_OVER_BF16 = 2.0
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -43,20 +52,31 @@ def _peaks():
         return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
 
 
+def _tensor_peaks(peaks, mxfp8):
+    """(burst, sustained, label) tensor peaks for the routed GEMMs' dtype."""
+    if not mxfp8:
+        return peaks["bf16"], peaks["bf16_sustained"], peaks["src"] + " bf16"
+    return (peaks["bf16"] * FP8_OVER_BF16, peaks["bf16_sustained"] * FP8_OVER_BF16,
+            peaks["src"] + f" bf16 x nominal mxfp8/bf16 ratio {FP8_OVER_BF16:g}")
+
+
 def _workload(name, tokens=0, experts=0):
+    """(shape, description, mxfp8) of a named workload."""
     import dataclasses
 
     from synth.inputs import CONFIGS
-    s = CONFIGS[name]
+    s = CONFIGS["dsv3" if name == "dsv3_mxfp8" else name]
     desc = {
         "dsv3": "DSV3-shaped BF16 MoE layer forward+backward",
         "qwen3": "Qwen3-235B-shaped BF16 MoE layer forward+backward (Zipf-skewed routing)",
         "tiny": "tiny BF16 MoE layer forward+backward",
+        "dsv3_mxfp8": "DSV3-shaped MXFP8 MoE layer forward+backward (routed experts MXFP8, "
+                      "router and shared expert BF16, BF16 outputs)",
     }[name]
     if tokens or experts:  # scaled-down variant (profiling captures)
         s = dataclasses.replace(s, T=tokens or s.T, E=experts or s.E)
         desc += f" (scaled: T={s.T}, E={s.E})"
-    return s, desc
+    return s, desc, name == "dsv3_mxfp8"
 
 
 def _flops(s):
@@ -157,7 +177,7 @@ def _lazy_experts(t):
     return Lazy()
 
 
-def _oracle_step(inp, s, tokens):
+def _oracle_step(inp, s, tokens, mxfp8=False):
     """The CPU oracle's forward + backward on a token sample (test infrastructure,
     used only for the reported CPU baseline)."""
     import torch
@@ -171,7 +191,7 @@ def _oracle_step(inp, s, tokens):
     sh = {}
     if s.n_shared:
         sh = dict(ws_gate=f(inp["Ws_gate"]), ws_up=f(inp["Ws_up"]), ws_down=f(inp["Ws_down"]))
-    fwd = O.moe_forward(x, wr, wg, wu, wd, s.k, router_bias=bias, **sh)
+    fwd = O.moe_forward(x, wr, wg, wu, wd, s.k, router_bias=bias, mxfp8=mxfp8, **sh)
     O.moe_backward(x, wr, wg, wu, wd, dy, fwd, dense_expert_grads=False, **sh)
 
 
@@ -182,7 +202,7 @@ def _cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(inp, s, n_tokens, rounds, seed=1):
+def cpu_baseline(inp, s, n_tokens, rounds, seed=1, mxfp8=False):
     """Oracle forward+backward on `rounds` independent random samples of
     `n_tokens` tokens each (each round upcasts only the experts its tokens
     touch, which bounds host memory)."""
@@ -192,11 +212,12 @@ def cpu_baseline(inp, s, n_tokens, rounds, seed=1):
     for _ in range(rounds):
         tokens = torch.randperm(s.T, generator=g)[:n_tokens].sort().values.to(inp["x"].device)
         t0 = time.perf_counter()
-        _oracle_step(inp, s, tokens)
+        _oracle_step(inp, s, tokens, mxfp8)
         dt += time.perf_counter() - t0
     n = n_tokens * rounds
     return {"value": n / dt, "unit": "tokens/s", "cores": _cpu_cores(), "kind": "oracle",
-            "sample": f"float64 numpy oracle forward+backward, {rounds} rounds of {n_tokens} random tokens "
+            "sample": f"float64 numpy oracle forward+backward{' (MXFP8 emulation)' if mxfp8 else ''}, "
+                      f"{rounds} rounds of {n_tokens} random tokens "
                       f"of the same workload ({n} tokens, expert weights upcast on first use per round), "
                       f"{dt:.1f} s; numpy BLAS default threading"}
 
@@ -208,16 +229,16 @@ def run_reference(args):
     if rank != 0:
         return 0
     from synth.inputs import make_inputs
-    s, desc = _workload(args.workload, args.tokens, args.experts)
+    s, desc, mx = _workload(args.workload, args.tokens, args.experts)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = make_inputs(s, seed=0, device=dev)
     per_step = args.ref_tokens
     g = torch.Generator().manual_seed(1)
     for _ in range(args.warmup):
-        _oracle_step(inp, s, torch.randperm(s.T, generator=g)[:per_step].sort().values.to(dev))
+        _oracle_step(inp, s, torch.randperm(s.T, generator=g)[:per_step].sort().values.to(dev), mx)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_step(inp, s, torch.randperm(s.T, generator=g)[:per_step].sort().values.to(dev))
+        _oracle_step(inp, s, torch.randperm(s.T, generator=g)[:per_step].sort().values.to(dev), mx)
     dt = (time.perf_counter() - t0) / args.steps
     value = per_step / dt
     line = {
@@ -241,13 +262,15 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="dsv3", choices=["dsv3", "qwen3", "tiny"])
+    ap.add_argument("--workload", default="dsv3", choices=["dsv3", "qwen3", "tiny", "dsv3_mxfp8"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (scaled-down profiling runs)")
     ap.add_argument("--experts", type=int, default=0, help="override E (scaled-down profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=4, help="oracle tokens per cpu_baseline round (0 = skip)")
     ap.add_argument("--cpu-rounds", type=int, default=4, help="cpu_baseline rounds")
     ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per reference step")
+    ap.add_argument("--cpu-mx", action="store_true",
+                    help="also time the MXFP8 oracle for dsv3_mxfp8 (about 11 min per token)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -278,9 +301,12 @@ def main():
         return float(t.item())
 
     _abi.load()
-    s, desc = _workload(args.workload, args.tokens, args.experts)
+    s, desc, mx = _workload(args.workload, args.tokens, args.experts)
     inp = make_inputs(s, seed=rank, device="cuda")
-    cfg = _abi.make_config(s.T, s.d, s.I, s.E, s.k, s.n_shared, s.I_shared)
+    cfg = _abi.make_config(s.T, s.d, s.I, s.E, s.k, s.n_shared, s.I_shared,
+                           precision=_abi.MOE_MXFP8 if mx else _abi.MOE_BF16)
+    if mx:
+        layer.quantize_weights(cfg, inp)
     bufs = layer.MoEBuffers(cfg)
     grads = layer.alloc_grads(cfg)
     y = torch.empty(s.T, s.d, dtype=torch.bfloat16, device="cuda")
@@ -325,9 +351,18 @@ def main():
         layer.forward(cfg, inp, bufs, y)
     ms_fwd = max_over_ranks(timed(lambda: layer.forward(cfg, inp, bufs, y), args.steps))
 
+    wq = None
+    if mx:  # the once-per-weight-update quantization pass, timed on its own
+        ms_wq = max_over_ranks(timed(lambda: layer.quantize_weights(cfg, inp), args.steps))
+
     tokens = s.T * world
     flops_tok = _flops(s)
     peaks = _peaks()
+    t_burst, t_sust, t_src = _tensor_peaks(peaks, mx)
+    if mx:
+        wq = {"ms": ms_wq, "per": "weight update",
+              "value_incl": tokens / ((ms + ms_wq) * 1e-3), "unit": "tokens/s",
+              "note": "fwd+bwd step plus one weight quantization pass"}
     value = tokens / (ms * 1e-3)
     tflops = value * 3 * flops_tok / 1e12
     fwd_value = tokens / (ms_fwd * 1e-3)
@@ -343,10 +378,10 @@ def main():
         achieved = fl / (ms_top / n_top * 1e-3) / 1e12
         traffic = NCU_TRAFFIC.get((args.workload, top)) if not (args.tokens or args.experts) else None
         roofline = {"kernel": top, "bound": "tensor", "achieved": achieved,
-                    "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                    "frac": achieved / peaks["bf16_sustained"], "traffic": traffic,
+                    "peak": t_sust, "unit": "TFLOP/s",
+                    "frac": achieved / t_sust, "traffic": traffic,
                     "algorithmic_flops_per_launch": fl,
-                    "peak_src": peaks["src"] + " bf16 sustained (kernel timed inside a long step)"}
+                    "peak_src": t_src + " sustained (kernel timed inside a long step)"}
 
     e2e = None
     if not args.no_e2e:
@@ -375,19 +410,27 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_tokens > 0:
-        cpu = cpu_baseline(inp, s, args.cpu_tokens, args.cpu_rounds)
+        if mx and not args.cpu_mx:
+            # The MXFP8 oracle round-trips every expert weight it touches
+            # (about 15 s per [2048, 7168] matrix on one core, 48 per token).
+            cpu = {"value": None, "unit": "tokens/s", "cores": _cpu_cores(), "kind": "oracle",
+                   "sample": "not timed by default: the MXFP8 oracle takes about 11 min per token "
+                             "(--cpu-mx --cpu-tokens 1 --cpu-rounds 1 times one token)"}
+        else:
+            cpu = cpu_baseline(inp, s, args.cpu_tokens, args.cpu_rounds, mxfp8=mx)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "mxfp8" if mx else "bf16", "data": "synthetic",
             "config": {"workload": desc, "T": s.T, "d": s.d, "I": s.I, "E": s.E, "top_k": s.k,
                        "n_shared": s.n_shared, "I_shared": s.I_shared, "tokens_per_gpu": s.T,
                        "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (x 235 MB, expert weights 22.6 GB at dsv3); no flush"},
-            "tflops": tflops, "pct_bf16_peak": tflops / peaks["bf16"],
-            "pct_bf16_peak_sustained": tflops / peaks["bf16_sustained"],
+            "tflops": tflops, "pct_tensor_peak": tflops / t_burst,
+            "pct_tensor_peak_sustained": tflops / t_sust, "tensor_peak_src": t_src,
+            "weight_quant": wq,
             "fwd": {"value": fwd_value, "unit": "tokens/s", "ms": ms_fwd,
                     "tflops": fwd_value * flops_tok / 1e12},
             "roofline": roofline,
