@@ -244,7 +244,7 @@ def bf16_round(v):
     the nearest bfloat16 (8-bit significand), ties to the even significand --
     the value a float32 computation leaves after a bfloat16 store.  Used only
     where an MXFP8 quantization decision is taken on a stored bf16 tensor
-    (reading R12)."""
+    (reading R12: the saved a and b of the MXFP8 backward)."""
     f = np.ascontiguousarray(np.asarray(v, np.float64).astype(np.float32))
     u = f.view(np.uint32).astype(np.uint64)
     u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
@@ -327,8 +327,8 @@ def expert_backward(x_rows, dy_rows, g, a, b, h, w_gate_e, w_up_e, w_down_e, mxf
     the unquantized h and dh [Blog, "MXFP8 support", "Router weight gradient
     computation"].  Each quantization decision is taken on the value the
     layer holds at that point (reading R12): a and b as saved in bf16 (h is
-    recomputed from them); da and db unrounded for the dx operand; da, db and
-    g*h after their bf16 store for the weight-gradient operands.
+    recomputed from them); da, db and g*h unrounded, both for the dx operand
+    and for the weight-gradient operands.
     """
     x_rows, dy_rows = _f64(x_rows), _f64(dy_rows)
     wg, wu, wd = _f64(w_gate_e), _f64(w_up_e), _f64(w_down_e)
@@ -348,8 +348,7 @@ def expert_backward(x_rows, dy_rows, g, a, b, h, w_gate_e, w_up_e, w_down_e, mxf
     dadb = mx_round(np.concatenate([da, db], axis=1), axis=-1)
     wgu = mx_round(np.concatenate([wg, wu], axis=0), axis=0)
     xr = _mx_rows(x_rows)
-    da_s, db_s, hg_s = bf16_round(da), bf16_round(db), bf16_round(hg)
-    return (_mx_rows(da_s).T @ xr, _mx_rows(db_s).T @ xr, _mx_rows(dy_rows).T @ _mx_rows(hg_s), dg,
+    return (_mx_rows(da).T @ xr, _mx_rows(db).T @ xr, _mx_rows(dy_rows).T @ _mx_rows(hg), dg,
             dadb @ wgu)
 
 
