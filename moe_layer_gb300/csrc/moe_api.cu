@@ -47,16 +47,14 @@ enum ProfLabel : int {
   PL_DOWN_ROUTED, PL_DOWN_SHARED, PL_COMBINE, PL_DGRAD_DOWN_ROUTED, PL_DGRAD_DOWN_SHARED,
   PL_ROUTER_GRAD, PL_DGRAD_GATEUP_ROUTED, PL_DGRAD_GATEUP_SHARED, PL_UNPERMUTE, PL_ROUTER_WGRAD,
   PL_WGRAD_DOWN, PL_WGRAD_GATE, PL_WGRAD_UP, PL_WGRAD_SHARED_DOWN, PL_WGRAD_SHARED_GATE,
-  PL_WGRAD_SHARED_UP, PL_PERMUTE_DY, PL_MX_WEIGHTS, PL_MX_QUANT_X, PL_MX_QUANT_DY, PL_MX_TRANSPOSE,
-  PL_COUNT
+  PL_WGRAD_SHARED_UP, PL_PERMUTE_DY, PL_MX_WEIGHTS, PL_MX_QUANT_X, PL_MX_QUANT_DY, PL_COUNT
 };
 static const char* const kProfNames[PL_COUNT] = {
     "router_gemm", "topk_count", "chunk_scan", "scatter", "permute_x", "gateup_shared", "gateup_routed",
     "down_routed", "down_shared", "combine", "dgrad_down_routed", "dgrad_down_shared",
     "router_grad", "dgrad_gateup_routed", "dgrad_gateup_shared", "unpermute", "router_wgrad",
     "wgrad_down", "wgrad_gate", "wgrad_up", "wgrad_shared_down", "wgrad_shared_gate",
-    "wgrad_shared_up", "permute_dy", "mx_quantize_weights", "mx_permute_quant_x", "mx_permute_quant_dy",
-    "mx_transpose_quant"};
+    "wgrad_shared_up", "permute_dy", "mx_quantize_weights", "mx_permute_quant_x", "mx_permute_quant_dy"};
 
 struct ProfRecord {
   int label;
@@ -143,17 +141,21 @@ void carve_routing(Carver& c, const Shape& s, Routing& r) {
 
 struct Saved {
   Routing rt;
-  __nv_bfloat16* xp;   // [Rp, d] x rows in expert-grouped order
+  __nv_bfloat16* xp;   // [Rp, d] x rows in expert-grouped order (bf16 mode)
   __nv_bfloat16* ab;   // [Rp, 2I]
   __nv_bfloat16* abs;  // [T, 2Is]
+  uint8_t *xt, *xt_sf;  // MXFP8: the x rows transposed, quantized along the tokens [d, Rp]
 };
 void carve_saved(void* base, const Shape& s, Saved& v, size_t* bytes) {
   Carver c(base);
   c.take<char>(kAlign);
   carve_routing(c, s, v.rt);
-  v.xp = c.take<__nv_bfloat16>(s.Rp * s.d);
+  const int64_t m = s.mx ? 1 : 0;
+  v.xp = c.take<__nv_bfloat16>((1 - m) * s.Rp * s.d);
   v.ab = c.take<__nv_bfloat16>(s.Rp * 2 * s.I);
   v.abs = c.take<__nv_bfloat16>(s.S ? s.T * 2 * s.Is : 0);
+  v.xt = c.take<uint8_t>(m * s.Rp * s.d);
+  v.xt_sf = c.take<uint8_t>(m * mx_sf_alloc(s.d, s.Rp));
   if (bytes) *bytes = c.off;
 }
 
@@ -179,7 +181,7 @@ void carve_fwd(void* base, const Shape& s, FwdWs& w, size_t* bytes) {
   w.chunk_counts = c.take<int32_t>(s.nchunk * s.E);
   w.chunk_base = c.take<int32_t>(s.nchunk * s.E);
   carve_routing(c, s, w.rt);
-  w.xp = c.take<__nv_bfloat16>(s.Rp * s.d);
+  w.xp = c.take<__nv_bfloat16>(s.mx ? 0 : s.Rp * s.d);
   w.h = c.take<__nv_bfloat16>(s.mx ? 0 : s.Rp * s.I);
   w.hs = c.take<__nv_bfloat16>(s.S ? s.T * s.Is : 0);
   w.o = c.take<__nv_bfloat16>(s.Rp * s.d);
@@ -204,22 +206,22 @@ struct BwdWs {
   float* dl_row;         // [Rp]
   __nv_bfloat16* dxp;    // [Rp, d]
   __nv_bfloat16* dxs;    // [T, d]
-  // MXFP8: E4M3 codes + scales of the GEMM operands.  Row operands along
-  // their columns; the *_t ones are transposes (token rows become K, blocks
-  // of 32 tokens) for the weight gradients.
+  // MXFP8: E4M3 codes + scales of the GEMM operands: *q are the expert-grouped
+  // rows quantized along their columns (dgrad operands); *t are transposes
+  // quantized along the token rows (K-major weight-gradient operands).
   uint8_t *dyq, *dyq_sf;      // [Rp, d]
   uint8_t *dadbq, *dadbq_sf;  // [Rp, 2I]
-  uint8_t *dy_t, *dy_t_sf;    // [d, Rp]
-  uint8_t *hg_t, *hg_t_sf;    // [I, Rp]
-  uint8_t *dadb_t, *dadb_t_sf;  // [2I, Rp]
-  uint8_t *x_t, *x_t_sf;      // [d, Rp]
+  uint8_t *dyt, *dyt_sf;      // [d, Rp]
+  uint8_t *dadbt, *dadbt_sf;  // [2I, Rp]
+  uint8_t *hgt, *hgt_sf;      // [I, Rp]
 };
 void carve_bwd(void* base, const Shape& s, BwdWs& w, size_t* bytes) {
   Carver c(base);
   w.status = c.take<int>(kAlign / sizeof(int));
-  w.dyp = c.take<__nv_bfloat16>(s.Rp * s.d);
-  w.dadb = c.take<__nv_bfloat16>(s.Rp * 2 * s.I);
-  w.hg = c.take<__nv_bfloat16>(s.Rp * s.I);
+  const int64_t bf = s.mx ? 0 : 1;  // bf16 intermediates that MXFP8 mode does not keep
+  w.dyp = c.take<__nv_bfloat16>(bf * s.Rp * s.d);
+  w.dadb = c.take<__nv_bfloat16>(bf * s.Rp * 2 * s.I);
+  w.hg = c.take<__nv_bfloat16>(bf * s.Rp * s.I);
   w.dg_part = c.take<float>(s.Rp * s.nparts);
   w.dadbs = c.take<__nv_bfloat16>(s.S ? s.T * 2 * s.Is : 0);
   w.hs = c.take<__nv_bfloat16>(s.S ? s.T * s.Is : 0);
@@ -232,14 +234,12 @@ void carve_bwd(void* base, const Shape& s, BwdWs& w, size_t* bytes) {
   w.dyq_sf = c.take<uint8_t>(m * mx_sf_alloc(s.Rp, s.d));
   w.dadbq = c.take<uint8_t>(m * s.Rp * 2 * s.I);
   w.dadbq_sf = c.take<uint8_t>(m * mx_sf_alloc(s.Rp, 2 * s.I));
-  w.dy_t = c.take<uint8_t>(m * s.d * s.Rp);
-  w.dy_t_sf = c.take<uint8_t>(m * mx_sf_alloc(s.d, s.Rp));
-  w.hg_t = c.take<uint8_t>(m * s.I * s.Rp);
-  w.hg_t_sf = c.take<uint8_t>(m * mx_sf_alloc(s.I, s.Rp));
-  w.dadb_t = c.take<uint8_t>(m * 2 * s.I * s.Rp);
-  w.dadb_t_sf = c.take<uint8_t>(m * mx_sf_alloc(2 * s.I, s.Rp));
-  w.x_t = c.take<uint8_t>(m * s.d * s.Rp);
-  w.x_t_sf = c.take<uint8_t>(m * mx_sf_alloc(s.d, s.Rp));
+  w.dyt = c.take<uint8_t>(m * s.Rp * s.d);
+  w.dyt_sf = c.take<uint8_t>(m * mx_sf_alloc(s.d, s.Rp));
+  w.dadbt = c.take<uint8_t>(m * s.Rp * 2 * s.I);
+  w.dadbt_sf = c.take<uint8_t>(m * mx_sf_alloc(2 * s.I, s.Rp));
+  w.hgt = c.take<uint8_t>(m * s.Rp * s.I);
+  w.hgt_sf = c.take<uint8_t>(m * mx_sf_alloc(s.I, s.Rp));
   if (bytes) *bytes = c.off;
 }
 
@@ -320,7 +320,7 @@ moe_status tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, in
   return MOE_OK;
 }
 
-// E4M3 operand [rows, cols] (K = cols), boxes of 128 columns x box_rows.
+// E4M3 K-major operand [rows, cols] (K = cols), boxes of 128 columns x box_rows.
 moe_status qmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
   if (!make_tmap_u8(m, base, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
                     static_cast<uint32_t>(box_rows)))
@@ -450,8 +450,9 @@ moe_status forward_routed_mx(const Shape& s, const moe_weights* wts, const Routi
     p.N = I;
     p.K = d;
     p.b_group_rows = I;
-    if (sv) {
-      MOE_TRY(omap2(&p.tmO0, &p.tmO0h, sv->ab, s.Rp, 2 * s.I));
+    if (sv) {  // a and b rows kept for the backward (direct row stores)
+      p.out = sv->ab;
+      p.ldo = 2 * s.I;
       p.store_ab = 1;
     }
     p.I = I;
@@ -484,27 +485,20 @@ moe_status forward_routed_mx(const Shape& s, const moe_weights* wts, const Routi
 }
 
 // Weight gradients of the routed experts in MXFP8 mode.  Their reduction axis
-// is the token rows of each expert, so dy, g*h, [da | db] and x are first
-// transposed and quantized in blocks of 32 rows (expert groups start on
-// 128-row boundaries, so a block never mixes experts); then
+// is the token rows of each expert; the operands arrive transposed and
+// quantized along those rows (blocks of 32; expert groups start on 128-row
+// boundaries, so a block never mixes experts):
 //   dW_down[e] = dy^T (g h),  dW_gate[e] = da^T x,  dW_up[e] = db^T x
-// run as K-major block-scaled GEMMs over [row_start[e], row_start[e+1]).
+// as K-major block-scaled GEMMs over [row_start[e], row_start[e+1]).
 moe_status wgrad_routed_mx(const Shape& s, const Routing& rt, const Saved& sv, const BwdWs& w,
                            const moe_grads* g, cudaStream_t st) {
-  const int Rp = static_cast<int>(s.Rp), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
-  const int E = static_cast<int>(s.E);
-  const int32_t* used = rt.row_start + E;  // rows past the last group are never read
-  MOE_LAUNCH(PL_MX_TRANSPOSE, st, launch_mx_cols(w.dyp, d, 0, Rp, d, 1, w.dy_t, Rp, 0, 0, w.dy_t_sf, d, used, st));
-  MOE_LAUNCH(PL_MX_TRANSPOSE, st, launch_mx_cols(w.hg, I, 0, Rp, I, 1, w.hg_t, Rp, 0, 0, w.hg_t_sf, I, used, st));
-  MOE_LAUNCH(PL_MX_TRANSPOSE, st, launch_mx_cols(w.dadb, 2 * s.I, 0, Rp, 2 * I, 1, w.dadb_t, Rp, 0, 0, w.dadb_t_sf,
-                                                 2 * s.I, used, st));
-  MOE_LAUNCH(PL_MX_TRANSPOSE, st, launch_mx_cols(sv.xp, d, 0, Rp, d, 1, w.x_t, Rp, 0, 0, w.x_t_sf, d, used, st));
+  const int d = static_cast<int>(s.d), I = static_cast<int>(s.I), E = static_cast<int>(s.E);
   {
     GemmParams p;  // dW_down[e] = dy_rows^T . (g h)
     zero_params(p);
-    MOE_TRY(qmap(&p.tmA, w.dy_t, s.d, s.Rp, kBM));
-    MOE_TRY(qmap(&p.tmB0, w.hg_t, s.I, s.Rp, kBN));
-    set_mx_scales(p, w.dy_t_sf, s.d, w.hg_t_sf, nullptr, s.I);
+    MOE_TRY(qmap(&p.tmA, w.dyt, s.d, s.Rp, kBM));
+    MOE_TRY(qmap(&p.tmB0, w.hgt, s.I, s.Rp, kBN));
+    set_mx_scales(p, w.dyt_sf, s.d, w.hgt_sf, nullptr, s.I);
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.M_out = d;
@@ -516,9 +510,9 @@ moe_status wgrad_routed_mx(const Shape& s, const Routing& rt, const Saved& sv, c
   for (int half = 0; half < 2; ++half) {
     GemmParams p;  // dW_gate[e] = da^T . x_rows ; dW_up[e] = db^T . x_rows
     zero_params(p);
-    MOE_TRY(qmap(&p.tmA, w.dadb_t, 2 * s.I, s.Rp, kBM));
-    MOE_TRY(qmap(&p.tmB0, w.x_t, s.d, s.Rp, kBN));
-    set_mx_scales(p, w.dadb_t_sf, 2 * s.I, w.x_t_sf, nullptr, s.d);
+    MOE_TRY(qmap(&p.tmA, w.dadbt, 2 * s.I, s.Rp, kBM));
+    MOE_TRY(qmap(&p.tmB0, sv.xt, s.d, s.Rp, kBN));
+    set_mx_scales(p, w.dadbt_sf, 2 * s.I, sv.xt_sf, nullptr, s.d);
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.M_out = I;
@@ -578,14 +572,14 @@ moe_status moe_quantize_weights_mxfp8(const moe_config* cfg, const moe_weights* 
   const auto* Wu = static_cast<const __nv_bfloat16*>(w->W_up);
   const auto* Wd = static_cast<const __nv_bfloat16*>(w->W_down);
   const int d = static_cast<int>(s.d), I = static_cast<int>(s.I), E = static_cast<int>(s.E);
-  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_rows(Wg, d, nullptr, nullptr, s.E * s.I, d, m.wg, m.wg_sf, nullptr, st));
-  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_rows(Wu, d, nullptr, nullptr, s.E * s.I, d, m.wu, m.wu_sf, nullptr, st));
-  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_rows(Wd, I, nullptr, nullptr, s.E * s.d, I, m.wd, m.wd_sf, nullptr, st));
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_rows(Wg, d, s.E * s.I, d, m.wg, m.wg_sf, st));
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_rows(Wu, d, s.E * s.I, d, m.wu, m.wu_sf, st));
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_rows(Wd, I, s.E * s.d, I, m.wd, m.wd_sf, st));
   // W_down[e] is [d, I]: its transpose [I, d] quantized along d
-  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wd, I, s.d * s.I, d, I, E, m.wdt, d, I, 0, m.wdt_sf, s.E * s.I, nullptr, st));
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wd, I, s.d * s.I, d, I, E, m.wdt, d, I, 0, m.wdt_sf, s.E * s.I, st));
   // W_gate[e], W_up[e] are [I, d]: [W_gate; W_up]^T is [d, 2I], quantized along 2I
-  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wg, d, s.I * s.d, I, d, E, m.wgut, 2 * s.I, d, 0, m.wgut_sf, s.E * s.d, nullptr, st));
-  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wu, d, s.I * s.d, I, d, E, m.wgut, 2 * s.I, d, I, m.wgut_sf, s.E * s.d, nullptr, st));
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wg, d, s.I * s.d, I, d, E, m.wgut, 2 * s.I, d, 0, m.wgut_sf, s.E * s.d, st));
+  MOE_LAUNCH(PL_MX_WEIGHTS, st, launch_mx_cols(Wu, d, s.I * s.d, I, d, E, m.wgut, 2 * s.I, d, I, m.wgut_sf, s.E * s.d, st));
   return MOE_OK;
 }
 
@@ -640,10 +634,10 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
   // dispatch: x rows into expert-grouped order (zeros in padding rows); in
   // MXFP8 mode quantized on the way, the bf16 copy kept only for training
   __nv_bfloat16* xp = saved ? sv.xp : w.xp;
-  if (s.mx)
-    MOE_LAUNCH(PL_MX_QUANT_X, st, launch_mx_rows(static_cast<const __nv_bfloat16*>(x), d, rt.perm_token_pad,
-                                                 rt.row_start + E, s.Rp, d, w.xq, w.xq_sf,
-                                                 saved ? sv.xp : nullptr, st));
+  if (s.mx)  // along d for gate/up; in training also along the tokens for dW_gate, dW_up
+    MOE_LAUNCH(PL_MX_QUANT_X, st, launch_mx_permute_dual(static_cast<const __nv_bfloat16*>(x), d, rt.perm_token_pad,
+                                                         rt.row_start + E, s.Rp, d, w.xq, w.xq_sf,
+                                                         saved ? sv.xt : nullptr, saved ? sv.xt_sf : nullptr, st));
   else
     MOE_LAUNCH(PL_PERMUTE_X, st, launch_permute_rows(static_cast<const __nv_bfloat16*>(x), rt.perm_token_pad,
                                                     rt.row_start + E, static_cast<int>(s.Rp), d, xp, st));
@@ -760,9 +754,10 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
   if (s.mx) carve_mx(const_cast<void*>(wts->mxfp8), s, m, nullptr);
   // dy rows into expert-grouped order (zeros in padding rows); in MXFP8 mode
   // quantized on the way (the bf16 copy feeds the transposed quantization)
-  if (s.mx)
-    MOE_LAUNCH(PL_MX_QUANT_DY, st, launch_mx_rows(static_cast<const __nv_bfloat16*>(dy), d, rt.perm_token_pad,
-                                                  rt.row_start + E, s.Rp, d, w.dyq, w.dyq_sf, w.dyp, st));
+  if (s.mx)  // along d for the dgrad of down, along the tokens for dW_down
+    MOE_LAUNCH(PL_MX_QUANT_DY, st, launch_mx_permute_dual(static_cast<const __nv_bfloat16*>(dy), d, rt.perm_token_pad,
+                                                          rt.row_start + E, s.Rp, d, w.dyq, w.dyq_sf, w.dyt,
+                                                          w.dyt_sf, st));
   else
     MOE_LAUNCH(PL_PERMUTE_DY, st, launch_permute_rows(static_cast<const __nv_bfloat16*>(dy), rt.perm_token_pad,
                                                      rt.row_start + E, static_cast<int>(s.Rp), d, w.dyp, st));
@@ -781,16 +776,20 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.N = I;
     p.K = d;
     p.b_group_rows = I;
-    p.out = w.dadb;
-    p.ldo = 2 * s.I;
-    p.out2 = w.hg;
-    p.ldo2 = s.I;
     p.out3 = w.dg_part;
     p.ldo3 = static_cast<int>(s.nparts);
     p.ab = sv.ab;
     p.I = I;
     p.tile_start = rt.tile_start;
     p.row_scale = rt.perm_w_pad;
+    p.qt = w.dadbt;
+    p.qt_ld = s.Rp;
+    p.qt_sf = w.dadbt_sf;
+    p.qt_rb = cdiv(2 * s.I, 128);
+    p.qt2 = w.hgt;
+    p.qt2_ld = s.Rp;
+    p.qt2_sf = w.hgt_sf;
+    p.qt2_rb = cdiv(s.I, 128);
     p.qout = w.dadbq;
     p.qld = 2 * s.I;
     p.qsf = w.dadbq_sf;

@@ -58,13 +58,14 @@ cudaError_t launch_unpermute(const __nv_bfloat16* dxp, const __nv_bfloat16* dxs,
                              int k, __nv_bfloat16* dx, cudaStream_t st);
 
 // ---- MXFP8 quantization (mxfp8.cu)
-cudaError_t launch_mx_rows(const __nv_bfloat16* src, long long src_ld, const int32_t* idx,
-                           const int32_t* total_rows, int64_t R, int K, uint8_t* dst, uint8_t* sf,
-                           __nv_bfloat16* dst_bf16, cudaStream_t st);
+cudaError_t launch_mx_rows(const __nv_bfloat16* src, long long src_ld, int64_t R, int K, uint8_t* dst,
+                           uint8_t* sf, cudaStream_t st);
+cudaError_t launch_mx_permute_dual(const __nv_bfloat16* src, long long src_ld, const int32_t* idx,
+                                   const int32_t* total_rows, int64_t R, int K, uint8_t* rq, uint8_t* rq_sf,
+                                   uint8_t* tq, uint8_t* tq_sf, cudaStream_t st);
 cudaError_t launch_mx_cols(const __nv_bfloat16* src, long long src_ld, long long src_bstride, int rows,
                            int cols, int batch, uint8_t* dst, long long dst_ld, long long dst_brows,
-                           int k_off, uint8_t* sf, long long dst_rows_total, const int32_t* total_rows,
-                           cudaStream_t st);
+                           int k_off, uint8_t* sf, long long dst_rows_total, cudaStream_t st);
 // Bytes of the scale array of an MXFP8 operand with `rows` rows and K columns.
 inline size_t mx_sf_bytes(int64_t rows, int64_t K) {
   return static_cast<size_t>(((rows + 127) / 128) * (K / 128) * 512);
@@ -82,12 +83,12 @@ enum GemmKind : int {
   GK_DGRAD_DOWN,     // dy rows . W_down (MN-major), SwiGLU backward epilogue
   GK_DGRAD_GATEUP,   // [da|db] rows . [W_gate; W_up] (MN-major, two stacks along K)
   GK_WGRAD,          // A^T . B over a group's rows (both MN-major): weight gradients
-  // MXFP8 block-scaled forms (E4M3 operands, all K-major):
+  // MXFP8 block-scaled forms (E4M3 operands):
   GK_MX_GATEUP,       // x rows . [W_gate; W_up]^T, SwiGLU epilogue quantizing h
   GK_MX_DOWN,         // h rows . W_down^T, scaled by the router weight
   GK_MX_DGRAD_DOWN,   // dy rows . W_down (as W_down^T rows), SwiGLU backward quantizing [da|db]
   GK_MX_DGRAD_GATEUP, // [da|db] rows . [W_gate; W_up] (as its transpose's rows)
-  GK_MX_WGRAD,        // weight gradients from operands transposed to token-major K
+  GK_MX_WGRAD,        // weight gradients from transposes quantized along the tokens
   GK_COUNT
 };
 cudaError_t launch_gemm(GemmKind kind, const GemmParams& p, int grid, cudaStream_t st);

@@ -2,7 +2,6 @@
 // block scale rule X = 2^(floor(log2(amax)) - 8) and the tcgen05.cp scale
 // block layout.  Shared by the quantization kernels and the GEMM epilogues.
 #pragma once
-#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace moe {
@@ -24,21 +23,29 @@ __device__ __forceinline__ int mx_scale_exp(float amax) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
-__device__ __forceinline__ uint8_t to_e4m3(float v) {
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+// Two values to two E4M3 codes (round to nearest even, saturating to +-448):
+// `lo` in bits 0..7, `hi` in bits 8..15.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 2^-e for a block exponent e in [-127, 119] (exact, built from its bits;
+// a finite block maximum gives e <= 127 - 8).
+__device__ __forceinline__ float mx_inv_scale(int e) {
+  return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
 }
 
 // Quantizes 32 values with scale 2^e into 32 E4M3 bytes (two 16-byte words).
+// v * 2^-e is exact in fp32 whenever its magnitude is at least 2^-126; below
+// that the E4M3 code is zero either way.
 __device__ __forceinline__ void quant32(const float* v, int e, uint4& lo, uint4& hi) {
-  const float inv = ldexpf(1.0f, -e);  // exact power of two
+  const float inv = mx_inv_scale(e);
   uint32_t w[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    w[i] = static_cast<uint32_t>(to_e4m3(v[4 * i] * inv)) |
-           (static_cast<uint32_t>(to_e4m3(v[4 * i + 1] * inv)) << 8) |
-           (static_cast<uint32_t>(to_e4m3(v[4 * i + 2] * inv)) << 16) |
-           (static_cast<uint32_t>(to_e4m3(v[4 * i + 3] * inv)) << 24);
-  }
+  for (int i = 0; i < 8; ++i)
+    w[i] = e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) | (e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
   lo = make_uint4(w[0], w[1], w[2], w[3]);
   hi = make_uint4(w[4], w[5], w[6], w[7]);
 }
@@ -62,6 +69,11 @@ __device__ __forceinline__ uint32_t quant32_store(const float* v, uint8_t* dst) 
 __device__ __forceinline__ size_t sf_word_offset(int64_t row, int64_t kgroup, int64_t rblocks) {
   return static_cast<size_t>((kgroup * rblocks + row / 128) * 512 + 16 * (row % 32) +
                              4 * ((row % 128) / 32));
+}
+// Byte offset of the scale of (MN index mn, reduction index k) for an operand
+// whose MN extent is rblocks * 128.
+__device__ __forceinline__ size_t sf_byte_offset(int64_t mn, int64_t k, int64_t rblocks) {
+  return sf_word_offset(mn, k / 128, rblocks) + static_cast<size_t>((k % 128) / 32);
 }
 
 }  // namespace moe

@@ -20,52 +20,29 @@ namespace moe {
 
 namespace {
 
-// Row-wise quantization: dst row r = src row idx[r] (or row r when idx is
-// null; a negative index gives a zero row), blocks of 32 along the row.
-// Optionally also writes the (gathered) bf16 row to dst_bf16.  One group of
-// four threads per (row, 128-column group).
+// Row-wise quantization of a [R, K] bf16 matrix (row pitch src_ld), blocks
+// of 32 along the row.  One group of four threads per (row, 128-column group).
 constexpr int kQThreads = 256;
 __global__ void __launch_bounds__(kQThreads)
-    mx_rows_kernel(const __nv_bfloat16* __restrict__ src, long long src_ld, const int32_t* __restrict__ idx,
-                   const int32_t* __restrict__ total_rows, int64_t R, int K,
-                   uint8_t* __restrict__ dst, uint8_t* __restrict__ sf, __nv_bfloat16* __restrict__ dst_bf16) {
+    mx_rows_kernel(const __nv_bfloat16* __restrict__ src, long long src_ld, int64_t R, int K,
+                   uint8_t* __restrict__ dst, uint8_t* __restrict__ sf) {
   const int64_t ng = K / 128;
   const int64_t units = R * ng;
-  const int64_t rows_used = total_rows ? static_cast<int64_t>(__ldg(total_rows)) : R;
   for (int64_t u = (static_cast<int64_t>(blockIdx.x) * kQThreads + threadIdx.x) / 4; u < units;
        u += static_cast<int64_t>(gridDim.x) * kQThreads / 4) {
     const int64_t r = u / ng, g = u - r * ng;
-    if (r >= rows_used) continue;  // rows past the used total are never read
     const int j = threadIdx.x & 3;
     const int col = static_cast<int>(g * 128 + 32 * j);
     float v[32];
-    bool live = true;
-    int64_t srow = r;
-    if (idx && live) {
-      const int t = __ldg(idx + r);
-      live = t >= 0;
-      srow = t;
-    }
-    if (live) {
-      const uint4* s4 = reinterpret_cast<const uint4*>(src + srow * src_ld + col);
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + r * src_ld + col);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 w = __ldg(s4 + q);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = __ldg(s4 + q);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[8 * q + 2 * i] = bf16lo(ws[i]);
-          v[8 * q + 2 * i + 1] = bf16hi(ws[i]);
-        }
-        if (dst_bf16) reinterpret_cast<uint4*>(dst_bf16 + r * static_cast<int64_t>(K) + col)[q] = w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = 0.f;
-      if (dst_bf16) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          reinterpret_cast<uint4*>(dst_bf16 + r * static_cast<int64_t>(K) + col)[q] = make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < 4; ++i) {
+        v[8 * q + 2 * i] = bf16lo(ws[i]);
+        v[8 * q + 2 * i + 1] = bf16hi(ws[i]);
       }
     }
     float amax = 0.f;
@@ -77,14 +54,89 @@ __global__ void __launch_bounds__(kQThreads)
     uint4* d4 = reinterpret_cast<uint4*>(dst + r * static_cast<int64_t>(K) + col);
     d4[0] = lo;
     d4[1] = hi;
-    // the four scale codes of this (row, 128-column group) form one word; only
-    // the group's four lanes take part (other groups of the warp may have left
-    // the loop)
-    const unsigned gmask = 0xFu << (threadIdx.x & 28u);
+    // the four scale codes of this (row, 128-column group) form one word
     uint32_t code = static_cast<uint32_t>(e + 127) << (8 * j);
-    code |= __shfl_xor_sync(gmask, code, 1);
-    code |= __shfl_xor_sync(gmask, code, 2);
+    code |= __shfl_xor_sync(0xffffffffu, code, 1);
+    code |= __shfl_xor_sync(0xffffffffu, code, 2);
     if (j == 0) *reinterpret_cast<uint32_t*>(sf + sf_word_offset(r, g, (R + 127) / 128)) = code;
+  }
+}
+
+// Dispatch with quantization: dst row r is src row idx[r] (a zero row for a
+// negative index); rows from *total_rows on are left alone.  Writes up to two
+// MXFP8 copies of the gathered [R, K] matrix:
+//   rq  [R, K], blocks of 32 columns (operand of the GEMMs that reduce over K);
+//   tq  [K, R], the transpose, blocks of 32 consecutive rows of the gathered
+//       matrix (operand of the weight gradients, whose reduction axis is the
+//       rows; groups start on 128-row boundaries, so a block never mixes
+//       experts); skipped when tq is null.
+// Block: one 128 x 128 tile (R and K multiples of 128), 256 threads; the bf16
+// tile sits in shared memory so that both quantizations read it along their
+// own axis.
+constexpr int kDualTile = 128;
+constexpr int kDualPitch = kDualTile + 8;  // bf16 elements per shared row (16-byte aligned rows)
+__global__ void __launch_bounds__(kQThreads)
+    mx_permute_dual_kernel(const __nv_bfloat16* __restrict__ src, long long src_ld,
+                           const int32_t* __restrict__ idx, const int32_t* __restrict__ total_rows,
+                           int64_t R, int K, uint8_t* __restrict__ rq, uint8_t* __restrict__ rq_sf,
+                           uint8_t* __restrict__ tq, uint8_t* __restrict__ tq_sf) {
+  __shared__ __align__(16) uint16_t tile[kDualTile][kDualPitch];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kDualTile;
+  const int c0 = blockIdx.x * kDualTile;
+  if (r0 >= (total_rows ? static_cast<int64_t>(__ldg(total_rows)) : R)) return;
+  // gather: 16 threads per row, 16 bytes each
+  for (int i = threadIdx.x; i < kDualTile * 16; i += kQThreads) {
+    const int r = i >> 4, q = i & 15;
+    const int64_t srow = idx ? static_cast<int64_t>(__ldg(idx + r0 + r)) : r0 + r;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (srow >= 0) w = __ldg(reinterpret_cast<const uint4*>(src + srow * src_ld + c0) + q);
+    *reinterpret_cast<uint4*>(&tile[r][8 * q]) = w;
+  }
+  __syncthreads();
+  {  // along the row: thread -> (row, 64-column half), two blocks of 32
+    const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
+    uint32_t word = 0;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      float v[32], amax = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = *reinterpret_cast<const uint4*>(&tile[r][64 * half + 32 * b + 8 * q]);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[8 * q + 2 * k] = bf16lo(ws[k]);
+          v[8 * q + 2 * k + 1] = bf16hi(ws[k]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      const int e = mx_scale_exp(amax);
+      uint4 lo, hi;
+      quant32(v, e, lo, hi);
+      uint4* d4 = reinterpret_cast<uint4*>(rq + (r0 + r) * K + c0 + 64 * half + 32 * b);
+      d4[0] = lo;
+      d4[1] = hi;
+      word |= static_cast<uint32_t>(e + 127) << (8 * (2 * half + b));
+    }
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    if (half == 0) *reinterpret_cast<uint32_t*>(rq_sf + sf_word_offset(r0 + r, c0 / 128, (R + 127) / 128)) = word;
+  }
+  if (!tq) return;
+  {  // along the rows: thread -> (column pair, 32-row block)
+    const int pc = threadIdx.x & 63, tb = threadIdx.x >> 6;
+    float v0[32], v1[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[32 * tb + i][2 * pc]);
+      v0[i] = bf16lo(w);
+      v1[i] = bf16hi(w);
+    }
+    const int64_t c = c0 + 2 * pc;
+    const uint32_t s0 = quant32_store(v0, tq + c * R + r0 + 32 * tb);
+    const uint32_t s1 = quant32_store(v1, tq + (c + 1) * R + r0 + 32 * tb);
+    tq_sf[sf_byte_offset(c, r0 + 32 * tb, K / 128)] = static_cast<uint8_t>(s0);
+    tq_sf[sf_byte_offset(c + 1, r0 + 32 * tb, K / 128)] = static_cast<uint8_t>(s1);
   }
 }
 
@@ -92,16 +144,13 @@ __global__ void __launch_bounds__(kQThreads)
 // a GEMM whose reduction axis is `rows`.  Writes dst[c, k_off + r] (row pitch
 // dst_ld, K-major for the GEMM) with blocks of 32 along r.  blockIdx.z walks a
 // batch of such matrices (per expert): src += z * src_bstride, dst row offset
-// += z * dst_brows.  Tile: 128 rows x 64 columns per block.  When total_rows
-// is given, source rows from *total_rows on are neither read nor written
-// (whole 128-row tiles; *total_rows is a multiple of 128 there).
+// += z * dst_brows.  Tile: 128 rows x 64 columns per block.
 __global__ void __launch_bounds__(kQThreads)
     mx_cols_kernel(const __nv_bfloat16* __restrict__ src, long long src_ld, long long src_bstride, int rows,
                    int cols, uint8_t* __restrict__ dst, long long dst_ld, long long dst_brows, int k_off,
-                   uint8_t* __restrict__ sf, long long dst_rows_total, const int32_t* __restrict__ total_rows) {
+                   uint8_t* __restrict__ sf, long long dst_rows_total) {
   __shared__ float tile[128][65];
   const int r0 = blockIdx.y * 128, c0 = blockIdx.x * 64;
-  if (total_rows && r0 >= __ldg(total_rows)) return;
   const __nv_bfloat16* s = src + static_cast<long long>(blockIdx.z) * src_bstride;
   // coalesced load: each warp reads rows, 64 columns = 128 bytes per row
   for (int i = threadIdx.x; i < 128 * 32; i += kQThreads) {
@@ -144,26 +193,33 @@ __global__ void __launch_bounds__(kQThreads)
 
 }  // namespace
 
-cudaError_t launch_mx_rows(const __nv_bfloat16* src, long long src_ld, const int32_t* idx,
-                           const int32_t* total_rows, int64_t R, int K, uint8_t* dst, uint8_t* sf,
-                           __nv_bfloat16* dst_bf16, cudaStream_t st) {
+cudaError_t launch_mx_rows(const __nv_bfloat16* src, long long src_ld, int64_t R, int K, uint8_t* dst,
+                           uint8_t* sf, cudaStream_t st) {
   if (R <= 0) return cudaSuccess;
   const int64_t units = R * (K / 128);
   int64_t blocks = (units * 4 + kQThreads - 1) / kQThreads;
   if (blocks > 65535LL * 16) blocks = 65535LL * 16;
-  mx_rows_kernel<<<static_cast<unsigned>(blocks), kQThreads, 0, st>>>(src, src_ld, idx, total_rows, R, K,
-                                                                      dst, sf, dst_bf16);
+  mx_rows_kernel<<<static_cast<unsigned>(blocks), kQThreads, 0, st>>>(src, src_ld, R, K, dst, sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_permute_dual(const __nv_bfloat16* src, long long src_ld, const int32_t* idx,
+                                   const int32_t* total_rows, int64_t R, int K, uint8_t* rq, uint8_t* rq_sf,
+                                   uint8_t* tq, uint8_t* tq_sf, cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  if (K % kDualTile || R % kDualTile) return cudaErrorInvalidValue;
+  dim3 grid(K / kDualTile, static_cast<unsigned>(R / kDualTile));
+  mx_permute_dual_kernel<<<grid, kQThreads, 0, st>>>(src, src_ld, idx, total_rows, R, K, rq, rq_sf, tq, tq_sf);
   return cudaGetLastError();
 }
 
 cudaError_t launch_mx_cols(const __nv_bfloat16* src, long long src_ld, long long src_bstride, int rows,
                            int cols, int batch, uint8_t* dst, long long dst_ld, long long dst_brows,
-                           int k_off, uint8_t* sf, long long dst_rows_total, const int32_t* total_rows,
-                           cudaStream_t st) {
+                           int k_off, uint8_t* sf, long long dst_rows_total, cudaStream_t st) {
   if (rows <= 0 || cols <= 0 || batch <= 0) return cudaSuccess;
   dim3 grid((cols + 63) / 64, (rows + 127) / 128, batch);
   mx_cols_kernel<<<grid, kQThreads, 0, st>>>(src, src_ld, src_bstride, rows, cols, dst, dst_ld, dst_brows,
-                                             k_off, sf, dst_rows_total, total_rows);
+                                             k_off, sf, dst_rows_total);
   return cudaGetLastError();
 }
 

@@ -60,18 +60,21 @@ constexpr int kGemmThreads = 256;
 constexpr int kStageBoxBytes = 32 * 128;   // one epilogue staging box: 32 rows x 128 bytes
 
 // Epilogue staging: per epilogue warp two 4 KB boxes (bf16 mode) that TMA
-// stores to global memory while the next box is being filled; one box in
-// MXFP8 mode, whose scale stages use the rest of shared memory.
+// stores to global memory while the next box is being filled; in MXFP8 mode,
+// whose scale stages use part of shared memory, one box, or the 32 x 33 fp32
+// transpose buffer of the SwiGLU backward, in 5 KB per warp.
 template <bool MX>
 __host__ __device__ constexpr int epi_slots() { return MX ? 1 : 2; }
+template <bool MX>
+__host__ __device__ constexpr int epi_warp_bytes() { return MX ? 5 * 1024 : 2 * 32 * 128; }
 template <bool MX>
 __host__ __device__ constexpr int acc_bufs() { return MX ? 1 : 2; }
 template <bool MX>
 __host__ __device__ constexpr int stage_k() { return MX ? kBKmx : kBK; }
 template <bool MX>
 __host__ __device__ constexpr int gemm_smem_bytes_for() {
-  return 1024 + kStages * kStageBytes + (MX ? kStages * kSfStageBytes : 0) +
-         4 * epi_slots<MX>() * kStageBoxBytes + 256;
+  return 1024 + kStages * kStageBytes + (MX ? kStages * kSfStageBytes : 0) + 4 * epi_warp_bytes<MX>() +
+         256;
 }
 constexpr int kGemmSmemBytes = gemm_smem_bytes_for<false>();
 
@@ -126,12 +129,24 @@ struct GemmParams {
   const __nv_bfloat16* ab;
   int I;
   int store_ab;
-  // MXFP8 quantized epilogue output (E4M3 rows + scales): h for
-  // EPI_SWIGLU_FWD, [da|db] for EPI_SWIGLU_BWD; null when not wanted.
+  // MXFP8 quantized epilogue output (E4M3 rows + scales), required in MXFP8
+  // mode: h for EPI_SWIGLU_FWD (whose a and b rows then go to `out` when
+  // store_ab), [da|db] for EPI_SWIGLU_BWD.
   uint8_t* qout;
   long long qld;
   uint8_t* qsf;
   long long q_rb;
+  // MXFP8 EPI_SWIGLU_BWD: the transposes [da|db]^T ([2I, rows]) and (g*h)^T
+  // ([I, rows]) quantized along the token rows (blocks of 32), the K-major
+  // operands of the weight gradients.  These replace the bf16 out / out2.
+  uint8_t* qt;
+  long long qt_ld;
+  uint8_t* qt_sf;
+  long long qt_rb;
+  uint8_t* qt2;
+  long long qt2_ld;
+  uint8_t* qt2_sf;
+  long long qt2_rb;
   int* status;
 };
 
@@ -278,7 +293,7 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
       // ---- A operand
       if constexpr (AM == A_K_TILE) {
         if (lane == 0) tma_load_2d(sA, &p.tmA, kabs, arow, full);
-      } else {  // A_MN_TILE: both 64-column chunks with one 3-D box
+      } else {  // A_MN_TILE (bf16): both 64-column chunks with one 3-D box
         if (lane == 0) tma_load_3d(sA, &p.tmA, 0, kabs, (p.a_col_off + t.m0) / 64, full);
       }
       // ---- B operand
@@ -372,6 +387,8 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
         tc_cp_32x128b(sfa_t, sfs);
         tc_cp_32x128b(sfa_t + 8, sfs + 512);
         tc_cp_32x128b(sfa_t + 12, sfs + 1024);
+        // both operands K-major: K = 32 is 32 bytes along the swizzled row
+        static_assert(!a_mn && !b_mn, "MXFP8 operands are K-major");
 #pragma unroll
         for (int kk = 0; kk < kBKmx / 32; ++kk) {
           tc_mma_mxf8(d_tmem, smem_desc_sw128(sA + kk * 32, 16, 1024),
@@ -454,23 +471,31 @@ struct EpiStager {
   }
 };
 
-template <int EPI, int SCH, bool MX>
+template <int EPI, int SCH>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf0, uint32_t acce0,
                                               uint32_t tmem_base, uint32_t s_staging, int num_tiles,
                                               volatile int* abort_flag, int warp_e, int lane) {
-  constexpr int BK = stage_k<MX>();
   int acc = 0;
   uint32_t aph = 0;
-  EpiStager<epi_slots<MX>()> stg{
-      s_staging + static_cast<uint32_t>(warp_e) * epi_slots<MX>() * kStageBoxBytes, 0, lane};
+  EpiStager<2> stg{s_staging + static_cast<uint32_t>(warp_e) * 2 * kStageBoxBytes, 0, lane};
   for (int tau = blockIdx.x; tau < num_tiles; tau += gridDim.x) {
-    const TileInfo t = gemm_tile<EPI, SCH, BK>(p, tau);
+    const TileInfo t = gemm_tile<EPI, SCH, kBK>(p, tau);
     // Tile row held by this thread's TMEM lane: lane l of warp w is row 32w + l
     // of an M=128 accumulator; an M=64 accumulator keeps rows 16w..16w+15 in
     // lanes 0..15 of each warp (lanes 16..31 hold nothing of this tile).
     const int wrows = t.m64 ? 16 : 32;
     const bool lane_ok = lane < wrows;
     const int row = warp_e * wrows + lane;
+    if constexpr (EPI == EPI_SWIGLU_BWD) {  // the saved a, b of this tile's rows: into L2 while the MMAs run
+      if (lane_ok && row < t.rows_valid) {
+        const char* ar = reinterpret_cast<const char*>(p.ab + (static_cast<long long>(t.row0) + row) * (2LL * p.I) + t.n0);
+        const int lines = min(kBN, p.N - t.n0) / 64;
+        for (int q = 0; q < lines; ++q) {
+          prefetch_l2(ar + 128 * q);
+          prefetch_l2(ar + 2LL * p.I + 128 * q);
+        }
+      }
+    }
     const bool ok = mbar_wait(accf0 + 8 * acc, aph, abort_flag, p.status);
     if (!__all_sync(0xffffffffu, ok)) break;
     tc_fence_after();
@@ -518,11 +543,6 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
           }
         }
       } else if constexpr (EPI == EPI_SWIGLU_FWD) {
-        // quantized h (MXFP8): the tile's 128 h columns are one 128-column
-        // group, so each row's four block scales form one word
-        const bool q_out = MX && p.qout != nullptr;
-        const bool q_in_mem = q_out && lane_ok;
-        uint32_t qword = 0;
         for (int c0 = 0; c0 < kBN / 2 && t.n0 + c0 < p.N; c0 += 64) {
           float a[64], b[64];
           tmem_ld32(tr + c0, a);
@@ -543,20 +563,8 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
           }
 #pragma unroll
           for (int i = 0; i < 64; ++i) a[i] = a[i] * sigmoidf_(a[i]) * b[i];
-          if (q_out) {
-            if constexpr (MX) {
-              if (q_in_mem) {
-                uint8_t* q = p.qout + grow * p.qld + t.n0 + c0;
-                qword |= quant32_store(a, q) << (8 * (c0 / 32));
-                qword |= quant32_store(a + 32, q + 32) << (8 * (c0 / 32 + 1));
-              }
-            }
-          } else {
-            stg.row64_2d(o1, a, t.n0 + c0, r0);
-          }
+          stg.row64_2d(o1, a, t.n0 + c0, r0);
         }
-        if (MX && q_in_mem)
-          *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, t.n0 / 128, p.q_rb)) = qword;
       } else if constexpr (EPI == EPI_BF16) {
         float scale = 1.f;
         if (p.row_scale && p.dense_rows == 0 && lane_ok) scale = __ldg(p.row_scale + grow);
@@ -571,8 +579,6 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
           stg.row64_2d(o0, v, t.n0 + c0, r0);
         }
       } else {  // EPI_SWIGLU_BWD: direct row stores; a long K loop hides this epilogue
-        // columns per step: 16, or 32 in MXFP8 mode (one scale block of da and db)
-        constexpr int CW = MX ? 32 : 16;
         const bool in_mem = p.dense_rows > 0 ? real : lane_ok;
         __nv_bfloat16* dadb = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
         __nv_bfloat16* hg = reinterpret_cast<__nv_bfloat16*>(p.out2) + grow * p.ldo2;
@@ -580,60 +586,38 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
         float g = 1.f;
         if (in_mem && real && p.row_scale) g = __ldg(p.row_scale + grow);
         float dgp = 0.f;
-        uint32_t wa = 0, wb = 0;  // MXFP8: scale words of da and db for the current 128 columns
-        for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += CW) {
-          float dh[CW];
-          if constexpr (CW == 32) {
-            tmem_ld32(tr + c0, dh);
-          } else {
-            tmem_ld16(tr + c0, dh);
-          }
+        for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 16) {
+          float dh[16];
+          tmem_ld16(tr + c0, dh);
           tmem_ld_wait();
           if (in_mem) {
-            float da[CW], db[CW], hv[CW];
+            float da[16], db[16], hv[16];
+            if (real) {
+              float a[16], b[16];
+              load_bf16x16(abr + t.n0 + c0, a);
+              load_bf16x16(abr + p.I + t.n0 + c0, b);
 #pragma unroll
-            for (int h16 = 0; h16 < CW / 16; ++h16) {
-              if (real) {
-                float a[16], b[16];
-                load_bf16x16(abr + t.n0 + c0 + 16 * h16, a);
-                load_bf16x16(abr + p.I + t.n0 + c0 + 16 * h16, b);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  const float sg = sigmoidf_(a[i]);
-                  const float silu = a[i] * sg;
-                  const float hh = silu * b[i];
-                  const float d = dh[16 * h16 + i];
-                  dgp += d * hh;
-                  const float dhs = g * d;
-                  da[16 * h16 + i] = dhs * b[i] * sg * (1.f + a[i] * (1.f - sg));
-                  db[16 * h16 + i] = dhs * silu;
-                  hv[16 * h16 + i] = g * hh;
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  da[16 * h16 + i] = 0.f;
-                  db[16 * h16 + i] = 0.f;
-                  hv[16 * h16 + i] = 0.f;
-                }
+              for (int i = 0; i < 16; ++i) {
+                const float sg = sigmoidf_(a[i]);
+                const float silu = a[i] * sg;
+                const float hh = silu * b[i];
+                dgp += dh[i] * hh;
+                const float dhs = g * dh[i];
+                da[i] = dhs * b[i] * sg * (1.f + a[i] * (1.f - sg));
+                db[i] = dhs * silu;
+                hv[i] = g * hh;
               }
-              store_bf16x16(dadb + t.n0 + c0 + 16 * h16, *reinterpret_cast<const float(*)[16]>(da + 16 * h16));
-              store_bf16x16(dadb + p.I + t.n0 + c0 + 16 * h16, *reinterpret_cast<const float(*)[16]>(db + 16 * h16));
-              store_bf16x16(hg + t.n0 + c0 + 16 * h16, *reinterpret_cast<const float(*)[16]>(hv + 16 * h16));
-            }
-            if constexpr (MX) {
-              if (p.qout) {
-                const int col = t.n0 + c0, j = (col / 32) & 3;
-                wa |= quant32_store(da, p.qout + grow * p.qld + col) << (8 * j);
-                wb |= quant32_store(db, p.qout + grow * p.qld + p.I + col) << (8 * j);
-                if (j == 3) {
-                  *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, col / 128, p.q_rb)) = wa;
-                  *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, (p.I + col) / 128, p.q_rb)) = wb;
-                  wa = 0;
-                  wb = 0;
-                }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                da[i] = 0.f;
+                db[i] = 0.f;
+                hv[i] = 0.f;
               }
             }
+            store_bf16x16(dadb + t.n0 + c0, da);
+            store_bf16x16(dadb + p.I + t.n0 + c0, db);
+            store_bf16x16(hg + t.n0 + c0, hv);
           }
         }
         if (in_mem && p.out3) p.out3[grow * p.ldo3 + t.nt] = real ? dgp : 0.f;
@@ -642,9 +626,252 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(acce0 + 8 * acc);
-    if (++acc == acc_bufs<MX>()) {
+    if (++acc == 2) {
       acc = 0;
       aph ^= 1;
+    }
+  }
+  // every TMA store of this warp has finished before the CTA may exit
+  if (lane == 0) bulk_wait_group<0>();
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ MXFP8 epilogue
+// In MXFP8 mode the scale ring leaves room for only one 256-column
+// accumulator.  So that the next tile's MMAs need not wait for the whole
+// epilogue, each warp first copies 192 of the accumulator columns into spare
+// TMEM columns (the stash), handles the other 64 straight from the
+// accumulator, releases the accumulator, and finishes from the stash while the
+// tensor cores already work on the next tile.
+constexpr uint32_t kStashCol = kSfTmemCol + kStages * kSfTmemStride;
+constexpr int kStashCols = 192;
+static_assert(kStashCol + kStashCols <= static_cast<uint32_t>(kTmemCols), "TMEM budget");
+
+// Stores 32 floats of a row as bf16 (64 bytes, 16-byte aligned).
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v) {
+  store_bf16x16(dst, *reinterpret_cast<const float(*)[16]>(v));
+  store_bf16x16(dst + 16, *reinterpret_cast<const float(*)[16]>(v + 16));
+}
+
+// Quantization along the token rows of a 32-column chunk held one row per
+// lane (v[i] = this lane's value in column i): the warp transposes it through
+// its 32 x 33 fp32 buffer, then lane c quantizes column c (32 tokens, one MX
+// block) into 32 bytes at dst + c * ld.  Returns the E8M0 code of column c.
+__device__ __forceinline__ uint32_t quant32_tok(const float* v, float* buf, uint8_t* dst, long long ld,
+                                                int lane) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) buf[lane * 33 + i] = v[i];
+  __syncwarp();
+  float c[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) c[r] = buf[r * 33 + lane];
+  __syncwarp();
+  return quant32_store(c, dst + lane * ld);
+}
+
+template <int EPI, int SCH>
+__device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t accf0, uint32_t acce0,
+                                                 uint32_t tmem_base, uint32_t s_staging, uint8_t* warp_smem,
+                                                 int num_tiles, volatile int* abort_flag, int warp_e, int lane) {
+  static_assert(EPI != EPI_F32_BIAS, "no fp32 epilogue in MXFP8 mode");
+  uint32_t aph = 0;
+  EpiStager<1> stg{s_staging + static_cast<uint32_t>(warp_e * epi_warp_bytes<true>()), 0, lane};
+  const uint32_t lane_off = static_cast<uint32_t>(warp_e * 32) << 16;
+  const uint32_t acc = tmem_base + lane_off;
+  const uint32_t stash = tmem_base + lane_off + kStashCol;
+  const int row = warp_e * 32 + lane;  // MXFP8 groups are 128-row aligned: no 64-row tiles
+  for (int tau = blockIdx.x; tau < num_tiles; tau += gridDim.x) {
+    const TileInfo t = gemm_tile<EPI, SCH, kBKmx>(p, tau);
+    if constexpr (EPI == EPI_SWIGLU_BWD) {  // the saved a, b of this tile's rows: into L2 while the MMAs run
+      if (row < t.rows_valid) {
+        const char* ar = reinterpret_cast<const char*>(p.ab + (static_cast<long long>(t.row0) + row) * (2LL * p.I) + t.n0);
+        const int lines = min(kBN, p.N - t.n0) / 64;
+        for (int q = 0; q < lines; ++q) {
+          prefetch_l2(ar + 128 * q);
+          prefetch_l2(ar + 2LL * p.I + 128 * q);
+        }
+      }
+    }
+    const bool ok = mbar_wait(accf0, aph, abort_flag, p.status);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    tc_fence_after();
+    auto release = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0);
+      aph ^= 1;
+    };
+
+    if constexpr (EPI == EPI_BF16) {
+      const bool have = SCH == SCHED_WGRAD ? t.nkb > 0 : true;
+      float scale = 1.f;
+      int r0;
+      if constexpr (SCH == SCHED_WGRAD) {
+        r0 = t.m0 + warp_e * 32;
+      } else {
+        r0 = t.row0 + warp_e * 32;
+        if (p.row_scale && p.dense_rows == 0) scale = __ldg(p.row_scale + t.row0 + row);
+        if (row >= t.rows_valid) scale = 0.f;
+      }
+      auto emit64 = [&](int c0, float* v) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) v[i] *= scale;
+        const uint32_t box = stg.begin();
+        stage_row_sw128(box, lane, v);
+        if (SCH == SCHED_WGRAD && p.dense_rows == 0)
+          stg.store3d(&p.tmO0, box, t.n0 + c0, r0, t.e);
+        else
+          stg.store2d(&p.tmO0, box, t.n0 + c0, r0);
+      };
+      if (have) {
+        for (int c = 0; c < kStashCols && t.n0 + c < p.N; c += 32) tmem_copy32(stash + c, acc + c);
+        tmem_st_wait();
+      }
+      float v[64];
+      const bool tail = t.n0 + kStashCols < p.N;
+      if (tail && have) {
+        tmem_ld32(acc + kStashCols, v);
+        tmem_ld32(acc + kStashCols + 32, v + 32);
+        tmem_ld_wait();
+      }
+      release();
+      if (tail) {
+        if (!have) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) v[i] = 0.f;
+        }
+        emit64(kStashCols, v);
+      }
+      for (int c0 = 0; c0 < kStashCols && t.n0 + c0 < p.N; c0 += 64) {
+        if (have) {
+          tmem_ld32(stash + c0, v);
+          tmem_ld32(stash + c0 + 32, v + 32);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) v[i] = 0.f;
+        }
+        emit64(c0, v);
+      }
+    } else if constexpr (EPI == EPI_SWIGLU_FWD) {
+      // accumulator: gate columns 0..127, up columns 128..255 of the tile's 128
+      // h columns; stash: gate 0..95 -> +0, up 0..95 -> +96; h columns 96..127
+      // are done before the release
+      const bool real = row < t.rows_valid;
+      const long long grow = static_cast<long long>(t.row0) + row;
+      __nv_bfloat16* abw = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * p.ldo;
+      uint32_t qword = 0;
+      auto chunk = [&](int j, float* a, float* b) {  // h columns 32j..32j+31 of the tile
+        if (!real) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            a[i] = 0.f;
+            b[i] = 0.f;
+          }
+        }
+        if (p.store_ab) {
+          store_bf16x32(abw + t.n0 + 32 * j, a);
+          store_bf16x32(abw + p.I + t.n0 + 32 * j, b);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[i] = a[i] * sigmoidf_(a[i]) * b[i];
+        qword |= quant32_store(a, p.qout + grow * p.qld + t.n0 + 32 * j) << (8 * j);
+      };
+      for (int j = 0; j < 3; ++j) {
+        tmem_copy32(stash + 32 * j, acc + 32 * j);
+        tmem_copy32(stash + 96 + 32 * j, acc + kBN / 2 + 32 * j);
+      }
+      tmem_st_wait();
+      float a[32], b[32];
+      tmem_ld32(acc + 96, a);
+      tmem_ld32(acc + kBN / 2 + 96, b);
+      tmem_ld_wait();
+      release();
+      chunk(3, a, b);
+      for (int j = 0; j < 3; ++j) {
+        tmem_ld32(stash + 32 * j, a);
+        tmem_ld32(stash + 96 + 32 * j, b);
+        tmem_ld_wait();
+        chunk(j, a, b);
+      }
+      *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, t.n0 / 128, p.q_rb)) = qword;
+    } else {  // EPI_SWIGLU_BWD
+      // da, db quantized along the columns for the dgrad of gate/up (qout), and
+      // da, db, g*h quantized along the token rows for the weight gradients
+      // (qt, qt2): the warp's 32 lanes are 32 consecutive rows of one expert
+      const bool real = row < t.rows_valid;
+      const long long grow = static_cast<long long>(t.row0) + row;
+      const long long tok0 = static_cast<long long>(t.row0) + warp_e * 32;  // first row of the warp's block
+      const __nv_bfloat16* abr = p.ab + grow * (2LL * p.I);
+      const float g = (real && p.row_scale) ? __ldg(p.row_scale + grow) : 1.f;
+      float dgp = 0.f;
+      uint32_t wa[2] = {0, 0}, wb[2] = {0, 0};  // column-quant scale words of da and db per 128 columns
+      auto chunk = [&](int c0, const float* dh) {  // tile columns c0..c0+31
+        float da[32], db[32], hv[32];
+#pragma unroll
+        for (int h16 = 0; h16 < 2; ++h16) {
+          if (real) {
+            float a[16], b[16];
+            load_bf16x16(abr + t.n0 + c0 + 16 * h16, a);
+            load_bf16x16(abr + p.I + t.n0 + c0 + 16 * h16, b);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float sg = sigmoidf_(a[i]);
+              const float silu = a[i] * sg;
+              const float hh = silu * b[i];
+              const float d = dh[16 * h16 + i];
+              dgp += d * hh;
+              const float dhs = g * d;
+              da[16 * h16 + i] = dhs * b[i] * sg * (1.f + a[i] * (1.f - sg));
+              db[16 * h16 + i] = dhs * silu;
+              hv[16 * h16 + i] = g * hh;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              da[16 * h16 + i] = 0.f;
+              db[16 * h16 + i] = 0.f;
+              hv[16 * h16 + i] = 0.f;
+            }
+          }
+        }
+        const int col = t.n0 + c0;
+        const int j = (c0 / 32) & 3, q = c0 / 128;
+        wa[q] |= quant32_store(da, p.qout + grow * p.qld + col) << (8 * j);
+        wb[q] |= quant32_store(db, p.qout + grow * p.qld + p.I + col) << (8 * j);
+        float* buf = reinterpret_cast<float*>(warp_smem);
+        const uint32_t sa = quant32_tok(da, buf, p.qt + col * p.qt_ld + tok0, p.qt_ld, lane);
+        const uint32_t sb = quant32_tok(db, buf, p.qt + (p.I + col) * p.qt_ld + tok0, p.qt_ld, lane);
+        const uint32_t sh = quant32_tok(hv, buf, p.qt2 + col * p.qt2_ld + tok0, p.qt2_ld, lane);
+        p.qt_sf[sf_byte_offset(col + lane, tok0, p.qt_rb)] = static_cast<uint8_t>(sa);
+        p.qt_sf[sf_byte_offset(p.I + col + lane, tok0, p.qt_rb)] = static_cast<uint8_t>(sb);
+        p.qt2_sf[sf_byte_offset(col + lane, tok0, p.qt2_rb)] = static_cast<uint8_t>(sh);
+      };
+      for (int c = 0; c < kStashCols && t.n0 + c < p.N; c += 32) tmem_copy32(stash + c, acc + c);
+      tmem_st_wait();
+      float dh[2][32];
+      const bool tail = t.n0 + kStashCols < p.N;
+      if (tail) {
+        tmem_ld32(acc + kStashCols, dh[0]);
+        tmem_ld32(acc + kStashCols + 32, dh[1]);
+        tmem_ld_wait();
+      }
+      release();
+      if (tail) {
+        chunk(kStashCols, dh[0]);
+        chunk(kStashCols + 32, dh[1]);
+      }
+      for (int c0 = 0; c0 < kStashCols && t.n0 + c0 < p.N; c0 += 32) {
+        tmem_ld32(stash + c0, dh[0]);
+        tmem_ld_wait();
+        chunk(c0, dh[0]);
+      }
+      for (int q = 0; q < 2 && t.n0 + 128 * q < p.N; ++q) {
+        const int col = t.n0 + 128 * q;
+        *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, col / 128, p.q_rb)) = wa[q];
+        *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, (p.I + col) / 128, p.q_rb)) = wb[q];
+      }
+      if (p.out3) p.out3[grow * p.ldo3 + t.nt] = real ? dgp : 0.f;
     }
   }
   // every TMA store of this warp has finished before the CTA may exit
@@ -659,7 +886,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   constexpr int kSfBytes = MX ? kStages * kSfStageBytes : 0;
-  constexpr int kStagingBytes = 4 * epi_slots<MX>() * kStageBoxBytes;
+  constexpr int kStagingBytes = 4 * epi_warp_bytes<MX>();
   const uint32_t s_tiles = smem_u32(smem);
   const uint32_t s_staging = s_tiles + kStages * kStageBytes;
   const uint32_t s_sf = s_staging + kStagingBytes;
@@ -691,11 +918,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     tma_prefetch_desc(&p.tmB0);
     if (BMO == B_K_DUAL_N || BMO == B_MN_DUAL_K) tma_prefetch_desc(&p.tmB1);
     // only the output maps this launch stores through (the others may be unset)
-    if (EPI == EPI_BF16 || (EPI == EPI_SWIGLU_FWD && (p.store_ab || p.qout == nullptr))) {
+    if (EPI == EPI_BF16 || (EPI == EPI_SWIGLU_FWD && !MX)) {
       tma_prefetch_desc(&p.tmO0);
-      if (SCH == SCHED_ROWS) tma_prefetch_desc(&p.tmO0h);
+      if (SCH == SCHED_ROWS && !MX) tma_prefetch_desc(&p.tmO0h);
     }
-    if (EPI == EPI_SWIGLU_FWD && p.qout == nullptr) {
+    if (EPI == EPI_SWIGLU_FWD && !MX) {
       tma_prefetch_desc(&p.tmO1);
       tma_prefetch_desc(&p.tmO1h);
     }
@@ -717,8 +944,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
       gemm_mma<AM, BMO, EPI, SCH, MX>(p, s_tiles, s_sf, full0, empty0, accf0, acce0, drain,
                                       tmem_base, num_tiles, abort_flag);
   } else if (warp >= 4) {
-    gemm_epilogue<EPI, SCH, MX>(p, accf0, acce0, tmem_base, s_staging, num_tiles, abort_flag,
-                                warp - 4, lane);
+    if constexpr (MX)
+      gemm_epilogue_mx<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging,
+                                 smem + kStages * kStageBytes + (warp - 4) * epi_warp_bytes<MX>(), num_tiles,
+                                 abort_flag, warp - 4, lane);
+    else
+      gemm_epilogue<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging, num_tiles, abort_flag, warp - 4,
+                              lane);
   }
   tc_fence_before();
   __syncthreads();
