@@ -15,14 +15,15 @@ cudaError_t launch_gemm_inst(const GemmParams& p, int grid, cudaStream_t st) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   auto kfn = tc_gemm_kernel<AM, BMO, EPI, SCH, MX>;
-  constexpr int smem = gemm_smem_bytes_for<MX>();
+  constexpr int smem = gemm_smem_bytes_for<MX, EPI>();
+  constexpr int threads = gemm_threads<MX, EPI>();
   const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
   if (bit == 0 || !(configured.load() & bit)) {
     e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  kfn<<<grid, kGemmThreads, smem, st>>>(p);
+  kfn<<<grid, threads, smem, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -293,7 +293,9 @@ moe_status check_config(const moe_config* cfg, Shape& s) {
   s.Rp = s.R + s.E * (s.ra - 1);
   if (s.mx) s.Rp = (s.Rp + kRowAlignMx - 1) / kRowAlignMx * kRowAlignMx;  // whole scale blocks
   s.nchunk = (s.T + kChunkTokens - 1) / kChunkTokens;
-  s.nparts = (s.I + kBN - 1) / kBN;
+  // router-weight gradient partials per row: one per n-tile of the SwiGLU
+  // backward (two in MXFP8 mode, whose epilogue splits a tile's columns)
+  s.nparts = (s.mx ? 2 : 1) * ((s.I + kBN - 1) / kBN);
   const int64_t lim = (int64_t(1) << 31) - 1;
   if (s.Rp >= lim || s.T >= lim || s.d >= lim || s.I * s.E >= lim || s.d * s.E >= lim)
     return MOE_ERR_UNSUPPORTED;
@@ -476,7 +478,7 @@ moe_status forward_routed_mx(const Shape& s, const moe_weights* wts, const Routi
     p.N = d;
     p.K = I;
     p.b_group_rows = d;
-    MOE_TRY(omap2(&p.tmO0, &p.tmO0h, w.o, s.Rp, s.d));
+    MOE_TRY(omap(&p.tmO0, w.o, s.Rp, s.d));
     p.row_scale = rt.perm_w_pad;
     p.status = w.status;
     MOE_LAUNCH(PL_DOWN_ROUTED, st, launch_gemm(GK_MX_DOWN, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
@@ -852,7 +854,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.N = d;
     p.K = 2 * I;
     p.b_group_rows = d;
-    MOE_TRY(omap2(&p.tmO0, &p.tmO0h, w.dxp, s.Rp, s.d));
+    MOE_TRY(omap(&p.tmO0, w.dxp, s.Rp, s.d));
     p.tile_start = rt.tile_start;
     p.status = w.status;
     MOE_LAUNCH(PL_DGRAD_GATEUP_ROUTED, st, launch_gemm(GK_MX_DGRAD_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));

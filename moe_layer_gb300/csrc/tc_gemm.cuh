@@ -43,6 +43,11 @@
 
 namespace moe {
 
+enum AMode : int { A_K_TILE = 0, A_MN_TILE = 1 };
+enum BMode : int { B_K_TILE = 0, B_K_DUAL_N = 1, B_MN_TILE = 2, B_MN_DUAL_K = 3 };
+enum EpiMode : int { EPI_F32_BIAS = 0, EPI_SWIGLU_FWD = 1, EPI_BF16 = 2, EPI_SWIGLU_BWD = 3 };
+enum SchedMode : int { SCHED_ROWS = 0, SCHED_WGRAD = 1 };
+
 constexpr int kBM = 128;  // rows per tile (TMEM lanes)
 constexpr int kBN = 256;  // accumulator columns per tile
 constexpr int kBK = 64;   // bf16 K per stage: one 128-byte swizzle row
@@ -56,32 +61,39 @@ constexpr int kSfTmemCol = 256;            // MXFP8: first TMEM column of the sc
 constexpr int kSfTmemStride = 16;          // MXFP8: columns per stage (A at +0, B at +8)
 constexpr int kMNChunkBytes = kBK * 128;   // one 64-wide MN chunk of an MN-major tile
 constexpr int kTmemCols = 512;
-constexpr int kGemmThreads = 256;
+constexpr int kGemmThreads = 256;  // warps 0-3 roles (TMA, MMA, TMEM allocation, idle), 4-7 epilogue
 constexpr int kStageBoxBytes = 32 * 128;   // one epilogue staging box: 32 rows x 128 bytes
 
-// Epilogue staging: per epilogue warp two 4 KB boxes (bf16 mode) that TMA
-// stores to global memory while the next box is being filled; in MXFP8 mode,
-// whose scale stages use part of shared memory, one box, or the 32 x 33 fp32
-// transpose buffer of the SwiGLU backward, in 5 KB per warp.
-template <bool MX>
-__host__ __device__ constexpr int epi_slots() { return MX ? 1 : 2; }
-template <bool MX>
-__host__ __device__ constexpr int epi_warp_bytes() { return MX ? 5 * 1024 : 2 * 32 * 128; }
+// Epilogue warps.  One per TMEM lane quadrant (warps 4-7), except for the
+// MXFP8 SwiGLU backward, whose heavy epilogue gets two per quadrant (warps
+// 2-9, 320 threads; the TMEM allocator, warp 2, is one of them).
+template <bool MX, int EPI>
+__host__ __device__ constexpr bool epi_wide() { return MX && EPI == EPI_SWIGLU_BWD; }
+template <bool MX, int EPI>
+__host__ __device__ constexpr int epi_warps() { return epi_wide<MX, EPI>() ? 8 : 4; }
+template <bool MX, int EPI>
+__host__ __device__ constexpr int first_epi_warp() { return epi_wide<MX, EPI>() ? 2 : 4; }
+template <bool MX, int EPI>
+__host__ __device__ constexpr int gemm_threads() { return 32 * (first_epi_warp<MX, EPI>() + epi_warps<MX, EPI>()); }
+// Epilogue shared memory per epilogue warp: in bf16 mode two 4 KB staging
+// boxes that TMA stores to global memory while the next box is being filled;
+// in MXFP8 mode, whose scale stages use part of shared memory, one box (in 5 KB),
+// or for the SwiGLU backward the 32 x 17 fp32 transpose buffer.
+template <bool MX, int EPI>
+__host__ __device__ constexpr int epi_warp_bytes() {
+  return !MX ? 2 * 32 * 128 : (epi_wide<MX, EPI>() ? 32 * 17 * 4 : 5 * 1024);
+}
 template <bool MX>
 __host__ __device__ constexpr int acc_bufs() { return MX ? 1 : 2; }
 template <bool MX>
 __host__ __device__ constexpr int stage_k() { return MX ? kBKmx : kBK; }
-template <bool MX>
+template <bool MX, int EPI>
 __host__ __device__ constexpr int gemm_smem_bytes_for() {
-  return 1024 + kStages * kStageBytes + (MX ? kStages * kSfStageBytes : 0) + 4 * epi_warp_bytes<MX>() +
-         256;
+  return 1024 + kStages * kStageBytes + (MX ? kStages * kSfStageBytes : 0) +
+         epi_warps<MX, EPI>() * epi_warp_bytes<MX, EPI>() + 256;
 }
-constexpr int kGemmSmemBytes = gemm_smem_bytes_for<false>();
+constexpr int kGemmSmemBytes = gemm_smem_bytes_for<false, 0>();
 
-enum AMode : int { A_K_TILE = 0, A_MN_TILE = 1 };
-enum BMode : int { B_K_TILE = 0, B_K_DUAL_N = 1, B_MN_TILE = 2, B_MN_DUAL_K = 3 };
-enum EpiMode : int { EPI_F32_BIAS = 0, EPI_SWIGLU_FWD = 1, EPI_BF16 = 2, EPI_SWIGLU_BWD = 3 };
-enum SchedMode : int { SCHED_ROWS = 0, SCHED_WGRAD = 1 };
 
 struct GemmParams {
   // Operand maps: K-major operands are 2-D [rows, K] maps with 128-byte x rows
@@ -637,12 +649,14 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
 }
 
 // ------------------------------------------------------------------ MXFP8 epilogue
-// In MXFP8 mode the scale ring leaves room for only one 256-column
-// accumulator.  So that the next tile's MMAs need not wait for the whole
-// epilogue, each warp first copies 192 of the accumulator columns into spare
-// TMEM columns (the stash), handles the other 64 straight from the
-// accumulator, releases the accumulator, and finishes from the stash while the
-// tensor cores already work on the next tile.
+// MXFP8 mode has one 256-column accumulator: the scale ring takes the other
+// TMEM columns.  So that the next tile's MMAs need not wait for the whole
+// epilogue, each warp first copies three quarters of its accumulator columns
+// into spare TMEM columns (the stash), loads the last quarter, releases the
+// accumulator and finishes from the stash while the tensor cores work on the
+// next tile.  One epilogue warp per TMEM lane quadrant handles all 256
+// columns, except in the SwiGLU backward, where two warps per quadrant split
+// them (quad = warp index mod 4, half = which 128 columns).
 constexpr uint32_t kStashCol = kSfTmemCol + kStages * kSfTmemStride;
 constexpr int kStashCols = 192;
 static_assert(kStashCol + kStashCols <= static_cast<uint32_t>(kTmemCols), "TMEM budget");
@@ -654,42 +668,63 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
 }
 
 // Quantization along the token rows of a 32-column chunk held one row per
-// lane (v[i] = this lane's value in column i): the warp transposes it through
-// its 32 x 33 fp32 buffer, then lane c quantizes column c (32 tokens, one MX
-// block) into 32 bytes at dst + c * ld.  Returns the E8M0 code of column c.
-__device__ __forceinline__ uint32_t quant32_tok(const float* v, float* buf, uint8_t* dst, long long ld,
-                                                int lane) {
+// lane (v[i] = this lane's value in column i; the warp's 32 lanes are 32
+// consecutive rows, one MX block).  The warp transposes 16 columns at a time
+// through its 32 x 17 fp32 buffer; lane (c, h) takes rows 16h..16h+15 of
+// column c, the two halves agree on the block maximum, and each writes 16
+// codes of the transpose's row: dst + (16 pass + c) * ld + 16 h.  The E8M0
+// code of chunk column j goes to sf[sf_off(j)].
+template <class SfOff>
+__device__ __forceinline__ void quant32_tok(const float* v, float* buf, uint8_t* dst, long long ld, uint8_t* sf,
+                                            SfOff sf_off, int lane) {
+  const int c = lane & 15, h = lane >> 4;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) buf[lane * 33 + i] = v[i];
-  __syncwarp();
-  float c[32];
+  for (int pass = 0; pass < 2; ++pass) {
 #pragma unroll
-  for (int r = 0; r < 32; ++r) c[r] = buf[r * 33 + lane];
-  __syncwarp();
-  return quant32_store(c, dst + lane * ld);
+    for (int i = 0; i < 16; ++i) buf[lane * 17 + i] = v[16 * pass + i];
+    __syncwarp();
+    float u[16], amax = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      u[r] = buf[(16 * h + r) * 17 + c];
+      amax = fmaxf(amax, fabsf(u[r]));
+    }
+    __syncwarp();
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+    const int e = mx_scale_exp(amax);
+    const float inv = mx_inv_scale(e);
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = e4m3x2(u[4 * i] * inv, u[4 * i + 1] * inv) | (e4m3x2(u[4 * i + 2] * inv, u[4 * i + 3] * inv) << 16);
+    *reinterpret_cast<uint4*>(dst + (16 * pass + c) * ld + 16 * h) = make_uint4(w[0], w[1], w[2], w[3]);
+    if (h == 0) sf[sf_off(16 * pass + c)] = static_cast<uint8_t>(e + 127);
+  }
 }
 
 template <int EPI, int SCH>
 __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t accf0, uint32_t acce0,
-                                                 uint32_t tmem_base, uint32_t s_staging, uint8_t* warp_smem,
-                                                 int num_tiles, volatile int* abort_flag, int warp_e, int lane) {
+                                                 uint32_t tmem_base, uint32_t s_warp, float* buf, int num_tiles,
+                                                 volatile int* abort_flag, int quad, int half, int lane) {
   static_assert(EPI != EPI_F32_BIAS, "no fp32 epilogue in MXFP8 mode");
   uint32_t aph = 0;
-  EpiStager<1> stg{s_staging + static_cast<uint32_t>(warp_e * epi_warp_bytes<true>()), 0, lane};
-  const uint32_t lane_off = static_cast<uint32_t>(warp_e * 32) << 16;
+  EpiStager<1> stg{s_warp, 0, lane};
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   const uint32_t acc = tmem_base + lane_off;
-  const uint32_t stash = tmem_base + lane_off + kStashCol;
-  const int row = warp_e * 32 + lane;  // MXFP8 groups are 128-row aligned: no 64-row tiles
+  // wide (SwiGLU backward): 96 stash columns per warp; otherwise 192
+  const uint32_t stash = tmem_base + lane_off + kStashCol + half * (kStashCols / 2);
+  const int row = quad * 32 + lane;  // MXFP8 groups are 128-row aligned: no 64-row tiles
+  const int warp_e = quad;
   for (int tau = blockIdx.x; tau < num_tiles; tau += gridDim.x) {
     const TileInfo t = gemm_tile<EPI, SCH, kBKmx>(p, tau);
-    if constexpr (EPI == EPI_SWIGLU_BWD) {  // the saved a, b of this tile's rows: into L2 while the MMAs run
-      if (row < t.rows_valid) {
-        const char* ar = reinterpret_cast<const char*>(p.ab + (static_cast<long long>(t.row0) + row) * (2LL * p.I) + t.n0);
-        const int lines = min(kBN, p.N - t.n0) / 64;
-        for (int q = 0; q < lines; ++q) {
-          prefetch_l2(ar + 128 * q);
-          prefetch_l2(ar + 2LL * p.I + 128 * q);
-        }
+    if constexpr (EPI == EPI_SWIGLU_BWD) {  // the saved a, b of this warp's rows and columns: into L2 now
+      const int c0 = t.n0 + 128 * half;
+      if (row < t.rows_valid && c0 < p.N) {
+        const char* ar = reinterpret_cast<const char*>(p.ab + (static_cast<long long>(t.row0) + row) * (2LL * p.I) + c0);
+        prefetch_l2(ar);
+        prefetch_l2(ar + 128);
+        prefetch_l2(ar + 2LL * p.I);
+        prefetch_l2(ar + 2LL * p.I + 128);
       }
     }
     const bool ok = mbar_wait(accf0, aph, abort_flag, p.status);
@@ -796,16 +831,18 @@ __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t a
       }
       *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, t.n0 / 128, p.q_rb)) = qword;
     } else {  // EPI_SWIGLU_BWD
-      // da, db quantized along the columns for the dgrad of gate/up (qout), and
-      // da, db, g*h quantized along the token rows for the weight gradients
-      // (qt, qt2): the warp's 32 lanes are 32 consecutive rows of one expert
+      // this warp: tile columns 128 half .. +127 (one 128-column scale group);
+      // da, db quantized along the columns for the dgrad of gate/up (qout),
+      // and da, db, g*h along the token rows for the weight gradients (qt, qt2)
+      const int cw = 128 * half;
+      const bool valid = t.n0 + cw < p.N;  // N is a multiple of 128
       const bool real = row < t.rows_valid;
       const long long grow = static_cast<long long>(t.row0) + row;
-      const long long tok0 = static_cast<long long>(t.row0) + warp_e * 32;  // first row of the warp's block
+      const long long tok0 = static_cast<long long>(t.row0) + quad * 32;  // first row of the warp's block
       const __nv_bfloat16* abr = p.ab + grow * (2LL * p.I);
       const float g = (real && p.row_scale) ? __ldg(p.row_scale + grow) : 1.f;
       float dgp = 0.f;
-      uint32_t wa[2] = {0, 0}, wb[2] = {0, 0};  // column-quant scale words of da and db per 128 columns
+      uint32_t wa = 0, wb = 0;  // column-quant scale words of da and db
       auto chunk = [&](int c0, const float* dh) {  // tile columns c0..c0+31
         float da[32], db[32], hv[32];
 #pragma unroll
@@ -836,42 +873,37 @@ __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t a
           }
         }
         const int col = t.n0 + c0;
-        const int j = (c0 / 32) & 3, q = c0 / 128;
-        wa[q] |= quant32_store(da, p.qout + grow * p.qld + col) << (8 * j);
-        wb[q] |= quant32_store(db, p.qout + grow * p.qld + p.I + col) << (8 * j);
-        float* buf = reinterpret_cast<float*>(warp_smem);
-        const uint32_t sa = quant32_tok(da, buf, p.qt + col * p.qt_ld + tok0, p.qt_ld, lane);
-        const uint32_t sb = quant32_tok(db, buf, p.qt + (p.I + col) * p.qt_ld + tok0, p.qt_ld, lane);
-        const uint32_t sh = quant32_tok(hv, buf, p.qt2 + col * p.qt2_ld + tok0, p.qt2_ld, lane);
-        p.qt_sf[sf_byte_offset(col + lane, tok0, p.qt_rb)] = static_cast<uint8_t>(sa);
-        p.qt_sf[sf_byte_offset(p.I + col + lane, tok0, p.qt_rb)] = static_cast<uint8_t>(sb);
-        p.qt2_sf[sf_byte_offset(col + lane, tok0, p.qt2_rb)] = static_cast<uint8_t>(sh);
+        const int j = (c0 / 32) & 3;
+        wa |= quant32_store(da, p.qout + grow * p.qld + col) << (8 * j);
+        wb |= quant32_store(db, p.qout + grow * p.qld + p.I + col) << (8 * j);
+        quant32_tok(da, buf, p.qt + col * p.qt_ld + tok0, p.qt_ld, p.qt_sf,
+                    [&](int jc) { return sf_byte_offset(col + jc, tok0, p.qt_rb); }, lane);
+        quant32_tok(db, buf, p.qt + (p.I + col) * p.qt_ld + tok0, p.qt_ld, p.qt_sf,
+                    [&](int jc) { return sf_byte_offset(p.I + col + jc, tok0, p.qt_rb); }, lane);
+        quant32_tok(hv, buf, p.qt2 + col * p.qt2_ld + tok0, p.qt2_ld, p.qt2_sf,
+                    [&](int jc) { return sf_byte_offset(col + jc, tok0, p.qt2_rb); }, lane);
       };
-      for (int c = 0; c < kStashCols && t.n0 + c < p.N; c += 32) tmem_copy32(stash + c, acc + c);
-      tmem_st_wait();
-      float dh[2][32];
-      const bool tail = t.n0 + kStashCols < p.N;
-      if (tail) {
-        tmem_ld32(acc + kStashCols, dh[0]);
-        tmem_ld32(acc + kStashCols + 32, dh[1]);
+      float dh[32];
+      if (valid) {
+        for (int j = 0; j < 3; ++j) tmem_copy32(stash + 32 * j, acc + cw + 32 * j);
+        tmem_st_wait();
+        tmem_ld32(acc + cw + 96, dh);
         tmem_ld_wait();
       }
       release();
-      if (tail) {
-        chunk(kStashCols, dh[0]);
-        chunk(kStashCols + 32, dh[1]);
+      if (valid) {
+        chunk(cw + 96, dh);
+        for (int j = 0; j < 3; ++j) {
+          tmem_ld32(stash + 32 * j, dh);
+          tmem_ld_wait();
+          chunk(cw + 32 * j, dh);
+        }
+        const int col = t.n0 + cw;
+        *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, col / 128, p.q_rb)) = wa;
+        *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, (p.I + col) / 128, p.q_rb)) = wb;
       }
-      for (int c0 = 0; c0 < kStashCols && t.n0 + c0 < p.N; c0 += 32) {
-        tmem_ld32(stash + c0, dh[0]);
-        tmem_ld_wait();
-        chunk(c0, dh[0]);
-      }
-      for (int q = 0; q < 2 && t.n0 + 128 * q < p.N; ++q) {
-        const int col = t.n0 + 128 * q;
-        *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, col / 128, p.q_rb)) = wa[q];
-        *reinterpret_cast<uint32_t*>(p.qsf + sf_word_offset(grow, (p.I + col) / 128, p.q_rb)) = wb[q];
-      }
-      if (p.out3) p.out3[grow * p.ldo3 + t.nt] = real ? dgp : 0.f;
+      // router-weight gradient partials: one slot per (n-tile, column half)
+      if (p.out3) p.out3[grow * p.ldo3 + 2 * t.nt + half] = (real && valid) ? dgp : 0.f;
     }
   }
   // every TMA store of this warp has finished before the CTA may exit
@@ -881,12 +913,12 @@ __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t a
 
 // ------------------------------------------------------------------ kernel
 template <int AM, int BMO, int EPI, int SCH, bool MX = false>
-__global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(gemm_threads<MX, EPI>(), 1) tc_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   constexpr int kSfBytes = MX ? kStages * kSfStageBytes : 0;
-  constexpr int kStagingBytes = 4 * epi_warp_bytes<MX>();
+  constexpr int kStagingBytes = epi_warps<MX, EPI>() * epi_warp_bytes<MX, EPI>();
   const uint32_t s_tiles = smem_u32(smem);
   const uint32_t s_staging = s_tiles + kStages * kStageBytes;
   const uint32_t s_sf = s_staging + kStagingBytes;
@@ -909,7 +941,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(accf0 + 8 * i, 1);
-      mbar_init(acce0 + 8 * i, 4);
+      mbar_init(acce0 + 8 * i, epi_warps<MX, EPI>());
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -917,12 +949,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     tma_prefetch_desc(&p.tmA);
     tma_prefetch_desc(&p.tmB0);
     if (BMO == B_K_DUAL_N || BMO == B_MN_DUAL_K) tma_prefetch_desc(&p.tmB1);
-    // only the output maps this launch stores through (the others may be unset)
-    if (EPI == EPI_BF16 || (EPI == EPI_SWIGLU_FWD && !MX)) {
+    // only the output maps this launch stores through (MXFP8 mode stores directly)
+    if (!MX && (EPI == EPI_BF16 || EPI == EPI_SWIGLU_FWD)) {
       tma_prefetch_desc(&p.tmO0);
-      if (SCH == SCHED_ROWS && !MX) tma_prefetch_desc(&p.tmO0h);
+      if (SCH == SCHED_ROWS) tma_prefetch_desc(&p.tmO0h);
     }
-    if (EPI == EPI_SWIGLU_FWD && !MX) {
+    if (!MX && EPI == EPI_SWIGLU_FWD) {
       tma_prefetch_desc(&p.tmO1);
       tma_prefetch_desc(&p.tmO1h);
     }
@@ -943,11 +975,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     if (lane == 0)
       gemm_mma<AM, BMO, EPI, SCH, MX>(p, s_tiles, s_sf, full0, empty0, accf0, acce0, drain,
                                       tmem_base, num_tiles, abort_flag);
-  } else if (warp >= 4) {
+  } else if (warp >= first_epi_warp<MX, EPI>()) {
+    const int ew = warp - first_epi_warp<MX, EPI>();
+    constexpr int kWarpBytes = epi_warp_bytes<MX, EPI>();
     if constexpr (MX)
-      gemm_epilogue_mx<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging,
-                                 smem + kStages * kStageBytes + (warp - 4) * epi_warp_bytes<MX>(), num_tiles,
-                                 abort_flag, warp - 4, lane);
+      gemm_epilogue_mx<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging + ew * kWarpBytes,
+                                 reinterpret_cast<float*>(smem + kStages * kStageBytes + ew * kWarpBytes),
+                                 num_tiles, abort_flag, warp & 3, ew >> 2, lane);
     else
       gemm_epilogue<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging, num_tiles, abort_flag, warp - 4,
                               lane);
