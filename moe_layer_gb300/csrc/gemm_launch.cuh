@@ -15,8 +15,8 @@ cudaError_t launch_gemm_inst(const GemmParams& p, int grid, cudaStream_t st) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   auto kfn = tc_gemm_kernel<AM, BMO, EPI, SCH, MX>;
-  constexpr int smem = gemm_smem_bytes_for<MX, EPI>();
-  constexpr int threads = gemm_threads<MX, EPI>();
+  constexpr int smem = gemm_smem_bytes_for<MX, EPI, SCH>();
+  constexpr int threads = gemm_threads<MX, EPI, SCH>();
   const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
   if (bit == 0 || !(configured.load() & bit)) {
     e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -75,22 +75,30 @@ __global__ void __launch_bounds__(kQThreads)
 // own axis.
 constexpr int kDualTile = 128;
 constexpr int kDualPitch = kDualTile + 8;  // bf16 elements per shared row (16-byte aligned rows)
-__global__ void __launch_bounds__(kQThreads)
+__global__ void __launch_bounds__(kQThreads, 4)
     mx_permute_dual_kernel(const __nv_bfloat16* __restrict__ src, long long src_ld,
                            const int32_t* __restrict__ idx, const int32_t* __restrict__ total_rows,
                            int64_t R, int K, uint8_t* __restrict__ rq, uint8_t* __restrict__ rq_sf,
                            uint8_t* __restrict__ tq, uint8_t* __restrict__ tq_sf) {
   __shared__ __align__(16) uint16_t tile[kDualTile][kDualPitch];
+  // E8M0 words of the tile: [0] per row (4 column blocks), [1] per column (4 row blocks)
+  __shared__ __align__(16) uint32_t sfw[2][kDualTile];
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kDualTile;
   const int c0 = blockIdx.x * kDualTile;
   if (r0 >= (total_rows ? static_cast<int64_t>(__ldg(total_rows)) : R)) return;
-  // gather: 16 threads per row, 16 bytes each
-  for (int i = threadIdx.x; i < kDualTile * 16; i += kQThreads) {
-    const int r = i >> 4, q = i & 15;
-    const int64_t srow = idx ? static_cast<int64_t>(__ldg(idx + r0 + r)) : r0 + r;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (srow >= 0) w = __ldg(reinterpret_cast<const uint4*>(src + srow * src_ld + c0) + q);
-    *reinterpret_cast<uint4*>(&tile[r][8 * q]) = w;
+  {  // gather: 16 threads per row, 16 bytes each; all loads issued before the stores
+    uint4 w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = threadIdx.x + kQThreads * k, r = i >> 4, q = i & 15;
+      const int64_t srow = idx ? static_cast<int64_t>(__ldg(idx + r0 + r)) : r0 + r;
+      w[k] = srow >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + srow * src_ld + c0) + q) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = threadIdx.x + kQThreads * k;
+      *reinterpret_cast<uint4*>(&tile[i >> 4][8 * (i & 15)]) = w[k];
+    }
   }
   __syncthreads();
   {  // along the row: thread -> (row, 64-column half), two blocks of 32
@@ -120,23 +128,30 @@ __global__ void __launch_bounds__(kQThreads)
       word |= static_cast<uint32_t>(e + 127) << (8 * (2 * half + b));
     }
     word |= __shfl_xor_sync(0xffffffffu, word, 1);
-    if (half == 0) *reinterpret_cast<uint32_t*>(rq_sf + sf_word_offset(r0 + r, c0 / 128, (R + 127) / 128)) = word;
+    if (half == 0) sfw[0][r] = word;
   }
-  if (!tq) return;
-  {  // along the rows: thread -> (column pair, 32-row block)
-    const int pc = threadIdx.x & 63, tb = threadIdx.x >> 6;
-    float v0[32], v1[32];
+  if (tq) {  // along the rows: thread -> (column, two 32-row blocks), 32 codes of the transpose's row each
+    const int c = threadIdx.x & 127, tb0 = 2 * (threadIdx.x >> 7);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[32 * tb + i][2 * pc]);
-      v0[i] = bf16lo(w);
-      v1[i] = bf16hi(w);
+    for (int tb = tb0; tb < tb0 + 2; ++tb) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(static_cast<uint32_t>(tile[32 * tb + i][c]) << 16);
+      const uint32_t code = quant32_store(v, tq + static_cast<int64_t>(c0 + c) * R + r0 + 32 * tb);
+      reinterpret_cast<uint8_t*>(sfw[1])[4 * c + tb] = static_cast<uint8_t>(code);
     }
-    const int64_t c = c0 + 2 * pc;
-    const uint32_t s0 = quant32_store(v0, tq + c * R + r0 + 32 * tb);
-    const uint32_t s1 = quant32_store(v1, tq + (c + 1) * R + r0 + 32 * tb);
-    tq_sf[sf_byte_offset(c, r0 + 32 * tb, K / 128)] = static_cast<uint8_t>(s0);
-    tq_sf[sf_byte_offset(c + 1, r0 + 32 * tb, K / 128)] = static_cast<uint8_t>(s1);
+  }
+  __syncthreads();
+  // Each tile's scales are one whole 512-byte block per copy: bytes 16 t .. 16 t + 15
+  // hold the words of rows (columns) t, t + 32, t + 64, t + 96.
+  if (threadIdx.x < 32) {
+    const int t = threadIdx.x;
+    uint8_t* blk = rq_sf + ((c0 / 128) * ((R + 127) / 128) + r0 / 128) * 512;
+    *reinterpret_cast<uint4*>(blk + 16 * t) = make_uint4(sfw[0][t], sfw[0][t + 32], sfw[0][t + 64], sfw[0][t + 96]);
+  } else if (tq && threadIdx.x < 64) {
+    const int t = threadIdx.x - 32;
+    uint8_t* blk = tq_sf + ((r0 / 128) * (K / 128) + c0 / 128) * 512;
+    *reinterpret_cast<uint4*>(blk + 16 * t) = make_uint4(sfw[1][t], sfw[1][t + 32], sfw[1][t + 64], sfw[1][t + 96]);
   }
 }
 

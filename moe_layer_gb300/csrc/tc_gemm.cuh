@@ -65,34 +65,42 @@ constexpr int kGemmThreads = 256;  // warps 0-3 roles (TMA, MMA, TMEM allocation
 constexpr int kStageBoxBytes = 32 * 128;   // one epilogue staging box: 32 rows x 128 bytes
 
 // Epilogue warps.  One per TMEM lane quadrant (warps 4-7), except for the
-// MXFP8 SwiGLU backward, whose heavy epilogue gets two per quadrant (warps
-// 2-9, 320 threads; the TMEM allocator, warp 2, is one of them).
-template <bool MX, int EPI>
-__host__ __device__ constexpr bool epi_wide() { return MX && EPI == EPI_SWIGLU_BWD; }
-template <bool MX, int EPI>
-__host__ __device__ constexpr int epi_warps() { return epi_wide<MX, EPI>() ? 8 : 4; }
-template <bool MX, int EPI>
-__host__ __device__ constexpr int first_epi_warp() { return epi_wide<MX, EPI>() ? 2 : 4; }
-template <bool MX, int EPI>
-__host__ __device__ constexpr int gemm_threads() { return 32 * (first_epi_warp<MX, EPI>() + epi_warps<MX, EPI>()); }
-// Epilogue shared memory per epilogue warp: in bf16 mode two 4 KB staging
-// boxes that TMA stores to global memory while the next box is being filled;
-// in MXFP8 mode, whose scale stages use part of shared memory, one box (in 5 KB),
-// or for the SwiGLU backward the 32 x 17 fp32 transpose buffer.
-template <bool MX, int EPI>
+// MXFP8 SwiGLU backward, whose heavy epilogue would be slower than the MMAs
+// with one: it gets two per quadrant (warps 2-9, 320 threads; the TMEM
+// allocator, warp 2, is one of them), each taking half of the columns.
+template <bool MX, int EPI, int SCH>
+__host__ __device__ constexpr bool epi_wide() {
+  return MX && EPI == EPI_SWIGLU_BWD;
+}
+template <bool MX, int EPI, int SCH>
+__host__ __device__ constexpr int epi_warps() { return epi_wide<MX, EPI, SCH>() ? 8 : 4; }
+template <bool MX, int EPI, int SCH>
+__host__ __device__ constexpr int first_epi_warp() { return epi_wide<MX, EPI, SCH>() ? 2 : 4; }
+template <bool MX, int EPI, int SCH>
+__host__ __device__ constexpr int gemm_threads() {
+  return 32 * (first_epi_warp<MX, EPI, SCH>() + epi_warps<MX, EPI, SCH>());
+}
+// Epilogue shared memory per epilogue warp: in bf16 mode 4 KB staging boxes
+// (two per warp, one with 8 warps) that TMA stores to global memory while the
+// next box is being filled; in MXFP8 mode, whose scale stages use part of
+// shared memory, one box (in 5 KB), or for the SwiGLU backward the 32 x 17
+// fp32 transpose buffer.
+template <bool MX, int EPI, int SCH>
+__host__ __device__ constexpr int epi_slots() { return (!MX && !epi_wide<MX, EPI, SCH>()) ? 2 : 1; }
+template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int epi_warp_bytes() {
-  return !MX ? 2 * 32 * 128 : (epi_wide<MX, EPI>() ? 32 * 17 * 4 : 5 * 1024);
+  return !MX ? epi_slots<MX, EPI, SCH>() * 32 * 128 : (epi_wide<MX, EPI, SCH>() ? 32 * 17 * 4 : 5 * 1024);
 }
 template <bool MX>
 __host__ __device__ constexpr int acc_bufs() { return MX ? 1 : 2; }
 template <bool MX>
 __host__ __device__ constexpr int stage_k() { return MX ? kBKmx : kBK; }
-template <bool MX, int EPI>
+template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int gemm_smem_bytes_for() {
   return 1024 + kStages * kStageBytes + (MX ? kStages * kSfStageBytes : 0) +
-         epi_warps<MX, EPI>() * epi_warp_bytes<MX, EPI>() + 256;
+         epi_warps<MX, EPI, SCH>() * epi_warp_bytes<MX, EPI, SCH>() + 256;
 }
-constexpr int kGemmSmemBytes = gemm_smem_bytes_for<false, 0>();
+constexpr int kGemmSmemBytes = gemm_smem_bytes_for<false, 0, 0>();
 
 
 struct GemmParams {
@@ -485,11 +493,14 @@ struct EpiStager {
 
 template <int EPI, int SCH>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf0, uint32_t acce0,
-                                              uint32_t tmem_base, uint32_t s_staging, int num_tiles,
-                                              volatile int* abort_flag, int warp_e, int lane) {
+                                              uint32_t tmem_base, uint32_t s_warp, int num_tiles,
+                                              volatile int* abort_flag, int warp_e, int half, int lane) {
+  constexpr bool kWide = epi_wide<false, EPI, SCH>();
+  // columns of the tile this warp stores (a half with two warps per quadrant)
+  const int cbeg = kWide ? 128 * half : 0, cend = kWide ? cbeg + 128 : kBN;
   int acc = 0;
   uint32_t aph = 0;
-  EpiStager<2> stg{s_staging + static_cast<uint32_t>(warp_e) * 2 * kStageBoxBytes, 0, lane};
+  EpiStager<epi_slots<false, EPI, SCH>()> stg{s_warp, 0, lane};
   for (int tau = blockIdx.x; tau < num_tiles; tau += gridDim.x) {
     const TileInfo t = gemm_tile<EPI, SCH, kBK>(p, tau);
     // Tile row held by this thread's TMEM lane: lane l of warp w is row 32w + l
@@ -516,7 +527,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
 
     if constexpr (SCH == SCHED_WGRAD) {
       const int r0 = t.m0 + warp_e * 32;
-      for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 64) {
+      for (int c0 = cbeg; c0 < cend && t.n0 + c0 < p.N; c0 += 64) {
         float v[64];
         if (t.nkb > 0) {
           tmem_ld32(tr + c0, v);
@@ -913,12 +924,12 @@ __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t a
 
 // ------------------------------------------------------------------ kernel
 template <int AM, int BMO, int EPI, int SCH, bool MX = false>
-__global__ void __launch_bounds__(gemm_threads<MX, EPI>(), 1) tc_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   constexpr int kSfBytes = MX ? kStages * kSfStageBytes : 0;
-  constexpr int kStagingBytes = epi_warps<MX, EPI>() * epi_warp_bytes<MX, EPI>();
+  constexpr int kStagingBytes = epi_warps<MX, EPI, SCH>() * epi_warp_bytes<MX, EPI, SCH>();
   const uint32_t s_tiles = smem_u32(smem);
   const uint32_t s_staging = s_tiles + kStages * kStageBytes;
   const uint32_t s_sf = s_staging + kStagingBytes;
@@ -941,7 +952,7 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI>(), 1) tc_gemm_kernel(con
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(accf0 + 8 * i, 1);
-      mbar_init(acce0 + 8 * i, epi_warps<MX, EPI>());
+      mbar_init(acce0 + 8 * i, epi_warps<MX, EPI, SCH>());
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -975,16 +986,16 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI>(), 1) tc_gemm_kernel(con
     if (lane == 0)
       gemm_mma<AM, BMO, EPI, SCH, MX>(p, s_tiles, s_sf, full0, empty0, accf0, acce0, drain,
                                       tmem_base, num_tiles, abort_flag);
-  } else if (warp >= first_epi_warp<MX, EPI>()) {
-    const int ew = warp - first_epi_warp<MX, EPI>();
-    constexpr int kWarpBytes = epi_warp_bytes<MX, EPI>();
+  } else if (warp >= first_epi_warp<MX, EPI, SCH>()) {
+    const int ew = warp - first_epi_warp<MX, EPI, SCH>();
+    constexpr int kWarpBytes = epi_warp_bytes<MX, EPI, SCH>();
     if constexpr (MX)
       gemm_epilogue_mx<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging + ew * kWarpBytes,
                                  reinterpret_cast<float*>(smem + kStages * kStageBytes + ew * kWarpBytes),
                                  num_tiles, abort_flag, warp & 3, ew >> 2, lane);
     else
-      gemm_epilogue<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging, num_tiles, abort_flag, warp - 4,
-                              lane);
+      gemm_epilogue<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging + ew * kWarpBytes, num_tiles, abort_flag,
+                              warp & 3, ew >> 2, lane);
   }
   tc_fence_before();
   __syncthreads();
