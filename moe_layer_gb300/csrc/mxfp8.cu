@@ -12,6 +12,8 @@
 // inside it the byte of row r (0..127) and 32-column block j (0..3) sits at
 // 16 * (r % 32) + 4 * (r / 32) + j.  The GEMM copies one such block straight
 // into tensor memory per operand tile and stage.
+#include <atomic>
+
 #include "moe_internal.h"
 #include "mx_common.cuh"
 #include "ptx.cuh"
@@ -75,85 +77,117 @@ __global__ void __launch_bounds__(kQThreads)
 // own axis.
 constexpr int kDualTile = 128;
 constexpr int kDualPitch = kDualTile + 8;  // bf16 elements per shared row (16-byte aligned rows)
-__global__ void __launch_bounds__(kQThreads, 4)
+constexpr int kDualBlocksPerSm = 3;
+
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Persistent: each block walks tiles blockIdx.x, + gridDim.x, ...; the gather
+// of the next tile is in flight (cp.async, double-buffered) while the current
+// one is quantized.
+__global__ void __launch_bounds__(kQThreads, kDualBlocksPerSm)
     mx_permute_dual_kernel(const __nv_bfloat16* __restrict__ src, long long src_ld,
                            const int32_t* __restrict__ idx, const int32_t* __restrict__ total_rows,
                            int64_t R, int K, uint8_t* __restrict__ rq, uint8_t* __restrict__ rq_sf,
                            uint8_t* __restrict__ tq, uint8_t* __restrict__ tq_sf) {
-  __shared__ __align__(16) uint16_t tile[kDualTile][kDualPitch];
+  extern __shared__ __align__(16) uint8_t dual_smem[];
+  typedef uint16_t Tile[kDualTile][kDualPitch];
+  Tile* tiles = reinterpret_cast<Tile*>(dual_smem);  // two buffers
   // E8M0 words of the tile: [0] per row (4 column blocks), [1] per column (4 row blocks)
-  __shared__ __align__(16) uint32_t sfw[2][kDualTile];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kDualTile;
-  const int c0 = blockIdx.x * kDualTile;
-  if (r0 >= (total_rows ? static_cast<int64_t>(__ldg(total_rows)) : R)) return;
-  {  // gather: 16 threads per row, 16 bytes each; all loads issued before the stores
-    uint4 w[8];
+  uint32_t(*sfw)[kDualTile] = reinterpret_cast<uint32_t(*)[kDualTile]>(dual_smem + 2 * sizeof(Tile));
+  const int ncol = K / kDualTile;
+  const int64_t used = total_rows ? static_cast<int64_t>(__ldg(total_rows)) : R;
+  const int64_t ntiles = ((used + kDualTile - 1) / kDualTile) * ncol;  // only row tiles that hold used rows
+  auto gather = [&](int64_t tau, Tile& t) {  // 16 threads per row, 16 bytes each
+    const int64_t r0 = (tau / ncol) * kDualTile;
+    const int c0 = static_cast<int>(tau % ncol) * kDualTile;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int i = threadIdx.x + kQThreads * k, r = i >> 4, q = i & 15;
       const int64_t srow = idx ? static_cast<int64_t>(__ldg(idx + r0 + r)) : r0 + r;
-      w[k] = srow >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + srow * src_ld + c0) + q) : make_uint4(0, 0, 0, 0);
+      const __nv_bfloat16* g = src + (srow >= 0 ? srow : 0) * src_ld + c0 + 8 * q;
+      cp_async16(&t[r][8 * q], g, srow >= 0 ? 16 : 0);
     }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int i = threadIdx.x + kQThreads * k;
-      *reinterpret_cast<uint4*>(&tile[i >> 4][8 * (i & 15)]) = w[k];
+    cp_async_commit();
+  };
+  int buf = 0;
+  if (static_cast<int64_t>(blockIdx.x) < ntiles) gather(blockIdx.x, tiles[0]);
+  for (int64_t tau = blockIdx.x; tau < ntiles; tau += gridDim.x) {
+    const int64_t next = tau + gridDim.x;
+    if (next < ntiles) {
+      gather(next, tiles[buf ^ 1]);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
-  }
-  __syncthreads();
-  {  // along the row: thread -> (row, 64-column half), two blocks of 32
-    const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
-    uint32_t word = 0;
+    __syncthreads();
+    const Tile& tile = tiles[buf];
+    const int64_t r0 = (tau / ncol) * kDualTile;
+    const int c0 = static_cast<int>(tau % ncol) * kDualTile;
+    {  // along the row: thread -> (row, 64-column half), two blocks of 32
+      const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
+      uint32_t word = 0;
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      float v[32], amax = 0.f;
+      for (int b = 0; b < 2; ++b) {
+        float v[32], amax = 0.f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 w = *reinterpret_cast<const uint4*>(&tile[r][64 * half + 32 * b + 8 * q]);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        for (int q = 0; q < 4; ++q) {
+          const uint4 w = *reinterpret_cast<const uint4*>(&tile[r][64 * half + 32 * b + 8 * q]);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          v[8 * q + 2 * k] = bf16lo(ws[k]);
-          v[8 * q + 2 * k + 1] = bf16hi(ws[k]);
+          for (int k = 0; k < 4; ++k) {
+            v[8 * q + 2 * k] = bf16lo(ws[k]);
+            v[8 * q + 2 * k + 1] = bf16hi(ws[k]);
+          }
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const int e = mx_scale_exp(amax);
+        uint4 lo, hi;
+        quant32(v, e, lo, hi);
+        uint4* d4 = reinterpret_cast<uint4*>(rq + (r0 + r) * K + c0 + 64 * half + 32 * b);
+        d4[0] = lo;
+        d4[1] = hi;
+        word |= static_cast<uint32_t>(e + 127) << (8 * (2 * half + b));
       }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-      const int e = mx_scale_exp(amax);
-      uint4 lo, hi;
-      quant32(v, e, lo, hi);
-      uint4* d4 = reinterpret_cast<uint4*>(rq + (r0 + r) * K + c0 + 64 * half + 32 * b);
-      d4[0] = lo;
-      d4[1] = hi;
-      word |= static_cast<uint32_t>(e + 127) << (8 * (2 * half + b));
+      word |= __shfl_xor_sync(0xffffffffu, word, 1);
+      if (half == 0) sfw[0][r] = word;
     }
-    word |= __shfl_xor_sync(0xffffffffu, word, 1);
-    if (half == 0) sfw[0][r] = word;
-  }
-  if (tq) {  // along the rows: thread -> (column, two 32-row blocks), 32 codes of the transpose's row each
-    const int c = threadIdx.x & 127, tb0 = 2 * (threadIdx.x >> 7);
+    if (tq) {  // along the rows: thread -> (column, two 32-row blocks), 32 codes of the transpose's row each
+      const int c = threadIdx.x & 127, tb0 = 2 * (threadIdx.x >> 7);
 #pragma unroll
-    for (int tb = tb0; tb < tb0 + 2; ++tb) {
-      float v[32];
+      for (int tb = tb0; tb < tb0 + 2; ++tb) {
+        float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(static_cast<uint32_t>(tile[32 * tb + i][c]) << 16);
-      const uint32_t code = quant32_store(v, tq + static_cast<int64_t>(c0 + c) * R + r0 + 32 * tb);
-      reinterpret_cast<uint8_t*>(sfw[1])[4 * c + tb] = static_cast<uint8_t>(code);
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(static_cast<uint32_t>(tile[32 * tb + i][c]) << 16);
+        const uint32_t code = quant32_store(v, tq + static_cast<int64_t>(c0 + c) * R + r0 + 32 * tb);
+        reinterpret_cast<uint8_t*>(sfw[1])[4 * c + tb] = static_cast<uint8_t>(code);
+      }
     }
-  }
-  __syncthreads();
-  // Each tile's scales are one whole 512-byte block per copy: bytes 16 t .. 16 t + 15
-  // hold the words of rows (columns) t, t + 32, t + 64, t + 96.
-  if (threadIdx.x < 32) {
-    const int t = threadIdx.x;
-    uint8_t* blk = rq_sf + ((c0 / 128) * ((R + 127) / 128) + r0 / 128) * 512;
-    *reinterpret_cast<uint4*>(blk + 16 * t) = make_uint4(sfw[0][t], sfw[0][t + 32], sfw[0][t + 64], sfw[0][t + 96]);
-  } else if (tq && threadIdx.x < 64) {
-    const int t = threadIdx.x - 32;
-    uint8_t* blk = tq_sf + ((r0 / 128) * (K / 128) + c0 / 128) * 512;
-    *reinterpret_cast<uint4*>(blk + 16 * t) = make_uint4(sfw[1][t], sfw[1][t + 32], sfw[1][t + 64], sfw[1][t + 96]);
+    __syncthreads();
+    // Each tile's scales are one whole 512-byte block per copy: bytes 16 t .. 16 t + 15
+    // hold the words of rows (columns) t, t + 32, t + 64, t + 96.
+    if (threadIdx.x < 32) {
+      const int t = threadIdx.x;
+      uint8_t* blk = rq_sf + ((c0 / 128) * ((R + 127) / 128) + r0 / 128) * 512;
+      *reinterpret_cast<uint4*>(blk + 16 * t) = make_uint4(sfw[0][t], sfw[0][t + 32], sfw[0][t + 64], sfw[0][t + 96]);
+    } else if (tq && threadIdx.x < 64) {
+      const int t = threadIdx.x - 32;
+      uint8_t* blk = tq_sf + ((r0 / 128) * (K / 128) + c0 / 128) * 512;
+      *reinterpret_cast<uint4*>(blk + 16 * t) = make_uint4(sfw[1][t], sfw[1][t + 32], sfw[1][t + 64], sfw[1][t + 96]);
+    }
+    __syncthreads();  // sfw and this tile's buffer are free again
+    buf ^= 1;
   }
 }
+constexpr int kDualSmemBytes = 2 * kDualTile * kDualPitch * 2 + 2 * kDualTile * 4;
 
 // Transposing quantization: src is [rows, cols] (row pitch src_ld) and feeds
 // a GEMM whose reduction axis is `rows`.  Writes dst[c, k_off + r] (row pitch
@@ -223,8 +257,21 @@ cudaError_t launch_mx_permute_dual(const __nv_bfloat16* src, long long src_ld, c
                                    uint8_t* tq, uint8_t* tq_sf, cudaStream_t st) {
   if (R <= 0) return cudaSuccess;
   if (K % kDualTile || R % kDualTile) return cudaErrorInvalidValue;
-  dim3 grid(K / kDualTile, static_cast<unsigned>(R / kDualTile));
-  mx_permute_dual_kernel<<<grid, kQThreads, 0, st>>>(src, src_ld, idx, total_rows, R, K, rq, rq_sf, tq, tq_sf);
+  static std::atomic<unsigned long long> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit == 0 || !(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(mx_permute_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDualSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  const int64_t tiles = (R / kDualTile) * (K / kDualTile);
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * kDualBlocksPerSm;
+  const unsigned grid = static_cast<unsigned>(tiles < cap ? tiles : cap);
+  mx_permute_dual_kernel<<<grid, kQThreads, kDualSmemBytes, st>>>(src, src_ld, idx, total_rows, R, K, rq, rq_sf,
+                                                                 tq, tq_sf);
   return cudaGetLastError();
 }
 
