@@ -193,19 +193,27 @@ def e4m3_decode(code):
 
 
 E4M3_TABLE = np.array([e4m3_decode(c) for c in range(256)])
-_E4M3_POS = np.array([E4M3_TABLE[c] for c in range(0x7F)])  # 0x00..0x7E, ascending
 
 
 def e4m3_quantize(v):
     """Round float64 values to E4M3 codes: nearest value, ties to the even
-    mantissa (even code), magnitudes beyond 448 saturate to 448."""
+    mantissa (even code), magnitudes beyond 448 saturate to 448.
+
+    Written out from the format: the non-negative values of binade k
+    (2^k <= a < 2^(k+1), k = -6..8) are 2^k (1 + j/8), j = 0..7, code
+    8 (k + 7) + j; below 2^-6 the subnormals j 2^-9, code j.  So in every
+    binade (the subnormals counted with k = -6) the values are the multiples
+    m 2^(k-3) with m in [8, 16) (m in [0, 8) for the subnormals), code
+    8 (k + 7) + m - 8, and the nearest one is the magnitude rounded to a
+    multiple of 2^(k-3), ties to the even multiple (np.rint) -- the even code,
+    as m and the code have the same parity.  m = 16 is 2^(k+1), the first value
+    of the next binade, and the same formula gives its code."""
     v = np.asarray(v, np.float64)
     a = np.minimum(np.abs(v), E4M3_MAX)
-    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, len(_E4M3_POS) - 1)
-    lo = np.maximum(hi - 1, 0)
-    dlo, dhi = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
-    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
-    code = pick.astype(np.uint8)
+    _, ex = np.frexp(a)                      # a = f 2^ex, f in [0.5, 1): binade k = ex - 1
+    k = np.where(a < 2.0 ** -6, -6, ex.astype(np.int64) - 1)  # zero and subnormals: k = -6
+    m = np.rint(np.ldexp(a, 3 - k))          # a / 2^(k-3), exact scaling by a power of two
+    code = (8 * (k + 7) + m.astype(np.int64) - 8).astype(np.uint8)
     neg = (v < 0) & (code != 0)
     return np.where(neg, code | 0x80, code).astype(np.uint8)
 
@@ -220,7 +228,7 @@ def mx_quantize(v, axis=-1):
     amax = np.abs(blk).max(axis=-1)
     with np.errstate(divide="ignore"):
         e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 8, -127)
-    e = np.clip(e, -127, 127)
+    e = np.minimum(np.maximum(e, -127), 127)
     scale = np.ldexp(1.0, e.astype(np.int64))
     codes = e4m3_quantize(blk / scale[..., None]).reshape(shp)
     return np.moveaxis(codes, -1, axis), np.moveaxis((e + 127).astype(np.uint8), -1, axis)

@@ -395,3 +395,21 @@ def test_mxfp8_backward_takes_decisions_on_stored_values():
     f0 = O.expert_backward(x, dy, g, a0, b0, O.swiglu(a0, b0), wg, wu, wd)
     f1 = O.expert_backward(x, dy, g, a1, b1, O.swiglu(a1, b1), wg, wu, wd)
     assert not np.array_equal(f0[4], f1[4])
+
+
+def test_e4m3_quantize_matches_nearest_table_search_at_scale():
+    """The closed-form rounding equals a search for the nearest of the 127
+    non-negative code values (ties to the even code) on 200k values spanning
+    every binade, the subnormals, exact midpoints and the saturation range."""
+    rng = _rng(18)
+    pos = O.E4M3_TABLE[:0x7F]  # ascending non-negative values, codes 0x00..0x7E
+    mids = (pos[:-1] + pos[1:]) / 2
+    v = np.concatenate([rng.uniform(-1, 1, 100_000) * np.exp2(rng.uniform(-12, 10, 100_000)),
+                        mids, -mids, pos, np.nextafter(mids, 0), np.nextafter(mids, 1e9), [448.0, 460.0, 1e30]])
+    a = np.minimum(np.abs(v), 448.0)
+    hi = np.minimum(np.searchsorted(pos, a, side="left"), len(pos) - 1)
+    lo = np.maximum(hi - 1, 0)
+    dlo, dhi = a - pos[lo], pos[hi] - a
+    want = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    got = O.e4m3_quantize(v) & 0x7F
+    np.testing.assert_array_equal(got, want)
