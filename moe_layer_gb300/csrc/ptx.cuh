@@ -346,7 +346,9 @@ __device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* src, float (&v
   }
 }
 
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+// Logistic sigmoid with the fast exponential and an approximate reciprocal
+// (a few ulp of fp32): every output it feeds is rounded to bf16 or E4M3.
+__device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 // Writes one thread's 64 bf16 values (128 bytes) as row `row` (0..31) of a
 // 32 x 128-byte staging box in the 128-byte-swizzle layout TMA expects
