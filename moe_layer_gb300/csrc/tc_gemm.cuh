@@ -52,7 +52,7 @@ constexpr int kBM = 128;  // rows per tile (TMEM lanes)
 constexpr int kBN = 256;  // accumulator columns per tile
 constexpr int kBK = 64;   // bf16 K per stage: one 128-byte swizzle row
 constexpr int kBKmx = 128;  // MXFP8 K per stage: one 128-byte swizzle row of E4M3
-constexpr int kStages = 4;
+constexpr int kStages = 4;  // the most stages any instantiation uses
 constexpr int kATileBytes = kBM * 128;  // 16 KB (128 rows of 128 bytes)
 constexpr int kBTileBytes = kBN * 128;  // 32 KB
 constexpr int kStageBytes = kATileBytes + kBTileBytes;
@@ -85,6 +85,10 @@ __host__ __device__ constexpr int gemm_threads() {
 // next box is being filled; in MXFP8 mode, whose scale stages use part of
 // shared memory, one box (in 5 KB), or for the SwiGLU backward the 32 x 17
 // fp32 transpose buffer.
+// Pipeline stages per instantiation.  (Three stages with four staging boxes
+// per warp were measured for the weight gradients: slower than four stages.)
+template <bool MX, int EPI, int SCH>
+__host__ __device__ constexpr int gemm_stages() { return kStages; }
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int epi_slots() { return (!MX && !epi_wide<MX, EPI, SCH>()) ? 2 : 1; }
 template <bool MX, int EPI, int SCH>
@@ -97,7 +101,7 @@ template <bool MX>
 __host__ __device__ constexpr int stage_k() { return MX ? kBKmx : kBK; }
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int gemm_smem_bytes_for() {
-  return 1024 + kStages * kStageBytes + (MX ? kStages * kSfStageBytes : 0) +
+  return 1024 + gemm_stages<MX, EPI, SCH>() * (kStageBytes + (MX ? kSfStageBytes : 0)) +
          epi_warps<MX, EPI, SCH>() * epi_warp_bytes<MX, EPI, SCH>() + 256;
 }
 constexpr int kGemmSmemBytes = gemm_smem_bytes_for<false, 0, 0>();
@@ -286,9 +290,10 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
   int s = 0;
   uint32_t ph = 0;
   // Per stage: parity of the last load issued into it, or -1.
-  int issued_parity[kStages];
+  constexpr int ST = gemm_stages<MX, EPI, SCH>();
+  int issued_parity[ST];
 #pragma unroll
-  for (int i = 0; i < kStages; ++i) issued_parity[i] = -1;
+  for (int i = 0; i < ST; ++i) issued_parity[i] = -1;
   bool aborted = false;
 
   for (int tau = blockIdx.x; tau < num_tiles && !aborted; tau += gridDim.x) {
@@ -350,7 +355,7 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
         }
       }
       issued_parity[s] = static_cast<int>(ph);
-      if (++s == kStages) {
+      if (++s == ST) {
         s = 0;
         ph ^= 1;
       }
@@ -359,7 +364,7 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
   if (aborted && lane == 0) {
     // Loads still in flight must land before the CTA's shared memory goes away.
 #pragma unroll
-    for (int i = 0; i < kStages; ++i)
+    for (int i = 0; i < ST; ++i)
       if (issued_parity[i] >= 0)
         mbar_wait(full0 + 8 * i, static_cast<uint32_t>(issued_parity[i]), abort_flag, p.status,
                   false);
@@ -373,6 +378,7 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
                                          uint32_t acce0, uint32_t drain, uint32_t tmem_base,
                                          int num_tiles, volatile int* abort_flag) {
   constexpr int BK = stage_k<MX>();
+  constexpr int ST = gemm_stages<MX, EPI, SCH>();
   constexpr bool a_mn = (AM == A_MN_TILE);
   constexpr bool b_mn = (BMO == B_MN_TILE || BMO == B_MN_DUAL_K);
   constexpr uint32_t idesc128 = idesc_bf16_f32(kBM, kBN, a_mn ? 1 : 0, b_mn ? 1 : 0);
@@ -400,7 +406,7 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
       const uint32_t sA = s_tiles + s * kStageBytes;
       const uint32_t sB = sA + kATileBytes;
       if constexpr (MX) {
-        // scale ring slot s: reused by stage s + kStages, whose data can only
+        // scale ring slot s: reused by stage s + ST, whose data can only
         // have been loaded after these MMAs released stage s
         const uint32_t sfa_t = tmem_base + kSfTmemCol + s * kSfTmemStride;
         const uint32_t sfs = s_sf + s * kSfStageBytes;
@@ -427,7 +433,7 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
       }
       tc_commit(empty0 + 8 * s);
       issued = true;
-      if (++s == kStages) {
+      if (++s == ST) {
         s = 0;
         ph ^= 1;
       }
@@ -719,7 +725,7 @@ __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t a
                                                  volatile int* abort_flag, int quad, int half, int lane) {
   static_assert(EPI != EPI_F32_BIAS, "no fp32 epilogue in MXFP8 mode");
   uint32_t aph = 0;
-  EpiStager<1> stg{s_warp, 0, lane};
+  EpiStager<epi_slots<true, EPI, SCH>()> stg{s_warp, 0, lane};
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   const uint32_t acc = tmem_base + lane_off;
   // wide (SwiGLU backward): 96 stash columns per warp; otherwise 192
@@ -928,25 +934,26 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kerne
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  constexpr int kSfBytes = MX ? kStages * kSfStageBytes : 0;
+  constexpr int ST = gemm_stages<MX, EPI, SCH>();
+  constexpr int kSfBytes = MX ? ST * kSfStageBytes : 0;
   constexpr int kStagingBytes = epi_warps<MX, EPI, SCH>() * epi_warp_bytes<MX, EPI, SCH>();
   const uint32_t s_tiles = smem_u32(smem);
-  const uint32_t s_staging = s_tiles + kStages * kStageBytes;
+  const uint32_t s_staging = s_tiles + ST * kStageBytes;
   const uint32_t s_sf = s_staging + kStagingBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kStagingBytes + kSfBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ST * kStageBytes + kStagingBytes + kSfBytes);
   const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = full0 + 8 * kStages;
-  const uint32_t accf0 = empty0 + 8 * kStages;
+  const uint32_t empty0 = full0 + 8 * ST;
+  const uint32_t accf0 = empty0 + 8 * ST;
   const uint32_t acce0 = accf0 + 16;
   const uint32_t drain = acce0 + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * ST + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < ST; ++i) {
       mbar_init(full0 + 8 * i, 1);
       mbar_init(empty0 + 8 * i, 1);
     }
@@ -991,7 +998,7 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kerne
     constexpr int kWarpBytes = epi_warp_bytes<MX, EPI, SCH>();
     if constexpr (MX)
       gemm_epilogue_mx<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging + ew * kWarpBytes,
-                                 reinterpret_cast<float*>(smem + kStages * kStageBytes + ew * kWarpBytes),
+                                 reinterpret_cast<float*>(smem + ST * kStageBytes + ew * kWarpBytes),
                                  num_tiles, abort_flag, warp & 3, ew >> 2, lane);
     else
       gemm_epilogue<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging + ew * kWarpBytes, num_tiles, abort_flag,
