@@ -776,7 +776,7 @@ __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t a
           stg.store2d(&p.tmO0, box, t.n0 + c0, r0);
       };
       if (have) {
-        for (int c = 0; c < kStashCols && t.n0 + c < p.N; c += 32) tmem_copy32(stash + c, acc + c);
+        for (int c = 0; c < kStashCols && t.n0 + c < p.N; c += 96) tmem_copy96(stash + c, acc + c);
         tmem_st_wait();
       }
       float v[64];
@@ -829,10 +829,8 @@ __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t a
         for (int i = 0; i < 32; ++i) a[i] = a[i] * sigmoidf_(a[i]) * b[i];
         qword |= quant32_store(a, p.qout + grow * p.qld + t.n0 + 32 * j) << (8 * j);
       };
-      for (int j = 0; j < 3; ++j) {
-        tmem_copy32(stash + 32 * j, acc + 32 * j);
-        tmem_copy32(stash + 96 + 32 * j, acc + kBN / 2 + 32 * j);
-      }
+      tmem_copy96(stash, acc);
+      tmem_copy96(stash + 96, acc + kBN / 2);
       tmem_st_wait();
       float a[32], b[32];
       tmem_ld32(acc + 96, a);
@@ -902,7 +900,7 @@ __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t a
       };
       float dh[32];
       if (valid) {
-        for (int j = 0; j < 3; ++j) tmem_copy32(stash + 32 * j, acc + cw + 32 * j);
+        tmem_copy96(stash, acc + cw);
         tmem_st_wait();
         tmem_ld32(acc + cw + 96, dh);
         tmem_ld_wait();
