@@ -494,12 +494,13 @@ moe_status forward_routed_mx(const Shape& s, const moe_weights* wts, const Routi
 // as K-major block-scaled GEMMs over [row_start[e], row_start[e+1]).
 moe_status wgrad_routed_mx(const Shape& s, const Routing& rt, const Saved& sv, const BwdWs& w,
                            const moe_grads* g, cudaStream_t st) {
+  constexpr int kWgradBnMx = gemm_bn<true, EPI_BF16, SCHED_WGRAD>();  // 128-column tiles
   const int d = static_cast<int>(s.d), I = static_cast<int>(s.I), E = static_cast<int>(s.E);
   {
     GemmParams p;  // dW_down[e] = dy_rows^T . (g h)
     zero_params(p);
     MOE_TRY(qmap(&p.tmA, w.dyt, s.d, s.Rp, kBM));
-    MOE_TRY(qmap(&p.tmB0, w.hgt, s.I, s.Rp, kBN));
+    MOE_TRY(qmap(&p.tmB0, w.hgt, s.I, s.Rp, kWgradBnMx));
     set_mx_scales(p, w.dyt_sf, s.d, w.hgt_sf, nullptr, s.I);
     p.num_groups = E;
     p.row_start = rt.row_start;
@@ -507,13 +508,13 @@ moe_status wgrad_routed_mx(const Shape& s, const Routing& rt, const Saved& sv, c
     p.N = I;
     MOE_TRY(omap3(&p.tmO0, g->dW_down, s.E, s.d, s.I));
     p.status = w.status;
-    MOE_LAUNCH(PL_WGRAD_DOWN, st, launch_gemm(GK_MX_WGRAD, p, grid_for(s.E * cdiv(s.d, kBM) * cdiv(s.I, kBN)), st));
+    MOE_LAUNCH(PL_WGRAD_DOWN, st, launch_gemm(GK_MX_WGRAD, p, grid_for(s.E * cdiv(s.d, kBM) * cdiv(s.I, kWgradBnMx)), st));
   }
   for (int half = 0; half < 2; ++half) {
     GemmParams p;  // dW_gate[e] = da^T . x_rows ; dW_up[e] = db^T . x_rows
     zero_params(p);
     MOE_TRY(qmap(&p.tmA, w.dadbt, 2 * s.I, s.Rp, kBM));
-    MOE_TRY(qmap(&p.tmB0, sv.xt, s.d, s.Rp, kBN));
+    MOE_TRY(qmap(&p.tmB0, sv.xt, s.d, s.Rp, kWgradBnMx));
     set_mx_scales(p, w.dadbt_sf, 2 * s.I, sv.xt_sf, nullptr, s.d);
     p.num_groups = E;
     p.row_start = rt.row_start;
@@ -522,7 +523,7 @@ moe_status wgrad_routed_mx(const Shape& s, const Routing& rt, const Saved& sv, c
     p.a_col_off = half ? I : 0;
     MOE_TRY(omap3(&p.tmO0, half ? g->dW_up : g->dW_gate, s.E, s.I, s.d));
     p.status = w.status;
-    MOE_LAUNCH(half ? PL_WGRAD_UP : PL_WGRAD_GATE, st, launch_gemm(GK_MX_WGRAD, p, grid_for(s.E * cdiv(s.I, kBM) * cdiv(s.d, kBN)), st));
+    MOE_LAUNCH(half ? PL_WGRAD_UP : PL_WGRAD_GATE, st, launch_gemm(GK_MX_WGRAD, p, grid_for(s.E * cdiv(s.I, kBM) * cdiv(s.d, kWgradBnMx)), st));
   }
   return MOE_OK;
 }

@@ -64,6 +64,20 @@ constexpr int kTmemCols = 512;
 constexpr int kGemmThreads = 256;  // warps 0-3 roles (TMA, MMA, TMEM allocation, idle), 4-7 epilogue
 constexpr int kStageBoxBytes = 32 * 128;   // one epilogue staging box: 32 rows x 128 bytes
 
+// Tile width (accumulator columns) per instantiation: 256 everywhere.  A
+// width of 128 gives MXFP8 kernels room for two accumulators beside the scale
+// ring; measured for the MXFP8 weight gradients it was slower (2.11 -> 2.96 ms
+// at the DSV3 shape: twice the tiles, each with a fixed cost), so no
+// instantiation uses it.
+template <bool MX, int EPI, int SCH>
+__host__ __device__ constexpr int gemm_bn() { return kBN; }
+template <bool MX, int EPI, int SCH>
+__host__ __device__ constexpr int acc_bufs() { return (MX && gemm_bn<MX, EPI, SCH>() == kBN) ? 1 : 2; }
+template <bool MX, int EPI, int SCH>
+__host__ __device__ constexpr int stage_bytes() { return kATileBytes + gemm_bn<MX, EPI, SCH>() * 128; }
+template <bool MX, int EPI, int SCH>
+__host__ __device__ constexpr int sf_stage_bytes() { return MX ? 512 + gemm_bn<MX, EPI, SCH>() / 128 * 512 : 0; }
+
 // Epilogue warps.  One per TMEM lane quadrant (warps 4-7), except for the
 // MXFP8 SwiGLU backward, whose heavy epilogue would be slower than the MMAs
 // with one: it gets two per quadrant (warps 2-9, 320 threads; the TMEM
@@ -80,28 +94,34 @@ template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int gemm_threads() {
   return 32 * (first_epi_warp<MX, EPI, SCH>() + epi_warps<MX, EPI, SCH>());
 }
-// Epilogue shared memory per epilogue warp: in bf16 mode 4 KB staging boxes
-// (two per warp, one with 8 warps) that TMA stores to global memory while the
-// next box is being filled; in MXFP8 mode, whose scale stages use part of
-// shared memory, one box (in 5 KB), or for the SwiGLU backward the 32 x 17
-// fp32 transpose buffer.
-// Pipeline stages per instantiation.  (Three stages with four staging boxes
-// per warp were measured for the weight gradients: slower than four stages.)
+// Pipeline stages: four 48 KB stages, five 32 KB ones with 128-column tiles.
+// (Three stages with four staging boxes per warp were measured for the
+// weight gradients: slower than four stages.)
 template <bool MX, int EPI, int SCH>
-__host__ __device__ constexpr int gemm_stages() { return kStages; }
+__host__ __device__ constexpr int gemm_stages() { return gemm_bn<MX, EPI, SCH>() == kBN ? kStages : 5; }
+// MXFP8 kernels with a single accumulator run the stash epilogue; the ones
+// with two (the weight gradients) run the bf16-mode epilogue.
 template <bool MX, int EPI, int SCH>
-__host__ __device__ constexpr int epi_slots() { return (!MX && !epi_wide<MX, EPI, SCH>()) ? 2 : 1; }
+__host__ __device__ constexpr bool epi_mx_stash() { return MX && acc_bufs<MX, EPI, SCH>() == 1; }
+// Epilogue shared memory per epilogue warp: 4 KB staging boxes that TMA
+// stores to global memory while the next box is being filled (two per warp
+// with two accumulators); in the stash epilogue, whose kernels keep the scale
+// stages in shared memory too, one box (in 5 KB), or for the SwiGLU backward
+// the 32 x 17 fp32 transpose buffer.
+template <bool MX, int EPI, int SCH>
+__host__ __device__ constexpr int epi_slots() {
+  return (!epi_mx_stash<MX, EPI, SCH>() && !epi_wide<MX, EPI, SCH>()) ? 2 : 1;
+}
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int epi_warp_bytes() {
-  return !MX ? epi_slots<MX, EPI, SCH>() * 32 * 128 : (epi_wide<MX, EPI, SCH>() ? 32 * 17 * 4 : 5 * 1024);
+  return !epi_mx_stash<MX, EPI, SCH>() ? epi_slots<MX, EPI, SCH>() * 32 * 128
+                                       : (epi_wide<MX, EPI, SCH>() ? 32 * 17 * 4 : 5 * 1024);
 }
-template <bool MX>
-__host__ __device__ constexpr int acc_bufs() { return MX ? 1 : 2; }
 template <bool MX>
 __host__ __device__ constexpr int stage_k() { return MX ? kBKmx : kBK; }
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int gemm_smem_bytes_for() {
-  return 1024 + gemm_stages<MX, EPI, SCH>() * (kStageBytes + (MX ? kSfStageBytes : 0)) +
+  return 1024 + gemm_stages<MX, EPI, SCH>() * (stage_bytes<MX, EPI, SCH>() + sf_stage_bytes<MX, EPI, SCH>()) +
          epi_warps<MX, EPI, SCH>() * epi_warp_bytes<MX, EPI, SCH>() + 256;
 }
 constexpr int kGemmSmemBytes = gemm_smem_bytes_for<false, 0, 0>();
@@ -203,21 +223,21 @@ __device__ __forceinline__ int find_group(const int* row_start, int G, int row) 
   return lo;
 }
 
-template <int EPI, int SCH>
+template <int EPI, int SCH, int BN>
 __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
   if constexpr (SCH == SCHED_ROWS) {
     const int num_nt = (p.N + tile_out_cols<EPI>() - 1) / tile_out_cols<EPI>();
     if (p.dense_rows > 0) return ((p.dense_rows + kBM - 1) / kBM) * num_nt;
     return __ldg(p.tile_start + p.num_groups) * num_nt;
   } else {
-    const int num_nt = (p.N + kBN - 1) / kBN;
+    const int num_nt = (p.N + BN - 1) / BN;
     const int num_mt = (p.M_out + kBM - 1) / kBM;
     const int G = p.dense_rows > 0 ? 1 : p.num_groups;
     return G * num_mt * num_nt;
   }
 }
 
-template <int EPI, int SCH, int BK>
+template <int EPI, int SCH, int BK, int BN = kBN>
 __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau) {
   TileInfo t;
   if constexpr (SCH == SCHED_ROWS) {
@@ -254,7 +274,7 @@ __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau) {
     t.kb0 = 0;
     t.nkb = p.K / BK;
   } else {
-    const int num_nt = (p.N + kBN - 1) / kBN;
+    const int num_nt = (p.N + BN - 1) / BN;
     const int num_mt = (p.M_out + kBM - 1) / kBM;
     const int per_g = num_mt * num_nt;
     const int e = tau / per_g;
@@ -264,7 +284,7 @@ __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau) {
     t.e = e;
     t.m0 = mt * kBM;
     t.nt = nt;
-    t.n0 = nt * kBN;
+    t.n0 = nt * BN;
     t.row0 = 0;
     t.rows_valid = 0;
     t.m64 = 0;
@@ -286,7 +306,9 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
                                               uint32_t full0, uint32_t empty0, int num_tiles,
                                               volatile int* abort_flag, int lane) {
   constexpr int BK = stage_k<MX>();
-  constexpr uint32_t kTx = kStageBytes + (MX ? kSfStageBytes : 0);
+  constexpr int BN = gemm_bn<MX, EPI, SCH>();
+  constexpr int SB = stage_bytes<MX, EPI, SCH>(), SFB = sf_stage_bytes<MX, EPI, SCH>();
+  constexpr uint32_t kTx = SB + SFB;
   int s = 0;
   uint32_t ph = 0;
   // Per stage: parity of the last load issued into it, or -1.
@@ -297,7 +319,7 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
   bool aborted = false;
 
   for (int tau = blockIdx.x; tau < num_tiles && !aborted; tau += gridDim.x) {
-    const TileInfo t = gemm_tile<EPI, SCH, BK>(p, tau);
+    const TileInfo t = gemm_tile<EPI, SCH, BK, BN>(p, tau);
     // row coordinate of the A tile: token rows, or output rows of a weight gradient
     const int arow = SCH == SCHED_WGRAD ? p.a_col_off + t.m0 : t.row0;
     const int brow = t.e * p.b_group_rows + t.n0;
@@ -310,7 +332,7 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
         break;
       }
       const uint32_t full = full0 + 8 * s;
-      const uint32_t sA = s_tiles + s * kStageBytes;
+      const uint32_t sA = s_tiles + s * SB;
       const uint32_t sB = sA + kATileBytes;
       if (lane == 0) mbar_arrive_expect_tx(full, kTx);
       __syncwarp();
@@ -343,14 +365,14 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
       if constexpr (MX) {
         if (lane == 0) {
           const long long g = kabs / kBKmx;
-          const uint32_t sfs = s_sf + s * kSfStageBytes;
+          const uint32_t sfs = s_sf + s * SFB;
           bulk_load(sfs, p.sfa + (g * p.sfa_rb + arow / 128) * 512, 512, full);
           const size_t boff = static_cast<size_t>((g * p.sfb_rb + brow / 128) * 512);
           if constexpr (BMO == B_K_DUAL_N) {
             bulk_load(sfs + 512, p.sfb0 + boff, 512, full);
             bulk_load(sfs + 1024, p.sfb1 + boff, 512, full);
           } else {
-            bulk_load(sfs + 512, p.sfb0 + boff, 1024, full);
+            bulk_load(sfs + 512, p.sfb0 + boff, BN / 128 * 512, full);
           }
         }
       }
@@ -379,23 +401,25 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
                                          int num_tiles, volatile int* abort_flag) {
   constexpr int BK = stage_k<MX>();
   constexpr int ST = gemm_stages<MX, EPI, SCH>();
+  constexpr int BN = gemm_bn<MX, EPI, SCH>();
+  constexpr int SB = stage_bytes<MX, EPI, SCH>(), SFB = sf_stage_bytes<MX, EPI, SCH>();
   constexpr bool a_mn = (AM == A_MN_TILE);
   constexpr bool b_mn = (BMO == B_MN_TILE || BMO == B_MN_DUAL_K);
-  constexpr uint32_t idesc128 = idesc_bf16_f32(kBM, kBN, a_mn ? 1 : 0, b_mn ? 1 : 0);
-  constexpr uint32_t idesc64 = idesc_bf16_f32(kBM / 2, kBN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+  constexpr uint32_t idesc128 = idesc_bf16_f32(kBM, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+  constexpr uint32_t idesc64 = idesc_bf16_f32(kBM / 2, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
   int s = 0;
   uint32_t ph = 0;
   int acc = 0;
   uint32_t aph = 0;
   bool issued = false, aborted = false;
   for (int tau = blockIdx.x; tau < num_tiles && !aborted; tau += gridDim.x) {
-    const TileInfo t = gemm_tile<EPI, SCH, BK>(p, tau);
+    const TileInfo t = gemm_tile<EPI, SCH, BK, BN>(p, tau);
     if (!mbar_wait(acce0 + 8 * acc, aph ^ 1, abort_flag, p.status)) {
       aborted = true;
       break;
     }
     tc_fence_after();
-    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
     const uint32_t idesc = t.m64 ? idesc64 : idesc128;
     for (int kb = 0; kb < t.nkb; ++kb) {
       if (!mbar_wait(full0 + 8 * s, ph, abort_flag, p.status)) {
@@ -403,22 +427,22 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
         break;
       }
       tc_fence_after();
-      const uint32_t sA = s_tiles + s * kStageBytes;
+      const uint32_t sA = s_tiles + s * SB;
       const uint32_t sB = sA + kATileBytes;
       if constexpr (MX) {
         // scale ring slot s: reused by stage s + ST, whose data can only
         // have been loaded after these MMAs released stage s
         const uint32_t sfa_t = tmem_base + kSfTmemCol + s * kSfTmemStride;
-        const uint32_t sfs = s_sf + s * kSfStageBytes;
+        const uint32_t sfs = s_sf + s * SFB;
         tc_cp_32x128b(sfa_t, sfs);
         tc_cp_32x128b(sfa_t + 8, sfs + 512);
-        tc_cp_32x128b(sfa_t + 12, sfs + 1024);
+        if constexpr (BN == 256) tc_cp_32x128b(sfa_t + 12, sfs + 1024);
         // both operands K-major: K = 32 is 32 bytes along the swizzled row
         static_assert(!a_mn && !b_mn, "MXFP8 operands are K-major");
 #pragma unroll
         for (int kk = 0; kk < kBKmx / 32; ++kk) {
           tc_mma_mxf8(d_tmem, smem_desc_sw128(sA + kk * 32, 16, 1024),
-                      smem_desc_sw128(sB + kk * 32, 16, 1024), idesc_mxf8(kBM, kBN, kk), sfa_t,
+                      smem_desc_sw128(sB + kk * 32, 16, 1024), idesc_mxf8(kBM, BN, kk), sfa_t,
                       sfa_t + 8, (kb > 0 || kk > 0) ? 1u : 0u);
         }
       } else {
@@ -443,7 +467,7 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
       tc_commit(accf0 + 8 * acc);
     else
       mbar_arrive(accf0 + 8 * acc);
-    if (++acc == acc_bufs<MX>()) {
+    if (++acc == acc_bufs<MX, EPI, SCH>()) {
       acc = 0;
       aph ^= 1;
     }
@@ -497,18 +521,22 @@ struct EpiStager {
   }
 };
 
-template <int EPI, int SCH>
+// Epilogue with two accumulator buffers: every bf16-mode GEMM, and the MXFP8
+// weight gradients (whose output is bf16 as well; 128-column tiles).
+template <int EPI, int SCH, bool MX>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf0, uint32_t acce0,
                                               uint32_t tmem_base, uint32_t s_warp, int num_tiles,
                                               volatile int* abort_flag, int warp_e, int half, int lane) {
-  constexpr bool kWide = epi_wide<false, EPI, SCH>();
+  constexpr bool kWide = epi_wide<MX, EPI, SCH>();
+  constexpr int BN = gemm_bn<MX, EPI, SCH>();
+  constexpr int BK = stage_k<MX>();
   // columns of the tile this warp stores (a half with two warps per quadrant)
-  const int cbeg = kWide ? 128 * half : 0, cend = kWide ? cbeg + 128 : kBN;
+  const int cbeg = kWide ? 128 * half : 0, cend = kWide ? cbeg + 128 : BN;
   int acc = 0;
   uint32_t aph = 0;
-  EpiStager<epi_slots<false, EPI, SCH>()> stg{s_warp, 0, lane};
+  EpiStager<epi_slots<MX, EPI, SCH>()> stg{s_warp, 0, lane};
   for (int tau = blockIdx.x; tau < num_tiles; tau += gridDim.x) {
-    const TileInfo t = gemm_tile<EPI, SCH, kBK>(p, tau);
+    const TileInfo t = gemm_tile<EPI, SCH, BK, BN>(p, tau);
     // Tile row held by this thread's TMEM lane: lane l of warp w is row 32w + l
     // of an M=128 accumulator; an M=64 accumulator keeps rows 16w..16w+15 in
     // lanes 0..15 of each warp (lanes 16..31 hold nothing of this tile).
@@ -529,7 +557,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
     if (!__all_sync(0xffffffffu, ok)) break;
     tc_fence_after();
     const uint32_t tr = tmem_base + (static_cast<uint32_t>(warp_e * 32) << 16) +
-                        static_cast<uint32_t>(acc * kBN);
+                        static_cast<uint32_t>(acc * BN);
 
     if constexpr (SCH == SCHED_WGRAD) {
       const int r0 = t.m0 + warp_e * 32;
@@ -933,12 +961,13 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kerne
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   constexpr int ST = gemm_stages<MX, EPI, SCH>();
-  constexpr int kSfBytes = MX ? ST * kSfStageBytes : 0;
+  constexpr int SB = stage_bytes<MX, EPI, SCH>();
+  constexpr int kSfBytes = ST * sf_stage_bytes<MX, EPI, SCH>();
   constexpr int kStagingBytes = epi_warps<MX, EPI, SCH>() * epi_warp_bytes<MX, EPI, SCH>();
   const uint32_t s_tiles = smem_u32(smem);
-  const uint32_t s_staging = s_tiles + ST * kStageBytes;
+  const uint32_t s_staging = s_tiles + ST * SB;
   const uint32_t s_sf = s_staging + kStagingBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ST * kStageBytes + kStagingBytes + kSfBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ST * SB + kStagingBytes + kSfBytes);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * ST;
   const uint32_t accf0 = empty0 + 8 * ST;
@@ -983,7 +1012,7 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kerne
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int num_tiles = gemm_num_tiles<EPI, SCH>(p);
+  const int num_tiles = gemm_num_tiles<EPI, SCH, gemm_bn<MX, EPI, SCH>()>(p);
 
   if (warp == 0) {
     gemm_producer<AM, BMO, EPI, SCH, MX>(p, s_tiles, s_sf, full0, empty0, num_tiles, abort_flag, lane);
@@ -994,13 +1023,13 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kerne
   } else if (warp >= first_epi_warp<MX, EPI, SCH>()) {
     const int ew = warp - first_epi_warp<MX, EPI, SCH>();
     constexpr int kWarpBytes = epi_warp_bytes<MX, EPI, SCH>();
-    if constexpr (MX)
+    if constexpr (epi_mx_stash<MX, EPI, SCH>())
       gemm_epilogue_mx<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging + ew * kWarpBytes,
-                                 reinterpret_cast<float*>(smem + ST * kStageBytes + ew * kWarpBytes),
+                                 reinterpret_cast<float*>(smem + ST * SB + ew * kWarpBytes),
                                  num_tiles, abort_flag, warp & 3, ew >> 2, lane);
     else
-      gemm_epilogue<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging + ew * kWarpBytes, num_tiles, abort_flag,
-                              warp & 3, ew >> 2, lane);
+      gemm_epilogue<EPI, SCH, MX>(p, accf0, acce0, tmem_base, s_staging + ew * kWarpBytes, num_tiles, abort_flag,
+                                  warp & 3, ew >> 2, lane);
   }
   tc_fence_before();
   __syncthreads();
