@@ -89,3 +89,31 @@ def test_empty_batch_is_a_no_op(lib):
 def test_package_imports_without_gpu():
     import moe_layer_gb300
     assert moe_layer_gb300.moe_forward is _abi.moe_forward
+
+
+def test_mxfp8_weight_buffer_size_matches_documented_layout(lib):
+    """moe.h: W_gate and W_up [E*I, d], W_down [E*d, I], W_down^T [E*I, d] and
+    [W_gate; W_up]^T [E*d, 2I], each followed by its scales (R/128 x K/128
+    blocks of 512 bytes) and one spare block, every piece 256-byte aligned."""
+    E, d, I = 5, 384, 256
+    cfg = _abi.make_config(300, d, I, E, 2, precision=_abi.MOE_MXFP8)
+    al = lambda x: (x + 255) // 256 * 256
+    off = 0
+    for R, K in ((E * I, d), (E * I, d), (E * d, I), (E * I, d), (E * d, 2 * I)):
+        off = al(off) + R * K
+        off = al(off) + (R // 128) * (K // 128) * 512 + 512
+    assert _abi.moe_mxfp8_weights_size(cfg) == off
+    # bf16 configurations have no such buffer
+    assert lib.moe_mxfp8_weights_size(ctypes.byref(_abi.make_config(300, d, I, E, 2)),
+                                      ctypes.byref(ctypes.c_size_t())) == 2
+
+
+def test_mxfp8_forward_needs_the_quantized_weights(lib):
+    """MXFP8 mode rejects a missing or misaligned pre-quantized weight buffer
+    before launching anything (the pointers below are never dereferenced)."""
+    c = _abi.make_config(64, 128, 128, 4, 2, precision=_abi.MOE_MXFP8)
+    fake = 1 << 20  # 256-byte aligned placeholder address
+    w = _abi.MoeWeights(fake, 0, fake, fake, fake, 0, 0, 0, None)
+    assert lib.moe_forward(ctypes.byref(c), fake, ctypes.byref(w), fake, None, fake, None) == 1
+    w.mxfp8 = fake + 16  # not 256-byte aligned
+    assert lib.moe_forward(ctypes.byref(c), fake, ctypes.byref(w), fake, None, fake, None) == 1
