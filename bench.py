@@ -394,13 +394,32 @@ def main():
         inp_e2e = dict(inp)
         inp_e2e["x"] = xd
 
+        # Within a step, dy's upload overlaps the forward and y's download the
+        # backward (a side stream); x goes up before the forward and dx comes
+        # down after the backward.  Every copy of the step is inside it: the
+        # step ends when the side stream has finished too.
+        side = torch.cuda.Stream()
+        prev_done = torch.cuda.Event()
+        prev_done.record(stream)
+
         def e2e_step():
             xd.copy_(xh, non_blocking=True)
-            dyd.copy_(dyh, non_blocking=True)
+            with torch.cuda.stream(side):
+                side.wait_event(prev_done)  # the previous step no longer reads dyd or writes yh
+                dyd.copy_(dyh, non_blocking=True)
+                dy_up = torch.cuda.Event()
+                dy_up.record(side)
             layer.forward(cfg, inp_e2e, bufs, y)
+            y_done = torch.cuda.Event()
+            y_done.record(stream)
+            with torch.cuda.stream(side):
+                side.wait_event(y_done)
+                yh.copy_(y, non_blocking=True)
+            stream.wait_event(dy_up)
             layer.backward(cfg, inp_e2e, dyd, bufs, grads, dx)
-            yh.copy_(y, non_blocking=True)
             dxh.copy_(dx, non_blocking=True)
+            stream.wait_stream(side)  # y's download is part of the step
+            prev_done.record(stream)
 
         e2e_step()
         ms_e2e = max_over_ranks(timed(e2e_step, args.steps))
