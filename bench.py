@@ -394,13 +394,18 @@ def main():
         inp_e2e = dict(inp)
         inp_e2e["x"] = xd
 
-        # Within a step, dy's upload overlaps the forward and y's download the
-        # backward (a side stream); x goes up before the forward and dx comes
-        # down after the backward.  Every copy of the step is inside it: the
-        # step ends when the side stream has finished too.
+        # Within a step, dy's upload overlaps the forward, y's download the
+        # backward, and dx's download the weight gradients (moe_backward
+        # records dx_ready once dx is complete), on a side stream; x goes up
+        # before the forward.  Every copy of the step is inside it: the step
+        # ends when the side stream has finished too.
         side = torch.cuda.Stream()
         prev_done = torch.cuda.Event()
         prev_done.record(stream)
+        dx_ready = torch.cuda.Event()
+        dx_ready.record(stream)  # creates the CUDA event the library records
+        grads_e2e = dict(grads)
+        grads_e2e["dx_ready"] = dx_ready
 
         def e2e_step():
             xd.copy_(xh, non_blocking=True)
@@ -416,9 +421,11 @@ def main():
                 side.wait_event(y_done)
                 yh.copy_(y, non_blocking=True)
             stream.wait_event(dy_up)
-            layer.backward(cfg, inp_e2e, dyd, bufs, grads, dx)
-            dxh.copy_(dx, non_blocking=True)
-            stream.wait_stream(side)  # y's download is part of the step
+            layer.backward(cfg, inp_e2e, dyd, bufs, grads_e2e, dx)
+            with torch.cuda.stream(side):
+                side.wait_event(dx_ready)
+                dxh.copy_(dx, non_blocking=True)
+            stream.wait_stream(side)  # the downloads are part of the step
             prev_done.record(stream)
 
         e2e_step()

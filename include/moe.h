@@ -92,6 +92,9 @@ typedef struct {
   void* dWs_up;     /* [I_s, d] bf16 */
   void* dWs_down;   /* [d, I_s] bf16 */
   float* d_topk_w;  /* [T, top_k] fp32 router-weight gradient dL/dg, or NULL */
+  void* dx_ready;   /* cudaEvent_t or NULL: when given, moe_backward records it on the stream
+                       as soon as dx is complete, before the weight gradients are computed,
+                       so that a caller can start using dx (e.g. copy it out) early */
 } moe_grads;
 
 /* Byte sizes of the caller-allocated buffers for a configuration:

@@ -40,7 +40,7 @@ class MoeWeights(ctypes.Structure):
 class MoeGrads(ctypes.Structure):
     _fields_ = [("dW_router", ctypes.c_void_p), ("dW_gate", ctypes.c_void_p), ("dW_up", ctypes.c_void_p),
                 ("dW_down", ctypes.c_void_p), ("dWs_gate", ctypes.c_void_p), ("dWs_up", ctypes.c_void_p),
-                ("dWs_down", ctypes.c_void_p), ("d_topk_w", ctypes.c_void_p)]
+                ("dWs_down", ctypes.c_void_p), ("d_topk_w", ctypes.c_void_p), ("dx_ready", ctypes.c_void_p)]
 
 
 class MoeError(RuntimeError):
@@ -160,9 +160,16 @@ def make_weights(W_router, W_gate, W_up, W_down, router_bias=None, Ws_gate=None,
 
 
 def make_grads(dW_router, dW_gate, dW_up, dW_down, dWs_gate=None, dWs_up=None, dWs_down=None,
-               d_topk_w=None) -> MoeGrads:
+               d_topk_w=None, dx_ready=None) -> MoeGrads:
+    """dx_ready: optional torch.cuda.Event (recorded by moe_backward once dx is
+    complete, before the weight gradients)."""
+    ev = None
+    if dx_ready is not None:
+        ev = dx_ready.cuda_event if hasattr(dx_ready, "cuda_event") else int(dx_ready)
+        if not ev:
+            raise ValueError("dx_ready event has no CUDA event yet: record it once before passing it")
     return MoeGrads(_ptr(dW_router), _ptr(dW_gate), _ptr(dW_up), _ptr(dW_down), _ptr(dWs_gate),
-                    _ptr(dWs_up), _ptr(dWs_down), _ptr(d_topk_w))
+                    _ptr(dWs_up), _ptr(dWs_down), _ptr(d_topk_w), ev)
 
 
 def moe_forward(cfg, x, weights: MoeWeights, y, saved, ws, stream=None):

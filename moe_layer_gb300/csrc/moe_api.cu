@@ -895,6 +895,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
   MOE_LAUNCH(PL_UNPERMUTE, st, launch_unpermute(w.dxp, s.S ? w.dxs : nullptr, rt.route_row_pad, rt.topk_idx,
                                                 w.dl_tk, static_cast<const __nv_bfloat16*>(wts->W_router), T, d,
                                                 k, static_cast<__nv_bfloat16*>(dx), st));
+  // dx is complete: the weight gradients below do not touch it
+  if (g->dx_ready) MOE_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(g->dx_ready), st));
   MOE_LAUNCH(PL_ROUTER_WGRAD, st, launch_router_wgrad(w.dl_row, rt.perm_token_pad, rt.row_start, rt.counts,
                                                       static_cast<const __nv_bfloat16*>(x), E, d, g->dW_router, st));
   // weight gradients, reduced over each expert's full row range (no split-K)

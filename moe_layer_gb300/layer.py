@@ -62,7 +62,7 @@ def alloc_grads(cfg: _abi.MoeConfig, device="cuda", with_topk: bool = True) -> d
 
 def grads_struct(g: dict) -> _abi.MoeGrads:
     return _abi.make_grads(g["dW_router"], g["dW_gate"], g["dW_up"], g["dW_down"], g["dWs_gate"],
-                           g["dWs_up"], g["dWs_down"], g["d_topk_w"])
+                           g["dWs_up"], g["dWs_down"], g["d_topk_w"], g.get("dx_ready"))
 
 
 def forward(cfg, inp: dict, bufs: MoEBuffers, y=None, stream=None):

@@ -190,3 +190,28 @@ def test_empty_batch():
     x = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
     w = _abi.MoeWeights()
     _abi.moe_forward(cfg, x, w, x, bufs.saved, bufs.fwd_ws)
+
+
+def test_dx_ready_event_marks_complete_dx():
+    """moe_backward records the optional dx_ready event once dx is final: a
+    copy taken on another stream after that event equals dx after the whole
+    backward (the weight gradients computed after it do not touch dx)."""
+    shape = SHAPES["wide"]
+    inp = _cuda(make_inputs(shape, seed=7, with_dy=True))
+    cfg = _abi.make_config(shape.T, shape.d, shape.I, shape.E, shape.k, shape.n_shared, shape.I_shared)
+    bufs = layer.MoEBuffers(cfg)
+    layer.forward(cfg, inp, bufs)
+    grads = layer.alloc_grads(cfg)
+    ev = torch.cuda.Event()
+    ev.record()
+    grads["dx_ready"] = ev
+    dx = torch.empty(shape.T, shape.d, dtype=torch.bfloat16, device="cuda")
+    early = torch.empty_like(dx)
+    side = torch.cuda.Stream()
+    layer.backward(cfg, inp, inp["dy"], bufs, grads, dx)
+    with torch.cuda.stream(side):
+        side.wait_event(ev)
+        early.copy_(dx)
+    torch.cuda.synchronize()
+    assert torch.equal(early, dx)
+    assert _abi.moe_read_device_status(bufs.bwd_ws) == 0
