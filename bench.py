@@ -100,11 +100,14 @@ def _kernel_flops(name, s):
     return table.get(name)
 
 
-# DRAM bytes per launch (read + write) of kernels measured with ncu
-# (dram__bytes_read.sum + dram__bytes_write.sum, one pass) on the named
-# workload; see profiles/tc_gemm_dgrad_gateup.md.  Remove an entry when its
-# kernel changes.
-NCU_TRAFFIC = {}
+# DRAM bytes per launch (read + write) of the dominant kernel, measured with
+# ncu (dram__bytes_read.sum + dram__bytes_write.sum, one pass over the full
+# workload, first timed step).  An entry must be removed or re-measured when
+# its kernel changes.
+NCU_TRAFFIC = {
+    ("dsv3", "gateup_routed"): 18.049e9 + 1.697e9,
+    ("dsv3_mxfp8", "gateup_routed"): 9.031e9 + 1.496e9,
+}
 
 
 class ClockSampler:
