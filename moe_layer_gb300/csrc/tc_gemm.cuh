@@ -25,18 +25,20 @@
 //          into a ring of TMEM columns next to the accumulator before issuing
 //          the stage's four MMAs.
 //
-// Roles per CTA (256 threads, one CTA per SM, persistent over tiles):
+// Roles per CTA (one CTA per SM, persistent over tiles; 256 threads):
 //   warp 0      TMA producer (lane 0 issues the tile loads)
 //   warp 1      MMA issuer (lane 0)
 //   warp 2      TMEM allocator (512 columns)
 //   warps 4..7  epilogue: TMEM -> registers -> fused math -> swizzled smem
-//               staging -> TMA bulk stores
-// Pipelines: kStages smem stages (full/empty mbarriers) and accumulator
-// buffers (acc_full/acc_empty): two 256-column buffers in bf16 mode so the
-// epilogue of tile i overlaps the MMAs of tile i+1; one in MXFP8 mode, whose
-// other TMEM columns hold the scale ring.  Every wait is bounded (see
-// mbar_wait): a stuck pipeline records MOE_ERR_DEVICE_TIMEOUT in the status
-// word and the CTA exits cleanly.
+//               staging -> TMA bulk stores (or direct stores)
+// The MXFP8 SwiGLU backward runs 320 threads with epilogue warps 2..9, two per
+// TMEM lane quadrant (see epi_wide).
+// Pipelines: smem stages (full/empty mbarriers) and accumulator buffers
+// (acc_full/acc_empty): two 256-column buffers in bf16 mode so the epilogue of
+// tile i overlaps the MMAs of tile i+1; one in MXFP8 mode, whose other TMEM
+// columns hold the scale ring and a stash for the epilogue.  Every wait is
+// bounded (see mbar_wait): a stuck pipeline records MOE_ERR_DEVICE_TIMEOUT in
+// the status word and the CTA exits cleanly.
 #pragma once
 #include "mx_common.cuh"
 #include "ptx.cuh"
@@ -52,7 +54,7 @@ constexpr int kBM = 128;  // rows per tile (TMEM lanes)
 constexpr int kBN = 256;  // accumulator columns per tile
 constexpr int kBK = 64;   // bf16 K per stage: one 128-byte swizzle row
 constexpr int kBKmx = 128;  // MXFP8 K per stage: one 128-byte swizzle row of E4M3
-constexpr int kStages = 4;  // the most stages any instantiation uses
+constexpr int kStages = 4;  // pipeline stages with 256-column tiles
 constexpr int kATileBytes = kBM * 128;  // 16 KB (128 rows of 128 bytes)
 constexpr int kBTileBytes = kBN * 128;  // 32 KB
 constexpr int kStageBytes = kATileBytes + kBTileBytes;
@@ -162,9 +164,10 @@ struct GemmParams {
   const uint8_t* sfb1;     // scales of the second stack (B_K_DUAL_N)
   long long sfb_rb;
   // ---- epilogue
-  void* out;               // direct-store outputs: EPI_F32_BIAS logits; EPI_SWIGLU_BWD [da|db]
+  void* out;               // direct-store outputs: EPI_F32_BIAS logits; bf16 EPI_SWIGLU_BWD [da|db];
+                           // MXFP8 EPI_SWIGLU_FWD the saved [a|b] rows
   long long ldo;
-  void* out2;              // EPI_SWIGLU_BWD g*h
+  void* out2;              // bf16 EPI_SWIGLU_BWD g*h
   long long ldo2;
   float* out3;
   int ldo3;
