@@ -102,10 +102,9 @@ def _kernel_flops(name, s):
 
 # DRAM bytes per launch (read + write) of the dominant kernel, measured with
 # ncu (dram__bytes_read.sum + dram__bytes_write.sum, one pass over the full
-# workload, first timed step).  An entry must be removed or re-measured when
-# its kernel changes.
+# workload, first timed step; summed over the kernels of the step).  An entry
+# must be removed or re-measured when its kernel changes.
 NCU_TRAFFIC = {
-    ("dsv3", "gateup_routed"): 18.049e9 + 1.697e9,
     ("dsv3_mxfp8", "gateup_routed"): 9.031e9 + 1.496e9,
 }
 
@@ -370,11 +369,13 @@ def main():
     tflops = value * 3 * flops_tok / 1e12
     fwd_value = tokens / (ms_fwd * 1e-3)
 
-    launches = sum(n for n, _ in prof.values())
-    kern_ms = {k: v[1] for k, v in prof.items()}
+    # prof: {step: (calls, kernels, total ms)}; a grouped row GEMM step runs as
+    # two kernels (its 2-SM pass and the pass over leftover tiles)
+    launches = sum(nk for _, nk, _ in prof.values())
+    kern_ms = {k: v[2] for k, v in prof.items()}
     total_kern = sum(kern_ms.values())
     top = max(kern_ms, key=kern_ms.get)
-    n_top, ms_top = prof[top]
+    n_top, nk_top, ms_top = prof[top]
     fl = _kernel_flops(top, s)
     roofline = None
     if fl is not None:
@@ -384,6 +385,7 @@ def main():
                     "peak": t_sust, "unit": "TFLOP/s",
                     "frac": achieved / t_sust, "traffic": traffic,
                     "algorithmic_flops_per_launch": fl,
+                    "kernels_per_launch": nk_top / n_top,
                     "peak_src": t_src + " sustained (kernel timed inside a long step)"}
 
     e2e = None

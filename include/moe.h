@@ -188,12 +188,15 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
 moe_status moe_read_device_status(void* ws, void* stream);
 
 /* Diagnostics, not part of the layer's computation.  While profiling is
- * enabled (process-wide), every kernel launch of this library is bracketed by
+ * enabled (process-wide), every launch step of this library is bracketed by
  * two CUDA events recorded on the launching stream, which costs a few
- * microseconds per launch.  moe_profile_report waits for the recorded events,
- * writes one line per kernel, "<name> <launches> <total_ms>\n", into buf
- * (host memory, NUL-terminated, truncated to buflen bytes) and clears the
- * records.  Returns MOE_ERR_CUDA if an event could not be read. */
+ * microseconds per step.  moe_profile_report waits for the recorded events,
+ * writes one line per step name, "<name> <calls> <kernels> <total_ms>\n"
+ * (calls: timed calls; kernels: kernels they launched, more than calls where
+ * one step runs as several kernels, e.g. a grouped GEMM's 2-SM pass and its
+ * pass over leftover tiles), into buf (host memory, NUL-terminated, truncated
+ * to buflen bytes) and clears the records.  Returns MOE_ERR_CUDA if an event
+ * could not be read. */
 moe_status moe_profile_enable(int enable);
 moe_status moe_profile_report(char* buf, size_t buflen);
 

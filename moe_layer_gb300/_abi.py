@@ -192,11 +192,11 @@ def moe_profile_enable(enable: bool = True):
 
 
 def moe_profile_report() -> dict:
-    """{kernel name: (launches, total_ms)} for the launches recorded since the last report."""
+    """{step name: (calls, kernels, total_ms)} for the calls recorded since the last report."""
     buf = ctypes.create_string_buffer(1 << 16)
     _check(load().moe_profile_report(buf, len(buf)), "moe_profile_report")
     out = {}
     for line in buf.value.decode().splitlines():
-        name, n, ms = line.split()
-        out[name] = (int(n), float(ms))
+        name, n, nk, ms = line.split()
+        out[name] = (int(n), int(nk), float(ms))
     return out

@@ -1,5 +1,6 @@
 // Launch helper for one instantiation of the tensor-core GEMM: sets the
-// dynamic shared-memory limit once per device, then launches persistently.
+// dynamic shared-memory limit once per device, then launches persistently
+// (2-SM instantiations as clusters of two CTAs, on an even grid).
 #pragma once
 #include <atomic>
 
@@ -23,8 +24,43 @@ cudaError_t launch_gemm_inst(const GemmParams& p, int grid, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  kfn<<<grid, threads, smem, st>>>(p);
-  return cudaGetLastError();
+  if constexpr (SCH == SCHED_ROWS2) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid < 2 ? 2 : grid & ~1));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kfn, p);
+  } else {
+    kfn<<<grid, threads, smem, st>>>(p);
+    return cudaGetLastError();
+  }
+}
+
+// The bf16 row GEMMs other than the router projection: a 2-SM pass over the
+// pairs of m-tiles, then a 1-SM pass over the last m-tile of every group
+// (or dense row range) with an odd number of them.  Grouped problems launch
+// the second pass always (their tile counts live on the device; with no odd
+// group its CTAs exit at once).
+template <int AM, int BMO, int EPI>
+cudaError_t launch_rows_two_pass(const GemmParams& p, int grid, cudaStream_t st) {
+  const int dense_mt = p.dense_rows > 0 ? (p.dense_rows + kBM - 1) / kBM : 0;
+  if (p.dense_rows == 0 || dense_mt >= 2) {
+    const cudaError_t e = launch_gemm_inst<AM, BMO, EPI, SCHED_ROWS2>(p, grid, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (p.dense_rows > 0 && dense_mt % 2 == 0) return cudaSuccess;
+  GemmParams q = p;
+  q.part = 1;
+  if (p.dense_rows == 0 || dense_mt >= 2) ++extra_kernel_launches();
+  return launch_gemm_inst<AM, BMO, EPI, SCHED_ROWS>(q, grid, st);
 }
 
 cudaError_t launch_gemm_fwd(GemmKind kind, const GemmParams& p, int grid, cudaStream_t st);

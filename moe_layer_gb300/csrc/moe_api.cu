@@ -58,6 +58,7 @@ static const char* const kProfNames[PL_COUNT] = {
 
 struct ProfRecord {
   int label;
+  int kernels;
   cudaEvent_t start, stop;
 };
 struct Profiler {
@@ -70,6 +71,11 @@ Profiler& profiler() {
   return p;
 }
 
+int& extra_kernel_launches() {
+  static thread_local int n = 0;
+  return n;
+}
+
 template <class F>
 moe_status prof_launch(int label, cudaStream_t st, F&& f) {
   Profiler& P = profiler();
@@ -77,11 +83,12 @@ moe_status prof_launch(int label, cudaStream_t st, F&& f) {
   cudaEvent_t a = nullptr, b = nullptr;
   if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) return MOE_ERR_CUDA;
   cudaEventRecord(a, st);
+  extra_kernel_launches() = 0;
   const cudaError_t e = f();
   cudaEventRecord(b, st);
   {
     std::lock_guard<std::mutex> g(P.mu);
-    P.recs.push_back({label, a, b});
+    P.recs.push_back({label, 1 + extra_kernel_launches(), a, b});
   }
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -118,6 +125,8 @@ struct Routing {
   int32_t* offsets;
   int32_t* row_start;
   int32_t* tile_start;
+  int32_t* pair_start;  // prefix of floor(tiles / 2) per expert
+  int32_t* rem_start;   // prefix of experts with an odd tile count
   int32_t* perm_token;
   int32_t* route_row;
   int32_t* perm_token_pad;
@@ -132,6 +141,8 @@ void carve_routing(Carver& c, const Shape& s, Routing& r) {
   r.offsets = c.take<int32_t>(s.E + 1);
   r.row_start = c.take<int32_t>(s.E + 1);
   r.tile_start = c.take<int32_t>(s.E + 1);
+  r.pair_start = c.take<int32_t>(s.E + 1);
+  r.rem_start = c.take<int32_t>(s.E + 1);
   r.perm_token = c.take<int32_t>(s.R);
   r.route_row = c.take<int32_t>(s.T * s.k);
   r.perm_token_pad = c.take<int32_t>(s.Rp);
@@ -341,6 +352,8 @@ moe_status mnmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, i
   return MOE_OK;
 }
 
+// The bf16 row GEMMs other than the router projection load B in halves: 128-row
+// boxes (K-major) or two 64-column chunks (MN-major); see launch_rows_two_pass.
 // Output map: boxes of 64 columns x 32 rows (one epilogue warp's staging box).
 moe_status omap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
   return tmap(m, base, rows, cols, 64, 32);
@@ -398,7 +411,7 @@ moe_status run_routing(const Shape& s, const void* x, const void* W_router, cons
                              chunk_base, rt.counts, st));
   MOE_LAUNCH(PL_SCATTER, st, launch_scatter(rt.topk_idx, rt.topk_w, static_cast<int>(s.T), static_cast<int>(s.E),
                           static_cast<int>(s.k), static_cast<int>(s.ra), chunk_base, rt.counts, rt.offsets, rt.row_start,
-                          rt.tile_start, rt.perm_token, rt.route_row, rt.perm_token_pad,
+                          rt.tile_start, rt.pair_start, rt.rem_start, rt.perm_token, rt.route_row, rt.perm_token_pad,
                           rt.route_row_pad, rt.perm_w_pad, st));
   return MOE_OK;
 }
@@ -448,6 +461,8 @@ moe_status forward_routed_mx(const Shape& s, const moe_weights* wts, const Routi
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.tile_start = rt.tile_start;
+    p.pair_start = rt.pair_start;
+    p.rem_start = rt.rem_start;
     p.counts = rt.counts;
     p.N = I;
     p.K = d;
@@ -474,6 +489,8 @@ moe_status forward_routed_mx(const Shape& s, const moe_weights* wts, const Routi
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.tile_start = rt.tile_start;
+    p.pair_start = rt.pair_start;
+    p.rem_start = rt.rem_start;
     p.counts = rt.counts;
     p.N = d;
     p.K = I;
@@ -690,6 +707,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
       p.tmO0h = p.tmO1h;
     }
     p.tile_start = rt.tile_start;
+    p.pair_start = rt.pair_start;
+    p.rem_start = rt.rem_start;
     p.store_ab = saved ? 1 : 0;
     p.I = I;
     p.status = w.status;
@@ -700,7 +719,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, w.h, s.Rp, s.I, 64, kBM));
-    MOE_TRY(tmap(&p.tmB0, wts->W_down, s.E * s.d, s.I, 64, kBN));
+    MOE_TRY(tmap(&p.tmB0, wts->W_down, s.E * s.d, s.I, 64, kBN / 2));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.counts = rt.counts;
@@ -709,6 +728,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.b_group_rows = d;
     MOE_TRY(omap2(&p.tmO0, &p.tmO0h, w.o, s.Rp, s.d));
     p.tile_start = rt.tile_start;
+    p.pair_start = rt.pair_start;
+    p.rem_start = rt.rem_start;
     p.row_scale = rt.perm_w_pad;
     p.status = w.status;
     MOE_LAUNCH(PL_DOWN_ROUTED, st, launch_gemm(GK_DOWN, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
@@ -719,7 +740,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, w.hs, s.T, s.Is, 64, kBM));
-    MOE_TRY(tmap(&p.tmB0, wts->Ws_down, s.d, s.Is, 64, kBN));
+    MOE_TRY(tmap(&p.tmB0, wts->Ws_down, s.d, s.Is, 64, kBN / 2));
     p.dense_rows = T;
     p.N = d;
     p.K = static_cast<int>(s.Is);
@@ -784,6 +805,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.ab = sv.ab;
     p.I = I;
     p.tile_start = rt.tile_start;
+    p.pair_start = rt.pair_start;
+    p.rem_start = rt.rem_start;
     p.row_scale = rt.perm_w_pad;
     p.qt = w.dadbt;
     p.qt_ld = s.Rp;
@@ -803,7 +826,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, w.dyp, s.Rp, s.d, 64, kBM));
-    MOE_TRY(mnmap(&p.tmB0, wts->W_down, s.E * s.d, s.I, 4));
+    MOE_TRY(mnmap(&p.tmB0, wts->W_down, s.E * s.d, s.I, 2));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.counts = rt.counts;
@@ -819,6 +842,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.ab = sv.ab;
     p.I = I;
     p.tile_start = rt.tile_start;
+    p.pair_start = rt.pair_start;
+    p.rem_start = rt.rem_start;
     p.row_scale = rt.perm_w_pad;
     p.status = w.status;
     MOE_LAUNCH(PL_DGRAD_DOWN_ROUTED, st, launch_gemm(GK_DGRAD_DOWN, p, grid_for(cdiv(s.Rp, kBM) * s.nparts), st));
@@ -827,7 +852,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, dy, s.T, s.d, 64, kBM));
-    MOE_TRY(mnmap(&p.tmB0, wts->Ws_down, s.d, s.Is, 4));
+    MOE_TRY(mnmap(&p.tmB0, wts->Ws_down, s.d, s.Is, 2));
     p.dense_rows = T;
     p.N = Is;
     p.K = d;
@@ -857,14 +882,16 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.b_group_rows = d;
     MOE_TRY(omap(&p.tmO0, w.dxp, s.Rp, s.d));
     p.tile_start = rt.tile_start;
+    p.pair_start = rt.pair_start;
+    p.rem_start = rt.rem_start;
     p.status = w.status;
     MOE_LAUNCH(PL_DGRAD_GATEUP_ROUTED, st, launch_gemm(GK_MX_DGRAD_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
   } else {
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, w.dadb, s.Rp, 2 * s.I, 64, kBM));
-    MOE_TRY(mnmap(&p.tmB0, wts->W_gate, s.E * s.I, s.d, 4));
-    MOE_TRY(mnmap(&p.tmB1, wts->W_up, s.E * s.I, s.d, 4));
+    MOE_TRY(mnmap(&p.tmB0, wts->W_gate, s.E * s.I, s.d, 2));
+    MOE_TRY(mnmap(&p.tmB1, wts->W_up, s.E * s.I, s.d, 2));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.counts = rt.counts;
@@ -874,6 +901,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.b_split = I;
     MOE_TRY(omap2(&p.tmO0, &p.tmO0h, w.dxp, s.Rp, s.d));
     p.tile_start = rt.tile_start;
+    p.pair_start = rt.pair_start;
+    p.rem_start = rt.rem_start;
     p.status = w.status;
     MOE_LAUNCH(PL_DGRAD_GATEUP_ROUTED, st, launch_gemm(GK_DGRAD_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
   }
@@ -881,8 +910,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, w.dadbs, s.T, 2 * s.Is, 64, kBM));
-    MOE_TRY(mnmap(&p.tmB0, wts->Ws_gate, s.Is, s.d, 4));
-    MOE_TRY(mnmap(&p.tmB1, wts->Ws_up, s.Is, s.d, 4));
+    MOE_TRY(mnmap(&p.tmB0, wts->Ws_gate, s.Is, s.d, 2));
+    MOE_TRY(mnmap(&p.tmB1, wts->Ws_up, s.Is, s.d, 2));
     p.dense_rows = T;
     p.N = d;
     p.K = 2 * Is;
@@ -985,7 +1014,7 @@ moe_status moe_profile_report(char* buf, size_t buflen) {
     recs.swap(P.recs);
   }
   double total[PL_COUNT] = {0};
-  long long count[PL_COUNT] = {0};
+  long long count[PL_COUNT] = {0}, kernels[PL_COUNT] = {0};
   moe_status status = MOE_OK;
   for (const ProfRecord& r : recs) {
     float ms = 0.f;
@@ -993,6 +1022,7 @@ moe_status moe_profile_report(char* buf, size_t buflen) {
       status = MOE_ERR_CUDA;
     total[r.label] += ms;
     count[r.label] += 1;
+    kernels[r.label] += r.kernels;
     cudaEventDestroy(r.start);
     cudaEventDestroy(r.stop);
   }
@@ -1000,7 +1030,7 @@ moe_status moe_profile_report(char* buf, size_t buflen) {
   for (int i = 0; i < PL_COUNT; ++i) {
     if (!count[i]) continue;
     char line[128];
-    snprintf(line, sizeof(line), "%s %lld %.6f\n", kProfNames[i], count[i], total[i]);
+    snprintf(line, sizeof(line), "%s %lld %lld %.6f\n", kProfNames[i], count[i], kernels[i], total[i]);
     out += line;
   }
   if (buf && buflen) {

@@ -33,10 +33,12 @@ cudaError_t launch_chunk_scan(const int32_t* chunk_counts, int nchunk, int E, in
                               int32_t* counts, cudaStream_t st);
 cudaError_t launch_scatter(const int32_t* topk_idx, const float* topk_w, int T, int E, int k,
                            int row_align, const int32_t* chunk_base, const int32_t* counts, int32_t* offsets,
-                           int32_t* row_start, int32_t* tile_start, int32_t* perm_token,
-                           int32_t* route_row,
+                           int32_t* row_start, int32_t* tile_start, int32_t* pair_start, int32_t* rem_start,
+                           int32_t* perm_token, int32_t* route_row,
                            int32_t* perm_token_pad, int32_t* route_row_pad, float* perm_w_pad,
                            cudaStream_t st);
+// pair_start / rem_start (optional, [E+1]): prefixes of floor(tiles / 2) and
+// of (tiles & 1) per expert, tiles = its 128-row GEMM tiles.
 
 // ---- memory-bound kernels (elementwise.cu)
 cudaError_t launch_combine(const __nv_bfloat16* o, const __nv_bfloat16* ys,
@@ -92,6 +94,10 @@ enum GemmKind : int {
   GK_COUNT
 };
 cudaError_t launch_gemm(GemmKind kind, const GemmParams& p, int grid, cudaStream_t st);
+// Kernels launched beyond the first by the current launch call on this host
+// thread (a launch helper that issues several adds to it; the per-kernel
+// timing resets and reads it around each call).
+int& extra_kernel_launches();
 int gemm_smem_bytes();
 
 // Number of SMs of the current device (cached per device).

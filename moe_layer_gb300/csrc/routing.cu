@@ -149,58 +149,76 @@ __global__ void __launch_bounds__(kChunkWarps * 32)
                    int E, int k, int align, const int32_t* __restrict__ chunk_base,
                    const int32_t* __restrict__ counts, int32_t* __restrict__ offsets_out,
                    int32_t* __restrict__ row_start_out, int32_t* __restrict__ tile_start_out,
+                   int32_t* __restrict__ pair_start_out, int32_t* __restrict__ rem_start_out,
                    int32_t* __restrict__ perm_token,
                    int32_t* __restrict__ route_row, int32_t* __restrict__ perm_token_pad,
                    int32_t* __restrict__ route_row_pad, float* __restrict__ perm_w_pad) {
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_rs[kMaxExperts + 1];
   __shared__ int s_ts[kMaxExperts + 1];
+  __shared__ int s_ps[kMaxExperts + 1];
+  __shared__ int s_qs[kMaxExperts + 1];
   __shared__ int wcnt[kChunkWarps][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // 1. expert offsets: exclusive prefix of counts, of padded row counts and of
-  //    GEMM row tiles
+  // 1. expert offsets: exclusive prefix of counts, of padded row counts, of
+  //    GEMM row tiles, of pairs of row tiles and of experts with an odd
+  //    number of row tiles (the GEMMs that run tile pairs on SM pairs)
   if (warp == 0) {
     const int per = (E + 31) / 32;
-    int sum = 0, psum = 0, tsum = 0;
+    int sum = 0, psum = 0, tsum = 0, qsum = 0, osum = 0;
     for (int i = 0; i < per; ++i) {
       const int e = lane * per + i;
       if (e < E) {
         const int c = __ldg(counts + e);
+        const int tiles = row_tiles(c, align);
         sum += c;
         psum += pad_rows(c, align);
-        tsum += row_tiles(c, align);
+        tsum += tiles;
+        qsum += tiles >> 1;
+        osum += tiles & 1;
       }
     }
-    int inc = sum, pinc = psum, tinc = tsum;
+    int inc = sum, pinc = psum, tinc = tsum, qinc = qsum, oinc = osum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int o = __shfl_up_sync(kFull, inc, off);
       const int po = __shfl_up_sync(kFull, pinc, off);
       const int to = __shfl_up_sync(kFull, tinc, off);
+      const int qo = __shfl_up_sync(kFull, qinc, off);
+      const int oo = __shfl_up_sync(kFull, oinc, off);
       if (lane >= off) {
         inc += o;
         pinc += po;
         tinc += to;
+        qinc += qo;
+        oinc += oo;
       }
     }
-    int run = inc - sum, prun = pinc - psum, trun = tinc - tsum;
+    int run = inc - sum, prun = pinc - psum, trun = tinc - tsum, qrun = qinc - qsum, orun = oinc - osum;
     for (int i = 0; i < per; ++i) {
       const int e = lane * per + i;
       if (e < E) {
         s_off[e] = run;
         s_rs[e] = prun;
         s_ts[e] = trun;
+        s_ps[e] = qrun;
+        s_qs[e] = orun;
         const int c = __ldg(counts + e);
+        const int tiles = row_tiles(c, align);
         run += c;
         prun += pad_rows(c, align);
-        trun += row_tiles(c, align);
+        trun += tiles;
+        qrun += tiles >> 1;
+        orun += tiles & 1;
       }
     }
     if (lane == 31) {
       s_off[E] = inc;
       s_rs[E] = pinc;
       s_ts[E] = tinc;
+      s_ps[E] = qinc;
+      s_qs[E] = oinc;
     }
   }
   for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) wcnt[i / E][i % E] = 0;
@@ -210,6 +228,8 @@ __global__ void __launch_bounds__(kChunkWarps * 32)
       offsets_out[e] = s_off[e];
       row_start_out[e] = s_rs[e];
       tile_start_out[e] = s_ts[e];
+      if (pair_start_out) pair_start_out[e] = s_ps[e];
+      if (rem_start_out) rem_start_out[e] = s_qs[e];
     }
   }
   // padding rows of the padded layout: no token, weight 0
@@ -284,12 +304,13 @@ cudaError_t launch_chunk_scan(const int32_t* chunk_counts, int nchunk, int E, in
 
 cudaError_t launch_scatter(const int32_t* topk_idx, const float* topk_w, int T, int E, int k,
                            int row_align, const int32_t* chunk_base, const int32_t* counts, int32_t* offsets,
-                           int32_t* row_start, int32_t* tile_start, int32_t* perm_token,
-                           int32_t* route_row, int32_t* perm_token_pad, int32_t* route_row_pad,
-                           float* perm_w_pad, cudaStream_t st) {
+                           int32_t* row_start, int32_t* tile_start, int32_t* pair_start, int32_t* rem_start,
+                           int32_t* perm_token, int32_t* route_row, int32_t* perm_token_pad,
+                           int32_t* route_row_pad, float* perm_w_pad, cudaStream_t st) {
   const int nchunk = (T + kChunkTokens - 1) / kChunkTokens;
   scatter_kernel<<<nchunk, kChunkWarps * 32, 0, st>>>(topk_idx, topk_w, T, E, k, row_align, chunk_base, counts,
-                                                      offsets, row_start, tile_start, perm_token,
+                                                      offsets, row_start, tile_start, pair_start, rem_start,
+                                                      perm_token,
                                                       route_row, perm_token_pad, route_row_pad,
                                                       perm_w_pad);
   return cudaGetLastError();

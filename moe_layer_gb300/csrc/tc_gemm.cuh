@@ -48,7 +48,9 @@ namespace moe {
 enum AMode : int { A_K_TILE = 0, A_MN_TILE = 1 };
 enum BMode : int { B_K_TILE = 0, B_K_DUAL_N = 1, B_MN_TILE = 2, B_MN_DUAL_K = 3 };
 enum EpiMode : int { EPI_F32_BIAS = 0, EPI_SWIGLU_FWD = 1, EPI_BF16 = 2, EPI_SWIGLU_BWD = 3 };
-enum SchedMode : int { SCHED_ROWS = 0, SCHED_WGRAD = 1 };
+// SCHED_ROWS2: row tiles in pairs of m-tiles of one group on one n-tile, each
+// pair computed by a cluster of two CTAs with cta_group::2 MMAs (M = 256).
+enum SchedMode : int { SCHED_ROWS = 0, SCHED_WGRAD = 1, SCHED_ROWS2 = 2 };
 
 constexpr int kBM = 128;  // rows per tile (TMEM lanes)
 constexpr int kBN = 256;  // accumulator columns per tile
@@ -75,8 +77,12 @@ template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int gemm_bn() { return kBN; }
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int acc_bufs() { return (MX && gemm_bn<MX, EPI, SCH>() == kBN) ? 1 : 2; }
+// A stage holds the A tile and the B tile, or in the 2-SM mode this CTA's
+// half of B.
 template <bool MX, int EPI, int SCH>
-__host__ __device__ constexpr int stage_bytes() { return kATileBytes + gemm_bn<MX, EPI, SCH>() * 128; }
+__host__ __device__ constexpr int stage_bytes() {
+  return kATileBytes + (SCH == SCHED_ROWS2 ? gemm_bn<MX, EPI, SCH>() / 2 : gemm_bn<MX, EPI, SCH>()) * 128;
+}
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int sf_stage_bytes() { return MX ? 512 + gemm_bn<MX, EPI, SCH>() / 128 * 512 : 0; }
 
@@ -96,11 +102,13 @@ template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int gemm_threads() {
   return 32 * (first_epi_warp<MX, EPI, SCH>() + epi_warps<MX, EPI, SCH>());
 }
-// Pipeline stages: four 48 KB stages, five 32 KB ones with 128-column tiles.
-// (Three stages with four staging boxes per warp were measured for the
-// weight gradients: slower than four stages.)
+// Pipeline stages: four 48 KB stages, six 32 KB ones in the 2-SM mode, five
+// 32 KB ones with 128-column tiles.  (Three stages with four staging boxes
+// per warp were measured for the weight gradients: slower than four stages.)
 template <bool MX, int EPI, int SCH>
-__host__ __device__ constexpr int gemm_stages() { return gemm_bn<MX, EPI, SCH>() == kBN ? kStages : 5; }
+__host__ __device__ constexpr int gemm_stages() {
+  return SCH == SCHED_ROWS2 ? 6 : (gemm_bn<MX, EPI, SCH>() == kBN ? kStages : 5);
+}
 // MXFP8 kernels with a single accumulator run the stash epilogue; the ones
 // with two (the weight gradients) run the bf16-mode epilogue.
 template <bool MX, int EPI, int SCH>
@@ -128,6 +136,21 @@ __host__ __device__ constexpr int gemm_smem_bytes_for() {
 }
 constexpr int kGemmSmemBytes = gemm_smem_bytes_for<false, 0, 0>();
 
+// The bf16 row GEMMs other than the router projection run as two launches:
+// a 2-SM pass (SCHED_ROWS2) over pairs of m-tiles, and a 1-SM pass over the
+// last m-tile of every group with an odd number of them.  A 128 x 256 tile
+// per SM stages 48 KB per K step and its MMAs read as much again from shared
+// memory; with the B tile split between the two SMs of a pair both become
+// 32 KB.  Measured at the DSV3 shape, staging only half of the gate/up weight
+// tile took that kernel from 5.73 to 5.17 ms, while multicasting halves of a
+// shared operand between two CTAs (fewer L2 reads, same shared-memory
+// traffic) gained nothing: shared-memory traffic per SM bounds these GEMMs.
+// Both passes load B in halves (128-row or two-chunk boxes), so they share
+// their tensor maps.
+template <bool MX, int EPI, int SCH>
+__host__ __device__ constexpr bool b_halves() {
+  return !MX && SCH != SCHED_WGRAD && EPI != EPI_F32_BIAS;
+}
 
 struct GemmParams {
   // Operand maps: K-major operands are 2-D [rows, K] maps with 128-byte x rows
@@ -150,6 +173,10 @@ struct GemmParams {
   int num_groups;          // number of groups (experts) when grouped
   const int* row_start;    // [G+1] padded row offsets, multiples of 64 (128 in MXFP8 mode)
   const int* tile_start;   // [G+1] prefix of 128-row tiles per group (grouped SCHED_ROWS)
+  const int* pair_start;   // [G+1] prefix of floor(tiles / 2) per group (grouped SCHED_ROWS2)
+  const int* rem_start;    // [G+1] prefix of groups with an odd tile count (grouped, part 1)
+  int part;                // SCHED_ROWS: 0 every tile; 1 only the last m-tile of groups
+                           // (or dense row ranges) with an odd number of m-tiles
   const int* counts;       // [G] real rows per group (grouped)
   int N;                   // output columns
   int K;                   // reduction length (SCHED_ROWS)
@@ -226,12 +253,18 @@ __device__ __forceinline__ int find_group(const int* row_start, int G, int row) 
   return lo;
 }
 
+// Work items per launch: tiles, or in the 2-SM mode pairs of tiles.
 template <int EPI, int SCH, int BN>
 __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
-  if constexpr (SCH == SCHED_ROWS) {
+  if constexpr (SCH != SCHED_WGRAD) {
     const int num_nt = (p.N + tile_out_cols<EPI>() - 1) / tile_out_cols<EPI>();
-    if (p.dense_rows > 0) return ((p.dense_rows + kBM - 1) / kBM) * num_nt;
-    return __ldg(p.tile_start + p.num_groups) * num_nt;
+    if (p.dense_rows > 0) {
+      const int mt = (p.dense_rows + kBM - 1) / kBM;
+      if (SCH == SCHED_ROWS2) return (mt / 2) * num_nt;
+      return (p.part ? (mt & 1) : mt) * num_nt;
+    }
+    const int* prefix = SCH == SCHED_ROWS2 ? p.pair_start : (p.part ? p.rem_start : p.tile_start);
+    return __ldg(prefix + p.num_groups) * num_nt;
   } else {
     const int num_nt = (p.N + BN - 1) / BN;
     const int num_mt = (p.M_out + kBM - 1) / kBM;
@@ -240,36 +273,68 @@ __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
   }
 }
 
+// Rows of m-tile mt of group e (grouped row problems).
+__device__ __forceinline__ void grouped_rows(const GemmParams& p, int e, int mt, TileInfo& t) {
+  t.e = e;
+  t.row0 = __ldg(p.row_start + e) + mt * kBM;
+  t.m64 = (__ldg(p.row_start + e + 1) - t.row0) < kBM ? 1 : 0;
+  t.rows_valid = max(0, min(t.m64 ? kBM / 2 : kBM, __ldg(p.counts + e) - mt * kBM));
+}
+
+// Tile of work item tau.  Row problems: grouped ones go expert by expert,
+// n-tile outer and m-tile inner, so that CTAs running at the same time share
+// one weight tile while the expert's activation rows stay in L2; dense ones
+// go m-tile outer, n-tile inner (the weight panel stays L2-resident while
+// the rows stream once).  In the 2-SM mode item tau is a pair of m-tiles
+// (2j, 2j+1) on one n-tile, of which the CTA of rank `rank` takes 2j + rank.
 template <int EPI, int SCH, int BK, int BN = kBN>
-__device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau) {
+__device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau, uint32_t rank = 0) {
   TileInfo t;
-  if constexpr (SCH == SCHED_ROWS) {
+  if constexpr (SCH != SCHED_WGRAD) {
     constexpr int W = tile_out_cols<EPI>();
     const int num_nt = (p.N + W - 1) / W;
+    const int r = static_cast<int>(rank);
     int mt, nt;
     if (p.dense_rows > 0) {
-      // m-tiles outer, n-tiles inner: the weight panel stays L2-resident while
-      // activation rows stream once.
-      mt = tau / num_nt;
-      nt = tau - mt * num_nt;
+      const int dense_mt = (p.dense_rows + kBM - 1) / kBM;
+      if (SCH == SCHED_ROWS2) {
+        mt = 2 * (tau / num_nt) + r;
+        nt = tau % num_nt;
+      } else if (p.part) {
+        mt = dense_mt - 1;
+        nt = tau;
+      } else {
+        mt = tau / num_nt;
+        nt = tau - mt * num_nt;
+      }
       t.e = 0;
       t.row0 = mt * kBM;
       t.rows_valid = min(kBM, p.dense_rows - t.row0);
       t.m64 = 0;
     } else {
-      // expert outer, n-tile, m-tile inner: CTAs running at the same time share
-      // one weight tile, the expert's activation rows stay in L2.
-      const int q = tau / num_nt;
-      const int e = find_group(p.tile_start, p.num_groups, q);
-      const int ts = __ldg(p.tile_start + e);
-      const int mt_e = __ldg(p.tile_start + e + 1) - ts;
-      const int local = tau - ts * num_nt;
-      nt = local / mt_e;
-      mt = local - nt * mt_e;
-      t.e = e;
-      t.row0 = __ldg(p.row_start + e) + mt * kBM;
-      t.m64 = (__ldg(p.row_start + e + 1) - t.row0) < kBM ? 1 : 0;
-      t.rows_valid = max(0, min(t.m64 ? kBM / 2 : kBM, __ldg(p.counts + e) - mt * kBM));
+      const int G = p.num_groups;
+      int e;
+      if (SCH == SCHED_ROWS2) {
+        e = find_group(p.pair_start, G, tau / num_nt);
+        const int ps = __ldg(p.pair_start + e);
+        const int np = __ldg(p.pair_start + e + 1) - ps;
+        const int local = tau - ps * num_nt;
+        nt = local / np;
+        mt = 2 * (local - nt * np) + r;
+      } else if (p.part) {
+        e = find_group(p.rem_start, G, tau / num_nt);
+        nt = tau - __ldg(p.rem_start + e) * num_nt;
+        mt = __ldg(p.tile_start + e + 1) - __ldg(p.tile_start + e) - 1;
+      } else {
+        const int q = tau / num_nt;
+        e = find_group(p.tile_start, G, q);
+        const int ts = __ldg(p.tile_start + e);
+        const int mt_e = __ldg(p.tile_start + e + 1) - ts;
+        const int local = tau - ts * num_nt;
+        nt = local / mt_e;
+        mt = local - nt * mt_e;
+      }
+      grouped_rows(p, e, mt, t);
     }
     t.m0 = 0;
     t.nt = nt;
@@ -303,15 +368,50 @@ __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau) {
   return t;
 }
 
+// The loop every role runs: items first, first + stride, ... below count;
+// in the 2-SM mode over cluster indices, `rank` being the CTA's in the pair.
+struct WorkRange {
+  int first, stride, count;
+  uint32_t rank;
+};
+
 // ------------------------------------------------------------------ producer
+// Half h of a 256-column B tile (its rows n0 + 128h .. n0 + 128h + 127): one
+// 128-row K-major box, the gate (h = 0) or up (h = 1) stack of a dual-N
+// operand, or two 64-column chunks of an MN-major operand, into dst.  PAIR:
+// completion on the pair's full barrier (shared::cluster address).
+template <int BMO, bool PAIR>
+__device__ __forceinline__ void load_b_half(const GemmParams& p, uint32_t dst, const TileInfo& t, int kabs,
+                                            int brow, int h, uint32_t bar) {
+  if constexpr (BMO == B_K_TILE || BMO == B_K_DUAL_N) {
+    const void* map = (BMO == B_K_DUAL_N && h) ? &p.tmB1 : &p.tmB0;
+    const int row = BMO == B_K_TILE ? brow + h * (kBN / 2) : brow;
+    if constexpr (PAIR)
+      tma_load_2d_pair(dst, map, kabs, row, bar);
+    else
+      tma_load_2d(dst, map, kabs, row, bar);
+  } else {
+    const bool second = BMO == B_MN_DUAL_K && kabs >= p.b_split;
+    const void* map = second ? &p.tmB1 : &p.tmB0;
+    const int krow = t.e * p.b_group_rows + (second ? kabs - p.b_split : kabs);
+    if constexpr (PAIR)
+      tma_load_3d_pair(dst, map, 0, krow, t.n0 / 64 + 2 * h, bar);
+    else
+      tma_load_3d(dst, map, 0, krow, t.n0 / 64 + 2 * h, bar);
+  }
+}
+
 template <int AM, int BMO, int EPI, int SCH, bool MX>
 __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_tiles, uint32_t s_sf,
-                                              uint32_t full0, uint32_t empty0, int num_tiles,
+                                              uint32_t full0, uint32_t empty0, const WorkRange& wr,
                                               volatile int* abort_flag, int lane) {
+  constexpr bool PAIR = SCH == SCHED_ROWS2;
+  constexpr bool HALVES = b_halves<MX, EPI, SCH>();
   constexpr int BK = stage_k<MX>();
   constexpr int BN = gemm_bn<MX, EPI, SCH>();
   constexpr int SB = stage_bytes<MX, EPI, SCH>(), SFB = sf_stage_bytes<MX, EPI, SCH>();
   constexpr uint32_t kTx = SB + SFB;
+  static_assert(!HALVES || (AM == A_K_TILE && BN == kBN && !MX), "B halves: bf16, K-major A, 256-column tiles");
   int s = 0;
   uint32_t ph = 0;
   // Per stage: parity of the last load issued into it, or -1.
@@ -320,9 +420,11 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
 #pragma unroll
   for (int i = 0; i < ST; ++i) issued_parity[i] = -1;
   bool aborted = false;
+  // 2-SM mode: both CTAs' loads complete on the even CTA's full barriers
+  const uint32_t lead_full0 = PAIR ? mapa_shared(full0, 0) : full0;
 
-  for (int tau = blockIdx.x; tau < num_tiles && !aborted; tau += gridDim.x) {
-    const TileInfo t = gemm_tile<EPI, SCH, BK, BN>(p, tau);
+  for (int w = wr.first; w < wr.count && !aborted; w += wr.stride) {
+    const TileInfo t = gemm_tile<EPI, SCH, BK, BN>(p, w, wr.rank);
     // row coordinate of the A tile: token rows, or output rows of a weight gradient
     const int arow = SCH == SCHED_WGRAD ? p.a_col_off + t.m0 : t.row0;
     const int brow = t.e * p.b_group_rows + t.n0;
@@ -337,45 +439,65 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
       const uint32_t full = full0 + 8 * s;
       const uint32_t sA = s_tiles + s * SB;
       const uint32_t sB = sA + kATileBytes;
-      if (lane == 0) mbar_arrive_expect_tx(full, kTx);
-      __syncwarp();
       const int kabs = (t.kb0 + kb) * BK;
-      // ---- A operand
-      if constexpr (AM == A_K_TILE) {
-        if (lane == 0) tma_load_2d(sA, &p.tmA, kabs, arow, full);
-      } else {  // A_MN_TILE (bf16): both 64-column chunks with one 3-D box
-        if (lane == 0) tma_load_3d(sA, &p.tmA, 0, kabs, (p.a_col_off + t.m0) / 64, full);
-      }
-      // ---- B operand
-      if constexpr (BMO == B_K_TILE) {
-        if (lane == 0) tma_load_2d(sB, &p.tmB0, kabs, brow, full);
-      } else if constexpr (BMO == B_K_DUAL_N) {
+      if constexpr (PAIR) {
+        // this CTA's 128 rows of A and its half of B; the even CTA's
+        // barrier counts both CTAs' bytes
         if (lane == 0) {
-          tma_load_2d(sB, &p.tmB0, kabs, brow, full);
-          tma_load_2d(sB + kBTileBytes / 2, &p.tmB1, kabs, brow, full);
+          if (wr.rank == 0) mbar_arrive_expect_tx(full, 2 * kTx);
+          const uint32_t fb = lead_full0 + 8 * s;
+          tma_load_2d_pair(sA, &p.tmA, kabs, arow, fb);
+          load_b_half<BMO, true>(p, sB, t, kabs, brow, static_cast<int>(wr.rank), fb);
         }
-      } else if constexpr (BMO == B_MN_TILE) {  // four 64-column chunks, one 3-D box
-        if (lane == 0) tma_load_3d(sB, &p.tmB0, 0, t.e * p.b_group_rows + kabs, t.n0 / 64, full);
-      } else {  // B_MN_DUAL_K
+        __syncwarp();
+      } else if constexpr (HALVES) {
         if (lane == 0) {
-          const bool second = kabs >= p.b_split;
-          const int kk = second ? kabs - p.b_split : kabs;
-          tma_load_3d(sB, second ? (const void*)&p.tmB1 : (const void*)&p.tmB0, 0,
-                      t.e * p.b_group_rows + kk, t.n0 / 64, full);
+          mbar_arrive_expect_tx(full, kTx);
+          tma_load_2d(sA, &p.tmA, kabs, arow, full);
+          load_b_half<BMO, false>(p, sB, t, kabs, brow, 0, full);
+          load_b_half<BMO, false>(p, sB + kBTileBytes / 2, t, kabs, brow, 1, full);
         }
-      }
-      // ---- MXFP8 scales of this stage's A and B tiles (one 128-column group)
-      if constexpr (MX) {
-        if (lane == 0) {
-          const long long g = kabs / kBKmx;
-          const uint32_t sfs = s_sf + s * SFB;
-          bulk_load(sfs, p.sfa + (g * p.sfa_rb + arow / 128) * 512, 512, full);
-          const size_t boff = static_cast<size_t>((g * p.sfb_rb + brow / 128) * 512);
-          if constexpr (BMO == B_K_DUAL_N) {
-            bulk_load(sfs + 512, p.sfb0 + boff, 512, full);
-            bulk_load(sfs + 1024, p.sfb1 + boff, 512, full);
-          } else {
-            bulk_load(sfs + 512, p.sfb0 + boff, BN / 128 * 512, full);
+        __syncwarp();
+      } else {
+        if (lane == 0) mbar_arrive_expect_tx(full, kTx);
+        __syncwarp();
+        // ---- A operand
+        if constexpr (AM == A_K_TILE) {
+          if (lane == 0) tma_load_2d(sA, &p.tmA, kabs, arow, full);
+        } else {  // A_MN_TILE (bf16): both 64-column chunks with one 3-D box
+          if (lane == 0) tma_load_3d(sA, &p.tmA, 0, kabs, (p.a_col_off + t.m0) / 64, full);
+        }
+        // ---- B operand
+        if constexpr (BMO == B_K_TILE) {
+          if (lane == 0) tma_load_2d(sB, &p.tmB0, kabs, brow, full);
+        } else if constexpr (BMO == B_K_DUAL_N) {
+          if (lane == 0) {
+            tma_load_2d(sB, &p.tmB0, kabs, brow, full);
+            tma_load_2d(sB + kBTileBytes / 2, &p.tmB1, kabs, brow, full);
+          }
+        } else if constexpr (BMO == B_MN_TILE) {  // four 64-column chunks, one 3-D box
+          if (lane == 0) tma_load_3d(sB, &p.tmB0, 0, t.e * p.b_group_rows + kabs, t.n0 / 64, full);
+        } else {  // B_MN_DUAL_K
+          if (lane == 0) {
+            const bool second = kabs >= p.b_split;
+            const int kk = second ? kabs - p.b_split : kabs;
+            tma_load_3d(sB, second ? (const void*)&p.tmB1 : (const void*)&p.tmB0, 0,
+                        t.e * p.b_group_rows + kk, t.n0 / 64, full);
+          }
+        }
+        // ---- MXFP8 scales of this stage's A and B tiles (one 128-column group)
+        if constexpr (MX) {
+          if (lane == 0) {
+            const long long g = kabs / kBKmx;
+            const uint32_t sfs = s_sf + s * SFB;
+            bulk_load(sfs, p.sfa + (g * p.sfa_rb + arow / 128) * 512, 512, full);
+            const size_t boff = static_cast<size_t>((g * p.sfb_rb + brow / 128) * 512);
+            if constexpr (BMO == B_K_DUAL_N) {
+              bulk_load(sfs + 512, p.sfb0 + boff, 512, full);
+              bulk_load(sfs + 1024, p.sfb1 + boff, 512, full);
+            } else {
+              bulk_load(sfs + 512, p.sfb0 + boff, BN / 128 * 512, full);
+            }
           }
         }
       }
@@ -386,13 +508,28 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
       }
     }
   }
-  if (aborted && lane == 0) {
-    // Loads still in flight must land before the CTA's shared memory goes away.
+  if (aborted && lane == 0 && (!PAIR || wr.rank == 0)) {
+    // Loads still in flight must land before the CTA's shared memory goes
+    // away (2-SM mode: the even CTA's barriers also count the odd CTA's).
 #pragma unroll
     for (int i = 0; i < ST; ++i)
       if (issued_parity[i] >= 0)
         mbar_wait(full0 + 8 * i, static_cast<uint32_t>(issued_parity[i]), abort_flag, p.status,
                   false);
+  }
+  if constexpr (PAIR) {
+    // The even CTA's MMA commits arrive on both CTAs' empty barriers: wait for
+    // the last round of every stage to be released, so that none of them is
+    // still in flight when the CTA exits.
+    if (!aborted && lane == 0) {
+      for (int i = 0; i < ST; ++i) {
+        if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, p.status)) break;
+        if (++s == ST) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+    }
   }
 }
 
@@ -401,29 +538,34 @@ template <int AM, int BMO, int EPI, int SCH, bool MX>
 __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, uint32_t s_sf,
                                          uint32_t full0, uint32_t empty0, uint32_t accf0,
                                          uint32_t acce0, uint32_t drain, uint32_t tmem_base,
-                                         int num_tiles, volatile int* abort_flag) {
+                                         const WorkRange& wr, volatile int* abort_flag) {
+  // 2-SM mode: the even CTA issues the pair's MMAs (M = 256: its 128 rows of
+  // A and the odd CTA's), the odd CTA's MMA warp has nothing to do
+  constexpr bool PAIR = SCH == SCHED_ROWS2;
+  if (PAIR && wr.rank != 0) return;
   constexpr int BK = stage_k<MX>();
   constexpr int ST = gemm_stages<MX, EPI, SCH>();
   constexpr int BN = gemm_bn<MX, EPI, SCH>();
   constexpr int SB = stage_bytes<MX, EPI, SCH>(), SFB = sf_stage_bytes<MX, EPI, SCH>();
   constexpr bool a_mn = (AM == A_MN_TILE);
   constexpr bool b_mn = (BMO == B_MN_TILE || BMO == B_MN_DUAL_K);
-  constexpr uint32_t idesc128 = idesc_bf16_f32(kBM, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+  constexpr uint32_t idesc128 = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
   constexpr uint32_t idesc64 = idesc_bf16_f32(kBM / 2, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
   int s = 0;
   uint32_t ph = 0;
   int acc = 0;
   uint32_t aph = 0;
   bool issued = false, aborted = false;
-  for (int tau = blockIdx.x; tau < num_tiles && !aborted; tau += gridDim.x) {
-    const TileInfo t = gemm_tile<EPI, SCH, BK, BN>(p, tau);
+  for (int w = wr.first; w < wr.count && !aborted; w += wr.stride) {
+    const TileInfo t = gemm_tile<EPI, SCH, BK, BN>(p, w, wr.rank);
     if (!mbar_wait(acce0 + 8 * acc, aph ^ 1, abort_flag, p.status)) {
       aborted = true;
       break;
     }
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-    const uint32_t idesc = t.m64 ? idesc64 : idesc128;
+    // a pair always runs M = 256 (the rows past a 64-row tail are not stored)
+    const uint32_t idesc = (t.m64 && !PAIR) ? idesc64 : idesc128;
     for (int kb = 0; kb < t.nkb; ++kb) {
       if (!mbar_wait(full0 + 8 * s, ph, abort_flag, p.status)) {
         aborted = true;
@@ -455,10 +597,16 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
                                    : smem_desc_sw128(sA + kk * 32, 16, 1024);
           const uint64_t bd = b_mn ? smem_desc_sw128(sB + kk * 2048, kMNChunkBytes, 1024)
                                    : smem_desc_sw128(sB + kk * 32, 16, 1024);
-          tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          if constexpr (PAIR)
+            tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          else
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
         }
       }
-      tc_commit(empty0 + 8 * s);
+      if constexpr (PAIR)
+        tc_commit_pair_mc(empty0 + 8 * s, 3);  // frees the stage in both CTAs
+      else
+        tc_commit(empty0 + 8 * s);
       issued = true;
       if (++s == ST) {
         s = 0;
@@ -466,10 +614,18 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
       }
     }
     if (aborted) break;
-    if (t.nkb > 0)
+    if constexpr (PAIR) {
+      if (t.nkb > 0) {
+        tc_commit_pair_mc(accf0 + 8 * acc, 3);
+      } else {
+        mbar_arrive(accf0 + 8 * acc);
+        mbar_arrive_remote(mapa_shared(accf0 + 8 * acc, 1));
+      }
+    } else if (t.nkb > 0) {
       tc_commit(accf0 + 8 * acc);
-    else
+    } else {
       mbar_arrive(accf0 + 8 * acc);
+    }
     if (++acc == acc_bufs<MX, EPI, SCH>()) {
       acc = 0;
       aph ^= 1;
@@ -477,7 +633,10 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
   }
   if (aborted && issued) {
     // MMAs still in flight must finish before TMEM is released.
-    tc_commit(drain);
+    if constexpr (PAIR)
+      tc_commit_pair(drain);
+    else
+      tc_commit(drain);
     mbar_wait(drain, 0, abort_flag, p.status, false);
   }
 }
@@ -528,7 +687,7 @@ struct EpiStager {
 // weight gradients (whose output is bf16 as well; 128-column tiles).
 template <int EPI, int SCH, bool MX>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf0, uint32_t acce0,
-                                              uint32_t tmem_base, uint32_t s_warp, int num_tiles,
+                                              uint32_t tmem_base, uint32_t s_warp, const WorkRange& wr,
                                               volatile int* abort_flag, int warp_e, int half, int lane) {
   constexpr bool kWide = epi_wide<MX, EPI, SCH>();
   constexpr int BN = gemm_bn<MX, EPI, SCH>();
@@ -538,13 +697,20 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
   int acc = 0;
   uint32_t aph = 0;
   EpiStager<epi_slots<MX, EPI, SCH>()> stg{s_warp, 0, lane};
-  for (int tau = blockIdx.x; tau < num_tiles; tau += gridDim.x) {
-    const TileInfo t = gemm_tile<EPI, SCH, BK, BN>(p, tau);
+  constexpr bool PAIR = SCH == SCHED_ROWS2;
+  // 2-SM mode: the accumulator is released on the even CTA's barrier
+  const uint32_t acce_lead = PAIR ? mapa_shared(acce0, 0) : acce0;
+  for (int w = wr.first; w < wr.count; w += wr.stride) {
+    const TileInfo t = gemm_tile<EPI, SCH, BK, BN>(p, w, wr.rank);
     // Tile row held by this thread's TMEM lane: lane l of warp w is row 32w + l
     // of an M=128 accumulator; an M=64 accumulator keeps rows 16w..16w+15 in
-    // lanes 0..15 of each warp (lanes 16..31 hold nothing of this tile).
-    const int wrows = t.m64 ? 16 : 32;
-    const bool lane_ok = lane < wrows;
+    // lanes 0..15 of each warp (lanes 16..31 hold nothing of this tile).  A
+    // pair's tile always has the M=128 layout: for a 64-row tail tile, warps
+    // 2 and 3 hold rows of the next group, which they must not store.
+    const bool m64l = t.m64 && !PAIR;
+    const int wrows = m64l ? 16 : 32;
+    const bool warp_live = !(PAIR && t.m64 && warp_e >= 2);
+    const bool lane_ok = warp_live && lane < wrows;
     const int row = warp_e * wrows + lane;
     if constexpr (EPI == EPI_SWIGLU_BWD) {  // the saved a, b of this tile's rows: into L2 while the MMAs run
       if (lane_ok && row < t.rows_valid) {
@@ -585,8 +751,8 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
       const bool real = lane_ok && row < t.rows_valid;
       const long long grow = static_cast<long long>(t.row0) + row;
       const int r0 = t.row0 + warp_e * wrows;
-      const CUtensorMap* o0 = t.m64 ? &p.tmO0h : &p.tmO0;
-      const CUtensorMap* o1 = t.m64 ? &p.tmO1h : &p.tmO1;
+      const CUtensorMap* o0 = m64l ? &p.tmO0h : &p.tmO0;
+      const CUtensorMap* o1 = m64l ? &p.tmO1h : &p.tmO1;
       if constexpr (EPI == EPI_F32_BIAS) {
         const bool in_mem = p.dense_rows > 0 ? real : lane_ok;
         float* o = reinterpret_cast<float*>(p.out) + grow * p.ldo;
@@ -603,7 +769,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
           }
         }
       } else if constexpr (EPI == EPI_SWIGLU_FWD) {
-        for (int c0 = 0; c0 < kBN / 2 && t.n0 + c0 < p.N; c0 += 64) {
+        for (int c0 = 0; c0 < kBN / 2 && t.n0 + c0 < p.N && warp_live; c0 += 64) {
           float a[64], b[64];
           tmem_ld32(tr + c0, a);
           tmem_ld32(tr + c0 + 32, a + 32);
@@ -629,7 +795,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
         float scale = 1.f;
         if (p.row_scale && p.dense_rows == 0 && lane_ok) scale = __ldg(p.row_scale + grow);
         if (!real) scale = 0.f;
-        for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 64) {
+        for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N && warp_live; c0 += 64) {
           float v[64];
           tmem_ld32(tr + c0, v);
           tmem_ld32(tr + c0 + 32, v + 32);
@@ -685,7 +851,12 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+    if (lane == 0) {
+      if (PAIR && wr.rank != 0)
+        mbar_arrive_remote(acce_lead + 8 * acc);
+      else
+        mbar_arrive(acce0 + 8 * acc);
+    }
     if (++acc == 2) {
       acc = 0;
       aph ^= 1;
@@ -752,7 +923,7 @@ __device__ __forceinline__ void quant32_tok(const float* v, float* buf, uint8_t*
 
 template <int EPI, int SCH>
 __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t accf0, uint32_t acce0,
-                                                 uint32_t tmem_base, uint32_t s_warp, float* buf, int num_tiles,
+                                                 uint32_t tmem_base, uint32_t s_warp, float* buf, const WorkRange& wr,
                                                  volatile int* abort_flag, int quad, int half, int lane) {
   static_assert(EPI != EPI_F32_BIAS, "no fp32 epilogue in MXFP8 mode");
   uint32_t aph = 0;
@@ -763,8 +934,9 @@ __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t a
   const uint32_t stash = tmem_base + lane_off + kStashCol + half * (kStashCols / 2);
   const int row = quad * 32 + lane;  // MXFP8 groups are 128-row aligned: no 64-row tiles
   const int warp_e = quad;
-  for (int tau = blockIdx.x; tau < num_tiles; tau += gridDim.x) {
-    const TileInfo t = gemm_tile<EPI, SCH, kBKmx>(p, tau);
+  static_assert(SCH != SCHED_ROWS2, "MXFP8 kernels run on one SM per tile");
+  for (int w = wr.first; w < wr.count; w += wr.stride) {
+    const TileInfo t = gemm_tile<EPI, SCH, kBKmx>(p, w);
     if constexpr (EPI == EPI_SWIGLU_BWD) {  // the saved a, b of this warp's rows and columns: into L2 now
       const int c0 = t.n0 + 128 * half;
       if (row < t.rows_valid && c0 < p.N) {
@@ -982,6 +1154,8 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kerne
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  constexpr bool PAIR = SCH == SCHED_ROWS2;
+  constexpr int CG = PAIR ? 2 : 1;
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < ST; ++i) {
       mbar_init(full0 + 8 * i, 1);
@@ -989,7 +1163,8 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kerne
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(accf0 + 8 * i, 1);
-      mbar_init(acce0 + 8 * i, epi_warps<MX, EPI, SCH>());
+      // 2-SM mode: the even CTA's counts both CTAs' epilogue warps
+      mbar_init(acce0 + 8 * i, (PAIR ? 2 : 1) * epi_warps<MX, EPI, SCH>());
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -1008,37 +1183,53 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kerne
     }
   }
   if (warp == 2) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<CG>(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
   __syncthreads();
+  // 2-SM mode: the peer's barriers are initialised before anything reaches them
+  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int num_tiles = gemm_num_tiles<EPI, SCH, gemm_bn<MX, EPI, SCH>()>(p);
+  WorkRange wr;
+  if constexpr (PAIR) {
+    wr.first = static_cast<int>(cluster_id_x());
+    wr.stride = static_cast<int>(num_clusters_x());
+    wr.count = gemm_num_tiles<EPI, SCH, gemm_bn<MX, EPI, SCH>()>(p);
+    wr.rank = cluster_ctarank();
+  } else {
+    wr.first = blockIdx.x;
+    wr.stride = gridDim.x;
+    wr.count = gemm_num_tiles<EPI, SCH, gemm_bn<MX, EPI, SCH>()>(p);
+    wr.rank = 0;
+  }
 
   if (warp == 0) {
-    gemm_producer<AM, BMO, EPI, SCH, MX>(p, s_tiles, s_sf, full0, empty0, num_tiles, abort_flag, lane);
+    gemm_producer<AM, BMO, EPI, SCH, MX>(p, s_tiles, s_sf, full0, empty0, wr, abort_flag, lane);
   } else if (warp == 1) {
     if (lane == 0)
       gemm_mma<AM, BMO, EPI, SCH, MX>(p, s_tiles, s_sf, full0, empty0, accf0, acce0, drain,
-                                      tmem_base, num_tiles, abort_flag);
+                                      tmem_base, wr, abort_flag);
   } else if (warp >= first_epi_warp<MX, EPI, SCH>()) {
     const int ew = warp - first_epi_warp<MX, EPI, SCH>();
     constexpr int kWarpBytes = epi_warp_bytes<MX, EPI, SCH>();
     if constexpr (epi_mx_stash<MX, EPI, SCH>())
       gemm_epilogue_mx<EPI, SCH>(p, accf0, acce0, tmem_base, s_staging + ew * kWarpBytes,
                                  reinterpret_cast<float*>(smem + ST * SB + ew * kWarpBytes),
-                                 num_tiles, abort_flag, warp & 3, ew >> 2, lane);
+                                 wr, abort_flag, warp & 3, ew >> 2, lane);
     else
-      gemm_epilogue<EPI, SCH, MX>(p, accf0, acce0, tmem_base, s_staging + ew * kWarpBytes, num_tiles, abort_flag,
+      gemm_epilogue<EPI, SCH, MX>(p, accf0, acce0, tmem_base, s_staging + ew * kWarpBytes, wr, abort_flag,
                                   warp & 3, ew >> 2, lane);
   }
   tc_fence_before();
   __syncthreads();
+  // 2-SM mode: neither CTA leaves (or frees TMEM) while the pair's MMAs or
+  // signals may still reach it
+  if constexpr (PAIR) cluster_sync();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc<CG>(tmem_base, kTmemCols);
   }
 }
 
