@@ -10,7 +10,7 @@ cudaError_t launch_gemm_bwd(GemmKind kind, const GemmParams& p, int grid, cudaSt
     case GK_DGRAD_GATEUP:
       return launch_rows_two_pass<A_K_TILE, B_MN_DUAL_K, EPI_BF16>(p, grid, st);
     case GK_WGRAD:
-      return launch_gemm_inst<A_MN_TILE, B_MN_TILE, EPI_BF16, SCHED_WGRAD>(p, grid, st);
+      return launch_wgrad_two_pass<A_MN_TILE, B_MN_TILE>(p, grid, st);
     default:
       return cudaErrorInvalidValue;
   }

@@ -24,7 +24,7 @@ cudaError_t launch_gemm_inst(const GemmParams& p, int grid, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  if constexpr (SCH == SCHED_ROWS2) {
+  if constexpr (sched_pair(SCH)) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid < 2 ? 2 : grid & ~1));
     cfg.blockDim = dim3(threads);
@@ -61,6 +61,22 @@ cudaError_t launch_rows_two_pass(const GemmParams& p, int grid, cudaStream_t st)
   q.part = 1;
   if (p.dense_rows == 0 || dense_mt >= 2) ++extra_kernel_launches();
   return launch_gemm_inst<AM, BMO, EPI, SCHED_ROWS>(q, grid, st);
+}
+
+// Weight gradients likewise: pairs of m-tiles (weight rows) on SM pairs, and
+// the last m-tile on one SM when M_out / 128 is odd.
+template <int AM, int BMO>
+cudaError_t launch_wgrad_two_pass(const GemmParams& p, int grid, cudaStream_t st) {
+  const int num_mt = (p.M_out + kBM - 1) / kBM;
+  if (num_mt >= 2) {
+    const cudaError_t e = launch_gemm_inst<AM, BMO, EPI_BF16, SCHED_WGRAD2>(p, grid, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (num_mt % 2 == 0) return cudaSuccess;
+  GemmParams q = p;
+  q.part = 1;
+  if (num_mt >= 2) ++extra_kernel_launches();
+  return launch_gemm_inst<AM, BMO, EPI_BF16, SCHED_WGRAD>(q, grid, st);
 }
 
 cudaError_t launch_gemm_fwd(GemmKind kind, const GemmParams& p, int grid, cudaStream_t st);

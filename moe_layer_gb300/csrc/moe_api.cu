@@ -352,8 +352,9 @@ moe_status mnmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, i
   return MOE_OK;
 }
 
-// The bf16 row GEMMs other than the router projection load B in halves: 128-row
-// boxes (K-major) or two 64-column chunks (MN-major); see launch_rows_two_pass.
+// The bf16 GEMMs other than the router projection load B in halves: 128-row
+// boxes (K-major) or two 64-column chunks (MN-major); see launch_rows_two_pass
+// and launch_wgrad_two_pass.
 // Output map: boxes of 64 columns x 32 rows (one epilogue warp's staging box).
 moe_status omap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
   return tmap(m, base, rows, cols, 64, 32);
@@ -936,7 +937,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     GemmParams p;  // dW_down[e] = dy_rows^T . (g h)
     zero_params(p);
     MOE_TRY(mnmap(&p.tmA, w.dyp, s.Rp, s.d, 2));
-    MOE_TRY(mnmap(&p.tmB0, w.hg, s.Rp, s.I, 4));
+    MOE_TRY(mnmap(&p.tmB0, w.hg, s.Rp, s.I, 2));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.M_out = d;
@@ -949,7 +950,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     GemmParams p;  // dW_gate[e] = da^T . x_rows ; dW_up[e] = db^T . x_rows
     zero_params(p);
     MOE_TRY(mnmap(&p.tmA, w.dadb, s.Rp, 2 * s.I, 2));
-    MOE_TRY(mnmap(&p.tmB0, sv.xp, s.Rp, s.d, 4));
+    MOE_TRY(mnmap(&p.tmB0, sv.xp, s.Rp, s.d, 2));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.M_out = I;
@@ -965,7 +966,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
       GemmParams p;  // dWs_down = dy^T . h_s
       zero_params(p);
       MOE_TRY(mnmap(&p.tmA, dy, s.T, s.d, 2));
-      MOE_TRY(mnmap(&p.tmB0, w.hs, s.T, s.Is, 4));
+      MOE_TRY(mnmap(&p.tmB0, w.hs, s.T, s.Is, 2));
       p.dense_rows = T;
       p.M_out = d;
       p.N = Is;
@@ -977,7 +978,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
       GemmParams p;  // dWs_gate = da_s^T . x ; dWs_up = db_s^T . x
       zero_params(p);
       MOE_TRY(mnmap(&p.tmA, w.dadbs, s.T, 2 * s.Is, 2));
-      MOE_TRY(mnmap(&p.tmB0, x, s.T, s.d, 4));
+      MOE_TRY(mnmap(&p.tmB0, x, s.T, s.d, 2));
       p.dense_rows = T;
       p.M_out = Is;
       p.N = d;

@@ -48,9 +48,12 @@ namespace moe {
 enum AMode : int { A_K_TILE = 0, A_MN_TILE = 1 };
 enum BMode : int { B_K_TILE = 0, B_K_DUAL_N = 1, B_MN_TILE = 2, B_MN_DUAL_K = 3 };
 enum EpiMode : int { EPI_F32_BIAS = 0, EPI_SWIGLU_FWD = 1, EPI_BF16 = 2, EPI_SWIGLU_BWD = 3 };
-// SCHED_ROWS2: row tiles in pairs of m-tiles of one group on one n-tile, each
-// pair computed by a cluster of two CTAs with cta_group::2 MMAs (M = 256).
-enum SchedMode : int { SCHED_ROWS = 0, SCHED_WGRAD = 1, SCHED_ROWS2 = 2 };
+// SCHED_ROWS2 / SCHED_WGRAD2: the same tiles in pairs of m-tiles on one
+// n-tile, each pair computed by a cluster of two CTAs with cta_group::2 MMAs
+// (M = 256).
+enum SchedMode : int { SCHED_ROWS = 0, SCHED_WGRAD = 1, SCHED_ROWS2 = 2, SCHED_WGRAD2 = 3 };
+__host__ __device__ constexpr bool sched_wgrad(int sch) { return sch == SCHED_WGRAD || sch == SCHED_WGRAD2; }
+__host__ __device__ constexpr bool sched_pair(int sch) { return sch == SCHED_ROWS2 || sch == SCHED_WGRAD2; }
 
 constexpr int kBM = 128;  // rows per tile (TMEM lanes)
 constexpr int kBN = 256;  // accumulator columns per tile
@@ -81,7 +84,7 @@ __host__ __device__ constexpr int acc_bufs() { return (MX && gemm_bn<MX, EPI, SC
 // half of B.
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int stage_bytes() {
-  return kATileBytes + (SCH == SCHED_ROWS2 ? gemm_bn<MX, EPI, SCH>() / 2 : gemm_bn<MX, EPI, SCH>()) * 128;
+  return kATileBytes + (sched_pair(SCH) ? gemm_bn<MX, EPI, SCH>() / 2 : gemm_bn<MX, EPI, SCH>()) * 128;
 }
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int sf_stage_bytes() { return MX ? 512 + gemm_bn<MX, EPI, SCH>() / 128 * 512 : 0; }
@@ -107,7 +110,7 @@ __host__ __device__ constexpr int gemm_threads() {
 // per warp were measured for the weight gradients: slower than four stages.)
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int gemm_stages() {
-  return SCH == SCHED_ROWS2 ? 6 : (gemm_bn<MX, EPI, SCH>() == kBN ? kStages : 5);
+  return sched_pair(SCH) ? 6 : (gemm_bn<MX, EPI, SCH>() == kBN ? kStages : 5);
 }
 // MXFP8 kernels with a single accumulator run the stash epilogue; the ones
 // with two (the weight gradients) run the bf16-mode epilogue.
@@ -136,9 +139,9 @@ __host__ __device__ constexpr int gemm_smem_bytes_for() {
 }
 constexpr int kGemmSmemBytes = gemm_smem_bytes_for<false, 0, 0>();
 
-// The bf16 row GEMMs other than the router projection run as two launches:
-// a 2-SM pass (SCHED_ROWS2) over pairs of m-tiles, and a 1-SM pass over the
-// last m-tile of every group with an odd number of them.  A 128 x 256 tile
+// The bf16 GEMMs other than the router projection run as two launches: a
+// 2-SM pass (SCHED_ROWS2, SCHED_WGRAD2) over pairs of m-tiles, and a 1-SM
+// pass over the last m-tile of every group with an odd number of them.  A 128 x 256 tile
 // per SM stages 48 KB per K step and its MMAs read as much again from shared
 // memory; with the B tile split between the two SMs of a pair both become
 // 32 KB.  Measured at the DSV3 shape, staging only half of the gate/up weight
@@ -149,7 +152,7 @@ constexpr int kGemmSmemBytes = gemm_smem_bytes_for<false, 0, 0>();
 // their tensor maps.
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr bool b_halves() {
-  return !MX && SCH != SCHED_WGRAD && EPI != EPI_F32_BIAS;
+  return !MX && EPI != EPI_F32_BIAS;
 }
 
 struct GemmParams {
@@ -175,8 +178,9 @@ struct GemmParams {
   const int* tile_start;   // [G+1] prefix of 128-row tiles per group (grouped SCHED_ROWS)
   const int* pair_start;   // [G+1] prefix of floor(tiles / 2) per group (grouped SCHED_ROWS2)
   const int* rem_start;    // [G+1] prefix of groups with an odd tile count (grouped, part 1)
-  int part;                // SCHED_ROWS: 0 every tile; 1 only the last m-tile of groups
-                           // (or dense row ranges) with an odd number of m-tiles
+  int part;                // 1-SM passes: 0 every tile; 1 only the last m-tile of groups
+                           // (or dense row ranges, or weight gradients) with an odd
+                           // number of m-tiles
   const int* counts;       // [G] real rows per group (grouped)
   int N;                   // output columns
   int K;                   // reduction length (SCHED_ROWS)
@@ -256,7 +260,7 @@ __device__ __forceinline__ int find_group(const int* row_start, int G, int row) 
 // Work items per launch: tiles, or in the 2-SM mode pairs of tiles.
 template <int EPI, int SCH, int BN>
 __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
-  if constexpr (SCH != SCHED_WGRAD) {
+  if constexpr (!sched_wgrad(SCH)) {
     const int num_nt = (p.N + tile_out_cols<EPI>() - 1) / tile_out_cols<EPI>();
     if (p.dense_rows > 0) {
       const int mt = (p.dense_rows + kBM - 1) / kBM;
@@ -269,7 +273,8 @@ __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
     const int num_nt = (p.N + BN - 1) / BN;
     const int num_mt = (p.M_out + kBM - 1) / kBM;
     const int G = p.dense_rows > 0 ? 1 : p.num_groups;
-    return G * num_mt * num_nt;
+    if (SCH == SCHED_WGRAD2) return G * (num_mt / 2) * num_nt;
+    return G * (p.part ? (num_mt & 1) : num_mt) * num_nt;
   }
 }
 
@@ -290,7 +295,7 @@ __device__ __forceinline__ void grouped_rows(const GemmParams& p, int e, int mt,
 template <int EPI, int SCH, int BK, int BN = kBN>
 __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau, uint32_t rank = 0) {
   TileInfo t;
-  if constexpr (SCH != SCHED_WGRAD) {
+  if constexpr (!sched_wgrad(SCH)) {
     constexpr int W = tile_out_cols<EPI>();
     const int num_nt = (p.N + W - 1) / W;
     const int r = static_cast<int>(rank);
@@ -342,13 +347,28 @@ __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau, uint
     t.kb0 = 0;
     t.nkb = p.K / BK;
   } else {
+    // weight gradients: group outer, m-tile, n-tile inner
     const int num_nt = (p.N + BN - 1) / BN;
     const int num_mt = (p.M_out + kBM - 1) / kBM;
-    const int per_g = num_mt * num_nt;
-    const int e = tau / per_g;
-    const int local = tau - e * per_g;
-    const int mt = local / num_nt;
-    const int nt = local - mt * num_nt;
+    int e, mt, nt;
+    if (SCH == SCHED_WGRAD2) {
+      const int per_g = (num_mt / 2) * num_nt;
+      e = tau / per_g;
+      const int local = tau - e * per_g;
+      const int j = local / num_nt;
+      nt = local - j * num_nt;
+      mt = 2 * j + static_cast<int>(rank);
+    } else if (p.part) {
+      e = tau / num_nt;
+      nt = tau - e * num_nt;
+      mt = num_mt - 1;
+    } else {
+      const int per_g = num_mt * num_nt;
+      e = tau / per_g;
+      const int local = tau - e * per_g;
+      mt = local / num_nt;
+      nt = local - mt * num_nt;
+    }
     t.e = e;
     t.m0 = mt * kBM;
     t.nt = nt;
@@ -401,17 +421,35 @@ __device__ __forceinline__ void load_b_half(const GemmParams& p, uint32_t dst, c
   }
 }
 
+// The A tile: 128 K-major rows from arow, or (MN-major, weight gradients)
+// both 64-column chunks of the M range with one 3-D box.
+template <int AM, bool PAIR>
+__device__ __forceinline__ void load_a(const GemmParams& p, uint32_t dst, const TileInfo& t, int kabs, int arow,
+                                       uint32_t bar) {
+  if constexpr (AM == A_K_TILE) {
+    if constexpr (PAIR)
+      tma_load_2d_pair(dst, &p.tmA, kabs, arow, bar);
+    else
+      tma_load_2d(dst, &p.tmA, kabs, arow, bar);
+  } else {
+    if constexpr (PAIR)
+      tma_load_3d_pair(dst, &p.tmA, 0, kabs, (p.a_col_off + t.m0) / 64, bar);
+    else
+      tma_load_3d(dst, &p.tmA, 0, kabs, (p.a_col_off + t.m0) / 64, bar);
+  }
+}
+
 template <int AM, int BMO, int EPI, int SCH, bool MX>
 __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_tiles, uint32_t s_sf,
                                               uint32_t full0, uint32_t empty0, const WorkRange& wr,
                                               volatile int* abort_flag, int lane) {
-  constexpr bool PAIR = SCH == SCHED_ROWS2;
+  constexpr bool PAIR = sched_pair(SCH);
   constexpr bool HALVES = b_halves<MX, EPI, SCH>();
   constexpr int BK = stage_k<MX>();
   constexpr int BN = gemm_bn<MX, EPI, SCH>();
   constexpr int SB = stage_bytes<MX, EPI, SCH>(), SFB = sf_stage_bytes<MX, EPI, SCH>();
   constexpr uint32_t kTx = SB + SFB;
-  static_assert(!HALVES || (AM == A_K_TILE && BN == kBN && !MX), "B halves: bf16, K-major A, 256-column tiles");
+  static_assert(!HALVES || (BN == kBN && !MX), "B halves: bf16, 256-column tiles");
   int s = 0;
   uint32_t ph = 0;
   // Per stage: parity of the last load issued into it, or -1.
@@ -426,7 +464,7 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
   for (int w = wr.first; w < wr.count && !aborted; w += wr.stride) {
     const TileInfo t = gemm_tile<EPI, SCH, BK, BN>(p, w, wr.rank);
     // row coordinate of the A tile: token rows, or output rows of a weight gradient
-    const int arow = SCH == SCHED_WGRAD ? p.a_col_off + t.m0 : t.row0;
+    const int arow = sched_wgrad(SCH) ? p.a_col_off + t.m0 : t.row0;
     const int brow = t.e * p.b_group_rows + t.n0;
     for (int kb = 0; kb < t.nkb; ++kb) {
       bool ok = true;
@@ -440,22 +478,19 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
       const uint32_t sA = s_tiles + s * SB;
       const uint32_t sB = sA + kATileBytes;
       const int kabs = (t.kb0 + kb) * BK;
-      if constexpr (PAIR) {
-        // this CTA's 128 rows of A and its half of B; the even CTA's
-        // barrier counts both CTAs' bytes
+      if constexpr (PAIR || HALVES) {
+        // 2-SM mode: this CTA's 128 rows (or MN columns) of A and its half of
+        // B, the even CTA's barrier counting both CTAs' bytes
         if (lane == 0) {
-          if (wr.rank == 0) mbar_arrive_expect_tx(full, 2 * kTx);
-          const uint32_t fb = lead_full0 + 8 * s;
-          tma_load_2d_pair(sA, &p.tmA, kabs, arow, fb);
-          load_b_half<BMO, true>(p, sB, t, kabs, brow, static_cast<int>(wr.rank), fb);
-        }
-        __syncwarp();
-      } else if constexpr (HALVES) {
-        if (lane == 0) {
-          mbar_arrive_expect_tx(full, kTx);
-          tma_load_2d(sA, &p.tmA, kabs, arow, full);
-          load_b_half<BMO, false>(p, sB, t, kabs, brow, 0, full);
-          load_b_half<BMO, false>(p, sB + kBTileBytes / 2, t, kabs, brow, 1, full);
+          if (!PAIR || wr.rank == 0) mbar_arrive_expect_tx(full, PAIR ? 2 * kTx : kTx);
+          const uint32_t fb = PAIR ? lead_full0 + 8 * s : full;
+          load_a<AM, PAIR>(p, sA, t, kabs, arow, fb);
+          if constexpr (PAIR) {
+            load_b_half<BMO, true>(p, sB, t, kabs, brow, static_cast<int>(wr.rank), fb);
+          } else {
+            load_b_half<BMO, false>(p, sB, t, kabs, brow, 0, full);
+            load_b_half<BMO, false>(p, sB + kBTileBytes / 2, t, kabs, brow, 1, full);
+          }
         }
         __syncwarp();
       } else {
@@ -541,7 +576,7 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
                                          const WorkRange& wr, volatile int* abort_flag) {
   // 2-SM mode: the even CTA issues the pair's MMAs (M = 256: its 128 rows of
   // A and the odd CTA's), the odd CTA's MMA warp has nothing to do
-  constexpr bool PAIR = SCH == SCHED_ROWS2;
+  constexpr bool PAIR = sched_pair(SCH);
   if (PAIR && wr.rank != 0) return;
   constexpr int BK = stage_k<MX>();
   constexpr int ST = gemm_stages<MX, EPI, SCH>();
@@ -697,7 +732,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
   int acc = 0;
   uint32_t aph = 0;
   EpiStager<epi_slots<MX, EPI, SCH>()> stg{s_warp, 0, lane};
-  constexpr bool PAIR = SCH == SCHED_ROWS2;
+  constexpr bool PAIR = sched_pair(SCH);
   // 2-SM mode: the accumulator is released on the even CTA's barrier
   const uint32_t acce_lead = PAIR ? mapa_shared(acce0, 0) : acce0;
   for (int w = wr.first; w < wr.count; w += wr.stride) {
@@ -728,7 +763,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
     const uint32_t tr = tmem_base + (static_cast<uint32_t>(warp_e * 32) << 16) +
                         static_cast<uint32_t>(acc * BN);
 
-    if constexpr (SCH == SCHED_WGRAD) {
+    if constexpr (sched_wgrad(SCH)) {
       const int r0 = t.m0 + warp_e * 32;
       for (int c0 = cbeg; c0 < cend && t.n0 + c0 < p.N; c0 += 64) {
         float v[64];
@@ -934,7 +969,7 @@ __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t a
   const uint32_t stash = tmem_base + lane_off + kStashCol + half * (kStashCols / 2);
   const int row = quad * 32 + lane;  // MXFP8 groups are 128-row aligned: no 64-row tiles
   const int warp_e = quad;
-  static_assert(SCH != SCHED_ROWS2, "MXFP8 kernels run on one SM per tile");
+  static_assert(!sched_pair(SCH), "MXFP8 kernels run on one SM per tile");
   for (int w = wr.first; w < wr.count; w += wr.stride) {
     const TileInfo t = gemm_tile<EPI, SCH, kBKmx>(p, w);
     if constexpr (EPI == EPI_SWIGLU_BWD) {  // the saved a, b of this warp's rows and columns: into L2 now
@@ -1154,7 +1189,7 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kerne
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  constexpr bool PAIR = SCH == SCHED_ROWS2;
+  constexpr bool PAIR = sched_pair(SCH);
   constexpr int CG = PAIR ? 2 : 1;
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < ST; ++i) {
@@ -1175,7 +1210,7 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kerne
     // only the output maps this launch stores through (MXFP8 mode stores directly)
     if (!MX && (EPI == EPI_BF16 || EPI == EPI_SWIGLU_FWD)) {
       tma_prefetch_desc(&p.tmO0);
-      if (SCH == SCHED_ROWS) tma_prefetch_desc(&p.tmO0h);
+      if (!sched_wgrad(SCH)) tma_prefetch_desc(&p.tmO0h);
     }
     if (!MX && EPI == EPI_SWIGLU_FWD) {
       tma_prefetch_desc(&p.tmO1);
