@@ -96,6 +96,11 @@ SHAPES = {
     "single_expert": MoEShape(T=200, d=128, I=128, E=1, k=1, n_shared=0, I_shared=0, w_std=0.05),
     "zipf_zero": MoEShape(T=640, d=256, I=128, E=32, k=4, n_shared=1, I_shared=128, w_std=0.05,
                           zipf=True, zero_experts=8),
+    # every expert and the shared expert have a single 64-row tile (the GEMMs' SM-pair pass has
+    # no work, all tiles go through the one-SM pass); dW_gate/dW_up have one 128-row output
+    # tile, dW_down three (one SM pair plus one tile on one SM)
+    "small_T": MoEShape(T=64, d=384, I=128, E=8, k=2, n_shared=1, I_shared=128, w_std=0.05),
+    "single_token": MoEShape(T=1, d=256, I=256, E=16, k=4, n_shared=1, I_shared=256, w_std=0.05),
 }
 
 
