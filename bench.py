@@ -275,6 +275,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per reference step")
     ap.add_argument("--cpu-mx", action="store_true",
                     help="also time the MXFP8 oracle for dsv3_mxfp8 (about 11 min per token)")
+    ap.add_argument("--replay", action="store_true",
+                    help="MOE_FLAG_REPLAY: save only the routing, recompute x rows, a and b in the backward")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -308,7 +310,8 @@ def main():
     s, desc, mx = _workload(args.workload, args.tokens, args.experts)
     inp = make_inputs(s, seed=rank, device="cuda")
     cfg = _abi.make_config(s.T, s.d, s.I, s.E, s.k, s.n_shared, s.I_shared,
-                           precision=_abi.MOE_MXFP8 if mx else _abi.MOE_BF16)
+                           precision=_abi.MOE_MXFP8 if mx else _abi.MOE_BF16,
+                           flags=_abi.MOE_FLAG_REPLAY if args.replay else 0)
     if mx:
         layer.quantize_weights(cfg, inp)
     bufs = layer.MoEBuffers(cfg)
@@ -460,6 +463,7 @@ def main():
             "config": {"workload": desc, "T": s.T, "d": s.d, "I": s.I, "E": s.E, "top_k": s.k,
                        "n_shared": s.n_shared, "I_shared": s.I_shared, "tokens_per_gpu": s.T,
                        "parallelism": f"replicas x{world}",
+                       "activations": "replayed in the backward" if args.replay else "saved",
                        "l2": "inputs larger than L2 (x 235 MB, expert weights 22.6 GB at dsv3); no flush"},
             "tflops": tflops, "pct_tensor_peak": tflops / t_burst,
             "pct_tensor_peak_sustained": tflops / t_sust, "tensor_peak_src": t_src,

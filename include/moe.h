@@ -58,6 +58,18 @@ typedef enum {
 
 typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
 
+/* moe_config.flags.
+ * MOE_FLAG_REPLAY: the saved state holds only the routing; moe_backward first
+ *   recomputes the forward up to the SwiGLU activation (the expert-grouped x
+ *   rows, a and b, routed and shared) into its workspace ("forward activation
+ *   replay", Mixture-of-Kittens blog post, section "Reversed ring to minimize
+ *   forward replay during backward").  The saved buffer shrinks by
+ *   Rp*(2d + 4I) + T*4*I_shared bytes in bf16 mode (Rp: routes padded per
+ *   expert), the backward workspace grows by about as much, and the backward
+ *   does the dispatch and gate/up GEMMs again.  Results are bitwise identical
+ *   to those without the flag. */
+#define MOE_FLAG_REPLAY 1u
+
 typedef struct {
   int64_t T;        /* tokens */
   int64_t d;        /* model dimension */
@@ -67,7 +79,7 @@ typedef struct {
   int64_t n_shared; /* shared experts: 0 or 1 */
   int64_t I_shared; /* shared expert intermediate dimension (ignored if n_shared == 0) */
   int32_t precision;/* moe_precision */
-  uint32_t flags;   /* reserved, must be 0 */
+  uint32_t flags;   /* MOE_FLAG_* bits; any other bit gives MOE_ERR_UNSUPPORTED */
 } moe_config;
 
 typedef struct {
@@ -99,7 +111,8 @@ typedef struct {
 
 /* Byte sizes of the caller-allocated buffers for a configuration:
  *   fwd_ws  scratch for moe_forward and moe_route_topk
- *   saved   state moe_forward leaves for moe_backward (routing, a and b)
+ *   saved   state moe_forward leaves for moe_backward (routing; the x rows, a
+ *           and b unless MOE_FLAG_REPLAY)
  *   bwd_ws  scratch for moe_backward
  * Each buffer must be 256-byte aligned; its first 256 bytes hold the device
  * status word and must be zero before the buffer's first use. */

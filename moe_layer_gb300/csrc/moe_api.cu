@@ -99,8 +99,9 @@ constexpr size_t kAlign = 256;
 
 struct Shape {
   int64_t T, d, I, E, k, S, Is, R, Rp, nchunk, nparts;
-  int64_t ra;  // row alignment of the expert groups
-  bool mx;     // MXFP8 routed experts
+  int64_t ra;   // row alignment of the expert groups
+  bool mx;      // MXFP8 routed experts
+  bool replay;  // saved state = routing only; the backward recomputes the rest
 };
 
 // Carves 256-byte aligned sub-buffers from a base pointer (or only sizes them
@@ -150,23 +151,35 @@ void carve_routing(Carver& c, const Shape& s, Routing& r) {
   r.perm_w_pad = c.take<float>(s.Rp);
 }
 
-struct Saved {
-  Routing rt;
+// The forward's activations the backward needs: the x rows for the weight
+// gradients of gate/up and the pre-activations a, b of the SwiGLU backward.
+struct Acts {
   __nv_bfloat16* xp;   // [Rp, d] x rows in expert-grouped order (bf16 mode)
   __nv_bfloat16* ab;   // [Rp, 2I]
   __nv_bfloat16* abs;  // [T, 2Is]
   uint8_t *xt, *xt_sf;  // MXFP8: the x rows transposed, quantized along the tokens [d, Rp]
 };
+void carve_acts(Carver& c, const Shape& s, Acts& a) {
+  const int64_t m = s.mx ? 1 : 0;
+  a.xp = c.take<__nv_bfloat16>((1 - m) * s.Rp * s.d);
+  a.ab = c.take<__nv_bfloat16>(s.Rp * 2 * s.I);
+  a.abs = c.take<__nv_bfloat16>(s.S ? s.T * 2 * s.Is : 0);
+  a.xt = c.take<uint8_t>(m * s.Rp * s.d);
+  a.xt_sf = c.take<uint8_t>(m * mx_sf_alloc(s.d, s.Rp));
+}
+
+// State moe_forward leaves for moe_backward: the routing, and the activations
+// unless they are replayed (MOE_FLAG_REPLAY; then act lives in the backward
+// workspace).
+struct Saved {
+  Routing rt;
+  Acts act;
+};
 void carve_saved(void* base, const Shape& s, Saved& v, size_t* bytes) {
   Carver c(base);
   c.take<char>(kAlign);
   carve_routing(c, s, v.rt);
-  const int64_t m = s.mx ? 1 : 0;
-  v.xp = c.take<__nv_bfloat16>((1 - m) * s.Rp * s.d);
-  v.ab = c.take<__nv_bfloat16>(s.Rp * 2 * s.I);
-  v.abs = c.take<__nv_bfloat16>(s.S ? s.T * 2 * s.Is : 0);
-  v.xt = c.take<uint8_t>(m * s.Rp * s.d);
-  v.xt_sf = c.take<uint8_t>(m * mx_sf_alloc(s.d, s.Rp));
+  if (!s.replay) carve_acts(c, s, v.act);
   if (bytes) *bytes = c.off;
 }
 
@@ -225,6 +238,7 @@ struct BwdWs {
   uint8_t *dyt, *dyt_sf;      // [d, Rp]
   uint8_t *dadbt, *dadbt_sf;  // [2I, Rp]
   uint8_t *hgt, *hgt_sf;      // [I, Rp]
+  Acts act;                   // MOE_FLAG_REPLAY: the recomputed activations
 };
 void carve_bwd(void* base, const Shape& s, BwdWs& w, size_t* bytes) {
   Carver c(base);
@@ -251,6 +265,7 @@ void carve_bwd(void* base, const Shape& s, BwdWs& w, size_t* bytes) {
   w.dadbt_sf = c.take<uint8_t>(m * mx_sf_alloc(2 * s.I, s.Rp));
   w.hgt = c.take<uint8_t>(m * s.Rp * s.I);
   w.hgt_sf = c.take<uint8_t>(m * mx_sf_alloc(s.I, s.Rp));
+  if (s.replay) carve_acts(c, s, w.act);
   if (bytes) *bytes = c.off;
 }
 
@@ -287,7 +302,7 @@ moe_status check_config(const moe_config* cfg, Shape& s) {
     return MOE_ERR_INVALID_ARG;
   if (cfg->precision != MOE_BF16 && cfg->precision != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
   if (cfg->precision == MOE_MXFP8 && (cfg->d % 128 || cfg->I % 128)) return MOE_ERR_UNSUPPORTED;
-  if (cfg->flags != 0) return MOE_ERR_UNSUPPORTED;
+  if (cfg->flags & ~MOE_FLAG_REPLAY) return MOE_ERR_UNSUPPORTED;
   if (cfg->E > kMaxExperts || cfg->top_k > kMaxTopK || cfg->top_k > cfg->E) return MOE_ERR_UNSUPPORTED;
   if (cfg->n_shared > 1) return MOE_ERR_UNSUPPORTED;
   if (cfg->d % 64 || cfg->I % 64 || (cfg->n_shared && cfg->I_shared % 64)) return MOE_ERR_UNSUPPORTED;
@@ -300,6 +315,7 @@ moe_status check_config(const moe_config* cfg, Shape& s) {
   s.Is = cfg->n_shared ? cfg->I_shared : 0;
   s.R = s.T * s.k;
   s.mx = cfg->precision == MOE_MXFP8;
+  s.replay = (cfg->flags & MOE_FLAG_REPLAY) != 0;
   s.ra = s.mx ? kRowAlignMx : kRowAlign;
   s.Rp = s.R + s.E * (s.ra - 1);
   if (s.mx) s.Rp = (s.Rp + kRowAlignMx - 1) / kRowAlignMx * kRowAlignMx;  // whole scale blocks
@@ -443,64 +459,149 @@ void set_mx_scales(GemmParams& p, const uint8_t* sfa, int64_t a_rows, const uint
   p.sfb_rb = cdiv(b_rows, 128);
 }
 
-// Routed experts of the forward in MXFP8 mode (blog section "MXFP8 support"):
-// x rows already quantized (w.xq); gate/up with the SwiGLU epilogue writing h
-// as E4M3 + scales; down projection on the quantized h, scaled by the router
-// weight of each row.
-moe_status forward_routed_mx(const Shape& s, const moe_weights* wts, const Routing& rt, const Saved* sv,
-                             const FwdWs& w, cudaStream_t st) {
+// Routed gate/up of the forward in MXFP8 mode (blog section "MXFP8 support"):
+// on the quantized x rows xq, the SwiGLU epilogue writing h as E4M3 + scales
+// (hq) and, when act is given, the a and b rows for the backward.
+moe_status gateup_routed_mx(const Shape& s, const moe_weights* wts, const Routing& rt, const Acts* act,
+                            const uint8_t* xq, const uint8_t* xq_sf, uint8_t* hq, uint8_t* hq_sf, int* status,
+                            cudaStream_t st) {
   MxWeights m;
   carve_mx(const_cast<void*>(wts->mxfp8), s, m, nullptr);
-  const int d = static_cast<int>(s.d), I = static_cast<int>(s.I), E = static_cast<int>(s.E);
-  {
+  GemmParams p;
+  zero_params(p);
+  MOE_TRY(qmap(&p.tmA, xq, s.Rp, s.d, kBM));
+  MOE_TRY(qmap(&p.tmB0, m.wg, s.E * s.I, s.d, kBN / 2));
+  MOE_TRY(qmap(&p.tmB1, m.wu, s.E * s.I, s.d, kBN / 2));
+  set_mx_scales(p, xq_sf, s.Rp, m.wg_sf, m.wu_sf, s.E * s.I);
+  p.num_groups = static_cast<int>(s.E);
+  p.row_start = rt.row_start;
+  p.tile_start = rt.tile_start;
+  p.pair_start = rt.pair_start;
+  p.rem_start = rt.rem_start;
+  p.counts = rt.counts;
+  p.N = static_cast<int>(s.I);
+  p.K = static_cast<int>(s.d);
+  p.b_group_rows = static_cast<int>(s.I);
+  if (act) {  // a and b rows kept for the backward (direct row stores)
+    p.out = act->ab;
+    p.ldo = 2 * s.I;
+    p.store_ab = 1;
+  }
+  p.I = static_cast<int>(s.I);
+  p.qout = hq;
+  p.qld = s.I;
+  p.qsf = hq_sf;
+  p.q_rb = cdiv(s.Rp, 128);
+  p.status = status;
+  MOE_LAUNCH(PL_GATEUP_ROUTED, st, launch_gemm(GK_MX_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.I, kBN / 2)), st));
+  return MOE_OK;
+}
+
+// Routed down projection in MXFP8 mode, on the quantized h rows, scaled by
+// the router weight of each row.
+moe_status down_routed_mx(const Shape& s, const moe_weights* wts, const Routing& rt, const FwdWs& w,
+                          cudaStream_t st) {
+  MxWeights m;
+  carve_mx(const_cast<void*>(wts->mxfp8), s, m, nullptr);
+  GemmParams p;
+  zero_params(p);
+  MOE_TRY(qmap(&p.tmA, w.hq, s.Rp, s.I, kBM));
+  MOE_TRY(qmap(&p.tmB0, m.wd, s.E * s.d, s.I, kBN));
+  set_mx_scales(p, w.hq_sf, s.Rp, m.wd_sf, nullptr, s.E * s.d);
+  p.num_groups = static_cast<int>(s.E);
+  p.row_start = rt.row_start;
+  p.tile_start = rt.tile_start;
+  p.pair_start = rt.pair_start;
+  p.rem_start = rt.rem_start;
+  p.counts = rt.counts;
+  p.N = static_cast<int>(s.d);
+  p.K = static_cast<int>(s.I);
+  p.b_group_rows = static_cast<int>(s.d);
+  MOE_TRY(omap(&p.tmO0, w.o, s.Rp, s.d));
+  p.row_scale = rt.perm_w_pad;
+  p.status = w.status;
+  MOE_LAUNCH(PL_DOWN_ROUTED, st, launch_gemm(GK_MX_DOWN, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
+  return MOE_OK;
+}
+
+// Buffers the forward's first half writes besides the activations it keeps.
+struct GateUpOut {
+  __nv_bfloat16* xp;    // bf16 mode: [Rp, d] x rows, when no activations are kept
+  __nv_bfloat16* h;     // bf16 mode: [Rp, I] SwiGLU output
+  __nv_bfloat16* hs;    // [T, Is] shared expert's SwiGLU output
+  uint8_t *xq, *xq_sf;  // MXFP8: [Rp, d] x rows quantized along d
+  uint8_t *hq, *hq_sf;  // MXFP8: [Rp, I] h quantized along I
+  int* status;
+};
+
+// The forward up to the SwiGLU activation: dispatch of x (quantized on the
+// way in MXFP8 mode) and the gate/up projections with the SwiGLU epilogue,
+// shared and routed.  act: where the activations the backward needs go (the
+// x rows, a and b), or null in inference.  The backward runs this again when
+// the saved state holds only the routing (forward activation replay).
+moe_status forward_gateup(const Shape& s, const void* x, const moe_weights* wts, const Routing& rt,
+                          const Acts* act, const GateUpOut& o, cudaStream_t st) {
+  const int T = static_cast<int>(s.T), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
+  const int E = static_cast<int>(s.E);
+  // dispatch: x rows into expert-grouped order (zeros in padding rows); in
+  // MXFP8 mode quantized on the way, the bf16 copy kept only for training
+  __nv_bfloat16* xp = act ? act->xp : o.xp;
+  if (s.mx)  // along d for gate/up; in training also along the tokens for dW_gate, dW_up
+    MOE_LAUNCH(PL_MX_QUANT_X, st, launch_mx_permute_dual(static_cast<const __nv_bfloat16*>(x), d, rt.perm_token_pad,
+                                                         rt.row_start + E, s.Rp, d, o.xq, o.xq_sf,
+                                                         act ? act->xt : nullptr, act ? act->xt_sf : nullptr, st));
+  else
+    MOE_LAUNCH(PL_PERMUTE_X, st, launch_permute_rows(static_cast<const __nv_bfloat16*>(x), rt.perm_token_pad,
+                                                    rt.row_start + E, static_cast<int>(s.Rp), d, xp, st));
+  // shared expert gate/up + SwiGLU (dense rows of x)
+  if (s.S) {
     GemmParams p;
     zero_params(p);
-    MOE_TRY(qmap(&p.tmA, w.xq, s.Rp, s.d, kBM));
-    MOE_TRY(qmap(&p.tmB0, m.wg, s.E * s.I, s.d, kBN / 2));
-    MOE_TRY(qmap(&p.tmB1, m.wu, s.E * s.I, s.d, kBN / 2));
-    set_mx_scales(p, w.xq_sf, s.Rp, m.wg_sf, m.wu_sf, s.E * s.I);
-    p.num_groups = E;
-    p.row_start = rt.row_start;
-    p.tile_start = rt.tile_start;
-    p.pair_start = rt.pair_start;
-    p.rem_start = rt.rem_start;
-    p.counts = rt.counts;
-    p.N = I;
+    MOE_TRY(tmap(&p.tmA, x, s.T, s.d, 64, kBM));
+    MOE_TRY(tmap(&p.tmB0, wts->Ws_gate, s.Is, s.d, 64, kBN / 2));
+    MOE_TRY(tmap(&p.tmB1, wts->Ws_up, s.Is, s.d, 64, kBN / 2));
+    p.dense_rows = T;
+    p.N = static_cast<int>(s.Is);
     p.K = d;
-    p.b_group_rows = I;
-    if (sv) {  // a and b rows kept for the backward (direct row stores)
-      p.out = sv->ab;
-      p.ldo = 2 * s.I;
-      p.store_ab = 1;
-    }
-    p.I = I;
-    p.qout = w.hq;
-    p.qld = s.I;
-    p.qsf = w.hq_sf;
-    p.q_rb = cdiv(s.Rp, 128);
-    p.status = w.status;
-    MOE_LAUNCH(PL_GATEUP_ROUTED, st, launch_gemm(GK_MX_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.I, kBN / 2)), st));
+    MOE_TRY(omap(&p.tmO1, o.hs, s.T, s.Is));
+    if (act)
+      MOE_TRY(omap(&p.tmO0, act->abs, s.T, 2 * s.Is));
+    else
+      p.tmO0 = p.tmO1;  // a and b are not kept in inference
+    p.tmO0h = p.tmO0;  // dense rows: no tail tiles
+    p.tmO1h = p.tmO1;
+    p.store_ab = act ? 1 : 0;
+    p.I = static_cast<int>(s.Is);
+    p.status = o.status;
+    MOE_LAUNCH(PL_GATEUP_SHARED, st, launch_gemm(GK_GATEUP, p, grid_for(cdiv(s.T, kBM) * cdiv(s.Is, kBN / 2)), st));
   }
-  {
-    GemmParams p;
-    zero_params(p);
-    MOE_TRY(qmap(&p.tmA, w.hq, s.Rp, s.I, kBM));
-    MOE_TRY(qmap(&p.tmB0, m.wd, s.E * s.d, s.I, kBN));
-    set_mx_scales(p, w.hq_sf, s.Rp, m.wd_sf, nullptr, s.E * s.d);
-    p.num_groups = E;
-    p.row_start = rt.row_start;
-    p.tile_start = rt.tile_start;
-    p.pair_start = rt.pair_start;
-    p.rem_start = rt.rem_start;
-    p.counts = rt.counts;
-    p.N = d;
-    p.K = I;
-    p.b_group_rows = d;
-    MOE_TRY(omap(&p.tmO0, w.o, s.Rp, s.d));
-    p.row_scale = rt.perm_w_pad;
-    p.status = w.status;
-    MOE_LAUNCH(PL_DOWN_ROUTED, st, launch_gemm(GK_MX_DOWN, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
+  if (s.mx) return gateup_routed_mx(s, wts, rt, act, o.xq, o.xq_sf, o.hq, o.hq_sf, o.status, st);
+  // routed gate/up + SwiGLU over the expert-grouped rows
+  GemmParams p;
+  zero_params(p);
+  MOE_TRY(tmap(&p.tmA, xp, s.Rp, s.d, 64, kBM));
+  MOE_TRY(tmap(&p.tmB0, wts->W_gate, s.E * s.I, s.d, 64, kBN / 2));
+  MOE_TRY(tmap(&p.tmB1, wts->W_up, s.E * s.I, s.d, 64, kBN / 2));
+  p.num_groups = E;
+  p.row_start = rt.row_start;
+  p.counts = rt.counts;
+  p.N = I;
+  p.K = d;
+  p.b_group_rows = I;
+  MOE_TRY(omap2(&p.tmO1, &p.tmO1h, o.h, s.Rp, s.I));
+  if (act) {
+    MOE_TRY(omap2(&p.tmO0, &p.tmO0h, act->ab, s.Rp, 2 * s.I));
+  } else {
+    p.tmO0 = p.tmO1;  // a and b are not kept in inference
+    p.tmO0h = p.tmO1h;
   }
+  p.tile_start = rt.tile_start;
+  p.pair_start = rt.pair_start;
+  p.rem_start = rt.rem_start;
+  p.store_ab = act ? 1 : 0;
+  p.I = I;
+  p.status = o.status;
+  MOE_LAUNCH(PL_GATEUP_ROUTED, st, launch_gemm(GK_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.I, kBN / 2)), st));
   return MOE_OK;
 }
 
@@ -510,7 +611,7 @@ moe_status forward_routed_mx(const Shape& s, const moe_weights* wts, const Routi
 // boundaries, so a block never mixes experts):
 //   dW_down[e] = dy^T (g h),  dW_gate[e] = da^T x,  dW_up[e] = db^T x
 // as K-major block-scaled GEMMs over [row_start[e], row_start[e+1]).
-moe_status wgrad_routed_mx(const Shape& s, const Routing& rt, const Saved& sv, const BwdWs& w,
+moe_status wgrad_routed_mx(const Shape& s, const Routing& rt, const Acts& act, const BwdWs& w,
                            const moe_grads* g, cudaStream_t st) {
   constexpr int kWgradBnMx = gemm_bn<true, EPI_BF16, SCHED_WGRAD>();  // 128-column tiles
   const int d = static_cast<int>(s.d), I = static_cast<int>(s.I), E = static_cast<int>(s.E);
@@ -532,8 +633,8 @@ moe_status wgrad_routed_mx(const Shape& s, const Routing& rt, const Saved& sv, c
     GemmParams p;  // dW_gate[e] = da^T . x_rows ; dW_up[e] = db^T . x_rows
     zero_params(p);
     MOE_TRY(qmap(&p.tmA, w.dadbt, 2 * s.I, s.Rp, kBM));
-    MOE_TRY(qmap(&p.tmB0, sv.xt, s.d, s.Rp, kWgradBnMx));
-    set_mx_scales(p, w.dadbt_sf, 2 * s.I, sv.xt_sf, nullptr, s.d);
+    MOE_TRY(qmap(&p.tmB0, act.xt, s.d, s.Rp, kWgradBnMx));
+    set_mx_scales(p, w.dadbt_sf, 2 * s.I, act.xt_sf, nullptr, s.d);
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.M_out = I;
@@ -652,71 +753,14 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
   const int T = static_cast<int>(s.T), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
   const int E = static_cast<int>(s.E);
 
-  // dispatch: x rows into expert-grouped order (zeros in padding rows); in
-  // MXFP8 mode quantized on the way, the bf16 copy kept only for training
-  __nv_bfloat16* xp = saved ? sv.xp : w.xp;
-  if (s.mx)  // along d for gate/up; in training also along the tokens for dW_gate, dW_up
-    MOE_LAUNCH(PL_MX_QUANT_X, st, launch_mx_permute_dual(static_cast<const __nv_bfloat16*>(x), d, rt.perm_token_pad,
-                                                         rt.row_start + E, s.Rp, d, w.xq, w.xq_sf,
-                                                         saved ? sv.xt : nullptr, saved ? sv.xt_sf : nullptr, st));
-  else
-    MOE_LAUNCH(PL_PERMUTE_X, st, launch_permute_rows(static_cast<const __nv_bfloat16*>(x), rt.perm_token_pad,
-                                                    rt.row_start + E, static_cast<int>(s.Rp), d, xp, st));
-  // shared expert gate/up + SwiGLU (dense rows of x)
-  if (s.S) {
-    GemmParams p;
-    zero_params(p);
-    MOE_TRY(tmap(&p.tmA, x, s.T, s.d, 64, kBM));
-    MOE_TRY(tmap(&p.tmB0, wts->Ws_gate, s.Is, s.d, 64, kBN / 2));
-    MOE_TRY(tmap(&p.tmB1, wts->Ws_up, s.Is, s.d, 64, kBN / 2));
-    p.dense_rows = T;
-    p.N = static_cast<int>(s.Is);
-    p.K = d;
-    MOE_TRY(omap(&p.tmO1, w.hs, s.T, s.Is));
-    if (saved)
-      MOE_TRY(omap(&p.tmO0, sv.abs, s.T, 2 * s.Is));
-    else
-      p.tmO0 = p.tmO1;  // a and b are not kept in inference
-    p.tmO0h = p.tmO0;  // dense rows: no tail tiles
-    p.tmO1h = p.tmO1;
-    p.store_ab = saved ? 1 : 0;
-    p.I = static_cast<int>(s.Is);
-    p.status = w.status;
-    MOE_LAUNCH(PL_GATEUP_SHARED, st, launch_gemm(GK_GATEUP, p, grid_for(cdiv(s.T, kBM) * cdiv(s.Is, kBN / 2)), st));
-  }
+  // the activations the backward needs go to the saved state, unless it keeps
+  // only the routing (MOE_FLAG_REPLAY) or there is none (inference)
+  const GateUpOut o{w.xp, w.h, w.hs, w.xq, w.xq_sf, w.hq, w.hq_sf, w.status};
+  MOE_TRY(forward_gateup(s, x, wts, rt, (saved && !s.replay) ? &sv.act : nullptr, o, st));
   if (s.mx) {
-    MOE_TRY(forward_routed_mx(s, wts, rt, saved ? &sv : nullptr, w, st));
+    MOE_TRY(down_routed_mx(s, wts, rt, w, st));
   } else {
-  // routed gate/up + SwiGLU over the expert-grouped rows
-  {
-    GemmParams p;
-    zero_params(p);
-    MOE_TRY(tmap(&p.tmA, xp, s.Rp, s.d, 64, kBM));
-    MOE_TRY(tmap(&p.tmB0, wts->W_gate, s.E * s.I, s.d, 64, kBN / 2));
-    MOE_TRY(tmap(&p.tmB1, wts->W_up, s.E * s.I, s.d, 64, kBN / 2));
-    p.num_groups = E;
-    p.row_start = rt.row_start;
-    p.counts = rt.counts;
-    p.N = I;
-    p.K = d;
-    p.b_group_rows = I;
-    MOE_TRY(omap2(&p.tmO1, &p.tmO1h, w.h, s.Rp, s.I));
-    if (saved) {
-      MOE_TRY(omap2(&p.tmO0, &p.tmO0h, sv.ab, s.Rp, 2 * s.I));
-    } else {
-      p.tmO0 = p.tmO1;  // a and b are not kept in inference
-      p.tmO0h = p.tmO1h;
-    }
-    p.tile_start = rt.tile_start;
-    p.pair_start = rt.pair_start;
-    p.rem_start = rt.rem_start;
-    p.store_ab = saved ? 1 : 0;
-    p.I = I;
-    p.status = w.status;
-    MOE_LAUNCH(PL_GATEUP_ROUTED, st, launch_gemm(GK_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.I, kBN / 2)), st));
-  }
-  // routed down projection, scaled by the router weight of each row
-  {
+    // routed down projection, scaled by the router weight of each row
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, w.h, s.Rp, s.I, 64, kBM));
@@ -734,7 +778,6 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.row_scale = rt.perm_w_pad;
     p.status = w.status;
     MOE_LAUNCH(PL_DOWN_ROUTED, st, launch_gemm(GK_DOWN, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
-  }
   }
   // shared down projection
   if (s.S) {
@@ -774,6 +817,16 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
   carve_bwd(ws, s, w, nullptr);
   const int T = static_cast<int>(s.T), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
   const int E = static_cast<int>(s.E), k = static_cast<int>(s.k), Is = static_cast<int>(s.Is);
+  // MOE_FLAG_REPLAY: the saved state holds only the routing; recompute the
+  // forward up to the SwiGLU into the workspace.  Its h outputs and quantized
+  // x rows land in buffers this backward overwrites later (hg, hs; in MXFP8
+  // mode dadbq and dyq), the same kernels on the same inputs as the forward,
+  // so a and b are bitwise those the forward produced.
+  const Acts& act = s.replay ? w.act : sv.act;
+  if (s.replay) {
+    const GateUpOut o{nullptr, w.hg, w.hs, w.dyq, w.dyq_sf, w.dadbq, w.dadbq_sf, w.status};
+    MOE_TRY(forward_gateup(s, x, wts, rt, &w.act, o, st));
+  }
 
   MxWeights m;
   if (s.mx) carve_mx(const_cast<void*>(wts->mxfp8), s, m, nullptr);
@@ -803,7 +856,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.b_group_rows = I;
     p.out3 = w.dg_part;
     p.ldo3 = static_cast<int>(s.nparts);
-    p.ab = sv.ab;
+    p.ab = act.ab;
     p.I = I;
     p.tile_start = rt.tile_start;
     p.pair_start = rt.pair_start;
@@ -840,7 +893,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.ldo2 = s.I;
     p.out3 = w.dg_part;
     p.ldo3 = static_cast<int>(s.nparts);
-    p.ab = sv.ab;
+    p.ab = act.ab;
     p.I = I;
     p.tile_start = rt.tile_start;
     p.pair_start = rt.pair_start;
@@ -861,7 +914,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.ldo = 2 * s.Is;
     p.out2 = w.hs;
     p.ldo2 = s.Is;
-    p.ab = sv.abs;
+    p.ab = act.abs;
     p.I = Is;
     p.status = w.status;
     MOE_LAUNCH(PL_DGRAD_DOWN_SHARED, st, launch_gemm(GK_DGRAD_DOWN, p, grid_for(cdiv(s.T, kBM) * cdiv(s.Is, kBN)), st));
@@ -931,7 +984,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
                                                       static_cast<const __nv_bfloat16*>(x), E, d, g->dW_router, st));
   // weight gradients, reduced over each expert's full row range (no split-K)
   if (s.mx) {
-    MOE_TRY(wgrad_routed_mx(s, rt, sv, w, g, st));
+    MOE_TRY(wgrad_routed_mx(s, rt, act, w, g, st));
   } else {
   {
     GemmParams p;  // dW_down[e] = dy_rows^T . (g h)
@@ -950,7 +1003,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     GemmParams p;  // dW_gate[e] = da^T . x_rows ; dW_up[e] = db^T . x_rows
     zero_params(p);
     MOE_TRY(mnmap(&p.tmA, w.dadb, s.Rp, 2 * s.I, 2));
-    MOE_TRY(mnmap(&p.tmB0, sv.xp, s.Rp, s.d, 2));
+    MOE_TRY(mnmap(&p.tmB0, act.xp, s.Rp, s.d, 2));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.M_out = I;

@@ -47,6 +47,26 @@ def test_workspace_sizes_scale_with_shape(lib):
     assert big[1] >= 16384 * 8 * 2 * 2048 * 2
 
 
+def test_replay_flag_moves_the_activations_from_saved_to_the_backward_workspace(lib):
+    T, d, I, E, k, Is = 4096, 1024, 512, 64, 6, 256
+    base = _abi.moe_workspace_size(_abi.make_config(T, d, I, E, k, 1, Is))
+    rep = _abi.moe_workspace_size(_abi.make_config(T, d, I, E, k, 1, Is, flags=_abi.MOE_FLAG_REPLAY))
+    Rp = T * k + E * 63  # routes padded to 64 rows per expert (bf16 mode)
+    acts = Rp * (2 * d + 4 * I) + 4 * T * Is  # x rows, a and b, the shared expert's a and b
+    slack = 5 * 256  # 256-byte alignment of each buffer
+    assert rep[0] == base[0]
+    assert abs((base[1] - rep[1]) - acts) <= slack
+    assert abs((rep[2] - base[2]) - acts) <= slack
+    # routing only: a few ints per route and per expert
+    assert rep[1] < 64 * T * k
+
+
+def test_unknown_flag_bits_rejected(lib):
+    a = ctypes.c_size_t()
+    c = _abi.make_config(512, 256, 128, 8, 2, flags=2)
+    assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(a), None, None) == 2
+
+
 @pytest.mark.parametrize("cfg,code", [
     ((512, 100, 128, 8, 2, 0, 0), 2),     # d not a multiple of 64
     ((512, 256, 96, 8, 2, 0, 0), 2),      # I not a multiple of 64

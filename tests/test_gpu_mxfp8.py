@@ -98,11 +98,11 @@ def _cuda(inp):
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
-def _run_mx(shape, seed=0, backward=True):
+def _run_mx(shape, seed=0, backward=True, flags=0):
     inp_cpu = make_inputs(shape, seed=seed, with_dy=backward)
     inp = _cuda(inp_cpu)
     cfg = _abi.make_config(shape.T, shape.d, shape.I, shape.E, shape.k, shape.n_shared, shape.I_shared,
-                           precision=_abi.MOE_MXFP8)
+                           precision=_abi.MOE_MXFP8, flags=flags)
     layer.quantize_weights(cfg, inp)
     bufs = layer.MoEBuffers(cfg, training=backward)
     y = layer.forward(cfg, inp, bufs)
@@ -161,6 +161,17 @@ def test_mxfp8_inference_matches_training_forward_and_is_deterministic(monkeypat
     for key in b["grads"]:
         if b["grads"][key] is not None:
             assert torch.equal(b["grads"][key], c["grads"][key]), key
+
+
+def test_mxfp8_replay_matches_saved_activations_bitwise():
+    shape = MX_SHAPES["mx_zipf_zero"]
+    a = _run_mx(shape, seed=1)
+    b = _run_mx(shape, seed=1, flags=_abi.MOE_FLAG_REPLAY)
+    assert torch.equal(a["y"], b["y"])
+    assert torch.equal(a["dx"], b["dx"])
+    for key in a["grads"]:
+        if a["grads"][key] is not None:
+            assert torch.equal(a["grads"][key], b["grads"][key]), key
 
 
 def test_mxfp8_forward_requires_quantized_weights():

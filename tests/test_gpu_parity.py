@@ -69,10 +69,11 @@ def test_routing_bit_exact_on_given_logits(T, E, k, ties):
     np.testing.assert_allclose(g["topk_w"], w, rtol=1e-6, atol=1e-7)
 
 
-def _run_layer(shape, seed=0, backward=True):
+def _run_layer(shape, seed=0, backward=True, flags=0):
     inp_cpu = make_inputs(shape, seed=seed, with_dy=backward)
     inp = _cuda(inp_cpu)
-    cfg = _abi.make_config(shape.T, shape.d, shape.I, shape.E, shape.k, shape.n_shared, shape.I_shared)
+    cfg = _abi.make_config(shape.T, shape.d, shape.I, shape.E, shape.k, shape.n_shared, shape.I_shared,
+                           flags=flags)
     bufs = layer.MoEBuffers(cfg, training=backward)
     y = layer.forward(cfg, inp, bufs)
     res = {"y": y, "inp_cpu": inp_cpu, "cfg": cfg, "bufs": bufs, "inp": inp}
@@ -174,6 +175,22 @@ def test_bitwise_determinism(grid_limit, monkeypatch):
     if grid_limit:
         monkeypatch.setenv("MOE_GRID_LIMIT", grid_limit)
     b = _run_layer(shape, seed=5)
+    assert torch.equal(a["y"], b["y"])
+    assert torch.equal(a["dx"], b["dx"])
+    for key in a["grads"]:
+        if a["grads"][key] is not None:
+            assert torch.equal(a["grads"][key], b["grads"][key]), key
+
+
+@pytest.mark.parametrize("name", ["ragged", "noshared", "zipf_zero"])
+def test_replay_matches_saved_activations_bitwise(name):
+    """MOE_FLAG_REPLAY (saved state = routing only, the backward recomputes the
+    x rows, a and b) gives bitwise the outputs and gradients of the path that
+    saves them, with a saved buffer that holds no activations."""
+    shape = SHAPES[name]
+    a = _run_layer(shape, seed=SEEDS.get(name, 0))
+    b = _run_layer(shape, seed=SEEDS.get(name, 0), flags=_abi.MOE_FLAG_REPLAY)
+    assert b["bufs"].saved.numel() < a["bufs"].saved.numel()
     assert torch.equal(a["y"], b["y"])
     assert torch.equal(a["dx"], b["dx"])
     for key in a["grads"]:
