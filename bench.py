@@ -1,7 +1,7 @@
 """Benchmark of the MoE layer hot path (forward + backward) through the C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload dsv3|qwen3|tiny|dsv3_mxfp8]
+                    [--workload dsv3|qwen3|tiny|dsv3_mxfp8|kimi_k27|glm52|qwen35|dsv4pro]
 
 One step = forward + backward of the whole layer on one batch of seeded
 synthetic input of the workload (default: the DeepSeek-V3-shaped layer,
@@ -72,6 +72,10 @@ def _workload(name, tokens=0, experts=0):
         "tiny": "tiny BF16 MoE layer forward+backward",
         "dsv3_mxfp8": "DSV3-shaped MXFP8 MoE layer forward+backward (routed experts MXFP8, "
                       "router and shared expert BF16, BF16 outputs)",
+        "kimi_k27": "Kimi-K2.7-shaped BF16 MoE layer forward+backward (E=384, d=7168, I=2048, top-8)",
+        "glm52": "GLM-5.2-shaped BF16 MoE layer forward+backward (E=256, d=6144, I=2048, top-8)",
+        "qwen35": "Qwen3.5-397B-A17B-shaped BF16 MoE layer forward+backward (E=512, d=4096, I=1024, top-10)",
+        "dsv4pro": "DeepSeek-V4-Pro-shaped BF16 MoE layer forward+backward (E=384, d=7168, I=3072, top-6)",
     }[name]
     if tokens or experts:  # scaled-down variant (profiling captures)
         s = dataclasses.replace(s, T=tokens or s.T, E=experts or s.E)
@@ -266,7 +270,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="dsv3", choices=["dsv3", "qwen3", "tiny", "dsv3_mxfp8"])
+    ap.add_argument("--workload", default="dsv3",
+                    choices=["dsv3", "qwen3", "tiny", "dsv3_mxfp8", "kimi_k27", "glm52", "qwen35", "dsv4pro"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (scaled-down profiling runs)")
     ap.add_argument("--experts", type=int, default=0, help="override E (scaled-down profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -178,6 +178,8 @@ struct GemmParams {
   const int* tile_start;   // [G+1] prefix of 128-row tiles per group (grouped SCHED_ROWS)
   const int* pair_start;   // [G+1] prefix of floor(tiles / 2) per group (grouped SCHED_ROWS2)
   const int* rem_start;    // [G+1] prefix of groups with an odd tile count (grouped, part 1)
+  const int* pair_mode;    // grouped rows: device flag, 0 = no SM pairs (the 2-SM pass has no
+                           // work, the 1-SM pass with part 1 takes every tile); null = 1
   int part;                // 1-SM passes: 0 every tile; 1 only the last m-tile of groups
                            // (or dense row ranges, or weight gradients) with an odd
                            // number of m-tiles
@@ -257,6 +259,11 @@ __device__ __forceinline__ int find_group(const int* row_start, int G, int row) 
   return lo;
 }
 
+// Grouped rows: whether the routing chose SM pairs, and whether a 1-SM launch
+// with part 1 takes only the odd groups' last m-tiles (else every tile).
+__device__ __forceinline__ bool pairs_on(const GemmParams& p) { return !p.pair_mode || __ldg(p.pair_mode) != 0; }
+__device__ __forceinline__ bool leftover_only(const GemmParams& p) { return p.part && pairs_on(p); }
+
 // Work items per launch: tiles, or in the 2-SM mode pairs of tiles.
 template <int EPI, int SCH, int BN>
 __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
@@ -267,7 +274,8 @@ __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
       if (SCH == SCHED_ROWS2) return (mt / 2) * num_nt;
       return (p.part ? (mt & 1) : mt) * num_nt;
     }
-    const int* prefix = SCH == SCHED_ROWS2 ? p.pair_start : (p.part ? p.rem_start : p.tile_start);
+    if (SCH == SCHED_ROWS2 && !pairs_on(p)) return 0;
+    const int* prefix = SCH == SCHED_ROWS2 ? p.pair_start : (leftover_only(p) ? p.rem_start : p.tile_start);
     return __ldg(prefix + p.num_groups) * num_nt;
   } else {
     const int num_nt = (p.N + BN - 1) / BN;
@@ -326,7 +334,7 @@ __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau, uint
         const int local = tau - ps * num_nt;
         nt = local / np;
         mt = 2 * (local - nt * np) + r;
-      } else if (p.part) {
+      } else if (leftover_only(p)) {
         e = find_group(p.rem_start, G, tau / num_nt);
         nt = tau - __ldg(p.rem_start + e) * num_nt;
         mt = __ldg(p.tile_start + e + 1) - __ldg(p.tile_start + e) - 1;

@@ -15,6 +15,12 @@ benchmark; distributions are fixed here and restated in the design doc):
          distributions as dsv3 plus a per-expert router bias
          b_e = alpha * log(rank_e ** -1.2), rank_e a seeded permutation of 1..E
          (Zipf 1.2 skew, alpha fixed below so expert loads span roughly 10x)
+  kimi_k27, glm52, qwen35, dsv4pro
+         the open-weight model shapes the Mixture-of-Kittens blog benchmarks
+         (E, d, I, top-k): (384, 7168, 2048, 8), (256, 6144, 2048, 8),
+         (512, 4096, 1024, 10), (384, 7168, 3072, 6); the blog gives only those
+         four numbers, the rest is as dsv3 (T=16384, one shared expert of
+         width I, same distributions)
   sweep  dsv3 shapes at T in {512, 2048, 8192, 32768}; optional Zipf bias as
          qwen3; optionally 8 experts (ids E-8..E-1) get bias -inf so they
          receive no tokens
@@ -55,6 +61,10 @@ CONFIGS = {
     "tiny": MoEShape(T=512, d=256, I=128, E=8, k=2, n_shared=1, I_shared=128, w_std=0.02),
     "dsv3": MoEShape(T=16384, d=7168, I=2048, E=256, k=8, n_shared=1, I_shared=2048, w_std=0.006),
     "qwen3": MoEShape(T=8192, d=4096, I=1536, E=128, k=8, n_shared=0, I_shared=0, w_std=0.006, zipf=True),
+    "kimi_k27": MoEShape(T=16384, d=7168, I=2048, E=384, k=8, n_shared=1, I_shared=2048, w_std=0.006),
+    "glm52": MoEShape(T=16384, d=6144, I=2048, E=256, k=8, n_shared=1, I_shared=2048, w_std=0.006),
+    "qwen35": MoEShape(T=16384, d=4096, I=1024, E=512, k=10, n_shared=1, I_shared=1024, w_std=0.006),
+    "dsv4pro": MoEShape(T=16384, d=7168, I=3072, E=384, k=6, n_shared=1, I_shared=3072, w_std=0.006),
 }
 
 

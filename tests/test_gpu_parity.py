@@ -102,12 +102,16 @@ SHAPES = {
     # tile, dW_down three (one SM pair plus one tile on one SM)
     "small_T": MoEShape(T=64, d=384, I=128, E=8, k=2, n_shared=1, I_shared=128, w_std=0.05),
     "single_token": MoEShape(T=1, d=256, I=256, E=16, k=4, n_shared=1, I_shared=256, w_std=0.05),
+    # four of eight experts with an odd m-tile count in 44 tiles: the routing picks SM pairs,
+    # and the odd experts' last m-tiles go through the one-SM pass (the other shapes here run
+    # either without odd experts or, with many, every tile on one SM)
+    "pairs_leftover": MoEShape(T=2560, d=512, I=256, E=8, k=2, n_shared=1, I_shared=128, w_std=0.05),
 }
 
 
 # seeds chosen so that no token has a top-k boundary gap below 1e-4 (checked
 # below on the oracle's float64 logits)
-SEEDS = {"noshared": 2}
+SEEDS = {"noshared": 2, "pairs_leftover": 2}
 
 
 @pytest.mark.parametrize("name", list(SHAPES))
