@@ -16,8 +16,11 @@
 // "Overlapping computation and communication in MoE"; paper section 2.1).
 //
 // Two number formats:
-//   bf16   kind::f16 MMAs (128x256x16), K = 64 per pipeline stage, operands
-//          K-major or MN-major;
+//   bf16   kind::f16 MMAs, K = 64 per pipeline stage, operands K-major or
+//          MN-major: 128x256x16 on one SM (router projection; grouped GEMMs
+//          when the routing leaves many odd experts), or 256x256x16 on a pair
+//          of SMs (SCHED_ROWS2 / SCHED_WGRAD2, cta_group::2: each SM holds its
+//          128 rows of A and half of B) for every other bf16 GEMM;
 //   MXFP8  (MX = true; blog section "MXFP8 support") kind::mxf8f6f4 block-scaled
 //          MMAs (128x256x32) on E4M3 operands, both K-major, K = 128 per stage.
 //          Each stage also brings the E8M0 scales of its A and B tiles (one
@@ -25,9 +28,10 @@
 //          into a ring of TMEM columns next to the accumulator before issuing
 //          the stage's four MMAs.
 //
-// Roles per CTA (one CTA per SM, persistent over tiles; 256 threads):
+// Roles per CTA (one CTA per SM, persistent over tiles; 256 threads; in the
+// 2-SM modes clusters of two CTAs):
 //   warp 0      TMA producer (lane 0 issues the tile loads)
-//   warp 1      MMA issuer (lane 0)
+//   warp 1      MMA issuer (lane 0; in a pair, the even CTA's only)
 //   warp 2      TMEM allocator (512 columns)
 //   warps 4..7  epilogue: TMEM -> registers -> fused math -> swizzled smem
 //               staging -> TMA bulk stores (or direct stores)
@@ -36,9 +40,12 @@
 // Pipelines: smem stages (full/empty mbarriers) and accumulator buffers
 // (acc_full/acc_empty): two 256-column buffers in bf16 mode so the epilogue of
 // tile i overlaps the MMAs of tile i+1; one in MXFP8 mode, whose other TMEM
-// columns hold the scale ring and a stash for the epilogue.  Every wait is
-// bounded (see mbar_wait): a stuck pipeline records MOE_ERR_DEVICE_TIMEOUT in
-// the status word and the CTA exits cleanly.
+// columns hold the scale ring and a stash for the epilogue.  In a pair, the
+// even CTA's full barriers count both CTAs' loads, its MMA commits free the
+// stage and fill the accumulator in both CTAs, and both CTAs' epilogues
+// release the accumulator on the even CTA's barrier.  Every wait is bounded
+// (see mbar_wait): a stuck pipeline records MOE_ERR_DEVICE_TIMEOUT in the
+// status word and the CTA exits cleanly.
 #pragma once
 #include "mx_common.cuh"
 #include "ptx.cuh"
