@@ -421,6 +421,12 @@ moe_status run_routing(const Shape& s, const void* x, const void* W_router, cons
     p.ldo = s.E;
     p.bias = bias;
     p.status = status;
+    // Test hook for the device-side failure path: with MOE_DEBUG_STALL_ROUTER
+    // set, the router projection's first stage waits for 16 bytes that never
+    // come; its bounded waits run out (about 4 s each) and the launch records
+    // MOE_ERR_DEVICE_TIMEOUT instead of hanging.
+    if (const char* v = getenv("MOE_DEBUG_STALL_ROUTER"))
+      if (v[0] && v[0] != '0') p.debug_extra_tx = 16;
     MOE_LAUNCH(PL_ROUTER_GEMM, st, launch_gemm(GK_ROUTER, p, grid_for(cdiv(s.T, kBM) * cdiv(s.E, kBN)), st));
     lg = logits;
   }

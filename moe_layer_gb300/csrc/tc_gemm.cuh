@@ -235,6 +235,10 @@ struct GemmParams {
   uint8_t* qt2_sf;
   long long qt2_rb;
   int* status;
+  // Test hook (0 normally): bytes the first pipeline stage of each CTA's first
+  // tile expects beyond what its loads bring, so that its MMA warp's bounded
+  // wait runs out (one-SM mode only).
+  uint32_t debug_extra_tx;
 };
 
 template <int EPI>
@@ -509,7 +513,7 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
         }
         __syncwarp();
       } else {
-        if (lane == 0) mbar_arrive_expect_tx(full, kTx);
+        if (lane == 0) mbar_arrive_expect_tx(full, kTx + ((w == wr.first && kb == 0) ? p.debug_extra_tx : 0u));
         __syncwarp();
         // ---- A operand
         if constexpr (AM == A_K_TILE) {
@@ -558,9 +562,11 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
       }
     }
   }
-  if (aborted && lane == 0 && (!PAIR || wr.rank == 0)) {
+  if (lane == 0 && (!PAIR || wr.rank == 0)) {
     // Loads still in flight must land before the CTA's shared memory goes
-    // away (2-SM mode: the even CTA's barriers also count the odd CTA's).
+    // away (2-SM mode: the even CTA's barriers also count the odd CTA's).  In
+    // a run without faults these phases have completed already; after an
+    // abort (the MMA warp may never have waited for them) the wait is bounded.
 #pragma unroll
     for (int i = 0; i < ST; ++i)
       if (issued_parity[i] >= 0)
