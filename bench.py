@@ -60,7 +60,7 @@ def _tensor_peaks(peaks, mxfp8):
             peaks["src"] + f" bf16 x nominal mxfp8/bf16 ratio {FP8_OVER_BF16:g}")
 
 
-def _workload(name, tokens=0, experts=0):
+def _workload(name, tokens=0, experts=0, zipf=False, zero_experts=0):
     """(shape, description, mxfp8) of a named workload."""
     import dataclasses
 
@@ -77,9 +77,12 @@ def _workload(name, tokens=0, experts=0):
         "qwen35": "Qwen3.5-397B-A17B-shaped BF16 MoE layer forward+backward (E=512, d=4096, I=1024, top-10)",
         "dsv4pro": "DeepSeek-V4-Pro-shaped BF16 MoE layer forward+backward (E=384, d=7168, I=3072, top-6)",
     }[name]
-    if tokens or experts:  # scaled-down variant (profiling captures)
+    if tokens or experts:  # scaled variant (token sweep, profiling captures)
         s = dataclasses.replace(s, T=tokens or s.T, E=experts or s.E)
         desc += f" (scaled: T={s.T}, E={s.E})"
+    if zipf or zero_experts:  # the granularity sweep's skewed routing
+        s = dataclasses.replace(s, zipf=zipf or s.zipf, zero_experts=zero_experts)
+        desc += f" (Zipf {1.2 if s.zipf else 0} router bias, {zero_experts} experts never chosen)"
     return s, desc, name == "dsv3_mxfp8"
 
 
@@ -237,7 +240,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     from synth.inputs import make_inputs
-    s, desc, mx = _workload(args.workload, args.tokens, args.experts)
+    s, desc, mx = _workload(args.workload, args.tokens, args.experts, args.zipf, args.zero_experts)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = make_inputs(s, seed=0, device=dev)
     per_step = args.ref_tokens
@@ -280,6 +283,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per reference step")
     ap.add_argument("--cpu-mx", action="store_true",
                     help="also time the MXFP8 oracle for dsv3_mxfp8 (about 11 min per token)")
+    ap.add_argument("--zipf", action="store_true", help="Zipf(1.2)-skewed router bias (the sweep's skewed routing)")
+    ap.add_argument("--zero-experts", type=int, default=0, help="that many experts never chosen (bias -inf)")
     ap.add_argument("--replay", action="store_true",
                     help="MOE_FLAG_REPLAY: save only the routing, recompute x rows, a and b in the backward")
     args = ap.parse_args()
@@ -312,7 +317,7 @@ def main():
         return float(t.item())
 
     _abi.load()
-    s, desc, mx = _workload(args.workload, args.tokens, args.experts)
+    s, desc, mx = _workload(args.workload, args.tokens, args.experts, args.zipf, args.zero_experts)
     inp = make_inputs(s, seed=rank, device="cuda")
     cfg = _abi.make_config(s.T, s.d, s.I, s.E, s.k, s.n_shared, s.I_shared,
                            precision=_abi.MOE_MXFP8 if mx else _abi.MOE_BF16,

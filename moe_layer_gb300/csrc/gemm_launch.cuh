@@ -64,9 +64,12 @@ cudaError_t launch_rows_two_pass(const GemmParams& p, int grid, cudaStream_t st)
 }
 
 // Weight gradients likewise: pairs of m-tiles (weight rows) on SM pairs, and
-// the last m-tile on one SM when M_out / 128 is odd.
+// the last m-tile on one SM when M_out / 128 is odd; or all on one SM when
+// the host asks (wgrad_one_sm: short K, where a pair's two epilogues, which
+// its MMAs wait for, cost more than the halved shared-memory traffic saves).
 template <int AM, int BMO>
 cudaError_t launch_wgrad_two_pass(const GemmParams& p, int grid, cudaStream_t st) {
+  if (p.wgrad_one_sm) return launch_gemm_inst<AM, BMO, EPI_BF16, SCHED_WGRAD>(p, grid, st);
   const int num_mt = (p.M_out + kBM - 1) / kBM;
   if (num_mt >= 2) {
     const cudaError_t e = launch_gemm_inst<AM, BMO, EPI_BF16, SCHED_WGRAD2>(p, grid, st);

@@ -239,6 +239,9 @@ struct GemmParams {
   // tile expects beyond what its loads bring, so that its MMA warp's bounded
   // wait runs out (one-SM mode only).
   uint32_t debug_extra_tx;
+  // Weight gradients: run every tile on one SM (part 0) instead of pairs; set
+  // by the host when the experts' row ranges (the K of these GEMMs) are short
+  int wgrad_one_sm;
 };
 
 template <int EPI>
