@@ -114,8 +114,9 @@ typedef struct {
  *   saved   state moe_forward leaves for moe_backward (routing; the x rows, a
  *           and b unless MOE_FLAG_REPLAY)
  *   bwd_ws  scratch for moe_backward
- * Each buffer must be 256-byte aligned; its first 256 bytes hold the device
- * status word and must be zero before the buffer's first use. */
+ * Each buffer must be 256-byte aligned (moe_route_topk, moe_forward and
+ * moe_backward return MOE_ERR_INVALID_ARG otherwise); its first 256 bytes hold
+ * the device status word and must be zero before the buffer's first use. */
 moe_status moe_workspace_size(const moe_config* cfg, size_t* fwd_ws, size_t* saved, size_t* bwd_ws);
 
 /* MXFP8 mode (precision = MOE_MXFP8, d and I multiples of 128; blog section

@@ -296,6 +296,8 @@ void carve_mx(void* base, const Shape& s, MxWeights& m, size_t* bytes) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Workspaces and the saved state: their sub-buffers take 32-byte vector accesses.
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 
 moe_status check_config(const moe_config* cfg, Shape& s) {
   if (!cfg) return MOE_ERR_INVALID_ARG;
@@ -729,6 +731,7 @@ moe_status moe_route_topk(const moe_config* cfg, const void* x, const void* W_ro
   Shape s;
   MOE_TRY(check_config(cfg, s));
   if (!ws) return MOE_ERR_WORKSPACE;
+  if (!aligned256(ws)) return MOE_ERR_INVALID_ARG;
   if (s.T == 0) return MOE_OK;
   if (!topk_idx || !topk_w || !counts || !offsets || !perm_token || !route_row)
     return MOE_ERR_INVALID_ARG;
@@ -753,9 +756,10 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
   Shape s;
   MOE_TRY(check_config(cfg, s));
   if (!ws) return MOE_ERR_WORKSPACE;
+  if (!aligned256(ws)) return MOE_ERR_INVALID_ARG;
   if (s.T == 0) return MOE_OK;
   MOE_TRY(check_weights(s, wts, true));
-  if (!x || !y || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  if (!x || !y || !aligned16(x) || !aligned16(y) || !aligned256(saved)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   FwdWs w;
   carve_fwd(ws, s, w, nullptr);
@@ -821,9 +825,11 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
   Shape s;
   MOE_TRY(check_config(cfg, s));
   if (!ws) return MOE_ERR_WORKSPACE;
+  if (!aligned256(ws)) return MOE_ERR_INVALID_ARG;
   if (s.T == 0) return MOE_OK;
   MOE_TRY(check_weights(s, wts, true));
-  if (!x || !dy || !saved || !dx || !g || !aligned16(x) || !aligned16(dy) || !aligned16(dx))
+  if (!x || !dy || !saved || !dx || !g || !aligned16(x) || !aligned16(dy) || !aligned16(dx) ||
+      !aligned256(saved))
     return MOE_ERR_INVALID_ARG;
   if (!g->dW_router || !g->dW_gate || !g->dW_up || !g->dW_down) return MOE_ERR_INVALID_ARG;
   if (s.S && (!g->dWs_gate || !g->dWs_up || !g->dWs_down)) return MOE_ERR_INVALID_ARG;

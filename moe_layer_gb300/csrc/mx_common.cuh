@@ -4,6 +4,8 @@
 #pragma once
 #include <stdint.h>
 
+#include "ptx.cuh"
+
 namespace moe {
 
 // floor(log2(a)) for a > 0 (fp32, normal or subnormal).
@@ -50,8 +52,8 @@ __device__ __forceinline__ void quant32(const float* v, int e, uint4& lo, uint4&
   hi = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-// Quantizes 32 values in place of a row: writes the 32 codes to dst (16-byte
-// aligned) and returns the E8M0 code of their block.
+// Quantizes 32 values in place of a row: writes the 32 codes to dst (32-byte
+// aligned, one 256-bit store) and returns the E8M0 code of their block.
 __device__ __forceinline__ uint32_t quant32_store(const float* v, uint8_t* dst) {
   float amax = 0.f;
 #pragma unroll
@@ -59,8 +61,7 @@ __device__ __forceinline__ uint32_t quant32_store(const float* v, uint8_t* dst) 
   const int e = mx_scale_exp(amax);
   uint4 lo, hi;
   quant32(v, e, lo, hi);
-  reinterpret_cast<uint4*>(dst)[0] = lo;
-  reinterpret_cast<uint4*>(dst)[1] = hi;
+  st_global_v8(dst, lo, hi);
   return static_cast<uint32_t>(e + 127);
 }
 

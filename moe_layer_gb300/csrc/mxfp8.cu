@@ -74,7 +74,11 @@ __global__ void __launch_bounds__(kQThreads)
 //       experts); skipped when tq is null.
 // Block: one 128 x 128 tile (R and K multiples of 128), 256 threads; the bf16
 // tile sits in shared memory so that both quantizations read it along their
-// own axis.
+// own axis, both without bank conflicts: the row quantization gives the eight
+// threads of a quarter warp eight different rows (the 272-byte row pitch puts
+// them in different banks), the transposed one reads two adjacent columns per
+// 32-bit load.  Each thread's 32 output bytes of a block go out as one
+// 256-bit store (a whole 32-byte sector; rq, tq 32-byte aligned).
 constexpr int kDualTile = 128;
 constexpr int kDualPitch = kDualTile + 8;  // bf16 elements per shared row (16-byte aligned rows)
 constexpr int kDualBlocksPerSm = 3;
@@ -89,9 +93,26 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// Quantizes one column of 32 rows held two columns per word (hi: the upper
+// bf16 of each word) with scale 2^e into 32 E4M3 bytes.
+__device__ __forceinline__ void quant32_col(const uint32_t* w, bool hi, int e, uint4& q0, uint4& q1) {
+  const float inv = mx_inv_scale(e);
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = (hi ? bf16hi(w[4 * i + j]) : bf16lo(w[4 * i + j])) * inv;
+    o[i] = e4m3x2(v[0], v[1]) | (e4m3x2(v[2], v[3]) << 16);
+  }
+  q0 = make_uint4(o[0], o[1], o[2], o[3]);
+  q1 = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 // Persistent: each block walks tiles blockIdx.x, + gridDim.x, ...; the gather
 // of the next tile is in flight (cp.async, double-buffered) while the current
-// one is quantized.
+// one is quantized, and the source row indices of the tile after it are
+// loaded meanwhile.
 __global__ void __launch_bounds__(kQThreads, kDualBlocksPerSm)
     mx_permute_dual_kernel(const __nv_bfloat16* __restrict__ src, long long src_ld,
                            const int32_t* __restrict__ idx, const int32_t* __restrict__ total_rows,
@@ -100,39 +121,53 @@ __global__ void __launch_bounds__(kQThreads, kDualBlocksPerSm)
   extern __shared__ __align__(16) uint8_t dual_smem[];
   typedef uint16_t Tile[kDualTile][kDualPitch];
   Tile* tiles = reinterpret_cast<Tile*>(dual_smem);  // two buffers
-  // E8M0 words of the tile: [0] per row (4 column blocks), [1] per column (4 row blocks)
-  uint32_t(*sfw)[kDualTile] = reinterpret_cast<uint32_t(*)[kDualTile]>(dual_smem + 2 * sizeof(Tile));
+  // E8M0 words of the tile, double-buffered: [buf][0] per row (4 column
+  // blocks), [buf][1] per column (4 row blocks)
+  typedef uint32_t ScaleWords[2][kDualTile];
+  ScaleWords* sfw = reinterpret_cast<ScaleWords*>(dual_smem + 2 * sizeof(Tile));
   const int ncol = K / kDualTile;
   const int64_t used = total_rows ? static_cast<int64_t>(__ldg(total_rows)) : R;
   const int64_t ntiles = ((used + kDualTile - 1) / kDualTile) * ncol;  // only row tiles that hold used rows
-  auto gather = [&](int64_t tau, Tile& t) {  // 16 threads per row, 16 bytes each
+  // gather: thread -> rows (tid / 16) + 16 k, 16 bytes at column 8 (tid % 16)
+  const int grow = threadIdx.x >> 4, gq = threadIdx.x & 15;
+  auto load_rows = [&](int64_t tau, int32_t (&ix)[8]) {
     const int64_t r0 = (tau / ncol) * kDualTile;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      ix[k] = idx ? __ldg(idx + r0 + grow + 16 * k) : static_cast<int32_t>(r0 + grow + 16 * k);
+  };
+  auto gather = [&](int64_t tau, const int32_t (&ix)[8], Tile& t) {
     const int c0 = static_cast<int>(tau % ncol) * kDualTile;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int i = threadIdx.x + kQThreads * k, r = i >> 4, q = i & 15;
-      const int64_t srow = idx ? static_cast<int64_t>(__ldg(idx + r0 + r)) : r0 + r;
-      const __nv_bfloat16* g = src + (srow >= 0 ? srow : 0) * src_ld + c0 + 8 * q;
-      cp_async16(&t[r][8 * q], g, srow >= 0 ? 16 : 0);
+      const int64_t srow = ix[k];
+      const __nv_bfloat16* g = src + (srow >= 0 ? srow : 0) * src_ld + c0 + 8 * gq;
+      cp_async16(&t[grow + 16 * k][8 * gq], g, srow >= 0 ? 16 : 0);
     }
     cp_async_commit();
   };
+  int32_t ix[8];
   int buf = 0;
-  if (static_cast<int64_t>(blockIdx.x) < ntiles) gather(blockIdx.x, tiles[0]);
+  if (static_cast<int64_t>(blockIdx.x) < ntiles) {
+    load_rows(blockIdx.x, ix);
+    gather(blockIdx.x, ix, tiles[0]);
+    if (static_cast<int64_t>(blockIdx.x) + gridDim.x < ntiles) load_rows(blockIdx.x + gridDim.x, ix);
+  }
   for (int64_t tau = blockIdx.x; tau < ntiles; tau += gridDim.x) {
     const int64_t next = tau + gridDim.x;
     if (next < ntiles) {
-      gather(next, tiles[buf ^ 1]);
+      gather(next, ix, tiles[buf ^ 1]);
+      if (next + gridDim.x < ntiles) load_rows(next + gridDim.x, ix);
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
-    __syncthreads();
+    __syncthreads();  // tile `buf` is in shared memory
     const Tile& tile = tiles[buf];
     const int64_t r0 = (tau / ncol) * kDualTile;
     const int c0 = static_cast<int>(tau % ncol) * kDualTile;
     {  // along the row: thread -> (row, 64-column half), two blocks of 32
-      const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
+      const int r = (threadIdx.x & 7) + 8 * (threadIdx.x >> 4), half = (threadIdx.x >> 3) & 1;
       uint32_t word = 0;
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
@@ -152,42 +187,50 @@ __global__ void __launch_bounds__(kQThreads, kDualBlocksPerSm)
         const int e = mx_scale_exp(amax);
         uint4 lo, hi;
         quant32(v, e, lo, hi);
-        uint4* d4 = reinterpret_cast<uint4*>(rq + (r0 + r) * K + c0 + 64 * half + 32 * b);
-        d4[0] = lo;
-        d4[1] = hi;
+        st_global_v8(rq + (r0 + r) * K + c0 + 64 * half + 32 * b, lo, hi);
         word |= static_cast<uint32_t>(e + 127) << (8 * (2 * half + b));
       }
-      word |= __shfl_xor_sync(0xffffffffu, word, 1);
-      if (half == 0) sfw[0][r] = word;
+      word |= __shfl_xor_sync(0xffffffffu, word, 8);  // the row's other half
+      if (half == 0) sfw[buf][0][r] = word;
     }
-    if (tq) {  // along the rows: thread -> (column, two 32-row blocks), 32 codes of the transpose's row each
-      const int c = threadIdx.x & 127, tb0 = 2 * (threadIdx.x >> 7);
+    if (tq) {  // along the rows: thread -> (column pair, 32-row block)
+      const int cp = threadIdx.x & 63, tb = threadIdx.x >> 6;
+      uint32_t w[32];
+      __nv_bfloat162 m2 = __floats2bfloat162_rn(0.f, 0.f);
 #pragma unroll
-      for (int tb = tb0; tb < tb0 + 2; ++tb) {
-        float v[32];
+      for (int i = 0; i < 32; ++i) {
+        w[i] = *reinterpret_cast<const uint32_t*>(&tile[32 * tb + i][2 * cp]);
+        m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[i])));
+      }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(static_cast<uint32_t>(tile[32 * tb + i][c]) << 16);
-        const uint32_t code = quant32_store(v, tq + static_cast<int64_t>(c0 + c) * R + r0 + 32 * tb);
-        reinterpret_cast<uint8_t*>(sfw[1])[4 * c + tb] = static_cast<uint8_t>(code);
+      for (int h = 0; h < 2; ++h) {
+        const int e = mx_scale_exp(h ? __high2float(m2) : __low2float(m2));
+        uint4 q0, q1;
+        quant32_col(w, h != 0, e, q0, q1);
+        st_global_v8(tq + static_cast<int64_t>(c0 + 2 * cp + h) * R + r0 + 32 * tb, q0, q1);
+        reinterpret_cast<uint8_t*>(sfw[buf][1])[4 * (2 * cp + h) + tb] = static_cast<uint8_t>(e + 127);
       }
     }
-    __syncthreads();
+    __syncthreads();  // scale words complete; tile `buf` no longer read
     // Each tile's scales are one whole 512-byte block per copy: bytes 16 t .. 16 t + 15
-    // hold the words of rows (columns) t, t + 32, t + 64, t + 96.
+    // hold the words of rows (columns) t, t + 32, t + 64, t + 96.  The next
+    // iteration writes the other scale buffer, and the one after that passes
+    // the next iteration's second barrier first.
     if (threadIdx.x < 32) {
       const int t = threadIdx.x;
+      const uint32_t* sw = sfw[buf][0];
       uint8_t* blk = rq_sf + ((c0 / 128) * ((R + 127) / 128) + r0 / 128) * 512;
-      *reinterpret_cast<uint4*>(blk + 16 * t) = make_uint4(sfw[0][t], sfw[0][t + 32], sfw[0][t + 64], sfw[0][t + 96]);
+      *reinterpret_cast<uint4*>(blk + 16 * t) = make_uint4(sw[t], sw[t + 32], sw[t + 64], sw[t + 96]);
     } else if (tq && threadIdx.x < 64) {
       const int t = threadIdx.x - 32;
+      const uint32_t* sw = sfw[buf][1];
       uint8_t* blk = tq_sf + ((r0 / 128) * (K / 128) + c0 / 128) * 512;
-      *reinterpret_cast<uint4*>(blk + 16 * t) = make_uint4(sfw[1][t], sfw[1][t + 32], sfw[1][t + 64], sfw[1][t + 96]);
+      *reinterpret_cast<uint4*>(blk + 16 * t) = make_uint4(sw[t], sw[t + 32], sw[t + 64], sw[t + 96]);
     }
-    __syncthreads();  // sfw and this tile's buffer are free again
     buf ^= 1;
   }
 }
-constexpr int kDualSmemBytes = 2 * kDualTile * kDualPitch * 2 + 2 * kDualTile * 4;
+constexpr int kDualSmemBytes = 2 * kDualTile * kDualPitch * 2 + 2 * 2 * kDualTile * 4;
 
 // Transposing quantization: src is [rows, cols] (row pitch src_ld) and feeds
 // a GEMM whose reduction axis is `rows`.  Writes dst[c, k_off + r] (row pitch

@@ -445,7 +445,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Stores 16 floats as 16 bf16 (32 bytes, 16-byte aligned destination).
+// 32 bytes to or from global memory in one 256-bit access (32-byte aligned
+// address).  When the lanes of a warp each write a different row, a pair of
+// 16-byte stores leaves every 32-byte sector half written in between, for the
+// L2 to merge; one 256-bit store writes whole sectors.
+__device__ __forceinline__ void st_global_v8(void* p, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+__device__ __forceinline__ void ld_global_v8(const void* p, uint4& a, uint4& b) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+               : "l"(p)
+               : "memory");
+}
+
+// Stores 16 floats as 16 bf16 (32 bytes, 32-byte aligned destination).
 __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float (&v)[16]) {
   uint4 a, b;
   a.x = pack_bf16x2(v[0], v[1]);
@@ -456,12 +472,12 @@ __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float (&
   b.y = pack_bf16x2(v[10], v[11]);
   b.z = pack_bf16x2(v[12], v[13]);
   b.w = pack_bf16x2(v[14], v[15]);
-  reinterpret_cast<uint4*>(dst)[0] = a;
-  reinterpret_cast<uint4*>(dst)[1] = b;
+  st_global_v8(dst, a, b);
 }
+// Loads 16 bf16 as 16 floats (32 bytes, 32-byte aligned source).
 __device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* src, float (&v)[16]) {
-  const uint4 a = reinterpret_cast<const uint4*>(src)[0];
-  const uint4 b = reinterpret_cast<const uint4*>(src)[1];
+  uint4 a, b;
+  ld_global_v8(src, a, b);
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {

@@ -100,6 +100,24 @@ def test_null_arguments_rejected_before_launch(lib):
     assert lib.moe_forward(ctypes.byref(c), None, ctypes.byref(w), None, None, 256, None) == 1
 
 
+def test_misaligned_workspace_or_saved_state_rejected(lib):
+    """moe.h: the workspaces and the saved state are 256-byte aligned (their
+    sub-buffers take 32-byte vector accesses); a misaligned one is an invalid
+    argument, rejected before anything is launched (the placeholder addresses
+    are never dereferenced)."""
+    c = _abi.make_config(64, 128, 64, 4, 2)
+    fake = 1 << 20
+    w = _abi.MoeWeights(fake, 0, fake, fake, fake, 0, 0, 0, None)
+    assert lib.moe_forward(ctypes.byref(c), fake, ctypes.byref(w), fake, None, fake + 16, None) == 1
+    assert lib.moe_forward(ctypes.byref(c), fake, ctypes.byref(w), fake, fake + 32, fake, None) == 1
+    i32 = ctypes.c_void_p(fake)
+    assert lib.moe_route_topk(ctypes.byref(c), fake, fake, None, None, None, i32, i32, i32, i32, i32, i32,
+                              fake + 128, None) == 1
+    g = _abi.MoeGrads(fake, fake, fake, fake, 0, 0, 0, None, None)
+    assert lib.moe_backward(ctypes.byref(c), fake, ctypes.byref(w), fake, fake + 64, fake, ctypes.byref(g),
+                            fake, None) == 1
+
+
 def test_empty_batch_is_a_no_op(lib):
     c = _abi.make_config(0, 128, 64, 4, 2)
     w = _abi.MoeWeights()
