@@ -17,6 +17,7 @@ cudaError_t launch_gemm_inst(const GemmParams& p, int grid, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   auto kfn = tc_gemm_kernel<AM, BMO, EPI, SCH, MX>;
   constexpr int smem = gemm_smem_bytes_for<MX, EPI, SCH>();
+  static_assert(smem <= 227 * 1024, "shared memory of one CTA");
   constexpr int threads = gemm_threads<MX, EPI, SCH>();
   const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
   if (bit == 0 || !(configured.load() & bit)) {
@@ -65,11 +66,13 @@ cudaError_t launch_rows_two_pass(const GemmParams& p, int grid, cudaStream_t st)
 
 // Weight gradients likewise: pairs of m-tiles (weight rows) on SM pairs, and
 // the last m-tile on one SM when M_out / 128 is odd; or all on one SM when
-// the host asks (wgrad_one_sm: short K, where a pair's two epilogues, which
-// its MMAs wait for, cost more than the halved shared-memory traffic saves).
+// the host asks (wgrad_mode 1: short K, where a pair's two epilogues, which
+// its MMAs wait for, cost more than the halved shared-memory traffic saves;
+// wgrad_mode 2: the shortest K, with twice the epilogue warps).
 template <int AM, int BMO>
 cudaError_t launch_wgrad_two_pass(const GemmParams& p, int grid, cudaStream_t st) {
-  if (p.wgrad_one_sm) return launch_gemm_inst<AM, BMO, EPI_BF16, SCHED_WGRAD>(p, grid, st);
+  if (p.wgrad_mode == 2) return launch_gemm_inst<AM, BMO, EPI_BF16, SCHED_WGRAD_WIDE>(p, grid, st);
+  if (p.wgrad_mode == 1) return launch_gemm_inst<AM, BMO, EPI_BF16, SCHED_WGRAD>(p, grid, st);
   const int num_mt = (p.M_out + kBM - 1) / kBM;
   if (num_mt >= 2) {
     const cudaError_t e = launch_gemm_inst<AM, BMO, EPI_BF16, SCHED_WGRAD2>(p, grid, st);

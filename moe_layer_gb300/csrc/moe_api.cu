@@ -409,8 +409,10 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // The routed weight gradients reduce over each expert's rows: with fewer than
 // 384 per expert on average they run on one SM per tile rather than on SM
 // pairs (measured at the DSV3 shape: 16 rows, pairs 1.70 ms against 1.45 on
-// one SM per gradient; 512 rows, pairs 2.97 against 3.36 ms).
-bool wgrad_one_sm(const Shape& s) { return s.R < 384 * s.E; }
+// one SM per gradient; 512 rows, pairs 2.97 against 3.36 ms), and with fewer
+// than 128 with eight epilogue warps (64 rows: 1.45-1.53 -> 1.27-1.29 ms per
+// gradient; 256 rows: 2.02-2.08 -> 2.39-2.63 ms, so not there).
+int wgrad_mode(const Shape& s) { return s.R < 128 * s.E ? 2 : (s.R < 384 * s.E ? 1 : 0); }
 
 // ---------------------------------------------------------------- routing
 moe_status run_routing(const Shape& s, const void* x, const void* W_router, const float* bias,
@@ -1023,7 +1025,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.row_start = rt.row_start;
     p.M_out = d;
     p.N = I;
-    p.wgrad_one_sm = wgrad_one_sm(s);
+    p.wgrad_mode = wgrad_mode(s);
     MOE_TRY(omap3(&p.tmO0, g->dW_down, s.E, s.d, s.I));
     p.status = w.status;
     MOE_LAUNCH(PL_WGRAD_DOWN, st, launch_gemm(GK_WGRAD, p, grid_for(s.E * cdiv(s.d, kBM) * cdiv(s.I, kBN)), st));
@@ -1037,7 +1039,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.row_start = rt.row_start;
     p.M_out = I;
     p.N = d;
-    p.wgrad_one_sm = wgrad_one_sm(s);
+    p.wgrad_mode = wgrad_mode(s);
     p.a_col_off = half ? I : 0;
     MOE_TRY(omap3(&p.tmO0, half ? g->dW_up : g->dW_gate, s.E, s.I, s.d));
     p.status = w.status;

@@ -35,8 +35,8 @@
 //   warp 2      TMEM allocator (512 columns)
 //   warps 4..7  epilogue: TMEM -> registers -> fused math -> swizzled smem
 //               staging -> TMA bulk stores (or direct stores)
-// The MXFP8 SwiGLU backward runs 320 threads with epilogue warps 2..9, two per
-// TMEM lane quadrant (see epi_wide).
+// The MXFP8 SwiGLU backward and SCHED_WGRAD_WIDE run 320 threads with
+// epilogue warps 2..9, two per TMEM lane quadrant (see epi_wide).
 // Pipelines: smem stages (full/empty mbarriers) and accumulator buffers
 // (acc_full/acc_empty): two 256-column buffers in bf16 mode so the epilogue of
 // tile i overlaps the MMAs of tile i+1; one in MXFP8 mode, whose other TMEM
@@ -58,8 +58,12 @@ enum EpiMode : int { EPI_F32_BIAS = 0, EPI_SWIGLU_FWD = 1, EPI_BF16 = 2, EPI_SWI
 // SCHED_ROWS2 / SCHED_WGRAD2: the same tiles in pairs of m-tiles on one
 // n-tile, each pair computed by a cluster of two CTAs with cta_group::2 MMAs
 // (M = 256).
-enum SchedMode : int { SCHED_ROWS = 0, SCHED_WGRAD = 1, SCHED_ROWS2 = 2, SCHED_WGRAD2 = 3 };
-__host__ __device__ constexpr bool sched_wgrad(int sch) { return sch == SCHED_WGRAD || sch == SCHED_WGRAD2; }
+// SCHED_WGRAD_WIDE: weight gradients on one SM with eight epilogue warps (see
+// epi_wide), for the shortest K loops.
+enum SchedMode : int { SCHED_ROWS = 0, SCHED_WGRAD = 1, SCHED_ROWS2 = 2, SCHED_WGRAD2 = 3, SCHED_WGRAD_WIDE = 4 };
+__host__ __device__ constexpr bool sched_wgrad(int sch) {
+  return sch == SCHED_WGRAD || sch == SCHED_WGRAD2 || sch == SCHED_WGRAD_WIDE;
+}
 __host__ __device__ constexpr bool sched_pair(int sch) { return sch == SCHED_ROWS2 || sch == SCHED_WGRAD2; }
 
 constexpr int kBM = 128;  // rows per tile (TMEM lanes)
@@ -96,13 +100,15 @@ __host__ __device__ constexpr int stage_bytes() {
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int sf_stage_bytes() { return MX ? 512 + gemm_bn<MX, EPI, SCH>() / 128 * 512 : 0; }
 
-// Epilogue warps.  One per TMEM lane quadrant (warps 4-7), except for the
-// MXFP8 SwiGLU backward, whose heavy epilogue would be slower than the MMAs
-// with one: it gets two per quadrant (warps 2-9, 320 threads; the TMEM
+// Epilogue warps.  One per TMEM lane quadrant (warps 4-7), except where the
+// epilogue would be slower than the MMAs with one: the MXFP8 SwiGLU backward
+// (heavy arithmetic) and the bf16 weight gradients of experts with very few
+// rows (SCHED_WGRAD_WIDE: a 128 x 256 tile to store after a K loop of a few
+// MMAs).  Those get two per quadrant (warps 2-9, 320 threads; the TMEM
 // allocator, warp 2, is one of them), each taking half of the columns.
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr bool epi_wide() {
-  return MX && EPI == EPI_SWIGLU_BWD;
+  return (MX && EPI == EPI_SWIGLU_BWD) || (!MX && EPI == EPI_BF16 && SCH == SCHED_WGRAD_WIDE);
 }
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int epi_warps() { return epi_wide<MX, EPI, SCH>() ? 8 : 4; }
@@ -113,10 +119,13 @@ __host__ __device__ constexpr int gemm_threads() {
   return 32 * (first_epi_warp<MX, EPI, SCH>() + epi_warps<MX, EPI, SCH>());
 }
 // Pipeline stages: four 48 KB stages, six 32 KB ones in the 2-SM mode, five
-// 32 KB ones with 128-column tiles.  (Three stages with four staging boxes
-// per warp were measured for the weight gradients: slower than four stages.)
+// 32 KB ones with 128-column tiles, three 48 KB ones in SCHED_WGRAD_WIDE,
+// whose eight epilogue warps take 64 KB of staging (with K loops of a few
+// MMAs per tile, deeper rings buy nothing there; with longer ones the fourth
+// stage is worth more than the wide epilogue).
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int gemm_stages() {
+  if (!MX && epi_wide<MX, EPI, SCH>()) return 3;
   return sched_pair(SCH) ? 6 : (gemm_bn<MX, EPI, SCH>() == kBN ? kStages : 5);
 }
 // MXFP8 kernels with a single accumulator run the stash epilogue; the ones
@@ -130,7 +139,7 @@ __host__ __device__ constexpr bool epi_mx_stash() { return MX && acc_bufs<MX, EP
 // the 32 x 17 fp32 transpose buffer.
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int epi_slots() {
-  return (!epi_mx_stash<MX, EPI, SCH>() && !epi_wide<MX, EPI, SCH>()) ? 2 : 1;
+  return (!epi_mx_stash<MX, EPI, SCH>() && !(MX && epi_wide<MX, EPI, SCH>())) ? 2 : 1;
 }
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int epi_warp_bytes() {
@@ -239,9 +248,11 @@ struct GemmParams {
   // tile expects beyond what its loads bring, so that its MMA warp's bounded
   // wait runs out (one-SM mode only).
   uint32_t debug_extra_tx;
-  // Weight gradients: run every tile on one SM (part 0) instead of pairs; set
-  // by the host when the experts' row ranges (the K of these GEMMs) are short
-  int wgrad_one_sm;
+  // Weight gradients, chosen by the host from the experts' row ranges (the K
+  // of these GEMMs): 0 pairs of m-tiles on SM pairs (and the last m-tile on
+  // one SM), 1 every tile on one SM (short K), 2 every tile on one SM with
+  // the wide epilogue (the shortest K).
+  int wgrad_mode;
 };
 
 template <int EPI>
