@@ -23,11 +23,16 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-// Softmax + top-k for the tokens of one chunk (kWarpTokens tokens per warp).
+// Softmax + top-k for the tokens of one chunk (kTopkWarpTokens tokens per
+// warp: the selection is a chain of dependent shuffles, so the kernel is
+// latency bound and wants many warps per SM).
 // Selection: logits descending, equal logits to the lower expert index.
 // Weights: exp(l_j - l_max) / sum over the k selected (softmax over all E
 // logits restricted to the selection and renormalized).
-__global__ void __launch_bounds__(kChunkWarps * 32)
+constexpr int kTopkWarps = 16;
+constexpr int kTopkWarpTokens = kChunkTokens / kTopkWarps;
+static_assert(kChunkTokens % kTopkWarps == 0, "whole tokens per warp");
+__global__ void __launch_bounds__(kTopkWarps * 32)
     topk_count_kernel(const float* __restrict__ logits, int T, int E, int k,
                       int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                       int32_t* __restrict__ chunk_counts, int* status) {
@@ -36,8 +41,8 @@ __global__ void __launch_bounds__(kChunkWarps * 32)
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nS = (E + 31) >> 5;
-  const int t0 = blockIdx.x * kChunkTokens + warp * kWarpTokens;
-  for (int i = 0; i < kWarpTokens; ++i) {
+  const int t0 = blockIdx.x * kChunkTokens + warp * kTopkWarpTokens;
+  for (int i = 0; i < kTopkWarpTokens; ++i) {
     const int t = t0 + i;
     if (t >= T) break;
     const float* lr = logits + static_cast<size_t>(t) * E;
@@ -296,8 +301,8 @@ __global__ void __launch_bounds__(kChunkWarps * 32)
 cudaError_t launch_topk_count(const float* logits, int T, int E, int k, int32_t* topk_idx,
                               float* topk_w, int32_t* chunk_counts, int* status, cudaStream_t st) {
   const int nchunk = (T + kChunkTokens - 1) / kChunkTokens;
-  topk_count_kernel<<<nchunk, kChunkWarps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w,
-                                                         chunk_counts, status);
+  topk_count_kernel<<<nchunk, kTopkWarps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w,
+                                                        chunk_counts, status);
   return cudaGetLastError();
 }
 
