@@ -113,7 +113,7 @@ def _kernel_flops(name, s):
 # must be removed or re-measured when its kernel changes.
 NCU_TRAFFIC = {
     # the 2-SM pass and the pass over odd experts' last m-tiles, summed
-    ("dsv3", "gateup_routed"): 18.550e9 + 1.597e9 + 7.651e9 + 0.101e9,
+    ("dsv3", "gateup_routed"): 17.939e9 + 1.596e9 + 7.656e9 + 0.101e9,
     ("dsv3_mxfp8", "gateup_routed"): 9.005e9 + 1.499e9,
 }
 
