@@ -634,7 +634,7 @@ moe_status forward_gateup(const Shape& s, const void* x, const moe_weights* wts,
 // as K-major block-scaled GEMMs over [row_start[e], row_start[e+1]).
 moe_status wgrad_routed_mx(const Shape& s, const Routing& rt, const Acts& act, const BwdWs& w,
                            const moe_grads* g, cudaStream_t st) {
-  constexpr int kWgradBnMx = gemm_bn<true, EPI_BF16, SCHED_WGRAD>();  // 128-column tiles
+  constexpr int kWgradBnMx = gemm_bn<true, EPI_BF16, SCHED_WGRAD>();  // output tile width
   const int d = static_cast<int>(s.d), I = static_cast<int>(s.I), E = static_cast<int>(s.E);
   {
     GemmParams p;  // dW_down[e] = dy_rows^T . (g h)

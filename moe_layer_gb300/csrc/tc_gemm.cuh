@@ -118,8 +118,9 @@ template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int gemm_threads() {
   return 32 * (first_epi_warp<MX, EPI, SCH>() + epi_warps<MX, EPI, SCH>());
 }
-// Pipeline stages: four 48 KB stages, six 32 KB ones in the 2-SM mode, five
-// 32 KB ones with 128-column tiles, three 48 KB ones in SCHED_WGRAD_WIDE,
+// Pipeline stages: four 48 KB stages, six 32 KB ones in the 2-SM mode (five
+// 32 KB ones with 128-column tiles, which no instantiation uses), three 48 KB
+// ones in SCHED_WGRAD_WIDE,
 // whose eight epilogue warps take 64 KB of staging (with K loops of a few
 // MMAs per tile, deeper rings buy nothing there; with longer ones the fourth
 // stage is worth more than the wide epilogue).
@@ -128,8 +129,9 @@ __host__ __device__ constexpr int gemm_stages() {
   if (!MX && epi_wide<MX, EPI, SCH>()) return 3;
   return sched_pair(SCH) ? 6 : (gemm_bn<MX, EPI, SCH>() == kBN ? kStages : 5);
 }
-// MXFP8 kernels with a single accumulator run the stash epilogue; the ones
-// with two (the weight gradients) run the bf16-mode epilogue.
+// MXFP8 kernels, with a single 256-column accumulator beside the scale ring,
+// run the stash epilogue (with 128-column tiles and two accumulators they
+// would run the bf16-mode one).
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr bool epi_mx_stash() { return MX && acc_bufs<MX, EPI, SCH>() == 1; }
 // Epilogue shared memory per epilogue warp: 4 KB staging boxes that TMA
@@ -753,8 +755,8 @@ struct EpiStager {
   }
 };
 
-// Epilogue with two accumulator buffers: every bf16-mode GEMM, and the MXFP8
-// weight gradients (whose output is bf16 as well; 128-column tiles).
+// Epilogue with two accumulator buffers: every bf16-mode GEMM (and MXFP8 ones
+// with 128-column tiles, whose output is bf16 as well; no instantiation).
 template <int EPI, int SCH, bool MX>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf0, uint32_t acce0,
                                               uint32_t tmem_base, uint32_t s_warp, const WorkRange& wr,
