@@ -17,8 +17,6 @@
 
 namespace moe {
 
-int gemm_smem_bytes() { return kGemmSmemBytes; }
-
 int device_sm_count() {
   static std::atomic<int> cache[64];
   int dev = 0;

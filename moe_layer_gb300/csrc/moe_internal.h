@@ -100,7 +100,6 @@ cudaError_t launch_gemm(GemmKind kind, const GemmParams& p, int grid, cudaStream
 // thread (a launch helper that issues several adds to it; the per-kernel
 // timing resets and reads it around each call).
 int& extra_kernel_launches();
-int gemm_smem_bytes();
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

@@ -155,7 +155,6 @@ __host__ __device__ constexpr int gemm_smem_bytes_for() {
   return 1024 + gemm_stages<MX, EPI, SCH>() * (stage_bytes<MX, EPI, SCH>() + sf_stage_bytes<MX, EPI, SCH>()) +
          epi_warps<MX, EPI, SCH>() * epi_warp_bytes<MX, EPI, SCH>() + 256;
 }
-constexpr int kGemmSmemBytes = gemm_smem_bytes_for<false, 0, 0>();
 
 // The bf16 GEMMs other than the router projection run as two launches: a
 // 2-SM pass (SCHED_ROWS2, SCHED_WGRAD2) over pairs of m-tiles, and a 1-SM
