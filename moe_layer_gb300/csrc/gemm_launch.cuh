@@ -46,10 +46,10 @@ cudaError_t launch_gemm_inst(const GemmParams& p, int grid, cudaStream_t st) {
 }
 
 // The bf16 row GEMMs other than the router projection: a 2-SM pass over the
-// pairs of m-tiles, then a 1-SM pass over the last m-tile of every group
-// (or dense row range) with an odd number of them.  Grouped problems launch
-// the second pass always (their tile counts live on the device; with no odd
-// group its CTAs exit at once).
+// pairs of m-tiles, then a 1-SM pass over the rest: every tile of each expert
+// with an odd number of them (grouped rows), or the last m-tile of an odd
+// dense row range.  Grouped problems launch both passes always (their tile
+// counts live on the device; a pass without tiles exits at once).
 template <int AM, int BMO, int EPI>
 cudaError_t launch_rows_two_pass(const GemmParams& p, int grid, cudaStream_t st) {
   const int dense_mt = p.dense_rows > 0 ? (p.dense_rows + kBM - 1) / kBM : 0;

@@ -124,9 +124,8 @@ struct Routing {
   int32_t* offsets;
   int32_t* row_start;
   int32_t* tile_start;
-  int32_t* pair_start;  // prefix of floor(tiles / 2) per expert
-  int32_t* rem_start;   // prefix of experts with an odd tile count
-  int32_t* pair_mode;   // 1: grouped GEMMs on SM pairs + a pass for odd experts; 0: all on one SM
+  int32_t* pair_start;  // prefix of the tile pairs per expert (run on SM pairs)
+  int32_t* rem_start;   // prefix of the tiles per expert that run on one SM
   int32_t* perm_token;
   int32_t* route_row;
   int32_t* perm_token_pad;
@@ -143,7 +142,6 @@ void carve_routing(Carver& c, const Shape& s, Routing& r) {
   r.tile_start = c.take<int32_t>(s.E + 1);
   r.pair_start = c.take<int32_t>(s.E + 1);
   r.rem_start = c.take<int32_t>(s.E + 1);
-  r.pair_mode = c.take<int32_t>(1);
   r.perm_token = c.take<int32_t>(s.R);
   r.route_row = c.take<int32_t>(s.T * s.k);
   r.perm_token_pad = c.take<int32_t>(s.Rp);
@@ -444,7 +442,7 @@ moe_status run_routing(const Shape& s, const void* x, const void* W_router, cons
                              chunk_base, rt.counts, st));
   MOE_LAUNCH(PL_SCATTER, st, launch_scatter(rt.topk_idx, rt.topk_w, static_cast<int>(s.T), static_cast<int>(s.E),
                           static_cast<int>(s.k), static_cast<int>(s.ra), chunk_base, rt.counts, rt.offsets, rt.row_start,
-                          rt.tile_start, rt.pair_start, rt.rem_start, rt.pair_mode, rt.perm_token, rt.route_row, rt.perm_token_pad,
+                          rt.tile_start, rt.pair_start, rt.rem_start, rt.perm_token, rt.route_row, rt.perm_token_pad,
                           rt.route_row_pad, rt.perm_w_pad, st));
   return MOE_OK;
 }
@@ -494,7 +492,6 @@ moe_status gateup_routed_mx(const Shape& s, const moe_weights* wts, const Routin
   p.tile_start = rt.tile_start;
   p.pair_start = rt.pair_start;
   p.rem_start = rt.rem_start;
-  p.pair_mode = rt.pair_mode;
   p.counts = rt.counts;
   p.N = static_cast<int>(s.I);
   p.K = static_cast<int>(s.d);
@@ -530,7 +527,6 @@ moe_status down_routed_mx(const Shape& s, const moe_weights* wts, const Routing&
   p.tile_start = rt.tile_start;
   p.pair_start = rt.pair_start;
   p.rem_start = rt.rem_start;
-  p.pair_mode = rt.pair_mode;
   p.counts = rt.counts;
   p.N = static_cast<int>(s.d);
   p.K = static_cast<int>(s.I);
@@ -616,7 +612,6 @@ moe_status forward_gateup(const Shape& s, const void* x, const moe_weights* wts,
   p.tile_start = rt.tile_start;
   p.pair_start = rt.pair_start;
   p.rem_start = rt.rem_start;
-  p.pair_mode = rt.pair_mode;
   p.store_ab = act ? 1 : 0;
   p.I = I;
   p.status = o.status;
@@ -796,7 +791,6 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     p.tile_start = rt.tile_start;
     p.pair_start = rt.pair_start;
     p.rem_start = rt.rem_start;
-    p.pair_mode = rt.pair_mode;
     p.row_scale = rt.perm_w_pad;
     p.status = w.status;
     MOE_LAUNCH(PL_DOWN_ROUTED, st, launch_gemm(GK_DOWN, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
@@ -885,7 +879,6 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.tile_start = rt.tile_start;
     p.pair_start = rt.pair_start;
     p.rem_start = rt.rem_start;
-    p.pair_mode = rt.pair_mode;
     p.row_scale = rt.perm_w_pad;
     p.qt = w.dadbt;
     p.qt_ld = s.Rp;
@@ -923,7 +916,6 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.tile_start = rt.tile_start;
     p.pair_start = rt.pair_start;
     p.rem_start = rt.rem_start;
-    p.pair_mode = rt.pair_mode;
     p.row_scale = rt.perm_w_pad;
     p.status = w.status;
     MOE_LAUNCH(PL_DGRAD_DOWN_ROUTED, st, launch_gemm(GK_DGRAD_DOWN, p, grid_for(cdiv(s.Rp, kBM) * s.nparts), st));
@@ -964,7 +956,6 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.tile_start = rt.tile_start;
     p.pair_start = rt.pair_start;
     p.rem_start = rt.rem_start;
-    p.pair_mode = rt.pair_mode;
     p.status = w.status;
     MOE_LAUNCH(PL_DGRAD_GATEUP_ROUTED, st, launch_gemm(GK_MX_DGRAD_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
   } else {
@@ -984,7 +975,6 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.tile_start = rt.tile_start;
     p.pair_start = rt.pair_start;
     p.rem_start = rt.rem_start;
-    p.pair_mode = rt.pair_mode;
     p.status = w.status;
     MOE_LAUNCH(PL_DGRAD_GATEUP_ROUTED, st, launch_gemm(GK_DGRAD_GATEUP, p, grid_for(cdiv(s.Rp, kBM) * cdiv(s.d, kBN)), st));
   }

@@ -34,13 +34,14 @@ cudaError_t launch_chunk_scan(const int32_t* chunk_counts, int nchunk, int E, in
 cudaError_t launch_scatter(const int32_t* topk_idx, const float* topk_w, int T, int E, int k,
                            int row_align, const int32_t* chunk_base, const int32_t* counts, int32_t* offsets,
                            int32_t* row_start, int32_t* tile_start, int32_t* pair_start, int32_t* rem_start,
-                           int32_t* pair_mode, int32_t* perm_token, int32_t* route_row,
+                           int32_t* perm_token, int32_t* route_row,
                            int32_t* perm_token_pad, int32_t* route_row_pad, float* perm_w_pad,
                            cudaStream_t st);
-// pair_start / rem_start (optional, [E+1]): prefixes of floor(tiles / 2) and
-// of (tiles & 1) per expert, tiles = its 128-row GEMM tiles; pair_mode
-// (optional, one int): 1 when the grouped GEMMs should run tile pairs on SM
-// pairs (few odd experts), 0 when every tile should run on one SM.
+// pair_start / rem_start (optional, [E+1]): prefixes, over the experts, of the
+// tile pairs that run on SM pairs and of the tiles that run on one SM, tiles =
+// an expert's 128-row GEMM tiles: an even count runs as tiles / 2 pairs, an
+// odd count entirely on one SM (so that no expert's weights are read by both
+// passes).
 
 // ---- memory-bound kernels (elementwise.cu)
 cudaError_t launch_combine(const __nv_bfloat16* o, const __nv_bfloat16* ys,

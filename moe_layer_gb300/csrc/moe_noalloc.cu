@@ -154,7 +154,7 @@ extern "C" moe_status moe_route_topk_noalloc(const moe_config* cfg, const void* 
     return MOE_ERR_CUDA;
   if (launch_chunk_scan(chunk_counts, nchunk, Ei, chunk_base, counts, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_scatter(topk_idx, topk_w, Ti, Ei, ki, kRowAlign, chunk_base, counts, offsets, row_start, tile_start,
-                     nullptr, nullptr, nullptr, perm_token, route_row, perm_token_pad, route_row_pad, perm_w_pad, st) != cudaSuccess)
+                     nullptr, nullptr, perm_token, route_row, perm_token_pad, route_row_pad, perm_w_pad, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -149,13 +149,17 @@ __device__ __forceinline__ int row_tiles(int c, int align) {
   return (pad_rows(c, align) + kTileRows - 1) / kTileRows;
 }
 
+// Tile pairs of an expert with `tiles` GEMM row tiles: all of them pair up when
+// the count is even; an odd count runs every tile on one SM (a lone last tile
+// would make that pass read the expert's weights a second time).
+__device__ __forceinline__ int expert_pairs(int tiles) { return (tiles & 1) ? 0 : tiles >> 1; }
+
 __global__ void __launch_bounds__(kChunkWarps * 32)
     scatter_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int T,
                    int E, int k, int align, const int32_t* __restrict__ chunk_base,
                    const int32_t* __restrict__ counts, int32_t* __restrict__ offsets_out,
                    int32_t* __restrict__ row_start_out, int32_t* __restrict__ tile_start_out,
                    int32_t* __restrict__ pair_start_out, int32_t* __restrict__ rem_start_out,
-                   int32_t* __restrict__ pair_mode_out,
                    int32_t* __restrict__ perm_token,
                    int32_t* __restrict__ route_row, int32_t* __restrict__ perm_token_pad,
                    int32_t* __restrict__ route_row_pad, float* __restrict__ perm_w_pad) {
@@ -168,8 +172,8 @@ __global__ void __launch_bounds__(kChunkWarps * 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // 1. expert offsets: exclusive prefix of counts, of padded row counts, of
-  //    GEMM row tiles, of pairs of row tiles and of experts with an odd
-  //    number of row tiles (the GEMMs that run tile pairs on SM pairs)
+  //    GEMM row tiles, and of the tiles the grouped GEMMs run in pairs on SM
+  //    pairs and alone on one SM (expert_pairs)
   if (warp == 0) {
     const int per = (E + 31) / 32;
     int sum = 0, psum = 0, tsum = 0, qsum = 0, osum = 0;
@@ -181,8 +185,8 @@ __global__ void __launch_bounds__(kChunkWarps * 32)
         sum += c;
         psum += pad_rows(c, align);
         tsum += tiles;
-        qsum += tiles >> 1;
-        osum += tiles & 1;
+        qsum += expert_pairs(tiles);
+        osum += tiles - 2 * expert_pairs(tiles);
       }
     }
     int inc = sum, pinc = psum, tinc = tsum, qinc = qsum, oinc = osum;
@@ -215,8 +219,8 @@ __global__ void __launch_bounds__(kChunkWarps * 32)
         run += c;
         prun += pad_rows(c, align);
         trun += tiles;
-        qrun += tiles >> 1;
-        orun += tiles & 1;
+        qrun += expert_pairs(tiles);
+        orun += tiles - 2 * expert_pairs(tiles);
       }
     }
     if (lane == 31) {
@@ -237,10 +241,6 @@ __global__ void __launch_bounds__(kChunkWarps * 32)
       if (pair_start_out) pair_start_out[e] = s_ps[e];
       if (rem_start_out) rem_start_out[e] = s_qs[e];
     }
-    // Tile pairs on SM pairs pay only while few experts leave an odd m-tile to
-    // a second, one-SM pass (which reads those experts' weights again): at
-    // most one such tile per 8 (measured: 123 of 1147 gained, about 1 in 3 lost).
-    if (pair_mode_out && threadIdx.x == 0) pair_mode_out[0] = (8 * s_qs[E] <= s_ts[E]) ? 1 : 0;
   }
   // padding rows of the padded layout: no token, weight 0
   for (int e = blockIdx.x; e < E; e += gridDim.x) {
@@ -315,12 +315,12 @@ cudaError_t launch_chunk_scan(const int32_t* chunk_counts, int nchunk, int E, in
 cudaError_t launch_scatter(const int32_t* topk_idx, const float* topk_w, int T, int E, int k,
                            int row_align, const int32_t* chunk_base, const int32_t* counts, int32_t* offsets,
                            int32_t* row_start, int32_t* tile_start, int32_t* pair_start, int32_t* rem_start,
-                           int32_t* pair_mode, int32_t* perm_token, int32_t* route_row, int32_t* perm_token_pad,
+                           int32_t* perm_token, int32_t* route_row, int32_t* perm_token_pad,
                            int32_t* route_row_pad, float* perm_w_pad, cudaStream_t st) {
   const int nchunk = (T + kChunkTokens - 1) / kChunkTokens;
   scatter_kernel<<<nchunk, kChunkWarps * 32, 0, st>>>(topk_idx, topk_w, T, E, k, row_align, chunk_base, counts,
                                                       offsets, row_start, tile_start, pair_start, rem_start,
-                                                      pair_mode, perm_token,
+                                                      perm_token,
                                                       route_row, perm_token_pad, route_row_pad,
                                                       perm_w_pad);
   return cudaGetLastError();

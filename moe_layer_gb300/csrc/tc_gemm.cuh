@@ -17,10 +17,11 @@
 //
 // Two number formats:
 //   bf16   kind::f16 MMAs, K = 64 per pipeline stage, operands K-major or
-//          MN-major: 128x256x16 on one SM (router projection; grouped GEMMs
-//          when the routing leaves many odd experts), or 256x256x16 on a pair
-//          of SMs (SCHED_ROWS2 / SCHED_WGRAD2, cta_group::2: each SM holds its
-//          128 rows of A and half of B) for every other bf16 GEMM;
+//          MN-major: 128x256x16 on one SM (router projection; the experts
+//          with an odd number of row tiles; weight gradients of experts with
+//          few rows), or 256x256x16 on a pair of SMs (SCHED_ROWS2 /
+//          SCHED_WGRAD2, cta_group::2: each SM holds its 128 rows of A and
+//          half of B) for the other bf16 GEMM tiles;
 //   MXFP8  (MX = true; blog section "MXFP8 support") kind::mxf8f6f4 block-scaled
 //          MMAs (128x256x32) on E4M3 operands, both K-major, K = 128 per stage.
 //          Each stage also brings the E8M0 scales of its A and B tiles (one
@@ -158,7 +159,9 @@ __host__ __device__ constexpr int gemm_smem_bytes_for() {
 
 // The bf16 GEMMs other than the router projection run as two launches: a
 // 2-SM pass (SCHED_ROWS2, SCHED_WGRAD2) over pairs of m-tiles, and a 1-SM
-// pass over the last m-tile of every group with an odd number of them.  A 128 x 256 tile
+// pass over the rest (grouped rows: every tile of the experts with an odd
+// number of them, so that no expert's weights are streamed by both passes;
+// dense rows and weight gradients: the last m-tile of an odd count).  A 128 x 256 tile
 // per SM stages 48 KB per K step and its MMAs read as much again from shared
 // memory; with the B tile split between the two SMs of a pair both become
 // 32 KB.  Measured at the DSV3 shape, staging only half of the gate/up weight
@@ -193,13 +196,12 @@ struct GemmParams {
   int num_groups;          // number of groups (experts) when grouped
   const int* row_start;    // [G+1] padded row offsets, multiples of 64 (128 in MXFP8 mode)
   const int* tile_start;   // [G+1] prefix of 128-row tiles per group (grouped SCHED_ROWS)
-  const int* pair_start;   // [G+1] prefix of floor(tiles / 2) per group (grouped SCHED_ROWS2)
-  const int* rem_start;    // [G+1] prefix of groups with an odd tile count (grouped, part 1)
-  const int* pair_mode;    // grouped rows: device flag, 0 = no SM pairs (the 2-SM pass has no
-                           // work, the 1-SM pass with part 1 takes every tile); null = 1
-  int part;                // 1-SM passes: 0 every tile; 1 only the last m-tile of groups
-                           // (or dense row ranges, or weight gradients) with an odd
-                           // number of m-tiles
+  const int* pair_start;   // [G+1] prefix of tile pairs per group (grouped SCHED_ROWS2)
+  const int* rem_start;    // [G+1] prefix of the tiles per group left to one SM (grouped, part 1)
+  int part;                // 1-SM passes: 0 every tile; 1 only the tiles that are not in
+                           // pairs (grouped rows: every tile of a group with an odd tile
+                           // count; dense rows and weight gradients: the last m-tile when
+                           // the m-tile count is odd)
   const int* counts;       // [G] real rows per group (grouped)
   int N;                   // output columns
   int K;                   // reduction length (SCHED_ROWS)
@@ -285,11 +287,6 @@ __device__ __forceinline__ int find_group(const int* row_start, int G, int row) 
   return lo;
 }
 
-// Grouped rows: whether the routing chose SM pairs, and whether a 1-SM launch
-// with part 1 takes only the odd groups' last m-tiles (else every tile).
-__device__ __forceinline__ bool pairs_on(const GemmParams& p) { return !p.pair_mode || __ldg(p.pair_mode) != 0; }
-__device__ __forceinline__ bool leftover_only(const GemmParams& p) { return p.part && pairs_on(p); }
-
 // Work items per launch: tiles, or in the 2-SM mode pairs of tiles.
 template <int EPI, int SCH, int BN>
 __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
@@ -300,8 +297,7 @@ __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
       if (SCH == SCHED_ROWS2) return (mt / 2) * num_nt;
       return (p.part ? (mt & 1) : mt) * num_nt;
     }
-    if (SCH == SCHED_ROWS2 && !pairs_on(p)) return 0;
-    const int* prefix = SCH == SCHED_ROWS2 ? p.pair_start : (leftover_only(p) ? p.rem_start : p.tile_start);
+    const int* prefix = SCH == SCHED_ROWS2 ? p.pair_start : (p.part ? p.rem_start : p.tile_start);
     return __ldg(prefix + p.num_groups) * num_nt;
   } else {
     const int num_nt = (p.N + BN - 1) / BN;
@@ -360,10 +356,14 @@ __device__ __forceinline__ TileInfo gemm_tile(const GemmParams& p, int tau, uint
         const int local = tau - ps * num_nt;
         nt = local / np;
         mt = 2 * (local - nt * np) + r;
-      } else if (leftover_only(p)) {
+      } else if (p.part) {
+        // this expert's m-tiles that are not in pairs: the ones after its pairs
         e = find_group(p.rem_start, G, tau / num_nt);
-        nt = tau - __ldg(p.rem_start + e) * num_nt;
-        mt = __ldg(p.tile_start + e + 1) - __ldg(p.tile_start + e) - 1;
+        const int rs = __ldg(p.rem_start + e);
+        const int nr = __ldg(p.rem_start + e + 1) - rs;
+        const int local = tau - rs * num_nt;
+        nt = local / nr;
+        mt = 2 * (__ldg(p.pair_start + e + 1) - __ldg(p.pair_start + e)) + (local - nt * nr);
       } else {
         const int q = tau / num_nt;
         e = find_group(p.tile_start, G, q);

@@ -98,13 +98,13 @@ SHAPES = {
     "zipf_zero": MoEShape(T=640, d=256, I=128, E=32, k=4, n_shared=1, I_shared=128, w_std=0.05,
                           zipf=True, zero_experts=8),
     # every expert and the shared expert have a single 64-row tile (the GEMMs' SM-pair pass has
-    # no work, all tiles go through the one-SM pass); dW_gate/dW_up have one 128-row output
-    # tile, dW_down three (one SM pair plus one tile on one SM)
+    # no work, all tiles go through the one-SM pass); the weight gradients run on one SM with
+    # eight epilogue warps (16 rows per expert)
     "small_T": MoEShape(T=64, d=384, I=128, E=8, k=2, n_shared=1, I_shared=128, w_std=0.05),
     "single_token": MoEShape(T=1, d=256, I=256, E=16, k=4, n_shared=1, I_shared=256, w_std=0.05),
-    # four of eight experts with an odd m-tile count in 44 tiles: the routing picks SM pairs,
-    # and the odd experts' last m-tiles go through the one-SM pass (the other shapes here run
-    # either without odd experts or, with many, every tile on one SM)
+    # four of eight experts with an odd m-tile count in 44 tiles: the even experts' tiles run in
+    # pairs on SM pairs and every tile of the odd ones on one SM, so both passes of each grouped
+    # GEMM have work; 640 rows per expert put the weight gradients on SM pairs
     "pairs_leftover": MoEShape(T=2560, d=512, I=256, E=8, k=2, n_shared=1, I_shared=128, w_std=0.05),
 }
 
