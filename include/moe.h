@@ -59,15 +59,15 @@ typedef enum {
 typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
 
 /* moe_config.flags.
- * MOE_FLAG_REPLAY: the saved state holds only the routing; moe_backward first
- *   recomputes the forward up to the SwiGLU activation (the expert-grouped x
- *   rows, a and b, routed and shared) into its workspace ("forward activation
- *   replay", Mixture-of-Kittens blog post, section "Reversed ring to minimize
- *   forward replay during backward").  The saved buffer shrinks by
- *   Rp*(2d + 4I) + T*4*I_shared bytes in bf16 mode (Rp: routes padded per
- *   expert), the backward workspace grows by about as much, and the backward
- *   does the dispatch and gate/up GEMMs again.  Results are bitwise identical
- *   to those without the flag. */
+ * MOE_FLAG_REPLAY: the saved state holds the routing and the shared expert's
+ *   a and b only; moe_backward first recomputes the routed experts' forward
+ *   up to the SwiGLU activation (the expert-grouped x rows, a and b) into its
+ *   workspace ("forward activation replay", Mixture-of-Kittens blog post,
+ *   section "Reversed ring to minimize forward replay during backward").  The
+ *   saved buffer shrinks by Rp*(2d + 4I) bytes in bf16 mode (Rp: routes padded
+ *   per expert), the backward workspace grows by as much, and the backward
+ *   does the dispatch and the routed gate/up GEMM again.  Results are bitwise
+ *   identical to those without the flag. */
 #define MOE_FLAG_REPLAY 1u
 
 typedef struct {
@@ -111,8 +111,9 @@ typedef struct {
 
 /* Byte sizes of the caller-allocated buffers for a configuration:
  *   fwd_ws  scratch for moe_forward and moe_route_topk
- *   saved   state moe_forward leaves for moe_backward (routing; the x rows, a
- *           and b unless MOE_FLAG_REPLAY)
+ *   saved   state moe_forward leaves for moe_backward (routing; the shared
+ *           expert's a and b; the routed x rows, a and b unless
+ *           MOE_FLAG_REPLAY)
  *   bwd_ws  scratch for moe_backward
  * Each buffer must be 256-byte aligned (moe_route_topk, moe_forward and
  * moe_backward return MOE_ERR_INVALID_ARG otherwise); its first 256 bytes hold

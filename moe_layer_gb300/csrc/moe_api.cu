@@ -157,18 +157,19 @@ struct Acts {
   __nv_bfloat16* abs;  // [T, 2Is]
   uint8_t *xt, *xt_sf;  // MXFP8: the x rows transposed, quantized along the tokens [d, Rp]
 };
-void carve_acts(Carver& c, const Shape& s, Acts& a) {
+// The routed experts' activations (everything in Acts but abs).
+void carve_routed_acts(Carver& c, const Shape& s, Acts& a) {
   const int64_t m = s.mx ? 1 : 0;
   a.xp = c.take<__nv_bfloat16>((1 - m) * s.Rp * s.d);
   a.ab = c.take<__nv_bfloat16>(s.Rp * 2 * s.I);
-  a.abs = c.take<__nv_bfloat16>(s.S ? s.T * 2 * s.Is : 0);
   a.xt = c.take<uint8_t>(m * s.Rp * s.d);
   a.xt_sf = c.take<uint8_t>(m * mx_sf_alloc(s.d, s.Rp));
 }
 
-// State moe_forward leaves for moe_backward: the routing, and the activations
-// unless they are replayed (MOE_FLAG_REPLAY; then act lives in the backward
-// workspace).
+// State moe_forward leaves for moe_backward: the routing, the shared expert's
+// a and b, and the routed experts' activations unless they are replayed
+// (MOE_FLAG_REPLAY; then those live in the backward workspace: the shared
+// expert's are T rows against the routed T·k, not worth recomputing).
 struct Saved {
   Routing rt;
   Acts act;
@@ -177,7 +178,9 @@ void carve_saved(void* base, const Shape& s, Saved& v, size_t* bytes) {
   Carver c(base);
   c.take<char>(kAlign);
   carve_routing(c, s, v.rt);
-  if (!s.replay) carve_acts(c, s, v.act);
+  v.act = Acts{};
+  v.act.abs = c.take<__nv_bfloat16>(s.S ? s.T * 2 * s.Is : 0);
+  if (!s.replay) carve_routed_acts(c, s, v.act);
   if (bytes) *bytes = c.off;
 }
 
@@ -263,7 +266,8 @@ void carve_bwd(void* base, const Shape& s, BwdWs& w, size_t* bytes) {
   w.dadbt_sf = c.take<uint8_t>(m * mx_sf_alloc(2 * s.I, s.Rp));
   w.hgt = c.take<uint8_t>(m * s.Rp * s.I);
   w.hgt_sf = c.take<uint8_t>(m * mx_sf_alloc(s.I, s.Rp));
-  if (s.replay) carve_acts(c, s, w.act);
+  w.act = Acts{};
+  if (s.replay) carve_routed_acts(c, s, w.act);
   if (bytes) *bytes = c.off;
 }
 
@@ -542,7 +546,9 @@ moe_status down_routed_mx(const Shape& s, const moe_weights* wts, const Routing&
 struct GateUpOut {
   __nv_bfloat16* xp;    // bf16 mode: [Rp, d] x rows, when no activations are kept
   __nv_bfloat16* h;     // bf16 mode: [Rp, I] SwiGLU output
+  bool shared;          // also run the shared expert's gate/up (when there is one)
   __nv_bfloat16* hs;    // [T, Is] shared expert's SwiGLU output
+  __nv_bfloat16* abs;   // [T, 2Is] shared expert's a and b, or null when not kept
   uint8_t *xq, *xq_sf;  // MXFP8: [Rp, d] x rows quantized along d
   uint8_t *hq, *hq_sf;  // MXFP8: [Rp, I] h quantized along I
   int* status;
@@ -550,9 +556,10 @@ struct GateUpOut {
 
 // The forward up to the SwiGLU activation: dispatch of x (quantized on the
 // way in MXFP8 mode) and the gate/up projections with the SwiGLU epilogue,
-// shared and routed.  act: where the activations the backward needs go (the
-// x rows, a and b), or null in inference.  The backward runs this again when
-// the saved state holds only the routing (forward activation replay).
+// shared (if o.shared) and routed.  act: where the routed activations the
+// backward needs go (the x rows, a and b), or null in inference.  The backward
+// runs the routed part again when the saved state holds only the routing and
+// the shared expert's a and b (forward activation replay).
 moe_status forward_gateup(const Shape& s, const void* x, const moe_weights* wts, const Routing& rt,
                           const Acts* act, const GateUpOut& o, cudaStream_t st) {
   const int T = static_cast<int>(s.T), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
@@ -568,7 +575,7 @@ moe_status forward_gateup(const Shape& s, const void* x, const moe_weights* wts,
     MOE_LAUNCH(PL_PERMUTE_X, st, launch_permute_rows(static_cast<const __nv_bfloat16*>(x), rt.perm_token_pad,
                                                     rt.row_start + E, static_cast<int>(s.Rp), d, xp, st));
   // shared expert gate/up + SwiGLU (dense rows of x)
-  if (s.S) {
+  if (s.S && o.shared) {
     GemmParams p;
     zero_params(p);
     MOE_TRY(tmap(&p.tmA, x, s.T, s.d, 64, kBM));
@@ -578,13 +585,13 @@ moe_status forward_gateup(const Shape& s, const void* x, const moe_weights* wts,
     p.N = static_cast<int>(s.Is);
     p.K = d;
     MOE_TRY(omap(&p.tmO1, o.hs, s.T, s.Is));
-    if (act)
-      MOE_TRY(omap(&p.tmO0, act->abs, s.T, 2 * s.Is));
+    if (o.abs)
+      MOE_TRY(omap(&p.tmO0, o.abs, s.T, 2 * s.Is));
     else
       p.tmO0 = p.tmO1;  // a and b are not kept in inference
     p.tmO0h = p.tmO0;  // dense rows: no tail tiles
     p.tmO1h = p.tmO1;
-    p.store_ab = act ? 1 : 0;
+    p.store_ab = o.abs ? 1 : 0;
     p.I = static_cast<int>(s.Is);
     p.status = o.status;
     MOE_LAUNCH(PL_GATEUP_SHARED, st, launch_gemm(GK_GATEUP, p, grid_for(cdiv(s.T, kBM) * cdiv(s.Is, kBN / 2)), st));
@@ -771,7 +778,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
 
   // the activations the backward needs go to the saved state, unless it keeps
   // only the routing (MOE_FLAG_REPLAY) or there is none (inference)
-  const GateUpOut o{w.xp, w.h, w.hs, w.xq, w.xq_sf, w.hq, w.hq_sf, w.status};
+  const GateUpOut o{w.xp, w.h, true, w.hs, saved ? sv.act.abs : nullptr, w.xq, w.xq_sf, w.hq, w.hq_sf, w.status};
   MOE_TRY(forward_gateup(s, x, wts, rt, (saved && !s.replay) ? &sv.act : nullptr, o, st));
   if (s.mx) {
     MOE_TRY(down_routed_mx(s, wts, rt, w, st));
@@ -835,15 +842,17 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
   carve_bwd(ws, s, w, nullptr);
   const int T = static_cast<int>(s.T), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
   const int E = static_cast<int>(s.E), k = static_cast<int>(s.k), Is = static_cast<int>(s.Is);
-  // MOE_FLAG_REPLAY: the saved state holds only the routing; recompute the
-  // forward up to the SwiGLU into the workspace.  Its h outputs and quantized
-  // x rows land in buffers this backward overwrites later (hg, hs; in MXFP8
-  // mode dadbq and dyq), the same kernels on the same inputs as the forward,
-  // so a and b are bitwise those the forward produced.
-  const Acts& act = s.replay ? w.act : sv.act;
+  // MOE_FLAG_REPLAY: the saved state holds the routing and the shared
+  // expert's a and b; recompute the routed experts' forward up to the SwiGLU
+  // into the workspace.  Its h outputs and quantized x rows land in buffers
+  // this backward overwrites later (hg; in MXFP8 mode dadbq and dyq), the same
+  // kernels on the same inputs as the forward, so a and b are bitwise those
+  // the forward produced.
+  Acts act = s.replay ? w.act : sv.act;
+  act.abs = sv.act.abs;  // the shared expert's a and b are always saved
   if (s.replay) {
-    const GateUpOut o{nullptr, w.hg, w.hs, w.dyq, w.dyq_sf, w.dadbq, w.dadbq_sf, w.status};
-    MOE_TRY(forward_gateup(s, x, wts, rt, &w.act, o, st));
+    const GateUpOut o{nullptr, w.hg, false, nullptr, nullptr, w.dyq, w.dyq_sf, w.dadbq, w.dadbq_sf, w.status};
+    MOE_TRY(forward_gateup(s, x, wts, rt, &act, o, st));
   }
 
   MxWeights m;
