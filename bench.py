@@ -118,6 +118,29 @@ NCU_TRAFFIC = {
 }
 
 
+class _Ranks:
+    """The replicas' only cross-rank steps: a barrier around each timed region
+    and the slowest rank's time (the job's time).  `device` holds the reduced
+    value: "cuda" with NCCL, "cpu" with gloo."""
+
+    def __init__(self, world, device):
+        self.world, self.device = world, device
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max(self, v):
+        if self.world == 1:
+            return v
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([v], dtype=torch.float64, device=self.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle sampling during the timed region."""
 
@@ -304,17 +327,8 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    ranks = _Ranks(world, "cuda")
+    barrier, max_over_ranks = ranks.barrier, ranks.max
 
     _abi.load()
     s, desc, mx = _workload(args.workload, args.tokens, args.experts, args.zipf, args.zero_experts)
