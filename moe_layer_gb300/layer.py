@@ -78,3 +78,38 @@ def backward(cfg, inp: dict, dy, bufs: MoEBuffers, grads: dict, dx=None, stream=
     _abi.moe_backward(cfg, inp["x"], weights_from(inp), dy, bufs.saved, dx, grads_struct(grads),
                       bufs.bwd_ws, stream)
     return dx
+
+
+class MoEFunction(torch.autograd.Function):
+    """torch.autograd wrapper: y = MoE(x) with moe_forward, and in the backward
+    dx and every weight gradient from one moe_backward call.  Argument
+    marshalling only.  `bufs` holds this call's saved state, so each layer (and
+    each call whose backward is still pending) needs its own MoEBuffers.
+    Gradients come back in the parameters' dtypes (dW_router is computed in
+    fp32).  MXFP8 mode: pass the pre-quantized weight buffer as `mxfp8`.
+
+        y = MoEFunction.apply(cfg, bufs, x, W_router, W_gate, W_up, W_down,
+                              Ws_gate, Ws_up, Ws_down, router_bias, mxfp8)
+    """
+
+    _NAMES = ("x", "W_router", "W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down", "router_bias", "mxfp8")
+
+    @staticmethod
+    def forward(ctx, cfg, bufs, x, W_router, W_gate, W_up, W_down, Ws_gate=None, Ws_up=None, Ws_down=None,
+                router_bias=None, mxfp8=None):
+        x = x.contiguous()
+        inp = dict(zip(MoEFunction._NAMES, (x, W_router, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down,
+                                            router_bias, mxfp8)))
+        y = forward(cfg, inp, bufs)
+        ctx.save_for_backward(x, W_router, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, router_bias, mxfp8)
+        ctx.cfg, ctx.bufs = cfg, bufs
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        cfg, bufs = ctx.cfg, ctx.bufs
+        inp = dict(zip(MoEFunction._NAMES, ctx.saved_tensors))
+        g = alloc_grads(cfg, device=dy.device, with_topk=False)
+        dx = backward(cfg, inp, dy.contiguous(), bufs, g)
+        return (None, None, dx, g["dW_router"], g["dW_gate"], g["dW_up"], g["dW_down"], g["dWs_gate"],
+                g["dWs_up"], g["dWs_down"], None, None)
