@@ -69,6 +69,12 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
  *   does the dispatch and the routed gate/up GEMM again.  Results are bitwise
  *   identical to those without the flag. */
 #define MOE_FLAG_REPLAY 1u
+/* MOE_FLAG_WGRAD_FP32: moe_backward writes dW_gate, dW_up, dW_down and dWs_*
+ *   as fp32 (same shapes; each buffer 32-byte aligned) instead of bf16: the
+ *   same fp32 accumulators without the final rounding, for callers that
+ *   accumulate gradients in fp32.  bf16 mode only (with MOE_MXFP8 it gives
+ *   MOE_ERR_UNSUPPORTED).  dW_router is fp32 either way. */
+#define MOE_FLAG_WGRAD_FP32 2u
 
 typedef struct {
   int64_t T;        /* tokens */
@@ -97,12 +103,12 @@ typedef struct {
 
 typedef struct {
   float* dW_router; /* [E, d] fp32 */
-  void* dW_gate;    /* [E, I, d] bf16 */
-  void* dW_up;      /* [E, I, d] bf16 */
-  void* dW_down;    /* [E, d, I] bf16 */
-  void* dWs_gate;   /* [I_s, d] bf16 (n_shared == 1) */
-  void* dWs_up;     /* [I_s, d] bf16 */
-  void* dWs_down;   /* [d, I_s] bf16 */
+  void* dW_gate;    /* [E, I, d] bf16 (fp32 with MOE_FLAG_WGRAD_FP32) */
+  void* dW_up;      /* [E, I, d] bf16 (likewise) */
+  void* dW_down;    /* [E, d, I] bf16 (likewise) */
+  void* dWs_gate;   /* [I_s, d] bf16 (n_shared == 1; likewise) */
+  void* dWs_up;     /* [I_s, d] bf16 (likewise) */
+  void* dWs_down;   /* [d, I_s] bf16 (likewise) */
   float* d_topk_w;  /* [T, top_k] fp32 router-weight gradient dL/dg, or NULL */
   void* dx_ready;   /* cudaEvent_t or NULL: when given, moe_backward records it on the stream
                        as soon as dx is complete, before the weight gradients are computed,

@@ -19,6 +19,7 @@ MOE_BF16 = 0
 MOE_MXFP8 = 1
 # moe_config.flags bits (include/moe.h)
 MOE_FLAG_REPLAY = 1
+MOE_FLAG_WGRAD_FP32 = 2
 
 EXPORTED = ["moe_workspace_size", "moe_mxfp8_weights_size", "moe_quantize_weights_mxfp8",
             "moe_route_topk", "moe_route_topk_noalloc", "moe_forward",

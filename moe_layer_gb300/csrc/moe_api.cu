@@ -99,7 +99,8 @@ struct Shape {
   int64_t T, d, I, E, k, S, Is, R, Rp, nchunk, nparts;
   int64_t ra;   // row alignment of the expert groups
   bool mx;      // MXFP8 routed experts
-  bool replay;  // saved state = routing only; the backward recomputes the rest
+  bool replay;     // saved state without the routed activations; the backward recomputes them
+  bool wgrad_f32;  // weight gradients written in fp32
 };
 
 // Carves 256-byte aligned sub-buffers from a base pointer (or only sizes them
@@ -306,7 +307,8 @@ moe_status check_config(const moe_config* cfg, Shape& s) {
     return MOE_ERR_INVALID_ARG;
   if (cfg->precision != MOE_BF16 && cfg->precision != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
   if (cfg->precision == MOE_MXFP8 && (cfg->d % 128 || cfg->I % 128)) return MOE_ERR_UNSUPPORTED;
-  if (cfg->flags & ~MOE_FLAG_REPLAY) return MOE_ERR_UNSUPPORTED;
+  if (cfg->flags & ~(MOE_FLAG_REPLAY | MOE_FLAG_WGRAD_FP32)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->precision == MOE_MXFP8 && (cfg->flags & MOE_FLAG_WGRAD_FP32)) return MOE_ERR_UNSUPPORTED;
   if (cfg->E > kMaxExperts || cfg->top_k > kMaxTopK || cfg->top_k > cfg->E) return MOE_ERR_UNSUPPORTED;
   if (cfg->n_shared > 1) return MOE_ERR_UNSUPPORTED;
   if (cfg->d % 64 || cfg->I % 64 || (cfg->n_shared && cfg->I_shared % 64)) return MOE_ERR_UNSUPPORTED;
@@ -320,6 +322,7 @@ moe_status check_config(const moe_config* cfg, Shape& s) {
   s.R = s.T * s.k;
   s.mx = cfg->precision == MOE_MXFP8;
   s.replay = (cfg->flags & MOE_FLAG_REPLAY) != 0;
+  s.wgrad_f32 = (cfg->flags & MOE_FLAG_WGRAD_FP32) != 0;
   s.ra = s.mx ? kRowAlignMx : kRowAlign;
   s.Rp = s.R + s.E * (s.ra - 1);
   if (s.mx) s.Rp = (s.Rp + kRowAlignMx - 1) / kRowAlignMx * kRowAlignMx;  // whole scale blocks
@@ -834,6 +837,10 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     return MOE_ERR_INVALID_ARG;
   if (!g->dW_router || !g->dW_gate || !g->dW_up || !g->dW_down) return MOE_ERR_INVALID_ARG;
   if (s.S && (!g->dWs_gate || !g->dWs_up || !g->dWs_down)) return MOE_ERR_INVALID_ARG;
+  if (s.wgrad_f32) {  // fp32 weight gradients go out in 32-byte vector stores
+    for (const void* q : {g->dW_gate, g->dW_up, g->dW_down, g->dWs_gate, g->dWs_up, g->dWs_down})
+      if (reinterpret_cast<uintptr_t>(q) & 31u) return MOE_ERR_INVALID_ARG;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Saved sv;
   carve_saved(const_cast<void*>(saved), s, sv, nullptr);
@@ -1024,6 +1031,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.N = I;
     p.wgrad_mode = wgrad_mode(s);
     MOE_TRY(omap3(&p.tmO0, g->dW_down, s.E, s.d, s.I));
+    if (s.wgrad_f32) p.out_f32 = static_cast<float*>(g->dW_down);
     p.status = w.status;
     MOE_LAUNCH(PL_WGRAD_DOWN, st, launch_gemm(GK_WGRAD, p, grid_for(s.E * cdiv(s.d, kBM) * cdiv(s.I, kBN)), st));
   }
@@ -1039,6 +1047,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.wgrad_mode = wgrad_mode(s);
     p.a_col_off = half ? I : 0;
     MOE_TRY(omap3(&p.tmO0, half ? g->dW_up : g->dW_gate, s.E, s.I, s.d));
+    if (s.wgrad_f32) p.out_f32 = static_cast<float*>(half ? g->dW_up : g->dW_gate);
     p.status = w.status;
     MOE_LAUNCH(half ? PL_WGRAD_UP : PL_WGRAD_GATE, st, launch_gemm(GK_WGRAD, p, grid_for(s.E * cdiv(s.I, kBM) * cdiv(s.d, kBN)), st));
   }
@@ -1053,6 +1062,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
       p.M_out = d;
       p.N = Is;
       MOE_TRY(omap(&p.tmO0, g->dWs_down, s.d, s.Is));
+      if (s.wgrad_f32) p.out_f32 = static_cast<float*>(g->dWs_down);
       p.status = w.status;
       MOE_LAUNCH(PL_WGRAD_SHARED_DOWN, st, launch_gemm(GK_WGRAD, p, grid_for(cdiv(s.d, kBM) * cdiv(s.Is, kBN)), st));
     }
@@ -1066,6 +1076,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
       p.N = d;
       p.a_col_off = half ? Is : 0;
       MOE_TRY(omap(&p.tmO0, half ? g->dWs_up : g->dWs_gate, s.Is, s.d));
+      if (s.wgrad_f32) p.out_f32 = static_cast<float*>(half ? g->dWs_up : g->dWs_gate);
       p.status = w.status;
       MOE_LAUNCH(half ? PL_WGRAD_SHARED_UP : PL_WGRAD_SHARED_GATE, st, launch_gemm(GK_WGRAD, p, grid_for(cdiv(s.Is, kBM) * cdiv(s.d, kBN)), st));
     }

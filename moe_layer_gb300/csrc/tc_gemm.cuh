@@ -256,6 +256,9 @@ struct GemmParams {
   // one SM), 1 every tile on one SM (short K), 2 every tile on one SM with
   // the wide epilogue (the shortest K).
   int wgrad_mode;
+  // Weight gradients: when set, the output in fp32 ([G, M_out, N], or
+  // [M_out, N] for dense rows; 32-byte aligned) instead of bf16 through tmO0.
+  float* out_f32;
 };
 
 template <int EPI>
@@ -801,8 +804,8 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
 
     if constexpr (sched_wgrad(SCH)) {
       const int r0 = t.m0 + warp_e * 32;
-      for (int c0 = cbeg; c0 < cend && t.n0 + c0 < p.N; c0 += 64) {
-        float v[64];
+      // 64 accumulator columns of this lane's row (zeros for an expert without rows)
+      auto load64 = [&](int c0, float* v) {
         if (t.nkb > 0) {
           tmem_ld32(tr + c0, v);
           tmem_ld32(tr + c0 + 32, v + 32);
@@ -811,12 +814,35 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
 #pragma unroll
           for (int i = 0; i < 64; ++i) v[i] = 0.f;
         }
-        const uint32_t box = stg.begin();
-        stage_row_sw128(box, lane, v);
-        if (p.dense_rows > 0)
-          stg.store2d(&p.tmO0, box, t.n0 + c0, r0);
-        else
-          stg.store3d(&p.tmO0, box, t.n0 + c0, r0, t.e);
+      };
+      if (p.out_f32) {  // fp32 weight gradients: this lane's row in 256-bit stores
+        const int row = r0 + lane;
+        const long long grow = (p.dense_rows > 0 ? 0LL : static_cast<long long>(t.e) * p.M_out) + row;
+        for (int c0 = cbeg; c0 < cend && t.n0 + c0 < p.N; c0 += 64) {
+          float v[64];
+          load64(c0, v);
+          if (row < p.M_out) {
+            float* dst = p.out_f32 + grow * p.N + t.n0 + c0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              st_global_v8(dst + 8 * q,
+                           make_uint4(__float_as_uint(v[8 * q]), __float_as_uint(v[8 * q + 1]),
+                                      __float_as_uint(v[8 * q + 2]), __float_as_uint(v[8 * q + 3])),
+                           make_uint4(__float_as_uint(v[8 * q + 4]), __float_as_uint(v[8 * q + 5]),
+                                      __float_as_uint(v[8 * q + 6]), __float_as_uint(v[8 * q + 7])));
+          }
+        }
+      } else {
+        for (int c0 = cbeg; c0 < cend && t.n0 + c0 < p.N; c0 += 64) {
+          float v[64];
+          load64(c0, v);
+          const uint32_t box = stg.begin();
+          stage_row_sw128(box, lane, v);
+          if (p.dense_rows > 0)
+            stg.store2d(&p.tmO0, box, t.n0 + c0, r0);
+          else
+            stg.store3d(&p.tmO0, box, t.n0 + c0, r0, t.e);
+        }
       }
     } else {
       const bool real = lane_ok && row < t.rows_valid;

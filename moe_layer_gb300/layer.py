@@ -43,18 +43,19 @@ def quantize_weights(cfg, inp: dict, stream=None):
 def alloc_grads(cfg: _abi.MoeConfig, device="cuda", with_topk: bool = True) -> dict:
     dev = torch.device(device)
     T, d, I, E, k = cfg.T, cfg.d, cfg.I, cfg.E, cfg.top_k
+    wdt = torch.float32 if cfg.flags & _abi.MOE_FLAG_WGRAD_FP32 else torch.bfloat16
     g = {
         "dW_router": torch.empty(E, d, dtype=torch.float32, device=dev),
-        "dW_gate": torch.empty(E, I, d, dtype=torch.bfloat16, device=dev),
-        "dW_up": torch.empty(E, I, d, dtype=torch.bfloat16, device=dev),
-        "dW_down": torch.empty(E, d, I, dtype=torch.bfloat16, device=dev),
+        "dW_gate": torch.empty(E, I, d, dtype=wdt, device=dev),
+        "dW_up": torch.empty(E, I, d, dtype=wdt, device=dev),
+        "dW_down": torch.empty(E, d, I, dtype=wdt, device=dev),
         "d_topk_w": torch.empty(T, k, dtype=torch.float32, device=dev) if with_topk else None,
     }
     if cfg.n_shared:
         Is = cfg.I_shared
-        g["dWs_gate"] = torch.empty(Is, d, dtype=torch.bfloat16, device=dev)
-        g["dWs_up"] = torch.empty(Is, d, dtype=torch.bfloat16, device=dev)
-        g["dWs_down"] = torch.empty(d, Is, dtype=torch.bfloat16, device=dev)
+        g["dWs_gate"] = torch.empty(Is, d, dtype=wdt, device=dev)
+        g["dWs_up"] = torch.empty(Is, d, dtype=wdt, device=dev)
+        g["dWs_down"] = torch.empty(d, Is, dtype=wdt, device=dev)
     else:
         g["dWs_gate"] = g["dWs_up"] = g["dWs_down"] = None
     return g

@@ -66,8 +66,9 @@ def test_replay_flag_moves_the_activations_from_saved_to_the_backward_workspace(
 
 def test_unknown_flag_bits_rejected(lib):
     a = ctypes.c_size_t()
-    c = _abi.make_config(512, 256, 128, 8, 2, flags=2)
-    assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(a), None, None) == 2
+    for bit in (4, 1 << 31):  # bits 0 and 1 are MOE_FLAG_REPLAY and MOE_FLAG_WGRAD_FP32
+        c = _abi.make_config(512, 256, 128, 8, 2, flags=bit)
+        assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(a), None, None) == 2
 
 
 @pytest.mark.parametrize("cfg,code", [
@@ -118,6 +119,22 @@ def test_misaligned_workspace_or_saved_state_rejected(lib):
                               fake + 128, None) == 1
     g = _abi.MoeGrads(fake, fake, fake, fake, 0, 0, 0, None, None)
     assert lib.moe_backward(ctypes.byref(c), fake, ctypes.byref(w), fake, fake + 64, fake, ctypes.byref(g),
+                            fake, None) == 1
+
+
+def test_fp32_weight_gradient_flag(lib):
+    """moe.h: MOE_FLAG_WGRAD_FP32 is a bf16-mode option (MXFP8 gives MOE_ERR_UNSUPPORTED),
+    and its fp32 gradient buffers must be 32-byte aligned (checked before any launch; the
+    placeholder addresses are never dereferenced)."""
+    sz = ctypes.c_size_t()
+    c = _abi.make_config(64, 128, 64, 4, 2, flags=_abi.MOE_FLAG_WGRAD_FP32)
+    assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(sz), None, None) == 0
+    m = _abi.make_config(64, 128, 128, 4, 2, precision=_abi.MOE_MXFP8, flags=_abi.MOE_FLAG_WGRAD_FP32)
+    assert lib.moe_workspace_size(ctypes.byref(m), ctypes.byref(sz), None, None) == 2
+    fake = 1 << 20
+    w = _abi.MoeWeights(fake, 0, fake, fake, fake, 0, 0, 0, None)
+    g = _abi.MoeGrads(fake, fake + 16, fake, fake, 0, 0, 0, None, None)
+    assert lib.moe_backward(ctypes.byref(c), fake, ctypes.byref(w), fake, fake, fake, ctypes.byref(g),
                             fake, None) == 1
 
 

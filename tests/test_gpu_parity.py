@@ -202,6 +202,23 @@ def test_replay_matches_saved_activations_bitwise(name):
             assert torch.equal(a["grads"][key], b["grads"][key]), key
 
 
+@pytest.mark.parametrize("name", ["ragged", "wide", "small_T", "pairs_leftover"])
+def test_fp32_weight_gradients_round_to_the_bf16_ones(name):
+    """MOE_FLAG_WGRAD_FP32 writes the fp32 accumulators the bf16 path rounds: rounded to bf16
+    (nearest even) they are bitwise the bf16 weight gradients, and nothing else changes.  The
+    shapes cover the three weight-gradient schedules and output row counts that are not a
+    multiple of the 128-row tile (I = 192, I_s = 320)."""
+    b = _run_layer(SHAPES[name])
+    f = _run_layer(SHAPES[name], flags=_abi.MOE_FLAG_WGRAD_FP32)
+    for n in ("dW_gate", "dW_up", "dW_down", "dWs_gate", "dWs_up", "dWs_down"):
+        if b["grads"][n] is None:
+            continue
+        assert f["grads"][n].dtype == torch.float32, n
+        assert torch.equal(f["grads"][n].to(torch.bfloat16), b["grads"][n]), n
+    assert torch.equal(f["dx"], b["dx"])
+    assert torch.equal(f["grads"]["dW_router"], b["grads"]["dW_router"])
+
+
 def test_inference_without_saved_state_matches_training_forward():
     shape = SHAPES["ragged"]
     a = _run_layer(shape, seed=2, backward=False)
