@@ -309,7 +309,10 @@ def main():
     ap.add_argument("--zipf", action="store_true", help="Zipf(1.2)-skewed router bias (the sweep's skewed routing)")
     ap.add_argument("--zero-experts", type=int, default=0, help="that many experts never chosen (bias -inf)")
     ap.add_argument("--replay", action="store_true",
-                    help="MOE_FLAG_REPLAY: save only the routing, recompute x rows, a and b in the backward")
+                    help="MOE_FLAG_REPLAY: save the routing and the shared expert's a, b; recompute the routed "
+                         "x rows, a and b in the backward")
+    ap.add_argument("--wgrad-fp32", action="store_true",
+                    help="MOE_FLAG_WGRAD_FP32: weight gradients written in fp32 (bf16 mode)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -335,7 +338,8 @@ def main():
     inp = make_inputs(s, seed=rank, device="cuda")
     cfg = _abi.make_config(s.T, s.d, s.I, s.E, s.k, s.n_shared, s.I_shared,
                            precision=_abi.MOE_MXFP8 if mx else _abi.MOE_BF16,
-                           flags=_abi.MOE_FLAG_REPLAY if args.replay else 0)
+                           flags=(_abi.MOE_FLAG_REPLAY if args.replay else 0)
+                           | (_abi.MOE_FLAG_WGRAD_FP32 if args.wgrad_fp32 else 0))
     if mx:
         layer.quantize_weights(cfg, inp)
     bufs = layer.MoEBuffers(cfg)
@@ -488,6 +492,7 @@ def main():
                        "n_shared": s.n_shared, "I_shared": s.I_shared, "tokens_per_gpu": s.T,
                        "parallelism": f"replicas x{world}",
                        "activations": "replayed in the backward" if args.replay else "saved",
+                       "weight_grads": "fp32" if args.wgrad_fp32 else "bf16",
                        "l2": "inputs larger than L2 (x 235 MB, expert weights 22.6 GB at dsv3); no flush"},
             "tflops": tflops, "pct_tensor_peak": tflops / t_burst,
             "pct_tensor_peak_sustained": tflops / t_sust, "tensor_peak_src": t_src,
