@@ -70,9 +70,8 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
  *   identical to those without the flag. */
 #define MOE_FLAG_REPLAY 1u
 /* MOE_FLAG_WGRAD_FP32: moe_backward writes dW_gate, dW_up, dW_down and dWs_*
- *   as fp32 (same shapes; each buffer 32-byte aligned) instead of bf16: the
- *   same fp32 accumulators without the final rounding, for callers that
- *   accumulate gradients in fp32.  bf16 mode only (with MOE_MXFP8 it gives
+ *   as fp32 (same shapes) instead of bf16: the same fp32 accumulators without
+ *   the final rounding, for callers that accumulate gradients in fp32.  bf16 mode only (with MOE_MXFP8 it gives
  *   MOE_ERR_UNSUPPORTED).  dW_router is fp32 either way. */
 #define MOE_FLAG_WGRAD_FP32 2u
 

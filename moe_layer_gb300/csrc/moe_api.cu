@@ -389,6 +389,19 @@ moe_status omap2(CUtensorMap* m32, CUtensorMap* m16, const void* base, int64_t r
   return tmap(m16, base, rows, cols, 64, 16);
 }
 
+// fp32 output maps (the weight gradients with MOE_FLAG_WGRAD_FP32): boxes of
+// 32 columns x 32 rows, 128 bytes per box row as in the bf16 maps.
+moe_status omap_f32(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+  return make_tmap_f32(m, base, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows), 32, 32) ? MOE_OK
+                                                                                                  : MOE_ERR_CUDA;
+}
+moe_status omap3_f32(CUtensorMap* m, const void* base, int64_t G, int64_t rows, int64_t cols) {
+  return make_tmap_f32_3d(m, base, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                          static_cast<uint64_t>(G), 32, 32)
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
 // Per-expert output [G, rows, cols]: a box never crosses into the next expert.
 moe_status omap3(CUtensorMap* m, const void* base, int64_t G, int64_t rows, int64_t cols) {
   if (!make_tmap_bf16_3d(m, base, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
@@ -837,10 +850,11 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     return MOE_ERR_INVALID_ARG;
   if (!g->dW_router || !g->dW_gate || !g->dW_up || !g->dW_down) return MOE_ERR_INVALID_ARG;
   if (s.S && (!g->dWs_gate || !g->dWs_up || !g->dWs_down)) return MOE_ERR_INVALID_ARG;
-  if (s.wgrad_f32) {  // fp32 weight gradients go out in 32-byte vector stores
-    for (const void* q : {g->dW_gate, g->dW_up, g->dW_down, g->dWs_gate, g->dWs_up, g->dWs_down})
-      if (reinterpret_cast<uintptr_t>(q) & 31u) return MOE_ERR_INVALID_ARG;
-  }
+  // the gradient buffers take TMA stores: 16-byte aligned (checked here, before anything runs)
+  const void* gbufs[] = {g->dW_router, g->d_topk_w, g->dW_gate, g->dW_up, g->dW_down,
+                         g->dWs_gate, g->dWs_up, g->dWs_down};
+  for (const void* q : gbufs)
+    if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Saved sv;
   carve_saved(const_cast<void*>(saved), s, sv, nullptr);
@@ -1030,8 +1044,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.M_out = d;
     p.N = I;
     p.wgrad_mode = wgrad_mode(s);
-    MOE_TRY(omap3(&p.tmO0, g->dW_down, s.E, s.d, s.I));
-    if (s.wgrad_f32) p.out_f32 = static_cast<float*>(g->dW_down);
+    p.wgrad_f32 = s.wgrad_f32 ? 1 : 0;
+    MOE_TRY(s.wgrad_f32 ? omap3_f32(&p.tmO0, g->dW_down, s.E, s.d, s.I) : omap3(&p.tmO0, g->dW_down, s.E, s.d, s.I));
     p.status = w.status;
     MOE_LAUNCH(PL_WGRAD_DOWN, st, launch_gemm(GK_WGRAD, p, grid_for(s.E * cdiv(s.d, kBM) * cdiv(s.I, kBN)), st));
   }
@@ -1046,8 +1060,9 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     p.N = d;
     p.wgrad_mode = wgrad_mode(s);
     p.a_col_off = half ? I : 0;
-    MOE_TRY(omap3(&p.tmO0, half ? g->dW_up : g->dW_gate, s.E, s.I, s.d));
-    if (s.wgrad_f32) p.out_f32 = static_cast<float*>(half ? g->dW_up : g->dW_gate);
+    void* dW = half ? g->dW_up : g->dW_gate;
+    p.wgrad_f32 = s.wgrad_f32 ? 1 : 0;
+    MOE_TRY(s.wgrad_f32 ? omap3_f32(&p.tmO0, dW, s.E, s.I, s.d) : omap3(&p.tmO0, dW, s.E, s.I, s.d));
     p.status = w.status;
     MOE_LAUNCH(half ? PL_WGRAD_UP : PL_WGRAD_GATE, st, launch_gemm(GK_WGRAD, p, grid_for(s.E * cdiv(s.I, kBM) * cdiv(s.d, kBN)), st));
   }
@@ -1061,8 +1076,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
       p.dense_rows = T;
       p.M_out = d;
       p.N = Is;
-      MOE_TRY(omap(&p.tmO0, g->dWs_down, s.d, s.Is));
-      if (s.wgrad_f32) p.out_f32 = static_cast<float*>(g->dWs_down);
+      p.wgrad_f32 = s.wgrad_f32 ? 1 : 0;
+      MOE_TRY(s.wgrad_f32 ? omap_f32(&p.tmO0, g->dWs_down, s.d, s.Is) : omap(&p.tmO0, g->dWs_down, s.d, s.Is));
       p.status = w.status;
       MOE_LAUNCH(PL_WGRAD_SHARED_DOWN, st, launch_gemm(GK_WGRAD, p, grid_for(cdiv(s.d, kBM) * cdiv(s.Is, kBN)), st));
     }
@@ -1075,8 +1090,9 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
       p.M_out = Is;
       p.N = d;
       p.a_col_off = half ? Is : 0;
-      MOE_TRY(omap(&p.tmO0, half ? g->dWs_up : g->dWs_gate, s.Is, s.d));
-      if (s.wgrad_f32) p.out_f32 = static_cast<float*>(half ? g->dWs_up : g->dWs_gate);
+      void* dWs = half ? g->dWs_up : g->dWs_gate;
+      p.wgrad_f32 = s.wgrad_f32 ? 1 : 0;
+      MOE_TRY(s.wgrad_f32 ? omap_f32(&p.tmO0, dWs, s.Is, s.d) : omap(&p.tmO0, dWs, s.Is, s.d));
       p.status = w.status;
       MOE_LAUNCH(half ? PL_WGRAD_SHARED_UP : PL_WGRAD_SHARED_GATE, st, launch_gemm(GK_WGRAD, p, grid_for(cdiv(s.Is, kBM) * cdiv(s.d, kBN)), st));
     }

@@ -477,5 +477,18 @@ __device__ __forceinline__ void stage_row_sw128(uint32_t box, int row, const flo
                  : "memory");
   }
 }
+// Stages 32 floats of row `row` into a [32 rows x 128 B] fp32 box with the
+// 128-byte swizzle (16-byte chunk j of the row at chunk j ^ (row % 8)).
+__device__ __forceinline__ void stage_row_sw128_f32(uint32_t box, int row, const float* v) {
+  const uint32_t base = box + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t addr = base + ((static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(row) & 7u)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(__float_as_uint(v[4 * j])),
+                 "r"(__float_as_uint(v[4 * j + 1])), "r"(__float_as_uint(v[4 * j + 2])),
+                 "r"(__float_as_uint(v[4 * j + 3]))
+                 : "memory");
+  }
+}
 
 }  // namespace moe

@@ -256,9 +256,9 @@ struct GemmParams {
   // one SM), 1 every tile on one SM (short K), 2 every tile on one SM with
   // the wide epilogue (the shortest K).
   int wgrad_mode;
-  // Weight gradients: when set, the output in fp32 ([G, M_out, N], or
-  // [M_out, N] for dense rows; 32-byte aligned) instead of bf16 through tmO0.
-  float* out_f32;
+  // Weight gradients: nonzero when tmO0 maps an fp32 output (boxes of 32
+  // columns x 32 rows) instead of a bf16 one (64 x 32).
+  int wgrad_f32;
 };
 
 template <int EPI>
@@ -815,21 +815,18 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
           for (int i = 0; i < 64; ++i) v[i] = 0.f;
         }
       };
-      if (p.out_f32) {  // fp32 weight gradients: this lane's row in 256-bit stores
-        const int row = r0 + lane;
-        const long long grow = (p.dense_rows > 0 ? 0LL : static_cast<long long>(t.e) * p.M_out) + row;
+      if (p.wgrad_f32) {  // fp32 weight gradients: two 32-column fp32 boxes per 64 columns
         for (int c0 = cbeg; c0 < cend && t.n0 + c0 < p.N; c0 += 64) {
           float v[64];
           load64(c0, v);
-          if (row < p.M_out) {
-            float* dst = p.out_f32 + grow * p.N + t.n0 + c0;
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              st_global_v8(dst + 8 * q,
-                           make_uint4(__float_as_uint(v[8 * q]), __float_as_uint(v[8 * q + 1]),
-                                      __float_as_uint(v[8 * q + 2]), __float_as_uint(v[8 * q + 3])),
-                           make_uint4(__float_as_uint(v[8 * q + 4]), __float_as_uint(v[8 * q + 5]),
-                                      __float_as_uint(v[8 * q + 6]), __float_as_uint(v[8 * q + 7])));
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t box = stg.begin();
+            stage_row_sw128_f32(box, lane, v + 32 * h);
+            if (p.dense_rows > 0)
+              stg.store2d(&p.tmO0, box, t.n0 + c0 + 32 * h, r0);
+            else
+              stg.store3d(&p.tmO0, box, t.n0 + c0 + 32 * h, r0, t.e);
           }
         }
       } else {

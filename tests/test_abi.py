@@ -123,9 +123,9 @@ def test_misaligned_workspace_or_saved_state_rejected(lib):
 
 
 def test_fp32_weight_gradient_flag(lib):
-    """moe.h: MOE_FLAG_WGRAD_FP32 is a bf16-mode option (MXFP8 gives MOE_ERR_UNSUPPORTED),
-    and its fp32 gradient buffers must be 32-byte aligned (checked before any launch; the
-    placeholder addresses are never dereferenced)."""
+    """moe.h: MOE_FLAG_WGRAD_FP32 is a bf16-mode option (MXFP8 gives MOE_ERR_UNSUPPORTED);
+    gradient buffers, like every pointer, must be 16-byte aligned, checked before any launch
+    (the placeholder addresses are never dereferenced)."""
     sz = ctypes.c_size_t()
     c = _abi.make_config(64, 128, 64, 4, 2, flags=_abi.MOE_FLAG_WGRAD_FP32)
     assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(sz), None, None) == 0
@@ -133,7 +133,7 @@ def test_fp32_weight_gradient_flag(lib):
     assert lib.moe_workspace_size(ctypes.byref(m), ctypes.byref(sz), None, None) == 2
     fake = 1 << 20
     w = _abi.MoeWeights(fake, 0, fake, fake, fake, 0, 0, 0, None)
-    g = _abi.MoeGrads(fake, fake + 16, fake, fake, 0, 0, 0, None, None)
+    g = _abi.MoeGrads(fake, fake + 8, fake, fake, 0, 0, 0, None, None)
     assert lib.moe_backward(ctypes.byref(c), fake, ctypes.byref(w), fake, fake, fake, ctypes.byref(g),
                             fake, None) == 1
 
