@@ -23,16 +23,50 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// Selection order: a candidate (logit v, expert e) comes before another when
+// its logit is larger, or equal with a lower expert index.
+__device__ __forceinline__ bool beats(float va, int ea, float vb, int eb) {
+  return va > vb || (va == vb && ea < eb);
+}
+
+// Sorts N candidates into selection order with Batcher's odd-even merge
+// network (19 compare-exchanges for N = 8, 63 for N = 16), in registers.
+template <int N>
+__device__ __forceinline__ void sort_candidates(float (&v)[N], int (&e)[N]) {
+#pragma unroll
+  for (int p = 1; p < N; p <<= 1)
+#pragma unroll
+    for (int kk = p; kk >= 1; kk >>= 1)
+#pragma unroll
+      for (int j = kk % p; j + kk < N; j += 2 * kk)
+#pragma unroll
+        for (int i = 0; i < kk && i + j + kk < N; ++i)
+          if ((i + j) / (2 * p) == (i + j + kk) / (2 * p) && beats(v[i + j + kk], e[i + j + kk], v[i + j], e[i + j])) {
+            const float tv = v[i + j];
+            v[i + j] = v[i + j + kk];
+            v[i + j + kk] = tv;
+            const int te = e[i + j];
+            e[i + j] = e[i + j + kk];
+            e[i + j + kk] = te;
+          }
+}
+
 // Softmax + top-k for the tokens of one chunk (kTopkWarpTokens tokens per
-// warp: the selection is a chain of dependent shuffles, so the kernel is
-// latency bound and wants many warps per SM).
+// warp).  Lane l holds the logits of experts l, l + 32, ... (NS slots, NS >=
+// E / 32), sorts them once into selection order, and each of the k rounds
+// takes the best of the 32 lanes' heads (a shuffle reduction) and moves the
+// winning lane's list up by one.  A NaN logit becomes -inf with an index past
+// E: it loses to every real logit, and selecting it (only NaN left) records
+// MOE_ERR_DEVICE.
 // Selection: logits descending, equal logits to the lower expert index.
 // Weights: exp(l_j - l_max) / sum over the k selected (softmax over all E
 // logits restricted to the selection and renormalized).
 constexpr int kTopkWarps = 16;
 constexpr int kTopkWarpTokens = kChunkTokens / kTopkWarps;
 static_assert(kChunkTokens % kTopkWarps == 0, "whole tokens per warp");
-__global__ void __launch_bounds__(kTopkWarps * 32)
+constexpr int kNanIndex = 1 << 30;  // or-ed into a NaN logit's index
+template <int NS>  // two blocks per SM with 8 slots; 16 need more registers than that leaves
+__global__ void __launch_bounds__(kTopkWarps * 32, NS <= 8 ? 2 : 1)
     topk_count_kernel(const float* __restrict__ logits, int T, int E, int k,
                       int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                       int32_t* __restrict__ chunk_counts, int* status) {
@@ -40,44 +74,37 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nS = (E + 31) >> 5;
   const int t0 = blockIdx.x * kChunkTokens + warp * kTopkWarpTokens;
   for (int i = 0; i < kTopkWarpTokens; ++i) {
     const int t = t0 + i;
     if (t >= T) break;
     const float* lr = logits + static_cast<size_t>(t) * E;
-    float v[16];
-    uint32_t taken = 0;
+    float v[NS];
+    int ei[NS];
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
+    for (int s = 0; s < NS; ++s) {
       const int e = lane + 32 * s;
-      if (s < nS && e < E) {
-        v[s] = __ldg(lr + e);
+      if (e < E) {
+        const float x = __ldg(lr + e);
+        const bool nan = x != x;
+        v[s] = nan ? -INFINITY : x;
+        ei[s] = nan ? (e | kNanIndex) : e;
       } else {
         v[s] = -INFINITY;
-        taken |= 1u << s;
+        ei[s] = INT_MAX;
       }
     }
+    sort_candidates<NS>(v, ei);
     int my_e = 0;
     float my_v = 0.f;
     for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = INT_MAX;
-#pragma unroll
-      for (int s = 0; s < 16; ++s) {
-        if (!((taken >> s) & 1u)) {
-          const int e = lane + 32 * s;
-          if (v[s] > bv || (v[s] == bv && e < be)) {
-            bv = v[s];
-            be = e;
-          }
-        }
-      }
+      float bv = v[0];
+      int be = ei[0];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         const float ov = __shfl_xor_sync(kFull, bv, off);
         const int oe = __shfl_xor_sync(kFull, be, off);
-        if (ov > bv || (ov == bv && oe < be)) {
+        if (beats(ov, oe, bv, be)) {
           bv = ov;
           be = oe;
         }
@@ -85,8 +112,14 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
       if (be >= E) {  // only reachable with NaN logits
         if (lane == 0) atomicCAS(status, 0, kDevBadValue);
         be = 0;
-      } else if ((be & 31) == lane) {
-        taken |= 1u << (be >> 5);
+      } else if (ei[0] == be) {  // this lane's head was taken: move its list up
+#pragma unroll
+        for (int s = 0; s + 1 < NS; ++s) {
+          v[s] = v[s + 1];
+          ei[s] = ei[s + 1];
+        }
+        v[NS - 1] = -INFINITY;
+        ei[NS - 1] = INT_MAX;
       }
       if (lane == j) {
         my_e = be;
@@ -301,8 +334,12 @@ __global__ void __launch_bounds__(kChunkWarps * 32)
 cudaError_t launch_topk_count(const float* logits, int T, int E, int k, int32_t* topk_idx,
                               float* topk_w, int32_t* chunk_counts, int* status, cudaStream_t st) {
   const int nchunk = (T + kChunkTokens - 1) / kChunkTokens;
-  topk_count_kernel<<<nchunk, kTopkWarps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w,
-                                                        chunk_counts, status);
+  if (E <= 256)
+    topk_count_kernel<8><<<nchunk, kTopkWarps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w, chunk_counts,
+                                                             status);
+  else
+    topk_count_kernel<16><<<nchunk, kTopkWarps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w, chunk_counts,
+                                                              status);
   return cudaGetLastError();
 }
 

@@ -29,7 +29,7 @@ def _cuda(inp):
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
-def _route_on_logits(logits_cpu, k):
+def _route_on_logits(logits_cpu, k, expect_status=0):
     T, E = logits_cpu.shape
     cfg = _abi.make_config(T, 64, 64, E, k)
     bufs = layer.MoEBuffers(cfg, training=False)
@@ -46,7 +46,7 @@ def _route_on_logits(logits_cpu, k):
     _abi.moe_route_topk(cfg, None, None, None, lg, None, out["topk_idx"], out["topk_w"], out["counts"],
                         out["offsets"], out["perm_token"], out["route_row"], bufs.fwd_ws)
     torch.cuda.synchronize()
-    assert _abi.moe_read_device_status(bufs.fwd_ws) == 0
+    assert _abi.moe_read_device_status(bufs.fwd_ws) == expect_status
     return {k_: v.cpu().numpy() for k_, v in out.items()}
 
 
@@ -67,6 +67,27 @@ def test_routing_bit_exact_on_given_logits(T, E, k, ties):
     assert (g["perm_token"] == perm_token).all()
     assert (g["route_row"] == route_row).all()
     np.testing.assert_allclose(g["topk_w"], w, rtol=1e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("E", [64, 300])
+def test_nan_logits_are_passed_over_and_an_all_nan_token_is_reported(E):
+    """moe.h / the top-k kernel: a NaN logit loses to every real logit, so its token routes as if
+    that logit were below all others; a token with nothing but NaN left to choose records
+    MOE_ERR_DEVICE (5) in the status word.  E = 64 and 300 cover both register layouts."""
+    T, k = 96, 6
+    logits = random_logits(T, E, seed=11 + E, ties=True)
+    nan_cols = [0, 7, 33, E - 1]
+    ref = logits.clone()
+    ref[5, nan_cols] = -float("inf")
+    ref[6, 1::2] = -float("inf")
+    logits[5, nan_cols] = float("nan")
+    logits[6, 1::2] = float("nan")  # half the experts NaN, the rest still enough
+    g = _route_on_logits(logits, k)
+    idx, _ = O.topk_route(ref.numpy().astype(np.float64), k)
+    assert (g["topk_idx"] == idx).all()
+    bad = logits[:4].clone()
+    bad[2, :] = float("nan")
+    _route_on_logits(bad, k, expect_status=5)
 
 
 def _run_layer(shape, seed=0, backward=True, flags=0):
