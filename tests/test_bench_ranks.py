@@ -58,3 +58,21 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
                               ref_tokens=1, warmup=0, steps=1, gpus=2)
     assert bench.run_reference(args) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_one_contract_line_on_rank_zero(monkeypatch, capsys):
+    import json
+    monkeypatch.setenv("RANK", "0")
+    args = argparse.Namespace(workload="tiny", tokens=0, experts=0, zipf=False, zero_experts=0,
+                              ref_tokens=2, warmup=0, steps=1, gpus=1)
+    assert bench.run_reference(args) == 0
+    lines = capsys.readouterr().out.strip().splitlines()
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "tokens/s" and line["higher_is_better"] is True and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s",
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert line["config"]["tokens_per_step"] == 2
