@@ -94,8 +94,12 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// grid (E, ceil(d / 512)); each thread owns two adjacent columns
-constexpr int kRwThreads = 256;
+// dW_router[e, :] = sum over the rows routed to e of dlogit(row) * x[token(row), :]: only the
+// chosen logits carry a gradient, so the product is a gather over each expert's rows.
+// grid (E, ceil(d / 1024)); each thread owns eight adjacent columns (one 16-byte load per row)
+// and sums the rows in their permuted order, four gathers in flight.
+constexpr int kRwThreads = 128;
+constexpr int kRwCols = 8 * kRwThreads;
 __global__ void __launch_bounds__(kRwThreads)
     router_wgrad_kernel(const float* __restrict__ dl_row, const int32_t* __restrict__ perm_token_pad,
                         const int32_t* __restrict__ row_start, const int32_t* __restrict__ counts,
@@ -103,10 +107,13 @@ __global__ void __launch_bounds__(kRwThreads)
   __shared__ int s_tok[kRwThreads];
   __shared__ float s_dl[kRwThreads];
   const int e = blockIdx.x;
-  const int c = (blockIdx.y * kRwThreads + threadIdx.x) * 2;
+  const int c = blockIdx.y * kRwCols + threadIdx.x * 8;
   const int r0 = __ldg(row_start + e);
   const int n = __ldg(counts + e);
-  float a0 = 0.f, a1 = 0.f;
+  const __nv_bfloat16* xc = x + c;
+  float a[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) a[j] = 0.f;
   for (int base = 0; base < n; base += kRwThreads) {
     const int m = min(kRwThreads, n - base);
     __syncthreads();
@@ -116,17 +123,31 @@ __global__ void __launch_bounds__(kRwThreads)
     }
     __syncthreads();
     if (c < d) {
-      for (int i = 0; i < m; ++i) {
-        const uint32_t w =
-            __ldg(reinterpret_cast<const unsigned int*>(x + static_cast<size_t>(s_tok[i]) * d + c));
-        a0 += s_dl[i] * bf16lo(w);
-        a1 += s_dl[i] * bf16hi(w);
+      int i = 0;
+      for (; i + 4 <= m; i += 4) {
+        float u[4][8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ld8(xc + static_cast<size_t>(s_tok[i + q]) * d, u[q]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float g = s_dl[i + q];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) a[j] += g * u[q][j];
+        }
+      }
+      for (; i < m; ++i) {
+        float u[8];
+        ld8(xc + static_cast<size_t>(s_tok[i]) * d, u);
+        const float g = s_dl[i];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] += g * u[j];
       }
     }
   }
   if (c < d) {
-    dW[static_cast<size_t>(e) * d + c] = a0;
-    dW[static_cast<size_t>(e) * d + c + 1] = a1;
+    float4* out = reinterpret_cast<float4*>(dW + static_cast<size_t>(e) * d + c);
+    out[0] = make_float4(a[0], a[1], a[2], a[3]);
+    out[1] = make_float4(a[4], a[5], a[6], a[7]);
   }
 }
 
@@ -230,7 +251,7 @@ cudaError_t launch_router_wgrad(const float* dl_row, const int32_t* perm_token_p
                                 const int32_t* row_start, const int32_t* counts,
                                 const __nv_bfloat16* x, int E, int d, float* dW_router,
                                 cudaStream_t st) {
-  dim3 grid(E, (d + 2 * kRwThreads - 1) / (2 * kRwThreads));
+  dim3 grid(E, (d + kRwCols - 1) / kRwCols);
   router_wgrad_kernel<<<grid, kRwThreads, 0, st>>>(dl_row, perm_token_pad, row_start, counts, x, d,
                                                    dW_router);
   return cudaGetLastError();
