@@ -23,7 +23,7 @@ Sources (titles and sections of the pages that define the method):
   [Paper] "Mixture-of-Kittens: MoE Megakernel for NVL72s", section 2.1: outputs
           are summed using normalized router weights.
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings taken where the pages are silent:
   R1  the shared expert enters the sum with weight 1;
   R2  router weights: softmax over all E logits, restricted to the k selected
       experts and renormalized (equal to a softmax over the selected logits);
@@ -167,7 +167,7 @@ def _ffn(x_rows, w_gate, w_up, w_down, mxfp8=False):
 # ---------------------------------------------------------------- MXFP8
 # The MX block format (MXFP8 with E4M3 elements and E8M0 shared scales) that
 # the pages' MXFP8 mode uses [Blog, "MXFP8 support"; the MX format reference
-# the pages cite].  Reading taken here (listed in the design doc):
+# the pages cite].  Reading taken here:
 #   * a block is 32 consecutive elements along the reduction axis of the GEMM
 #     the operand feeds;
 #   * shared scale X = 2^(floor(log2(amax)) - 8), 8 being the largest exponent

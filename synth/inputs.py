@@ -5,7 +5,7 @@ none of the layer's arithmetic.  Both the CUDA path (tests, bench) and the CPU
 oracle's checks take their inputs from here.
 
 Workloads (shapes of the DeepSeek-V3-style layers the Mixture-of-Kittens pages
-benchmark; distributions are fixed here and restated in the design doc):
+benchmark; the value distributions are fixed here):
 
   tiny   T=512,   d=256,  I=128,  E=8,   k=2, one shared expert (I_s=128),
          x ~ N(0,1), every weight ~ N(0, 0.02)
