@@ -34,7 +34,11 @@ Readings taken where the pages are silent:
       so into W_router and x); an optional router bias is a constant.
 
 Parity pins: every function here is checked by tests/test_oracle_pins.py
-against brute force, closed forms, library routines or finite differences.
+against brute force, closed forms, library routines or finite differences;
+the MXFP8 composition (which GEMM operand is quantized along which axis, the
+token blocks of the weight gradients, the router and shared expert left in
+full precision) by tests/test_oracle_mx_composition.py, with operands exactly
+representable along one axis only, and planted mistakes that those pins catch.
 """
 from __future__ import annotations
 
