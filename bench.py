@@ -18,7 +18,13 @@ Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead
 dsv3_mxfp8 runs the same layer with the routed experts in MXFP8.  Its weights
 are quantized once per weight update (moe_quantize_weights_mxfp8); that pass is
 timed on its own and reported as "weight_quant", together with the throughput
-of a step that includes it.
+of a step that includes it.  Its tensor peak is measured in the same run
+(measure_mxfp8_peak).
+
+With the default workload the line also carries, under "workloads", the
+DSV3-shaped MXFP8 layer and the Qwen3-235B-shaped layer (Zipf routing), each
+timed the same way after the headline's buffers are freed (--no-extra skips
+them); the headline value stays the DSV3 BF16 one.
 """
 from __future__ import annotations
 
@@ -38,8 +44,65 @@ if ROOT not in sys.path:
 METRIC = "MoE layer tokens/s and TFLOPS (fwd, fwd+bwd) at 1 GB300, % of tensor peak"
 
 
-# Nominal dense FP8 (and MXFP8) / BF16 tensor rate ratio (4.5 vs 2.25 PFLOP/s).
+# Nominal dense FP8 (and MXFP8) / BF16 tensor rate ratio (4.5 vs 2.25 PFLOP/s):
+# the fallback when no block-scaled FP8 GEMM can be timed on the device.
 FP8_OVER_BF16 = 2.0
+
+
+def measure_mxfp8_peak(n=8192, sustain_s=4.0):
+    """Tensor peak for the MXFP8 GEMMs, measured on this device the way the
+    bf16 denominators are: a library GEMM of n^3 (2 n^3 flops) on E4M3 operands
+    with E8M0 scales per 32 elements along K (torch._scaled_mm, cuBLASLt),
+    best of 10 timed singly (burst) and back to back for sustain_s seconds
+    (sustained).  Falls back to per-tensor-scaled E4M3 (the same tensor rate)
+    where the block-scaled form is not available.  Returns a dict, or None."""
+    import torch
+    dev = "cuda"
+    g = torch.Generator(device=dev).manual_seed(0)
+    a = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn).t()  # column-major [K, N]
+    nsf = ((n + 127) // 128 * 128) * ((n // 32 + 3) // 4 * 4)
+    forms = []
+    if hasattr(torch, "float8_e8m0fnu"):
+        sf = torch.full((nsf,), 127, dtype=torch.uint8, device=dev).view(torch.float8_e8m0fnu)
+        forms.append(("mxfp8 (e4m3, e8m0 scales per 32 along K)", sf, sf))
+    one = torch.ones((), dtype=torch.float32, device=dev)
+    forms.append(("fp8 e4m3, per-tensor scale", one, one))
+    for label, sa, sb in forms:
+        try:
+            fn = lambda: torch._scaled_mm(a, b, sa, sb, out_dtype=torch.bfloat16)
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+        except Exception:
+            continue
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        reps, t_total = 0, 0.0
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        per = max(1, int(sustain_s * 1e3 / max(best, 1e-3) / 4))
+        t0 = time.perf_counter()
+        e0.record()
+        while time.perf_counter() - t0 < sustain_s:
+            for _ in range(per):
+                fn()
+            reps += per
+            torch.cuda.synchronize()
+        e1.record()
+        torch.cuda.synchronize()
+        t_total = e0.elapsed_time(e1)
+        fl = 2.0 * n ** 3
+        return {"form": label, "tflops": fl / (best * 1e-3) / 1e12,
+                "tflops_sustained": fl * reps / (t_total * 1e-3) / 1e12,
+                "how": f"torch._scaled_mm {n}^3 (2 n^3 flops), bf16 out: best of 10 (burst) and "
+                       f"{reps} back to back in {t_total / 1e3:.1f} s (sustained)"}
+    return None
 
 
 def _peaks():
@@ -52,10 +115,13 @@ def _peaks():
         return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
 
 
-def _tensor_peaks(peaks, mxfp8):
+def _tensor_peaks(peaks, mxfp8, mx_peak=None):
     """(burst, sustained, label) tensor peaks for the routed GEMMs' dtype."""
     if not mxfp8:
         return peaks["bf16"], peaks["bf16_sustained"], peaks["src"] + " bf16"
+    if mx_peak:
+        return (mx_peak["tflops"], mx_peak["tflops_sustained"],
+                f"measured in this run: {mx_peak['form']}, {mx_peak['how']}")
     return (peaks["bf16"] * FP8_OVER_BF16, peaks["bf16_sustained"] * FP8_OVER_BF16,
             peaks["src"] + f" bf16 x nominal mxfp8/bf16 ratio {FP8_OVER_BF16:g}")
 
@@ -236,6 +302,26 @@ def _cpu_cores():
         return os.cpu_count() or 1
 
 
+def _cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
 def cpu_baseline(inp, s, n_tokens, rounds, seed=1, mxfp8=False):
     """Oracle forward+backward on `rounds` independent random samples of
     `n_tokens` tokens each (each round upcasts only the experts its tokens
@@ -249,11 +335,13 @@ def cpu_baseline(inp, s, n_tokens, rounds, seed=1, mxfp8=False):
         _oracle_step(inp, s, tokens, mxfp8)
         dt += time.perf_counter() - t0
     n = n_tokens * rounds
-    return {"value": n / dt, "unit": "tokens/s", "cores": _cpu_cores(), "kind": "oracle",
+    return {"value": n / dt, "unit": "tokens/s", "cores": _cpu_cores(), "cpu": _cpu_model(), "kind": "oracle",
+            "extrapolated": True,
             "sample": f"float64 numpy oracle forward+backward{' (MXFP8 emulation)' if mxfp8 else ''}, "
                       f"{rounds} rounds of {n_tokens} random tokens "
                       f"of the same workload ({n} tokens, expert weights upcast on first use per round), "
-                      f"{dt:.1f} s; numpy BLAS default threading"}
+                      f"{dt:.1f} s; tokens/s extrapolated linearly from that sample (per-token cost); "
+                      f"numpy BLAS default threading"}
 
 
 def run_reference(args):
@@ -282,8 +370,10 @@ def run_reference(args):
         "config": {"workload": desc, "T": s.T, "d": s.d, "I": s.I, "E": s.E, "top_k": s.k,
                    "n_shared": s.n_shared, "I_shared": s.I_shared, "tokens_per_step": per_step},
         "tflops": value * 3 * _flops(s) / 1e12,
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cpu_cores(), "kind": "oracle",
-                         "sample": f"{per_step} random tokens per step, oracle forward+backward"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cpu_cores(), "cpu": _cpu_model(),
+                         "kind": "oracle", "extrapolated": True,
+                         "sample": f"{per_step} random tokens per step, oracle forward+backward; tokens/s "
+                                   f"extrapolated linearly from that sample"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -301,6 +391,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=0, help="override T (scaled-down profiling runs)")
     ap.add_argument("--experts", type=int, default=0, help="override E (scaled-down profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="with the default workload, skip the MXFP8 and Qwen3-shaped workloads measured after it")
     ap.add_argument("--cpu-tokens", type=int, default=4, help="oracle tokens per cpu_baseline round (0 = skip)")
     ap.add_argument("--cpu-rounds", type=int, default=4, help="cpu_baseline rounds")
     ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per reference step")
@@ -321,8 +413,7 @@ def main():
     import torch
     import torch.distributed as dist
 
-    from moe_layer_gb300 import _abi, layer
-    from synth.inputs import make_inputs
+    from moe_layer_gb300 import _abi
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -331,15 +422,69 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     ranks = _Ranks(world, "cuda")
-    barrier, max_over_ranks = ranks.barrier, ranks.max
 
     _abi.load()
-    s, desc, mx = _workload(args.workload, args.tokens, args.experts, args.zipf, args.zero_experts)
+    head = measure_workload(args, args.workload, world, rank, local, ranks, full=True)
+    # The other workloads the layer is benchmarked on, measured in the same run
+    # so that the printed line carries them too (the headline stays the first).
+    extras = {}
+    plain = not (args.tokens or args.experts or args.zipf or args.zero_experts or args.replay or args.wgrad_fp32)
+    if plain and args.workload == "dsv3" and not args.no_extra:
+        for name in ("dsv3_mxfp8", "qwen3"):
+            torch.cuda.empty_cache()
+            extras[name] = measure_workload(args, name, world, rank, local, ranks, full=False)
+
+    if rank == 0:
+        s = head.pop("_shape")
+        line = {
+            "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8" if head["mx"] else "bf16", "data": "synthetic",
+            "config": {"workload": head["workload"], "T": s.T, "d": s.d, "I": s.I, "E": s.E, "top_k": s.k,
+                       "n_shared": s.n_shared, "I_shared": s.I_shared, "tokens_per_gpu": s.T,
+                       "parallelism": f"replicas x{world}",
+                       "activations": "replayed in the backward" if args.replay else "saved",
+                       "weight_grads": "fp32" if args.wgrad_fp32 else "bf16",
+                       "l2": "inputs larger than L2 (x 235 MB, expert weights 22.6 GB at dsv3); no flush"},
+        }
+        for key in ("tflops", "pct_tensor_peak", "pct_tensor_peak_sustained", "tensor_peak_src", "weight_quant",
+                    "fwd", "roofline", "kernels_ms_per_step", "kernel_share", "gpu_launches", "e2e",
+                    "cpu_baseline", "clocks"):
+            line[key] = head.get(key)
+        if extras:
+            line["workloads"] = {}
+            for name, r in extras.items():
+                r.pop("_shape", None)
+                r.pop("mx", None)
+                line["workloads"][name] = r
+            line["gpu_launches_all_workloads"] = head["gpu_launches"] + sum(r["gpu_launches"] for r in extras.values())
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+_MX_PEAK = {}
+
+
+def measure_workload(args, name, world, rank, local, ranks, full):
+    """Times forward+backward steps of workload `name` (and the forward alone)
+    through the C ABI on resident inputs; with `full`, also the end-to-end step
+    with host copies and the CPU oracle baseline.  Returns a dict of results
+    (the step's buffers are freed on return)."""
+    import torch
+
+    from moe_layer_gb300 import _abi, layer
+    from synth.inputs import make_inputs
+
+    barrier, max_over_ranks = ranks.barrier, ranks.max
+    tok_override = (args.tokens, args.experts, args.zipf, args.zero_experts) if full else (0, 0, False, 0)
+    s, desc, mx = _workload(name, *tok_override)
     inp = make_inputs(s, seed=rank, device="cuda")
     cfg = _abi.make_config(s.T, s.d, s.I, s.E, s.k, s.n_shared, s.I_shared,
                            precision=_abi.MOE_MXFP8 if mx else _abi.MOE_BF16,
-                           flags=(_abi.MOE_FLAG_REPLAY if args.replay else 0)
-                           | (_abi.MOE_FLAG_WGRAD_FP32 if args.wgrad_fp32 else 0))
+                           flags=((_abi.MOE_FLAG_REPLAY if args.replay else 0)
+                                  | (_abi.MOE_FLAG_WGRAD_FP32 if args.wgrad_fp32 else 0)) if full else 0)
     if mx:
         layer.quantize_weights(cfg, inp)
     bufs = layer.MoEBuffers(cfg)
@@ -370,7 +515,7 @@ def main():
     torch.cuda.synchronize()
     st = _abi.moe_read_device_status(bufs.fwd_ws) or _abi.moe_read_device_status(bufs.bwd_ws)
     if st:
-        raise RuntimeError(f"device status {st} after warm-up")
+        raise RuntimeError(f"device status {st} after warm-up ({name})")
 
     # forward + backward: the headline, with per-kernel events and clock samples
     sampler = ClockSampler(local)
@@ -389,11 +534,13 @@ def main():
     wq = None
     if mx:  # the once-per-weight-update quantization pass, timed on its own
         ms_wq = max_over_ranks(timed(lambda: layer.quantize_weights(cfg, inp), args.steps))
+        if "peak" not in _MX_PEAK:
+            _MX_PEAK["peak"] = measure_mxfp8_peak()
 
     tokens = s.T * world
     flops_tok = _flops(s)
     peaks = _peaks()
-    t_burst, t_sust, t_src = _tensor_peaks(peaks, mx)
+    t_burst, t_sust, t_src = _tensor_peaks(peaks, mx, _MX_PEAK.get("peak") if mx else None)
     if mx:
         wq = {"ms": ms_wq, "per": "weight update",
               "value_incl": tokens / ((ms + ms_wq) * 1e-3), "unit": "tokens/s",
@@ -411,18 +558,21 @@ def main():
     n_top, nk_top, ms_top = prof[top]
     fl = _kernel_flops(top, s)
     roofline = None
+    scaled = any(tok_override)
     if fl is not None:
         achieved = fl / (ms_top / n_top * 1e-3) / 1e12
-        traffic = NCU_TRAFFIC.get((args.workload, top)) if not (args.tokens or args.experts) else None
+        traffic = NCU_TRAFFIC.get((name, top)) if not scaled else None
         roofline = {"kernel": top, "bound": "tensor", "achieved": achieved,
                     "peak": t_sust, "unit": "TFLOP/s",
                     "frac": achieved / t_sust, "traffic": traffic,
                     "algorithmic_flops_per_launch": fl,
                     "kernels_per_launch": nk_top / n_top,
                     "peak_src": t_src + " sustained (kernel timed inside a long step)"}
+        if mx:
+            roofline["frac_of_burst"] = achieved / t_burst
 
     e2e = None
-    if not args.no_e2e:
+    if full and not args.no_e2e:
         xh = inp["x"].cpu().pin_memory()
         dyh = inp["dy"].cpu().pin_memory()
         yh = torch.empty(s.T, s.d, dtype=torch.bfloat16).pin_memory()
@@ -473,43 +623,40 @@ def main():
                "d2h_bytes_per_step": 2 * nb, "ms_per_step": ms_e2e}
 
     cpu = None
-    if rank == 0 and world == 1 and args.cpu_tokens > 0:
+    if full and rank == 0 and world == 1 and args.cpu_tokens > 0:
         if mx and not args.cpu_mx:
             # The MXFP8 oracle round-trips every expert weight it touches
             # (about 15 s per [2048, 7168] matrix on one core, 48 per token).
-            cpu = {"value": None, "unit": "tokens/s", "cores": _cpu_cores(), "kind": "oracle",
+            cpu = {"value": None, "unit": "tokens/s", "cores": _cpu_cores(), "cpu": _cpu_model(), "kind": "oracle",
                    "sample": "not timed by default: the MXFP8 oracle takes about 11 min per token "
                              "(--cpu-mx --cpu-tokens 1 --cpu-rounds 1 times one token)"}
         else:
             cpu = cpu_baseline(inp, s, args.cpu_tokens, args.cpu_rounds, mxfp8=mx)
 
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "mxfp8" if mx else "bf16", "data": "synthetic",
-            "config": {"workload": desc, "T": s.T, "d": s.d, "I": s.I, "E": s.E, "top_k": s.k,
-                       "n_shared": s.n_shared, "I_shared": s.I_shared, "tokens_per_gpu": s.T,
-                       "parallelism": f"replicas x{world}",
-                       "activations": "replayed in the backward" if args.replay else "saved",
-                       "weight_grads": "fp32" if args.wgrad_fp32 else "bf16",
-                       "l2": "inputs larger than L2 (x 235 MB, expert weights 22.6 GB at dsv3); no flush"},
-            "tflops": tflops, "pct_tensor_peak": tflops / t_burst,
-            "pct_tensor_peak_sustained": tflops / t_sust, "tensor_peak_src": t_src,
-            "weight_quant": wq,
-            "fwd": {"value": fwd_value, "unit": "tokens/s", "ms": ms_fwd,
-                    "tflops": fwd_value * flops_tok / 1e12},
-            "roofline": roofline,
-            "kernels_ms_per_step": {k: round(v / args.steps, 4) for k, v in
-                                    sorted(kern_ms.items(), key=lambda kv: -kv[1])},
-            "kernel_share": {k: round(v / total_kern, 4) for k, v in kern_ms.items()},
-            "gpu_launches": launches,
-            "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
-    return 0
+    out = {
+        "_shape": s, "mx": mx, "workload": desc, "value": value, "unit": "tokens/s", "ms_per_step": ms,
+        "dtype": "mxfp8" if mx else "bf16",
+        "tflops": tflops, "pct_tensor_peak": tflops / t_burst,
+        "pct_tensor_peak_sustained": tflops / t_sust, "tensor_peak_src": t_src,
+        "weight_quant": wq,
+        "fwd": {"value": fwd_value, "unit": "tokens/s", "ms": ms_fwd,
+                "tflops": fwd_value * flops_tok / 1e12},
+        "roofline": roofline,
+        "kernels_ms_per_step": {k: round(v / args.steps, 4) for k, v in
+                                sorted(kern_ms.items(), key=lambda kv: -kv[1])},
+        "kernel_share": {k: round(v / total_kern, 4) for k, v in kern_ms.items()},
+        "gpu_launches": launches, "clocks": clocks,
+    }
+    if full:
+        out["e2e"], out["cpu_baseline"] = e2e, cpu
+    else:
+        out["config"] = {"T": s.T, "d": s.d, "I": s.I, "E": s.E, "top_k": s.k, "n_shared": s.n_shared,
+                         "I_shared": s.I_shared}
+    if mx and _MX_PEAK.get("peak"):
+        out["mxfp8_peak"] = _MX_PEAK["peak"]
+    del inp, bufs, grads, y, dx
+    torch.cuda.synchronize()
+    return out
 
 
 if __name__ == "__main__":

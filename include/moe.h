@@ -168,22 +168,28 @@ moe_status moe_route_topk(const moe_config* cfg, const void* x, const void* W_ro
  * owned by a pool fixed when the process starts, or they must not create
  * allocations while they run because an allocation can block, fail or
  * fragment memory that another component manages.  This call computes exactly
- * what moe_route_topk computes, with the same arguments and results, but keeps
- * its intermediate arrays in one static device array owned by the library
- * (8 MiB, resident on every GPU that loads the library until the process
- * exits) instead of in `ws`.  It allocates nothing.
+ * what moe_route_topk computes, with the same arguments (minus `ws`) and the
+ * same results, but keeps its intermediate arrays in one static device array
+ * owned by the library (9 MiB, resident on every GPU that loads the library
+ * until the process exits) instead of in `ws`.  It allocates nothing.
+ *   - It takes BF16 configurations with flags == 0 only; other precisions and
+ *     flags return MOE_ERR_UNSUPPORTED (the routing results do not depend on
+ *     them).  The rest of the configuration is checked as moe_route_topk
+ *     checks it.
  *   - logits_out is required when logits_in is NULL (the computed logits are
  *     not kept in the static array).
- *   - Shapes whose intermediates do not fit in the static array (about 64K
- *     tokens at top-8 with 256 experts) return MOE_ERR_UNSUPPORTED.
+ *   - The intermediates take about 12*T*k + 8*E*ceil(T/64) + 504*E bytes plus
+ *     2 KB: up to T = 65536 tokens fit at top-8 with 256 experts.  Larger
+ *     shapes return MOE_ERR_UNSUPPORTED before anything is enqueued.
  *   - The first call on a device looks up the device address of the static
  *     array (cudaGetSymbolAddress) with that device current; make that first
  *     call before capturing the stream into a CUDA graph.
  *   - All calls on a device share the array.  Calls whose GPU work overlaps
  *     (different streams without ordering between them) race on it and give
  *     wrong results; calls ordered on one stream are safe.
- *   - Device-side problems (NaN logits) are not reported; use moe_route_topk
- *     and moe_read_device_status when that matters. */
+ *   - Device-side problems are not reported: NaN logits, and a bounded wait
+ *     of the router projection that ran out (its results are then invalid).
+ *     Use moe_route_topk and moe_read_device_status when that matters. */
 moe_status moe_route_topk_noalloc(const moe_config* cfg, const void* x, const void* W_router,
                                   const float* router_bias, const float* logits_in, float* logits_out,
                                   int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,

@@ -27,9 +27,11 @@
 namespace moe {
 namespace {
 
-// Upper bound of the static scratch.  Holds the routing intermediates of up to
-// about 64K tokens at top-8 with 256 experts (see noalloc_bytes).
-constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+// Size of the static scratch.  The routing intermediates take about
+// 12 T k + 8 E ceil(T / 64) + 504 E bytes plus 2 KB (noalloc_bytes), so 9 MiB
+// hold up to 65536 tokens at top-8 with 256 experts (8.52 MB); larger shapes
+// are rejected.
+constexpr size_t kNoAllocScratchBytes = size_t(9) << 20;
 
 static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocScratchBytes];
 
@@ -98,10 +100,16 @@ extern "C" moe_status moe_route_topk_noalloc(const moe_config* cfg, const void* 
                                              float* logits_out, int32_t* topk_idx, float* topk_w,
                                              int32_t* counts, int32_t* offsets, int32_t* perm_token,
                                              int32_t* route_row, void* stream) {
+  // the configuration checks of moe_route_topk (the expert and shared-expert
+  // widths do not enter the routing, but a configuration moe_route_topk
+  // rejects is rejected here too)
   if (!cfg) return MOE_ERR_INVALID_ARG;
-  if (cfg->T < 0 || cfg->d <= 0 || cfg->E <= 0 || cfg->top_k <= 0) return MOE_ERR_INVALID_ARG;
+  if (cfg->T < 0 || cfg->d <= 0 || cfg->I <= 0 || cfg->E <= 0 || cfg->top_k <= 0 || cfg->n_shared < 0 ||
+      (cfg->n_shared && cfg->I_shared <= 0))
+    return MOE_ERR_INVALID_ARG;
   if (cfg->precision != MOE_BF16 || cfg->flags != 0) return MOE_ERR_UNSUPPORTED;
-  if (cfg->E > kMaxExperts || cfg->top_k > kMaxTopK || cfg->top_k > cfg->E || cfg->d % 64)
+  if (cfg->E > kMaxExperts || cfg->top_k > kMaxTopK || cfg->top_k > cfg->E || cfg->n_shared > 1 ||
+      cfg->d % 64 || cfg->I % 64 || (cfg->n_shared && cfg->I_shared % 64))
     return MOE_ERR_UNSUPPORTED;
   const int64_t T = cfg->T, E = cfg->E, k = cfg->top_k, d = cfg->d;
   if (T == 0) return MOE_OK;

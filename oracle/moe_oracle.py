@@ -46,7 +46,7 @@ import numpy as np
 
 __all__ = [
     "router_logits", "topk_route", "expert_schedule", "silu", "swiglu",
-    "moe_forward", "moe_backward", "expert_forward", "expert_backward",
+    "moe_forward", "moe_backward", "expert_forward", "expert_backward", "router_backward",
     "e4m3_decode", "e4m3_quantize", "mx_quantize", "mx_dequantize", "mx_round", "E4M3_TABLE",
     "bf16_round",
 ]
@@ -364,6 +364,20 @@ def expert_backward(x_rows, dy_rows, g, a, b, h, w_gate_e, w_up_e, w_down_e, mxf
             dadb @ wgu)
 
 
+def router_backward(topk_idx, topk_w, dg, x, w_router):
+    """Backward of the router given dL/dg (R2, R5): g = softmax over the
+    selected logits, so for a selected expert e of token t
+      dl_te = g_te (dg_te - sum_i g_ti dg_ti), and 0 for the others;
+    dW_router = dl^T x and the router's share of dx is dl W_router.
+    Returns (dlogits [T, E], dW_router [E, d], dx_router [T, d])."""
+    x, w, dg = _f64(x), _f64(topk_w), _f64(dg)
+    w_router = _f64(w_router)
+    s = np.sum(w * dg, axis=1, keepdims=True)
+    dlogits = np.zeros((x.shape[0], w_router.shape[0]))
+    np.put_along_axis(dlogits, np.asarray(topk_idx, np.int64), w * (dg - s), axis=1)
+    return dlogits, dlogits.T @ x, dlogits @ w_router
+
+
 def moe_backward(x, w_router, w_gate, w_up, w_down, dy, fwd,
                  ws_gate=None, ws_up=None, ws_down=None, dense_expert_grads=True):
     """Gradients of L = sum(dy * y) for the forward `fwd` (from moe_forward).
@@ -404,13 +418,8 @@ def moe_backward(x, w_router, w_gate, w_up, w_down, dy, fwd,
             w_gate[e], w_up[e], w_down[e], fwd.get("mxfp8", False))
         dg[toks, slots] = dg_e
         np.add.at(dx, toks, dx_rows)
-    # router
-    s = np.sum(w * dg, axis=1, keepdims=True)
-    dl_sel = w * (dg - s)
-    dlogits = np.zeros((T, E))
-    np.put_along_axis(dlogits, idx, dl_sel, axis=1)
-    dW_router = dlogits.T @ x
-    dx += dlogits @ _f64(w_router)
+    dlogits, dW_router, dx_router = router_backward(idx, w, dg, x, w_router)
+    dx += dx_router
     if dense_expert_grads:
         I = np.shape(w_gate[0])[0]
         dense = {"dW_gate": np.zeros((E, I, d)), "dW_up": np.zeros((E, I, d)),

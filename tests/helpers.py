@@ -83,3 +83,27 @@ def order_gap(logits, k):
     d = s[:, :kk - 1] - s[:, 1:kk]
     d = np.where(np.isfinite(d), d, np.inf)
     return d.min(axis=1)
+
+
+def full_router_grad_err(inp, topk_idx, topk_w, d_topk_w, dW_router):
+    """max|err| / max|ref| of the GPU's dW_router against the oracle's router
+    backward run on the GPU's own routing (ids, weights) and router-weight
+    gradient: the whole [E, d] gradient, at any size."""
+    _, ref, _ = O.router_backward(np.asarray(topk_idx.cpu(), np.int64), f64(topk_w), f64(d_topk_w),
+                                  f64(inp["x"]), f64(inp["W_router"]))
+    return rel_err(dW_router, ref)
+
+
+def shared_rows_err(inp, grads, cols):
+    """The shared expert's weight gradients restricted to intermediate columns
+    `cols` (rows of dWs_gate and dWs_up, columns of dWs_down), from the oracle's
+    SwiGLU expert with weight 1 (R1) on every token: those rows and columns
+    depend only on the same columns of the shared weights.  Returns the three
+    max|err| / max|ref|."""
+    c = torch.as_tensor(np.asarray(cols), device=inp["Ws_gate"].device)
+    x, dy = f64(inp["x"]), f64(inp["dy"])
+    wg, wu, wd = f64(inp["Ws_gate"][c]), f64(inp["Ws_up"][c]), f64(inp["Ws_down"][:, c])
+    a, b, h, _ = O.expert_forward(x, wg, wu, wd)
+    dWg, dWu, dWd, _, _ = O.expert_backward(x, dy, np.ones(x.shape[0]), a, b, h, wg, wu, wd)
+    return (rel_err(grads["dWs_gate"][c], dWg), rel_err(grads["dWs_up"][c], dWu),
+            rel_err(grads["dWs_down"][:, c], dWd))

@@ -16,7 +16,7 @@ from moe_layer_gb300 import _abi, layer
 from oracle import moe_oracle as O
 from synth.inputs import CONFIGS, make_inputs, sweep_shape
 
-from .helpers import ensure_lib, f64, order_gap, topk_gap
+from .helpers import ensure_lib, f64, full_router_grad_err, order_gap, shared_rows_err, topk_gap
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
@@ -150,7 +150,7 @@ def test_sampled_tokens_forward_backward(run):
     s, ref = run["shape"], run["ref_logits"]
     rng = np.random.default_rng(0)
     cand = np.nonzero(order_gap(ref, s.k) > 1e-3)[0]
-    tokens = np.sort(rng.choice(cand, size=3, replace=False))
+    tokens = np.sort(rng.choice(cand, size=6, replace=False))
     fwd, bwd = _oracle_tokens(run, torch.as_tensor(tokens, device="cuda"))
     y = f64(run["y"][tokens])
     dx = f64(run["dx"][tokens])
@@ -171,7 +171,7 @@ def test_sampled_expert_weight_gradients(run):
     touchy = set(srt[near, s.k - 1].tolist()) | set(srt[near, s.k].tolist()) if s.k < s.E else set()
     counts = np.bincount(ridx.ravel(), minlength=s.E)
     order = [e for e in np.argsort(-counts) if e not in touchy and counts[e] > 0]
-    experts = [order[0], order[len(order) // 2]]
+    experts = [order[0], order[len(order) // 2], order[-1]]
     for e in experts:
         t, j = np.nonzero(ridx == e)
         xs, dys = f64(inp["x"][torch.as_tensor(t, device="cuda")]), f64(inp["dy"][torch.as_tensor(t, device="cuda")])
@@ -185,6 +185,23 @@ def test_sampled_expert_weight_gradients(run):
     if s.zero_experts:
         for e in range(s.E - s.zero_experts, s.E):
             assert (run["grads"]["dW_gate"][e] == 0).all() and (run["grads"]["dW_down"][e] == 0).all()
+
+
+def test_router_weight_gradient_whole(run):
+    """dW_router [E, d] in full: the oracle's router backward on the GPU's
+    routing and its d_topk_w (the latter checked against the oracle on sampled
+    tokens above)."""
+    rt, g = run["rt"], run["grads"]
+    assert full_router_grad_err(run["inp"], rt["idx"], rt["w"], g["d_topk_w"], g["dW_router"]) <= TOL
+
+
+def test_sampled_shared_expert_weight_gradients(run):
+    s = run["shape"]
+    if not s.n_shared:
+        pytest.skip("no shared expert")
+    cols = np.sort(np.random.default_rng(2).choice(s.I_shared, size=4, replace=False))
+    errs = shared_rows_err(run["inp"], run["grads"], cols)
+    assert max(errs) <= TOL, errs
 
 
 def test_rerun_is_bitwise_identical(run):

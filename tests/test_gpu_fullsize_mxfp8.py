@@ -15,7 +15,7 @@ from moe_layer_gb300 import _abi, layer
 from oracle import moe_oracle as O
 from synth.inputs import CONFIGS, make_inputs
 
-from .helpers import ensure_lib, f64, order_gap, topk_gap
+from .helpers import ensure_lib, f64, full_router_grad_err, order_gap, shared_rows_err, topk_gap
 
 pytestmark = pytest.mark.gpu
 TOL_MX = 5e-2
@@ -54,10 +54,19 @@ def _run(shape, seed=0):
     grads = layer.alloc_grads(cfg)
     y = layer.forward(cfg, inp, bufs)
     dx = layer.backward(cfg, inp, inp["dy"], bufs, grads)
+    # the routing the forward used, through the routing entry point (the same
+    # bf16 router kernels; ids and weights do not depend on the precision)
+    T, E, k = shape.T, shape.E, shape.k
+    rcfg = _abi.make_config(T, shape.d, shape.I, E, k, shape.n_shared, shape.I_shared)
+    rbufs = layer.MoEBuffers(rcfg, training=False)
+    rt = dict(idx=torch.empty(T, k, dtype=torch.int32, device="cuda"), w=torch.empty(T, k, device="cuda"))
+    scratch = [torch.empty(n, dtype=torch.int32, device="cuda") for n in (E, E + 1, T * k, T * k)]
+    _abi.moe_route_topk(rcfg, inp["x"], inp["W_router"], None, None, None, rt["idx"], rt["w"], scratch[0],
+                        scratch[1], scratch[2], scratch[3].view(T, k), rbufs.fwd_ws)
     torch.cuda.synchronize()
     assert _abi.moe_read_device_status(bufs.fwd_ws) == 0
     assert _abi.moe_read_device_status(bufs.bwd_ws) == 0
-    return dict(inp=inp, y=y, dx=dx, grads=grads)
+    return dict(inp=inp, y=y, dx=dx, grads=grads, rt=rt)
 
 
 @pytest.fixture(scope="module")
@@ -109,6 +118,20 @@ def test_sampled_expert_weight_gradients(run):
     for gpu, refw, name in ((g["dW_gate"][e], dWg, "dW_gate"), (g["dW_up"][e], dWu, "dW_up"),
                             (g["dW_down"][e], dWd, "dW_down")):
         assert np.abs(f64(gpu) - refw).max() / np.abs(refw).max() <= TOL_MX, (name, e)
+
+
+def test_router_weight_gradient_whole(run):
+    """dW_router [E, d] in full (the router stays bf16 in MXFP8 mode): the
+    oracle's router backward on the GPU's routing and d_topk_w."""
+    rt, g = run["rt"], run["grads"]
+    assert full_router_grad_err(run["inp"], rt["idx"], rt["w"], g["d_topk_w"], g["dW_router"]) <= TOL_MX
+
+
+def test_sampled_shared_expert_weight_gradients(run):
+    """The shared expert stays bf16 in MXFP8 mode: sampled rows at the bf16 bound."""
+    cols = np.sort(np.random.default_rng(3).choice(run["shape"].I_shared, size=4, replace=False))
+    errs = shared_rows_err(run["inp"], run["grads"], cols)
+    assert max(errs) <= 1e-2, errs
 
 
 def test_rerun_is_bitwise_identical(run):

@@ -90,8 +90,13 @@ MX_SHAPES = {
     "mx_ragged": MoEShape(T=333, d=384, I=128, E=5, k=3, n_shared=0, I_shared=0, w_std=0.05),
     "mx_zipf_zero": MoEShape(T=640, d=256, I=384, E=32, k=4, n_shared=1, I_shared=128, w_std=0.05,
                              zipf=True, zero_experts=8),
+    # model shapes of the MoK blog ("Speedups"), scaled down with E, top-k and d:I kept
+    "mx_qwen35_scaled": MoEShape(T=256, d=512, I=128, E=512, k=10, n_shared=1, I_shared=128, w_std=0.05,
+                                 wr_std=0.1),
+    "mx_dsv4pro_scaled": MoEShape(T=256, d=896, I=384, E=384, k=6, n_shared=1, I_shared=384, w_std=0.03,
+                                  wr_std=0.1),
 }
-MX_SEEDS = {}
+MX_SEEDS = {"mx_qwen35_scaled": 2}
 
 
 def _cuda(inp):
@@ -118,14 +123,14 @@ def _run_mx(shape, seed=0, backward=True, flags=0):
     return res
 
 
-@pytest.mark.parametrize("name", list(MX_SHAPES))
-def test_mxfp8_forward_backward_parity(name):
+@pytest.mark.parametrize("name,flags", [(n, 0) for n in MX_SHAPES] + [("mx_zipf_zero", "replay")])
+def test_mxfp8_forward_backward_parity(name, flags):
     """Forward and backward in MXFP8 mode vs the oracle's MXFP8 emulation
     (every operand of the routed experts' GEMMs rounded through MXFP8 along
     its reduction axis), and measurably farther from the full-precision
-    oracle: the kernels do quantize."""
+    oracle: the kernels do quantize.  Also with forward activation replay."""
     shape = MX_SHAPES[name]
-    r = _run_mx(shape, seed=MX_SEEDS.get(name, 0))
+    r = _run_mx(shape, seed=MX_SEEDS.get(name, 0), flags=_abi.MOE_FLAG_REPLAY if flags == "replay" else 0)
     inp = r["inp_cpu"]
     fwd = oracle_forward(inp, shape.k, mxfp8=True)
     assert topk_gap(fwd["logits"], shape.k).min() > 1e-4, "seeded input has a near-tie"

@@ -127,18 +127,27 @@ SHAPES = {
     # pairs on SM pairs and every tile of the odd ones on one SM, so both passes of each grouped
     # GEMM have work; 640 rows per expert put the weight gradients on SM pairs
     "pairs_leftover": MoEShape(T=2560, d=512, I=256, E=8, k=2, n_shared=1, I_shared=128, w_std=0.05),
+    # the open-weight model shapes the MoK blog benchmarks ("Speedups"), scaled down with their
+    # E, top-k and d:I ratio kept: Kimi-K2.7 (384, 8, 3.5), GLM-5.2 (256, 8, 3), Qwen3.5-397B-A17B
+    # (512, 10, 4), DeepSeek-V4-Pro (384, 6, 7:3); logits spread wider so that seeds without
+    # near-ties exist at these E and k
+    "kimi_k27_scaled": MoEShape(T=256, d=448, I=128, E=384, k=8, n_shared=1, I_shared=128, w_std=0.05,
+                                wr_std=0.1),
+    "glm52_scaled": MoEShape(T=256, d=384, I=128, E=256, k=8, n_shared=1, I_shared=128, w_std=0.05, wr_std=0.1),
+    "qwen35_scaled": MoEShape(T=256, d=512, I=128, E=512, k=10, n_shared=1, I_shared=128, w_std=0.05,
+                              wr_std=0.1),
+    "dsv4pro_scaled": MoEShape(T=256, d=448, I=192, E=384, k=6, n_shared=1, I_shared=192, w_std=0.05,
+                               wr_std=0.1),
 }
 
 
 # seeds chosen so that no token has a top-k boundary gap below 1e-4 (checked
 # below on the oracle's float64 logits)
-SEEDS = {"noshared": 2, "pairs_leftover": 2}
+SEEDS = {"noshared": 2, "pairs_leftover": 2, "glm52_scaled": 1, "qwen35_scaled": 2}
 
 
-@pytest.mark.parametrize("name", list(SHAPES))
-def test_forward_backward_parity(name):
-    shape = SHAPES[name]
-    r = _run_layer(shape, seed=SEEDS.get(name, 0))
+def _check_against_oracle(shape, r):
+    """y, dx and every gradient of the run `r` against the oracle on its inputs."""
     inp = r["inp_cpu"]
     fwd = oracle_forward(inp, shape.k)
     # routing of the GPU (fp32 logits) vs the oracle (fp64 logits): identical
@@ -161,6 +170,32 @@ def test_forward_backward_parity(name):
             assert fwd["counts"][e] == 0
             for key in ["dW_gate", "dW_up", "dW_down", "dW_router"]:
                 assert (g[key][e] == 0).all(), (key, e)
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_forward_backward_parity(name):
+    shape = SHAPES[name]
+    _check_against_oracle(shape, _run_layer(shape, seed=SEEDS.get(name, 0)))
+
+
+FLAGS = {"replay": "MOE_FLAG_REPLAY", "wgrad_fp32": "MOE_FLAG_WGRAD_FP32",
+         "replay_wgrad_fp32": ("MOE_FLAG_REPLAY", "MOE_FLAG_WGRAD_FP32")}
+
+
+@pytest.mark.parametrize("flag", list(FLAGS))
+@pytest.mark.parametrize("name", ["ragged", "zipf_zero", "pairs_leftover", "qwen35_scaled"])
+def test_flag_paths_against_oracle(name, flag):
+    """Forward activation replay (the backward recomputes the routed x rows, a
+    and b) and fp32 weight gradients, each compared with the oracle itself."""
+    names = FLAGS[flag] if isinstance(FLAGS[flag], tuple) else (FLAGS[flag],)
+    flags = 0
+    for n in names:
+        flags |= getattr(_abi, n)
+    shape = SHAPES[name]
+    r = _run_layer(shape, seed=SEEDS.get(name, 0), flags=flags)
+    if flags & _abi.MOE_FLAG_WGRAD_FP32:
+        assert r["grads"]["dW_gate"].dtype == torch.float32
+    _check_against_oracle(shape, r)
 
 
 def test_routing_outputs_of_forward_match_oracle_routing():
