@@ -18,7 +18,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
-SOURCES = ["moe_api.cu", "routing.cu", "elementwise.cu", "gemm_fwd.cu", "gemm_bwd.cu", "moe_noalloc.cu", "mxfp8.cu", "gemm_mx.cu"]
+SOURCES = ["moe_api.cu", "routing.cu", "elementwise.cu", "gemm_fwd.cu", "gemm_bwd.cu", "moe_noalloc.cu", "mxfp8.cu",
+           "gemm_mx.cu", "route_fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + os.path.join(ROOT, "include")]
 

@@ -45,23 +45,23 @@ cudaError_t launch_gemm_inst(const GemmParams& p, int grid, cudaStream_t st) {
   }
 }
 
-// The bf16 row GEMMs other than the router projection: a 2-SM pass over the
+// The row GEMMs other than the router projection (bf16 and MXFP8): a 2-SM pass over the
 // pairs of m-tiles, then a 1-SM pass over the rest: every tile of each expert
 // with an odd number of them (grouped rows), or the last m-tile of an odd
 // dense row range.  Grouped problems launch both passes always (their tile
 // counts live on the device; a pass without tiles exits at once).
-template <int AM, int BMO, int EPI>
+template <int AM, int BMO, int EPI, bool MX = false>
 cudaError_t launch_rows_two_pass(const GemmParams& p, int grid, cudaStream_t st) {
   const int dense_mt = p.dense_rows > 0 ? (p.dense_rows + kBM - 1) / kBM : 0;
   if (p.dense_rows == 0 || dense_mt >= 2) {
-    const cudaError_t e = launch_gemm_inst<AM, BMO, EPI, SCHED_ROWS2>(p, grid, st);
+    const cudaError_t e = launch_gemm_inst<AM, BMO, EPI, SCHED_ROWS2, MX>(p, grid, st);
     if (e != cudaSuccess) return e;
   }
   if (p.dense_rows > 0 && dense_mt % 2 == 0) return cudaSuccess;
   GemmParams q = p;
   q.part = 1;
   if (p.dense_rows == 0 || dense_mt >= 2) ++extra_kernel_launches();
-  return launch_gemm_inst<AM, BMO, EPI, SCHED_ROWS>(q, grid, st);
+  return launch_gemm_inst<AM, BMO, EPI, SCHED_ROWS, MX>(q, grid, st);
 }
 
 // Weight gradients likewise: pairs of m-tiles (weight rows) on SM pairs, and

@@ -45,14 +45,15 @@ enum ProfLabel : int {
   PL_DOWN_ROUTED, PL_DOWN_SHARED, PL_COMBINE, PL_DGRAD_DOWN_ROUTED, PL_DGRAD_DOWN_SHARED,
   PL_ROUTER_GRAD, PL_DGRAD_GATEUP_ROUTED, PL_DGRAD_GATEUP_SHARED, PL_UNPERMUTE, PL_ROUTER_WGRAD,
   PL_WGRAD_DOWN, PL_WGRAD_GATE, PL_WGRAD_UP, PL_WGRAD_SHARED_DOWN, PL_WGRAD_SHARED_GATE,
-  PL_WGRAD_SHARED_UP, PL_PERMUTE_DY, PL_MX_WEIGHTS, PL_MX_QUANT_X, PL_MX_QUANT_DY, PL_COUNT
+  PL_WGRAD_SHARED_UP, PL_PERMUTE_DY, PL_MX_WEIGHTS, PL_MX_QUANT_X, PL_MX_QUANT_DY, PL_ROUTE_FUSED, PL_COUNT
 };
 static const char* const kProfNames[PL_COUNT] = {
     "router_gemm", "topk_count", "chunk_scan", "scatter", "permute_x", "gateup_shared", "gateup_routed",
     "down_routed", "down_shared", "combine", "dgrad_down_routed", "dgrad_down_shared",
     "router_grad", "dgrad_gateup_routed", "dgrad_gateup_shared", "unpermute", "router_wgrad",
     "wgrad_down", "wgrad_gate", "wgrad_up", "wgrad_shared_down", "wgrad_shared_gate",
-    "wgrad_shared_up", "permute_dy", "mx_quantize_weights", "mx_permute_quant_x", "mx_permute_quant_dy"};
+    "wgrad_shared_up", "permute_dy", "mx_quantize_weights", "mx_permute_quant_x", "mx_permute_quant_dy",
+    "route_fused"};
 
 struct ProfRecord {
   int label;
@@ -187,6 +188,7 @@ void carve_saved(void* base, const Shape& s, Saved& v, size_t* bytes) {
 
 struct FwdWs {
   int* status;
+  int* sync;  // [4] the fused routing launch's barrier counters and failure flag
   float* logits;
   int32_t* chunk_counts;
   int32_t* chunk_base;
@@ -203,6 +205,7 @@ struct FwdWs {
 void carve_fwd(void* base, const Shape& s, FwdWs& w, size_t* bytes) {
   Carver c(base);
   w.status = c.take<int>(kAlign / sizeof(int));
+  w.sync = c.take<int>(4);
   w.logits = c.take<float>(s.T * s.E);
   w.chunk_counts = c.take<int32_t>(s.nchunk * s.E);
   w.chunk_base = c.take<int32_t>(s.nchunk * s.E);
@@ -431,13 +434,27 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int wgrad_mode(const Shape& s) { return s.R < 128 * s.E ? 2 : (s.R < 384 * s.E ? 1 : 0); }
 
 // ---------------------------------------------------------------- routing
+// The routing runs as one persistent launch (route_fused.cu: router GEMM with
+// the top-k in its epilogue, scan and scatter) where it applies: logits
+// computed here, E <= 256, top_k <= 16, and a workspace with its sync words.
+// Otherwise, or with the environment variable MOE_ROUTING_SEPARATE set (the
+// tests compare the two bitwise), the separate kernels run.  zero_routing: the
+// routing arrays rt points into are one block (the saved state's or the
+// workspace's), zeroed before the fused launch so that a launch cut short by a
+// timeout leaves only in-range indices for the kernels after it.
+bool fused_routing_enabled() {
+  const char* v = getenv("MOE_ROUTING_SEPARATE");
+  return !(v && v[0] && v[0] != '0');
+}
+
 moe_status run_routing(const Shape& s, const void* x, const void* W_router, const float* bias,
                        const float* logits_in, float* logits, const Routing& rt,
-                       int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t st) {
+                       int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t st,
+                       int* sync = nullptr, bool zero_routing = false, bool keep_logits = true) {
   const float* lg = logits_in;
+  GemmParams p;
+  zero_params(p);
   if (!lg) {
-    GemmParams p;
-    zero_params(p);
     MOE_TRY(tmap(&p.tmA, x, s.T, s.d, 64, kBM));
     MOE_TRY(tmap(&p.tmB0, W_router, s.E, s.d, 64, kBN));
     p.dense_rows = static_cast<int>(s.T);
@@ -453,6 +470,45 @@ moe_status run_routing(const Shape& s, const void* x, const void* W_router, cons
     // MOE_ERR_DEVICE_TIMEOUT instead of hanging.
     if (const char* v = getenv("MOE_DEBUG_STALL_ROUTER"))
       if (v[0] && v[0] != '0') p.debug_extra_tx = 16;
+  }
+  if (!lg && sync && fused_routing_enabled() && route_fused_supported(s.E, s.k)) {
+    const int nchunk = static_cast<int>(s.nchunk);
+    MOE_CUDA(cudaMemsetAsync(chunk_counts, 0, static_cast<size_t>(s.nchunk * s.E) * sizeof(int32_t), st));
+    MOE_CUDA(cudaMemsetAsync(sync, 0, 4 * sizeof(int), st));
+    if (zero_routing) {
+      const char* beg = reinterpret_cast<const char*>(rt.topk_idx);
+      const char* end = reinterpret_cast<const char*>(rt.perm_w_pad + s.Rp);
+      MOE_CUDA(cudaMemsetAsync(rt.topk_idx, 0, static_cast<size_t>(end - beg), st));
+    }
+    p.out = keep_logits ? logits : nullptr;  // the fused launch writes logits only when asked
+    p.route_idx = rt.topk_idx;
+    p.route_w = rt.topk_w;
+    p.route_chunk = chunk_counts;
+    p.route_k = static_cast<int>(s.k);
+    const ScatterArgs sc{rt.topk_idx, rt.topk_w, static_cast<int>(s.T), static_cast<int>(s.E), static_cast<int>(s.k),
+                         static_cast<int>(s.ra), chunk_base, rt.counts, rt.offsets, rt.row_start, rt.tile_start,
+                         rt.pair_start, rt.rem_start, rt.perm_token, rt.route_row, rt.perm_token_pad,
+                         rt.route_row_pad, rt.perm_w_pad};
+    // Test hook: with MOE_DEBUG_STALL_COUNTER set, the first grid barrier waits
+    // for one arrival more than the grid has; every CTA's bounded wait runs out
+    // and the launch records MOE_ERR_DEVICE_TIMEOUT.
+    int extra = 0;
+    if (const char* v = getenv("MOE_DEBUG_STALL_COUNTER"))
+      if (v[0] && v[0] != '0') extra = 1;
+    const int grid = grid_for(device_sm_count());
+    cudaError_t e = cudaSuccess;
+    const moe_status ms = prof_launch(PL_ROUTE_FUSED, st, [&]() {
+      e = launch_route_fused(p, sc, chunk_counts, chunk_base, nchunk, status, sync, extra, grid, st);
+      return e;
+    });
+    if (ms == MOE_OK) return MOE_OK;
+    // a grid that cannot be resident at once (another context holding SMs):
+    // the separate kernels below
+    if (e != cudaErrorCooperativeLaunchTooLarge) return MOE_ERR_CUDA;
+    (void)cudaGetLastError();
+    p.out = logits;
+  }
+  if (!lg) {
     MOE_LAUNCH(PL_ROUTER_GEMM, st, launch_gemm(GK_ROUTER, p, grid_for(cdiv(s.T, kBM) * cdiv(s.E, kBN)), st));
     lg = logits;
   }
@@ -492,6 +548,19 @@ void set_mx_scales(GemmParams& p, const uint8_t* sfa, int64_t a_rows, const uint
   p.sfb1 = sfb1;
   p.sfb_rb = cdiv(b_rows, 128);
 }
+// The same scales for the row GEMMs, which run partly on SM pairs: also the
+// tensor maps over the scale arrays (K = the reduction length) that the pairs
+// load them through: 512-byte boxes for A and for each stack of a dual-N B,
+// 1024-byte ones (two 128-row blocks) for a single B.
+moe_status set_mx_row_scales(GemmParams& p, const uint8_t* sfa, int64_t a_rows, const uint8_t* sfb0,
+                             const uint8_t* sfb1, int64_t b_rows, int64_t K) {
+  set_mx_scales(p, sfa, a_rows, sfb0, sfb1, b_rows);
+  if (!make_tmap_bytes(&p.tmSfA, sfa, mx_sf_alloc(a_rows, K), 2) ||
+      !make_tmap_bytes(&p.tmSfB0, sfb0, mx_sf_alloc(b_rows, K), sfb1 ? 2 : 4) ||
+      (sfb1 && !make_tmap_bytes(&p.tmSfB1, sfb1, mx_sf_alloc(b_rows, K), 2)))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
 
 // Routed gate/up of the forward in MXFP8 mode (blog section "MXFP8 support"):
 // on the quantized x rows xq, the SwiGLU epilogue writing h as E4M3 + scales
@@ -506,7 +575,7 @@ moe_status gateup_routed_mx(const Shape& s, const moe_weights* wts, const Routin
   MOE_TRY(qmap(&p.tmA, xq, s.Rp, s.d, kBM));
   MOE_TRY(qmap(&p.tmB0, m.wg, s.E * s.I, s.d, kBN / 2));
   MOE_TRY(qmap(&p.tmB1, m.wu, s.E * s.I, s.d, kBN / 2));
-  set_mx_scales(p, xq_sf, s.Rp, m.wg_sf, m.wu_sf, s.E * s.I);
+  MOE_TRY(set_mx_row_scales(p, xq_sf, s.Rp, m.wg_sf, m.wu_sf, s.E * s.I, s.d));
   p.num_groups = static_cast<int>(s.E);
   p.row_start = rt.row_start;
   p.tile_start = rt.tile_start;
@@ -540,8 +609,8 @@ moe_status down_routed_mx(const Shape& s, const moe_weights* wts, const Routing&
   GemmParams p;
   zero_params(p);
   MOE_TRY(qmap(&p.tmA, w.hq, s.Rp, s.I, kBM));
-  MOE_TRY(qmap(&p.tmB0, m.wd, s.E * s.d, s.I, kBN));
-  set_mx_scales(p, w.hq_sf, s.Rp, m.wd_sf, nullptr, s.E * s.d);
+  MOE_TRY(qmap(&p.tmB0, m.wd, s.E * s.d, s.I, kBN / 2));
+  MOE_TRY(set_mx_row_scales(p, w.hq_sf, s.Rp, m.wd_sf, nullptr, s.E * s.d, s.I));
   p.num_groups = static_cast<int>(s.E);
   p.row_start = rt.row_start;
   p.tile_start = rt.tile_start;
@@ -610,6 +679,12 @@ moe_status forward_gateup(const Shape& s, const void* x, const moe_weights* wts,
     p.store_ab = o.abs ? 1 : 0;
     p.I = static_cast<int>(s.Is);
     p.status = o.status;
+    // Test hook for the failure path of the SM-pair kernels: with
+    // MOE_DEBUG_STALL_PAIR set, the even CTA of every pair of the shared
+    // expert's gate/up waits for 16 bytes that never come; both CTAs' bounded
+    // waits run out and the launch records MOE_ERR_DEVICE_TIMEOUT.
+    if (const char* v = getenv("MOE_DEBUG_STALL_PAIR"))
+      if (v[0] && v[0] != '0') p.debug_extra_tx = 16;
     MOE_LAUNCH(PL_GATEUP_SHARED, st, launch_gemm(GK_GATEUP, p, grid_for(cdiv(s.T, kBM) * cdiv(s.Is, kBN / 2)), st));
   }
   if (s.mx) return gateup_routed_mx(s, wts, rt, act, o.xq, o.xq_sf, o.hq, o.hq_sf, o.status, st);
@@ -764,9 +839,10 @@ moe_status moe_route_topk(const moe_config* cfg, const void* x, const void* W_ro
   rt.offsets = offsets;
   rt.perm_token = perm_token;
   rt.route_row = route_row;
+  // the fused launch writes the logits only where the caller asks for them
   float* logits = logits_out ? logits_out : w.logits;
   return run_routing(s, x, W_router, router_bias, logits_in, logits, rt, w.chunk_counts,
-                     w.chunk_base, w.status, st);
+                     w.chunk_base, w.status, st, w.sync, false, logits_out != nullptr);
 }
 
 moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* wts, void* y,
@@ -787,15 +863,17 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* 
     carve_saved(saved, s, sv, nullptr);
     rt = sv.rt;
   }
+  // the activations the backward needs go to the saved state, unless it keeps
+  // only the routing (MOE_FLAG_REPLAY) or there is none (inference)
+  const bool keep_acts = saved && !s.replay;
+  // the logits are not kept (the separate kernels pass them through the workspace)
   MOE_TRY(run_routing(s, x, wts->W_router, wts->router_bias, nullptr, w.logits, rt, w.chunk_counts,
-                      w.chunk_base, w.status, st));
+                      w.chunk_base, w.status, st, w.sync, true, false));
   const int T = static_cast<int>(s.T), d = static_cast<int>(s.d), I = static_cast<int>(s.I);
   const int E = static_cast<int>(s.E);
 
-  // the activations the backward needs go to the saved state, unless it keeps
-  // only the routing (MOE_FLAG_REPLAY) or there is none (inference)
   const GateUpOut o{w.xp, w.h, true, w.hs, saved ? sv.act.abs : nullptr, w.xq, w.xq_sf, w.hq, w.hq_sf, w.status};
-  MOE_TRY(forward_gateup(s, x, wts, rt, (saved && !s.replay) ? &sv.act : nullptr, o, st));
+  MOE_TRY(forward_gateup(s, x, wts, rt, keep_acts ? &sv.act : nullptr, o, st));
   if (s.mx) {
     MOE_TRY(down_routed_mx(s, wts, rt, w, st));
   } else {
@@ -894,8 +972,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     GemmParams p;
     zero_params(p);
     MOE_TRY(qmap(&p.tmA, w.dyq, s.Rp, s.d, kBM));
-    MOE_TRY(qmap(&p.tmB0, m.wdt, s.E * s.I, s.d, kBN));
-    set_mx_scales(p, w.dyq_sf, s.Rp, m.wdt_sf, nullptr, s.E * s.I);
+    MOE_TRY(qmap(&p.tmB0, m.wdt, s.E * s.I, s.d, kBN / 2));
+    MOE_TRY(set_mx_row_scales(p, w.dyq_sf, s.Rp, m.wdt_sf, nullptr, s.E * s.I, s.d));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.counts = rt.counts;
@@ -974,8 +1052,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
     GemmParams p;
     zero_params(p);
     MOE_TRY(qmap(&p.tmA, w.dadbq, s.Rp, 2 * s.I, kBM));
-    MOE_TRY(qmap(&p.tmB0, m.wgut, s.E * s.d, 2 * s.I, kBN));
-    set_mx_scales(p, w.dadbq_sf, s.Rp, m.wgut_sf, nullptr, s.E * s.d);
+    MOE_TRY(qmap(&p.tmB0, m.wgut, s.E * s.d, 2 * s.I, kBN / 2));
+    MOE_TRY(set_mx_row_scales(p, w.dadbq_sf, s.Rp, m.wgut_sf, nullptr, s.E * s.d, 2 * s.I));
     p.num_groups = E;
     p.row_start = rt.row_start;
     p.counts = rt.counts;

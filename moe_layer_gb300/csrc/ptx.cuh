@@ -260,14 +260,41 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
-// Copies a 32 x 128-bit block (512 contiguous bytes of shared memory) into
-// TMEM lanes 0..31 of all four lane quadrants, four 32-bit columns.
-__device__ __forceinline__ void tc_cp_32x128b(uint32_t taddr, uint32_t saddr) {
+// The pair form of tc_mma_mxf8 (issued by one thread of the even CTA of a
+// cluster pair, M = 256: 128 rows of A and N/2 rows of B in each CTA's shared
+// memory at the same offsets).  Each CTA's TMEM holds the scales of its own
+// 128 rows of A and of all N rows of B at sfa_tmem / sfb_tmem.
+__device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory descriptor of a 32 x 128-bit block for tcgen05.cp.
+__device__ __forceinline__ uint64_t cp_desc_32x128b(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
   d |= static_cast<uint64_t>(128 >> 4) << 32;  // 8-row core-matrix stride
   d |= static_cast<uint64_t>(1) << 46;
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+  return d;
+}
+
+// Copies a 32 x 128-bit block (512 contiguous bytes of shared memory) into
+// TMEM lanes 0..31 of all four lane quadrants, four 32-bit columns.
+__device__ __forceinline__ void tc_cp_32x128b(uint32_t taddr, uint32_t saddr) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(cp_desc_32x128b(saddr))
+               : "memory");
+}
+// The pair form, issued by the even CTA's MMA thread: each CTA's block at
+// shared-memory offset saddr goes into its own TMEM at taddr.
+__device__ __forceinline__ void tc_cp_32x128b_pair(uint32_t taddr, uint32_t saddr) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(cp_desc_32x128b(saddr))
+               : "memory");
 }
 
 // Instruction descriptor of the block-scaled kind::mxf8f6f4 MMA: E4M3 A and B

@@ -50,12 +50,16 @@
 #pragma once
 #include "mx_common.cuh"
 #include "ptx.cuh"
+#include "routing_dev.cuh"
 
 namespace moe {
 
 enum AMode : int { A_K_TILE = 0, A_MN_TILE = 1 };
 enum BMode : int { B_K_TILE = 0, B_K_DUAL_N = 1, B_MN_TILE = 2, B_MN_DUAL_K = 3 };
-enum EpiMode : int { EPI_F32_BIAS = 0, EPI_SWIGLU_FWD = 1, EPI_BF16 = 2, EPI_SWIGLU_BWD = 3 };
+// EPI_ROUTE: the router projection with the routing's softmax + top-k fused
+// into the epilogue (route_fused.cu): each epilogue thread holds one token's
+// logits, E <= 256 columns of the tile.
+enum EpiMode : int { EPI_F32_BIAS = 0, EPI_SWIGLU_FWD = 1, EPI_BF16 = 2, EPI_SWIGLU_BWD = 3, EPI_ROUTE = 4 };
 // SCHED_ROWS2 / SCHED_WGRAD2: the same tiles in pairs of m-tiles on one
 // n-tile, each pair computed by a cluster of two CTAs with cta_group::2 MMAs
 // (M = 256).
@@ -128,6 +132,9 @@ __host__ __device__ constexpr int gemm_threads() {
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr int gemm_stages() {
   if (!MX && epi_wide<MX, EPI, SCH>()) return 3;
+  // MXFP8 on SM pairs: four 32 KB stages, as many as the TMEM scale ring
+  // has slots (the accumulator, the ring and the epilogue stash fill TMEM)
+  if (MX && sched_pair(SCH)) return kStages;
   return sched_pair(SCH) ? 6 : (gemm_bn<MX, EPI, SCH>() == kBN ? kStages : 5);
 }
 // MXFP8 kernels, with a single 256-column accumulator beside the scale ring,
@@ -169,10 +176,14 @@ __host__ __device__ constexpr int gemm_smem_bytes_for() {
 // shared operand between two CTAs (fewer L2 reads, same shared-memory
 // traffic) gained nothing: shared-memory traffic per SM bounds these GEMMs.
 // Both passes load B in halves (128-row or two-chunk boxes), so they share
-// their tensor maps.
+// their tensor maps.  The MXFP8 row GEMMs run the same two passes; on SM
+// pairs each CTA also loads the scales of its 128 rows of A and of all of B
+// (which both CTAs' MMAs read from their own TMEM) through tmSfA / tmSfB*.
 template <bool MX, int EPI, int SCH>
 __host__ __device__ constexpr bool b_halves() {
-  return !MX && EPI != EPI_F32_BIAS;
+  // the router projection (fp32 logits, or with the fused top-k) loads its
+  // 256-row B tile with one box
+  return EPI != EPI_F32_BIAS && EPI != EPI_ROUTE && (!MX || !sched_wgrad(SCH));
 }
 
 struct GemmParams {
@@ -191,6 +202,12 @@ struct GemmParams {
   // problems (an M=64 accumulator leaves 16 rows per epilogue warp).
   CUtensorMap tmO0h;
   CUtensorMap tmO1h;
+  // MXFP8 on SM pairs: the scale arrays of A (512-byte boxes) and of B (one
+  // 1024-byte box, or 512 bytes from each stack of a dual-N operand), viewed
+  // as [bytes / 256, 256] (make_tmap_bytes).
+  CUtensorMap tmSfA;
+  CUtensorMap tmSfB0;
+  CUtensorMap tmSfB1;
   // ---- schedule
   int dense_rows;          // > 0: a single group of this many rows; 0: grouped by row_start
   int num_groups;          // number of groups (experts) when grouped
@@ -248,8 +265,9 @@ struct GemmParams {
   long long qt2_rb;
   int* status;
   // Test hook (0 normally): bytes the first pipeline stage of each CTA's first
-  // tile expects beyond what its loads bring, so that its MMA warp's bounded
-  // wait runs out (one-SM mode only).
+  // tile expects beyond what its loads bring (on SM pairs: the even CTA's, whose
+  // barrier counts both CTAs' loads), so that its MMA warp's bounded wait runs
+  // out and both CTAs of the pair take their abort paths.
   uint32_t debug_extra_tx;
   // Weight gradients, chosen by the host from the experts' row ranges (the K
   // of these GEMMs): 0 pairs of m-tiles on SM pairs (and the last m-tile on
@@ -259,7 +277,18 @@ struct GemmParams {
   // Weight gradients: nonzero when tmO0 maps an fp32 output (boxes of 32
   // columns x 32 rows) instead of a bf16 one (64 x 32).
   int wgrad_f32;
+  // EPI_ROUTE: top-k ids and weights [T, route_k], per-chunk expert
+  // histograms [ceil(T / kChunkTokens), N] (N = E; `out` optionally receives
+  // the logits, with the bias added).
+  int32_t* route_idx;
+  float* route_w;
+  int32_t* route_chunk;
+  int route_k;
 };
+
+// The softmax + top-k fused into the router projection's epilogue keeps a
+// sorted list of this many candidates per token (top_k <= kRouteMaxK).
+constexpr int kRouteMaxK = 16;
 
 template <int EPI>
 __host__ __device__ constexpr int tile_out_cols() {
@@ -486,7 +515,7 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
   constexpr int BN = gemm_bn<MX, EPI, SCH>();
   constexpr int SB = stage_bytes<MX, EPI, SCH>(), SFB = sf_stage_bytes<MX, EPI, SCH>();
   constexpr uint32_t kTx = SB + SFB;
-  static_assert(!HALVES || (BN == kBN && !MX), "B halves: bf16, 256-column tiles");
+  static_assert(!HALVES || BN == kBN, "B halves: 256-column tiles");
   int s = 0;
   uint32_t ph = 0;
   // Per stage: parity of the last load issued into it, or -1.
@@ -519,7 +548,8 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
         // 2-SM mode: this CTA's 128 rows (or MN columns) of A and its half of
         // B, the even CTA's barrier counting both CTAs' bytes
         if (lane == 0) {
-          if (!PAIR || wr.rank == 0) mbar_arrive_expect_tx(full, PAIR ? 2 * kTx : kTx);
+          if (!PAIR || wr.rank == 0)
+            mbar_arrive_expect_tx(full, (PAIR ? 2 * kTx : kTx) + ((w == wr.first && kb == 0) ? p.debug_extra_tx : 0u));
           const uint32_t fb = PAIR ? lead_full0 + 8 * s : full;
           load_a<AM, PAIR>(p, sA, t, kabs, arow, fb);
           if constexpr (PAIR) {
@@ -527,6 +557,31 @@ __device__ __forceinline__ void gemm_producer(const GemmParams& p, uint32_t s_ti
           } else {
             load_b_half<BMO, false>(p, sB, t, kabs, brow, 0, full);
             load_b_half<BMO, false>(p, sB + kBTileBytes / 2, t, kabs, brow, 1, full);
+          }
+          if constexpr (MX) {
+            // scales of this CTA's A rows and of the whole B tile (both CTAs of a
+            // pair hold all of B's: each CTA's MMA half reads them from its TMEM)
+            const long long g = kabs / kBKmx;
+            const uint32_t sfs = s_sf + s * SFB;
+            const int ablk = static_cast<int>(g * p.sfa_rb + arow / 128);
+            const int bblk = static_cast<int>(g * p.sfb_rb + brow / 128);
+            if constexpr (PAIR) {
+              tma_load_2d_pair(sfs, &p.tmSfA, 0, 2 * ablk, fb);
+              if constexpr (BMO == B_K_DUAL_N) {
+                tma_load_2d_pair(sfs + 512, &p.tmSfB0, 0, 2 * bblk, fb);
+                tma_load_2d_pair(sfs + 1024, &p.tmSfB1, 0, 2 * bblk, fb);
+              } else {
+                tma_load_2d_pair(sfs + 512, &p.tmSfB0, 0, 2 * bblk, fb);
+              }
+            } else {
+              bulk_load(sfs, p.sfa + static_cast<size_t>(ablk) * 512, 512, full);
+              if constexpr (BMO == B_K_DUAL_N) {
+                bulk_load(sfs + 512, p.sfb0 + static_cast<size_t>(bblk) * 512, 512, full);
+                bulk_load(sfs + 1024, p.sfb1 + static_cast<size_t>(bblk) * 512, 512, full);
+              } else {
+                bulk_load(sfs + 512, p.sfb0 + static_cast<size_t>(bblk) * 512, BN / 128 * 512, full);
+              }
+            }
           }
         }
         __syncwarp();
@@ -624,6 +679,7 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
   constexpr bool a_mn = (AM == A_MN_TILE);
   constexpr bool b_mn = (BMO == B_MN_TILE || BMO == B_MN_DUAL_K);
   constexpr uint32_t idesc128 = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+  constexpr int kMxM = PAIR ? 2 * kBM : kBM;
   constexpr uint32_t idesc64 = idesc_bf16_f32(kBM / 2, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
   int s = 0;
   uint32_t ph = 0;
@@ -653,16 +709,25 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, uint32_t s_tiles, 
         // have been loaded after these MMAs released stage s
         const uint32_t sfa_t = tmem_base + kSfTmemCol + s * kSfTmemStride;
         const uint32_t sfs = s_sf + s * SFB;
-        tc_cp_32x128b(sfa_t, sfs);
-        tc_cp_32x128b(sfa_t + 8, sfs + 512);
-        if constexpr (BN == 256) tc_cp_32x128b(sfa_t + 12, sfs + 1024);
+        if constexpr (PAIR) {  // each CTA's scale blocks into its own TMEM
+          tc_cp_32x128b_pair(sfa_t, sfs);
+          tc_cp_32x128b_pair(sfa_t + 8, sfs + 512);
+          tc_cp_32x128b_pair(sfa_t + 12, sfs + 1024);
+        } else {
+          tc_cp_32x128b(sfa_t, sfs);
+          tc_cp_32x128b(sfa_t + 8, sfs + 512);
+          if constexpr (BN == 256) tc_cp_32x128b(sfa_t + 12, sfs + 1024);
+        }
         // both operands K-major: K = 32 is 32 bytes along the swizzled row
         static_assert(!a_mn && !b_mn, "MXFP8 operands are K-major");
 #pragma unroll
         for (int kk = 0; kk < kBKmx / 32; ++kk) {
-          tc_mma_mxf8(d_tmem, smem_desc_sw128(sA + kk * 32, 16, 1024),
-                      smem_desc_sw128(sB + kk * 32, 16, 1024), idesc_mxf8(kBM, BN, kk), sfa_t,
-                      sfa_t + 8, (kb > 0 || kk > 0) ? 1u : 0u);
+          const uint64_t ad = smem_desc_sw128(sA + kk * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(sB + kk * 32, 16, 1024);
+          if constexpr (PAIR)
+            tc_mma_mxf8_pair(d_tmem, ad, bd, idesc_mxf8(kMxM, BN, kk), sfa_t, sfa_t + 8, (kb > 0 || kk > 0) ? 1u : 0u);
+          else
+            tc_mma_mxf8(d_tmem, ad, bd, idesc_mxf8(kMxM, BN, kk), sfa_t, sfa_t + 8, (kb > 0 || kk > 0) ? 1u : 0u);
         }
       } else {
 #pragma unroll
@@ -757,6 +822,72 @@ struct EpiStager {
   }
 };
 
+// EPI_ROUTE, one tile of 128 tokens: this thread's token (row `grow` of the
+// dense rows) reads its E logits (+ bias) from TMEM 16 columns at a time, sorts
+// each 16 into selection order (logits descending, equal logits to the lower
+// expert index; a NaN as -inf with an index past E) with a sorting network and
+// merges them into its running list of the KM best (route_merge_top), then
+// writes the top-k ids and router weights (exp(l_j - l_0) over their sum, in
+// the summation order of route_weight_sum) and adds its picks to the expert
+// histogram of its chunk (integer atomics into route_chunk, which starts at
+// zero).  The logits also go to `out` when it is set.  `release` frees the
+// accumulator as soon as the logits are read.  KM: 8 for top_k <= 8, else 16.
+template <int KM, class Release>
+__device__ __forceinline__ void epi_route(const GemmParams& p, uint32_t tr, bool real, int grow, Release release) {
+  const int E = p.N, k = p.route_k;
+  float lv[KM];
+  int le[KM];
+#pragma unroll
+  for (int s = 0; s < KM; ++s) {
+    lv[s] = -INFINITY;
+    le[s] = INT_MAX;
+  }
+  float* lo = (real && p.out) ? reinterpret_cast<float*>(p.out) + static_cast<long long>(grow) * p.ldo : nullptr;
+  for (int c0 = 0; c0 < E; c0 += 16) {
+    float v[16];
+    int ei[16];
+    tmem_ld16(tr + c0, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int n = c0 + i;
+      if (n < E) {
+        const float x = v[i] + (p.bias ? __ldg(p.bias + n) : 0.f);
+        if (lo) lo[n] = x;
+        route_candidate(x, n, v[i], ei[i]);
+      } else {
+        v[i] = -INFINITY;
+        ei[i] = INT_MAX;
+      }
+    }
+    route_sort<16>(v, ei);
+    route_merge_top<KM, 16>(lv, le, v, ei);
+  }
+  release();
+  if (!real) return;
+  float ex[KM];
+  const float m = lv[0];
+#pragma unroll
+  for (int s = 0; s < KM; ++s) ex[s] = s < k ? expf(lv[s] - m) : 0.f;
+  const float sum = route_weight_sum<KM>(ex, k);
+  int32_t* hist = p.route_chunk + static_cast<size_t>(grow / kChunkTokens) * E;
+  int32_t* oi = p.route_idx + static_cast<size_t>(grow) * k;
+  float* ow = p.route_w + static_cast<size_t>(grow) * k;
+#pragma unroll
+  for (int s = 0; s < KM; ++s) {
+    if (s < k) {
+      int e = le[s];
+      if (e >= E) {  // only reachable with NaN logits
+        if (p.status) atomicCAS(p.status, 0, kDevBadValue);
+        e = 0;
+      }
+      oi[s] = e;
+      ow[s] = ex[s] / sum;
+      atomicAdd(hist + e, 1);
+    }
+  }
+}
+
 // Epilogue with two accumulator buffers: every bf16-mode GEMM (and MXFP8 ones
 // with 128-column tiles, whose output is bf16 as well; no instantiation).
 template <int EPI, int SCH, bool MX>
@@ -847,7 +978,17 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
       const int r0 = t.row0 + warp_e * wrows;
       const CUtensorMap* o0 = m64l ? &p.tmO0h : &p.tmO0;
       const CUtensorMap* o1 = m64l ? &p.tmO1h : &p.tmO1;
-      if constexpr (EPI == EPI_F32_BIAS) {
+      if constexpr (EPI == EPI_ROUTE) {
+        auto release = [&]() {  // frees the accumulator once the logits are read
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+        };
+        if (p.route_k <= 8)
+          epi_route<8>(p, tr, real, static_cast<int>(grow), release);
+        else
+          epi_route<kRouteMaxK>(p, tr, real, static_cast<int>(grow), release);
+      } else if constexpr (EPI == EPI_F32_BIAS) {
         const bool in_mem = p.dense_rows > 0 ? real : lane_ok;
         float* o = reinterpret_cast<float*>(p.out) + grow * p.ldo;
         for (int c0 = 0; c0 < kBN && t.n0 + c0 < p.N; c0 += 16) {
@@ -943,13 +1084,15 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t accf
         if (in_mem && p.out3) p.out3[grow * p.ldo3 + t.nt] = real ? dgp : 0.f;
       }
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      if (PAIR && wr.rank != 0)
-        mbar_arrive_remote(acce_lead + 8 * acc);
-      else
-        mbar_arrive(acce0 + 8 * acc);
+    if constexpr (EPI != EPI_ROUTE) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR && wr.rank != 0)
+          mbar_arrive_remote(acce_lead + 8 * acc);
+        else
+          mbar_arrive(acce0 + 8 * acc);
+      }
     }
     if (++acc == 2) {
       acc = 0;
@@ -1028,9 +1171,12 @@ __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t a
   const uint32_t stash = tmem_base + lane_off + kStashCol + half * (kStashCols / 2);
   const int row = quad * 32 + lane;  // MXFP8 groups are 128-row aligned: no 64-row tiles
   const int warp_e = quad;
-  static_assert(!sched_pair(SCH), "MXFP8 kernels run on one SM per tile");
+  // SM pairs: each CTA's epilogue takes its own 128 rows (its m-tile of the
+  // pair) and releases the accumulator on the even CTA's barrier
+  constexpr bool PAIR = sched_pair(SCH);
+  const uint32_t acce_lead = PAIR ? mapa_shared(acce0, 0) : acce0;
   for (int w = wr.first; w < wr.count; w += wr.stride) {
-    const TileInfo t = gemm_tile<EPI, SCH, kBKmx>(p, w);
+    const TileInfo t = gemm_tile<EPI, SCH, kBKmx>(p, w, wr.rank);
     if constexpr (EPI == EPI_SWIGLU_BWD) {  // the saved a, b of this warp's rows and columns: into L2 now
       const int c0 = t.n0 + 128 * half;
       if (row < t.rows_valid && c0 < p.N) {
@@ -1047,7 +1193,12 @@ __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t a
     auto release = [&]() {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce0);
+      if (lane == 0) {
+        if (PAIR && wr.rank != 0)
+          mbar_arrive_remote(acce_lead);
+        else
+          mbar_arrive(acce0);
+      }
       aph ^= 1;
     };
 
@@ -1224,9 +1375,11 @@ __device__ __forceinline__ void gemm_epilogue_mx(const GemmParams& p, uint32_t a
 }
 
 // ------------------------------------------------------------------ kernel
+// The whole GEMM on one CTA (or CTA pair): barrier and TMEM set-up, the roles,
+// and the teardown (TMEM freed).  Returns whether the CTA finished without an
+// abort (a bounded wait that ran out).
 template <int AM, int BMO, int EPI, int SCH, bool MX = false>
-__global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kernel(const __grid_constant__ GemmParams p) {
-  extern __shared__ uint8_t smem_raw[];
+__device__ __forceinline__ bool tc_gemm_run(const GemmParams& p, uint8_t* smem_raw) {
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   constexpr int ST = gemm_stages<MX, EPI, SCH>();
@@ -1266,6 +1419,11 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kerne
     tma_prefetch_desc(&p.tmA);
     tma_prefetch_desc(&p.tmB0);
     if (BMO == B_K_DUAL_N || BMO == B_MN_DUAL_K) tma_prefetch_desc(&p.tmB1);
+    if (MX && PAIR) {
+      tma_prefetch_desc(&p.tmSfA);
+      tma_prefetch_desc(&p.tmSfB0);
+      if (BMO == B_K_DUAL_N) tma_prefetch_desc(&p.tmSfB1);
+    }
     // only the output maps this launch stores through (MXFP8 mode stores directly)
     if (!MX && (EPI == EPI_BF16 || EPI == EPI_SWIGLU_FWD)) {
       tma_prefetch_desc(&p.tmO0);
@@ -1325,6 +1483,15 @@ __global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kerne
     tc_fence_after();
     tmem_dealloc<CG>(tmem_base, kTmemCols);
   }
+  const bool ok = *abort_flag == 0;
+  __syncthreads();
+  return ok;
+}
+
+template <int AM, int BMO, int EPI, int SCH, bool MX = false>
+__global__ void __launch_bounds__(gemm_threads<MX, EPI, SCH>(), 1) tc_gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  tc_gemm_run<AM, BMO, EPI, SCH, MX>(p, smem_raw);
 }
 
 }  // namespace moe

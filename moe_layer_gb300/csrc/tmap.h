@@ -62,6 +62,23 @@ inline bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t inner, uin
   return r == CUDA_SUCCESS;
 }
 
+// A byte array of `bytes` (a multiple of 256) viewed as [bytes / 256, 256],
+// boxes of 256 x box_rows bytes, no swizzle: the MXFP8 scale blocks (512
+// bytes each), fetched by the tiled TMA form so that a CTA pair's loads can
+// complete on the even CTA's barrier.
+inline bool make_tmap_bytes(CUtensorMap* map, const void* base, uint64_t bytes, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn || bytes % 256) return false;
+  cuuint64_t dims[2] = {256, bytes / 256};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {256, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Row-major bf16 matrix [rows, cols] (cols a multiple of 64) viewed as
 // {64 elements, rows, cols / 64 chunks} with boxes of 64 x box_rows x
 // box_chunks.  One box lands in shared memory as box_chunks consecutive

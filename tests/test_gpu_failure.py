@@ -17,7 +17,7 @@ from oracle import moe_oracle as O
 
 from synth.inputs import MoEShape, make_inputs
 
-from .helpers import ensure_lib, f64, topk_gap
+from .helpers import ensure_lib, f64, oracle_forward, rel_err, topk_gap
 
 pytestmark = pytest.mark.gpu
 MOE_ERR_DEVICE_TIMEOUT = 6
@@ -73,3 +73,35 @@ def test_stuck_pipeline_reports_timeout_and_the_context_stays_usable(monkeypatch
     ridx, _ = O.topk_route(ref, shape.k)
     safe = topk_gap(ref, shape.k) > 1e-4
     assert (out["idx"].cpu().numpy()[safe] == ridx[safe]).all()
+
+
+def test_stuck_sm_pair_pipeline_reports_timeout_and_the_context_stays_usable(monkeypatch):
+    """The same on the SM-pair GEMMs (cta_group::2): MOE_DEBUG_STALL_PAIR makes
+    the even CTA of every pair of the shared expert's gate/up wait for bytes
+    that never come.  Its MMA warp gives up, its producer drains, and the odd
+    CTA, whose stage releases never arrive, gives up on its own bounded waits;
+    both reach the final cluster barrier.  The forward returns with the
+    timeout status, and the next forward on the context matches the oracle."""
+    # T = 512: four 128-row m-tiles of the shared expert's dense rows, two
+    # pairs; d = 512: eight K stages for six pipeline slots
+    shape = MoEShape(T=512, d=512, I=128, E=8, k=2, n_shared=1, I_shared=128, w_std=0.05)
+    inp_cpu = make_inputs(shape, seed=0, with_dy=False)
+    inp = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp_cpu.items()}
+    cfg = _abi.make_config(shape.T, shape.d, shape.I, shape.E, shape.k, shape.n_shared, shape.I_shared)
+
+    monkeypatch.setenv("MOE_DEBUG_STALL_PAIR", "1")
+    bufs = layer.MoEBuffers(cfg, training=False)
+    t0 = time.monotonic()
+    layer.forward(cfg, inp, bufs)
+    status = _abi.moe_read_device_status(bufs.fwd_ws)  # synchronizes the stream
+    elapsed = time.monotonic() - t0
+    assert status == MOE_ERR_DEVICE_TIMEOUT
+    assert 1.0 < elapsed < 60.0, elapsed
+
+    monkeypatch.delenv("MOE_DEBUG_STALL_PAIR")
+    bufs = layer.MoEBuffers(cfg, training=False)
+    y = layer.forward(cfg, inp, bufs)
+    assert _abi.moe_read_device_status(bufs.fwd_ws) == 0
+    fwd = oracle_forward(inp_cpu, shape.k)
+    assert topk_gap(fwd["logits"], shape.k).min() > 1e-4
+    assert rel_err(y, fwd["y"]) <= 1e-2

@@ -90,13 +90,16 @@ MX_SHAPES = {
     "mx_ragged": MoEShape(T=333, d=384, I=128, E=5, k=3, n_shared=0, I_shared=0, w_std=0.05),
     "mx_zipf_zero": MoEShape(T=640, d=256, I=384, E=32, k=4, n_shared=1, I_shared=128, w_std=0.05,
                              zipf=True, zero_experts=8),
+    # 603-690 rows per expert: four experts with an even number of 128-row tiles (their GEMM
+    # tiles run on SM pairs) and four with an odd number (one SM per tile); d % 256 == 128
+    "mx_pairs_leftover": MoEShape(T=2560, d=384, I=256, E=8, k=2, n_shared=1, I_shared=128, w_std=0.05),
     # model shapes of the MoK blog ("Speedups"), scaled down with E, top-k and d:I kept
     "mx_qwen35_scaled": MoEShape(T=256, d=512, I=128, E=512, k=10, n_shared=1, I_shared=128, w_std=0.05,
                                  wr_std=0.1),
     "mx_dsv4pro_scaled": MoEShape(T=256, d=896, I=384, E=384, k=6, n_shared=1, I_shared=384, w_std=0.03,
                                   wr_std=0.1),
 }
-MX_SEEDS = {"mx_qwen35_scaled": 2}
+MX_SEEDS = {"mx_qwen35_scaled": 2, "mx_pairs_leftover": 1}
 
 
 def _cuda(inp):
