@@ -5,6 +5,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <string>
@@ -495,7 +496,9 @@ moe_status run_routing(const Shape& s, const void* x, const void* W_router, cons
     int extra = 0;
     if (const char* v = getenv("MOE_DEBUG_STALL_COUNTER"))
       if (v[0] && v[0] != '0') extra = 1;
-    const int grid = grid_for(device_sm_count());
+    // as many CTAs as the widest stage has work for: row tiles of the GEMM,
+    // chunks of the scatter, warps of the scan (eight experts per CTA)
+    const int grid = grid_for(std::max<int64_t>(std::max<int64_t>(cdiv(s.T, kBM), s.nchunk), cdiv(s.E, 8)));
     cudaError_t e = cudaSuccess;
     const moe_status ms = prof_launch(PL_ROUTE_FUSED, st, [&]() {
       e = launch_route_fused(p, sc, chunk_counts, chunk_base, nchunk, status, sync, extra, grid, st);
