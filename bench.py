@@ -586,8 +586,9 @@ def measure_workload(args, name, world, rank, local, ranks, full):
         # Within a step, dy's upload overlaps the forward, y's download the
         # backward, and dx's download the weight gradients (moe_backward
         # records dx_ready once dx is complete), on a side stream; x goes up
-        # before the forward.  Every copy of the step is inside it: the step
-        # ends when the side stream has finished too.
+        # before the forward, and dy after x (the two uploads would otherwise
+        # share the host link, delaying x).  Every copy of the step is inside
+        # it: the step ends when the side stream has finished too.
         side = torch.cuda.Stream()
         prev_done = torch.cuda.Event()
         prev_done.record(stream)
@@ -598,8 +599,11 @@ def measure_workload(args, name, world, rank, local, ranks, full):
 
         def e2e_step():
             xd.copy_(xh, non_blocking=True)
+            x_up = torch.cuda.Event()
+            x_up.record(stream)
             with torch.cuda.stream(side):
                 side.wait_event(prev_done)  # the previous step no longer reads dyd or writes yh
+                side.wait_event(x_up)
                 dyd.copy_(dyh, non_blocking=True)
                 dy_up = torch.cuda.Event()
                 dy_up.record(side)
