@@ -5,8 +5,10 @@ properties that hold at any size.
 
 Workloads: the DSV3-shaped layer (T=16384, d=7168, I=2048, E=256, top-8, one
 shared expert), the Qwen3-235B-shaped layer with Zipf-skewed routing (T=8192,
-d=4096, I=1536, E=128, no shared expert), and two points of the token sweep at
-DSV3 dims (T=512 with Zipf skew and 8 zero-token experts, T=32768 uniform).
+d=4096, I=1536, E=128, no shared expert), and four points of the token sweep
+at DSV3 dims, one per weight-gradient schedule: T=512 and T=2048 with Zipf skew
+and 8 zero-token experts (one SM per tile with eight epilogue warps), T=8192
+uniform (one SM per tile), T=32768 uniform (SM pairs, as at T=16384).
 """
 import numpy as np
 import pytest
@@ -25,6 +27,8 @@ WORKLOADS = {
     "dsv3": CONFIGS["dsv3"],
     "qwen3": CONFIGS["qwen3"],
     "sweep512_zipf_zero": sweep_shape(512, zipf=True, zero_experts=8),
+    "sweep2048_zipf_zero": sweep_shape(2048, zipf=True, zero_experts=8),
+    "sweep8192": sweep_shape(8192),
     "sweep32768": sweep_shape(32768),
 }
 
