@@ -7,8 +7,8 @@
 //                  softmax backward dl_tj = g_tj (dg_tj - sum_i g_ti dg_ti)
 //   router_wgrad   dW_router[e] = sum over e's rows (ascending) of dl_row x_token
 //   unpermute      dx_t = dx_shared,t + sum_j dxp[row(t, j)] + sum_j dl_tj W_router[e_tj]
-//   permute_rows   copies token rows into the expert-grouped row order (the
-//                  "dispatch" of the pages, local to one GPU)
+//   scatter_rows   copies each token row to its k rows of the expert-grouped
+//                  row order (the "dispatch" of the pages, local to one GPU)
 #include "moe_internal.h"
 #include "ptx.cuh"
 
@@ -193,42 +193,57 @@ __global__ void __launch_bounds__(kEwThreads)
   }
 }
 
-// dst[r] = src[idx[r]] for every row r of the padded expert-grouped layout
-// (idx -1 marks a padding row, which gets zeros).  Blocks past the padded total
-// written by the scatter kernel return at once.
+// The dispatch as a scatter: block t < T reads token t's row once and writes
+// it to its k rows of the padded expert-grouped layout (route_row_pad);
+// block T + e writes zeros into expert e's padding rows.  Every row of the
+// layout is written once, as by a gather over the rows, but each source row
+// is read once instead of k times (the source, larger than L2 at full size,
+// would otherwise come from DRAM k times).
+constexpr int kScatterChunks = 4;  // 16-byte chunks per thread in flight
 __global__ void __launch_bounds__(kEwThreads)
-    permute_rows_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __restrict__ idx,
-                        const int32_t* __restrict__ total_rows, int d,
-                        __nv_bfloat16* __restrict__ dst) {
-  const int r = blockIdx.x;
-  if (r >= __ldg(total_rows)) return;
-  const int t = __ldg(idx + r);
-  const uint4* s = reinterpret_cast<const uint4*>(src + static_cast<size_t>(t < 0 ? 0 : t) * d);
-  uint4* o = reinterpret_cast<uint4*>(dst + static_cast<size_t>(r) * d);
+    scatter_rows_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __restrict__ route_row_pad,
+                        const int32_t* __restrict__ row_start, const int32_t* __restrict__ counts, int T, int d,
+                        int k, __nv_bfloat16* __restrict__ dst) {
+  __shared__ int s_rows[kMaxTopK];
+  const int b = blockIdx.x;
   const int nv = d / 8;
-  if (t < 0) {
-    for (int v = threadIdx.x; v < nv; v += blockDim.x) o[v] = make_uint4(0, 0, 0, 0);
+  if (b >= T) {  // padding rows of expert b - T
+    const int e = b - T;
+    const int beg = __ldg(row_start + e) + __ldg(counts + e), end = __ldg(row_start + e + 1);
+    for (int r = beg; r < end; ++r) {
+      uint4* o = reinterpret_cast<uint4*>(dst + static_cast<size_t>(r) * d);
+      for (int v = threadIdx.x; v < nv; v += blockDim.x) o[v] = make_uint4(0, 0, 0, 0);
+    }
     return;
   }
-  int v = threadIdx.x;
-  for (; v + 3 * kEwThreads < nv; v += 4 * kEwThreads) {
-    const uint4 a0 = __ldg(s + v), a1 = __ldg(s + v + kEwThreads);
-    const uint4 a2 = __ldg(s + v + 2 * kEwThreads), a3 = __ldg(s + v + 3 * kEwThreads);
-    o[v] = a0;
-    o[v + kEwThreads] = a1;
-    o[v + 2 * kEwThreads] = a2;
-    o[v + 3 * kEwThreads] = a3;
+  if (threadIdx.x < k) s_rows[threadIdx.x] = __ldg(route_row_pad + static_cast<size_t>(b) * k + threadIdx.x);
+  __syncthreads();
+  const uint4* s = reinterpret_cast<const uint4*>(src + static_cast<size_t>(b) * d);
+  for (int v0 = threadIdx.x; v0 < nv; v0 += kScatterChunks * kEwThreads) {
+    uint4 a[kScatterChunks];
+#pragma unroll
+    for (int i = 0; i < kScatterChunks; ++i) {
+      const int v = v0 + i * kEwThreads;
+      if (v < nv) a[i] = __ldg(s + v);
+    }
+    for (int j = 0; j < k; ++j) {
+      uint4* o = reinterpret_cast<uint4*>(dst + static_cast<size_t>(s_rows[j]) * d);
+#pragma unroll
+      for (int i = 0; i < kScatterChunks; ++i) {
+        const int v = v0 + i * kEwThreads;
+        if (v < nv) o[v] = a[i];
+      }
+    }
   }
-  for (; v < nv; v += kEwThreads) o[v] = __ldg(s + v);
 }
 
 }  // namespace
 
-cudaError_t launch_permute_rows(const __nv_bfloat16* src, const int32_t* idx_pad,
-                                const int32_t* total_rows, int rows_max, int d,
-                                __nv_bfloat16* dst, cudaStream_t st) {
-  if (rows_max <= 0) return cudaSuccess;
-  permute_rows_kernel<<<rows_max, kEwThreads, 0, st>>>(src, idx_pad, total_rows, d, dst);
+cudaError_t launch_scatter_rows(const __nv_bfloat16* src, const int32_t* route_row_pad, const int32_t* row_start,
+                                const int32_t* counts, int T, int E, int d, int k, __nv_bfloat16* dst,
+                                cudaStream_t st) {
+  if (T + E <= 0) return cudaSuccess;
+  scatter_rows_kernel<<<T + E, kEwThreads, 0, st>>>(src, route_row_pad, row_start, counts, T, d, k, dst);
   return cudaGetLastError();
 }
 

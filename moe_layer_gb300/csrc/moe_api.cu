@@ -660,8 +660,8 @@ moe_status forward_gateup(const Shape& s, const void* x, const moe_weights* wts,
                                                          rt.row_start + E, s.Rp, d, o.xq, o.xq_sf,
                                                          act ? act->xt : nullptr, act ? act->xt_sf : nullptr, st));
   else
-    MOE_LAUNCH(PL_PERMUTE_X, st, launch_permute_rows(static_cast<const __nv_bfloat16*>(x), rt.perm_token_pad,
-                                                    rt.row_start + E, static_cast<int>(s.Rp), d, xp, st));
+    MOE_LAUNCH(PL_PERMUTE_X, st, launch_scatter_rows(static_cast<const __nv_bfloat16*>(x), rt.route_row_pad,
+                                                    rt.row_start, rt.counts, T, E, d, static_cast<int>(s.k), xp, st));
   // shared expert gate/up + SwiGLU (dense rows of x)
   if (s.S && o.shared) {
     GemmParams p;
@@ -966,8 +966,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
                                                           rt.row_start + E, s.Rp, d, w.dyq, w.dyq_sf, w.dyt,
                                                           w.dyt_sf, st));
   else
-    MOE_LAUNCH(PL_PERMUTE_DY, st, launch_permute_rows(static_cast<const __nv_bfloat16*>(dy), rt.perm_token_pad,
-                                                     rt.row_start + E, static_cast<int>(s.Rp), d, w.dyp, st));
+    MOE_LAUNCH(PL_PERMUTE_DY, st, launch_scatter_rows(static_cast<const __nv_bfloat16*>(dy), rt.route_row_pad,
+                                                     rt.row_start, rt.counts, T, E, d, static_cast<int>(s.k), w.dyp, st));
   // dgrad of the down projection with the fused SwiGLU backward and the
   // router-weight gradient partials <h, dh> per n-tile; in MXFP8 mode the
   // epilogue also quantizes [da | db] for the gate/up dgrad

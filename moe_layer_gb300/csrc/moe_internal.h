@@ -54,9 +54,9 @@ cudaError_t launch_router_wgrad(const float* dl_row, const int32_t* perm_token_p
                                 const int32_t* row_start, const int32_t* counts,
                                 const __nv_bfloat16* x, int E, int d, float* dW_router,
                                 cudaStream_t st);
-cudaError_t launch_permute_rows(const __nv_bfloat16* src, const int32_t* idx_pad,
-                                const int32_t* total_rows, int rows_max, int d,
-                                __nv_bfloat16* dst, cudaStream_t st);
+cudaError_t launch_scatter_rows(const __nv_bfloat16* src, const int32_t* route_row_pad, const int32_t* row_start,
+                                const int32_t* counts, int T, int E, int d, int k, __nv_bfloat16* dst,
+                                cudaStream_t st);
 cudaError_t launch_unpermute(const __nv_bfloat16* dxp, const __nv_bfloat16* dxs,
                              const int32_t* route_row_pad, const int32_t* topk_idx,
                              const float* dl_tk, const __nv_bfloat16* W_router, int T, int d,
