@@ -4,8 +4,11 @@
 // tile on one SM.  Measured at the DSV3 shape (same box, alternating runs):
 // on SM pairs gate/up took 3.49-3.50 ms against 3.50-3.55 on one SM, but the
 // down projection 1.86-1.87 against 1.76-1.78 and the dgrad of gate/up
-// 3.33-3.34 against 3.20-3.23: with a single accumulator beside the scale
-// ring, a pair's MMAs wait on both CTAs' epilogues at every tile.
+// 3.33-3.34 against 3.20-3.23.  Unlike the bf16 GEMMs, the MXFP8 ones are
+// not bound by the shared-memory traffic that pairs halve (their scale
+// transfers and copies cost 10-13 %, the single accumulator's hand-off about
+// 2 %; a block-scaled 128x256x32 MMA issues in as many cycles as a bf16
+// 128x256x16 one).
 #include "gemm_launch.cuh"
 
 namespace moe {
