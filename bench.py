@@ -449,7 +449,7 @@ def main():
                        "l2": "inputs larger than L2 (x 235 MB, expert weights 22.6 GB at dsv3); no flush"},
         }
         for key in ("tflops", "pct_tensor_peak", "pct_tensor_peak_sustained", "tensor_peak_src", "weight_quant",
-                    "fwd", "roofline", "kernels_ms_per_step", "kernel_share", "gpu_launches", "e2e",
+                    "fwd", "fwd_inference", "roofline", "kernels_ms_per_step", "kernel_share", "gpu_launches", "e2e",
                     "cpu_baseline", "clocks"):
             line[key] = head.get(key)
         if extras:
@@ -531,6 +531,13 @@ def measure_workload(args, name, world, rank, local, ranks, full):
     for _ in range(2):
         layer.forward(cfg, inp, bufs, y)
     ms_fwd = max_over_ranks(timed(lambda: layer.forward(cfg, inp, bufs, y), args.steps))
+    # forward for serving: no saved state (the routed experts' a, b and, in
+    # MXFP8 mode, the transposed activation copies are not written)
+    ibufs = layer.MoEBuffers(cfg, training=False)
+    for _ in range(2):
+        layer.forward(cfg, inp, ibufs, y)
+    ms_inf = max_over_ranks(timed(lambda: layer.forward(cfg, inp, ibufs, y), args.steps))
+    del ibufs
 
     wq = None
     if mx:  # the once-per-weight-update quantization pass, timed on its own
@@ -645,7 +652,9 @@ def measure_workload(args, name, world, rank, local, ranks, full):
         "pct_tensor_peak_sustained": tflops / t_sust, "tensor_peak_src": t_src,
         "weight_quant": wq,
         "fwd": {"value": fwd_value, "unit": "tokens/s", "ms": ms_fwd,
-                "tflops": fwd_value * flops_tok / 1e12},
+                "tflops": fwd_value * flops_tok / 1e12, "note": "the forward of a training step (state saved)"},
+        "fwd_inference": {"value": tokens / (ms_inf * 1e-3), "unit": "tokens/s", "ms": ms_inf,
+                          "tflops": tokens / (ms_inf * 1e-3) * flops_tok / 1e12, "note": "no saved state"},
         "roofline": roofline,
         "kernels_ms_per_step": {k: round(v / args.steps, 4) for k, v in
                                 sorted(kern_ms.items(), key=lambda kv: -kv[1])},

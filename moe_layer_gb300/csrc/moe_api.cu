@@ -656,9 +656,10 @@ moe_status forward_gateup(const Shape& s, const void* x, const moe_weights* wts,
   // MXFP8 mode quantized on the way, the bf16 copy kept only for training
   __nv_bfloat16* xp = act ? act->xp : o.xp;
   if (s.mx)  // along d for gate/up; in training also along the tokens for dW_gate, dW_up
-    MOE_LAUNCH(PL_MX_QUANT_X, st, launch_mx_permute_dual(static_cast<const __nv_bfloat16*>(x), d, rt.perm_token_pad,
-                                                         rt.row_start + E, s.Rp, d, o.xq, o.xq_sf,
-                                                         act ? act->xt : nullptr, act ? act->xt_sf : nullptr, st));
+    MOE_LAUNCH(PL_MX_QUANT_X, st, launch_mx_dispatch(static_cast<const __nv_bfloat16*>(x), d, T, static_cast<int>(s.k), E,
+                                                     rt.perm_token_pad, rt.route_row_pad, rt.row_start, rt.counts, s.Rp,
+                                                     d, o.xq, o.xq_sf, act ? act->xt : nullptr,
+                                                     act ? act->xt_sf : nullptr, st));
   else
     MOE_LAUNCH(PL_PERMUTE_X, st, launch_scatter_rows(static_cast<const __nv_bfloat16*>(x), rt.route_row_pad,
                                                     rt.row_start, rt.counts, T, E, d, static_cast<int>(s.k), xp, st));

@@ -68,6 +68,15 @@ cudaError_t launch_mx_rows(const __nv_bfloat16* src, long long src_ld, int64_t R
 cudaError_t launch_mx_permute_dual(const __nv_bfloat16* src, long long src_ld, const int32_t* idx,
                                    const int32_t* total_rows, int64_t R, int K, uint8_t* rq, uint8_t* rq_sf,
                                    uint8_t* tq, uint8_t* tq_sf, cudaStream_t st);
+// The dispatch with MXFP8 quantization of the rows of src [T, K] into the
+// padded expert-grouped layout of R rows: rq (blocks of 32 along K, zeros in
+// padding rows) and, when tq is given, its transpose tq [K, R]
+// (launch_mx_permute_dual); without tq, rq alone as a scatter of the token
+// rows (each read once).
+cudaError_t launch_mx_dispatch(const __nv_bfloat16* src, long long src_ld, int T, int k, int E,
+                               const int32_t* perm_token_pad, const int32_t* route_row_pad, const int32_t* row_start,
+                               const int32_t* counts, int64_t R, int K, uint8_t* rq, uint8_t* rq_sf, uint8_t* tq,
+                               uint8_t* tq_sf, cudaStream_t st);
 cudaError_t launch_mx_cols(const __nv_bfloat16* src, long long src_ld, long long src_bstride, int rows,
                            int cols, int batch, uint8_t* dst, long long dst_ld, long long dst_brows,
                            int k_off, uint8_t* sf, long long dst_rows_total, cudaStream_t st);

@@ -64,6 +64,77 @@ __global__ void __launch_bounds__(kQThreads)
   }
 }
 
+// The dispatch without the transposed copy (the forward of a call that keeps
+// no state) as a scatter: each token row of src [T, K] is quantized once
+// along K (blocks of 32, the arithmetic of mx_rows_kernel: one group of four
+// threads per (token, 128-column group)) and written to the token's k rows of
+// the padded expert-grouped layout (route_row_pad), codes and scale words
+// alike; blocks past the tokens' ones write zero codes and zero scale words
+// into each expert's padding rows.  The bytes are those of the gathered
+// quantization below (a row's blocks do not depend on the expert), but each
+// source row is read once instead of k times.  (With the transposed copy to
+// write too, the gather serves both copies at once; a scatter beside a
+// transposed-only gather measured slower.)
+__global__ void __launch_bounds__(kQThreads)
+    mx_scatter_rows_kernel(const __nv_bfloat16* __restrict__ src, long long src_ld, int T, int k,
+                           const int32_t* __restrict__ route_row_pad, const int32_t* __restrict__ row_start,
+                           const int32_t* __restrict__ counts, int64_t R, int K, int token_blocks,
+                           uint8_t* __restrict__ rq, uint8_t* __restrict__ rq_sf) {
+  const int64_t ng = K / 128;
+  const int64_t rblocks = (R + 127) / 128;
+  const int j = threadIdx.x & 3;
+  if (static_cast<int>(blockIdx.x) >= token_blocks) {  // padding rows of expert blockIdx.x - token_blocks
+    const int e = static_cast<int>(blockIdx.x) - token_blocks;
+    const int64_t beg = __ldg(row_start + e) + __ldg(counts + e), end = __ldg(row_start + e + 1);
+    const int64_t units = (end - beg) * ng;
+    for (int64_t u = threadIdx.x / 4; u < units; u += kQThreads / 4) {
+      const int64_t r = beg + u / ng, g = u % ng;
+      uint4* d4 = reinterpret_cast<uint4*>(rq + r * static_cast<int64_t>(K) + g * 128 + 32 * j);
+      d4[0] = make_uint4(0, 0, 0, 0);
+      d4[1] = make_uint4(0, 0, 0, 0);
+      if (j == 0) *reinterpret_cast<uint32_t*>(rq_sf + sf_word_offset(r, g, rblocks)) = 0u;
+    }
+    return;
+  }
+  const int64_t units = static_cast<int64_t>(T) * ng;
+  for (int64_t u = (static_cast<int64_t>(blockIdx.x) * kQThreads + threadIdx.x) / 4; u < units;
+       u += static_cast<int64_t>(token_blocks) * kQThreads / 4) {
+    const int64_t t = u / ng, g = u - t * ng;
+    const int col = static_cast<int>(g * 128 + 32 * j);
+    float v[32];
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + t * src_ld + col);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = __ldg(s4 + q);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[8 * q + 2 * i] = bf16lo(ws[i]);
+        v[8 * q + 2 * i + 1] = bf16hi(ws[i]);
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int e = mx_scale_exp(amax);
+    uint4 lo, hi;
+    quant32(v, e, lo, hi);
+    // the quad's four codes form one word (a quad is active or not as a whole;
+    // the last pass of the loop may leave other quads of the warp out)
+    const unsigned quad = 0xfu << (threadIdx.x & 28);
+    uint32_t code = static_cast<uint32_t>(e + 127) << (8 * j);
+    code |= __shfl_xor_sync(quad, code, 1);
+    code |= __shfl_xor_sync(quad, code, 2);
+    for (int s = 0; s < k; ++s) {
+      const int64_t r = __ldg(route_row_pad + t * k + s);
+      uint4* d4 = reinterpret_cast<uint4*>(rq + r * static_cast<int64_t>(K) + col);
+      d4[0] = lo;
+      d4[1] = hi;
+      if (j == 0) *reinterpret_cast<uint32_t*>(rq_sf + sf_word_offset(r, g, rblocks)) = code;
+    }
+  }
+}
+
 // Dispatch with quantization: dst row r is src row idx[r] (a zero row for a
 // negative index); rows from *total_rows on are left alone.  Writes up to two
 // MXFP8 copies of the gathered [R, K] matrix:
@@ -315,6 +386,23 @@ cudaError_t launch_mx_permute_dual(const __nv_bfloat16* src, long long src_ld, c
   const unsigned grid = static_cast<unsigned>(tiles < cap ? tiles : cap);
   mx_permute_dual_kernel<<<grid, kQThreads, kDualSmemBytes, st>>>(src, src_ld, idx, total_rows, R, K, rq, rq_sf,
                                                                  tq, tq_sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_dispatch(const __nv_bfloat16* src, long long src_ld, int T, int k, int E,
+                               const int32_t* perm_token_pad, const int32_t* route_row_pad, const int32_t* row_start,
+                               const int32_t* counts, int64_t R, int K, uint8_t* rq, uint8_t* rq_sf, uint8_t* tq,
+                               uint8_t* tq_sf, cudaStream_t st) {
+  if (tq) return launch_mx_permute_dual(src, src_ld, perm_token_pad, row_start + E, R, K, rq, rq_sf, tq, tq_sf, st);
+  if (R <= 0) return cudaSuccess;
+  if (K % kDualTile || R % kDualTile) return cudaErrorInvalidValue;
+  const int64_t ng = K / 128;
+  const int64_t want = (static_cast<int64_t>(T) * ng * 4 + kQThreads - 1) / kQThreads;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+  const int token_blocks = static_cast<int>(want < cap ? want : cap);
+  if (token_blocks + E <= 0) return cudaSuccess;
+  mx_scatter_rows_kernel<<<token_blocks + E, kQThreads, 0, st>>>(src, src_ld, T, k, route_row_pad, row_start, counts,
+                                                                 R, K, token_blocks, rq, rq_sf);
   return cudaGetLastError();
 }
 

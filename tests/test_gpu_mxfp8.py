@@ -191,3 +191,23 @@ def test_mxfp8_forward_requires_quantized_weights():
     with pytest.raises(_abi.MoeError) as ei:
         layer.forward(cfg, inp, bufs)
     assert ei.value.code == 1
+
+
+@pytest.mark.parametrize("name", ["mx_small", "mx_ragged", "mx_zipf_zero", "mx_qwen35_scaled"])
+def test_stateless_forward_equals_training_forward_bitwise(name):
+    """A forward that keeps no state quantizes the dispatched rows with its own
+    kernel (a scatter of the token rows) instead of the gather that also
+    writes the transposed copy for the weight gradients: the codes and scales
+    are the same, so y is bitwise the training forward's (which the other
+    tests check against the oracle)."""
+    shape = MX_SHAPES[name]
+    inp = _cuda(make_inputs(shape, seed=MX_SEEDS.get(name, 0), with_dy=False))
+    cfg = _abi.make_config(shape.T, shape.d, shape.I, shape.E, shape.k, shape.n_shared, shape.I_shared,
+                           precision=_abi.MOE_MXFP8)
+    layer.quantize_weights(cfg, inp)
+    y_train = layer.forward(cfg, inp, layer.MoEBuffers(cfg))
+    ibufs = layer.MoEBuffers(cfg, training=False)
+    y_inf = layer.forward(cfg, inp, ibufs)
+    torch.cuda.synchronize()
+    assert _abi.moe_read_device_status(ibufs.fwd_ws) == 0
+    assert torch.equal(y_inf, y_train)
