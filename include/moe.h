@@ -182,8 +182,7 @@ moe_status moe_route_topk(const moe_config* cfg, const void* x, const void* W_ro
  *     2 KB: up to T = 65536 tokens fit at top-8 with 256 experts.  Larger
  *     shapes return MOE_ERR_UNSUPPORTED before anything is enqueued.
  *   - The first call on a device looks up the device address of the static
- *     array (cudaGetSymbolAddress) with that device current; make that first
- *     call before capturing the stream into a CUDA graph.
+ *     array (cudaGetSymbolAddress) with that device current.
  *   - All calls on a device share the array.  Calls whose GPU work overlaps
  *     (different streams without ordering between them) race on it and give
  *     wrong results; calls ordered on one stream are safe.
