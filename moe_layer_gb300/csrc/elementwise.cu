@@ -5,10 +5,14 @@
 //                  the router weight is already applied by the down GEMM)
 //   router_grad    dg_tj = sum of the per-n-tile partials of <h, dh>, then the
 //                  softmax backward dl_tj = g_tj (dg_tj - sum_i g_ti dg_ti)
-//   router_wgrad   dW_router[e] = sum over e's rows (ascending) of dl_row x_token
+//   router_wgrad   dW_router[e] = sum over e's rows of dl_row x_token: in chunks
+//                  of rows (ascending), the chunks' sums added in order
 //   unpermute      dx_t = dx_shared,t + sum_j dxp[row(t, j)] + sum_j dl_tj W_router[e_tj]
 //   scatter_rows   copies each token row to its k rows of the expert-grouped
 //                  row order (the "dispatch" of the pages, local to one GPU)
+#include <algorithm>
+#include <climits>
+
 #include "moe_internal.h"
 #include "ptx.cuh"
 
@@ -95,21 +99,93 @@ __global__ void __launch_bounds__(256)
 }
 
 // dW_router[e, :] = sum over the rows routed to e of dlogit(row) * x[token(row), :]: only the
-// chosen logits carry a gradient, so the product is a gather over each expert's rows.
-// grid (E, ceil(d / 1024)); each thread owns eight adjacent columns (one 16-byte load per row)
-// and sums the rows in their permuted order, four gathers in flight.
+// chosen logits carry a gradient, so the product is a gather over each expert's rows.  Each
+// expert's rows are cut into chunks of `chunk` rows (a quarter above the average rows per
+// expert, at least 256), so that an expert routed several times the average (skewed routing)
+// is spread over several blocks.  router_wgrad_part_kernel sums one chunk per block (rows
+// ascending): the further chunks of the experts that have them (grid z = 0, in expert order;
+// dispatched first, so that they run beside the first chunks) and the first chunk of every
+// expert (z = 1, block x = the expert).  The sum of an
+// expert's only chunk goes to dW_router, the others to fp32 partials (slot e for the first
+// chunk, E + j for further chunk j); router_wgrad_sum_kernel adds those experts' partials in
+// chunk order and zeroes the experts without rows.  Each thread owns eight adjacent columns
+// (one 16-byte load per row), four gathers in flight.
 constexpr int kRwThreads = 128;
 constexpr int kRwCols = 8 * kRwThreads;
-__global__ void __launch_bounds__(kRwThreads)
-    router_wgrad_kernel(const float* __restrict__ dl_row, const int32_t* __restrict__ perm_token_pad,
-                        const int32_t* __restrict__ row_start, const int32_t* __restrict__ counts,
-                        const __nv_bfloat16* __restrict__ x, int d, float* __restrict__ dW) {
+
+__device__ __forceinline__ int rw_chunks(const int32_t* __restrict__ counts, int e, int chunk) {
+  return (__ldg(counts + e) + chunk - 1) / chunk;
+}
+
+// s_pre[e] = number of further chunks (past the first) of the experts before e, e = 0..E
+// (E <= kMaxExperts = 4 per thread).  Called by every thread of the block.
+__device__ __forceinline__ void rw_extra_prefix(const int32_t* __restrict__ counts, int E, int chunk, int* s_pre,
+                                                int* s_warp) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  int c[4], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = 4 * t + j;
+    c[j] = e < E ? max(0, rw_chunks(counts, e, chunk) - 1) : 0;
+    sum += c[j];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) s_warp[w] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int i = 0; i < w; ++i) base += s_warp[i];
+  int ex = base + incl - sum;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (4 * t + j < E) s_pre[4 * t + j] = ex;
+    ex += c[j];
+  }
+  if (t == kRwThreads - 1) s_pre[E] = ex;  // the total: experts past E have none
+  __syncthreads();
+}
+
+// grid (max(E, bound on the further chunks), ceil(d / kRwCols), 2).  Twelve blocks per SM: all
+// of an expert-per-block grid of the DSV3 shape (256 x 7) is resident at once.
+__global__ void __launch_bounds__(kRwThreads, 12)
+    router_wgrad_part_kernel(const float* __restrict__ dl_row, const int32_t* __restrict__ perm_token_pad,
+                             const int32_t* __restrict__ row_start, const int32_t* __restrict__ counts,
+                             const __nv_bfloat16* __restrict__ x, int E, int d, int chunk,
+                             float* __restrict__ part, float* __restrict__ dW) {
+  __shared__ int s_pre[kMaxExperts + 1];
+  __shared__ int s_warp[kRwThreads / 32];
   __shared__ int s_tok[kRwThreads];
   __shared__ float s_dl[kRwThreads];
-  const int e = blockIdx.x;
+  int e, q, slot;  // expert, its chunk, the partial slot
+  if (blockIdx.z == 1) {
+    e = blockIdx.x;
+    if (e >= E || __ldg(counts + e) == 0) return;
+    q = 0;
+    slot = e;
+  } else {
+    rw_extra_prefix(counts, E, chunk, s_pre, s_warp);
+    const int j = blockIdx.x;
+    if (j >= s_pre[E]) return;
+    int lo = 0, hi = E - 1;  // the expert of this chunk: the last e with s_pre[e] <= j
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pre[mid] <= j)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    e = lo;
+    q = 1 + j - s_pre[e];
+    slot = E + j;
+  }
+  const int first = q * chunk;
+  const int r0 = __ldg(row_start + e) + first;
+  const int n = min(chunk, __ldg(counts + e) - first);
   const int c = blockIdx.y * kRwCols + threadIdx.x * 8;
-  const int r0 = __ldg(row_start + e);
-  const int n = __ldg(counts + e);
   const __nv_bfloat16* xc = x + c;
   float a[8];
 #pragma unroll
@@ -124,15 +200,20 @@ __global__ void __launch_bounds__(kRwThreads)
     __syncthreads();
     if (c < d) {
       int i = 0;
-      for (; i + 4 <= m; i += 4) {
-        float u[4][8];
+      for (; i + 4 <= m; i += 4) {  // four rows' loads issued before any is used
+        uint4 raw[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ld8(xc + static_cast<size_t>(s_tok[i + q]) * d, u[q]);
+        for (int k4 = 0; k4 < 4; ++k4)
+          raw[k4] = __ldg(reinterpret_cast<const uint4*>(xc + static_cast<size_t>(s_tok[i + k4]) * d));
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float g = s_dl[i + q];
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const float g = s_dl[i + k4];
+          const uint32_t w[4] = {raw[k4].x, raw[k4].y, raw[k4].z, raw[k4].w};
 #pragma unroll
-          for (int j = 0; j < 8; ++j) a[j] += g * u[q][j];
+          for (int j = 0; j < 4; ++j) {
+            a[2 * j] += g * bf16lo(w[j]);
+            a[2 * j + 1] += g * bf16hi(w[j]);
+          }
         }
       }
       for (; i < m; ++i) {
@@ -145,10 +226,45 @@ __global__ void __launch_bounds__(kRwThreads)
     }
   }
   if (c < d) {
-    float4* out = reinterpret_cast<float4*>(dW + static_cast<size_t>(e) * d + c);
+    const bool only = blockIdx.z == 1 && __ldg(counts + e) <= chunk;
+    float* o = only ? dW + static_cast<size_t>(e) * d : part + static_cast<size_t>(slot) * d;
+    float4* out = reinterpret_cast<float4*>(o + c);
     out[0] = make_float4(a[0], a[1], a[2], a[3]);
     out[1] = make_float4(a[4], a[5], a[6], a[7]);
   }
+}
+
+// grid (E, ceil(d / kRwCols)): dW_router[e] = the sum of e's chunk partials in chunk order for an
+// expert with several chunks, zero for one without rows (router_wgrad_part_kernel wrote the
+// others).
+__global__ void __launch_bounds__(kRwThreads)
+    router_wgrad_sum_kernel(const int32_t* __restrict__ counts, const float* __restrict__ part, int E, int d,
+                            int chunk, float* __restrict__ dW) {
+  __shared__ int s_pre[kMaxExperts + 1];
+  __shared__ int s_warp[kRwThreads / 32];
+  const int e = blockIdx.x;
+  const int nch = rw_chunks(counts, e, chunk);
+  if (nch == 1) return;
+  const int c = blockIdx.y * kRwCols + threadIdx.x * 8;
+  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+  if (nch > 1) {
+    rw_extra_prefix(counts, E, chunk, s_pre, s_warp);
+    if (c >= d) return;
+    const float4* p = reinterpret_cast<const float4*>(part + static_cast<size_t>(e) * d + c);
+    a0 = __ldg(p);
+    a1 = __ldg(p + 1);
+#pragma unroll 4
+    for (int j = s_pre[e]; j < s_pre[e + 1]; ++j) {
+      p = reinterpret_cast<const float4*>(part + static_cast<size_t>(E + j) * d + c);
+      const float4 u0 = __ldg(p), u1 = __ldg(p + 1);
+      a0.x += u0.x; a0.y += u0.y; a0.z += u0.z; a0.w += u0.w;
+      a1.x += u1.x; a1.y += u1.y; a1.z += u1.z; a1.w += u1.w;
+    }
+  }
+  if (c >= d) return;
+  float4* out = reinterpret_cast<float4*>(dW + static_cast<size_t>(e) * d + c);
+  out[0] = a0;
+  out[1] = a1;
 }
 
 __global__ void __launch_bounds__(kEwThreads)
@@ -264,11 +380,24 @@ cudaError_t launch_router_grad(const float* dg_part, int nparts, const int32_t* 
 
 cudaError_t launch_router_wgrad(const float* dl_row, const int32_t* perm_token_pad,
                                 const int32_t* row_start, const int32_t* counts,
-                                const __nv_bfloat16* x, int E, int d, float* dW_router,
-                                cudaStream_t st) {
-  dim3 grid(E, (d + kRwCols - 1) / kRwCols);
-  router_wgrad_kernel<<<grid, kRwThreads, 0, st>>>(dl_row, perm_token_pad, row_start, counts, x, d,
-                                                   dW_router);
+                                const __nv_bfloat16* x, int E, int d, int64_t R, float* part,
+                                int64_t part_floats, float* dW_router, cudaStream_t st) {
+  // chunk: a quarter above the average rows per expert, in whole 128-row steps, at least 256
+  const int64_t avg = (R + E - 1) / E;
+  const int64_t chunk = std::max<int64_t>(256, (avg + avg / 4 + 127) / 128 * 128);
+  if (chunk > INT_MAX) return cudaErrorInvalidValue;
+  // further chunks (past each expert's first): at most sum_e counts[e] / chunk = R / chunk
+  const int64_t extra = (R + chunk - 1) / chunk;
+  if ((E + extra) * d > part_floats || extra > INT_MAX) return cudaErrorInvalidValue;
+  const int ncb = (d + kRwCols - 1) / kRwCols;
+  const unsigned gx = static_cast<unsigned>(std::max<int64_t>(E, extra));
+  router_wgrad_part_kernel<<<dim3(gx, ncb, 2), kRwThreads, 0, st>>>(
+      dl_row, perm_token_pad, row_start, counts, x, E, d, static_cast<int>(chunk), part, dW_router);
+  const cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  ++extra_kernel_launches();
+  router_wgrad_sum_kernel<<<dim3(E, ncb), kRwThreads, 0, st>>>(counts, part, E, d, static_cast<int>(chunk),
+                                                                dW_router);
   return cudaGetLastError();
 }
 

@@ -50,10 +50,12 @@ cudaError_t launch_combine(const __nv_bfloat16* o, const __nv_bfloat16* ys,
 cudaError_t launch_router_grad(const float* dg_part, int nparts, const int32_t* route_row_pad,
                                const float* topk_w, int T, int k, float* d_topk_w, float* dl_tk,
                                float* dl_row, cudaStream_t st);
+// part: scratch of part_floats floats for the per-chunk partial sums, at least
+// (ceil(R / 256) + E) * d (R = the routed rows, sum of counts).
 cudaError_t launch_router_wgrad(const float* dl_row, const int32_t* perm_token_pad,
                                 const int32_t* row_start, const int32_t* counts,
-                                const __nv_bfloat16* x, int E, int d, float* dW_router,
-                                cudaStream_t st);
+                                const __nv_bfloat16* x, int E, int d, int64_t R, float* part,
+                                int64_t part_floats, float* dW_router, cudaStream_t st);
 cudaError_t launch_scatter_rows(const __nv_bfloat16* src, const int32_t* route_row_pad, const int32_t* row_start,
                                 const int32_t* counts, int T, int E, int d, int k, __nv_bfloat16* dst,
                                 cudaStream_t st);
