@@ -127,6 +127,10 @@ SHAPES = {
     # pairs on SM pairs and every tile of the odd ones on one SM, so both passes of each grouped
     # GEMM have work; 640 rows per expert put the weight gradients on SM pairs
     "pairs_leftover": MoEShape(T=2560, d=512, I=256, E=8, k=2, n_shared=1, I_shared=128, w_std=0.05),
+    # two experts take every token (the other six are never chosen): 2048 rows each, four row
+    # chunks of the router weight gradient per expert (summed as partials in chunk order), and
+    # six experts whose gradients must be exact zeros
+    "two_hot": MoEShape(T=2048, d=256, I=128, E=8, k=2, n_shared=0, I_shared=0, w_std=0.05, zero_experts=6),
     # the open-weight model shapes the MoK blog benchmarks ("Speedups"), scaled down with their
     # E, top-k and d:I ratio kept: Kimi-K2.7 (384, 8, 3.5), GLM-5.2 (256, 8, 3), Qwen3.5-397B-A17B
     # (512, 10, 4), DeepSeek-V4-Pro (384, 6, 7:3); logits spread wider so that seeds without
