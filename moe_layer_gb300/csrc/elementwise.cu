@@ -105,11 +105,11 @@ __global__ void __launch_bounds__(256)
 // is spread over several blocks.  router_wgrad_part_kernel sums one chunk per block (rows
 // ascending): the further chunks of the experts that have them (grid z = 0, in expert order;
 // dispatched first, so that they run beside the first chunks) and the first chunk of every
-// expert (z = 1, block x = the expert).  The sum of an
-// expert's only chunk goes to dW_router, the others to fp32 partials (slot e for the first
-// chunk, E + j for further chunk j); router_wgrad_sum_kernel adds those experts' partials in
-// chunk order and zeroes the experts without rows.  Each thread owns eight adjacent columns
-// (one 16-byte load per row), four gathers in flight.
+// expert (z = 1, block x = the expert).  The sum of an expert's only chunk goes to dW_router,
+// the others to fp32 partials (slot e for the first chunk, E + j for further chunk j);
+// router_wgrad_sum_kernel adds those experts' partials in chunk order and zeroes the experts
+// without rows.  Each thread owns eight adjacent columns (one 16-byte load per row), four
+// gathers in flight.
 constexpr int kRwThreads = 128;
 constexpr int kRwCols = 8 * kRwThreads;
 
@@ -149,8 +149,9 @@ __device__ __forceinline__ void rw_extra_prefix(const int32_t* __restrict__ coun
   __syncthreads();
 }
 
-// grid (max(E, bound on the further chunks), ceil(d / kRwCols), 2).  Twelve blocks per SM: all
-// of an expert-per-block grid of the DSV3 shape (256 x 7) is resident at once.
+// grid (max(E, bound on the further chunks), ceil(d / kRwCols), 2).  Twelve blocks per SM (at
+// most 42 registers a thread): one block per expert and column block, 256 x 7 of them, are all
+// resident at once.
 __global__ void __launch_bounds__(kRwThreads, 12)
     router_wgrad_part_kernel(const float* __restrict__ dl_row, const int32_t* __restrict__ perm_token_pad,
                              const int32_t* __restrict__ row_start, const int32_t* __restrict__ counts,
