@@ -100,9 +100,9 @@ __global__ void __launch_bounds__(256)
 
 // dW_router[e, :] = sum over the rows routed to e of dlogit(row) * x[token(row), :]: only the
 // chosen logits carry a gradient, so the product is a gather over each expert's rows.  Each
-// expert's rows are cut into chunks of `chunk` rows (a quarter above the average rows per
-// expert, at least 256), so that an expert routed several times the average (skewed routing)
-// is spread over several blocks.  router_wgrad_part_kernel sums one chunk per block (rows
+// expert's rows are cut into chunks of `chunk` rows (sized so that the chunks about fill the
+// resident blocks, and no fewer than one per expert at a quarter above the average), so that an
+// expert routed several times the average (skewed routing) is spread over several blocks.  router_wgrad_part_kernel sums one chunk per block (rows
 // ascending): the further chunks of the experts that have them (grid z = 0, in expert order;
 // dispatched first, so that they run beside the first chunks) and the first chunk of every
 // expert (z = 1, block x = the expert).  The sum of an expert's only chunk goes to dW_router,
@@ -383,14 +383,16 @@ cudaError_t launch_router_wgrad(const float* dl_row, const int32_t* perm_token_p
                                 const int32_t* row_start, const int32_t* counts,
                                 const __nv_bfloat16* x, int E, int d, int64_t R, float* part,
                                 int64_t part_floats, float* dW_router, cudaStream_t st) {
-  // chunk: a quarter above the average rows per expert, in whole 128-row steps, at least 256
-  const int64_t avg = (R + E - 1) / E;
-  const int64_t chunk = std::max<int64_t>(256, (avg + avg / 4 + 127) / 128 * 128);
+  const int ncb = (d + kRwCols - 1) / kRwCols;
+  // chunk: about one chunk per resident block (12 per SM) or per expert, whichever is more, with
+  // a quarter of slack so that experts near the average stay whole; 128-row steps, at least 128
+  const int64_t target = std::max<int64_t>(E, int64_t(device_sm_count()) * 12 / ncb);
+  const int64_t want = (R + R / 4 + target - 1) / target;
+  const int64_t chunk = std::max<int64_t>(128, (want + 127) / 128 * 128);
   if (chunk > INT_MAX) return cudaErrorInvalidValue;
   // further chunks (past each expert's first): at most sum_e counts[e] / chunk = R / chunk
   const int64_t extra = (R + chunk - 1) / chunk;
   if ((E + extra) * d > part_floats || extra > INT_MAX) return cudaErrorInvalidValue;
-  const int ncb = (d + kRwCols - 1) / kRwCols;
   const unsigned gx = static_cast<unsigned>(std::max<int64_t>(E, extra));
   router_wgrad_part_kernel<<<dim3(gx, ncb, 2), kRwThreads, 0, st>>>(
       dl_row, perm_token_pad, row_start, counts, x, E, d, static_cast<int>(chunk), part, dW_router);

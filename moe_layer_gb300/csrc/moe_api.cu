@@ -1111,7 +1111,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const moe_weights*
   // dx is complete: the weight gradients below do not touch it
   if (g->dx_ready) MOE_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(g->dx_ready), st));
   // dxp is no longer read: its Rp x d bf16 hold the router weight gradient's per-chunk
-  // partial sums, at most (R / 256 + E + 1) x d floats (Rp >= R + 63 E)
+  // partial sums, at most (R / 128 + E + 1) x d floats (Rp >= R + 63 E)
   MOE_LAUNCH(PL_ROUTER_WGRAD, st, launch_router_wgrad(w.dl_row, rt.perm_token_pad, rt.row_start, rt.counts,
                                                       static_cast<const __nv_bfloat16*>(x), E, d, s.R,
                                                       reinterpret_cast<float*>(w.dxp), s.Rp * s.d / 2,

@@ -51,7 +51,7 @@ cudaError_t launch_router_grad(const float* dg_part, int nparts, const int32_t* 
                                const float* topk_w, int T, int k, float* d_topk_w, float* dl_tk,
                                float* dl_row, cudaStream_t st);
 // part: scratch of part_floats floats for the per-chunk partial sums, at least
-// (ceil(R / 256) + E) * d (R = the routed rows, sum of counts).
+// (ceil(R / 128) + E) * d (R = the routed rows, sum of counts).
 cudaError_t launch_router_wgrad(const float* dl_row, const int32_t* perm_token_pad,
                                 const int32_t* row_start, const int32_t* counts,
                                 const __nv_bfloat16* x, int E, int d, int64_t R, float* part,
